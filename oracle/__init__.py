@@ -1,0 +1,41 @@
+"""fp64 CPU oracle of the EAGLE-3 MLA draft-head step — TEST INFRASTRUCTURE ONLY.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and the ``cpu_baseline`` / reference
+arm of ``bench.py`` may import or call this package.  The product path (the
+C-ABI library and its Python binding) never does; it shares no code with it.
+
+Sources (cited by title and section):
+  [MAX-walkthrough]  "Eagle3 DeepseekV3 speculative decoding architecture: a full
+                     walkthrough of MAX's eagle3_deepseekV3 module" (xxmr.cn/news/219581)
+  [MAX-API]          "max.pipelines.architectures.eagle3_deepseekV3" API reference
+                     (max.modular.com), class Eagle3DeepseekV3DraftConfig
+  [ModelOpt-EAGLE]   "EAGLE head deep dive: inside Model Optimizer's speculative-decoding
+                     draft model" (discosf.com/news/5068204)
+
+Every function is a plain fp64 numpy statement of its definition (no blocking,
+fusion or reordering).  Pins (``tests/test_oracle_*.py``):
+  rms_norm          closed form on a hand example, scale invariance, unit-RMS output
+  yarn_inv_freq     factor 1 == plain RoPE; YaRN's defining rotation-count property on
+                    the DeepseekV3 parameters; hand-computed band edges (golden file)
+  yarn_mscale       hand value 1 + 0.1 ln 40 (golden file)
+  rope_interleaved  complex-multiplication formulation, norm preservation, position 0
+                    identity, relative-position invariance, composition R(a)R(b)=R(a+b)
+  linear / silu     brute-force triple loop; torch.nn.functional.silu in fp64
+  mla_attention     torch scaled_dot_product_attention (fp64) on explicit K/V; single key
+                    returns its value; equal keys return the mean; causal first row;
+                    absorbed == unabsorbed to fp64 round-off
+  argmax_lowest     brute force with planted ties
+  d2t_remap         zero offsets give identity; brute force
+  accept            full match gives gamma; first mismatch gives 0; brute force
+  draft_extend /    composition invariants: one T-row extend == T one-row extends
+  draft_decode_step (same cache rows and hidden); batch and page-placement independence;
+                    residual pass-through with zeroed projections; fc only on 3H input
+The whole head has no worked numeric example on the pages: beyond the invariants
+above its parity is unpinned (the 2H concat order is a reading that only permutes
+weight columns and cannot be pinned).
+"""
+from .head import (  # noqa: F401
+    F64, rms_norm, linear, silu, yarn_inv_freq, yarn_mscale, rope_cos_sin, rope_interleaved,
+    softmax_scale, split_kv_b, mla_attention, decoder_rows, final_logits, argmax_lowest,
+    top2_gap, d2t_remap, SeqCache, draft_extend, draft_decode_step, draft_round, accept,
+)

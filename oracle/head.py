@@ -1,0 +1,360 @@
+"""fp64 oracle of the EAGLE-3 MLA draft head — test infrastructure only (see package docstring).
+
+Notation: H hidden, n_h heads, d_q q_lora_rank, d_c kv_lora_rank, d_n qk_nope, d_r qk_rope,
+d_v v_head, I intermediate, V_t target vocab, V_d draft vocab.  Weights follow nn.Linear:
+W[out, in], y = x W^T.  ``hyper`` is a plain dict with those sizes and the YaRN / norm
+constants; ``W`` maps weight names to arrays (any float dtype, widened to fp64 on use).
+"""
+from __future__ import annotations
+
+import math
+
+import numpy as np
+
+F64 = np.float64
+
+
+def _f64(a):
+    return np.asarray(a, dtype=F64)
+
+
+# ----------------------------------------------------------------------------
+# Elementary operations
+# ----------------------------------------------------------------------------
+def rms_norm(x, w, eps):
+    """RMSNorm over the last axis: x / sqrt(mean(x^2) + eps) * w.
+
+    The draft head normalises both input streams and every sub-layer input this way,
+    with rms_norm_eps = 1e-6 ([MAX-API] Eagle3DeepseekV3DraftConfig; [MAX-walkthrough] §4).
+    """
+    x = _f64(x)
+    ms = np.mean(x * x, axis=-1, keepdims=True)
+    return x / np.sqrt(ms + eps) * _f64(w)
+
+
+def linear(x, W):
+    """Bias-free linear layer y = x W^T with W stored [out, in] ([MAX-walkthrough] §4: fc,
+    o_proj and the dense MLP carry no bias; attention_bias=False in [MAX-API])."""
+    return _f64(x) @ _f64(W).T
+
+
+def silu(x):
+    """SiLU(x) = x * sigmoid(x) (hidden_act='silu', [MAX-API])."""
+    x = _f64(x)
+    return x / (1.0 + np.exp(-x))
+
+
+# ----------------------------------------------------------------------------
+# DeepSeek YaRN rotary embedding (interleaved pairs)
+# ----------------------------------------------------------------------------
+def yarn_inv_freq(d, theta, factor, original_max_pos, beta_fast, beta_slow):
+    """Per-pair angular frequencies of YaRN ("DeepseekYarnRotaryEmbedding", [MAX-walkthrough] §4,
+    with rope_scaling beta_fast / beta_slow, §5).
+
+    The pages name the method but do not print it; this is YaRN's published construction:
+    pair i < d/2 has the plain RoPE frequency theta^(-2i/d) ("extrapolated") or that
+    frequency divided by ``factor`` ("interpolated").  A pair whose wavelength fits at least
+    beta_fast times into the original context keeps the plain frequency, one that fits
+    fewer than beta_slow times is fully interpolated, and a linear ramp over the pair index
+    blends the band in between.  The band edges are the (real) pair indices at which the
+    rotation count over the original context equals beta:
+        corr(beta) = d * ln(L0 / (2 pi beta)) / (2 ln theta),
+    lo = max(floor(corr(beta_fast)), 0), hi = min(ceil(corr(beta_slow)), d - 1).
+    """
+    i = np.arange(d // 2, dtype=F64)
+    extra = theta ** (-2.0 * i / d)
+    inter = extra / factor
+
+    def corr(beta):
+        return d * math.log(original_max_pos / (2.0 * math.pi * beta)) / (2.0 * math.log(theta))
+
+    lo = max(math.floor(corr(beta_fast)), 0)
+    hi = min(math.ceil(corr(beta_slow)), d - 1)
+    if lo == hi:
+        hi += 0.001
+    ramp = np.clip((i - lo) / (hi - lo), 0.0, 1.0)
+    return inter * ramp + extra * (1.0 - ramp)
+
+
+def yarn_mscale(factor, mscale):
+    """YaRN magnitude factor m(f, mu) = 0.1 mu ln f + 1 for f > 1, else 1 (reading: not printed)."""
+    if factor <= 1.0:
+        return 1.0
+    return 0.1 * mscale * math.log(factor) + 1.0
+
+
+def rope_cos_sin(positions, hyper):
+    """cos/sin [len(positions), d_r/2] of angle p * omega_i, scaled by
+    m(f, mscale) / m(f, mscale_all_dim) (reading)."""
+    d = hyper["qk_rope_dim"]
+    inv = yarn_inv_freq(d, hyper["rope_theta"], hyper["yarn_factor"], hyper["yarn_original_max_pos"],
+                        hyper["yarn_beta_fast"], hyper["yarn_beta_slow"])
+    ang = _f64(positions)[:, None] * inv[None, :]
+    scale = yarn_mscale(hyper["yarn_factor"], hyper["yarn_mscale"]) / \
+        yarn_mscale(hyper["yarn_factor"], hyper["yarn_mscale_all_dim"])
+    return np.cos(ang) * scale, np.sin(ang) * scale
+
+
+def rope_interleaved(x, positions, hyper):
+    """Rotate interleaved pairs (x_2i, x_2i+1) by angle p * omega_i (rope_interleave=True,
+    [MAX-API]); reading: the pairs are rotated in place, counter-clockwise:
+        x'_2i   = x_2i cos - x_2i+1 sin
+        x'_2i+1 = x_2i sin + x_2i+1 cos.
+    ``x`` is [T, ..., d_r] with one position per leading row."""
+    x = _f64(x)
+    cos, sin = rope_cos_sin(positions, hyper)
+    shape = (x.shape[0],) + (1,) * (x.ndim - 2) + (cos.shape[1],)
+    cos = cos.reshape(shape)
+    sin = sin.reshape(shape)
+    a = x[..., 0::2]
+    b = x[..., 1::2]
+    out = np.empty_like(x)
+    out[..., 0::2] = a * cos - b * sin
+    out[..., 1::2] = a * sin + b * cos
+    return out
+
+
+def softmax_scale(hyper):
+    """sigma = (d_n + d_r)^(-1/2) * m(f, mscale_all_dim)^2 (reading: YaRN attention scaling
+    folded into the softmax scale, as DeepSeek's MLA does)."""
+    m = yarn_mscale(hyper["yarn_factor"], hyper["yarn_mscale_all_dim"])
+    return (hyper["qk_nope_dim"] + hyper["qk_rope_dim"]) ** -0.5 * m * m
+
+
+# ----------------------------------------------------------------------------
+# MLA attention over a one-layer latent cache
+# ----------------------------------------------------------------------------
+def split_kv_b(kv_b, hyper):
+    """kv_b [n_h (d_n + d_v), d_c] -> (W_UK [n_h, d_n, d_c], W_UV [n_h, d_v, d_c]).
+
+    Reading: kv_b's output is viewed per head as [d_n | d_v] (key part first)."""
+    nh, dn, dv, dc = hyper["n_heads"], hyper["qk_nope_dim"], hyper["v_head_dim"], hyper["kv_lora_rank"]
+    w = _f64(kv_b).reshape(nh, dn + dv, dc)
+    return w[:, :dn, :], w[:, dn:, :]
+
+
+def mla_attention(q, positions, cache, kv_b, hyper, absorbed=False):
+    """Attention of query rows over one sequence's latent cache ([MAX-walkthrough] §4: a single
+    MLA decoder layer; its cache is a one-layer view of the target's, [MAX-API]).
+
+    q        [T, n_h, d_n + d_r]   (q_pe part already rotated)
+    cache    [L, d_c + d_r]        rows [c_kv_hat | k_r_rot] indexed by position
+    returns  o [T, n_h, d_v]
+
+    Row i at position p attends to cache slots 0..p (causal; a decode row sees itself).
+    Unabsorbed (the definition): k_h,t = [W_UK,h c_t ; k_r,t], v_h,t = W_UV,h c_t,
+    s_t = sigma q_h . k_h,t, o_h = sum_t softmax(s)_t v_h,t.
+    ``absorbed=True`` evaluates the same quantity as q_lat,h = W_UK,h^T q_nope,h,
+    s_t = sigma (q_lat,h . c_t + q_pe,h . k_r,t), o_h = W_UV,h (sum_t p_t c_t); the tests pin
+    it to the unabsorbed form, and large parity cases use it to keep the fp64 cost low.
+    """
+    q = _f64(q)
+    cache = _f64(cache)
+    dn, dc = hyper["qk_nope_dim"], hyper["kv_lora_rank"]
+    sigma = softmax_scale(hyper)
+    W_UK, W_UV = split_kv_b(kv_b, hyper)
+    T, nh = q.shape[0], q.shape[1]
+    out = np.empty((T, nh, hyper["v_head_dim"]), dtype=F64)
+    maxp = int(np.max(positions)) + 1
+    c = cache[:maxp, :dc]
+    kr = cache[:maxp, dc:]
+    if not absorbed:
+        k_nope = np.einsum("tc,hnc->htn", c, W_UK)   # [n_h, L, d_n]
+        v = np.einsum("tc,hvc->htv", c, W_UV)        # [n_h, L, d_v]
+    for i in range(T):
+        n = int(positions[i]) + 1
+        q_nope = q[i, :, :dn]
+        q_pe = q[i, :, dn:]
+        rope_part = q_pe @ kr[:n].T                                   # [n_h, n]
+        if absorbed:
+            q_lat = np.einsum("hn,hnc->hc", q_nope, W_UK)             # [n_h, d_c]
+            s = sigma * (q_lat @ c[:n].T + rope_part)
+        else:
+            s = sigma * (np.einsum("hn,htn->ht", q_nope, k_nope[:, :n]) + rope_part)
+        s = s - s.max(axis=1, keepdims=True)
+        p = np.exp(s)
+        p /= p.sum(axis=1, keepdims=True)
+        if absorbed:
+            o_lat = p @ c[:n]                                         # [n_h, d_c]
+            out[i] = np.einsum("hc,hvc->hv", o_lat, W_UV)
+        else:
+            out[i] = np.einsum("ht,htv->hv", p, v[:, :n])
+    return out
+
+
+# ----------------------------------------------------------------------------
+# The decoder chain
+# ----------------------------------------------------------------------------
+class SeqCache:
+    """One sequence's logical latent cache: fp64 rows [capacity, d_c + d_r] and its length."""
+
+    def __init__(self, rows, capacity):
+        rows = _f64(rows)
+        self.data = np.zeros((capacity, rows.shape[1]), dtype=F64)
+        self.data[:rows.shape[0]] = rows
+        self.length = rows.shape[0]
+
+    def copy(self):
+        c = SeqCache(self.data[:0], self.data.shape[0])
+        c.data = self.data.copy()
+        c.length = self.length
+        return c
+
+
+def decoder_rows(hyper, W, f, tokens, positions, cache: SeqCache, absorbed=False, trace=None):
+    """One decoder pass over T rows of one sequence ([MAX-walkthrough] §4, Eagle3MLADraft.__call__).
+
+    f       [T, H]  fused hidden: fc output (extend) or the previous step's h2 (decode);
+                    it is also the residual stream (reading)
+    tokens  [T]     target-vocab ids; the embedding is the target's table ([MAX-walkthrough] §5)
+    Appends the rows' latent entries at their positions, returns h2 [T, H] (before the final norm).
+    """
+    eps = hyper["rms_eps"]
+    nh, dn, dr, dc = hyper["n_heads"], hyper["qk_nope_dim"], hyper["qk_rope_dim"], hyper["kv_lora_rank"]
+    f = _f64(f)
+    T = f.shape[0]
+    positions = np.asarray(positions, dtype=np.int64)
+    e = _f64(W["embed"][np.asarray(tokens, dtype=np.int64)])
+    # two streams normalised separately, then concatenated to 2H: [norm(embed) | norm(fused)]
+    # ([ModelOpt-EAGLE] part 3; [MAX-walkthrough] §4; the order is a reading)
+    x = np.concatenate([rms_norm(e, W["input_norm"], eps), rms_norm(f, W["hidden_norm"], eps)], axis=1)
+    # MLA projections at 2H input ([ModelOpt-EAGLE] part 3: first-layer q/k/v input doubled)
+    c_q = rms_norm(linear(x, W["q_a"]), W["q_a_norm"], eps)
+    kv = linear(x, W["kv_a"])
+    c_kv = rms_norm(kv[:, :dc], W["kv_a_norm"], eps)
+    k_r = rope_interleaved(kv[:, dc:], positions, hyper)
+    q = linear(c_q, W["q_b"]).reshape(T, nh, dn + dr)
+    q[:, :, dn:] = rope_interleaved(q[:, :, dn:], positions, hyper)
+    # latent KV append: slot = position
+    need = int(positions.max()) + 1
+    if need > cache.data.shape[0]:
+        grow = np.zeros((need - cache.data.shape[0], cache.data.shape[1]), dtype=F64)
+        cache.data = np.concatenate([cache.data, grow], axis=0)
+    cache.data[positions] = np.concatenate([c_kv, k_r], axis=1)
+    cache.length = max(cache.length, need)
+    o = mla_attention(q, positions, cache.data, W["kv_b"], hyper, absorbed=absorbed)
+    # o_proj (heads * v_head_dim -> H) and residual; post-attention norm; dense SiLU MLP; residual
+    h1 = linear(o.reshape(T, -1), W["o"]) + f
+    y = rms_norm(h1, W["post_attn_norm"], eps)
+    m = silu(linear(y, W["gate"])) * linear(y, W["up"])
+    h2 = linear(m, W["down"]) + h1
+    if trace is not None:
+        trace.update(x=x, c_q=c_q, c_kv=c_kv, k_r=k_r, q=q, o=o, h1=h1, y=y, m=m, h2=h2)
+    return h2
+
+
+def final_logits(hyper, W, h2):
+    """Final RMSNorm and the head's own lm_head over the draft vocabulary
+    ([MAX-walkthrough] §4; [ModelOpt-EAGLE] part 4: bias-free Linear(H, draft_vocab))."""
+    z = rms_norm(h2, W["final_norm"], hyper["rms_eps"])
+    return linear(z, W["lm_head"])
+
+
+def argmax_lowest(v):
+    """Index of the maximum of a 1-D vector; among equal maxima the lowest index (reading)."""
+    v = _f64(v)
+    return int(np.flatnonzero(v == v.max())[0])
+
+
+def top2_gap(v):
+    """Difference between the largest and second-largest entries of a 1-D vector."""
+    s = np.sort(_f64(v))
+    return float(s[-1] - s[-2])
+
+
+def d2t_remap(d, d2t):
+    """Draft id -> target id by adding the per-id offset: t = d + d2t[d]
+    ([ModelOpt-EAGLE] part 4); identity when no table is given."""
+    d = np.asarray(d, dtype=np.int64)
+    if d2t is None:
+        return d.astype(np.int32)
+    return (d + np.asarray(d2t, dtype=np.int64)[d]).astype(np.int32)
+
+
+# ----------------------------------------------------------------------------
+# Head calls
+# ----------------------------------------------------------------------------
+def draft_extend(hyper, W, aux, tokens, positions, row_offsets, caches, absorbed=False):
+    """Extend: fc fuses the three aux states (early, middle, late) from 3H to H with no bias
+    ([MAX-walkthrough] §4; [ModelOpt-EAGLE] part 2), then the decoder chain over each
+    sequence's new rows; the last row of each sequence is scored ([MAX-walkthrough] §4:
+    last-token gather by input_row_offsets).
+
+    aux: three arrays [N, H]; caches: list of SeqCache (mutated).
+    Returns dict(h2 [B, H], logits [B, V_d], d [B]).
+    """
+    B = len(row_offsets) - 1
+    fused_in = np.concatenate([_f64(a) for a in aux], axis=1)        # [N, 3H]
+    assert fused_in.shape[1] == 3 * hyper["hidden"], "fc applies only to a 3H-wide input"
+    h2_last, logits = [], []
+    for b in range(B):
+        r0, r1 = int(row_offsets[b]), int(row_offsets[b + 1])
+        f = linear(fused_in[r0:r1], W["fc"])
+        h2 = decoder_rows(hyper, W, f, tokens[r0:r1], positions[r0:r1], caches[b], absorbed)
+        h2_last.append(h2[-1])
+        logits.append(final_logits(hyper, W, h2[-1:])[0])
+    logits = np.stack(logits)
+    return dict(h2=np.stack(h2_last), logits=logits, d=np.array([argmax_lowest(l) for l in logits]))
+
+
+def draft_decode_step(hyper, W, h_prev, tokens, caches, absorbed=False):
+    """One autoregressive draft step ([MAX-walkthrough] §9: decode steps, one token per sequence;
+    [ModelOpt-EAGLE] TTT section: each step feeds on the previous step's own hidden state).
+    The carried H-wide hidden skips fc ([MAX-walkthrough] §4).  Token of sequence b sits at
+    position = current cache length of b."""
+    B = len(tokens)
+    h2s, logits = [], []
+    for b in range(B):
+        pos = np.array([caches[b].length])
+        h2 = decoder_rows(hyper, W, _f64(h_prev[b])[None, :], np.array([tokens[b]]), pos, caches[b], absorbed)
+        h2s.append(h2[0])
+        logits.append(final_logits(hyper, W, h2)[0])
+    logits = np.stack(logits)
+    return dict(h2=np.stack(h2s), logits=logits, d=np.array([argmax_lowest(l) for l in logits]))
+
+
+def draft_round(hyper, W, d2t, gamma, aux, tokens, positions, row_offsets, caches,
+                absorbed=False, forced=None):
+    """A drafting round: the extend gives the first draft token, then gamma - 1 decode steps;
+    every draft id is mapped to the target vocab before it is output and before it is
+    embedded (reading; the embedding table is the target's).
+
+    ``forced`` [B, gamma] (optional) feeds those tokens forward instead of the oracle's own
+    choices (used where a near-tie lets a correct implementation pick another token).
+    Returns dict(tokens [B, gamma] (oracle's own choices), hidden [gamma, B, H],
+    logits [gamma, B, V_d], draft [gamma, B]).
+    """
+    ext = draft_extend(hyper, W, aux, tokens, positions, row_offsets, caches, absorbed)
+    B = len(row_offsets) - 1
+    toks = np.zeros((B, gamma), dtype=np.int32)
+    hid, lgs, drafts = [ext["h2"]], [ext["logits"]], [ext["d"]]
+    toks[:, 0] = d2t_remap(ext["d"], d2t)
+    h = ext["h2"]
+    for s in range(1, gamma):
+        feed = toks[:, s - 1] if forced is None else np.asarray(forced)[:, s - 1]
+        st = draft_decode_step(hyper, W, h, feed, caches, absorbed)
+        toks[:, s] = d2t_remap(st["d"], d2t)
+        hid.append(st["h2"])
+        lgs.append(st["logits"])
+        drafts.append(st["d"])
+        h = st["h2"]
+    return dict(tokens=toks, hidden=np.stack(hid), logits=np.stack(lgs), draft=np.stack(drafts))
+
+
+def accept(draft, target):
+    """Greedy acceptance ([MAX-walkthrough] §10: greedy argmax acceptance): the accepted length of a
+    sequence is the number of leading positions where the drafted token equals the target's.
+    Returns (acc [B], hist [gamma + 1]) with hist[k] = number of sequences with acc == k."""
+    draft = np.asarray(draft)
+    target = np.asarray(target)
+    B, G = draft.shape
+    acc = np.zeros(B, dtype=np.int32)
+    for b in range(B):
+        k = 0
+        while k < G and draft[b, k] == target[b, k]:
+            k += 1
+        acc[b] = k
+    hist = np.zeros(G + 1, dtype=np.int32)
+    for k in acc:
+        hist[k] += 1
+    return acc, hist

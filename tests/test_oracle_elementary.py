@@ -1,0 +1,266 @@
+"""Pins of the oracle's elementary operations against facts fixed independently of its code:
+hand examples, closed forms, invariants, library routines and brute force."""
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+
+GOLD = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _hyper(d=64, theta=1e4, factor=40.0, L0=4096, bf=32.0, bs=1.0, ms=1.0, msa=1.0, dn=128, nh=2, dv=8, dc=16):
+    return dict(qk_rope_dim=d, rope_theta=theta, yarn_factor=factor, yarn_original_max_pos=L0,
+                yarn_beta_fast=bf, yarn_beta_slow=bs, yarn_mscale=ms, yarn_mscale_all_dim=msa,
+                qk_nope_dim=dn, n_heads=nh, v_head_dim=dv, kv_lora_rank=dc)
+
+
+# ---------------------------------------------------------------- RMSNorm
+def test_rmsnorm_hand_example():
+    # x = (3, 4): mean square 12.5, so y = x / sqrt(12.5) * w when eps = 0
+    y = O.rms_norm(np.array([3.0, 4.0]), np.array([1.0, 2.0]), 0.0)
+    assert y[0] == pytest.approx(3.0 / math.sqrt(12.5), rel=1e-15)
+    assert y[1] == pytest.approx(8.0 / math.sqrt(12.5), rel=1e-15)
+    # with eps the denominator is sqrt(12.5 + eps)
+    y = O.rms_norm(np.array([3.0, 4.0]), np.ones(2), 0.5)
+    assert y[1] == pytest.approx(4.0 / math.sqrt(13.0), rel=1e-15)
+
+
+def test_rmsnorm_unit_rms_and_scale_invariance():
+    rng = np.random.default_rng(0)
+    x = rng.standard_normal((5, 300))
+    y = O.rms_norm(x, np.ones(300), 1e-6)
+    ms = np.mean(x * x, axis=1)
+    np.testing.assert_allclose(np.sqrt(np.mean(y * y, axis=1)), np.sqrt(ms / (ms + 1e-6)), rtol=1e-13)
+    np.testing.assert_allclose(O.rms_norm(7.5 * x, np.ones(300), 0.0), O.rms_norm(x, np.ones(300), 0.0), rtol=1e-13)
+    # the weight multiplies elementwise after normalisation
+    w = rng.standard_normal(300)
+    np.testing.assert_allclose(O.rms_norm(x, w, 1e-6), y * w, rtol=1e-13)
+
+
+# ---------------------------------------------------------------- YaRN
+def test_yarn_factor_one_is_plain_rope():
+    inv = O.yarn_inv_freq(64, 1e4, 1.0, 4096, 32.0, 1.0)
+    plain = np.array([1.0 / (10000.0 ** (2 * i / 64)) for i in range(32)])
+    np.testing.assert_allclose(inv, plain, rtol=1e-14)
+
+
+def test_yarn_golden_band_edges_dsv3():
+    g = json.load(open(os.path.join(GOLD, "yarn_dsv3.json")))
+    d, theta, L0, f = g["d"], g["theta"], g["original_max_pos"], g["factor"]
+    inv = O.yarn_inv_freq(d, theta, f, L0, g["beta_fast"], g["beta_slow"])
+    plain = np.array([theta ** (-2 * i / d) for i in range(d // 2)])
+    lo, hi = g["lo"], g["hi"]
+    # below the band the plain frequency is kept; above it the frequency is divided by the factor
+    np.testing.assert_allclose(inv[:lo + 1], plain[:lo + 1], rtol=1e-14)
+    np.testing.assert_allclose(inv[hi:], plain[hi:] / f, rtol=1e-14)
+    # inside the band it is strictly between the two
+    mid = slice(lo + 1, hi)
+    assert np.all(inv[mid] < plain[mid]) and np.all(inv[mid] > plain[mid] / f)
+    # YaRN's defining property: kept pairs turn at least beta_fast times over the original window,
+    # fully interpolated pairs at most beta_slow times
+    turns = L0 * plain / (2 * math.pi)
+    assert np.all(turns[:lo + 1] >= g["beta_fast"])
+    assert np.all(turns[hi:] <= g["beta_slow"])
+    assert turns[lo] == pytest.approx(g["rotations_pair10"], abs=0.01)
+    assert turns[hi] == pytest.approx(g["rotations_pair23"], abs=0.001)
+    # the blended frequency falls monotonically with the pair index
+    assert np.all(np.diff(inv) < 0)
+
+
+def test_yarn_mscale_golden_and_special_cases():
+    g = json.load(open(os.path.join(GOLD, "yarn_dsv3.json")))
+    assert O.yarn_mscale(40.0, 1.0) == pytest.approx(g["mscale_factor40_mu1"], rel=1e-15)
+    assert O.yarn_mscale(1.0, 1.0) == 1.0          # no scaling without extension
+    assert O.yarn_mscale(math.e ** 10, 1.0) == pytest.approx(2.0, rel=1e-15)
+    # equal mscale and mscale_all_dim leave cos/sin unscaled
+    h = _hyper()
+    c, s = O.rope_cos_sin(np.array([0, 5]), h)
+    assert np.allclose(c[0], 1.0) and np.allclose(s[0], 0.0)
+    np.testing.assert_allclose(c ** 2 + s ** 2, 1.0, rtol=1e-14)
+    # factor 1: sigma is the textbook 1/sqrt(d_qk)
+    assert O.softmax_scale(_hyper(factor=1.0)) == pytest.approx(1 / math.sqrt(192), rel=1e-15)
+    assert O.softmax_scale(_hyper()) == pytest.approx(g["mscale_factor40_mu1"] ** 2 / math.sqrt(192), rel=1e-14)
+
+
+# ---------------------------------------------------------------- RoPE
+def test_rope_hand_quarter_turn():
+    # one pair, frequency chosen so that position 1 is a quarter turn: (1, 0) -> (0, 1)
+    h = _hyper(d=2, theta=1e4, factor=1.0)
+    # with d = 2 the only pair has omega = theta^0 = 1 rad per position
+    x = np.array([[1.0, 0.0]])
+    y = O.rope_interleaved(x, np.array([math.pi / 2]), h)
+    np.testing.assert_allclose(y, [[0.0, 1.0]], atol=1e-15)
+    y = O.rope_interleaved(np.array([[0.0, 1.0]]), np.array([math.pi / 2]), h)
+    np.testing.assert_allclose(y, [[-1.0, 0.0]], atol=1e-15)
+
+
+def test_rope_matches_complex_multiplication():
+    h = _hyper()
+    rng = np.random.default_rng(1)
+    x = rng.standard_normal((7, 64))
+    pos = rng.integers(0, 100000, size=7)
+    y = O.rope_interleaved(x, pos, h)
+    inv = O.yarn_inv_freq(64, 1e4, 40.0, 4096, 32.0, 1.0)
+    z = (x[:, 0::2] + 1j * x[:, 1::2]) * np.exp(1j * pos[:, None] * inv[None, :])
+    np.testing.assert_allclose(y[:, 0::2], z.real, rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(y[:, 1::2], z.imag, rtol=1e-12, atol=1e-12)
+
+
+def test_rope_invariants():
+    h = _hyper()
+    rng = np.random.default_rng(2)
+    q = rng.standard_normal((1, 64))
+    k = rng.standard_normal((1, 64))
+    # position 0 is the identity, pair norms are preserved
+    np.testing.assert_allclose(O.rope_interleaved(q, np.array([0]), h), q, rtol=0, atol=0)
+    y = O.rope_interleaved(q, np.array([12345]), h)
+    np.testing.assert_allclose(y[0, 0::2] ** 2 + y[0, 1::2] ** 2, q[0, 0::2] ** 2 + q[0, 1::2] ** 2, rtol=1e-12)
+    # relative-position invariance of the dot product
+    def dot(pq, pk):
+        return float((O.rope_interleaved(q, np.array([pq]), h) @ O.rope_interleaved(k, np.array([pk]), h).T)[0, 0])
+    assert dot(100, 37) == pytest.approx(dot(1063, 1000), rel=1e-9)
+    # composition R(a) R(b) = R(a + b)
+    ab = O.rope_interleaved(O.rope_interleaved(q, np.array([300]), h), np.array([45]), h)
+    np.testing.assert_allclose(ab, O.rope_interleaved(q, np.array([345]), h), rtol=1e-10, atol=1e-12)
+
+
+# ---------------------------------------------------------------- linear / SiLU
+def test_linear_brute_force():
+    rng = np.random.default_rng(3)
+    x = rng.standard_normal((3, 5))
+    W = rng.standard_normal((4, 5))
+    y = O.linear(x, W)
+    for i in range(3):
+        for j in range(4):
+            s = 0.0
+            for k in range(5):
+                s += x[i, k] * W[j, k]
+            assert y[i, j] == pytest.approx(s, rel=1e-14, abs=1e-15)
+
+
+def test_silu_library_and_closed_form():
+    x = np.linspace(-20, 20, 81)
+    ref = torch.nn.functional.silu(torch.tensor(x, dtype=torch.float64)).numpy()
+    np.testing.assert_allclose(O.silu(x), ref, rtol=1e-14, atol=1e-300)
+    assert O.silu(np.array([0.0]))[0] == 0.0
+    assert O.silu(np.array([1.0]))[0] == pytest.approx(1.0 / (1.0 + math.exp(-1.0)), rel=1e-15)
+
+
+# ---------------------------------------------------------------- attention
+def _attn_case(seed, T=3, L=9, nh=3, dn=4, dr=2, dv=5, dc=6):
+    rng = np.random.default_rng(seed)
+    h = _hyper(d=dr, dn=dn, nh=nh, dv=dv, dc=dc, factor=4.0, L0=16)
+    q = rng.standard_normal((T, nh, dn + dr))
+    cache = rng.standard_normal((L, dc + dr))
+    kv_b = rng.standard_normal((nh * (dn + dv), dc))
+    pos = np.arange(L - T, L)
+    return h, q, cache, kv_b, pos
+
+
+def test_attention_matches_torch_sdpa():
+    h, q, cache, kv_b, pos = _attn_case(4)
+    nh, dn, dv, dc = h["n_heads"], h["qk_nope_dim"], h["v_head_dim"], h["kv_lora_rank"]
+    o = O.mla_attention(q, pos, cache, kv_b, h)
+    # explicit per-head keys / values from the raw kv_b rows
+    W = kv_b.reshape(nh, dn + dv, dc)
+    c, kr = cache[:, :dc], cache[:, dc:]
+    sigma = O.softmax_scale(h)
+    for i, p in enumerate(pos):
+        for hh in range(nh):
+            K = np.concatenate([c[:p + 1] @ W[hh, :dn].T, kr[:p + 1]], axis=1)
+            V = c[:p + 1] @ W[hh, dn:].T
+            ref = torch.nn.functional.scaled_dot_product_attention(
+                torch.tensor(q[i, hh][None, None, None]), torch.tensor(K[None, None]),
+                torch.tensor(V[None, None]), scale=sigma)[0, 0, 0].numpy()
+            np.testing.assert_allclose(o[i, hh], ref, rtol=1e-12, atol=1e-13)
+
+
+def test_attention_special_cases():
+    h, q, cache, kv_b, _ = _attn_case(5, T=1, L=6)
+    nh, dn, dv, dc = h["n_heads"], h["qk_nope_dim"], h["v_head_dim"], h["kv_lora_rank"]
+    W = kv_b.reshape(nh, dn + dv, dc)
+    # a row at position 0 sees only slot 0: output is exactly slot 0's value projection
+    o = O.mla_attention(q, np.array([0]), cache, kv_b, h)
+    for hh in range(nh):
+        np.testing.assert_allclose(o[0, hh], W[hh, dn:] @ cache[0, :dc], rtol=1e-13)
+    # all-equal keys: the output is the mean of the values (equal scores)
+    c2 = cache.copy()
+    c2[:, dc:] = c2[0, dc:]              # same rope key everywhere
+    kv2 = kv_b.reshape(nh, dn + dv, dc).copy()
+    kv2[:, :dn] = 0.0                    # no-position keys contribute nothing
+    o = O.mla_attention(q, np.array([5]), c2, kv2.reshape(-1, dc), h)
+    for hh in range(nh):
+        np.testing.assert_allclose(o[0, hh], kv2[hh, dn:] @ c2[:6, :dc].mean(axis=0), rtol=1e-12)
+
+
+def test_absorbed_equals_unabsorbed():
+    for seed in range(3):
+        h, q, cache, kv_b, pos = _attn_case(10 + seed, T=4, L=12)
+        a = O.mla_attention(q, pos, cache, kv_b, h, absorbed=False)
+        b = O.mla_attention(q, pos, cache, kv_b, h, absorbed=True)
+        np.testing.assert_allclose(a, b, rtol=1e-11, atol=1e-12)
+
+
+def test_attention_is_convex_combination():
+    # softmax rows sum to one: with W_UV = identity-like, outputs stay in the hull of the latents
+    h, q, cache, kv_b, pos = _attn_case(6, T=2, L=7, dv=6, dc=6)
+    nh, dn, dv, dc = h["n_heads"], h["qk_nope_dim"], h["v_head_dim"], h["kv_lora_rank"]
+    W = kv_b.reshape(nh, dn + dv, dc).copy()
+    W[:, dn:] = np.eye(dc)
+    o = O.mla_attention(q, pos, cache, W.reshape(-1, dc), h)
+    ones = np.ones(dc)
+    cache1 = cache.copy()
+    cache1[:, :dc] = 1.0  # every latent equal to one: any convex combination returns one
+    o1 = O.mla_attention(q, pos, cache1, W.reshape(-1, dc), h)
+    np.testing.assert_allclose(o1, np.broadcast_to(ones, o1.shape), rtol=1e-13)
+    for i, p in enumerate(pos):
+        lo = cache[:p + 1, :dc].min(axis=0)
+        hi = cache[:p + 1, :dc].max(axis=0)
+        assert np.all(o[i] >= lo - 1e-12) and np.all(o[i] <= hi + 1e-12)
+
+
+# ---------------------------------------------------------------- argmax / d2t / accept
+def test_argmax_brute_force_and_ties():
+    rng = np.random.default_rng(7)
+    for _ in range(50):
+        v = rng.integers(-5, 5, size=37).astype(np.float64)   # many ties
+        best = None
+        for i, x in enumerate(v):
+            if best is None or x > v[best]:
+                best = i
+        assert O.argmax_lowest(v) == best
+    v = np.zeros(10)
+    v[3] = v[7] = 2.0
+    assert O.argmax_lowest(v) == 3
+    assert O.top2_gap(np.array([1.0, 5.0, 4.5])) == pytest.approx(0.5)
+
+
+def test_d2t_remap():
+    d = np.array([0, 5, 9])
+    assert list(O.d2t_remap(d, np.zeros(10, dtype=np.int32))) == [0, 5, 9]
+    assert list(O.d2t_remap(d, None)) == [0, 5, 9]
+    table = np.arange(10, dtype=np.int32) * 3
+    assert list(O.d2t_remap(d, table)) == [0, 5 + 15, 9 + 27]
+
+
+def test_accept_cases_and_brute_force():
+    rng = np.random.default_rng(8)
+    d = rng.integers(0, 5, size=(40, 6))
+    acc, hist = O.accept(d, d)
+    assert np.all(acc == 6) and hist[6] == 40 and hist.sum() == 40
+    t = d.copy()
+    t[:, 0] += 1
+    acc, hist = O.accept(d, t)
+    assert np.all(acc == 0) and hist[0] == 40
+    t = rng.integers(0, 2, size=(40, 6))
+    d = rng.integers(0, 2, size=(40, 6))
+    acc, hist = O.accept(d, t)
+    for b in range(40):
+        k = next((i for i in range(6) if d[b, i] != t[b, i]), 6)
+        assert acc[b] == k
+    assert list(hist) == [int((acc == k).sum()) for k in range(7)]
