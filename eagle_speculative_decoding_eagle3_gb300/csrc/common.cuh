@@ -1,0 +1,100 @@
+// Shared device helpers of the EAGLE-3 draft-head kernels (sm_103a).
+#pragma once
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+namespace e3 {
+
+typedef __nv_bfloat16 bf16;
+
+constexpr int kWarp = 32;
+
+// --------------------------------------------------------------------------------------------
+// scalar conversions
+__device__ __forceinline__ float to_f(float x) { return x; }
+__device__ __forceinline__ float to_f(bf16 x) { return __bfloat162float(x); }
+template <typename T> __device__ __forceinline__ T from_f(float x);
+template <> __device__ __forceinline__ float from_f<float>(float x) { return x; }
+template <> __device__ __forceinline__ bf16 from_f<bf16>(float x) { return __float2bfloat16_rn(x); }
+
+__device__ __forceinline__ float bf_lo(uint32_t u) { return __uint_as_float(u << 16); }
+__device__ __forceinline__ float bf_hi(uint32_t u) { return __uint_as_float(u & 0xFFFF0000u); }
+
+// --------------------------------------------------------------------------------------------
+// 16-byte loads.  `stream` loads bypass L1 allocation: weights are touched once per call.
+__device__ __forceinline__ uint4 ld_stream16(const void* p) {
+    uint4 r;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w) : "l"(p));
+    return r;
+}
+__device__ __forceinline__ uint4 ld_cached16(const void* p) {
+    return __ldg(reinterpret_cast<const uint4*>(p));
+}
+
+// Eight consecutive elements widened to fp32.
+struct F8 { float v[8]; };
+
+__device__ __forceinline__ void unpack_bf16x8(const uint4& u, float* v) {
+    v[0] = bf_lo(u.x); v[1] = bf_hi(u.x); v[2] = bf_lo(u.y); v[3] = bf_hi(u.y);
+    v[4] = bf_lo(u.z); v[5] = bf_hi(u.z); v[6] = bf_lo(u.w); v[7] = bf_hi(u.w);
+}
+__device__ __forceinline__ void unpack_f32x4(const uint4& u, float* v) {
+    v[0] = __uint_as_float(u.x); v[1] = __uint_as_float(u.y);
+    v[2] = __uint_as_float(u.z); v[3] = __uint_as_float(u.w);
+}
+
+template <typename T> struct Raw8;                     // raw storage of 8 elements
+template <> struct Raw8<bf16> { uint4 a; };
+template <> struct Raw8<float> { uint4 a, b; };
+
+template <bool kStream, typename T> __device__ __forceinline__ Raw8<T> ld8(const T* p);
+template <> __device__ __forceinline__ Raw8<bf16> ld8<true, bf16>(const bf16* p) { return {ld_stream16(p)}; }
+template <> __device__ __forceinline__ Raw8<bf16> ld8<false, bf16>(const bf16* p) { return {ld_cached16(p)}; }
+template <> __device__ __forceinline__ Raw8<float> ld8<true, float>(const float* p) {
+    return {ld_stream16(p), ld_stream16(p + 4)};
+}
+template <> __device__ __forceinline__ Raw8<float> ld8<false, float>(const float* p) {
+    return {ld_cached16(p), ld_cached16(p + 4)};
+}
+__device__ __forceinline__ void widen(const Raw8<bf16>& r, float* v) { unpack_bf16x8(r.a, v); }
+__device__ __forceinline__ void widen(const Raw8<float>& r, float* v) {
+    unpack_f32x4(r.a, v); unpack_f32x4(r.b, v + 4);
+}
+__device__ __forceinline__ Raw8<bf16> zero8(bf16*) { return {make_uint4(0, 0, 0, 0)}; }
+__device__ __forceinline__ Raw8<float> zero8(float*) { return {make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0)}; }
+
+// --------------------------------------------------------------------------------------------
+// reductions
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    return v;
+}
+// Block-wide sum; `scratch` holds >= 32 floats.  All threads receive the result.
+__device__ __forceinline__ float block_sum(float v, float* scratch) {
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5, nw = (blockDim.x + 31) >> 5;
+    v = warp_sum(v);
+    __syncthreads();
+    if (lane == 0) scratch[w] = v;
+    __syncthreads();
+    float t = (lane < nw) ? scratch[lane] : 0.f;
+    return warp_sum(t);
+}
+
+// (value, index) maximum with the lowest index winning ties; NaN never wins.
+__device__ __forceinline__ bool better(float v, int i, float bv, int bi) {
+    return v > bv || (v == bv && i < bi);
+}
+
+__device__ __forceinline__ void set_err(int* err, int bit) { atomicOr(err, bit); }
+
+__device__ __forceinline__ float silu(float x) { return x / (1.f + __expf(-x)); }
+
+}  // namespace e3

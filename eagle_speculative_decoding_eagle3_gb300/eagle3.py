@@ -1,0 +1,175 @@
+"""ctypes binding of libeagle3 (include/eagle3.h): argument marshalling only.
+
+Every function here has the C name and forwards to the library; all compute runs in its CUDA
+kernels.  Pointer arguments accept a torch tensor (its data_ptr), an int address, or None.
+The library must be built first (``build.build()``); loading fails loudly if it is missing.
+"""
+from __future__ import annotations
+
+import ctypes as C
+import os
+
+_LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libeagle3.so")
+
+OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_STATE, ERR_OOM, ERR_CUDA, ERR_DEVICE_RANGE = range(7)
+F32, BF16 = 0, 1
+DEVERR_TOKEN, DEVERR_POSITION, DEVERR_D2T, DEVERR_PAGE, DEVERR_ROWS = 1, 2, 4, 8, 16
+
+
+class eagle3_config_t(C.Structure):
+    _fields_ = [(n, C.c_int32) for n in (
+        "hidden", "n_heads", "q_lora_rank", "kv_lora_rank", "qk_nope_dim", "qk_rope_dim", "v_head_dim",
+        "intermediate", "target_vocab", "draft_vocab", "max_batch", "max_tokens_per_extend", "max_ctx",
+        "page_size", "max_pages_per_seq")] + [(n, C.c_float) for n in (
+            "rms_eps", "rope_theta", "yarn_factor", "yarn_beta_fast", "yarn_beta_slow", "yarn_mscale",
+            "yarn_mscale_all_dim")] + [("yarn_original_max_pos", C.c_int32), ("rope_interleave", C.c_int32),
+                                       ("dtype", C.c_int32)]
+
+
+WEIGHT_NAMES = ("embed", "fc", "input_norm", "hidden_norm", "q_a", "q_a_norm", "q_b", "kv_a", "kv_a_norm", "kv_b",
+                "o", "post_attn_norm", "gate", "up", "down", "final_norm", "lm_head")
+
+
+class eagle3_weights_t(C.Structure):
+    _fields_ = [(n, C.c_void_p) for n in WEIGHT_NAMES]
+
+
+class eagle3_kv_t(C.Structure):
+    _fields_ = [("data", C.c_void_p), ("block_table", C.c_void_p), ("lengths", C.c_void_p),
+                ("num_pages", C.c_int32)]
+
+
+class Eagle3Error(RuntimeError):
+    def __init__(self, fn, status):
+        self.status = status
+        msg = _lib().eagle3_status_string(status).decode()
+        if status == ERR_CUDA:
+            msg += f" (cudaError {_lib().eagle3_last_cuda_error()})"
+        super().__init__(f"{fn}: {msg} [{status}]")
+
+
+_L = None
+
+
+def _lib():
+    global _L
+    if _L is None:
+        if not os.path.exists(_LIB_PATH):
+            raise RuntimeError(f"libeagle3.so is not built ({_LIB_PATH}); run build.build() first")
+        lib = C.CDLL(_LIB_PATH)
+        P = C.c_void_p
+        lib.eagle3_status_string.restype = C.c_char_p
+        lib.eagle3_status_string.argtypes = [C.c_int]
+        lib.eagle3_last_cuda_error.restype = C.c_int32
+        lib.eagle3_draft_create.argtypes = [C.POINTER(eagle3_config_t), C.POINTER(eagle3_weights_t), C.POINTER(P)]
+        lib.eagle3_draft_workspace_bytes.argtypes = [C.POINTER(eagle3_config_t), C.POINTER(C.c_size_t)]
+        lib.eagle3_draft_extend.argtypes = [P, C.POINTER(P), P, P, P, C.c_int32, C.c_int32, C.POINTER(eagle3_kv_t),
+                                            P, P, P]
+        lib.eagle3_draft_decode.argtypes = [P, C.c_int32, P, C.POINTER(eagle3_kv_t), P, P, P, P]
+        lib.eagle3_accept.argtypes = [P, P, C.c_int32, C.c_int32, P, P, P]
+        lib.eagle3_draft_get_error.argtypes = [P, C.POINTER(C.c_int32)]
+        lib.eagle3_draft_clear_error.argtypes = [P, P]
+        lib.eagle3_draft_destroy.argtypes = [P]
+        for f in ("eagle3_draft_create", "eagle3_draft_workspace_bytes", "eagle3_draft_extend", "eagle3_draft_decode",
+                  "eagle3_accept", "eagle3_draft_get_error", "eagle3_draft_clear_error", "eagle3_draft_destroy"):
+            getattr(lib, f).restype = C.c_int
+        _L = lib
+    return _L
+
+
+def library_path() -> str:
+    return _LIB_PATH
+
+
+def _ptr(x):
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    return x.data_ptr()
+
+
+def _stream(s):
+    if s is None:
+        return None
+    if isinstance(s, int):
+        return s
+    return s.cuda_stream
+
+
+def _check(fn, status):
+    if status != OK:
+        raise Eagle3Error(fn, status)
+
+
+def make_config(**fields) -> eagle3_config_t:
+    c = eagle3_config_t()
+    defaults = dict(rms_eps=1e-6, rope_theta=1e4, yarn_factor=1.0, yarn_beta_fast=32.0, yarn_beta_slow=1.0,
+                    yarn_mscale=1.0, yarn_mscale_all_dim=1.0, yarn_original_max_pos=4096, rope_interleave=1)
+    defaults.update(fields)
+    for k, v in defaults.items():
+        setattr(c, k, v)
+    return c
+
+
+def make_weights(tensors) -> eagle3_weights_t:
+    w = eagle3_weights_t()
+    for n in WEIGHT_NAMES:
+        setattr(w, n, _ptr(tensors[n]))
+    return w
+
+
+def make_kv(data, block_table, lengths, num_pages) -> eagle3_kv_t:
+    return eagle3_kv_t(_ptr(data), _ptr(block_table), _ptr(lengths), int(num_pages))
+
+
+def eagle3_status_string(status: int) -> str:
+    return _lib().eagle3_status_string(status).decode()
+
+
+def eagle3_draft_workspace_bytes(config: eagle3_config_t) -> int:
+    n = C.c_size_t()
+    _check("eagle3_draft_workspace_bytes", _lib().eagle3_draft_workspace_bytes(C.byref(config), C.byref(n)))
+    return n.value
+
+
+def eagle3_draft_create(config: eagle3_config_t, weights: eagle3_weights_t) -> int:
+    h = C.c_void_p()
+    _check("eagle3_draft_create", _lib().eagle3_draft_create(C.byref(config), C.byref(weights), C.byref(h)))
+    return h.value
+
+
+def eagle3_draft_extend(handle, aux_hidden, tokens, positions, row_offsets, batch, num_tokens, cache: eagle3_kv_t,
+                        hidden_out=None, logits_out=None, stream=None):
+    aux = (C.c_void_p * 3)(*[_ptr(a) for a in aux_hidden])
+    _check("eagle3_draft_extend", _lib().eagle3_draft_extend(
+        handle, aux, _ptr(tokens), _ptr(positions), _ptr(row_offsets), int(batch), int(num_tokens), C.byref(cache),
+        _ptr(hidden_out), _ptr(logits_out), _stream(stream)))
+
+
+def eagle3_draft_decode(handle, gamma, d2t, cache: eagle3_kv_t, draft_tokens, hidden_out=None, logits_out=None,
+                        stream=None):
+    _check("eagle3_draft_decode", _lib().eagle3_draft_decode(
+        handle, int(gamma), _ptr(d2t), C.byref(cache), _ptr(draft_tokens), _ptr(hidden_out), _ptr(logits_out),
+        _stream(stream)))
+
+
+def eagle3_accept(draft, target, batch, gamma, accepted_len, hist=None, stream=None):
+    _check("eagle3_accept", _lib().eagle3_accept(_ptr(draft), _ptr(target), int(batch), int(gamma),
+                                                 _ptr(accepted_len), _ptr(hist), _stream(stream)))
+
+
+def eagle3_draft_get_error(handle) -> int:
+    v = C.c_int32()
+    st = _lib().eagle3_draft_get_error(handle, C.byref(v))
+    if st not in (OK, ERR_DEVICE_RANGE):
+        raise Eagle3Error("eagle3_draft_get_error", st)
+    return v.value
+
+
+def eagle3_draft_clear_error(handle, stream=None):
+    _check("eagle3_draft_clear_error", _lib().eagle3_draft_clear_error(handle, _stream(stream)))
+
+
+def eagle3_draft_destroy(handle):
+    _check("eagle3_draft_destroy", _lib().eagle3_draft_destroy(handle))

@@ -1,0 +1,93 @@
+"""Device-side harness: puts a seeded workload's tensors in HBM and drives the C ABI.
+
+Used by the tests, ``bench.py`` and ``__graft_entry__.smoke``.  It only moves data (host arrays
+from ``workloads`` to torch device tensors) and calls the binding; every step of the head runs
+in libeagle3's kernels.
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass
+
+import numpy as np
+import torch
+
+from . import eagle3 as E
+
+
+def to_device(arr: np.ndarray, device="cuda") -> torch.Tensor:
+    """Stored array (fp32, int32, or uint16 bf16 bits) -> device tensor of the same bits."""
+    arr = np.ascontiguousarray(arr)
+    if arr.dtype == np.uint16:
+        return torch.from_numpy(arr.view(np.int16)).to(device).view(torch.bfloat16)
+    return torch.from_numpy(arr).to(device)
+
+
+def config_for(w, max_batch=None, max_tokens=None) -> E.eagle3_config_t:
+    return E.make_config(
+        hidden=w.hidden, n_heads=w.n_heads, q_lora_rank=w.q_lora_rank, kv_lora_rank=w.kv_lora_rank,
+        qk_nope_dim=w.qk_nope_dim, qk_rope_dim=w.qk_rope_dim, v_head_dim=w.v_head_dim,
+        intermediate=w.intermediate, target_vocab=w.target_vocab, draft_vocab=w.draft_vocab,
+        max_batch=max_batch or w.batch, max_tokens_per_extend=max_tokens or max(w.batch * w.t_new, w.batch),
+        max_ctx=w.max_ctx, page_size=w.page_size, max_pages_per_seq=w.max_pages_per_seq,
+        rms_eps=w.rms_eps, rope_theta=w.rope_theta, yarn_factor=w.yarn_factor, yarn_beta_fast=w.yarn_beta_fast,
+        yarn_beta_slow=w.yarn_beta_slow, yarn_mscale=w.yarn_mscale, yarn_mscale_all_dim=w.yarn_mscale_all_dim,
+        yarn_original_max_pos=w.yarn_original_max_pos, rope_interleave=1,
+        dtype=E.BF16 if w.dtype == "bf16" else E.F32)
+
+
+@dataclass
+class DeviceCache:
+    data: torch.Tensor
+    block_table: torch.Tensor
+    lengths: torch.Tensor
+    num_pages: int
+
+    def kv(self) -> E.eagle3_kv_t:
+        return E.make_kv(self.data, self.block_table, self.lengths, self.num_pages)
+
+
+class DeviceHead:
+    """A created draft head whose weights live in device tensors owned by this object."""
+
+    def __init__(self, w, stored_weights, device="cuda", max_batch=None, max_tokens=None):
+        self.w = w
+        self.device = device
+        self.tensors = {n: to_device(stored_weights[n], device) for n in E.WEIGHT_NAMES}
+        self.config = config_for(w, max_batch, max_tokens)
+        self.handle = E.eagle3_draft_create(self.config, E.make_weights(self.tensors))
+
+    def close(self):
+        if self.handle:
+            E.eagle3_draft_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    # -- inputs ----------------------------------------------------------------------------
+    def cache(self, paged) -> DeviceCache:
+        return DeviceCache(data=to_device(paged.data, self.device),
+                           block_table=to_device(paged.block_table, self.device),
+                           lengths=to_device(paged.lengths.astype(np.int32), self.device),
+                           num_pages=paged.data.shape[0])
+
+    def extend_inputs(self, ex):
+        return dict(aux=[to_device(a, self.device) for a in ex.aux],
+                    tokens=to_device(ex.tokens, self.device), positions=to_device(ex.positions, self.device),
+                    row_offsets=to_device(ex.row_offsets, self.device))
+
+    # -- calls -----------------------------------------------------------------------------
+    def extend(self, dev_in, cache: DeviceCache, hidden_out=None, logits_out=None, stream=None):
+        batch = dev_in["row_offsets"].numel() - 1
+        E.eagle3_draft_extend(self.handle, dev_in["aux"], dev_in["tokens"], dev_in["positions"],
+                              dev_in["row_offsets"], batch, dev_in["tokens"].numel(), cache.kv(),
+                              hidden_out, logits_out, stream)
+
+    def decode(self, gamma, d2t, cache: DeviceCache, draft_tokens, hidden_out=None, logits_out=None, stream=None):
+        E.eagle3_draft_decode(self.handle, gamma, d2t, cache.kv(), draft_tokens, hidden_out, logits_out, stream)
+
+    def error_word(self) -> int:
+        return E.eagle3_draft_get_error(self.handle)

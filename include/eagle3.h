@@ -1,0 +1,205 @@
+/*
+ * eagle3.h — C ABI of the GB300 (sm_103a) EAGLE-3 draft head for an MLA (DeepseekV3-shaped) target.
+ *
+ * The head, per token: fc fuses three target hidden states (early, middle, late; 3H -> H, no
+ * bias); the token embedding (the target's table) and the fused state are RMS-normalised
+ * separately and concatenated to 2H; one MLA decoder layer runs at 2H input (q_a -> q_lora,
+ * kv_a -> kv_lora + rope, interleaved YaRN RoPE, attention over a one-layer latent KV cache,
+ * o_proj heads*v_head_dim -> H, residual), then a dense SiLU-gated MLP with residual; the
+ * final RMSNorm and the head's own lm_head give logits whose argmax, mapped through the
+ * optional d2t table, is the draft token.  Drafting runs autoregressively for gamma tokens;
+ * greedy acceptance compares drafts with target tokens.
+ *
+ * Sources (page title, section):
+ *   "Eagle3 DeepseekV3 speculative decoding architecture: a full walkthrough of MAX's
+ *    eagle3_deepseekV3 module" (xxmr.cn) — §4 Eagle3MLADraft forward, §5 weight sharing and
+ *    rope_scaling override, §7 one-layer draft KV, §9 prefill = step 0 / decode = steps 1..K,
+ *    §10 greedy acceptance without mid-graph allocation;
+ *   "max.pipelines.architectures.eagle3_deepseekV3" API reference (max.modular.com) —
+ *    Eagle3DeepseekV3DraftConfig defaults, construct_kv_params (one-layer view of the cache);
+ *   "EAGLE head deep dive: inside Model Optimizer's speculative-decoding draft model"
+ *    (discosf.com) — part 2 fc fusion, part 3 doubled first-layer input, part 4 draft
+ *    vocabulary lm_head and the additive d2t table.
+ *
+ * Conventions for every call:
+ *   - Pointers are DEVICE pointers unless the comment says "host".
+ *   - `stream` is a cudaStream_t passed as void* (NULL = the legacy default stream).  All
+ *     compute calls are asynchronous on it and allocate nothing, so they can be recorded in a
+ *     CUDA graph.
+ *   - Weight and cache memory is BORROWED: the caller owns it and keeps it alive and
+ *     unchanged (weights) while the handle uses it.  The handle owns only its workspace.
+ *   - Arguments the host can check are checked before anything is launched; a failed check
+ *     returns a status and launches nothing.  Range errors that only the device can see
+ *     (a token >= target_vocab, a d2t result outside [0, target_vocab), a position >= max_ctx,
+ *     a page index outside the cache) are clamped into range, set a bit in the handle's
+ *     sticky device error word, and are reported by eagle3_draft_get_error.
+ *   - Weights are row-major [out, in] like nn.Linear.  Pointers must be 16-byte aligned and
+ *     every inner dimension a multiple of 8.
+ */
+#ifndef EAGLE3_H
+#define EAGLE3_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define EAGLE3_API __attribute__((visibility("default")))
+#else
+#define EAGLE3_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    EAGLE3_OK = 0,
+    EAGLE3_ERR_INVALID_ARG = 1,   /* null pointer, size out of the configured bounds, misalignment */
+    EAGLE3_ERR_UNSUPPORTED = 2,   /* a shape or dtype this build does not implement */
+    EAGLE3_ERR_STATE = 3,         /* decode before any extend, or batch mismatch */
+    EAGLE3_ERR_OOM = 4,           /* workspace allocation failed at create */
+    EAGLE3_ERR_CUDA = 5,          /* a CUDA runtime call failed (see eagle3_last_cuda_error) */
+    EAGLE3_ERR_DEVICE_RANGE = 6   /* returned by eagle3_draft_get_error when the error word is set */
+} eagle3_status_t;
+
+typedef enum { EAGLE3_F32 = 0, EAGLE3_BF16 = 1 } eagle3_dtype_t;
+
+/* Device error word bits (eagle3_draft_get_error). */
+#define EAGLE3_DEVERR_TOKEN    1   /* an input token id was outside [0, target_vocab) */
+#define EAGLE3_DEVERR_POSITION 2   /* a position was >= max_ctx */
+#define EAGLE3_DEVERR_D2T      4   /* d + d2t[d] was outside [0, target_vocab) */
+#define EAGLE3_DEVERR_PAGE     8   /* a position's page was outside the block table or the cache */
+#define EAGLE3_DEVERR_ROWS     16  /* row_offsets were not non-decreasing within [0, num_tokens] */
+
+/* Head configuration (host struct, copied by create).  Field names follow the DeepseekV3 config
+ * (MAX API reference, Eagle3DeepseekV3DraftConfig). */
+typedef struct {
+    int32_t hidden;               /* H */
+    int32_t n_heads;              /* n_h */
+    int32_t q_lora_rank;          /* d_q */
+    int32_t kv_lora_rank;         /* d_c, the latent width cached per token */
+    int32_t qk_nope_dim;          /* d_n */
+    int32_t qk_rope_dim;          /* d_r, even */
+    int32_t v_head_dim;           /* d_v */
+    int32_t intermediate;         /* I of the dense MLP */
+    int32_t target_vocab;         /* V_t: rows of the (borrowed, target's) embedding */
+    int32_t draft_vocab;          /* V_d: rows of lm_head (== V_t when no d2t is used) */
+    int32_t max_batch;            /* sequences per call */
+    int32_t max_tokens_per_extend;/* rows per extend call */
+    int32_t max_ctx;              /* positions must be < max_ctx */
+    int32_t page_size;            /* cache slots per page */
+    int32_t max_pages_per_seq;    /* columns of the block table */
+    float rms_eps;                /* 1e-6 */
+    float rope_theta;             /* 1e4 */
+    float yarn_factor;            /* 1 disables YaRN */
+    float yarn_beta_fast;         /* 32 */
+    float yarn_beta_slow;         /* 1 */
+    float yarn_mscale;            /* 1 */
+    float yarn_mscale_all_dim;    /* 1 */
+    int32_t yarn_original_max_pos;/* 4096 */
+    int32_t rope_interleave;      /* must be 1: pairs (2i, 2i+1) rotate together */
+    eagle3_dtype_t dtype;         /* storage type of weights, aux states and cache */
+} eagle3_config_t;
+
+/* Device pointers to the head's weights (BORROWED).  Shapes [rows, cols], row-major. */
+typedef struct {
+    const void *embed;          /* [V_t, H]   the target's embedding table */
+    const void *fc;             /* [H, 3H]    columns: early | middle | late */
+    const void *input_norm;     /* [H]        RMSNorm weight of the embedding stream */
+    const void *hidden_norm;    /* [H]        RMSNorm weight of the fused stream */
+    const void *q_a;            /* [d_q, 2H] */
+    const void *q_a_norm;       /* [d_q] */
+    const void *q_b;            /* [n_h*(d_n+d_r), d_q]  per head: nope rows then rope rows */
+    const void *kv_a;           /* [d_c+d_r, 2H]         latent rows then rope rows */
+    const void *kv_a_norm;      /* [d_c] */
+    const void *kv_b;           /* [n_h*(d_n+d_v), d_c]  per head: key rows then value rows */
+    const void *o;              /* [H, n_h*d_v] */
+    const void *post_attn_norm; /* [H] */
+    const void *gate;           /* [I, H] */
+    const void *up;             /* [I, H] */
+    const void *down;           /* [H, I] */
+    const void *final_norm;     /* [H] */
+    const void *lm_head;        /* [V_d, H] */
+} eagle3_weights_t;
+
+/* The one-layer latent cache (BORROWED).  Slot p of sequence b is row (p % page_size) of page
+ * block_table[b * max_pages_per_seq + p / page_size].  A row is [c_kv_hat (d_c) | k_rope (d_r)],
+ * the normalised latent and the ROTATED rope key, in the configured dtype. */
+typedef struct {
+    void *data;                 /* [num_pages, page_size, d_c + d_r] */
+    const int32_t *block_table; /* [batch, max_pages_per_seq] */
+    int32_t *lengths;           /* [batch] cached tokens per sequence; extend/decode advance it */
+    int32_t num_pages;          /* host: pages in `data` */
+} eagle3_kv_t;
+
+typedef struct eagle3_draft eagle3_draft_t;
+
+/* Create a head.  Validates the config (sizes > 0, d_r even, inner dims multiples of 8,
+ * rope_interleave == 1), copies it, records the weight pointers, builds the YaRN cos/sin table
+ * (fp64 on the host, stored fp32) and allocates the workspace on the current device.
+ * Returns EAGLE3_ERR_INVALID_ARG / _UNSUPPORTED / _OOM / _CUDA; *out is NULL on failure. */
+EAGLE3_API eagle3_status_t eagle3_draft_create(const eagle3_config_t *config, const eagle3_weights_t *weights,
+                                    eagle3_draft_t **out);
+
+/* Bytes of device workspace create allocates for `config` (host-only; no CUDA call). */
+EAGLE3_API eagle3_status_t eagle3_draft_workspace_bytes(const eagle3_config_t *config, size_t *bytes);
+
+/* Extend (draft step 0, "Eagle3 DeepseekV3 in MAX" §4 and §9): runs the whole head over
+ * `num_tokens` new rows of `batch` sequences.
+ *   aux_hidden  host array of 3 device pointers, each [num_tokens, H] (early, middle, late)
+ *   tokens      [num_tokens] target-vocab ids paired with the aux rows
+ *   positions   [num_tokens] slot of each row; within a sequence strictly increasing, and every
+ *               slot below a row's position must already hold that sequence's cache entry
+ *   row_offsets [batch + 1] rows of sequence b are [row_offsets[b], row_offsets[b+1]), each >= 1
+ * Appends each row's latent entry at its position, sets lengths[b] = last position + 1, keeps
+ * the last row's hidden (before the final norm) and its draft-vocab argmax in the handle.
+ * Optional debug outputs (NULL to skip): hidden_out [batch, H] fp32, logits_out [batch, V_d] fp32
+ * of the last rows.  1 <= batch <= max_batch, batch <= num_tokens <= max_tokens_per_extend. */
+EAGLE3_API eagle3_status_t eagle3_draft_extend(eagle3_draft_t *d, const void *const aux_hidden[3],
+                                    const int32_t *tokens, const int32_t *positions,
+                                    const int32_t *row_offsets, int32_t batch, int32_t num_tokens,
+                                    eagle3_kv_t *cache, float *hidden_out, float *logits_out,
+                                    void *stream);
+
+/* Decode (draft steps 1..gamma-1, "Eagle3 DeepseekV3 in MAX" §9): writes
+ * draft_tokens[b, 0] = remap(d0) for the argmax d0 kept by extend, then runs gamma - 1
+ * autoregressive steps: step s embeds draft_tokens[:, s-1] at position lengths[b] with the
+ * previous step's hidden as the fused state (fc skipped), appends its latent entry, advances
+ * lengths, and writes draft_tokens[b, s].  remap(d) = d + d2t[d] when d2t is given ("EAGLE head
+ * deep dive" part 4), else d.
+ *   d2t           [V_d] int32 or NULL
+ *   draft_tokens  [batch, gamma] int32 out, target-vocab ids
+ *   hidden_out    [gamma - 1, batch, H] fp32 or NULL (hidden of each decode step)
+ *   logits_out    [gamma - 1, batch, V_d] fp32 or NULL
+ * `batch` is the last extend's.  Returns EAGLE3_ERR_STATE before any extend.  A second decode
+ * without a new extend continues from the same kept state and appends after the current lengths. */
+EAGLE3_API eagle3_status_t eagle3_draft_decode(eagle3_draft_t *d, int32_t gamma, const int32_t *d2t,
+                                    eagle3_kv_t *cache, int32_t *draft_tokens, float *hidden_out,
+                                    float *logits_out, void *stream);
+
+/* Greedy acceptance ("Eagle3 DeepseekV3 in MAX" §10): accepted_len[b] = number of leading
+ * positions i with draft[b, i] == target[b, i] (0..gamma).  hist (optional, [gamma + 1]) is
+ * overwritten with hist[k] = number of sequences with accepted_len == k.  No handle needed. */
+EAGLE3_API eagle3_status_t eagle3_accept(const int32_t *draft, const int32_t *target, int32_t batch,
+                              int32_t gamma, int32_t *accepted_len, int32_t *hist, void *stream);
+
+/* Read the sticky device error word (synchronises the device).  *device_error (host) receives
+ * the EAGLE3_DEVERR_* bits; returns EAGLE3_ERR_DEVICE_RANGE when any bit is set. */
+EAGLE3_API eagle3_status_t eagle3_draft_get_error(eagle3_draft_t *d, int32_t *device_error);
+
+/* Clear the sticky device error word (asynchronous on `stream`). */
+EAGLE3_API eagle3_status_t eagle3_draft_clear_error(eagle3_draft_t *d, void *stream);
+
+/* Free the workspace and the handle (synchronises the device).  NULL is accepted. */
+EAGLE3_API eagle3_status_t eagle3_draft_destroy(eagle3_draft_t *d);
+
+/* Static string for a status code. */
+EAGLE3_API const char *eagle3_status_string(eagle3_status_t s);
+
+/* The last CUDA error code seen by this library on this thread (0 if none). */
+EAGLE3_API int32_t eagle3_last_cuda_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* EAGLE3_H */

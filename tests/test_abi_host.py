@@ -1,0 +1,78 @@
+"""Host-only checks of the C ABI: the library builds, loads, exports every declared entry point,
+and rejects bad arguments before touching a GPU."""
+import ctypes as C
+import os
+import re
+
+import pytest
+
+from eagle_speculative_decoding_eagle3_gb300 import build as B
+from eagle_speculative_decoding_eagle3_gb300 import eagle3 as E
+
+HEADER_DIR = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    B.build()
+    return E._lib()
+
+
+def declared_functions():
+    names = []
+    for f in os.listdir(HEADER_DIR):
+        if f.endswith(".h"):
+            src = open(os.path.join(HEADER_DIR, f)).read()
+            names += re.findall(r"EAGLE3_API\s+[\w\s\*]+?\b(eagle3_\w+)\s*\(", src)
+    return sorted(set(names))
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = declared_functions()
+    assert len(names) >= 10, names
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_status_strings(lib):
+    assert E.eagle3_status_string(0) == "ok"
+    assert "CUDA" in E.eagle3_status_string(E.ERR_CUDA)
+    assert E.eagle3_status_string(99) == "unknown status"
+
+
+def _dsv3_config(**kw):
+    base = dict(hidden=7168, n_heads=128, q_lora_rank=1536, kv_lora_rank=512, qk_nope_dim=128, qk_rope_dim=64,
+                v_head_dim=128, intermediate=18432, target_vocab=129280, draft_vocab=32000, max_batch=1,
+                max_tokens_per_extend=1, max_ctx=4100, page_size=64, max_pages_per_seq=65, yarn_factor=40.0,
+                dtype=E.BF16)
+    base.update(kw)
+    return E.make_config(**base)
+
+
+def test_workspace_bytes_and_config_checks(lib):
+    n = E.eagle3_draft_workspace_bytes(_dsv3_config())
+    assert 0 < n < 1 << 30
+    # bigger batches need more workspace
+    assert E.eagle3_draft_workspace_bytes(_dsv3_config(max_batch=256, max_tokens_per_extend=256)) > n
+    bad = [dict(hidden=0), dict(qk_rope_dim=63), dict(rope_interleave=0), dict(dtype=7), dict(hidden=7164),
+           dict(kv_lora_rank=256), dict(draft_vocab=200000), dict(max_ctx=10_000), dict(rms_eps=0.0)]
+    for kw in bad:
+        with pytest.raises(E.Eagle3Error) as ei:
+            E.eagle3_draft_workspace_bytes(_dsv3_config(**kw))
+        assert ei.value.status in (E.ERR_INVALID_ARG, E.ERR_UNSUPPORTED), kw
+
+
+def test_null_arguments_are_rejected_without_a_gpu(lib):
+    h = C.c_void_p()
+    assert lib.eagle3_draft_create(None, None, C.byref(h)) == E.ERR_INVALID_ARG
+    cfg = _dsv3_config()
+    w = E.eagle3_weights_t()   # all null
+    assert lib.eagle3_draft_create(C.byref(cfg), C.byref(w), C.byref(h)) == E.ERR_INVALID_ARG
+    assert h.value is None
+    kv = E.eagle3_kv_t()
+    aux = (C.c_void_p * 3)()
+    assert lib.eagle3_draft_extend(None, aux, None, None, None, 1, 1, C.byref(kv), None, None, None) == \
+        E.ERR_INVALID_ARG
+    assert lib.eagle3_draft_decode(None, 3, None, C.byref(kv), None, None, None, None) == E.ERR_INVALID_ARG
+    assert lib.eagle3_accept(None, None, 1, 1, None, None, None) == E.ERR_INVALID_ARG
+    assert lib.eagle3_draft_destroy(None) == E.OK

@@ -1,0 +1,46 @@
+"""GPU-vs-oracle parity of whole drafting rounds (extend + gamma-1 decode steps + acceptance),
+through the C ABI, on seeded inputs."""
+import pytest
+
+import workloads as WL
+
+from parity import TOL_BF16, TOL_F32, check_round, run_round
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from eagle_speculative_decoding_eagle3_gb300 import build
+    build.build()
+
+
+def test_tiny_f32_round():
+    w = WL.workload("tiny_f32")
+    gpu, orc, seqs, paged = run_round(w)
+    rep = check_round(w, gpu, orc, seqs, paged, TOL_F32)
+    print(rep)
+
+
+def test_tiny_f32_ragged_and_page_crossing():
+    # ragged contexts, a page boundary inside the new rows, 5 sequences, longer round
+    w = WL.workload("tiny_f32", batch=5, ctx=(1, 45), t_new=7, gamma=5, accept_p=(0.7,) * 5, seed=77)
+    gpu, orc, seqs, paged = run_round(w)
+    print(check_round(w, gpu, orc, seqs, paged, TOL_F32))
+
+
+def test_tiny_f32_empty_cache_no_d2t():
+    # extend from an empty cache (causal attention among the new rows only), identity vocab map
+    w = WL.workload("tiny_f32", ctx=(0, 0), t_new=9, draft_vocab=2048, d2t=None, seed=78)
+    gpu, orc, seqs, paged = run_round(w)
+    print(check_round(w, gpu, orc, seqs, paged, TOL_F32))
+
+
+def test_mla_shaped_bf16_round():
+    # bf16 storage with the DeepseekV3 latent geometry (kv_lora 512, rope 64, nope 128, v 128) on a
+    # narrow hidden size; several tiles of context with ragged lengths
+    w = WL.workload("dsv3_b1", hidden=1024, n_heads=8, q_lora_rank=256, intermediate=2048,
+                    target_vocab=8192, draft_vocab=4096, batch=3, ctx=(100, 700), t_new=3, gamma=4,
+                    accept_p=(0.7,) * 4, seed=79)
+    gpu, orc, seqs, paged = run_round(w)
+    print(check_round(w, gpu, orc, seqs, paged, TOL_BF16))
