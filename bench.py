@@ -1,0 +1,463 @@
+#!/usr/bin/env python
+"""Throughput of the GB300 EAGLE-3 draft head: draft tokens/s per drafting round.
+
+A step is one drafting round of the whole hot path over one batch: extend (T_new new rows per
+sequence: fc fusion, the MLA decoder layer, final norm, lm_head argmax), gamma-1 autoregressive
+decode steps, and greedy acceptance against synthetic target tokens; the cache lengths are
+rewound between rounds so the context stays fixed.  value = batch * gamma * steps / time.
+
+    python bench.py [--gpus N --steps K --warmup W] [--workload dsv3_b1] [--impl reference]
+
+Prints ONE JSON line (rank 0).  Under torchrun every rank runs its own replica of the workload
+(sequences are independent; no collective on the data path) and the time is the max over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import ctypes
+import json
+import os
+import statistics
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "draft tokens/s on 1 GB300 (DSV3-shaped EAGLE3 head); % of HBM / tensor roofline"
+UNIT = "draft tokens/s"
+FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+
+
+# --------------------------------------------------------------------------------------------- setup
+def parse_args(argv=None):
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=100)
+    p.add_argument("--warmup", type=int, default=10)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--workload", default="dsv3_b1")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--e2e-steps", type=int, default=None)
+    return p.parse_args(argv)
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        try:
+            with open(path) as f:
+                d = json.load(f)
+            return d, "measured"
+        except Exception:
+            pass
+    return {}, "fallback"
+
+
+def peak_hbm(peaks):
+    for k in ("hbm_gbs", "hbm_GBs", "hbm"):
+        if k in peaks:
+            return float(peaks[k])
+    return FALLBACK_HBM_GBS
+
+
+# --------------------------------------------------------------------------------------------- clocks
+class ClockSampler:
+    """Samples SM clock and clock-event reasons through NVML (read-only) while running."""
+
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown", 0x2: "applications_clocks_setting"}
+
+    def __init__(self, cuda_index=0):
+        self.samples = []
+        self.max_mhz = None
+        self.ok = False
+        self._stop = threading.Event()
+        try:
+            nv = ctypes.CDLL("libnvidia-ml.so.1")
+            if nv.nvmlInit_v2() != 0:
+                return
+            self.nv = nv
+            self.h = ctypes.c_void_p()
+            idx = cuda_index
+            vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
+            if vis and vis.split(",")[0].strip().isdigit():
+                idx = int(vis.split(",")[cuda_index].strip())
+            if nv.nvmlDeviceGetHandleByIndex_v2(idx, ctypes.byref(self.h)) != 0:
+                return
+            mx = ctypes.c_uint()
+            nv.nvmlDeviceGetMaxClockInfo(self.h, 1, ctypes.byref(mx))
+            self.max_mhz = mx.value
+            self._reason_fn = getattr(nv, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+                getattr(nv, "nvmlDeviceGetCurrentClocksThrottleReasons")
+            self.ok = True
+        except Exception:
+            self.ok = False
+
+    def _one(self):
+        clk = ctypes.c_uint()
+        r = ctypes.c_ulonglong()
+        self.nv.nvmlDeviceGetClockInfo(self.h, 1, ctypes.byref(clk))
+        self._reason_fn(self.h, ctypes.byref(r))
+        self.samples.append((clk.value, r.value))
+
+    def _run(self):
+        while not self._stop.is_set():
+            self._one()
+            time.sleep(0.002)
+
+    def __enter__(self):
+        if self.ok:
+            self._one()
+            self._t = threading.Thread(target=self._run, daemon=True)
+            self._t.start()
+        return self
+
+    def __exit__(self, *a):
+        if self.ok:
+            self._stop.set()
+            self._t.join()
+            self._one()
+
+    def summary(self):
+        if not self.ok or not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvml unavailable"]}
+        mhz = [s[0] for s in self.samples]
+        bits = 0
+        for _, r in self.samples:
+            bits |= r
+        reasons = sorted(n for b, n in self.REASONS.items() if bits & b)
+        return {"sm_mhz": statistics.median(mhz), "sm_max_mhz": self.max_mhz, "reasons": reasons,
+                "samples": len(mhz)}
+
+
+# --------------------------------------------------------------------------------------------- bytes model
+def algorithmic_bytes(w, ctx_lengths):
+    """Algorithmic HBM bytes of each kernel launch kind for one round (weights + KV + activations).
+
+    Returns {kind: (bytes_per_launch, launches_per_round)}; activations are fp32 in the workspace.
+    """
+    ws = 2 if w.dtype == "bf16" else 4
+    B, T, G, H = w.batch, w.t_new, w.gamma, w.hidden
+    nh, dq, dc, dr, dn, dv, I = w.n_heads, w.q_lora_rank, w.kv_lora_rank, w.qk_rope_dim, w.qk_nope_dim, \
+        w.v_head_dim, w.intermediate
+    D, dqk = dc + dr, dn + dr
+    Me, Md = B * T, B          # rows of the extend call / of a decode step
+    steps = G - 1
+    out = {}
+
+    def add(kind, per_launch, n):
+        b, c = out.get(kind, (0.0, 0))
+        # average bytes per launch over the round
+        out[kind] = ((b * c + per_launch * n) / (c + n) if c + n else 0.0, c + n)
+
+    add("fc", H * 3 * H * ws + Me * 3 * H * ws + Me * H * 4, 1)
+    for M, n in ((Me, 1), (Md, steps)):
+        if n == 0:
+            continue
+        add("q_a_kv_a", (dq + D) * 2 * H * ws + M * 2 * H * 4 + M * (dq + D) * 4, n)
+        add("q_b", nh * dqk * dq * ws + M * dq * 4 + M * nh * dqk * 4, n)
+        add("absorb", nh * dn * dc * ws + M * nh * dqk * 4 + M * nh * D * 4, n)
+        add("combine_unabsorb", nh * dv * dc * ws + M * nh * dv * 4, n)
+        add("o_proj", H * nh * dv * ws + M * nh * dv * 4 + 2 * M * H * 4, n)
+        add("gate_up_silu", 2 * I * H * ws + M * H * 4 + M * I * 4, n)
+        add("down", H * I * ws + M * I * 4 + 2 * M * H * 4, n)
+        add("lm_head_argmax", w.draft_vocab * H * ws + B * H * 4, n)
+    # attention reads each row's context (pos + 1 latent rows)
+    L = [int(x) for x in ctx_lengths]
+    kv_ext = sum(sum(l + j + 1 for j in range(T)) for l in L) * D * ws
+    add("attention", kv_ext, 1)
+    for s in range(1, G):
+        add("attention", sum(l + T + s for l in L) * D * ws, 1)
+    return out
+
+
+# --------------------------------------------------------------------------------------------- our arm
+def run_ours(args, ws, rank, local):
+    import numpy as np
+    import torch
+
+    import workloads as WL
+    from eagle_speculative_decoding_eagle3_gb300 import build as BLD
+    from eagle_speculative_decoding_eagle3_gb300 import eagle3 as E
+    from eagle_speculative_decoding_eagle3_gb300 import harness as HN
+
+    torch.cuda.set_device(local)
+    BLD.build()
+    w = WL.workload(args.workload)
+    B, G, H = w.batch, w.gamma, w.hidden
+    stored = WL.make_weights(w)
+    lengths = WL.context_lengths(w)
+    paged = WL.make_cache(w, lengths)
+    ex = WL.make_extend(w, lengths)
+    d2t = WL.make_d2t(w)
+
+    head = HN.DeviceHead(w, stored)
+    cache = head.cache(paged)
+    len0 = cache.lengths.clone()
+    din = head.extend_inputs(ex)
+    d2t_dev = HN.to_device(d2t) if d2t is not None else None
+    toks = torch.zeros((B, G), dtype=torch.int32, device="cuda")
+    acc = torch.zeros(B, dtype=torch.int32, device="cuda")
+    hist = torch.zeros(G + 1, dtype=torch.int32, device="cuda")
+    stream = torch.cuda.current_stream()
+
+    # one round to fix the drafts, then synthetic targets from them (the drafts are deterministic)
+    head.extend(din, cache, stream=stream)
+    head.decode(G, d2t_dev, cache, toks, stream=stream)
+    torch.cuda.synchronize()
+    tgt = torch.from_numpy(WL.synthetic_targets(w, toks.cpu().numpy())).cuda()
+    assert head.error_word() == 0
+
+    def step(st):
+        cache.lengths.copy_(len0)
+        head.extend(din, cache, stream=st)
+        head.decode(G, d2t_dev, cache, toks, stream=st)
+        E.eagle3_accept(toks, tgt, B, G, acc, hist, stream=st)
+
+    for _ in range(args.warmup):
+        step(stream)
+    torch.cuda.synchronize()
+    barrier(ws)
+
+    # The timed region is one CUDA graph holding `steps` rounds, so host launch cost stays out of it.
+    # The library's tracing events are captured inside the graph: after the timed replay they hold
+    # that replay's per-kernel intervals.
+    E.eagle3_draft_profile_reset(head.handle)
+    E.eagle3_draft_profile_enable(head.handle, True)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        cap = torch.cuda.current_stream()
+        for _ in range(args.steps):
+            step(cap)
+    graph.replay()                      # untimed: uploads the graph and warms it
+    torch.cuda.synchronize()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clocks:
+        barrier(ws)
+        ev0.record(stream)
+        graph.replay()
+        ev1.record(stream)
+        torch.cuda.synchronize()
+    barrier(ws)
+    ms = ev0.elapsed_time(ev1)
+    ms_max = reduce_max(ms, ws)
+    prof = {}
+    launches = 0
+    for k in range(E.PROF_KINDS):
+        name, tot, timed, n = E.eagle3_draft_profile_read(head.handle, k)
+        if n:
+            prof[name] = (tot, timed)
+            launches += n
+    E.eagle3_draft_profile_enable(head.handle, False)
+    launches += args.steps  # one acceptance launch per round
+    assert head.error_word() == 0
+    del graph
+
+    # ---------------------------------------------------------------- end to end, host buffers
+    e2e_steps = args.e2e_steps or max(3, args.steps)
+    pin = lambda t: t.cpu().pin_memory()  # noqa: E731
+    h_aux = [pin(a) for a in din["aux"]]
+    h_tok, h_pos, h_ro = pin(din["tokens"]), pin(din["positions"]), pin(din["row_offsets"])
+    h_tgt = pin(tgt)
+    o_toks = torch.empty((B, G), dtype=torch.int32).pin_memory()
+    o_acc = torch.empty(B, dtype=torch.int32).pin_memory()
+    o_hist = torch.empty(G + 1, dtype=torch.int32).pin_memory()
+    d_in = {k: (v if k != "aux" else list(v)) for k, v in din.items()}
+    h2d = sum(a.numel() * a.element_size() for a in h_aux) + sum(
+        t.numel() * t.element_size() for t in (h_tok, h_pos, h_ro, h_tgt))
+    d2h = sum(t.numel() * t.element_size() for t in (o_toks, o_acc, o_hist))
+
+    def e2e_step():
+        for a, h in zip(d_in["aux"], h_aux):
+            a.copy_(h, non_blocking=True)
+        d_in["tokens"].copy_(h_tok, non_blocking=True)
+        d_in["positions"].copy_(h_pos, non_blocking=True)
+        d_in["row_offsets"].copy_(h_ro, non_blocking=True)
+        tgt.copy_(h_tgt, non_blocking=True)
+        cache.lengths.copy_(len0)
+        head.extend(d_in, cache, stream=stream)
+        head.decode(G, d2t_dev, cache, toks, stream=stream)
+        E.eagle3_accept(toks, tgt, B, G, acc, hist, stream=stream)
+        o_toks.copy_(toks, non_blocking=True)
+        o_acc.copy_(acc, non_blocking=True)
+        o_hist.copy_(hist, non_blocking=True)
+        stream.synchronize()
+
+    for _ in range(3):
+        e2e_step()
+    barrier(ws)
+    t0 = time.perf_counter()
+    for _ in range(e2e_steps):
+        e2e_step()
+    e2e_s = reduce_max(time.perf_counter() - t0, ws)
+
+    # ---------------------------------------------------------------- roofline of the dominant kernel
+    peaks, src = measured_peaks()
+    hbm = peak_hbm(peaks)
+    model = algorithmic_bytes(w, lengths)
+    kernels = {}
+    for name, (tot, n) in prof.items():
+        per = tot / n
+        entry = {"launches": n, "avg_us": round(per * 1e3, 2), "share": round(tot / sum(t for t, _ in prof.values()), 4)}
+        if name in model and model[name][0] > 0:
+            gbs = model[name][0] / (per * 1e-3) / 1e9
+            entry["algo_bytes"] = int(model[name][0])
+            entry["achieved_gbs"] = round(gbs, 1)
+            entry["hbm_frac"] = round(gbs / hbm, 4)
+        kernels[name] = entry
+    dom = max(prof, key=lambda k: prof[k][0])
+    dom_bytes = model.get(dom, (0.0, 0))[0]
+    dom_avg_s = prof[dom][0] / prof[dom][1] * 1e-3
+    achieved = dom_bytes / dom_avg_s / 1e9 if dom_avg_s > 0 else 0.0
+    round_bytes = sum(b * n for b, n in model.values())
+    step_s = ms_max / args.steps * 1e-3
+    tok_per_round = B * G
+    value = ws * tok_per_round * args.steps / (ms_max * 1e-3)
+
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": ws, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms_max / args.steps, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "data": "synthetic (seeded; random-init weights)",
+        "config": {"workload": f"{w.name}: DSV3-shaped EAGLE-3 head, batch {B}, context {w.ctx[0]}-{w.ctx[1]}, "
+                               f"T_new {w.t_new}, gamma {G}, draft vocab {w.draft_vocab}"
+                               + (" with d2t" if w.d2t else ""),
+                   "batch": B, "gamma": G, "ctx": list(w.ctx), "draft_vocab": w.draft_vocab,
+                   "step": "extend + (gamma-1) decode steps + acceptance",
+                   "l2": f"inputs larger than L2: {round_bytes / 1e9:.2f} GB of weights+KV streamed per step",
+                   "parallelism": f"replicas x{ws} (sequence-sharded, no collective)"},
+        "roofline": {"bound": "hbm", "kernel": dom, "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
+                     "frac": round(achieved / hbm, 4), "traffic": None,
+                     "peak_source": f"{src} ({'MEASURED_PEAKS.json hbm' if src == 'measured' else 'fallback 6.8 TB/s'})"},
+        "step_roofline": {"algo_bytes": int(round_bytes), "achieved_gbs": round(round_bytes / step_s / 1e9, 1),
+                          "frac": round(round_bytes / step_s / 1e9 / hbm, 4)},
+        "kernels": kernels,
+        "e2e": {"value": round(ws * tok_per_round * e2e_steps / e2e_s, 2), "unit": UNIT,
+                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)},
+        "gpu_launches": int(launches),
+        "clocks": clocks.summary(),
+    }
+    head.close()
+    return line, w, stored, lengths, paged, d2t
+
+
+# --------------------------------------------------------------------------------------------- oracle timing
+def oracle_sample(w, stored, lengths, seconds_budget=30.0, decode_only=False, seq=0):
+    """Time the fp64 oracle on a bounded sample: one round (extend + decode steps) of one sequence,
+    or a single decode step.  Returns (tokens, seconds, description)."""
+    import numpy as np
+
+    import oracle as O
+    import workloads as WL
+    W = WL.F32View(stored)
+    cache = [O.SeqCache(WL.as_f32(WL.cache_rows(w, seq, int(lengths[seq]))), w.max_ctx)]
+    ex = WL.make_extend(w, lengths, seqs=[seq])
+    d2t = WL.make_d2t(w)
+    hy = w.hyper()
+    t0 = time.perf_counter()
+    if decode_only:
+        rng = np.random.default_rng(seq)
+        h = rng.standard_normal((1, w.hidden))
+        O.draft_decode_step(hy, W, h, np.array([7]), cache, absorbed=True)
+        return 1, time.perf_counter() - t0, f"one fp64 decode step of sequence {seq} (absorbed attention form)"
+    toks = 0
+    aux = [WL.as_f32(a) for a in ex.aux]
+    out = O.draft_extend(hy, W, aux, ex.tokens, ex.positions, ex.row_offsets, cache, absorbed=True)
+    toks += 1
+    h, t = out["h2"], O.d2t_remap(out["d"], d2t)
+    for s in range(1, w.gamma):
+        if time.perf_counter() - t0 > seconds_budget:
+            break
+        st = O.draft_decode_step(hy, W, h, t, cache, absorbed=True)
+        h, t = st["h2"], O.d2t_remap(st["d"], d2t)
+        toks += 1
+    return toks, time.perf_counter() - t0, \
+        f"fp64 oracle: extend (T_new {w.t_new}) + {toks - 1} decode steps of sequence {seq} of {w.batch}"
+
+
+def host_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count()
+
+
+def run_reference(args, rank):
+    """The oracle as it stands, timed on the host cores; each step is one fp64 decode step of one sequence."""
+    import workloads as WL
+    w = WL.workload(args.workload)
+    stored = WL.make_weights(w)
+    lengths = WL.context_lengths(w)
+    for _ in range(args.warmup):
+        oracle_sample(w, stored, lengths, decode_only=True)
+    tot_t, tot_k = 0.0, 0
+    for i in range(args.steps):
+        k, t, desc = oracle_sample(w, stored, lengths, decode_only=True, seq=i % w.batch)
+        tot_t += t
+        tot_k += k
+    value = tot_k / tot_t
+    return {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": UNIT, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(tot_t / args.steps * 1e3, 2),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (seeded; random-init weights)",
+            "config": {"workload": f"{w.name}", "batch": w.batch, "gamma": w.gamma,
+                       "sample": "each step: one decode step (1 draft token) of one sequence"},
+            "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": host_cores(), "kind": "oracle",
+                             "sample": desc},
+            "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+# --------------------------------------------------------------------------------------------- distributed
+def barrier(ws):
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def reduce_max(x, ws):
+    if ws <= 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([float(x)], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    ws, rank, local = dist_env()
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args, rank)), flush=True)
+        return 0
+    if ws > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    line, w, stored, lengths, paged, d2t = run_ours(args, ws, rank, local)
+    if rank == 0 and not args.no_cpu_baseline:
+        toks, secs, desc = oracle_sample(w, stored, lengths)
+        line["cpu_baseline"] = {"value": round(toks / secs, 4), "unit": UNIT, "cores": host_cores(),
+                                "kind": "oracle", "sample": desc}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,4 +1,12 @@
 // C ABI of the EAGLE-3 MLA draft head: handle, argument checks, workspace, launch sequence.
+//
+// Two execution paths share one handle and one workspace:
+//  * rows <= 8 (batch-1 / small-batch decode): every linear layer is a weight-streaming GEMV on fp32
+//    activations (bound by reading the weights once);
+//  * rows > 8 with bf16 weights: every linear layer runs on the tcgen05 tensor-core GEMM with bf16
+//    activations produced by the preceding kernel, and the per-head absorb / value up-projection are
+//    batched tensor-core GEMMs.
+// Attention is the same absorbed split-K kernel on both paths.
 #include <math.h>
 #include <stdlib.h>
 #include <string.h>
@@ -10,8 +18,24 @@
 #include "kernels.h"
 
 using namespace e3;
+typedef __nv_bfloat16 bf16_t;
 
 static thread_local int g_last_cuda_error = 0;
+
+namespace {
+enum Kind {
+    K_FC = 0, K_EMBED, K_QKV_A, K_LATENT, K_Q_B, K_ABSORB, K_ATTN, K_COMBINE, K_O_PROJ, K_POST_NORM,
+    K_GATE_UP, K_DOWN, K_FINAL, K_LM_HEAD, K_ARGMAX, K_EMIT, K_ROPE_Q, K_UNABSORB, K_COUNT
+};
+static_assert(K_COUNT <= EAGLE3_PROF_KINDS, "profile kinds");
+const char* kKindNames[EAGLE3_PROF_KINDS] = {
+    "fc", "embed_norms", "q_a_kv_a", "latent_rope_append", "q_b", "absorb", "attention", "combine_unabsorb",
+    "o_proj", "post_attn_norm", "gate_up_silu", "down", "final_norm", "lm_head_argmax", "argmax_remap",
+    "emit_first", "rope_q", "unabsorb", "", "", "", "", "", ""};
+constexpr int kProfPairs = 32768;
+constexpr int kGemvMaxRows = 8;          // rows above this take the tensor-core path (bf16 heads)
+constexpr size_t kSplitKBytes = 64u << 20;
+}  // namespace
 
 struct eagle3_draft {
     eagle3_config_t cfg;
@@ -22,20 +46,66 @@ struct eagle3_draft {
     size_t ws_bytes = 0;
     int m_cap = 0;          // rows per call
     int splits_cap = 0;     // attention splits bound
-    int npart_lm = 0;       // lm_head argmax partials per row
-    // workspace views
+    int npart = 0;          // lm_head argmax partials per row of the latest scoring
+    bool tc_ok = false;     // the tensor-core path is available for this head
+    // workspace views (fp32 unless named _bf)
     float *f = nullptr, *carry = nullptr, *x = nullptr, *cqkv = nullptr, *cq_hat = nullptr, *q = nullptr,
           *qa = nullptr, *part_o = nullptr, *part_ml = nullptr, *o = nullptr, *h1 = nullptr, *y = nullptr,
           *mlp = nullptr, *h2 = nullptr, *z = nullptr, *pval = nullptr, *rope_cos = nullptr,
-          *rope_sin = nullptr;
+          *rope_sin = nullptr, *tc_part = nullptr;
+    bf16_t *qa_bf = nullptr, *x_bf = nullptr, *cqh_bf = nullptr, *q_bf = nullptr, *olat_bf = nullptr,
+           *o_bf = nullptr, *y_bf = nullptr, *m_bf = nullptr, *z_bf = nullptr, *wukt = nullptr;
     int *pidx = nullptr, *row_seq = nullptr, *row_pos = nullptr, *d0 = nullptr, *tok_in = nullptr,
         *err = nullptr;
     size_t part_rows = 0;   // capacity of the attention partials in (row, split) pairs
     int batch = 0;
     bool have_extend = false;
+    // native tracing: event pairs around launches, accumulated per kernel kind
+    bool prof_on = false;
+    std::vector<cudaEvent_t> prof_ev;
+    std::vector<int> prof_kind;
+    int prof_used = 0;
+    double prof_ms[EAGLE3_PROF_KINDS] = {};
+    int64_t prof_n[EAGLE3_PROF_KINDS] = {};
+    int64_t launches[EAGLE3_PROF_KINDS] = {};
 };
 
 namespace {
+
+// Runs `launch` (returning cudaError_t) bracketed by profiling events when enabled.
+template <typename F>
+cudaError_t traced(eagle3_draft& d, int kind, cudaStream_t st, F&& launch) {
+    d.launches[kind] += 1;
+    const bool rec = d.prof_on && d.prof_used < kProfPairs;
+    if (rec) {
+        cudaError_t e = cudaEventRecord(d.prof_ev[2 * d.prof_used], st);
+        if (e != cudaSuccess) return e;
+    }
+    cudaError_t e = launch();
+    if (e != cudaSuccess) return e;
+    if (rec) {
+        e = cudaEventRecord(d.prof_ev[2 * d.prof_used + 1], st);
+        if (e != cudaSuccess) return e;
+        d.prof_kind[d.prof_used] = kind;
+        d.prof_used += 1;
+    }
+    return cudaSuccess;
+}
+
+cudaError_t prof_flush(eagle3_draft& d) {
+    if (d.prof_used == 0) return cudaSuccess;
+    cudaError_t e = cudaEventSynchronize(d.prof_ev[2 * d.prof_used - 1]);
+    if (e != cudaSuccess) return e;
+    for (int i = 0; i < d.prof_used; ++i) {
+        float ms = 0.f;
+        e = cudaEventElapsedTime(&ms, d.prof_ev[2 * i], d.prof_ev[2 * i + 1]);
+        if (e != cudaSuccess) return e;
+        d.prof_ms[d.prof_kind[i]] += ms;
+        d.prof_n[d.prof_kind[i]] += 1;
+    }
+    d.prof_used = 0;
+    return cudaSuccess;
+}
 
 eagle3_status_t cuda_fail(cudaError_t e) {
     g_last_cuda_error = (int)e;
@@ -47,14 +117,18 @@ eagle3_status_t cuda_fail(cudaError_t e) {
         cudaError_t _e = (call);                       \
         if (_e != cudaSuccess) return cuda_fail(_e);   \
     } while (0)
+#define E3_TRY(call)                                   \
+    do {                                               \
+        cudaError_t _e = (call);                       \
+        if (_e != cudaSuccess) return _e;              \
+    } while (0)
 
 bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
 
-
-constexpr int kHeadsPerCta = 16;
-
 int attn_splits(const eagle3_draft& d, int M) {
-    const int hg = (d.cfg.n_heads + kHeadsPerCta - 1) / kHeadsPerCta;
+    const int hpc = attention_heads_per_cta(d.cfg.dtype == EAGLE3_BF16 ? BF16 : F32, d.cfg.kv_lora_rank,
+                                            d.cfg.qk_rope_dim);
+    const int hg = (d.cfg.n_heads + hpc - 1) / hpc;
     const long want = 2L * d.num_sms;
     long s = (want + (long)M * hg - 1) / ((long)M * hg);
     if (s < 1) s = 1;
@@ -80,6 +154,8 @@ eagle3_status_t check_config(const eagle3_config_t* c) {
     if (!attention_supported(c->kv_lora_rank, c->qk_rope_dim, c->qk_nope_dim, c->v_head_dim))
         return EAGLE3_ERR_UNSUPPORTED;
     if (c->draft_vocab > c->target_vocab) return EAGLE3_ERR_INVALID_ARG;
+    // row kernels hold a row in registers: H <= 16384, q_lora_rank and kv_lora_rank <= 2048
+    if (c->hidden > 16384 || c->q_lora_rank > 2048 || c->kv_lora_rank > 2048) return EAGLE3_ERR_UNSUPPORTED;
     if (!(c->rms_eps > 0.f) || !(c->rope_theta > 1.f) || !(c->yarn_factor >= 1.f) ||
         c->yarn_original_max_pos <= 0)
         return EAGLE3_ERR_INVALID_ARG;
@@ -97,6 +173,17 @@ eagle3_status_t check_weights(const eagle3_weights_t* w) {
     return EAGLE3_OK;
 }
 
+// The tensor-core path needs bf16 weights, every GEMM K a multiple of 64 and the q_a | kv_a split on a
+// 128-row tile boundary; otherwise large calls stay on the GEMV path.
+bool tc_supported(const eagle3_config_t& c) {
+    if (c.dtype != EAGLE3_BF16) return false;
+    const long ks[] = {c.hidden, c.q_lora_rank, c.kv_lora_rank, c.qk_nope_dim, (long)c.n_heads * c.v_head_dim,
+                       c.intermediate, c.qk_nope_dim + c.qk_rope_dim};
+    for (long k : ks)
+        if (k % 64) return false;
+    return c.q_lora_rank % 128 == 0 && c.kv_lora_rank == 512 && c.qk_rope_dim == 64;
+}
+
 // Workspace layout: one allocation carved into 256-byte aligned views.
 struct Layout {
     size_t off = 0;
@@ -108,8 +195,9 @@ struct Layout {
 };
 
 struct Offsets {
-    size_t f, carry, x, cqkv, cq_hat, q, qa, part_o, part_ml, o, h1, y, mlp, h2, z, pval, pidx, rope_cos,
-        rope_sin, row_seq, row_pos, d0, tok_in, err, total;
+    size_t f, carry, x, cqkv, cq_hat, q, qa, qa_bf, part_o, part_ml, o, h1, y, mlp, h2, z, pval, pidx, rope_cos,
+        rope_sin, row_seq, row_pos, d0, tok_in, err, x_bf, cqh_bf, q_bf, olat_bf, o_bf, y_bf, m_bf, z_bf, wukt,
+        tc_part, total;
     int m_cap, splits_cap, npart;
     size_t part_rows;
 };
@@ -118,7 +206,9 @@ Offsets plan(const eagle3_config_t& c, int num_sms) {
     Offsets o;
     const long M = c.max_tokens_per_extend > c.max_batch ? c.max_tokens_per_extend : c.max_batch;
     const long H = c.hidden, nh = c.n_heads, dqk = c.qk_nope_dim + c.qk_rope_dim;
-    const long D = c.kv_lora_rank + c.qk_rope_dim;
+    const long D = c.kv_lora_rank + c.qk_rope_dim, B = c.max_batch;
+    const bool tc = tc_supported(c);
+    const long Mt = tc ? M : 0;       // rows of the bf16 activation copies
     o.m_cap = (int)M;
     o.splits_cap = (c.max_ctx + 31) / 32;
     if (o.splits_cap > 64) o.splits_cap = 64;
@@ -126,14 +216,15 @@ Offsets plan(const eagle3_config_t& c, int num_sms) {
     // rows x splits never exceeds M + 2 * num_sms (splits = ceil(2 * SMs / (M * groups)) for small M)
     o.part_rows = (size_t)M + 2 * (size_t)num_sms + 1;
     Layout L;
-    const size_t f4 = 4;
+    const size_t f4 = 4, b2 = 2;
     o.f = L.take(M * H * f4);
-    o.carry = L.take((size_t)c.max_batch * H * f4);
+    o.carry = L.take(B * H * f4);
     o.x = L.take(M * 2 * H * f4);
     o.cqkv = L.take(M * (c.q_lora_rank + D) * f4);
     o.cq_hat = L.take(M * c.q_lora_rank * f4);
     o.q = L.take(M * nh * dqk * f4);
     o.qa = L.take(M * nh * D * f4);
+    o.qa_bf = L.take(M * nh * D * b2);
     o.part_o = L.take(o.part_rows * nh * c.kv_lora_rank * f4);
     o.part_ml = L.take(o.part_rows * nh * 2 * f4);
     o.o = L.take(M * nh * c.v_head_dim * f4);
@@ -141,16 +232,26 @@ Offsets plan(const eagle3_config_t& c, int num_sms) {
     o.y = L.take(M * H * f4);
     o.mlp = L.take(M * (size_t)c.intermediate * f4);
     o.h2 = L.take(M * H * f4);
-    o.z = L.take((size_t)c.max_batch * H * f4);
-    o.pval = L.take((size_t)c.max_batch * o.npart * f4);
-    o.pidx = L.take((size_t)c.max_batch * o.npart * 4);
+    o.z = L.take(B * H * f4);
+    o.pval = L.take(B * o.npart * f4);
+    o.pidx = L.take(B * o.npart * 4);
     o.rope_cos = L.take((size_t)c.max_ctx * (c.qk_rope_dim / 2) * f4);
     o.rope_sin = L.take((size_t)c.max_ctx * (c.qk_rope_dim / 2) * f4);
     o.row_seq = L.take(M * 4);
     o.row_pos = L.take(M * 4);
-    o.d0 = L.take((size_t)c.max_batch * 4);
-    o.tok_in = L.take((size_t)c.max_batch * 4);
+    o.d0 = L.take(B * 4);
+    o.tok_in = L.take(B * 4);
     o.err = L.take(4);
+    o.x_bf = L.take(Mt * 2 * H * b2);
+    o.cqh_bf = L.take(Mt * c.q_lora_rank * b2);
+    o.q_bf = L.take(Mt * nh * dqk * b2);
+    o.olat_bf = L.take(Mt * nh * c.kv_lora_rank * b2);
+    o.o_bf = L.take(Mt * nh * c.v_head_dim * b2);
+    o.y_bf = L.take(Mt * H * b2);
+    o.m_bf = L.take(Mt * (size_t)c.intermediate * b2);
+    o.z_bf = L.take((tc ? B : 0) * H * b2);
+    o.wukt = L.take(tc ? (size_t)nh * c.kv_lora_rank * c.qk_nope_dim * b2 : 0);
+    o.tc_part = L.take(tc ? kSplitKBytes : 0);
     o.total = L.off;
     return o;
 }
@@ -206,77 +307,202 @@ RowArgs row_args(const eagle3_draft& d, const eagle3_kv_t* kv) {
     return a;
 }
 
-GemvArgs gemv1(const eagle3_draft& d, const float* a, long lda, int K, const void* w, int N, float* y, long ldy) {
-    GemvArgs g;
-    memset(&g, 0, sizeof(g));
-    g.a[0] = a; g.lda[0] = lda; g.ka[0] = K; g.na = 1;
-    g.w[0] = w; g.nw[0] = N; g.nseg_w = 1;
-    g.N = N; g.K = K;
-    g.a_type = F32;
-    g.w_type = d.cfg.dtype == EAGLE3_BF16 ? BF16 : F32;
-    g.y = y; g.ldy = ldy;
-    return g;
+// ---------------------------------------------------------------------------------------------- linear
+// One bias-free linear layer y = X W^T + epilogue, on whichever path the row count selects.
+struct Lin {
+    int M = 0, N = 0, K = 0, epi = EPI_STORE;
+    // activations: up to 3 K-segments; fp32 for the GEMV path, bf16 for the tensor-core path
+    int na = 1;
+    const void* a32[3] = {nullptr, nullptr, nullptr};
+    bool a32_is_bf16 = false;       // the GEMV path may read bf16 activations (the aux states)
+    const bf16_t* a16[3] = {nullptr, nullptr, nullptr};
+    long lda[3] = {0, 0, 0};
+    int ka[3] = {0, 0, 0};
+    // weights: segment 0 rows [0, n0rows), segment 1 the rest (GLU: gate and up, N rows each)
+    const void* w0 = nullptr;
+    const void* w1 = nullptr;
+    int n0rows = 0, n1rows = 0;
+    float* y = nullptr; long ldy = 0;          // fp32 output (GEMV path always; tensor path when set)
+    bf16_t* ybf = nullptr; long ldybf = 0;     // bf16 output for the next tensor-core GEMM
+    const float* resid = nullptr; long ldr = 0;
+    float* logits = nullptr; long ldl = 0;     // ARGMAX debug output
+};
+
+bool use_tc(const eagle3_draft& d, int M) { return d.tc_ok && M > kGemvMaxRows; }
+
+// split-K count for a tensor-core GEMM: enough CTAs to stream the weights with every SM
+int tc_splits(const eagle3_draft& d, int M, int N, int K, int bn, bool glu) {
+    const long tiles = (long)((N + 127) / 128) * ((M + bn - 1) / bn);
+    if (tiles >= d.num_sms) return 1;
+    long s = (2L * d.num_sms + tiles - 1) / tiles;
+    const long kmax = K / 64 / 4;                // at least 4 K-blocks per split
+    if (s > kmax) s = kmax;
+    const long per = (long)(glu ? 2 : 1) * M * N * 4;
+    while (s > 1 && s * per > (long)kSplitKBytes) --s;
+    return s < 1 ? 1 : (int)s;
 }
 
-// The decoder chain from the concatenated input x to the scored hidden / argmax partials.
+cudaError_t run_linear(eagle3_draft& d, const Lin& L, int kind, cudaStream_t st) {
+    if (!use_tc(d, L.M)) {
+        GemvArgs g;
+        memset(&g, 0, sizeof(g));
+        for (int i = 0; i < L.na; ++i) { g.a[i] = L.a32[i]; g.lda[i] = L.lda[i]; g.ka[i] = L.ka[i]; }
+        g.na = L.na;
+        g.w[0] = L.w0; g.w[1] = L.w1;
+        g.nw[0] = L.n0rows; g.nw[1] = L.n1rows;
+        g.nseg_w = (L.epi != EPI_GLU && L.w1) ? 2 : 1;
+        g.M = L.M; g.N = L.N; g.K = L.K;
+        g.a_type = L.a32_is_bf16 ? BF16 : F32;
+        g.w_type = d.cfg.dtype == EAGLE3_BF16 ? BF16 : F32;
+        g.y = L.y; g.ldy = L.ldy;
+        g.resid = L.resid; g.ldr = L.ldr;
+        g.pval = d.pval; g.pidx = d.pidx; g.logits = L.logits; g.ldl = L.ldl;
+        if (L.epi == EPI_ARGMAX) d.npart = gemv_argmax_parts(L.N, d.num_sms);
+        return traced(d, kind, st, [&] { return launch_gemv(g, L.epi, d.num_sms, st); });
+    }
+    TcParams p;
+    memset(&p, 0, sizeof(p));
+    const int bn = tc_pick_bn(L.M);
+    const bool glu = L.epi == EPI_GLU;
+    if (!make_tma_2d(&p.mw[0], L.w0, glu ? L.N : L.n0rows, L.K, L.K, 128)) return cudaErrorInvalidValue;
+    if (L.w1 && !make_tma_2d(&p.mw[1], L.w1, glu ? L.N : L.n1rows, L.K, L.K, 128)) return cudaErrorInvalidValue;
+    for (int i = 0; i < L.na; ++i)
+        if (!make_tma_2d(&p.mx[i], L.a16[i], L.M, L.ka[i], L.lda[i], bn)) return cudaErrorInvalidValue;
+    p.np0 = L.w1 && !glu ? L.n0rows : 1 << 30;
+    p.N = L.N; p.M = L.M; p.K = L.K;
+    p.kseg[0] = L.na > 1 ? L.ka[0] / 64 : 1 << 30;
+    p.kseg[1] = L.na > 2 ? (L.ka[0] + L.ka[1]) / 64 : 1 << 30;
+    p.epi = L.epi;
+    p.y = L.y; p.ldy = L.ldy; p.ybf = L.ybf; p.ldybf = L.ldybf;
+    p.resid = L.resid; p.ldr = L.ldr;
+    p.part = d.tc_part;
+    p.pval = d.pval; p.pidx = d.pidx; p.logits = L.logits; p.ldl = L.ldl;
+    p.err = d.err;
+    p.nbatch = 1;
+    const int splits = L.epi == EPI_ARGMAX ? 1 : tc_splits(d, L.M, L.N, L.K, bn, glu);
+    cudaError_t e = traced(d, kind, st, [&] { return launch_tc_gemm(p, bn, splits, st); });
+    if (L.epi == EPI_ARGMAX) d.npart = p.npart;
+    return e;
+}
+
+Lin lin1(const eagle3_draft& d, int M, const float* a32, const bf16_t* a16, int K, const void* w, int N) {
+    Lin L;
+    L.M = M; L.N = N; L.K = K;
+    L.a32[0] = a32; L.a16[0] = a16; L.lda[0] = K; L.ka[0] = K;
+    L.w0 = w; L.n0rows = N;
+    (void)d;
+    return L;
+}
+
+// Per-head batched tensor-core GEMM: for head h, out[:, h*ycol + n] = X[:, h*kx : h*kx + K] W_h^T with
+// W_h the rows [h*wrows_stride + wrow0, + N) of `w` (row length K).
+cudaError_t run_batched(eagle3_draft& d, int kind, int M, const bf16_t* x, long ldx, int kx_per_head, const void* w,
+                        long wrows_total, int wrow0, int wrows_stride, int N, int K, float* y, bf16_t* ybf, long ldy,
+                        long ycol, cudaStream_t st) {
+    TcParams p;
+    memset(&p, 0, sizeof(p));
+    const int bn = tc_pick_bn(M);
+    // the map starts at row wrow0 so that batch h's tile row is h * wrows_stride
+    const bf16_t* wb = reinterpret_cast<const bf16_t*>(w) + (long)wrow0 * K;
+    if (!make_tma_2d(&p.mw[0], wb, wrows_total - wrow0, K, K, 128)) return cudaErrorInvalidValue;
+    if (!make_tma_2d(&p.mx[0], x, M, ldx, ldx, bn)) return cudaErrorInvalidValue;
+    p.np0 = 1 << 30;
+    p.N = N; p.M = M; p.K = K;
+    p.kseg[0] = p.kseg[1] = 1 << 30;
+    p.epi = EPI_STORE;
+    p.y = y; p.ldy = ldy; p.ybf = ybf; p.ldybf = ldy;
+    p.err = d.err;
+    p.nbatch = d.cfg.n_heads;
+    p.bw_rows = wrows_stride;
+    p.bq_kb = kx_per_head / 64;
+    p.by_col = ycol;
+    return traced(d, kind, st, [&] { return launch_tc_gemm(p, bn, 1, st); });
+}
+
+// The decoder chain from the concatenated input x to h2.
 // fused: the residual stream of the rows (fc output in extend, the carried hidden in decode).
 cudaError_t run_layer(eagle3_draft& d, eagle3_kv_t* kv, int M, const float* fused, cudaStream_t st) {
     const eagle3_config_t& c = d.cfg;
     const eagle3_weights_t& w = d.w;
-    const int H = c.hidden, dq = c.q_lora_rank, dc = c.kv_lora_rank, dr = c.qk_rope_dim;
-    const int nh = c.n_heads, dqk = c.qk_nope_dim + dr, D = dc + dr;
+    const int H = c.hidden, dq = c.q_lora_rank, dc = c.kv_lora_rank, dr = c.qk_rope_dim, dn = c.qk_nope_dim;
+    const int nh = c.n_heads, dqk = dn + dr, D = dc + dr, dv = c.v_head_dim, I = c.intermediate;
+    const bool tc = use_tc(d, M);
     RowArgs ra = row_args(d, kv);
-    cudaError_t e;
     // q_a | kv_a over the 2H input
     {
-        GemvArgs g = gemv1(d, d.x, 2L * H, 2 * H, w.q_a, dq + D, d.cqkv, dq + D);
-        g.w[1] = w.kv_a; g.nw[0] = dq; g.nw[1] = D; g.nseg_w = 2; g.M = M;
-        if ((e = launch_gemv(g, EPI_STORE, d.num_sms, st)) != cudaSuccess) return e;
+        Lin L = lin1(d, M, d.x, d.x_bf, 2 * H, w.q_a, dq + D);
+        L.w1 = w.kv_a; L.n0rows = dq; L.n1rows = D;
+        L.y = d.cqkv; L.ldy = dq + D;
+        E3_TRY(run_linear(d, L, K_QKV_A, st));
     }
-    if ((e = launch_latent(ra, M, d.cqkv, w.q_a_norm, w.kv_a_norm, d.rope_cos, d.rope_sin, d.row_seq, d.row_pos,
-                           kv->block_table, kv->data, d.cq_hat, st)) != cudaSuccess)
-        return e;
+    E3_TRY(traced(d, K_LATENT, st, [&] {
+        return launch_latent(ra, M, d.cqkv, w.q_a_norm, w.kv_a_norm, d.rope_cos, d.rope_sin, d.row_seq, d.row_pos,
+                             kv->block_table, kv->data, d.cq_hat, tc ? d.cqh_bf : nullptr, st);
+    }));
     {
-        GemvArgs g = gemv1(d, d.cq_hat, dq, dq, w.q_b, nh * dqk, d.q, (long)nh * dqk);
-        g.M = M;
-        if ((e = launch_gemv(g, EPI_STORE, d.num_sms, st)) != cudaSuccess) return e;
+        Lin L = lin1(d, M, d.cq_hat, d.cqh_bf, dq, w.q_b, nh * dqk);
+        L.y = d.q; L.ldy = (long)nh * dqk;
+        if (tc) { L.ybf = d.q_bf; L.ldybf = (long)nh * dqk; }
+        E3_TRY(run_linear(d, L, K_Q_B, st));
     }
     AttnArgs aa;
-    aa.M = M; aa.nh = nh; aa.dn = c.qk_nope_dim; aa.dr = dr; aa.dc = dc; aa.dv = c.v_head_dim;
+    memset(&aa, 0, sizeof(aa));
+    aa.M = M; aa.nh = nh; aa.dn = dn; aa.dr = dr; aa.dc = dc; aa.dv = dv;
     aa.sigma = attention_scale(c);
-    aa.page_size = c.page_size; aa.max_pages = c.max_pages_per_seq;
+    aa.page_size = c.page_size; aa.max_pages = c.max_pages_per_seq; aa.num_pages = kv->num_pages; aa.err = d.err;
     aa.splits = attn_splits(d, M);
     aa.dt = ra.dt;
     aa.row_seq = d.row_seq; aa.row_pos = d.row_pos; aa.block_table = kv->block_table;
     aa.cache = kv->data; aa.kv_b = w.kv_b; aa.q = d.q; aa.rope_cos = d.rope_cos; aa.rope_sin = d.rope_sin;
-    aa.qa = d.qa; aa.part_o = d.part_o; aa.part_ml = d.part_ml; aa.o = d.o;
-    if ((e = launch_absorb(aa, st)) != cudaSuccess) return e;
-    if ((e = launch_attention(aa, st)) != cudaSuccess) return e;
-    if ((e = launch_combine(aa, st)) != cudaSuccess) return e;
+    aa.qa = d.qa; aa.qa_bf = ra.dt == BF16 ? d.qa_bf : nullptr;
+    aa.part_o = d.part_o; aa.part_ml = d.part_ml; aa.o = d.o;
+    if (tc) {
+        // rope part, then q_lat,h = q_nope,h W_UK,h as a per-head GEMM against the transposed key weights
+        E3_TRY(traced(d, K_ROPE_Q, st, [&] { return launch_rope_q(aa, st); }));
+        E3_TRY(run_batched(d, K_ABSORB, M, d.q_bf, (long)nh * dqk, dqk, d.wukt, (long)nh * dc, 0, dc, dc, dn,
+                           nullptr, d.qa_bf, (long)nh * D, D, st));
+    } else {
+        E3_TRY(traced(d, K_ABSORB, st, [&] { return launch_absorb(aa, st); }));
+    }
+    E3_TRY(traced(d, K_ATTN, st, [&] { return launch_attention(aa, st); }));
+    if (tc) {
+        aa.olat_bf = d.olat_bf;
+        E3_TRY(traced(d, K_COMBINE, st, [&] { return launch_combine(aa, st); }));
+        // o_h = W_UV,h o_lat,h: per-head GEMM over the value rows of kv_b
+        E3_TRY(run_batched(d, K_UNABSORB, M, d.olat_bf, (long)nh * dc, dc, w.kv_b, (long)nh * (dn + dv), dn, dn + dv,
+                           dv, dc, nullptr, d.o_bf, (long)nh * dv, dv, st));
+    } else {
+        E3_TRY(traced(d, K_COMBINE, st, [&] { return launch_combine(aa, st); }));
+    }
     // o_proj + residual
     {
-        GemvArgs g = gemv1(d, d.o, (long)nh * c.v_head_dim, nh * c.v_head_dim, w.o, H, d.h1, H);
-        g.M = M; g.resid = fused; g.ldr = H;
-        if ((e = launch_gemv(g, EPI_RESID, d.num_sms, st)) != cudaSuccess) return e;
+        Lin L = lin1(d, M, d.o, d.o_bf, nh * dv, w.o, H);
+        L.epi = EPI_RESID; L.resid = fused; L.ldr = H;
+        L.y = d.h1; L.ldy = H;
+        E3_TRY(run_linear(d, L, K_O_PROJ, st));
     }
-    if ((e = launch_rmsnorm(M, H, c.rms_eps, ra.dt, d.h1, w.post_attn_norm, d.y, st)) != cudaSuccess) return e;
+    E3_TRY(traced(d, K_POST_NORM, st, [&] {
+        return launch_rmsnorm(M, H, c.rms_eps, ra.dt, d.h1, w.post_attn_norm, d.y, tc ? d.y_bf : nullptr, st);
+    }));
     {
-        GemvArgs g = gemv1(d, d.y, H, H, w.gate, c.intermediate, d.mlp, c.intermediate);
-        g.w[1] = w.up; g.nw[1] = c.intermediate; g.M = M;
-        if ((e = launch_gemv(g, EPI_GLU, d.num_sms, st)) != cudaSuccess) return e;
+        Lin L = lin1(d, M, d.y, d.y_bf, H, w.gate, I);
+        L.epi = EPI_GLU; L.w1 = w.up; L.n1rows = I;
+        if (tc) { L.ybf = d.m_bf; L.ldybf = I; } else { L.y = d.mlp; L.ldy = I; }
+        E3_TRY(run_linear(d, L, K_GATE_UP, st));
     }
     {
-        GemvArgs g = gemv1(d, d.mlp, c.intermediate, c.intermediate, w.down, H, d.h2, H);
-        g.M = M; g.resid = d.h1; g.ldr = H;
-        if ((e = launch_gemv(g, EPI_RESID, d.num_sms, st)) != cudaSuccess) return e;
+        Lin L = lin1(d, M, d.mlp, d.m_bf, I, w.down, H);
+        L.epi = EPI_RESID; L.resid = d.h1; L.ldr = H;
+        L.y = d.h2; L.ldy = H;
+        E3_TRY(run_linear(d, L, K_DOWN, st));
     }
     return cudaSuccess;
 }
 
 cudaError_t run_head(eagle3_draft& d, int batch, float* logits_out, cudaStream_t st) {
-    GemvArgs g = gemv1(d, d.z, d.cfg.hidden, d.cfg.hidden, d.w.lm_head, d.cfg.draft_vocab, nullptr, 0);
-    g.M = batch; g.pval = d.pval; g.pidx = d.pidx; g.logits = logits_out; g.ldl = d.cfg.draft_vocab;
-    return launch_gemv(g, EPI_ARGMAX, d.num_sms, st);
+    Lin L = lin1(d, batch, d.z, d.z_bf, d.cfg.hidden, d.w.lm_head, d.cfg.draft_vocab);
+    L.epi = EPI_ARGMAX; L.logits = logits_out; L.ldl = d.cfg.draft_vocab;
+    return run_linear(d, L, K_LM_HEAD, st);
 }
 
 bool kv_ok(const eagle3_kv_t* kv) {
@@ -335,24 +561,31 @@ eagle3_status_t eagle3_draft_create(const eagle3_config_t* config, const eagle3_
     d->ws_bytes = o.total;
     d->m_cap = o.m_cap;
     d->splits_cap = o.splits_cap;
-    d->npart_lm = o.npart;
+    d->npart = o.npart;
     d->part_rows = o.part_rows;
+    d->tc_ok = tc_supported(d->cfg);
     char* base = (char*)d->ws;
-    d->f = (float*)(base + o.f); d->carry = (float*)(base + o.carry); d->x = (float*)(base + o.x);
-    d->cqkv = (float*)(base + o.cqkv); d->cq_hat = (float*)(base + o.cq_hat); d->q = (float*)(base + o.q);
-    d->qa = (float*)(base + o.qa); d->part_o = (float*)(base + o.part_o); d->part_ml = (float*)(base + o.part_ml);
-    d->o = (float*)(base + o.o); d->h1 = (float*)(base + o.h1); d->y = (float*)(base + o.y);
-    d->mlp = (float*)(base + o.mlp); d->h2 = (float*)(base + o.h2); d->z = (float*)(base + o.z);
-    d->pval = (float*)(base + o.pval); d->pidx = (int*)(base + o.pidx);
-    d->rope_cos = (float*)(base + o.rope_cos); d->rope_sin = (float*)(base + o.rope_sin);
-    d->row_seq = (int*)(base + o.row_seq); d->row_pos = (int*)(base + o.row_pos);
-    d->d0 = (int*)(base + o.d0); d->tok_in = (int*)(base + o.tok_in); d->err = (int*)(base + o.err);
+    auto F = [&](size_t off) { return (float*)(base + off); };
+    auto Bf = [&](size_t off) { return (bf16_t*)(base + off); };
+    auto I = [&](size_t off) { return (int*)(base + off); };
+    d->f = F(o.f); d->carry = F(o.carry); d->x = F(o.x); d->cqkv = F(o.cqkv); d->cq_hat = F(o.cq_hat);
+    d->q = F(o.q); d->qa = F(o.qa); d->qa_bf = Bf(o.qa_bf); d->part_o = F(o.part_o); d->part_ml = F(o.part_ml);
+    d->o = F(o.o); d->h1 = F(o.h1); d->y = F(o.y); d->mlp = F(o.mlp); d->h2 = F(o.h2); d->z = F(o.z);
+    d->pval = F(o.pval); d->pidx = I(o.pidx); d->rope_cos = F(o.rope_cos); d->rope_sin = F(o.rope_sin);
+    d->row_seq = I(o.row_seq); d->row_pos = I(o.row_pos); d->d0 = I(o.d0); d->tok_in = I(o.tok_in);
+    d->err = I(o.err);
+    d->x_bf = Bf(o.x_bf); d->cqh_bf = Bf(o.cqh_bf); d->q_bf = Bf(o.q_bf); d->olat_bf = Bf(o.olat_bf);
+    d->o_bf = Bf(o.o_bf); d->y_bf = Bf(o.y_bf); d->m_bf = Bf(o.m_bf); d->z_bf = Bf(o.z_bf); d->wukt = Bf(o.wukt);
+    d->tc_part = F(o.tc_part);
     std::vector<float> cs, sn;
     yarn_table(d->cfg, cs, sn);
     e = cudaMemcpy(d->rope_cos, cs.data(), cs.size() * sizeof(float), cudaMemcpyHostToDevice);
     if (e == cudaSuccess) e = cudaMemcpy(d->rope_sin, sn.data(), sn.size() * sizeof(float), cudaMemcpyHostToDevice);
     if (e == cudaSuccess) e = cudaMemset(d->err, 0, sizeof(int));
     if (e == cudaSuccess) e = cudaMemset(d->carry, 0, (size_t)d->cfg.max_batch * d->cfg.hidden * sizeof(float));
+    if (e == cudaSuccess && d->tc_ok)
+        e = launch_transpose_wuk(d->w.kv_b, d->cfg.n_heads, d->cfg.qk_nope_dim, d->cfg.v_head_dim,
+                                 d->cfg.kv_lora_rank, d->wukt, 0);
     if (e == cudaSuccess) e = cudaDeviceSynchronize();
     if (e != cudaSuccess) {
         cudaFree(d->ws);
@@ -375,27 +608,38 @@ eagle3_status_t eagle3_draft_extend(eagle3_draft_t* d, const void* const aux_hid
         return EAGLE3_ERR_INVALID_ARG;
     cudaStream_t st = (cudaStream_t)stream;
     const int H = c.hidden, M = num_tokens;
+    const bool tc = use_tc(*d, M);
     RowArgs ra = row_args(*d, cache);
     // fc: f = [a_early | a_mid | a_late] W_fc^T  (3H -> H, no bias)
     {
-        GemvArgs g;
-        memset(&g, 0, sizeof(g));
-        for (int i = 0; i < 3; ++i) { g.a[i] = aux_hidden[i]; g.lda[i] = H; g.ka[i] = H; }
-        g.na = 3;
-        g.w[0] = d->w.fc; g.nw[0] = H; g.nseg_w = 1;
-        g.M = M; g.N = H; g.K = 3 * H;
-        g.a_type = ra.dt; g.w_type = ra.dt;
-        g.y = d->f; g.ldy = H;
-        E3_CUDA(launch_gemv(g, EPI_STORE, d->num_sms, st));
+        Lin L;
+        L.M = M; L.N = H; L.K = 3 * H; L.na = 3;
+        for (int i = 0; i < 3; ++i) {
+            L.a32[i] = aux_hidden[i];
+            L.a16[i] = (const bf16_t*)aux_hidden[i];
+            L.lda[i] = H; L.ka[i] = H;
+        }
+        L.a32_is_bf16 = ra.dt == BF16;
+        L.w0 = d->w.fc; L.n0rows = H;
+        L.y = d->f; L.ldy = H;
+        E3_CUDA(run_linear(*d, L, K_FC, st));
     }
-    E3_CUDA(launch_embed_norms(ra, false, M, tokens, positions, row_offsets, batch, nullptr, nullptr, d->f,
-                               d->w.embed, d->w.input_norm, d->w.hidden_norm, d->x, d->row_seq, d->row_pos, st));
+    E3_CUDA(traced(*d, K_EMBED, st, [&] {
+        return launch_embed_norms(ra, false, M, tokens, positions, row_offsets, batch, nullptr, nullptr, d->f,
+                                  d->w.embed, d->w.input_norm, d->w.hidden_norm, d->x, tc ? d->x_bf : nullptr,
+                                  d->row_seq, d->row_pos, st);
+    }));
     E3_CUDA(run_layer(*d, cache, M, d->f, st));
-    E3_CUDA(launch_final(ra, true, batch, row_offsets, d->h2, d->w.final_norm, d->row_pos, d->carry, d->z,
-                         hidden_out, cache->lengths, st));
+    const bool tch = use_tc(*d, batch);
+    E3_CUDA(traced(*d, K_FINAL, st, [&] {
+        return launch_final(ra, true, batch, M, row_offsets, d->h2, d->w.final_norm, d->row_pos, d->carry, d->z,
+                            tch ? d->z_bf : nullptr, hidden_out, cache->lengths, st);
+    }));
     E3_CUDA(run_head(*d, batch, logits_out, st));
-    E3_CUDA(launch_argmax_final(batch, d->npart_lm, d->pval, d->pidx, 0, nullptr, c.target_vocab, d->d0, nullptr,
-                                0, 0, nullptr, d->err, st));
+    E3_CUDA(traced(*d, K_ARGMAX, st, [&] {
+        return launch_argmax_final(batch, d->npart, d->pval, d->pidx, 0, nullptr, c.target_vocab, d->d0, nullptr, 0,
+                                   0, nullptr, d->err, st);
+    }));
     d->batch = batch;
     d->have_extend = true;
     return EAGLE3_OK;
@@ -409,20 +653,29 @@ eagle3_status_t eagle3_draft_decode(eagle3_draft_t* d, int32_t gamma, const int3
     const eagle3_config_t& c = d->cfg;
     cudaStream_t st = (cudaStream_t)stream;
     const int B = d->batch, H = c.hidden;
+    const bool tc = use_tc(*d, B);
     RowArgs ra = row_args(*d, cache);
-    E3_CUDA(launch_emit_first(B, d->d0, d2t, c.target_vocab, draft_tokens, gamma, d->tok_in, d->err, st));
+    E3_CUDA(traced(*d, K_EMIT, st, [&] {
+        return launch_emit_first(B, d->d0, d2t, c.target_vocab, draft_tokens, gamma, d->tok_in, d->err, st);
+    }));
     for (int s = 1; s < gamma; ++s) {
-        E3_CUDA(launch_embed_norms(ra, true, B, nullptr, nullptr, nullptr, B, d->tok_in, cache->lengths, d->carry,
-                                   d->w.embed, d->w.input_norm, d->w.hidden_norm, d->x, d->row_seq, d->row_pos,
-                                   st));
+        E3_CUDA(traced(*d, K_EMBED, st, [&] {
+            return launch_embed_norms(ra, true, B, nullptr, nullptr, nullptr, B, d->tok_in, cache->lengths, d->carry,
+                                      d->w.embed, d->w.input_norm, d->w.hidden_norm, d->x, tc ? d->x_bf : nullptr,
+                                      d->row_seq, d->row_pos, st);
+        }));
         E3_CUDA(run_layer(*d, cache, B, d->carry, st));
         float* ho = hidden_out ? hidden_out + (size_t)(s - 1) * B * H : nullptr;
         float* lo = logits_out ? logits_out + (size_t)(s - 1) * B * c.draft_vocab : nullptr;
-        E3_CUDA(launch_final(ra, false, B, nullptr, d->h2, d->w.final_norm, d->row_pos, d->carry, d->z, ho,
-                             cache->lengths, st));
+        E3_CUDA(traced(*d, K_FINAL, st, [&] {
+            return launch_final(ra, false, B, B, nullptr, d->h2, d->w.final_norm, d->row_pos, d->carry, d->z,
+                                tc ? d->z_bf : nullptr, ho, cache->lengths, st);
+        }));
         E3_CUDA(run_head(*d, B, lo, st));
-        E3_CUDA(launch_argmax_final(B, d->npart_lm, d->pval, d->pidx, 1, d2t, c.target_vocab, nullptr, draft_tokens,
-                                    gamma, s, d->tok_in, d->err, st));
+        E3_CUDA(traced(*d, K_ARGMAX, st, [&] {
+            return launch_argmax_final(B, d->npart, d->pval, d->pidx, 1, d2t, c.target_vocab, nullptr, draft_tokens,
+                                       gamma, s, d->tok_in, d->err, st);
+        }));
     }
     return EAGLE3_OK;
 }
@@ -448,9 +701,40 @@ eagle3_status_t eagle3_draft_clear_error(eagle3_draft_t* d, void* stream) {
     return EAGLE3_OK;
 }
 
+eagle3_status_t eagle3_draft_profile_enable(eagle3_draft_t* d, int32_t enable) {
+    if (!d) return EAGLE3_ERR_INVALID_ARG;
+    if (enable && d->prof_ev.empty()) {
+        d->prof_ev.resize(2 * kProfPairs);
+        d->prof_kind.resize(kProfPairs);
+        for (auto& ev : d->prof_ev) E3_CUDA(cudaEventCreate(&ev));
+    }
+    if (!enable) E3_CUDA(prof_flush(*d));
+    d->prof_on = enable != 0;
+    return EAGLE3_OK;
+}
+
+eagle3_status_t eagle3_draft_profile_read(eagle3_draft_t* d, int32_t kind, double* total_ms, int64_t* timed,
+                                          int64_t* launches, const char** name) {
+    if (!d || kind < 0 || kind >= EAGLE3_PROF_KINDS) return EAGLE3_ERR_INVALID_ARG;
+    E3_CUDA(prof_flush(*d));
+    if (total_ms) *total_ms = d->prof_ms[kind];
+    if (timed) *timed = d->prof_n[kind];
+    if (launches) *launches = d->launches[kind];
+    if (name) *name = kKindNames[kind];
+    return EAGLE3_OK;
+}
+
+eagle3_status_t eagle3_draft_profile_reset(eagle3_draft_t* d) {
+    if (!d) return EAGLE3_ERR_INVALID_ARG;
+    E3_CUDA(prof_flush(*d));
+    for (int k = 0; k < EAGLE3_PROF_KINDS; ++k) { d->prof_ms[k] = 0.0; d->prof_n[k] = 0; d->launches[k] = 0; }
+    return EAGLE3_OK;
+}
+
 eagle3_status_t eagle3_draft_destroy(eagle3_draft_t* d) {
     if (!d) return EAGLE3_OK;
     cudaDeviceSynchronize();
+    for (auto& ev : d->prof_ev) cudaEventDestroy(ev);
     cudaError_t e = cudaFree(d->ws);
     delete d;
     if (e != cudaSuccess) return cuda_fail(e);

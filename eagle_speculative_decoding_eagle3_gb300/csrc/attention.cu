@@ -5,10 +5,17 @@
 // are [c_kv_hat | k_rope].  With W_UK,h / W_UV,h the key / value rows of kv_b for head h:
 //   score_t = sigma (q_nope,h . W_UK,h c_t + q_pe,h . k_t) = sigma (q_lat,h . c_t + q_pe,h . k_t),
 //   o_h = sum_t p_t W_UV,h c_t = W_UV,h (sum_t p_t c_t),      q_lat,h = W_UK,h^T q_nope,h.
-// So the kernels never expand per-head keys or values: absorb forms q_lat; attention runs split-K
-// over the ragged context with a warp-level online softmax and writes per-split partials;
-// combine merges the splits and applies W_UV,h.
+// So no kernel expands per-head keys or values: absorb forms q_lat; attention runs split-K over the
+// ragged context with an online softmax and writes per-split partials; combine merges the splits
+// and applies W_UV,h.
+//
+// Two attention kernels share the partial format:
+//  * attention_mma_kernel (bf16 cache, d_c 512 / d_r 64): 16 heads x 32-token tiles on the tensor
+//    cores with mma.sync m16n8k16 (heads are the MMA rows, so the 16 heads of a CTA share one staged
+//    KV tile); the KV tiles are double-buffered with cp.async through the block table.
+//  * attention_kernel (any dtype, small latent): CUDA-core fallback used by the fp32 head.
 #include <float.h>
+#include <math.h>
 
 #include "common.cuh"
 #include "kernels.h"
@@ -22,16 +29,20 @@ constexpr int kHeadsPerWarp = 2;
 constexpr int kHeadsPerCta = kAttnWarps * kHeadsPerWarp;
 constexpr int kCombRows = 4;
 
-// qa[r, h] = [ W_UK,h^T q_nope[r, h] | RoPE(q_pe[r, h], pos_r) ]
+// qa[r, h] = [ W_UK,h^T q_nope[r, h] | RoPE(q_pe[r, h], pos_r) ]  (fp32, plus a bf16 copy when asked)
+// Thread (cc, rg) owns latent columns [8cc, 8cc+8) and W_UK rows rg, rg + RG, ...; row groups are
+// reduced through shared memory.
 template <typename T>
 __global__ void __launch_bounds__(256) absorb_kernel(const AttnArgs a) {
-    extern __shared__ float qn[];   // [kAbsRows][dn]
+    extern __shared__ float sm[];           // [kAbsRows][dn] q_nope, then [RG][kAbsRows][dc] partials
     const int h = blockIdx.x, r0 = blockIdx.y * kAbsRows;
     const int nr = min(kAbsRows, a.M - r0);
     const int dqk = a.dn + a.dr, D = a.dc + a.dr;
-    for (int t = threadIdx.x; t < nr * a.dn; t += blockDim.x) {
+    float* qn = sm;
+    float* part = sm + kAbsRows * a.dn;
+    for (int t = threadIdx.x; t < kAbsRows * a.dn; t += blockDim.x) {
         const int i = t / a.dn, k = t % a.dn;
-        qn[i * a.dn + k] = a.q[((long)(r0 + i) * a.nh + h) * dqk + k];
+        qn[t] = (i < nr) ? a.q[((long)(r0 + i) * a.nh + h) * dqk + k] : 0.f;
     }
     const int half = a.dr / 2;
     for (int t = threadIdx.x; t < nr * half; t += blockDim.x) {
@@ -40,25 +51,52 @@ __global__ void __launch_bounds__(256) absorb_kernel(const AttnArgs a) {
         const float c = a.rope_cos[(long)pos * half + p], s = a.rope_sin[(long)pos * half + p];
         const float* qp = a.q + ((long)(r0 + i) * a.nh + h) * dqk + a.dn;
         const float x0 = qp[2 * p], x1 = qp[2 * p + 1];
-        float* dst = a.qa + ((long)(r0 + i) * a.nh + h) * D + a.dc;
-        dst[2 * p] = x0 * c - x1 * s;
-        dst[2 * p + 1] = x0 * s + x1 * c;
+        const float y0 = x0 * c - x1 * s, y1 = x0 * s + x1 * c;
+        const long o = ((long)(r0 + i) * a.nh + h) * D + a.dc + 2 * p;
+        a.qa[o] = y0;
+        a.qa[o + 1] = y1;
+        if (a.qa_bf) { a.qa_bf[o] = __float2bfloat16_rn(y0); a.qa_bf[o + 1] = __float2bfloat16_rn(y1); }
     }
     __syncthreads();
+    const int nchunk = a.dc / 8;
+    const int RG = blockDim.x / nchunk;
+    const int cc = threadIdx.x % nchunk, rg = threadIdx.x / nchunk;
     const T* W = reinterpret_cast<const T*>(a.kv_b) + (long)h * (a.dn + a.dv) * a.dc;
-    for (int c = threadIdx.x; c < a.dc; c += blockDim.x) {
-        float acc[kAbsRows];
+    float acc[kAbsRows][8];
 #pragma unroll
-        for (int i = 0; i < kAbsRows; ++i) acc[i] = 0.f;
-        for (int k = 0; k < a.dn; ++k) {
-            const float w = to_f(W[(long)k * a.dc + c]);
+    for (int i = 0; i < kAbsRows; ++i)
 #pragma unroll
-            for (int i = 0; i < kAbsRows; ++i) acc[i] = fmaf(qn[i * a.dn + k], w, acc[i]);
+        for (int e = 0; e < 8; ++e) acc[i][e] = 0.f;
+    if (rg < RG) {
+#pragma unroll 4
+        for (int k = rg; k < a.dn; k += RG) {
+            float w[8];
+            widen(ld8<true>(W + (long)k * a.dc + 8 * cc), w);
+#pragma unroll
+            for (int i = 0; i < kAbsRows; ++i) {
+                const float q = qn[i * a.dn + k];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) acc[i][e] = fmaf(q, w[e], acc[i][e]);
+            }
         }
-        for (int i = 0; i < nr; ++i) a.qa[((long)(r0 + i) * a.nh + h) * D + c] = acc[i];
+#pragma unroll
+        for (int i = 0; i < kAbsRows; ++i)
+#pragma unroll
+            for (int e = 0; e < 8; ++e) part[((long)rg * kAbsRows + i) * a.dc + 8 * cc + e] = acc[i][e];
+    }
+    __syncthreads();
+    for (int t = threadIdx.x; t < nr * a.dc; t += blockDim.x) {
+        const int i = t / a.dc, c = t % a.dc;
+        float v = 0.f;
+        for (int g = 0; g < RG; ++g) v += part[((long)g * kAbsRows + i) * a.dc + c];
+        const long o = ((long)(r0 + i) * a.nh + h) * D + c;
+        a.qa[o] = v;
+        if (a.qa_bf) a.qa_bf[o] = __float2bfloat16_rn(v);
     }
 }
 
+// ------------------------------------------------------------------------------------------------
+// CUDA-core split-K attention (fp32 cache or small latent widths).
 // One (split, head group, row) per CTA.  Row r at position p attends to slots [0, p]; split s covers
 // a contiguous tile-aligned chunk of those slots.  Each warp owns two heads; lane j scores token j of
 // the staged tile, then the warp updates its running max / sum / output (lane holds DC/32 outputs).
@@ -102,6 +140,11 @@ __global__ void __launch_bounds__(kAttnWarps * 32) attention_kernel(const AttnAr
             const int j = t / WORDS, w = t % WORDS;
             const int slot = tt + j;
             const int page = bt[slot / a.page_size];
+            if (page < 0 || page >= a.num_pages) {   // a bad block table reads zeros and is flagged
+                kvs[j * ROWW + w] = 0u;
+                if (w == 0) set_err(a.err, 8);
+                continue;
+            }
             const uint32_t* src = reinterpret_cast<const uint32_t*>(
                 cache + ((long)page * a.page_size + slot % a.page_size) * D);
             kvs[j * ROWW + w] = src[w];
@@ -170,43 +213,260 @@ __global__ void __launch_bounds__(kAttnWarps * 32) attention_kernel(const AttnAr
     }
 }
 
+// ------------------------------------------------------------------------------------------------
+// Tensor-core split-K attention for the DeepseekV3 latent geometry (bf16, d_c 512, d_r 64).
+namespace mla_mma {
+constexpr int T = 32;             // tokens per tile
+constexpr int HEADS = 16;         // heads per CTA (the MMA M dimension)
+constexpr int D = 576, DC = 512;
+constexpr int ROW = D + 8;        // bf16 row stride: 1168 B, 16-byte aligned, an odd number of 16 B units
+constexpr int SROW = T + 8;       // fp32 score row stride
+constexpr int WARPS = 4;          // warp w scores tokens [8w, 8w+8) and owns output columns [128w, 128w+128)
+constexpr size_t SMEM = (size_t)HEADS * ROW * 2 + 2 * (size_t)T * ROW * 2 + (size_t)HEADS * SROW * 4;
+}  // namespace mla_mma
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+    return (uint32_t)__cvta_generic_to_shared(p);
+}
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t* r) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]) : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t* r) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]) : "r"(addr));
+}
+__device__ __forceinline__ void mma_bf16_16816(float* c, const uint32_t* a, uint32_t b0, uint32_t b1) {
+    asm volatile("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+                 "{%0,%1,%2,%3};"
+                 : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+                 : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+__device__ __forceinline__ void cp_async16(uint32_t saddr, const void* g) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(saddr), "l"(g));
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;"); }
+template <int N> __device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(N));
+}
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+    const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<const uint32_t*>(&v);
+}
+
+__global__ void __launch_bounds__(mla_mma::WARPS * 32) attention_mma_kernel(const AttnArgs a) {
+    using namespace mla_mma;
+    extern __shared__ __align__(16) unsigned char smraw[];
+    bf16* qs = reinterpret_cast<bf16*>(smraw);                  // [HEADS][ROW]
+    bf16* kvb = qs + HEADS * ROW;                              // [2][T][ROW]
+    float* ss = reinterpret_cast<float*>(kvb + 2 * T * ROW);   // [HEADS][SROW]
+    const int s = blockIdx.x, hg = blockIdx.y, r = blockIdx.z;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane >> 2, tig = lane & 3;
+    const int b = a.row_seq[r], pos = a.row_pos[r], n = pos + 1;
+    int chunk = (n + a.splits - 1) / a.splits;
+    chunk = (chunk + T - 1) / T * T;
+    const int t0 = s * chunk, t1 = min(n, t0 + chunk);
+    const int h0 = hg * HEADS;
+
+    for (int c = tid; c < HEADS * (D / 8); c += WARPS * 32) {
+        const int hh = c / (D / 8), q = c % (D / 8), h = h0 + hh;
+        uint4 v = make_uint4(0, 0, 0, 0);
+        if (h < a.nh) v = *reinterpret_cast<const uint4*>(a.qa_bf + ((long)r * a.nh + h) * D + 8 * q);
+        *reinterpret_cast<uint4*>(qs + hh * ROW + 8 * q) = v;
+    }
+    const bf16* cache = reinterpret_cast<const bf16*>(a.cache);
+    const int* bt = a.block_table + (long)b * a.max_pages;
+    auto load_tile = [&](int buf, int tt) {
+        bf16* dst = kvb + buf * T * ROW;
+        for (int c = tid; c < T * (D / 8); c += WARPS * 32) {
+            const int j = c / (D / 8), q = c % (D / 8), slot = tt + j;
+            bf16* d = dst + j * ROW + 8 * q;
+            const int page = (slot < t1) ? bt[slot / a.page_size] : -1;
+            if (page >= 0 && page < a.num_pages) {
+                cp_async16(smem_u32(d), cache + ((long)page * a.page_size + slot % a.page_size) * D + 8 * q);
+            } else {
+                *reinterpret_cast<uint4*>(d) = make_uint4(0, 0, 0, 0);
+                if (slot < t1 && q == 0) set_err(a.err, 8);
+            }
+        }
+        cp_async_commit();
+    };
+
+    float m_r[2] = {-INFINITY, -INFINITY}, l_r[2] = {0.f, 0.f};
+    float o[16][4];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+
+    if (t0 < t1) load_tile(0, t0);
+    int it = 0;
+    for (int tt = t0; tt < t1; tt += T, ++it) {
+        const int cnt = min(T, t1 - tt);
+        if (tt + T < t1) {
+            load_tile((it + 1) & 1, tt + T);
+            cp_async_wait<1>();
+        } else {
+            cp_async_wait<0>();
+        }
+        __syncthreads();
+        const bf16* K = kvb + (it & 1) * T * ROW;
+        // ---- scores of tokens [8w, 8w+8) for the 16 heads: two accumulators split the k-chain
+        float sacc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+        const uint32_t qrow = smem_u32(qs + ((lane & 7) + ((lane >> 3) & 1) * 8) * ROW + (lane >> 4) * 8);
+        const uint32_t krow = smem_u32(K + (8 * warp + (lane & 7)) * ROW + (lane >> 3) * 8);
+#pragma unroll 6
+        for (int ks = 0; ks < D / 16; ks += 2) {
+            uint32_t qa0[4], qa1[4], kb[4];
+            ldsm_x4(qrow + ks * 32, qa0);
+            ldsm_x4(qrow + (ks + 1) * 32, qa1);
+            ldsm_x4(krow + ks * 32, kb);
+            mma_bf16_16816(sacc[0], qa0, kb[0], kb[1]);
+            mma_bf16_16816(sacc[1], qa1, kb[2], kb[3]);
+        }
+        const int col0 = 8 * warp + 2 * tig;
+        float sv[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) sv[i] = (sacc[0][i] + sacc[1][i]) * a.sigma;
+        if (col0 >= cnt) sv[0] = sv[2] = -INFINITY;
+        if (col0 + 1 >= cnt) sv[1] = sv[3] = -INFINITY;
+        ss[g * SROW + col0] = sv[0];
+        ss[g * SROW + col0 + 1] = sv[1];
+        ss[(g + 8) * SROW + col0] = sv[2];
+        ss[(g + 8) * SROW + col0 + 1] = sv[3];
+        __syncthreads();
+        // ---- online softmax over the tile (every warp, for rows g and g + 8)
+        float p[2][2][4];   // [k-step][row][cols 2tig, 2tig+1, 2tig+8, 2tig+9]
+        float mx[2] = {-INFINITY, -INFINITY};
+#pragma unroll
+        for (int kk = 0; kk < 2; ++kk)
+#pragma unroll
+            for (int rr = 0; rr < 2; ++rr) {
+                const float* row = ss + (g + 8 * rr) * SROW + kk * 16 + 2 * tig;
+                p[kk][rr][0] = row[0];
+                p[kk][rr][1] = row[1];
+                p[kk][rr][2] = row[8];
+                p[kk][rr][3] = row[9];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) mx[rr] = fmaxf(mx[rr], p[kk][rr][e]);
+            }
+        float alpha[2];
+#pragma unroll
+        for (int rr = 0; rr < 2; ++rr) {
+            mx[rr] = fmaxf(mx[rr], __shfl_xor_sync(0xffffffffu, mx[rr], 1));
+            mx[rr] = fmaxf(mx[rr], __shfl_xor_sync(0xffffffffu, mx[rr], 2));
+            const float mn = fmaxf(m_r[rr], mx[rr]);
+            alpha[rr] = (m_r[rr] == -INFINITY) ? 0.f : __expf(m_r[rr] - mn);
+            float ls = 0.f;
+#pragma unroll
+            for (int kk = 0; kk < 2; ++kk)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    p[kk][rr][e] = __expf(p[kk][rr][e] - mn);
+                    ls += p[kk][rr][e];
+                }
+            ls += __shfl_xor_sync(0xffffffffu, ls, 1);
+            ls += __shfl_xor_sync(0xffffffffu, ls, 2);
+            l_r[rr] = l_r[rr] * alpha[rr] + ls;
+            m_r[rr] = mn;
+        }
+#pragma unroll
+        for (int nt = 0; nt < 16; ++nt) {
+            o[nt][0] *= alpha[0]; o[nt][1] *= alpha[0];
+            o[nt][2] *= alpha[1]; o[nt][3] *= alpha[1];
+        }
+        // ---- O[:, 128w : 128w+128] += P V
+#pragma unroll
+        for (int kk = 0; kk < 2; ++kk) {
+            uint32_t pa[4];
+            pa[0] = pack_bf16(p[kk][0][0], p[kk][0][1]);
+            pa[1] = pack_bf16(p[kk][1][0], p[kk][1][1]);
+            pa[2] = pack_bf16(p[kk][0][2], p[kk][0][3]);
+            pa[3] = pack_bf16(p[kk][1][2], p[kk][1][3]);
+            const uint32_t vrow = smem_u32(K + (kk * 16 + (lane & 7) + ((lane >> 3) & 1) * 8) * ROW + 128 * warp +
+                                           (lane >> 4) * 8);
+#pragma unroll
+            for (int nt = 0; nt < 16; nt += 2) {
+                uint32_t vb[4];
+                ldsm_x4_t(vrow + nt * 16, vb);
+                mma_bf16_16816(o[nt], pa, vb[0], vb[1]);
+                mma_bf16_16816(o[nt + 1], pa, vb[2], vb[3]);
+            }
+        }
+        __syncthreads();
+    }
+#pragma unroll
+    for (int rr = 0; rr < 2; ++rr) {
+        const int h = h0 + g + 8 * rr;
+        if (h >= a.nh) continue;
+        const long base = ((long)r * a.nh + h) * a.splits + s;
+        if (warp == 0 && tig == 0) {
+            a.part_ml[base * 2] = (t0 < t1) ? m_r[rr] : -FLT_MAX;
+            a.part_ml[base * 2 + 1] = l_r[rr];
+        }
+#pragma unroll
+        for (int nt = 0; nt < 16; ++nt) {
+            const int col = 128 * warp + nt * 8 + 2 * tig;
+            *reinterpret_cast<float2*>(a.part_o + base * DC + col) = make_float2(o[nt][2 * rr], o[nt][2 * rr + 1]);
+        }
+    }
+}
+
 // o[r, h*dv + j] = W_UV,h[j] . (sum_s e^{m_s - M} o_s / sum_s e^{m_s - M} l_s)
 template <typename T, int DC>
 __global__ void __launch_bounds__(256) combine_kernel(const AttnArgs a) {
     __shared__ float ol[kCombRows][DC];
+    __shared__ float wsp[kCombRows][64];
     const int h = blockIdx.x, r0 = blockIdx.y * kCombRows;
     const int nr = min(kCombRows, a.M - r0);
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    for (int i = 0; i < nr; ++i) {
-        const long base = ((long)(r0 + i) * a.nh + h) * a.splits;
-        float mx = -FLT_MAX;
-        for (int s = 0; s < a.splits; ++s) mx = fmaxf(mx, a.part_ml[(base + s) * 2]);
-        float den = 0.f;
-        for (int s = 0; s < a.splits; ++s) {
-            const float l = a.part_ml[(base + s) * 2 + 1];
-            if (l > 0.f) den += __expf(a.part_ml[(base + s) * 2] - mx) * l;
-        }
-        const float inv = den > 0.f ? 1.f / den : 0.f;
-        for (int c = threadIdx.x; c < DC; c += blockDim.x) {
-            float num = 0.f;
-            for (int s = 0; s < a.splits; ++s) {
+    const int S = a.splits;
+    if (threadIdx.x < 32 * kCombRows) {   // one warp per row: split weights e^{m_s - M} / den
+        const int i = warp;
+        if (i < nr) {
+            const long base = ((long)(r0 + i) * a.nh + h) * S;
+            float mx = -FLT_MAX;
+            for (int s = lane; s < S; s += 32) mx = fmaxf(mx, a.part_ml[(base + s) * 2]);
+            mx = warp_max(mx);
+            float den = 0.f;
+            for (int s = lane; s < S; s += 32) {
                 const float l = a.part_ml[(base + s) * 2 + 1];
-                if (l > 0.f) num += __expf(a.part_ml[(base + s) * 2] - mx) * a.part_o[(base + s) * DC + c];
+                const float e = l > 0.f ? __expf(a.part_ml[(base + s) * 2] - mx) : 0.f;
+                wsp[i][s] = e;
+                den += e * l;
             }
-            ol[i][c] = num * inv;
+            den = warp_sum(den);
+            const float inv = den > 0.f ? 1.f / den : 0.f;
+            __syncwarp();
+            for (int s = lane; s < S; s += 32) wsp[i][s] *= inv;
         }
     }
     __syncthreads();
+    for (int t = threadIdx.x; t < nr * DC; t += blockDim.x) {
+        const int i = t / DC, c = t % DC;
+        const long base = ((long)(r0 + i) * a.nh + h) * S;
+        float v = 0.f;
+        for (int s = 0; s < S; ++s) {
+            const float w = wsp[i][s];
+            if (w != 0.f) v = fmaf(w, a.part_o[(base + s) * DC + c], v);
+        }
+        ol[i][c] = v;
+        if (a.olat_bf) a.olat_bf[((long)(r0 + i) * a.nh + h) * DC + c] = __float2bfloat16_rn(v);
+    }
+    if (a.olat_bf) return;   // the value up-projection runs as a batched tensor-core GEMM instead
+    __syncthreads();
     const T* W = reinterpret_cast<const T*>(a.kv_b) + ((long)h * (a.dn + a.dv) + a.dn) * DC;
+    constexpr int NCH = DC / 8;
     for (int j = warp; j < a.dv; j += blockDim.x >> 5) {
         const T* wr = W + (long)j * DC;
         float acc[kCombRows];
 #pragma unroll
         for (int i = 0; i < kCombRows; ++i) acc[i] = 0.f;
-        for (int c = lane; c < DC; c += 32) {
-            const float w = to_f(wr[c]);
+        for (int c8 = lane; c8 < NCH; c8 += 32) {
+            float w[8];
+            widen(ld8<true>(wr + 8 * c8), w);
 #pragma unroll
-            for (int i = 0; i < kCombRows; ++i) acc[i] = fmaf(w, ol[i][c], acc[i]);
+            for (int i = 0; i < kCombRows; ++i)
+#pragma unroll
+                for (int e = 0; e < 8; ++e) acc[i] = fmaf(w[e], ol[i][8 * c8 + e], acc[i]);
         }
         for (int i = 0; i < nr; ++i) {
             const float v = warp_sum(acc[i]);
@@ -215,14 +475,75 @@ __global__ void __launch_bounds__(256) combine_kernel(const AttnArgs a) {
     }
 }
 
+// Rotated rope part of the query: qa[r, h, dc:] = RoPE(q_pe[r, h], pos_r) (fp32 and bf16).
+__global__ void rope_q_kernel(const AttnArgs a) {
+    const int r = blockIdx.x;
+    const int half = a.dr / 2, dqk = a.dn + a.dr, D = a.dc + a.dr;
+    const int pos = a.row_pos[r];
+    for (int t = threadIdx.x; t < a.nh * half; t += blockDim.x) {
+        const int h = t / half, p = t % half;
+        const float c = a.rope_cos[(long)pos * half + p], s = a.rope_sin[(long)pos * half + p];
+        const float* qp = a.q + ((long)r * a.nh + h) * dqk + a.dn;
+        const float x0 = qp[2 * p], x1 = qp[2 * p + 1];
+        const float y0 = x0 * c - x1 * s, y1 = x0 * s + x1 * c;
+        const long o = ((long)r * a.nh + h) * D + a.dc + 2 * p;
+        a.qa[o] = y0;
+        a.qa[o + 1] = y1;
+        if (a.qa_bf) *reinterpret_cast<uint32_t*>(a.qa_bf + o) = pack2_bf16(y0, y1);
+    }
+}
+
+// out[h, c, i] = kv_b[h (dn + dv) + i, c]: the key up-projection of each head, transposed so that the
+// absorbed query q_lat,h = W_UK,h^T q_nope,h is a K-major GEMM over i.
+__global__ void transpose_wuk_kernel(const bf16* kv_b, int nh, int dn, int dv, int dc, bf16* out) {
+    __shared__ bf16 tile[32][33];
+    const int h = blockIdx.z, c0 = blockIdx.x * 32, i0 = blockIdx.y * 32;
+    const bf16* W = kv_b + (long)h * (dn + dv) * dc;
+    for (int k = threadIdx.y; k < 32; k += blockDim.y) {
+        const int i = i0 + k, c = c0 + threadIdx.x;
+        tile[k][threadIdx.x] = (i < dn && c < dc) ? W[(long)i * dc + c] : __float2bfloat16_rn(0.f);
+    }
+    __syncthreads();
+    for (int k = threadIdx.y; k < 32; k += blockDim.y) {
+        const int c = c0 + k, i = i0 + threadIdx.x;
+        if (c < dc && i < dn) out[((long)h * dc + c) * dn + i] = tile[threadIdx.x][k];
+    }
+}
+
+cudaError_t launch_rope_q(const AttnArgs& a, cudaStream_t st) {
+    rope_q_kernel<<<a.M, 256, 0, st>>>(a);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_transpose_wuk(const void* kv_b, int nh, int dn, int dv, int dc, bf16* out, cudaStream_t st) {
+    dim3 grid((dc + 31) / 32, (dn + 31) / 32, nh);
+    transpose_wuk_kernel<<<grid, dim3(32, 8), 0, st>>>(reinterpret_cast<const bf16*>(kv_b), nh, dn, dv, dc, out);
+    return cudaGetLastError();
+}
+
 bool attention_supported(int dc, int dr, int dn, int dv) {
     (void)dn; (void)dv;
     return (dc == 512 && dr == 64) || (dc == 32 && dr == 16);
 }
 
+int attention_heads_per_cta(int dt, int dc, int dr) {
+    return (dt == BF16 && dc == 512 && dr == 64) ? mla_mma::HEADS : kHeadsPerCta;
+}
+
 cudaError_t launch_absorb(const AttnArgs& a, cudaStream_t st) {
     dim3 grid(a.nh, (a.M + kAbsRows - 1) / kAbsRows);
-    const size_t sm = (size_t)kAbsRows * a.dn * sizeof(float);
+    const int RG = 256 / (a.dc / 8);
+    const size_t sm = ((size_t)kAbsRows * a.dn + (size_t)RG * kAbsRows * a.dc) * sizeof(float);
+    static bool attr[2] = {false, false};
+    const int ti = a.dt == BF16 ? 1 : 0;
+    if (!attr[ti]) {
+        cudaError_t e = a.dt == BF16
+            ? cudaFuncSetAttribute(absorb_kernel<bf16>, cudaFuncAttributeMaxDynamicSharedMemorySize, 96 * 1024)
+            : cudaFuncSetAttribute(absorb_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize, 96 * 1024);
+        if (e != cudaSuccess) return e;
+        attr[ti] = true;
+    }
+    if (sm > 96 * 1024) return cudaErrorInvalidValue;
     if (a.dt == BF16) absorb_kernel<bf16><<<grid, 256, sm, st>>>(a);
     else absorb_kernel<float><<<grid, 256, sm, st>>>(a);
     return cudaGetLastError();
@@ -246,14 +567,29 @@ static cudaError_t attn_launch(const AttnArgs& a, cudaStream_t st) {
 }
 
 cudaError_t launch_attention(const AttnArgs& a, cudaStream_t st) {
-    if (a.dc == 512 && a.dr == 64)
-        return a.dt == BF16 ? attn_launch<bf16, 512, 64>(a, st) : attn_launch<float, 512, 64>(a, st);
+    if (a.dc == 512 && a.dr == 64) {
+        if (a.dt == BF16) {
+            static bool attr_set = false;
+            if (!attr_set) {
+                cudaError_t e = cudaFuncSetAttribute(attention_mma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                     (int)mla_mma::SMEM);
+                if (e != cudaSuccess) return e;
+                attr_set = true;
+            }
+            if (!a.qa_bf) return cudaErrorInvalidValue;
+            dim3 grid(a.splits, (a.nh + mla_mma::HEADS - 1) / mla_mma::HEADS, a.M);
+            attention_mma_kernel<<<grid, mla_mma::WARPS * 32, mla_mma::SMEM, st>>>(a);
+            return cudaGetLastError();
+        }
+        return attn_launch<float, 512, 64>(a, st);
+    }
     if (a.dc == 32 && a.dr == 16)
         return a.dt == BF16 ? attn_launch<bf16, 32, 16>(a, st) : attn_launch<float, 32, 16>(a, st);
     return cudaErrorInvalidValue;
 }
 
 cudaError_t launch_combine(const AttnArgs& a, cudaStream_t st) {
+    if (a.splits > 64) return cudaErrorInvalidValue;
     dim3 grid(a.nh, (a.M + kCombRows - 1) / kCombRows);
     if (a.dc == 512) {
         if (a.dt == BF16) combine_kernel<bf16, 512><<<grid, 256, 0, st>>>(a);

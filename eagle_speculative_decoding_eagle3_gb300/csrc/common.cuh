@@ -95,6 +95,11 @@ __device__ __forceinline__ bool better(float v, int i, float bv, int bi) {
 
 __device__ __forceinline__ void set_err(int* err, int bit) { atomicOr(err, bit); }
 
+__device__ __forceinline__ uint32_t pack2_bf16(float lo, float hi) {
+    const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<const uint32_t*>(&v);
+}
+
 __device__ __forceinline__ float silu(float x) { return x / (1.f + __expf(-x)); }
 
 }  // namespace e3

@@ -1,7 +1,9 @@
 // Internal launch interface of the draft-head kernels.  Host code (api.cu) fills these structs;
 // every launch_* enqueues its kernel(s) on `st` and returns the launch error.
 #pragma once
+#include <cuda.h>
 #include <cuda_runtime.h>
+#include <cuda_bf16.h>
 #include <stdint.h>
 
 namespace e3 {
@@ -47,20 +49,21 @@ struct RowArgs {
 cudaError_t launch_embed_norms(const RowArgs& a, bool decode, int M, const int* tokens, const int* positions,
                                const int* row_offsets, int batch, const int* tok_in, const int* lengths,
                                const float* fused, const void* embed, const void* w_in, const void* w_hid,
-                               float* x, int* row_seq, int* row_pos, cudaStream_t st);
+                               float* x, __nv_bfloat16* x_bf, int* row_seq, int* row_pos, cudaStream_t st);
 
 // latent norms, k_rope rotation and cache append
 cudaError_t launch_latent(const RowArgs& a, int M, const float* cqkv, const void* w_qa, const void* w_kva,
                           const float* rope_cos, const float* rope_sin, const int* row_seq, const int* row_pos,
-                          const int* block_table, void* cache, float* cq_hat, cudaStream_t st);
+                          const int* block_table, void* cache, float* cq_hat, __nv_bfloat16* cqh_bf,
+                          cudaStream_t st);
 
 cudaError_t launch_rmsnorm(int M, int H, float eps, DType wt, const float* x, const void* w, float* y,
-                           cudaStream_t st);
+                           __nv_bfloat16* y_bf, cudaStream_t st);
 
 // scored rows: b < batch; src row = extend ? row_offsets[b+1]-1 : b
-cudaError_t launch_final(const RowArgs& a, bool extend, int batch, const int* row_offsets, const float* h2,
-                         const void* w_final, const int* row_pos, float* carry, float* z, float* hidden_out,
-                         int* lengths, cudaStream_t st);
+cudaError_t launch_final(const RowArgs& a, bool extend, int batch, int M, const int* row_offsets, const float* h2,
+                         const void* w_final, const int* row_pos, float* carry, float* z, __nv_bfloat16* z_bf,
+                         float* hidden_out, int* lengths, cudaStream_t st);
 
 // argmax over partials; mode 0 (extend): d0[b] = d; mode 1 (decode step s): t = remap(d),
 // out_tokens[b*gamma + s] = t, tok_in[b] = t
@@ -79,7 +82,8 @@ cudaError_t launch_accept(const int* draft, const int* target, int batch, int ga
 struct AttnArgs {
     int M, nh, dn, dr, dc, dv;
     float sigma;
-    int page_size, max_pages, splits;
+    int page_size, max_pages, num_pages, splits;
+    int* err;
     DType dt;
     const int* row_seq; const int* row_pos; const int* block_table;
     const void* cache;
@@ -87,13 +91,47 @@ struct AttnArgs {
     const float* q;      // [M, nh*(dn+dr)]
     const float* rope_cos; const float* rope_sin;
     float* qa;           // [M, nh, dc+dr]   absorbed latent query | rotated rope query
+    __nv_bfloat16* qa_bf;  // bf16 copy of qa for the tensor-core kernel (nullptr: not written)
     float* part_o;       // [M, nh, splits, dc]
     float* part_ml;      // [M, nh, splits, 2]
     float* o;            // [M, nh*dv]
+    __nv_bfloat16* olat_bf;  // combine: when set, write o_lat [M, nh, dc] in bf16 and skip the W_UV product
 };
 cudaError_t launch_absorb(const AttnArgs& a, cudaStream_t st);
 cudaError_t launch_attention(const AttnArgs& a, cudaStream_t st);
 cudaError_t launch_combine(const AttnArgs& a, cudaStream_t st);
+// rotated rope query into qa / qa_bf[:, :, dc:] (the tensor-core path forms q_lat separately)
+cudaError_t launch_rope_q(const AttnArgs& a, cudaStream_t st);
+// W_UK,h^T for every head: out[h, c, i] = kv_b[h*(dn+dv) + i, c]  (bf16)
+cudaError_t launch_transpose_wuk(const void* kv_b, int nh, int dn, int dv, int dc, __nv_bfloat16* out,
+                                 cudaStream_t st);
 bool attention_supported(int dc, int dr, int dn, int dv);
+int attention_heads_per_cta(int dt, int dc, int dr);
+
+// ---------------------------------------------------------------- tcgen05 GEMM (bf16, many rows)
+// out[m, n] = sum_k W[n, k] X[m, k]; W from mw[0] (rows < np0) and mw[1] (rows >= np0, or the up
+// projection for GLU), X from mx[s] for K-blocks in segment s (boundaries kseg, in 64-wide blocks).
+struct TcParams {
+    CUtensorMap mw[2];
+    CUtensorMap mx[3];
+    int np0;
+    int N, M, K;
+    int kseg[2];
+    int nkb, kb_per_split, splits;   // set by the launcher
+    int nbatch;                   // batched GEMMs: batch z reads W rows + z*bw_rows, X K-blocks + z*bq_kb,
+    int bw_rows, bq_kb;           // and writes output columns + z*by_col (one X segment, no split)
+    long by_col;
+    int epi;                      // EPI_STORE / EPI_RESID / EPI_GLU / EPI_ARGMAX
+    float* y; long ldy;           // fp32 output (optional)
+    __nv_bfloat16* ybf; long ldybf;  // bf16 output (optional)
+    const float* resid; long ldr;
+    float* part;                  // split-K partials [splits][GLU ? 2 : 1][M][N]
+    float* pval; int* pidx; int npart;   // ARGMAX partials [M, npart] (npart set by the launcher)
+    float* logits; long ldl;
+    int* err;
+};
+bool make_tma_2d(CUtensorMap* map, const void* ptr, long rows, long cols, long ld, int box_rows);
+int tc_pick_bn(int M);
+cudaError_t launch_tc_gemm(TcParams& p, int bn, int splits, cudaStream_t st);
 
 }  // namespace e3

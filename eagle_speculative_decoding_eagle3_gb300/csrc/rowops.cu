@@ -11,16 +11,43 @@
 namespace e3 {
 
 constexpr int kRowThreads = 256;
+constexpr int kVecThreads = 1024;   // row kernels over H: one 8-element chunk per thread (two above 8192)
+constexpr int kVecChunks = 2;
+
+// Block-wide sums of two values; `scratch` holds >= 64 floats.
+__device__ __forceinline__ float2 block_sum2(float a, float b, float* scratch) {
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5, nw = (blockDim.x + 31) >> 5;
+    a = warp_sum(a);
+    b = warp_sum(b);
+    __syncthreads();
+    if (lane == 0) { scratch[w] = a; scratch[32 + w] = b; }
+    __syncthreads();
+    float ta = (lane < nw) ? scratch[lane] : 0.f, tb = (lane < nw) ? scratch[32 + lane] : 0.f;
+    return make_float2(warp_sum(ta), warp_sum(tb));
+}
+
+template <typename T> __device__ __forceinline__ void load_row8(const T* p, float* v) { widen(ld8<false>(p), v); }
+__device__ __forceinline__ void store_bf8(bf16* p, const float* v) {
+    uint4 u;
+    u.x = pack2_bf16(v[0], v[1]); u.y = pack2_bf16(v[2], v[3]);
+    u.z = pack2_bf16(v[4], v[5]); u.w = pack2_bf16(v[6], v[7]);
+    *reinterpret_cast<uint4*>(p) = u;
+}
+__device__ __forceinline__ void store_row8(float* p, const float* v) {
+    reinterpret_cast<float4*>(p)[0] = make_float4(v[0], v[1], v[2], v[3]);
+    reinterpret_cast<float4*>(p)[1] = make_float4(v[4], v[5], v[6], v[7]);
+}
 
 // x[r] = [ RMS(E[token]) * w_in | RMS(fused[r]) * w_hid ]  (2H wide).
 // The token embedding is the target's table ("Eagle3 DeepseekV3 in MAX" §5); the two streams are
 // normalised separately and concatenated ("EAGLE head deep dive" part 3; MAX §4).
 template <typename T>
-__global__ void __launch_bounds__(kRowThreads)
+__global__ void __launch_bounds__(kVecThreads)
 embed_norms_kernel(RowArgs a, int decode, const int* tokens, const int* positions, const int* row_offsets,
                    int batch, int M, const int* tok_in, const int* lengths, const float* fused,
-                   const T* embed, const T* w_in, const T* w_hid, float* x, int* row_seq, int* row_pos) {
-    __shared__ float red[32];
+                   const T* embed, const T* w_in, const T* w_hid, float* x, bf16* x_bf, int* row_seq,
+                   int* row_pos) {
+    __shared__ float red[64];
     const int r = blockIdx.x;
     int b, tok, pos;
     if (decode) {
@@ -53,23 +80,40 @@ embed_norms_kernel(RowArgs a, int decode, const int* tokens, const int* position
         pos = pos < 0 ? 0 : a.max_ctx - 1;
     }
     if (threadIdx.x == 0) { row_seq[r] = b; row_pos[r] = pos; }
-    const int H = a.H;
+    const int H = a.H, nch = H / 8;
     const T* e = embed + (long)tok * H;
     const float* f = fused + (long)r * H;
+    float ev[kVecChunks][8], fv[kVecChunks][8];
     float se = 0.f, sf = 0.f;
-    for (int k = threadIdx.x; k < H; k += blockDim.x) {
-        const float ev = to_f(e[k]);
-        const float fv = f[k];
-        se += ev * ev;
-        sf += fv * fv;
+#pragma unroll
+    for (int i = 0; i < kVecChunks; ++i) {
+        const int c = threadIdx.x + i * blockDim.x;
+        if (c < nch) {
+            load_row8(e + 8 * c, ev[i]);
+            load_row8(f + 8 * c, fv[i]);
+#pragma unroll
+            for (int k = 0; k < 8; ++k) { se += ev[i][k] * ev[i][k]; sf += fv[i][k] * fv[i][k]; }
+        }
     }
-    se = block_sum(se, red);
-    sf = block_sum(sf, red);
-    const float ie = rsqrtf(se / H + a.eps), iff = rsqrtf(sf / H + a.eps);
+    const float2 ss = block_sum2(se, sf, red);
+    const float ie = rsqrtf(ss.x / H + a.eps), iff = rsqrtf(ss.y / H + a.eps);
     float* xr = x + (long)r * 2 * H;
-    for (int k = threadIdx.x; k < H; k += blockDim.x) {
-        xr[k] = to_f(e[k]) * ie * to_f(w_in[k]);
-        xr[H + k] = f[k] * iff * to_f(w_hid[k]);
+#pragma unroll
+    for (int i = 0; i < kVecChunks; ++i) {
+        const int c = threadIdx.x + i * blockDim.x;
+        if (c < nch) {
+            float wi[8], wh[8], o1[8], o2[8];
+            load_row8(w_in + 8 * c, wi);
+            load_row8(w_hid + 8 * c, wh);
+#pragma unroll
+            for (int k = 0; k < 8; ++k) { o1[k] = ev[i][k] * ie * wi[k]; o2[k] = fv[i][k] * iff * wh[k]; }
+            store_row8(xr + 8 * c, o1);
+            store_row8(xr + H + 8 * c, o2);
+            if (x_bf) {
+                store_bf8(x_bf + (long)r * 2 * H + 8 * c, o1);
+                store_bf8(x_bf + (long)r * 2 * H + H + 8 * c, o2);
+            }
+        }
     }
 }
 
@@ -79,33 +123,53 @@ template <typename T>
 __global__ void __launch_bounds__(kRowThreads)
 latent_kernel(RowArgs a, const float* cqkv, const T* w_qa, const T* w_kva, const float* rope_cos,
               const float* rope_sin, const int* row_seq, const int* row_pos, const int* block_table, T* cache,
-              float* cq_hat) {
-    __shared__ float red[32];
+              float* cq_hat, bf16* cqh_bf) {
+    __shared__ float red[64];
     const int r = blockIdx.x;
     const int dq = a.dq, dc = a.dc, dr = a.dr;
     const float* cq = cqkv + (long)r * (dq + dc + dr);
     const float* ckv = cq + dq;
     const float* kr = ckv + dc;
+    const int t = threadIdx.x;
+    float qv[8], cv[8];
     float s1 = 0.f, s2 = 0.f;
-    for (int k = threadIdx.x; k < dq; k += blockDim.x) s1 += cq[k] * cq[k];
-    for (int k = threadIdx.x; k < dc; k += blockDim.x) s2 += ckv[k] * ckv[k];
-    s1 = block_sum(s1, red);
-    s2 = block_sum(s2, red);
-    const float i1 = rsqrtf(s1 / dq + a.eps), i2 = rsqrtf(s2 / dc + a.eps);
-    for (int k = threadIdx.x; k < dq; k += blockDim.x) cq_hat[(long)r * dq + k] = cq[k] * i1 * to_f(w_qa[k]);
-
+    if (t < dq / 8) {
+        load_row8(cq + 8 * t, qv);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) s1 += qv[k] * qv[k];
+    }
+    if (t < dc / 8) {
+        load_row8(ckv + 8 * t, cv);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) s2 += cv[k] * cv[k];
+    }
+    const float2 ss = block_sum2(s1, s2, red);
+    const float i1 = rsqrtf(ss.x / dq + a.eps), i2 = rsqrtf(ss.y / dc + a.eps);
+    if (t < dq / 8) {
+        float w[8];
+        load_row8(w_qa + 8 * t, w);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) qv[k] *= i1 * w[k];
+        store_row8(cq_hat + (long)r * dq + 8 * t, qv);
+        if (cqh_bf) store_bf8(cqh_bf + (long)r * dq + 8 * t, qv);
+    }
     const int b = row_seq[r], pos = row_pos[r];
     const int pi = pos / a.page_size;
     int page = -1;
     if (pi < a.max_pages) page = block_table[(long)b * a.max_pages + pi];
     if (page < 0 || page >= a.num_pages) {
-        if (threadIdx.x == 0) set_err(a.err, EAGLE3_DEVERR_PAGE);
+        if (t == 0) set_err(a.err, EAGLE3_DEVERR_PAGE);
         return;
     }
     T* dst = cache + ((long)page * a.page_size + pos % a.page_size) * (dc + dr);
-    for (int k = threadIdx.x; k < dc; k += blockDim.x) dst[k] = from_f<T>(ckv[k] * i2 * to_f(w_kva[k]));
+    if (t < dc / 8) {
+        float w[8];
+        load_row8(w_kva + 8 * t, w);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) dst[8 * t + k] = from_f<T>(cv[k] * i2 * w[k]);
+    }
     const int half = dr / 2;
-    for (int i = threadIdx.x; i < half; i += blockDim.x) {
+    for (int i = t; i < half; i += blockDim.x) {
         const float c = rope_cos[(long)pos * half + i], s = rope_sin[(long)pos * half + i];
         const float x0 = kr[2 * i], x1 = kr[2 * i + 1];
         dst[dc + 2 * i] = from_f<T>(x0 * c - x1 * s);
@@ -114,40 +178,80 @@ latent_kernel(RowArgs a, const float* cqkv, const T* w_qa, const T* w_kva, const
 }
 
 template <typename T>
-__global__ void __launch_bounds__(kRowThreads)
-rmsnorm_kernel(int H, float eps, const float* x, const T* w, float* y) {
-    __shared__ float red[32];
+__global__ void __launch_bounds__(kVecThreads)
+rmsnorm_kernel(int H, float eps, const float* x, const T* w, float* y, bf16* y_bf) {
+    __shared__ float red[64];
     const long r = blockIdx.x;
+    const int nch = H / 8;
     const float* xr = x + r * H;
+    float v[kVecChunks][8];
     float s = 0.f;
-    for (int k = threadIdx.x; k < H; k += blockDim.x) s += xr[k] * xr[k];
-    s = block_sum(s, red);
-    const float inv = rsqrtf(s / H + eps);
-    for (int k = threadIdx.x; k < H; k += blockDim.x) y[r * H + k] = xr[k] * inv * to_f(w[k]);
+#pragma unroll
+    for (int i = 0; i < kVecChunks; ++i) {
+        const int c = threadIdx.x + i * blockDim.x;
+        if (c < nch) {
+            load_row8(xr + 8 * c, v[i]);
+#pragma unroll
+            for (int k = 0; k < 8; ++k) s += v[i][k] * v[i][k];
+        }
+    }
+    const float inv = rsqrtf(block_sum2(s, 0.f, red).x / H + eps);
+#pragma unroll
+    for (int i = 0; i < kVecChunks; ++i) {
+        const int c = threadIdx.x + i * blockDim.x;
+        if (c < nch) {
+            float wv[8];
+            load_row8(w + 8 * c, wv);
+#pragma unroll
+            for (int k = 0; k < 8; ++k) v[i][k] *= inv * wv[k];
+            store_row8(y + r * H + 8 * c, v[i]);
+            if (y_bf) store_bf8(y_bf + r * H + 8 * c, v[i]);
+        }
+    }
 }
 
 // Scored row of each sequence (the last new row in extend, MAX §4 "gather last token"):
 // carry its hidden to the next step, normalise it for the lm_head, advance the cache length.
 template <typename T>
-__global__ void __launch_bounds__(kRowThreads)
-final_kernel(RowArgs a, int extend, const int* row_offsets, const float* h2, const T* w_final, const int* row_pos,
-             float* carry, float* z, float* hidden_out, int* lengths) {
-    __shared__ float red[32];
+__global__ void __launch_bounds__(kVecThreads)
+final_kernel(RowArgs a, int extend, int M, const int* row_offsets, const float* h2, const T* w_final,
+             const int* row_pos, float* carry, float* z, bf16* z_bf, float* hidden_out, int* lengths) {
+    __shared__ float red[64];
     const int b = blockIdx.x;
-    const int src = extend ? row_offsets[b + 1] - 1 : b;
-    const int H = a.H;
-    const float* h = h2 + (long)(src < 0 ? 0 : src) * H;
-    float s = 0.f;
-    for (int k = threadIdx.x; k < H; k += blockDim.x) {
-        const float v = h[k];
-        s += v * v;
-        carry[(long)b * H + k] = v;
-        if (hidden_out) hidden_out[(long)b * H + k] = v;
+    int src = extend ? row_offsets[b + 1] - 1 : b;
+    if (src < 0 || src >= M) {   // malformed row_offsets (also flagged by the embedding kernel)
+        if (threadIdx.x == 0) set_err(a.err, EAGLE3_DEVERR_ROWS);
+        src = src < 0 ? 0 : M - 1;
     }
-    s = block_sum(s, red);
-    const float inv = rsqrtf(s / H + a.eps);
-    for (int k = threadIdx.x; k < H; k += blockDim.x) z[(long)b * H + k] = h[k] * inv * to_f(w_final[k]);
-    if (threadIdx.x == 0) lengths[b] = row_pos[src < 0 ? 0 : src] + 1;
+    const int H = a.H, nch = H / 8;
+    const float* h = h2 + (long)src * H;
+    float v[kVecChunks][8];
+    float s = 0.f;
+#pragma unroll
+    for (int i = 0; i < kVecChunks; ++i) {
+        const int c = threadIdx.x + i * blockDim.x;
+        if (c < nch) {
+            load_row8(h + 8 * c, v[i]);
+#pragma unroll
+            for (int k = 0; k < 8; ++k) s += v[i][k] * v[i][k];
+            store_row8(carry + (long)b * H + 8 * c, v[i]);
+            if (hidden_out) store_row8(hidden_out + (long)b * H + 8 * c, v[i]);
+        }
+    }
+    const float inv = rsqrtf(block_sum2(s, 0.f, red).x / H + a.eps);
+#pragma unroll
+    for (int i = 0; i < kVecChunks; ++i) {
+        const int c = threadIdx.x + i * blockDim.x;
+        if (c < nch) {
+            float wv[8];
+            load_row8(w_final + 8 * c, wv);
+#pragma unroll
+            for (int k = 0; k < 8; ++k) v[i][k] *= inv * wv[k];
+            store_row8(z + (long)b * H + 8 * c, v[i]);
+            if (z_bf) store_bf8(z_bf + (long)b * H + 8 * c, v[i]);
+        }
+    }
+    if (threadIdx.x == 0) lengths[b] = row_pos[src] + 1;
 }
 
 __device__ __forceinline__ int remap_token(int d, const int* d2t, int Vt, int* err) {
@@ -227,44 +331,44 @@ accept_kernel(const int* draft, const int* target, int batch, int gamma, int* ac
 cudaError_t launch_embed_norms(const RowArgs& a, bool decode, int M, const int* tokens, const int* positions,
                                const int* row_offsets, int batch, const int* tok_in, const int* lengths,
                                const float* fused, const void* embed, const void* w_in, const void* w_hid,
-                               float* x, int* row_seq, int* row_pos, cudaStream_t st) {
+                               float* x, __nv_bfloat16* x_bf, int* row_seq, int* row_pos, cudaStream_t st) {
     if (a.dt == BF16)
-        embed_norms_kernel<bf16><<<M, kRowThreads, 0, st>>>(a, decode, tokens, positions, row_offsets, batch, M,
-            tok_in, lengths, fused, (const bf16*)embed, (const bf16*)w_in, (const bf16*)w_hid, x, row_seq, row_pos);
+        embed_norms_kernel<bf16><<<M, kVecThreads, 0, st>>>(a, decode, tokens, positions, row_offsets, batch, M,
+            tok_in, lengths, fused, (const bf16*)embed, (const bf16*)w_in, (const bf16*)w_hid, x, x_bf, row_seq, row_pos);
     else
-        embed_norms_kernel<float><<<M, kRowThreads, 0, st>>>(a, decode, tokens, positions, row_offsets, batch, M,
-            tok_in, lengths, fused, (const float*)embed, (const float*)w_in, (const float*)w_hid, x, row_seq, row_pos);
+        embed_norms_kernel<float><<<M, kVecThreads, 0, st>>>(a, decode, tokens, positions, row_offsets, batch, M,
+            tok_in, lengths, fused, (const float*)embed, (const float*)w_in, (const float*)w_hid, x, x_bf, row_seq, row_pos);
     return cudaGetLastError();
 }
 
 cudaError_t launch_latent(const RowArgs& a, int M, const float* cqkv, const void* w_qa, const void* w_kva,
                           const float* rope_cos, const float* rope_sin, const int* row_seq, const int* row_pos,
-                          const int* block_table, void* cache, float* cq_hat, cudaStream_t st) {
+                          const int* block_table, void* cache, float* cq_hat, __nv_bfloat16* cqh_bf, cudaStream_t st) {
     if (a.dt == BF16)
         latent_kernel<bf16><<<M, kRowThreads, 0, st>>>(a, cqkv, (const bf16*)w_qa, (const bf16*)w_kva, rope_cos,
-            rope_sin, row_seq, row_pos, block_table, (bf16*)cache, cq_hat);
+            rope_sin, row_seq, row_pos, block_table, (bf16*)cache, cq_hat, cqh_bf);
     else
         latent_kernel<float><<<M, kRowThreads, 0, st>>>(a, cqkv, (const float*)w_qa, (const float*)w_kva, rope_cos,
-            rope_sin, row_seq, row_pos, block_table, (float*)cache, cq_hat);
+            rope_sin, row_seq, row_pos, block_table, (float*)cache, cq_hat, cqh_bf);
     return cudaGetLastError();
 }
 
 cudaError_t launch_rmsnorm(int M, int H, float eps, DType wt, const float* x, const void* w, float* y,
-                           cudaStream_t st) {
-    if (wt == BF16) rmsnorm_kernel<bf16><<<M, kRowThreads, 0, st>>>(H, eps, x, (const bf16*)w, y);
-    else rmsnorm_kernel<float><<<M, kRowThreads, 0, st>>>(H, eps, x, (const float*)w, y);
+                           __nv_bfloat16* y_bf, cudaStream_t st) {
+    if (wt == BF16) rmsnorm_kernel<bf16><<<M, kVecThreads, 0, st>>>(H, eps, x, (const bf16*)w, y, y_bf);
+    else rmsnorm_kernel<float><<<M, kVecThreads, 0, st>>>(H, eps, x, (const float*)w, y, y_bf);
     return cudaGetLastError();
 }
 
-cudaError_t launch_final(const RowArgs& a, bool extend, int batch, const int* row_offsets, const float* h2,
-                         const void* w_final, const int* row_pos, float* carry, float* z, float* hidden_out,
-                         int* lengths, cudaStream_t st) {
+cudaError_t launch_final(const RowArgs& a, bool extend, int batch, int M, const int* row_offsets, const float* h2,
+                         const void* w_final, const int* row_pos, float* carry, float* z, __nv_bfloat16* z_bf,
+                         float* hidden_out, int* lengths, cudaStream_t st) {
     if (a.dt == BF16)
-        final_kernel<bf16><<<batch, kRowThreads, 0, st>>>(a, extend, row_offsets, h2, (const bf16*)w_final, row_pos,
-                                                          carry, z, hidden_out, lengths);
+        final_kernel<bf16><<<batch, kVecThreads, 0, st>>>(a, extend, M, row_offsets, h2, (const bf16*)w_final,
+                                                          row_pos, carry, z, z_bf, hidden_out, lengths);
     else
-        final_kernel<float><<<batch, kRowThreads, 0, st>>>(a, extend, row_offsets, h2, (const float*)w_final,
-                                                           row_pos, carry, z, hidden_out, lengths);
+        final_kernel<float><<<batch, kVecThreads, 0, st>>>(a, extend, M, row_offsets, h2, (const float*)w_final,
+                                                           row_pos, carry, z, z_bf, hidden_out, lengths);
     return cudaGetLastError();
 }
 

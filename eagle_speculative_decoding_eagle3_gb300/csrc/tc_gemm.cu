@@ -1,0 +1,391 @@
+// tcgen05 (5th-generation tensor core) GEMM for the linear layers at many activation rows.
+//
+// out[m, n] = sum_k W[n, k] X[m, k] for the bias-free projections of the draft head (fc, q_a | kv_a,
+// q_b, o_proj, gate | up, down, lm_head; "Eagle3 DeepseekV3 in MAX" §4) once the rows no longer fit
+// the weight-streaming GEMV (extend, or decode at large batch).
+//
+// Orientation: the WEIGHT tile is the MMA "A" operand (128 rows of W, the MMA M) and the ACTIVATION
+// tile is the MMA "B" operand (BN rows of X, the MMA N), so one tile is D^T[n, m] in TMEM with
+// lane = output feature n and column = token m.  A small batch then still fills the 128-row MMA, and
+// the epilogue's warp writes 32 consecutive features of one token: coalesced stores.
+//
+// Per CTA (192 threads): warp 0 issues TMA loads (128-byte swizzle, K-major) into a STAGES-deep
+// ring; warp 1 owns the TMEM accumulator and one elected lane issues tcgen05.mma (kind::f16, bf16
+// in, fp32 accumulate) and tcgen05.commit to release stages; warps 2-5 wait for the accumulator,
+// read it with tcgen05.ld and apply the epilogue (store, residual add, SiLU(gate) * up, row argmax,
+// or split-K partials).  Every mbarrier wait is bounded: a wait that runs out sets an error bit,
+// the CTA skips the rest of its work, drains its own copies (bounded), frees TMEM and returns.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <float.h>
+#include <limits.h>
+
+#include "common.cuh"
+#include "kernels.h"
+#include "../../include/eagle3.h"
+
+namespace e3 {
+namespace tc {
+
+constexpr int BM = 128;                 // weight rows per tile (MMA M)
+constexpr int BK = 64;                  // K per stage: one 128-byte swizzle atom of bf16
+constexpr int kThreads = 192;
+constexpr uint32_t kWaitLimit = 1u << 25;
+constexpr int kSmemBudget = 200 * 1024;
+
+__device__ __forceinline__ uint32_t su32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count));
+}
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.release.cta.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok) : "r"(bar), "r"(parity) : "memory");
+    return ok != 0;
+}
+// Bounded wait; false when the limit ran out.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+    for (uint32_t i = 0; i < kWaitLimit; ++i)
+        if (mbar_try(bar, parity)) return true;
+    return false;
+}
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, uint32_t bar, int c0, int c1) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4}], [%2];"
+        ::"r"(dst), "l"((uint64_t)map), "r"(bar), "r"(c0), "r"(c1) : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+// Shared-memory matrix descriptor: K-major tile written by TMA with 128-byte swizzle; rows are
+// 128 B apart and 8-row groups 1024 B apart (stride byte offset); version 1; layout SWIZZLE_128B.
+__device__ __forceinline__ uint64_t smem_desc(uint32_t addr) {
+    uint64_t d = (uint64_t)((addr & 0x3FFFFu) >> 4);
+    d |= (uint64_t)1 << 16;                 // leading byte offset (unused for swizzled K-major)
+    d |= (uint64_t)(1024 >> 4) << 32;       // stride byte offset
+    d |= (uint64_t)1 << 46;                 // descriptor version
+    d |= (uint64_t)2 << 61;                 // 128-byte swizzle
+    return d;
+}
+// Instruction descriptor, kind::f16: fp32 accumulate, bf16 A and B, both K-major, M = 128, N = bn.
+__host__ __device__ constexpr uint32_t instr_desc(int bn) {
+    return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(bn >> 3) << 17) | ((uint32_t)(BM >> 4) << 24);
+}
+__device__ __forceinline__ void mma_bf16(uint32_t dtmem, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+    asm volatile("{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+                 " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n"
+                 ::"r"(dtmem), "l"(a), "l"(b), "r"(idesc), "r"(acc));
+}
+__device__ __forceinline__ void mma_commit(uint32_t bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+                 : "memory");
+}
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float* v) {
+    uint32_t r[16];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+template <int BN, bool GLU> struct Cfg {
+    static constexpr int NP = GLU ? 2 : 1;
+    static constexpr int P_BYTES = BM * BK * 2;
+    static constexpr int Q_BYTES = BN * BK * 2;
+    static constexpr int STAGE = NP * P_BYTES + Q_BYTES;
+    static constexpr int STAGES = (kSmemBudget / STAGE) > 6 ? 6 : (kSmemBudget / STAGE);
+    static constexpr int COLS_USED = NP * BN;
+    static constexpr int TMEM_COLS = COLS_USED <= 32 ? 32 : COLS_USED <= 64 ? 64 : COLS_USED <= 128 ? 128
+                                   : COLS_USED <= 256 ? 256 : 512;
+    static constexpr int SMEM = STAGES * STAGE + 1024 + 256;
+};
+
+template <int BN, bool GLU>
+__global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_constant__ TcParams p) {
+    using C = Cfg<BN, GLU>;
+    extern __shared__ unsigned char smem_raw[];
+    unsigned char* base = reinterpret_cast<unsigned char*>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(base + C::STAGES * C::STAGE);
+    // bars[0..S) full, bars[S..2S) empty, bars[2S] accumulator ready
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * C::STAGES + 1);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int n0 = blockIdx.x * BM, m0 = blockIdx.y * BN;
+    const int split = blockIdx.z % p.splits, batch = blockIdx.z / p.splits;
+    const int kb0 = split * p.kb_per_split;
+    const int kb1 = min(p.nkb, kb0 + p.kb_per_split);
+    const int nkb = kb1 - kb0;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < C::STAGES; ++s) {
+            mbar_init(su32(&bars[s]), 1);
+            mbar_init(su32(&bars[C::STAGES + s]), 1);
+        }
+        mbar_init(su32(&bars[2 * C::STAGES]), 1);
+        *abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(su32(tmem_slot)),
+                     "r"(C::TMEM_COLS));
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    int issued = 0;
+
+    if (warp == 0 && lane == 0 && nkb > 0) {
+        // ---------------- TMA producer
+        const bool second = !GLU && n0 >= p.np0;
+        const CUtensorMap* mw = second ? &p.mw[1] : &p.mw[0];
+        const int wrow = (second ? n0 - p.np0 : n0) + batch * p.bw_rows;
+        for (int i = 0; i < nkb; ++i) {
+            const int s = i % C::STAGES;
+            const uint32_t ph = (uint32_t)(i / C::STAGES) & 1u;
+            if (!mbar_wait(su32(&bars[C::STAGES + s]), ph ^ 1u)) { *abort_flag = 1; break; }
+            if (*abort_flag) break;
+            unsigned char* st = base + s * C::STAGE;
+            const uint32_t full = su32(&bars[s]);
+            mbar_expect_tx(full, C::STAGE);
+            const int kb = kb0 + i;
+            tma_load_2d(su32(st), mw, full, kb * BK, wrow);
+            if (GLU) tma_load_2d(su32(st + C::P_BYTES), &p.mw[1], full, kb * BK, n0 + batch * p.bw_rows);
+            const int qs = kb >= p.kseg[1] ? 2 : (kb >= p.kseg[0] ? 1 : 0);
+            const int kl = kb - (qs == 0 ? 0 : p.kseg[qs - 1]) + batch * p.bq_kb;
+            tma_load_2d(su32(st + C::NP * C::P_BYTES), &p.mx[qs], full, kl * BK, m0);
+            ++issued;
+        }
+    } else if (warp == 1 && lane == 0 && nkb > 0) {
+        // ---------------- MMA issuer
+        constexpr uint32_t idesc = instr_desc(BN);
+        for (int i = 0; i < nkb; ++i) {
+            const int s = i % C::STAGES;
+            const uint32_t ph = (uint32_t)(i / C::STAGES) & 1u;
+            if (!mbar_wait(su32(&bars[s]), ph)) { *abort_flag = 1; break; }
+            tc_fence_after();
+            const uint32_t st = su32(base + s * C::STAGE);
+            const uint64_t da = smem_desc(st);
+            const uint64_t da2 = smem_desc(st + C::P_BYTES);
+            const uint64_t db = smem_desc(st + C::NP * C::P_BYTES);
+#pragma unroll
+            for (int kk = 0; kk < BK / 16; ++kk) {
+                const uint32_t acc = (i > 0 || kk > 0) ? 1u : 0u;
+                mma_bf16(tmem, da + 2 * kk, db + 2 * kk, idesc, acc);
+                if (GLU) mma_bf16(tmem + BN, da2 + 2 * kk, db + 2 * kk, idesc, acc);
+            }
+            mma_commit(su32(&bars[C::STAGES + s]));
+        }
+        mma_commit(su32(&bars[2 * C::STAGES]));
+    } else if (warp >= 2) {
+        // ---------------- epilogue: TMEM lanes [32q, 32q+32) are readable by warp q = warp % 4
+        const int q = warp & 3;
+        const int n = n0 + 32 * q + lane;
+        const long ncol = n + (long)batch * p.by_col;   // output column of feature n
+        const bool nvalid = n < p.N;
+        bool ok = nkb > 0 && mbar_wait(su32(&bars[2 * C::STAGES]), 0);
+        ok = __all_sync(0xffffffffu, ok);   // tcgen05.ld is warp-collective
+        if (!ok && nkb > 0) *abort_flag = 1;
+        tc_fence_after();
+        const uint32_t trow = tmem + ((uint32_t)(32 * q) << 16);
+        const bool split = gridDim.z > 1;
+        for (int c = 0; c < BN; c += 16) {
+            float v[16], u[16];
+            if (ok) {
+                tmem_ld16(trow + c, v);
+                if (GLU) tmem_ld16(trow + BN + c, u);
+            } else {
+#pragma unroll
+                for (int j = 0; j < 16; ++j) { v[j] = 0.f; u[j] = 0.f; }
+            }
+            if (p.epi == EPI_ARGMAX) {
+                // per token: (max, argmax) over this warp's 32 features, lowest index on ties
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                    float bvv = nvalid ? v[j] : -FLT_MAX;
+                    int bi = nvalid ? n : INT_MAX;
+                    const int m = m0 + c + j;
+                    if (p.logits && nvalid && m < p.M) p.logits[(long)m * p.ldl + ncol] = v[j];
+#pragma unroll
+                    for (int o = 16; o > 0; o >>= 1) {
+                        const float ov = __shfl_xor_sync(0xffffffffu, bvv, o);
+                        const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+                        if (better(ov, oi, bvv, bi)) { bvv = ov; bi = oi; }
+                    }
+                    if (lane == 0) {
+                        float* rv = reinterpret_cast<float*>(base);          // stage memory is idle now
+                        int* ri = reinterpret_cast<int*>(base + 4 * BN * sizeof(float));
+                        rv[q * BN + c + j] = bvv;
+                        ri[q * BN + c + j] = bi;
+                    }
+                }
+                continue;
+            }
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+                const int m = m0 + c + j;
+                if (!nvalid || m >= p.M) continue;
+                if (split) {
+                    const long plane = (long)p.M * p.N;
+                    float* part = p.part + (long)split * C::NP * plane;
+                    part[(long)m * p.N + n] = v[j];
+                    if (GLU) part[plane + (long)m * p.N + n] = u[j];
+                    continue;
+                }
+                float out;
+                if (GLU) out = silu(v[j]) * u[j];
+                else if (p.epi == EPI_RESID) out = v[j] + p.resid[(long)m * p.ldr + ncol];
+                else out = v[j];
+                if (p.y) p.y[(long)m * p.ldy + ncol] = out;
+                if (p.ybf) p.ybf[(long)m * p.ldybf + ncol] = __float2bfloat16_rn(out);
+            }
+        }
+        if (p.epi == EPI_ARGMAX) {
+            asm volatile("bar.sync 1, 128;" ::: "memory");   // the four epilogue warps
+            const float* rv = reinterpret_cast<const float*>(base);
+            const int* ri = reinterpret_cast<const int*>(base + 4 * BN * sizeof(float));
+            for (int j = threadIdx.x - 64; j < BN; j += 128) {
+                const int m = m0 + j;
+                if (m >= p.M) continue;
+                float b = rv[j];
+                int bi = ri[j];
+                for (int w = 1; w < 4; ++w)
+                    if (better(rv[w * BN + j], ri[w * BN + j], b, bi)) { b = rv[w * BN + j]; bi = ri[w * BN + j]; }
+                p.pval[(long)m * p.npart + blockIdx.x] = b;
+                p.pidx[(long)m * p.npart + blockIdx.x] = bi;
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (*abort_flag) {
+        if (threadIdx.x == 0) atomicOr(p.err, EAGLE3_DEVERR_TIMEOUT);
+        // drain this CTA's own copies still in flight (bounded) before its shared memory goes away
+        if (warp == 0 && lane == 0) {
+            for (int i = max(0, issued - C::STAGES); i < issued; ++i)
+                mbar_wait(su32(&bars[i % C::STAGES]), (uint32_t)(i / C::STAGES) & 1u);
+        }
+        __syncthreads();
+    }
+    if (warp == 1) {
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(C::TMEM_COLS));
+    }
+}
+
+// Split-K reduction: out = epi(sum_z part[z]) for STORE / RESID / GLU.
+__global__ void tc_splitk_reduce(const TcParams p, int splits, int glu) {
+    const long total = (long)p.M * p.N;
+    const long plane = total;
+    const int np = glu ? 2 : 1;
+    for (long i = blockIdx.x * (long)blockDim.x + threadIdx.x; i < total; i += (long)gridDim.x * blockDim.x) {
+        float v = 0.f, u = 0.f;
+        for (int z = 0; z < splits; ++z) {
+            v += p.part[(long)z * np * plane + i];
+            if (glu) u += p.part[(long)z * np * plane + plane + i];
+        }
+        const long m = i / p.N, n = i % p.N;
+        float out;
+        if (glu) out = silu(v) * u;
+        else if (p.epi == EPI_RESID) out = v + p.resid[m * p.ldr + n];
+        else out = v;
+        if (p.y) p.y[m * p.ldy + n] = out;
+        if (p.ybf) p.ybf[m * p.ldybf + n] = __float2bfloat16_rn(out);
+    }
+}
+
+}  // namespace tc
+
+// ------------------------------------------------------------------------------------------ host
+static PFN_cuTensorMapEncodeTiled_v12000 tma_encoder() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (!fn) {
+        cudaDriverEntryPointQueryResult q;
+        void* f = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess && q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+    }
+    return fn;
+}
+
+// 2-D bf16 tensor map over a row-major [rows, cols] matrix with row stride `ld` elements; box = 64 x box_rows.
+bool make_tma_2d(CUtensorMap* map, const void* ptr, long rows, long cols, long ld, int box_rows) {
+    auto enc = tma_encoder();
+    if (!enc || !ptr || ((uintptr_t)ptr & 15) || (ld * 2) % 16 || cols % 8) return false;
+    cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)ld * 2};
+    cuuint32_t box[2] = {(cuuint32_t)tc::BK, (cuuint32_t)box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int BN, bool GLU>
+static cudaError_t tc_launch_bn(const TcParams& p, dim3 grid, cudaStream_t st) {
+    using C = tc::Cfg<BN, GLU>;
+    static bool attr = false;
+    if (!attr) {
+        cudaError_t e = cudaFuncSetAttribute(tc::tc_gemm_kernel<BN, GLU>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             C::SMEM);
+        if (e != cudaSuccess) return e;
+        attr = true;
+    }
+    tc::tc_gemm_kernel<BN, GLU><<<grid, tc::kThreads, C::SMEM, st>>>(p);
+    return cudaGetLastError();
+}
+
+int tc_pick_bn(int M) {
+    if (M <= 16) return 16;
+    if (M <= 32) return 32;
+    if (M <= 64) return 64;
+    if (M <= 128) return 128;
+    return 256;
+}
+
+cudaError_t launch_tc_gemm(TcParams& p, int bn, int splits, cudaStream_t st) {
+    p.nkb = p.K / tc::BK;
+    if (splits < 1 || p.nbatch > 1) splits = 1;
+    if (p.nbatch < 1) p.nbatch = 1;
+    p.kb_per_split = (p.nkb + splits - 1) / splits;
+    splits = (p.nkb + p.kb_per_split - 1) / p.kb_per_split;
+    p.splits = splits;
+    dim3 grid((p.N + tc::BM - 1) / tc::BM, (p.M + bn - 1) / bn, splits * p.nbatch);
+    if (p.epi == EPI_ARGMAX) p.npart = grid.x;
+    const bool glu = p.epi == EPI_GLU;
+    cudaError_t e;
+#define TC_CASE(B)                                                                       \
+    case B:                                                                              \
+        e = glu ? tc_launch_bn<B, true>(p, grid, st) : tc_launch_bn<B, false>(p, grid, st); \
+        break;
+    switch (bn) {
+        TC_CASE(16)
+        TC_CASE(32)
+        TC_CASE(64)
+        TC_CASE(128)
+        TC_CASE(256)
+        default: return cudaErrorInvalidValue;
+    }
+#undef TC_CASE
+    if (e != cudaSuccess || splits == 1) return e;
+    const long total = (long)p.M * p.N;
+    int blocks = (int)((total + 255) / 256);
+    if (blocks > 4096) blocks = 4096;
+    tc::tc_splitk_reduce<<<blocks, 256, 0, st>>>(p, splits, glu ? 1 : 0);
+    return cudaGetLastError();
+}
+
+}  // namespace e3

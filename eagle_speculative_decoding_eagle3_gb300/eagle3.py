@@ -70,7 +70,12 @@ def _lib():
         lib.eagle3_draft_get_error.argtypes = [P, C.POINTER(C.c_int32)]
         lib.eagle3_draft_clear_error.argtypes = [P, P]
         lib.eagle3_draft_destroy.argtypes = [P]
-        for f in ("eagle3_draft_create", "eagle3_draft_workspace_bytes", "eagle3_draft_extend", "eagle3_draft_decode",
+        lib.eagle3_draft_profile_enable.argtypes = [P, C.c_int32]
+        lib.eagle3_draft_profile_read.argtypes = [P, C.c_int32, C.POINTER(C.c_double), C.POINTER(C.c_int64),
+                                                  C.POINTER(C.c_int64), C.POINTER(C.c_char_p)]
+        lib.eagle3_draft_profile_reset.argtypes = [P]
+        for f in ("eagle3_draft_profile_enable", "eagle3_draft_profile_read", "eagle3_draft_profile_reset",
+                  "eagle3_draft_create", "eagle3_draft_workspace_bytes", "eagle3_draft_extend", "eagle3_draft_decode",
                   "eagle3_accept", "eagle3_draft_get_error", "eagle3_draft_clear_error", "eagle3_draft_destroy"):
             getattr(lib, f).restype = C.c_int
         _L = lib
@@ -169,6 +174,25 @@ def eagle3_draft_get_error(handle) -> int:
 
 def eagle3_draft_clear_error(handle, stream=None):
     _check("eagle3_draft_clear_error", _lib().eagle3_draft_clear_error(handle, _stream(stream)))
+
+
+PROF_KINDS = 24
+
+
+def eagle3_draft_profile_enable(handle, enable=True):
+    _check("eagle3_draft_profile_enable", _lib().eagle3_draft_profile_enable(handle, int(bool(enable))))
+
+
+def eagle3_draft_profile_read(handle, kind):
+    """(name, total_ms, timed_launches, launches) of one kernel kind since the last reset (synchronises)."""
+    ms, t, n, name = C.c_double(), C.c_int64(), C.c_int64(), C.c_char_p()
+    _check("eagle3_draft_profile_read", _lib().eagle3_draft_profile_read(
+        handle, int(kind), C.byref(ms), C.byref(t), C.byref(n), C.byref(name)))
+    return name.value.decode(), ms.value, t.value, n.value
+
+
+def eagle3_draft_profile_reset(handle):
+    _check("eagle3_draft_profile_reset", _lib().eagle3_draft_profile_reset(handle))
 
 
 def eagle3_draft_destroy(handle):

@@ -70,6 +70,7 @@ typedef enum { EAGLE3_F32 = 0, EAGLE3_BF16 = 1 } eagle3_dtype_t;
 #define EAGLE3_DEVERR_D2T      4   /* d + d2t[d] was outside [0, target_vocab) */
 #define EAGLE3_DEVERR_PAGE     8   /* a position's page was outside the block table or the cache */
 #define EAGLE3_DEVERR_ROWS     16  /* row_offsets were not non-decreasing within [0, num_tokens] */
+#define EAGLE3_DEVERR_TIMEOUT  32  /* a bounded wait inside a tensor-core kernel ran out (work skipped) */
 
 /* Head configuration (host struct, copied by create).  Field names follow the DeepseekV3 config
  * (MAX API reference, Eagle3DeepseekV3DraftConfig). */
@@ -192,6 +193,20 @@ EAGLE3_API eagle3_status_t eagle3_draft_clear_error(eagle3_draft_t *d, void *str
 
 /* Free the workspace and the handle (synchronises the device).  NULL is accepted. */
 EAGLE3_API eagle3_status_t eagle3_draft_destroy(eagle3_draft_t *d);
+
+/* ---- Per-kernel timing (native tracing).  When enabled, every kernel launch of the handle is
+ * bracketed by CUDA events recorded on the launch stream; read() synchronises and accumulates the
+ * event intervals per kernel kind.  Launches are counted whether or not timing is enabled. */
+#define EAGLE3_PROF_KINDS 24
+EAGLE3_API eagle3_status_t eagle3_draft_profile_enable(eagle3_draft_t *d, int32_t enable);
+/* For kernel kind `kind` (0 <= kind < EAGLE3_PROF_KINDS) since the last reset: total milliseconds over
+ * the timed launches, the number of timed launches, and the number of launches (timed or not; the
+ * event pool times at most 32768 launches between reads).  Synchronises the device.  Launches recorded
+ * inside a CUDA graph report the intervals of the graph's latest replay.  *name (host, optional)
+ * receives a static kernel name. */
+EAGLE3_API eagle3_status_t eagle3_draft_profile_read(eagle3_draft_t *d, int32_t kind, double *total_ms,
+                                                     int64_t *timed, int64_t *launches, const char **name);
+EAGLE3_API eagle3_status_t eagle3_draft_profile_reset(eagle3_draft_t *d);
 
 /* Static string for a status code. */
 EAGLE3_API const char *eagle3_status_string(eagle3_status_t s);

@@ -62,7 +62,8 @@ def run_round(w, seqs=None, absorbed=False, with_logits=True, stored=None, d2t_o
     W = WL.F32View(stored)
     caches = [O.SeqCache(WL.as_f32(WL.cache_rows(w, b, int(lengths[b]))), w.max_ctx) for b in seqs]
     exs = WL.make_extend(w, lengths, seqs=seqs)
-    orc = O.draft_round(w.hyper(), W, d2t, w.gamma, exs.aux, exs.tokens, exs.positions, exs.row_offsets, caches,
+    aux = [WL.as_f32(a) for a in exs.aux]
+    orc = O.draft_round(w.hyper(), W, d2t, w.gamma, aux, exs.tokens, exs.positions, exs.row_offsets, caches,
                         absorbed=absorbed, forced=gpu["tokens"][seqs])
     orc["caches"] = caches
     orc["lengths"] = lengths

@@ -44,3 +44,11 @@ def test_mla_shaped_bf16_round():
                     accept_p=(0.7,) * 4, seed=79)
     gpu, orc, seqs, paged = run_round(w)
     print(check_round(w, gpu, orc, seqs, paged, TOL_BF16))
+
+
+def test_dsv3_b1_full_size_round():
+    # the batch-1 DeepseekV3-shaped workload at full size (4096-token cache, 32000-entry draft vocab
+    # with d2t), as the benchmark runs it; the oracle follows the unabsorbed definition
+    w = WL.workload("dsv3_b1")
+    gpu, orc, seqs, paged = run_round(w)
+    print(check_round(w, gpu, orc, seqs, paged, TOL_BF16))
