@@ -167,7 +167,7 @@ def algorithmic_bytes(w, ctx_lengths):
         add("q_a_kv_a", (dq + D) * 2 * H * ws + M * 2 * H * 4 + M * (dq + D) * 4, n)
         add("q_b", nh * dqk * dq * ws + M * dq * 4 + M * nh * dqk * 4, n)
         add("absorb", nh * dn * dc * ws + M * nh * dqk * 4 + M * nh * D * 4, n)
-        add("combine_unabsorb", nh * dv * dc * ws + M * nh * dv * 4, n)
+        add("unabsorb", nh * dv * dc * ws + M * nh * dc * 4 + M * nh * dv * 4, n)
         add("o_proj", H * nh * dv * ws + M * nh * dv * 4 + 2 * M * H * 4, n)
         add("gate_up_silu", 2 * I * H * ws + M * H * 4 + M * I * 4, n)
         add("down", H * I * ws + M * I * 4 + 2 * M * H * 4, n)
@@ -229,16 +229,38 @@ def run_ours(args, ws, rank, local):
     torch.cuda.synchronize()
     barrier(ws)
 
-    # The timed region is one CUDA graph holding `steps` rounds, so host launch cost stays out of it.
-    # The library's tracing events are captured inside the graph: after the timed replay they hold
-    # that replay's per-kernel intervals.
-    E.eagle3_draft_profile_reset(head.handle)
-    E.eagle3_draft_profile_enable(head.handle, True)
-    graph = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(graph):
-        cap = torch.cuda.current_stream()
-        for _ in range(args.steps):
-            step(cap)
+    def capture(kind_mask):
+        """CUDA graph of `steps` rounds; the launches of the kinds in kind_mask are bracketed by the
+        library's tracing events, captured as graph timestamp nodes."""
+        E.eagle3_draft_profile_reset(head.handle)
+        E.eagle3_draft_profile_enable(head.handle, kind_mask)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            cap = torch.cuda.current_stream()
+            for _ in range(args.steps):
+                step(cap)
+        return g
+
+    def read_profile():
+        prof, launches = {}, 0
+        for k in range(E.PROF_KINDS):
+            name, tot, timed, n = E.eagle3_draft_profile_read(head.handle, k)
+            if n:
+                prof[name] = (tot, timed, n, k)
+                launches += n
+        E.eagle3_draft_profile_enable(head.handle, 0)
+        return prof, launches
+
+    # Pass 1 (untimed): every kernel instrumented, to find the dominant kernel and its share.
+    g1 = capture(-1)
+    g1.replay()
+    torch.cuda.synchronize()
+    prof_all, _ = read_profile()
+    del g1
+    dom = max(prof_all, key=lambda k: prof_all[k][0])
+    # Pass 2 (timed): the same graph with only the dominant kernel bracketed by events, so the
+    # headline time carries almost no instrumentation; its launches give the roofline duration.
+    graph = capture(1 << prof_all[dom][3])
     graph.replay()                      # untimed: uploads the graph and warms it
     torch.cuda.synchronize()
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -251,14 +273,7 @@ def run_ours(args, ws, rank, local):
     barrier(ws)
     ms = ev0.elapsed_time(ev1)
     ms_max = reduce_max(ms, ws)
-    prof = {}
-    launches = 0
-    for k in range(E.PROF_KINDS):
-        name, tot, timed, n = E.eagle3_draft_profile_read(head.handle, k)
-        if n:
-            prof[name] = (tot, timed)
-            launches += n
-    E.eagle3_draft_profile_enable(head.handle, False)
+    prof_dom, launches = read_profile()
     launches += args.steps  # one acceptance launch per round
     assert head.error_word() == 0
     del graph
@@ -306,18 +321,19 @@ def run_ours(args, ws, rank, local):
     hbm = peak_hbm(peaks)
     model = algorithmic_bytes(w, lengths)
     kernels = {}
-    for name, (tot, n) in prof.items():
-        per = tot / n
-        entry = {"launches": n, "avg_us": round(per * 1e3, 2), "share": round(tot / sum(t for t, _ in prof.values()), 4)}
+    tot_all = sum(v[0] for v in prof_all.values())
+    for name, (tot, timed, n, _) in prof_all.items():
+        per = tot / timed
+        entry = {"launches": n, "avg_us": round(per * 1e3, 2), "share": round(tot / tot_all, 4)}
         if name in model and model[name][0] > 0:
             gbs = model[name][0] / (per * 1e-3) / 1e9
             entry["algo_bytes"] = int(model[name][0])
             entry["achieved_gbs"] = round(gbs, 1)
             entry["hbm_frac"] = round(gbs / hbm, 4)
         kernels[name] = entry
-    dom = max(prof, key=lambda k: prof[k][0])
+    dom_tot, dom_timed = prof_dom[dom][0], prof_dom[dom][1]
     dom_bytes = model.get(dom, (0.0, 0))[0]
-    dom_avg_s = prof[dom][0] / prof[dom][1] * 1e-3
+    dom_avg_s = dom_tot / dom_timed * 1e-3
     achieved = dom_bytes / dom_avg_s / 1e9 if dom_avg_s > 0 else 0.0
     round_bytes = sum(b * n for b, n in model.values())
     step_s = ms_max / args.steps * 1e-3
@@ -336,11 +352,14 @@ def run_ours(args, ws, rank, local):
                    "l2": f"inputs larger than L2: {round_bytes / 1e9:.2f} GB of weights+KV streamed per step",
                    "parallelism": f"replicas x{ws} (sequence-sharded, no collective)"},
         "roofline": {"bound": "hbm", "kernel": dom, "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
-                     "frac": round(achieved / hbm, 4), "traffic": None,
+                     "frac": round(achieved / hbm, 4), "traffic": None, "avg_us": round(dom_avg_s * 1e6, 2),
+                     "algo_bytes_per_launch": int(dom_bytes),
                      "peak_source": f"{src} ({'MEASURED_PEAKS.json hbm' if src == 'measured' else 'fallback 6.8 TB/s'})"},
         "step_roofline": {"algo_bytes": int(round_bytes), "achieved_gbs": round(round_bytes / step_s / 1e9, 1),
                           "frac": round(round_bytes / step_s / 1e9 / hbm, 4)},
         "kernels": kernels,
+        "kernels_note": "per-kernel times from an untimed replay of the same graph with every launch "
+                        "bracketed by events; the timed replay brackets only the roofline kernel",
         "e2e": {"value": round(ws * tok_per_round * e2e_steps / e2e_s, 2), "unit": UNIT,
                 "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)},
         "gpu_launches": int(launches),

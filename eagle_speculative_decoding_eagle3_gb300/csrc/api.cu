@@ -29,7 +29,7 @@ enum Kind {
 };
 static_assert(K_COUNT <= EAGLE3_PROF_KINDS, "profile kinds");
 const char* kKindNames[EAGLE3_PROF_KINDS] = {
-    "fc", "embed_norms", "q_a_kv_a", "latent_rope_append", "q_b", "absorb", "attention", "combine_unabsorb",
+    "fc", "embed_norms", "q_a_kv_a", "latent_rope_append", "q_b", "absorb", "attention", "merge_splits",
     "o_proj", "post_attn_norm", "gate_up_silu", "down", "final_norm", "lm_head_argmax", "argmax_remap",
     "emit_first", "rope_q", "unabsorb", "", "", "", "", "", ""};
 constexpr int kProfPairs = 32768;
@@ -52,7 +52,7 @@ struct eagle3_draft {
     float *f = nullptr, *carry = nullptr, *x = nullptr, *cqkv = nullptr, *cq_hat = nullptr, *q = nullptr,
           *qa = nullptr, *part_o = nullptr, *part_ml = nullptr, *o = nullptr, *h1 = nullptr, *y = nullptr,
           *mlp = nullptr, *h2 = nullptr, *z = nullptr, *pval = nullptr, *rope_cos = nullptr,
-          *rope_sin = nullptr, *tc_part = nullptr;
+          *rope_sin = nullptr, *tc_part = nullptr, *olat = nullptr;
     bf16_t *qa_bf = nullptr, *x_bf = nullptr, *cqh_bf = nullptr, *q_bf = nullptr, *olat_bf = nullptr,
            *o_bf = nullptr, *y_bf = nullptr, *m_bf = nullptr, *z_bf = nullptr, *wukt = nullptr;
     int *pidx = nullptr, *row_seq = nullptr, *row_pos = nullptr, *d0 = nullptr, *tok_in = nullptr,
@@ -61,7 +61,7 @@ struct eagle3_draft {
     int batch = 0;
     bool have_extend = false;
     // native tracing: event pairs around launches, accumulated per kernel kind
-    bool prof_on = false;
+    uint32_t prof_mask = 0;   // kinds whose launches are timed
     std::vector<cudaEvent_t> prof_ev;
     std::vector<int> prof_kind;
     int prof_used = 0;
@@ -76,15 +76,21 @@ namespace {
 template <typename F>
 cudaError_t traced(eagle3_draft& d, int kind, cudaStream_t st, F&& launch) {
     d.launches[kind] += 1;
-    const bool rec = d.prof_on && d.prof_used < kProfPairs;
+    const bool rec = ((d.prof_mask >> kind) & 1u) && d.prof_used < kProfPairs;
+    // Inside stream capture an event record must be "external" to become a timestamp node of the graph.
+    unsigned int flags = cudaEventRecordDefault;
     if (rec) {
-        cudaError_t e = cudaEventRecord(d.prof_ev[2 * d.prof_used], st);
+        cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+        cudaError_t e = cudaStreamIsCapturing(st, &cs);
+        if (e != cudaSuccess) return e;
+        if (cs == cudaStreamCaptureStatusActive) flags = cudaEventRecordExternal;
+        e = cudaEventRecordWithFlags(d.prof_ev[2 * d.prof_used], st, flags);
         if (e != cudaSuccess) return e;
     }
     cudaError_t e = launch();
     if (e != cudaSuccess) return e;
     if (rec) {
-        e = cudaEventRecord(d.prof_ev[2 * d.prof_used + 1], st);
+        e = cudaEventRecordWithFlags(d.prof_ev[2 * d.prof_used + 1], st, flags);
         if (e != cudaSuccess) return e;
         d.prof_kind[d.prof_used] = kind;
         d.prof_used += 1;
@@ -196,7 +202,7 @@ struct Layout {
 
 struct Offsets {
     size_t f, carry, x, cqkv, cq_hat, q, qa, qa_bf, part_o, part_ml, o, h1, y, mlp, h2, z, pval, pidx, rope_cos,
-        rope_sin, row_seq, row_pos, d0, tok_in, err, x_bf, cqh_bf, q_bf, olat_bf, o_bf, y_bf, m_bf, z_bf, wukt,
+        rope_sin, row_seq, row_pos, d0, tok_in, err, olat, x_bf, cqh_bf, q_bf, olat_bf, o_bf, y_bf, m_bf, z_bf, wukt,
         tc_part, total;
     int m_cap, splits_cap, npart;
     size_t part_rows;
@@ -242,6 +248,7 @@ Offsets plan(const eagle3_config_t& c, int num_sms) {
     o.d0 = L.take(B * 4);
     o.tok_in = L.take(B * 4);
     o.err = L.take(4);
+    o.olat = L.take((tc && M > 8 ? 8 : M) * nh * c.kv_lora_rank * f4);
     o.x_bf = L.take(Mt * 2 * H * b2);
     o.cqh_bf = L.take(Mt * c.q_lora_rank * b2);
     o.q_bf = L.take(Mt * nh * dqk * b2);
@@ -326,6 +333,9 @@ struct Lin {
     bf16_t* ybf = nullptr; long ldybf = 0;     // bf16 output for the next tensor-core GEMM
     const float* resid = nullptr; long ldr = 0;
     float* logits = nullptr; long ldl = 0;     // ARGMAX debug output
+    // grouped rows (GEMV path only): see GemvArgs
+    int w_grp = 0; long w_grp_stride = 0; int w_row0 = 0;
+    int a_grp = 0; long a_grp_stride = 0;
 };
 
 bool use_tc(const eagle3_draft& d, int M) { return d.tc_ok && M > kGemvMaxRows; }
@@ -357,6 +367,9 @@ cudaError_t run_linear(eagle3_draft& d, const Lin& L, int kind, cudaStream_t st)
         g.y = L.y; g.ldy = L.ldy;
         g.resid = L.resid; g.ldr = L.ldr;
         g.pval = d.pval; g.pidx = d.pidx; g.logits = L.logits; g.ldl = L.ldl;
+        g.w_grp = L.w_grp; g.w_grp_stride = L.w_grp_stride; g.w_row0 = L.w_row0;
+        g.a_grp = L.a_grp; g.a_grp_stride = L.a_grp_stride;
+        g.err = d.err;
         if (L.epi == EPI_ARGMAX) d.npart = gemv_argmax_parts(L.N, d.num_sms);
         return traced(d, kind, st, [&] { return launch_gemv(g, L.epi, d.num_sms, st); });
     }
@@ -465,14 +478,19 @@ cudaError_t run_layer(eagle3_draft& d, eagle3_kv_t* kv, int M, const float* fuse
         E3_TRY(traced(d, K_ABSORB, st, [&] { return launch_absorb(aa, st); }));
     }
     E3_TRY(traced(d, K_ATTN, st, [&] { return launch_attention(aa, st); }));
+    // merge the attention splits into o_lat, then o_h = W_UV,h o_lat,h over the value rows of kv_b
+    if (tc) aa.olat_bf = d.olat_bf; else aa.olat = d.olat;
+    E3_TRY(traced(d, K_COMBINE, st, [&] { return launch_merge(aa, st); }));
     if (tc) {
-        aa.olat_bf = d.olat_bf;
-        E3_TRY(traced(d, K_COMBINE, st, [&] { return launch_combine(aa, st); }));
-        // o_h = W_UV,h o_lat,h: per-head GEMM over the value rows of kv_b
         E3_TRY(run_batched(d, K_UNABSORB, M, d.olat_bf, (long)nh * dc, dc, w.kv_b, (long)nh * (dn + dv), dn, dn + dv,
                            dv, dc, nullptr, d.o_bf, (long)nh * dv, dv, st));
     } else {
-        E3_TRY(traced(d, K_COMBINE, st, [&] { return launch_combine(aa, st); }));
+        Lin L = lin1(d, M, d.olat, nullptr, dc, w.kv_b, nh * dv);
+        L.lda[0] = (long)nh * dc;
+        L.w_grp = dv; L.w_grp_stride = dn + dv; L.w_row0 = dn;
+        L.a_grp = dv; L.a_grp_stride = dc;
+        L.y = d.o; L.ldy = (long)nh * dv;
+        E3_TRY(run_linear(d, L, K_UNABSORB, st));
     }
     // o_proj + residual
     {
@@ -573,7 +591,7 @@ eagle3_status_t eagle3_draft_create(const eagle3_config_t* config, const eagle3_
     d->o = F(o.o); d->h1 = F(o.h1); d->y = F(o.y); d->mlp = F(o.mlp); d->h2 = F(o.h2); d->z = F(o.z);
     d->pval = F(o.pval); d->pidx = I(o.pidx); d->rope_cos = F(o.rope_cos); d->rope_sin = F(o.rope_sin);
     d->row_seq = I(o.row_seq); d->row_pos = I(o.row_pos); d->d0 = I(o.d0); d->tok_in = I(o.tok_in);
-    d->err = I(o.err);
+    d->err = I(o.err); d->olat = F(o.olat);
     d->x_bf = Bf(o.x_bf); d->cqh_bf = Bf(o.cqh_bf); d->q_bf = Bf(o.q_bf); d->olat_bf = Bf(o.olat_bf);
     d->o_bf = Bf(o.o_bf); d->y_bf = Bf(o.y_bf); d->m_bf = Bf(o.m_bf); d->z_bf = Bf(o.z_bf); d->wukt = Bf(o.wukt);
     d->tc_part = F(o.tc_part);
@@ -680,6 +698,21 @@ eagle3_status_t eagle3_draft_decode(eagle3_draft_t* d, int32_t gamma, const int3
     return EAGLE3_OK;
 }
 
+eagle3_status_t eagle3_linear(eagle3_draft_t* d, const void* x, const void* w, float* y, int32_t M, int32_t N,
+                              int32_t K, void* stream) {
+    if (!d || !x || !w || !y || M < 1 || N < 1 || K < 8 || K % 8) return EAGLE3_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(w) || !aligned16(y)) return EAGLE3_ERR_INVALID_ARG;
+    if (d->cfg.dtype != EAGLE3_BF16) return EAGLE3_ERR_UNSUPPORTED;
+    if (use_tc(*d, M) && K % 64) return EAGLE3_ERR_UNSUPPORTED;
+    Lin L;
+    L.M = M; L.N = N; L.K = K; L.na = 1;
+    L.a32[0] = x; L.a32_is_bf16 = true; L.a16[0] = (const bf16_t*)x; L.lda[0] = K; L.ka[0] = K;
+    L.w0 = w; L.n0rows = N;
+    L.y = y; L.ldy = N;
+    E3_CUDA(run_linear(*d, L, K_FC, (cudaStream_t)stream));
+    return EAGLE3_OK;
+}
+
 eagle3_status_t eagle3_accept(const int32_t* draft, const int32_t* target, int32_t batch, int32_t gamma,
                               int32_t* accepted_len, int32_t* hist, void* stream) {
     if (!draft || !target || !accepted_len) return EAGLE3_ERR_INVALID_ARG;
@@ -701,15 +734,15 @@ eagle3_status_t eagle3_draft_clear_error(eagle3_draft_t* d, void* stream) {
     return EAGLE3_OK;
 }
 
-eagle3_status_t eagle3_draft_profile_enable(eagle3_draft_t* d, int32_t enable) {
+eagle3_status_t eagle3_draft_profile_enable(eagle3_draft_t* d, int32_t kind_mask) {
     if (!d) return EAGLE3_ERR_INVALID_ARG;
-    if (enable && d->prof_ev.empty()) {
+    if (kind_mask && d->prof_ev.empty()) {
         d->prof_ev.resize(2 * kProfPairs);
         d->prof_kind.resize(kProfPairs);
         for (auto& ev : d->prof_ev) E3_CUDA(cudaEventCreate(&ev));
     }
-    if (!enable) E3_CUDA(prof_flush(*d));
-    d->prof_on = enable != 0;
+    if (!kind_mask) E3_CUDA(prof_flush(*d));
+    d->prof_mask = (uint32_t)kind_mask;
     return EAGLE3_OK;
 }
 

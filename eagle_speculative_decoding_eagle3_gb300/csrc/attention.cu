@@ -6,8 +6,8 @@
 //   score_t = sigma (q_nope,h . W_UK,h c_t + q_pe,h . k_t) = sigma (q_lat,h . c_t + q_pe,h . k_t),
 //   o_h = sum_t p_t W_UV,h c_t = W_UV,h (sum_t p_t c_t),      q_lat,h = W_UK,h^T q_nope,h.
 // So no kernel expands per-head keys or values: absorb forms q_lat; attention runs split-K over the
-// ragged context with an online softmax and writes per-split partials; combine merges the splits
-// and applies W_UV,h.
+// ragged context with an online softmax and writes per-split partials; merge combines the splits into
+// o_lat and a grouped GEMM applies W_UV,h.
 //
 // Two attention kernels share the partial format:
 //  * attention_mma_kernel (bf16 cache, d_c 512 / d_r 64): 16 heads x 32-token tiles on the tensor
@@ -27,17 +27,19 @@ constexpr int kTile = 32;
 constexpr int kAttnWarps = 8;
 constexpr int kHeadsPerWarp = 2;
 constexpr int kHeadsPerCta = kAttnWarps * kHeadsPerWarp;
-constexpr int kCombRows = 4;
 
 // qa[r, h] = [ W_UK,h^T q_nope[r, h] | RoPE(q_pe[r, h], pos_r) ]  (fp32, plus a bf16 copy when asked)
-// Thread (cc, rg) owns latent columns [8cc, 8cc+8) and W_UK rows rg, rg + RG, ...; row groups are
-// reduced through shared memory.
+// Grid (head, column block of kAbsCols latent columns, row block).  Thread (cc, rg) owns 8 columns and
+// the W_UK rows rg, rg + RG, ...: all of its (dn / RG) 16-byte weight loads are issued together, then
+// the RG row groups are reduced through shared memory.  The rope part is written by column block 0.
+constexpr int kAbsCols = 128;
 template <typename T>
 __global__ void __launch_bounds__(256) absorb_kernel(const AttnArgs a) {
-    extern __shared__ float sm[];           // [kAbsRows][dn] q_nope, then [RG][kAbsRows][dc] partials
-    const int h = blockIdx.x, r0 = blockIdx.y * kAbsRows;
+    extern __shared__ float sm[];           // [kAbsRows][dn] q_nope, then [RG][kAbsRows][cols] partials
+    const int h = blockIdx.x, cb = blockIdx.y, r0 = blockIdx.z * kAbsRows;
     const int nr = min(kAbsRows, a.M - r0);
     const int dqk = a.dn + a.dr, D = a.dc + a.dr;
+    const int cols = min(kAbsCols, a.dc), c0 = cb * cols;
     float* qn = sm;
     float* part = sm + kAbsRows * a.dn;
     for (int t = threadIdx.x; t < kAbsRows * a.dn; t += blockDim.x) {
@@ -45,51 +47,63 @@ __global__ void __launch_bounds__(256) absorb_kernel(const AttnArgs a) {
         qn[t] = (i < nr) ? a.q[((long)(r0 + i) * a.nh + h) * dqk + k] : 0.f;
     }
     const int half = a.dr / 2;
-    for (int t = threadIdx.x; t < nr * half; t += blockDim.x) {
-        const int i = t / half, p = t % half;
-        const int pos = a.row_pos[r0 + i];
-        const float c = a.rope_cos[(long)pos * half + p], s = a.rope_sin[(long)pos * half + p];
-        const float* qp = a.q + ((long)(r0 + i) * a.nh + h) * dqk + a.dn;
-        const float x0 = qp[2 * p], x1 = qp[2 * p + 1];
-        const float y0 = x0 * c - x1 * s, y1 = x0 * s + x1 * c;
-        const long o = ((long)(r0 + i) * a.nh + h) * D + a.dc + 2 * p;
-        a.qa[o] = y0;
-        a.qa[o + 1] = y1;
-        if (a.qa_bf) { a.qa_bf[o] = __float2bfloat16_rn(y0); a.qa_bf[o + 1] = __float2bfloat16_rn(y1); }
+    if (cb == 0) {
+        for (int t = threadIdx.x; t < nr * half; t += blockDim.x) {
+            const int i = t / half, p = t % half;
+            const int pos = a.row_pos[r0 + i];
+            const float c = a.rope_cos[(long)pos * half + p], s = a.rope_sin[(long)pos * half + p];
+            const float* qp = a.q + ((long)(r0 + i) * a.nh + h) * dqk + a.dn;
+            const float x0 = qp[2 * p], x1 = qp[2 * p + 1];
+            const float y0 = x0 * c - x1 * s, y1 = x0 * s + x1 * c;
+            const long o = ((long)(r0 + i) * a.nh + h) * D + a.dc + 2 * p;
+            a.qa[o] = y0;
+            a.qa[o + 1] = y1;
+            if (a.qa_bf) { a.qa_bf[o] = __float2bfloat16_rn(y0); a.qa_bf[o + 1] = __float2bfloat16_rn(y1); }
+        }
     }
     __syncthreads();
-    const int nchunk = a.dc / 8;
+    const int nchunk = cols / 8;
     const int RG = blockDim.x / nchunk;
     const int cc = threadIdx.x % nchunk, rg = threadIdx.x / nchunk;
-    const T* W = reinterpret_cast<const T*>(a.kv_b) + (long)h * (a.dn + a.dv) * a.dc;
+    const T* W = reinterpret_cast<const T*>(a.kv_b) + (long)h * (a.dn + a.dv) * a.dc + c0 + 8 * cc;
+    constexpr int kMaxLoads = 8;
     float acc[kAbsRows][8];
 #pragma unroll
     for (int i = 0; i < kAbsRows; ++i)
 #pragma unroll
         for (int e = 0; e < 8; ++e) acc[i][e] = 0.f;
-    if (rg < RG) {
-#pragma unroll 4
-        for (int k = rg; k < a.dn; k += RG) {
-            float w[8];
-            widen(ld8<true>(W + (long)k * a.dc + 8 * cc), w);
+    for (int k0 = rg; k0 < a.dn; k0 += RG * kMaxLoads) {
+        Raw8<T> wr[kMaxLoads];
 #pragma unroll
-            for (int i = 0; i < kAbsRows; ++i) {
-                const float q = qn[i * a.dn + k];
-#pragma unroll
-                for (int e = 0; e < 8; ++e) acc[i][e] = fmaf(q, w[e], acc[i][e]);
-            }
+        for (int j = 0; j < kMaxLoads; ++j) {
+            const int k = k0 + j * RG;
+            wr[j] = k < a.dn ? ld8<true>(W + (long)k * a.dc) : zero8((T*)nullptr);
         }
 #pragma unroll
-        for (int i = 0; i < kAbsRows; ++i)
+        for (int j = 0; j < kMaxLoads; ++j) {
+            const int k = k0 + j * RG;
+            if (k < a.dn) {
+                float w[8];
+                widen(wr[j], w);
 #pragma unroll
-            for (int e = 0; e < 8; ++e) part[((long)rg * kAbsRows + i) * a.dc + 8 * cc + e] = acc[i][e];
+                for (int i = 0; i < kAbsRows; ++i) {
+                    const float q = qn[i * a.dn + k];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) acc[i][e] = fmaf(q, w[e], acc[i][e]);
+                }
+            }
+        }
     }
+#pragma unroll
+    for (int i = 0; i < kAbsRows; ++i)
+#pragma unroll
+        for (int e = 0; e < 8; ++e) part[((long)rg * kAbsRows + i) * cols + 8 * cc + e] = acc[i][e];
     __syncthreads();
-    for (int t = threadIdx.x; t < nr * a.dc; t += blockDim.x) {
-        const int i = t / a.dc, c = t % a.dc;
+    for (int t = threadIdx.x; t < nr * cols; t += blockDim.x) {
+        const int i = t / cols, c = t % cols;
         float v = 0.f;
-        for (int g = 0; g < RG; ++g) v += part[((long)g * kAbsRows + i) * a.dc + c];
-        const long o = ((long)(r0 + i) * a.nh + h) * D + c;
+        for (int g = 0; g < RG; ++g) v += part[((long)g * kAbsRows + i) * cols + c];
+        const long o = ((long)(r0 + i) * a.nh + h) * D + c0 + c;
         a.qa[o] = v;
         if (a.qa_bf) a.qa_bf[o] = __float2bfloat16_rn(v);
     }
@@ -410,69 +424,54 @@ __global__ void __launch_bounds__(mla_mma::WARPS * 32) attention_mma_kernel(cons
     }
 }
 
-// o[r, h*dv + j] = W_UV,h[j] . (sum_s e^{m_s - M} o_s / sum_s e^{m_s - M} l_s)
-template <typename T, int DC>
-__global__ void __launch_bounds__(256) combine_kernel(const AttnArgs a) {
-    __shared__ float ol[kCombRows][DC];
-    __shared__ float wsp[kCombRows][64];
-    const int h = blockIdx.x, r0 = blockIdx.y * kCombRows;
-    const int nr = min(kCombRows, a.M - r0);
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+// Split-K merge: o_lat[r, h] = sum_s e^{m_s - M} o_s / sum_s e^{m_s - M} l_s (fp32 and/or bf16).
+// One CTA per (row, head); thread t owns latent columns [4t, 4t + 4).
+__global__ void __launch_bounds__(128) merge_kernel(const AttnArgs a) {
+    __shared__ float wsp[64];
+    const int h = blockIdx.x, r = blockIdx.y;
     const int S = a.splits;
-    if (threadIdx.x < 32 * kCombRows) {   // one warp per row: split weights e^{m_s - M} / den
-        const int i = warp;
-        if (i < nr) {
-            const long base = ((long)(r0 + i) * a.nh + h) * S;
-            float mx = -FLT_MAX;
-            for (int s = lane; s < S; s += 32) mx = fmaxf(mx, a.part_ml[(base + s) * 2]);
-            mx = warp_max(mx);
-            float den = 0.f;
-            for (int s = lane; s < S; s += 32) {
-                const float l = a.part_ml[(base + s) * 2 + 1];
-                const float e = l > 0.f ? __expf(a.part_ml[(base + s) * 2] - mx) : 0.f;
-                wsp[i][s] = e;
-                den += e * l;
-            }
-            den = warp_sum(den);
-            const float inv = den > 0.f ? 1.f / den : 0.f;
-            __syncwarp();
-            for (int s = lane; s < S; s += 32) wsp[i][s] *= inv;
+    const long base = ((long)r * a.nh + h) * S;
+    if (threadIdx.x < 32) {
+        const int lane = threadIdx.x;
+        float mx = -FLT_MAX;
+        for (int s = lane; s < S; s += 32) mx = fmaxf(mx, a.part_ml[(base + s) * 2]);
+        mx = warp_max(mx);
+        float den = 0.f;
+        for (int s = lane; s < S; s += 32) {
+            const float l = a.part_ml[(base + s) * 2 + 1];
+            const float e = l > 0.f ? __expf(a.part_ml[(base + s) * 2] - mx) : 0.f;
+            wsp[s] = e;
+            den += e * l;
         }
+        den = warp_sum(den);
+        const float inv = den > 0.f ? 1.f / den : 0.f;
+        __syncwarp();
+        for (int s = lane; s < S; s += 32) wsp[s] *= inv;
     }
     __syncthreads();
-    for (int t = threadIdx.x; t < nr * DC; t += blockDim.x) {
-        const int i = t / DC, c = t % DC;
-        const long base = ((long)(r0 + i) * a.nh + h) * S;
-        float v = 0.f;
+    for (int c = 4 * threadIdx.x; c < a.dc; c += 4 * blockDim.x) {
+        float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
         for (int s = 0; s < S; ++s) {
-            const float w = wsp[i][s];
-            if (w != 0.f) v = fmaf(w, a.part_o[(base + s) * DC + c], v);
+            const float w = wsp[s];
+            if (w == 0.f) continue;
+            const float4 o = *reinterpret_cast<const float4*>(a.part_o + (base + s) * a.dc + c);
+            v.x = fmaf(w, o.x, v.x); v.y = fmaf(w, o.y, v.y); v.z = fmaf(w, o.z, v.z); v.w = fmaf(w, o.w, v.w);
         }
-        ol[i][c] = v;
-        if (a.olat_bf) a.olat_bf[((long)(r0 + i) * a.nh + h) * DC + c] = __float2bfloat16_rn(v);
-    }
-    if (a.olat_bf) return;   // the value up-projection runs as a batched tensor-core GEMM instead
-    __syncthreads();
-    const T* W = reinterpret_cast<const T*>(a.kv_b) + ((long)h * (a.dn + a.dv) + a.dn) * DC;
-    constexpr int NCH = DC / 8;
-    for (int j = warp; j < a.dv; j += blockDim.x >> 5) {
-        const T* wr = W + (long)j * DC;
-        float acc[kCombRows];
-#pragma unroll
-        for (int i = 0; i < kCombRows; ++i) acc[i] = 0.f;
-        for (int c8 = lane; c8 < NCH; c8 += 32) {
-            float w[8];
-            widen(ld8<true>(wr + 8 * c8), w);
-#pragma unroll
-            for (int i = 0; i < kCombRows; ++i)
-#pragma unroll
-                for (int e = 0; e < 8; ++e) acc[i] = fmaf(w[e], ol[i][8 * c8 + e], acc[i]);
-        }
-        for (int i = 0; i < nr; ++i) {
-            const float v = warp_sum(acc[i]);
-            if (lane == 0) a.o[(long)(r0 + i) * a.nh * a.dv + h * a.dv + j] = v;
+        const long o = ((long)r * a.nh + h) * a.dc + c;
+        if (a.olat) *reinterpret_cast<float4*>(a.olat + o) = v;
+        if (a.olat_bf) {
+            uint2 u;
+            u.x = pack2_bf16(v.x, v.y);
+            u.y = pack2_bf16(v.z, v.w);
+            *reinterpret_cast<uint2*>(a.olat_bf + o) = u;
         }
     }
+}
+
+cudaError_t launch_merge(const AttnArgs& a, cudaStream_t st) {
+    if (a.splits > 64 || a.dc % 4) return cudaErrorInvalidValue;
+    merge_kernel<<<dim3(a.nh, a.M), 128, 0, st>>>(a);
+    return cudaGetLastError();
 }
 
 // Rotated rope part of the query: qa[r, h, dc:] = RoPE(q_pe[r, h], pos_r) (fp32 and bf16).
@@ -531,9 +530,11 @@ int attention_heads_per_cta(int dt, int dc, int dr) {
 }
 
 cudaError_t launch_absorb(const AttnArgs& a, cudaStream_t st) {
-    dim3 grid(a.nh, (a.M + kAbsRows - 1) / kAbsRows);
-    const int RG = 256 / (a.dc / 8);
-    const size_t sm = ((size_t)kAbsRows * a.dn + (size_t)RG * kAbsRows * a.dc) * sizeof(float);
+    const int cols = a.dc < kAbsCols ? a.dc : kAbsCols;
+    if (a.dc % cols) return cudaErrorInvalidValue;
+    dim3 grid(a.nh, a.dc / cols, (a.M + kAbsRows - 1) / kAbsRows);
+    const int RG = 256 / (cols / 8);
+    const size_t sm = ((size_t)kAbsRows * a.dn + (size_t)RG * kAbsRows * cols) * sizeof(float);
     static bool attr[2] = {false, false};
     const int ti = a.dt == BF16 ? 1 : 0;
     if (!attr[ti]) {
@@ -588,19 +589,5 @@ cudaError_t launch_attention(const AttnArgs& a, cudaStream_t st) {
     return cudaErrorInvalidValue;
 }
 
-cudaError_t launch_combine(const AttnArgs& a, cudaStream_t st) {
-    if (a.splits > 64) return cudaErrorInvalidValue;
-    dim3 grid(a.nh, (a.M + kCombRows - 1) / kCombRows);
-    if (a.dc == 512) {
-        if (a.dt == BF16) combine_kernel<bf16, 512><<<grid, 256, 0, st>>>(a);
-        else combine_kernel<float, 512><<<grid, 256, 0, st>>>(a);
-    } else if (a.dc == 32) {
-        if (a.dt == BF16) combine_kernel<bf16, 32><<<grid, 256, 0, st>>>(a);
-        else combine_kernel<float, 32><<<grid, 256, 0, st>>>(a);
-    } else {
-        return cudaErrorInvalidValue;
-    }
-    return cudaGetLastError();
-}
 
 }  // namespace e3

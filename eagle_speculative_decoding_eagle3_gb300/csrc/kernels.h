@@ -31,6 +31,12 @@ struct GemvArgs {
     float* pval; int* pidx;           // ARGMAX partials [M, npart]
     int npart;                        // ARGMAX: grid.x used (set by the launcher)
     float* logits; long ldl;          // ARGMAX: optional full logits
+    // grouped rows (per-head GEMVs over one weight tensor), off when 0:
+    //   output row n reads weight row (n / w_grp) * w_grp_stride + w_row0 + n % w_grp of w[0]
+    //   and the activation slice starting at element (n / a_grp) * a_grp_stride of a[0]
+    int w_grp; long w_grp_stride; int w_row0;
+    int a_grp; long a_grp_stride;
+    int* err;                         // device error word (bounded waits that ran out)
 };
 cudaError_t launch_gemv(GemvArgs& g, int epi, int num_sms, cudaStream_t st);
 int gemv_argmax_parts(int N, int num_sms);   // partial count of an ARGMAX launch over N columns
@@ -95,11 +101,13 @@ struct AttnArgs {
     float* part_o;       // [M, nh, splits, dc]
     float* part_ml;      // [M, nh, splits, 2]
     float* o;            // [M, nh*dv]
-    __nv_bfloat16* olat_bf;  // combine: when set, write o_lat [M, nh, dc] in bf16 and skip the W_UV product
+    __nv_bfloat16* olat_bf;  // merged latent output o_lat [M, nh, dc] in bf16 (optional)
+    float* olat;             // merged latent output o_lat [M, nh, dc] in fp32 (optional)
 };
 cudaError_t launch_absorb(const AttnArgs& a, cudaStream_t st);
 cudaError_t launch_attention(const AttnArgs& a, cudaStream_t st);
-cudaError_t launch_combine(const AttnArgs& a, cudaStream_t st);
+// split-K merge into o_lat (olat and/or olat_bf); the value up-projection then runs as a GEMM
+cudaError_t launch_merge(const AttnArgs& a, cudaStream_t st);
 // rotated rope query into qa / qa_bf[:, :, dc:] (the tensor-core path forms q_lat separately)
 cudaError_t launch_rope_q(const AttnArgs& a, cudaStream_t st);
 // W_UK,h^T for every head: out[h, c, i] = kv_b[h*(dn+dv) + i, c]  (bf16)

@@ -200,7 +200,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
         if (!ok && nkb > 0) *abort_flag = 1;
         tc_fence_after();
         const uint32_t trow = tmem + ((uint32_t)(32 * q) << 16);
-        const bool split = gridDim.z > 1;
+        const bool splitk = p.splits > 1;   // write fp32 partials for the reduction kernel
         for (int c = 0; c < BN; c += 16) {
             float v[16], u[16];
             if (ok) {
@@ -237,7 +237,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
             for (int j = 0; j < 16; ++j) {
                 const int m = m0 + c + j;
                 if (!nvalid || m >= p.M) continue;
-                if (split) {
+                if (splitk) {
                     const long plane = (long)p.M * p.N;
                     float* part = p.part + (long)split * C::NP * plane;
                     part[(long)m * p.N + n] = v[j];

@@ -67,6 +67,7 @@ def _lib():
                                             P, P, P]
         lib.eagle3_draft_decode.argtypes = [P, C.c_int32, P, C.POINTER(eagle3_kv_t), P, P, P, P]
         lib.eagle3_accept.argtypes = [P, P, C.c_int32, C.c_int32, P, P, P]
+        lib.eagle3_linear.argtypes = [P, P, P, P, C.c_int32, C.c_int32, C.c_int32, P]
         lib.eagle3_draft_get_error.argtypes = [P, C.POINTER(C.c_int32)]
         lib.eagle3_draft_clear_error.argtypes = [P, P]
         lib.eagle3_draft_destroy.argtypes = [P]
@@ -76,7 +77,7 @@ def _lib():
         lib.eagle3_draft_profile_reset.argtypes = [P]
         for f in ("eagle3_draft_profile_enable", "eagle3_draft_profile_read", "eagle3_draft_profile_reset",
                   "eagle3_draft_create", "eagle3_draft_workspace_bytes", "eagle3_draft_extend", "eagle3_draft_decode",
-                  "eagle3_accept", "eagle3_draft_get_error", "eagle3_draft_clear_error", "eagle3_draft_destroy"):
+                  "eagle3_accept", "eagle3_linear", "eagle3_draft_get_error", "eagle3_draft_clear_error", "eagle3_draft_destroy"):
             getattr(lib, f).restype = C.c_int
         _L = lib
     return _L
@@ -159,6 +160,11 @@ def eagle3_draft_decode(handle, gamma, d2t, cache: eagle3_kv_t, draft_tokens, hi
         _stream(stream)))
 
 
+def eagle3_linear(handle, x, w, y, M, N, K, stream=None):
+    _check("eagle3_linear", _lib().eagle3_linear(handle, _ptr(x), _ptr(w), _ptr(y), int(M), int(N), int(K),
+                                                 _stream(stream)))
+
+
 def eagle3_accept(draft, target, batch, gamma, accepted_len, hist=None, stream=None):
     _check("eagle3_accept", _lib().eagle3_accept(_ptr(draft), _ptr(target), int(batch), int(gamma),
                                                  _ptr(accepted_len), _ptr(hist), _stream(stream)))
@@ -179,8 +185,9 @@ def eagle3_draft_clear_error(handle, stream=None):
 PROF_KINDS = 24
 
 
-def eagle3_draft_profile_enable(handle, enable=True):
-    _check("eagle3_draft_profile_enable", _lib().eagle3_draft_profile_enable(handle, int(bool(enable))))
+def eagle3_draft_profile_enable(handle, kind_mask=-1):
+    """Time the launches of the kinds in `kind_mask` (bit k = kind k; -1 all, 0 off)."""
+    _check("eagle3_draft_profile_enable", _lib().eagle3_draft_profile_enable(handle, int(kind_mask)))
 
 
 def eagle3_draft_profile_read(handle, kind):

@@ -58,8 +58,8 @@ class DeviceHead:
 
     def close(self):
         if self.handle:
-            E.eagle3_draft_destroy(self.handle)
-            self.handle = None
+            h, self.handle = self.handle, None   # the library frees the handle even when it reports an error
+            E.eagle3_draft_destroy(h)
 
     def __del__(self):
         try:

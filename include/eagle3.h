@@ -178,6 +178,15 @@ EAGLE3_API eagle3_status_t eagle3_draft_decode(eagle3_draft_t *d, int32_t gamma,
                                     eagle3_kv_t *cache, int32_t *draft_tokens, float *hidden_out,
                                     float *logits_out, void *stream);
 
+/* One bias-free linear layer of the head's engine, exposed for callers and tests:
+ * y[m, n] = sum_k x[m, k] w[n, k] with x [M, K] and w [N, K] bf16 (row-major), y [M, N] fp32.
+ * It runs on the engine the head itself uses for M rows: the weight-streaming GEMV for M <= 8, the
+ * tcgen05 tensor-core GEMM above (K must then be a multiple of 64).  Uses the handle's workspace
+ * (so calls on one handle must not overlap) and reports timeouts in its error word.
+ * Returns EAGLE3_ERR_UNSUPPORTED for an fp32 head. */
+EAGLE3_API eagle3_status_t eagle3_linear(eagle3_draft_t *d, const void *x, const void *w, float *y, int32_t M,
+                                         int32_t N, int32_t K, void *stream);
+
 /* Greedy acceptance ("Eagle3 DeepseekV3 in MAX" §10): accepted_len[b] = number of leading
  * positions i with draft[b, i] == target[b, i] (0..gamma).  hist (optional, [gamma + 1]) is
  * overwritten with hist[k] = number of sequences with accepted_len == k.  No handle needed. */
@@ -194,11 +203,13 @@ EAGLE3_API eagle3_status_t eagle3_draft_clear_error(eagle3_draft_t *d, void *str
 /* Free the workspace and the handle (synchronises the device).  NULL is accepted. */
 EAGLE3_API eagle3_status_t eagle3_draft_destroy(eagle3_draft_t *d);
 
-/* ---- Per-kernel timing (native tracing).  When enabled, every kernel launch of the handle is
- * bracketed by CUDA events recorded on the launch stream; read() synchronises and accumulates the
- * event intervals per kernel kind.  Launches are counted whether or not timing is enabled. */
+/* ---- Per-kernel timing (native tracing).  Every launch of a kernel kind whose bit is set in
+ * `kind_mask` (bit k = kind k; -1 = all kinds, 0 = off) is bracketed by CUDA events recorded on the
+ * launch stream (as graph timestamp nodes when the stream is being captured); read() synchronises and
+ * accumulates the event intervals per kind.  Launches are counted whether or not they are timed.
+ * Turning timing off flushes the pending intervals. */
 #define EAGLE3_PROF_KINDS 24
-EAGLE3_API eagle3_status_t eagle3_draft_profile_enable(eagle3_draft_t *d, int32_t enable);
+EAGLE3_API eagle3_status_t eagle3_draft_profile_enable(eagle3_draft_t *d, int32_t kind_mask);
 /* For kernel kind `kind` (0 <= kind < EAGLE3_PROF_KINDS) since the last reset: total milliseconds over
  * the timed launches, the number of timed launches, and the number of launches (timed or not; the
  * event pool times at most 32768 launches between reads).  Synchronises the device.  Launches recorded

@@ -1,0 +1,40 @@
+"""GPU-vs-oracle parity of the head's linear-layer engine (weight-streaming GEMV for few rows, tcgen05
+GEMM above eight rows) through the C ABI entry point eagle3_linear."""
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+import workloads as WL
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def head():
+    from eagle_speculative_decoding_eagle3_gb300 import build
+    from eagle_speculative_decoding_eagle3_gb300 import harness as HN
+    build.build()
+    w = WL.workload("dsv3_b1", hidden=1024, n_heads=8, q_lora_rank=256, intermediate=2048, target_vocab=8192,
+                    draft_vocab=4096, batch=4, ctx=(64, 64), seed=90)
+    h = HN.DeviceHead(w, WL.make_weights(w))
+    yield h
+    h.close()
+
+
+@pytest.mark.parametrize("M", [1, 3, 8, 9, 24, 64, 200, 256, 300])
+@pytest.mark.parametrize("N,K", [(448, 1088), (2112, 1024)])
+def test_linear_matches_oracle(head, M, N, K):
+    from eagle_speculative_decoding_eagle3_gb300 import eagle3 as E
+    from eagle_speculative_decoding_eagle3_gb300 import harness as HN
+    x = WL.f32_to_bf16_bits(WL.normal((M, K), 1.0, 5, f"lin.x.{M}.{K}"))
+    w = WL.f32_to_bf16_bits(WL.normal((N, K), 0.02, 5, f"lin.w.{N}.{K}"))
+    xd, wd = HN.to_device(x), HN.to_device(w)
+    y = torch.full((M, N), float("nan"), dtype=torch.float32, device="cuda")
+    E.eagle3_linear(head.handle, xd, wd, y, M, N, K)
+    torch.cuda.synchronize()
+    assert head.error_word() == 0
+    ref = O.linear(WL.bf16_to_f32(x), WL.bf16_to_f32(w))
+    got = y.cpu().numpy().astype(np.float64)
+    err = np.abs(got - ref).max() / np.abs(ref).max()
+    assert err < 1e-5, err

@@ -52,3 +52,19 @@ def test_dsv3_b1_full_size_round():
     w = WL.workload("dsv3_b1")
     gpu, orc, seqs, paged = run_round(w)
     print(check_round(w, gpu, orc, seqs, paged, TOL_BF16))
+
+
+def test_mla_shaped_bf16_tensor_core_rounds():
+    # 24 sequences: the extend (48 rows) and every decode step (24 rows) take the tcgen05 path
+    w = WL.workload("dsv3_b1", hidden=1024, n_heads=8, q_lora_rank=256, intermediate=2048,
+                    target_vocab=8192, draft_vocab=4096, batch=24, ctx=(30, 700), t_new=2, gamma=3,
+                    accept_p=(0.7,) * 3, seed=80)
+    gpu, orc, seqs, paged = run_round(w)
+    print(check_round(w, gpu, orc, seqs, paged, TOL_BF16))
+
+
+def test_dsv3_extend_rows_tensor_core():
+    # full DeepseekV3 head dimensions, 2 sequences x 256 new rows on an empty cache (causal extend)
+    w = WL.workload("dsv3_extend", batch=2, t_new=256, gamma=2, accept_p=(0.7, 0.7))
+    gpu, orc, seqs, paged = run_round(w, absorbed=True)
+    print(check_round(w, gpu, orc, seqs, paged, TOL_BF16))
