@@ -35,6 +35,8 @@ constexpr int kHeadsPerCta = kAttnWarps * kHeadsPerWarp;
 constexpr int kAbsCols = 128;
 template <typename T>
 __global__ void __launch_bounds__(256) absorb_kernel(const AttnArgs a) {
+    pdl_trigger();
+    pdl_wait();
     extern __shared__ float sm[];           // [kAbsRows][dn] q_nope, then [RG][kAbsRows][cols] partials
     const int h = blockIdx.x, cb = blockIdx.y, r0 = blockIdx.z * kAbsRows;
     const int nr = min(kAbsRows, a.M - r0);
@@ -116,6 +118,8 @@ __global__ void __launch_bounds__(256) absorb_kernel(const AttnArgs a) {
 // the staged tile, then the warp updates its running max / sum / output (lane holds DC/32 outputs).
 template <typename T, int DC, int DR>
 __global__ void __launch_bounds__(kAttnWarps * 32) attention_kernel(const AttnArgs a) {
+    pdl_trigger();
+    pdl_wait();
     constexpr int D = DC + DR;
     constexpr int EPW = 4 / sizeof(T);          // elements per 32-bit word
     constexpr int WORDS = D / EPW;
@@ -269,6 +273,8 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
 }
 
 __global__ void __launch_bounds__(mla_mma::WARPS * 32) attention_mma_kernel(const AttnArgs a) {
+    pdl_trigger();
+    pdl_wait();
     using namespace mla_mma;
     extern __shared__ __align__(16) unsigned char smraw[];
     bf16* qs = reinterpret_cast<bf16*>(smraw);                  // [HEADS][ROW]
@@ -427,6 +433,8 @@ __global__ void __launch_bounds__(mla_mma::WARPS * 32) attention_mma_kernel(cons
 // Split-K merge: o_lat[r, h] = sum_s e^{m_s - M} o_s / sum_s e^{m_s - M} l_s (fp32 and/or bf16).
 // One CTA per (row, head); thread t owns latent columns [4t, 4t + 4).
 __global__ void __launch_bounds__(128) merge_kernel(const AttnArgs a) {
+    pdl_trigger();
+    pdl_wait();
     __shared__ float wsp[64];
     const int h = blockIdx.x, r = blockIdx.y;
     const int S = a.splits;
@@ -451,11 +459,19 @@ __global__ void __launch_bounds__(128) merge_kernel(const AttnArgs a) {
     __syncthreads();
     for (int c = 4 * threadIdx.x; c < a.dc; c += 4 * blockDim.x) {
         float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-        for (int s = 0; s < S; ++s) {
-            const float w = wsp[s];
-            if (w == 0.f) continue;
-            const float4 o = *reinterpret_cast<const float4*>(a.part_o + (base + s) * a.dc + c);
-            v.x = fmaf(w, o.x, v.x); v.y = fmaf(w, o.y, v.y); v.z = fmaf(w, o.z, v.z); v.w = fmaf(w, o.w, v.w);
+        // splits in batches of 8 so their L2 reads are in flight together
+        for (int s0 = 0; s0 < S; s0 += 8) {
+            float4 o[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+                o[j] = (s0 + j < S) ? *reinterpret_cast<const float4*>(a.part_o + (base + s0 + j) * a.dc + c)
+                                    : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const float w = (s0 + j < S) ? wsp[s0 + j] : 0.f;
+                v.x = fmaf(w, o[j].x, v.x); v.y = fmaf(w, o[j].y, v.y);
+                v.z = fmaf(w, o[j].z, v.z); v.w = fmaf(w, o[j].w, v.w);
+            }
         }
         const long o = ((long)r * a.nh + h) * a.dc + c;
         if (a.olat) *reinterpret_cast<float4*>(a.olat + o) = v;
@@ -470,12 +486,14 @@ __global__ void __launch_bounds__(128) merge_kernel(const AttnArgs a) {
 
 cudaError_t launch_merge(const AttnArgs& a, cudaStream_t st) {
     if (a.splits > 64 || a.dc % 4) return cudaErrorInvalidValue;
-    merge_kernel<<<dim3(a.nh, a.M), 128, 0, st>>>(a);
+    return launch_pdl(merge_kernel, dim3(a.nh, a.M), dim3(128), 0, st, a);
     return cudaGetLastError();
 }
 
 // Rotated rope part of the query: qa[r, h, dc:] = RoPE(q_pe[r, h], pos_r) (fp32 and bf16).
 __global__ void rope_q_kernel(const AttnArgs a) {
+    pdl_trigger();
+    pdl_wait();
     const int r = blockIdx.x;
     const int half = a.dr / 2, dqk = a.dn + a.dr, D = a.dc + a.dr;
     const int pos = a.row_pos[r];
@@ -510,7 +528,7 @@ __global__ void transpose_wuk_kernel(const bf16* kv_b, int nh, int dn, int dv, i
 }
 
 cudaError_t launch_rope_q(const AttnArgs& a, cudaStream_t st) {
-    rope_q_kernel<<<a.M, 256, 0, st>>>(a);
+    launch_pdl(rope_q_kernel, dim3(a.M), dim3(256), 0, st, a);
     return cudaGetLastError();
 }
 
@@ -545,8 +563,8 @@ cudaError_t launch_absorb(const AttnArgs& a, cudaStream_t st) {
         attr[ti] = true;
     }
     if (sm > 96 * 1024) return cudaErrorInvalidValue;
-    if (a.dt == BF16) absorb_kernel<bf16><<<grid, 256, sm, st>>>(a);
-    else absorb_kernel<float><<<grid, 256, sm, st>>>(a);
+    if (a.dt == BF16) launch_pdl(absorb_kernel<bf16>, dim3(grid), dim3(256), sm, st, a);
+    else launch_pdl(absorb_kernel<float>, dim3(grid), dim3(256), sm, st, a);
     return cudaGetLastError();
 }
 
@@ -563,7 +581,7 @@ static cudaError_t attn_launch(const AttnArgs& a, cudaStream_t st) {
         attr_set = true;
     }
     dim3 grid(a.splits, (a.nh + kHeadsPerCta - 1) / kHeadsPerCta, a.M);
-    attention_kernel<T, DC, DR><<<grid, kAttnWarps * 32, sm, st>>>(a);
+    launch_pdl(attention_kernel<T, DC, DR>, dim3(grid), dim3(kAttnWarps * 32), sm, st, a);
     return cudaGetLastError();
 }
 
@@ -579,7 +597,7 @@ cudaError_t launch_attention(const AttnArgs& a, cudaStream_t st) {
             }
             if (!a.qa_bf) return cudaErrorInvalidValue;
             dim3 grid(a.splits, (a.nh + mla_mma::HEADS - 1) / mla_mma::HEADS, a.M);
-            attention_mma_kernel<<<grid, mla_mma::WARPS * 32, mla_mma::SMEM, st>>>(a);
+            launch_pdl(attention_mma_kernel, dim3(grid), dim3(mla_mma::WARPS * 32), mla_mma::SMEM, st, a);
             return cudaGetLastError();
         }
         return attn_launch<float, 512, 64>(a, st);

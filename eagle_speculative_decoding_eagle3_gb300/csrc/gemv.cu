@@ -53,6 +53,9 @@ __global__ void __launch_bounds__(kGemvWarps * 32, kGemvCtasPerSm) gemv_kernel(c
 #pragma unroll
     for (int i = 0; i < MR; ++i) { best_v[i] = -FLT_MAX; best_i[i] = INT_MAX; }
 
+    // The first batch of weight loads does not depend on the previous kernel: issue it, then wait.
+    pdl_trigger();
+    bool waited = false;
     for (int p0 = r_begin; p0 < r_end; p0 += R) {
         const int nr = min(R, r_end - p0);
         const TW* wp[R][NW];
@@ -81,6 +84,7 @@ __global__ void __launch_bounds__(kGemvWarps * 32, kGemvCtasPerSm) gemv_kernel(c
                     for (int q = 0; q < NW; ++q)
                         wr[u][j][q] = (k < K && j < nr) ? ld8<true>(wp[j][q] + k) : zero8((TW*)nullptr);
             }
+            if (!waited) { pdl_wait(); waited = true; }
 #pragma unroll
             for (int u = 0; u < U; ++u) {
                 const int k = k0 + u * 256;
@@ -135,6 +139,7 @@ __global__ void __launch_bounds__(kGemvWarps * 32, kGemvCtasPerSm) gemv_kernel(c
         }
     }
 
+    if (!waited) pdl_wait();
     if (EPI == EPI_ARGMAX) {
         __shared__ float sv[kGemvWarps][MR];
         __shared__ int si[kGemvWarps][MR];
@@ -162,9 +167,11 @@ static void gemv_split(int N, int num_sms, int group, int* rows_per_warp, int* c
     int rpw = (int)((N + warps - 1) / warps);
     if (rpw < 1) rpw = 1;
     *R = rpw == 1 ? 1 : 4;
-    if (*R > 1) rpw = (rpw + 3) / 4 * 4;                 // whole passes
-    if (group && group % rpw != 0) {                     // passes must not straddle a group
-        while (group % rpw) ++rpw;
+    if (group && *R > 1) {                               // passes must not straddle a group
+        int r = (rpw + 3) / 4 * 4;
+        while (r <= group && group % r) r += 4;
+        if (r <= group && group % r == 0) rpw = r;
+        else *R = 1;                                     // one-row passes never straddle
     }
     *rows_per_warp = rpw;
     *ctas = (N + kGemvWarps * rpw - 1) / (kGemvWarps * rpw);
@@ -180,9 +187,8 @@ template <typename TA, typename TW, int MR, int EPI>
 static cudaError_t launch_r(const GemvArgs& g, int R, int rpw, int ctas, cudaStream_t st) {
     dim3 grid((g.M + MR - 1) / MR, ctas);
     dim3 block(kGemvWarps * 32);
-    if (R == 1) gemv_kernel<TA, TW, MR, EPI, 1><<<grid, block, 0, st>>>(g, rpw);
-    else gemv_kernel<TA, TW, MR, EPI, 4><<<grid, block, 0, st>>>(g, rpw);
-    return cudaGetLastError();
+    if (R == 1) return launch_pdl(gemv_kernel<TA, TW, MR, EPI, 1>, grid, block, 0, st, g, rpw);
+    return launch_pdl(gemv_kernel<TA, TW, MR, EPI, 4>, grid, block, 0, st, g, rpw);
 }
 
 template <typename TA, typename TW, int EPI>

@@ -47,6 +47,8 @@ embed_norms_kernel(RowArgs a, int decode, const int* tokens, const int* position
                    int batch, int M, const int* tok_in, const int* lengths, const float* fused,
                    const T* embed, const T* w_in, const T* w_hid, float* x, bf16* x_bf, int* row_seq,
                    int* row_pos) {
+    pdl_trigger();
+    pdl_wait();
     __shared__ float red[64];
     const int r = blockIdx.x;
     int b, tok, pos;
@@ -124,6 +126,8 @@ __global__ void __launch_bounds__(kRowThreads)
 latent_kernel(RowArgs a, const float* cqkv, const T* w_qa, const T* w_kva, const float* rope_cos,
               const float* rope_sin, const int* row_seq, const int* row_pos, const int* block_table, T* cache,
               float* cq_hat, bf16* cqh_bf) {
+    pdl_trigger();
+    pdl_wait();
     __shared__ float red[64];
     const int r = blockIdx.x;
     const int dq = a.dq, dc = a.dc, dr = a.dr;
@@ -180,6 +184,8 @@ latent_kernel(RowArgs a, const float* cqkv, const T* w_qa, const T* w_kva, const
 template <typename T>
 __global__ void __launch_bounds__(kVecThreads)
 rmsnorm_kernel(int H, float eps, const float* x, const T* w, float* y, bf16* y_bf) {
+    pdl_trigger();
+    pdl_wait();
     __shared__ float red[64];
     const long r = blockIdx.x;
     const int nch = H / 8;
@@ -216,6 +222,8 @@ template <typename T>
 __global__ void __launch_bounds__(kVecThreads)
 final_kernel(RowArgs a, int extend, int M, const int* row_offsets, const float* h2, const T* w_final,
              const int* row_pos, float* carry, float* z, bf16* z_bf, float* hidden_out, int* lengths) {
+    pdl_trigger();
+    pdl_wait();
     __shared__ float red[64];
     const int b = blockIdx.x;
     int src = extend ? row_offsets[b + 1] - 1 : b;
@@ -267,6 +275,8 @@ __device__ __forceinline__ int remap_token(int d, const int* d2t, int Vt, int* e
 __global__ void __launch_bounds__(kRowThreads)
 argmax_final_kernel(int npart, const float* pval, const int* pidx, int mode, const int* d2t, int Vt, int* d0,
                     int* out_tokens, int gamma, int s, int* tok_in, int* err) {
+    pdl_trigger();
+    pdl_wait();
     __shared__ float sv[kRowThreads / 32];
     __shared__ int si[kRowThreads / 32];
     const int b = blockIdx.x;
@@ -303,6 +313,8 @@ argmax_final_kernel(int npart, const float* pval, const int* pidx, int mode, con
 
 __global__ void emit_first_kernel(int batch, const int* d0, const int* d2t, int Vt, int* out_tokens, int gamma,
                                   int* tok_in, int* err) {
+    pdl_trigger();
+    pdl_wait();
     const int b = blockIdx.x * blockDim.x + threadIdx.x;
     if (b >= batch) return;
     const int t = remap_token(d0[b], d2t, Vt, err);
@@ -313,6 +325,8 @@ __global__ void emit_first_kernel(int batch, const int* d0, const int* d2t, int 
 // accepted_len[b] = leading positions where draft == target ("Eagle3 DeepseekV3 in MAX" §10).
 __global__ void __launch_bounds__(kRowThreads)
 accept_kernel(const int* draft, const int* target, int batch, int gamma, int* acc, int* hist) {
+    pdl_trigger();
+    pdl_wait();
     extern __shared__ int sh[];
     for (int k = threadIdx.x; k <= gamma; k += blockDim.x) sh[k] = 0;
     __syncthreads();
@@ -333,10 +347,10 @@ cudaError_t launch_embed_norms(const RowArgs& a, bool decode, int M, const int* 
                                const float* fused, const void* embed, const void* w_in, const void* w_hid,
                                float* x, __nv_bfloat16* x_bf, int* row_seq, int* row_pos, cudaStream_t st) {
     if (a.dt == BF16)
-        embed_norms_kernel<bf16><<<M, kVecThreads, 0, st>>>(a, decode, tokens, positions, row_offsets, batch, M,
+        launch_pdl(embed_norms_kernel<bf16>, dim3(M), dim3(kVecThreads), 0, st, a, decode, tokens, positions, row_offsets, batch, M,
             tok_in, lengths, fused, (const bf16*)embed, (const bf16*)w_in, (const bf16*)w_hid, x, x_bf, row_seq, row_pos);
     else
-        embed_norms_kernel<float><<<M, kVecThreads, 0, st>>>(a, decode, tokens, positions, row_offsets, batch, M,
+        launch_pdl(embed_norms_kernel<float>, dim3(M), dim3(kVecThreads), 0, st, a, decode, tokens, positions, row_offsets, batch, M,
             tok_in, lengths, fused, (const float*)embed, (const float*)w_in, (const float*)w_hid, x, x_bf, row_seq, row_pos);
     return cudaGetLastError();
 }
@@ -345,18 +359,18 @@ cudaError_t launch_latent(const RowArgs& a, int M, const float* cqkv, const void
                           const float* rope_cos, const float* rope_sin, const int* row_seq, const int* row_pos,
                           const int* block_table, void* cache, float* cq_hat, __nv_bfloat16* cqh_bf, cudaStream_t st) {
     if (a.dt == BF16)
-        latent_kernel<bf16><<<M, kRowThreads, 0, st>>>(a, cqkv, (const bf16*)w_qa, (const bf16*)w_kva, rope_cos,
+        launch_pdl(latent_kernel<bf16>, dim3(M), dim3(kRowThreads), 0, st, a, cqkv, (const bf16*)w_qa, (const bf16*)w_kva, rope_cos,
             rope_sin, row_seq, row_pos, block_table, (bf16*)cache, cq_hat, cqh_bf);
     else
-        latent_kernel<float><<<M, kRowThreads, 0, st>>>(a, cqkv, (const float*)w_qa, (const float*)w_kva, rope_cos,
+        launch_pdl(latent_kernel<float>, dim3(M), dim3(kRowThreads), 0, st, a, cqkv, (const float*)w_qa, (const float*)w_kva, rope_cos,
             rope_sin, row_seq, row_pos, block_table, (float*)cache, cq_hat, cqh_bf);
     return cudaGetLastError();
 }
 
 cudaError_t launch_rmsnorm(int M, int H, float eps, DType wt, const float* x, const void* w, float* y,
                            __nv_bfloat16* y_bf, cudaStream_t st) {
-    if (wt == BF16) rmsnorm_kernel<bf16><<<M, kVecThreads, 0, st>>>(H, eps, x, (const bf16*)w, y, y_bf);
-    else rmsnorm_kernel<float><<<M, kVecThreads, 0, st>>>(H, eps, x, (const float*)w, y, y_bf);
+    if (wt == BF16) launch_pdl(rmsnorm_kernel<bf16>, dim3(M), dim3(kVecThreads), 0, st, H, eps, x, (const bf16*)w, y, y_bf);
+    else launch_pdl(rmsnorm_kernel<float>, dim3(M), dim3(kVecThreads), 0, st, H, eps, x, (const float*)w, y, y_bf);
     return cudaGetLastError();
 }
 
@@ -364,10 +378,10 @@ cudaError_t launch_final(const RowArgs& a, bool extend, int batch, int M, const 
                          const void* w_final, const int* row_pos, float* carry, float* z, __nv_bfloat16* z_bf,
                          float* hidden_out, int* lengths, cudaStream_t st) {
     if (a.dt == BF16)
-        final_kernel<bf16><<<batch, kVecThreads, 0, st>>>(a, extend, M, row_offsets, h2, (const bf16*)w_final,
+        launch_pdl(final_kernel<bf16>, dim3(batch), dim3(kVecThreads), 0, st, a, extend, M, row_offsets, h2, (const bf16*)w_final,
                                                           row_pos, carry, z, z_bf, hidden_out, lengths);
     else
-        final_kernel<float><<<batch, kVecThreads, 0, st>>>(a, extend, M, row_offsets, h2, (const float*)w_final,
+        launch_pdl(final_kernel<float>, dim3(batch), dim3(kVecThreads), 0, st, a, extend, M, row_offsets, h2, (const float*)w_final,
                                                            row_pos, carry, z, z_bf, hidden_out, lengths);
     return cudaGetLastError();
 }
@@ -375,20 +389,20 @@ cudaError_t launch_final(const RowArgs& a, bool extend, int batch, int M, const 
 cudaError_t launch_argmax_final(int batch, int npart, const float* pval, const int* pidx, int mode,
                                 const int* d2t, int Vt, int* d0, int* out_tokens, int gamma, int s,
                                 int* tok_in, int* err, cudaStream_t st) {
-    argmax_final_kernel<<<batch, kRowThreads, 0, st>>>(npart, pval, pidx, mode, d2t, Vt, d0, out_tokens, gamma, s,
+    launch_pdl(argmax_final_kernel, dim3(batch), dim3(kRowThreads), 0, st, npart, pval, pidx, mode, d2t, Vt, d0, out_tokens, gamma, s,
                                                        tok_in, err);
     return cudaGetLastError();
 }
 
 cudaError_t launch_emit_first(int batch, const int* d0, const int* d2t, int Vt, int* out_tokens, int gamma,
                               int* tok_in, int* err, cudaStream_t st) {
-    emit_first_kernel<<<(batch + 127) / 128, 128, 0, st>>>(batch, d0, d2t, Vt, out_tokens, gamma, tok_in, err);
+    launch_pdl(emit_first_kernel, dim3((batch + 127) / 128), dim3(128), 0, st, batch, d0, d2t, Vt, out_tokens, gamma, tok_in, err);
     return cudaGetLastError();
 }
 
 cudaError_t launch_accept(const int* draft, const int* target, int batch, int gamma, int* acc, int* hist,
                           cudaStream_t st) {
-    accept_kernel<<<1, kRowThreads, (gamma + 1) * sizeof(int), st>>>(draft, target, batch, gamma, acc, hist);
+    launch_pdl(accept_kernel, dim3(1), dim3(kRowThreads), (gamma + 1) * sizeof(int), st, draft, target, batch, gamma, acc, hist);
     return cudaGetLastError();
 }
 

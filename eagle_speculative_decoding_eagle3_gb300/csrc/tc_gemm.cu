@@ -112,6 +112,7 @@ template <int BN, bool GLU> struct Cfg {
 
 template <int BN, bool GLU>
 __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_constant__ TcParams p) {
+    pdl_trigger();
     using C = Cfg<BN, GLU>;
     extern __shared__ unsigned char smem_raw[];
     unsigned char* base = reinterpret_cast<unsigned char*>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
@@ -146,6 +147,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
     int issued = 0;
+    pdl_wait();
 
     if (warp == 0 && lane == 0 && nkb > 0) {
         // ---------------- TMA producer
@@ -287,6 +289,8 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
 
 // Split-K reduction: out = epi(sum_z part[z]) for STORE / RESID / GLU.
 __global__ void tc_splitk_reduce(const TcParams p, int splits, int glu) {
+    pdl_trigger();
+    pdl_wait();
     const long total = (long)p.M * p.N;
     const long plane = total;
     const int np = glu ? 2 : 1;
@@ -344,7 +348,8 @@ static cudaError_t tc_launch_bn(const TcParams& p, dim3 grid, cudaStream_t st) {
         if (e != cudaSuccess) return e;
         attr = true;
     }
-    tc::tc_gemm_kernel<BN, GLU><<<grid, tc::kThreads, C::SMEM, st>>>(p);
+    cudaError_t le = launch_pdl(tc::tc_gemm_kernel<BN, GLU>, grid, dim3(tc::kThreads), (size_t)C::SMEM, st, p);
+    if (le != cudaSuccess) return le;
     return cudaGetLastError();
 }
 
@@ -384,7 +389,7 @@ cudaError_t launch_tc_gemm(TcParams& p, int bn, int splits, cudaStream_t st) {
     const long total = (long)p.M * p.N;
     int blocks = (int)((total + 255) / 256);
     if (blocks > 4096) blocks = 4096;
-    tc::tc_splitk_reduce<<<blocks, 256, 0, st>>>(p, splits, glu ? 1 : 0);
+    return launch_pdl(tc::tc_splitk_reduce, dim3(blocks), dim3(256), 0, st, p, splits, glu ? 1 : 0);
     return cudaGetLastError();
 }
 

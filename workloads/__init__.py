@@ -135,10 +135,10 @@ WORKLOADS: dict[str, Workload] = {
     "dsv3_b1": Workload(
         name="dsv3_b1", draft_vocab=32000, batch=1, ctx=(4096, 4096), t_new=1, gamma=3, d2t="sorted",
         accept_p=(0.7, 0.7, 0.7), seed=1001, **_DSV3),
-    # the batch-1 layer shapes with a small vocabulary and context: keeps profiler captures (which save
+    # the batch-1 layer shapes and context with a small vocabulary: keeps profiler captures (which save
     # and restore device memory around every replay pass) to about 1.5 GB on the device
     "dsv3_b1_small": Workload(
-        name="dsv3_b1_small", draft_vocab=4096, batch=1, ctx=(512, 512), t_new=1, gamma=3, d2t="sorted",
+        name="dsv3_b1_small", draft_vocab=4096, batch=1, ctx=(4096, 4096), t_new=1, gamma=3, d2t="sorted",
         accept_p=(0.7, 0.7, 0.7), seed=1005, **dict(_DSV3, target_vocab=8192)),
     # batch-64 decode, ragged contexts, full-vocab head without d2t
     "dsv3_b64": Workload(
