@@ -218,7 +218,9 @@ Offsets plan(const eagle3_config_t& c, int num_sms) {
     o.m_cap = (int)M;
     o.splits_cap = (c.max_ctx + 31) / 32;
     if (o.splits_cap > 64) o.splits_cap = 64;
+    // argmax partials per scored row: the GEMV writes one per CTA, the tensor-core GEMM one per 128 rows
     o.npart = gemv_argmax_parts(c.draft_vocab, num_sms);
+    if (tc && (c.draft_vocab + 127) / 128 > o.npart) o.npart = (c.draft_vocab + 127) / 128;
     // rows x splits never exceeds M + 2 * num_sms (splits = ceil(2 * SMs / (M * groups)) for small M)
     o.part_rows = (size_t)M + 2 * (size_t)num_sms + 1;
     Layout L;

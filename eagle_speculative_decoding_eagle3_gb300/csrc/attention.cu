@@ -10,8 +10,8 @@
 // o_lat and a grouped GEMM applies W_UV,h.
 //
 // Two attention kernels share the partial format:
-//  * attention_mma_kernel (bf16 cache, d_c 512 / d_r 64): 16 heads x 32-token tiles on the tensor
-//    cores with mma.sync m16n8k16 (heads are the MMA rows, so the 16 heads of a CTA share one staged
+//  * attention_mma_kernel (bf16 cache, d_c 512 / d_r 64): 64 heads x 32-token tiles on the tensor
+//    cores with mma.sync m16n8k16 (heads are the MMA rows, so the 64 heads of a CTA share one staged
 //    KV tile); the KV tiles are double-buffered with cp.async through the block table.
 //  * attention_kernel (any dtype, small latent): CUDA-core fallback used by the fp32 head.
 #include <float.h>
@@ -35,13 +35,26 @@ constexpr int kHeadsPerCta = kAttnWarps * kHeadsPerWarp;
 constexpr int kAbsCols = 128;
 template <typename T>
 __global__ void __launch_bounds__(256) absorb_kernel(const AttnArgs a) {
-    pdl_trigger();
-    pdl_wait();
     extern __shared__ float sm[];           // [kAbsRows][dn] q_nope, then [RG][kAbsRows][cols] partials
+    constexpr int kMaxLoads = 8;
     const int h = blockIdx.x, cb = blockIdx.y, r0 = blockIdx.z * kAbsRows;
     const int nr = min(kAbsRows, a.M - r0);
     const int dqk = a.dn + a.dr, D = a.dc + a.dr;
     const int cols = min(kAbsCols, a.dc), c0 = cb * cols;
+    const int nchunk = cols / 8;
+    const int RG = blockDim.x / nchunk;
+    const int cc = threadIdx.x % nchunk, rg = threadIdx.x / nchunk;
+    const T* W = reinterpret_cast<const T*>(a.kv_b) + (long)h * (a.dn + a.dv) * a.dc + c0 + 8 * cc;
+    // the first batch of weight loads (all of them for d_n <= RG * kMaxLoads) precedes the wait on the
+    // kernel that produced q
+    pdl_trigger();
+    Raw8<T> wr[kMaxLoads];
+#pragma unroll
+    for (int j = 0; j < kMaxLoads; ++j) {
+        const int k = rg + j * RG;
+        wr[j] = (rg < RG && k < a.dn) ? ld8<true>(W + (long)k * a.dc) : zero8((T*)nullptr);
+    }
+    pdl_wait();
     float* qn = sm;
     float* part = sm + kAbsRows * a.dn;
     for (int t = threadIdx.x; t < kAbsRows * a.dn; t += blockDim.x) {
@@ -64,22 +77,18 @@ __global__ void __launch_bounds__(256) absorb_kernel(const AttnArgs a) {
         }
     }
     __syncthreads();
-    const int nchunk = cols / 8;
-    const int RG = blockDim.x / nchunk;
-    const int cc = threadIdx.x % nchunk, rg = threadIdx.x / nchunk;
-    const T* W = reinterpret_cast<const T*>(a.kv_b) + (long)h * (a.dn + a.dv) * a.dc + c0 + 8 * cc;
-    constexpr int kMaxLoads = 8;
     float acc[kAbsRows][8];
 #pragma unroll
     for (int i = 0; i < kAbsRows; ++i)
 #pragma unroll
         for (int e = 0; e < 8; ++e) acc[i][e] = 0.f;
-    for (int k0 = rg; k0 < a.dn; k0 += RG * kMaxLoads) {
-        Raw8<T> wr[kMaxLoads];
+    for (int k0 = rg; rg < RG && k0 < a.dn; k0 += RG * kMaxLoads) {
+        if (k0 != rg) {
 #pragma unroll
-        for (int j = 0; j < kMaxLoads; ++j) {
-            const int k = k0 + j * RG;
-            wr[j] = k < a.dn ? ld8<true>(W + (long)k * a.dc) : zero8((T*)nullptr);
+            for (int j = 0; j < kMaxLoads; ++j) {
+                const int k = k0 + j * RG;
+                wr[j] = k < a.dn ? ld8<true>(W + (long)k * a.dc) : zero8((T*)nullptr);
+            }
         }
 #pragma unroll
         for (int j = 0; j < kMaxLoads; ++j) {
@@ -96,10 +105,14 @@ __global__ void __launch_bounds__(256) absorb_kernel(const AttnArgs a) {
             }
         }
     }
+    if (rg < RG) {
 #pragma unroll
-    for (int i = 0; i < kAbsRows; ++i)
-#pragma unroll
-        for (int e = 0; e < 8; ++e) part[((long)rg * kAbsRows + i) * cols + 8 * cc + e] = acc[i][e];
+        for (int i = 0; i < kAbsRows; ++i) {
+            float4* dst = reinterpret_cast<float4*>(part + ((long)rg * kAbsRows + i) * cols + 8 * cc);
+            dst[0] = make_float4(acc[i][0], acc[i][1], acc[i][2], acc[i][3]);
+            dst[1] = make_float4(acc[i][4], acc[i][5], acc[i][6], acc[i][7]);
+        }
+    }
     __syncthreads();
     for (int t = threadIdx.x; t < nr * cols; t += blockDim.x) {
         const int i = t / cols, c = t % cols;
@@ -235,11 +248,11 @@ __global__ void __launch_bounds__(kAttnWarps * 32) attention_kernel(const AttnAr
 // Tensor-core split-K attention for the DeepseekV3 latent geometry (bf16, d_c 512, d_r 64).
 namespace mla_mma {
 constexpr int T = 32;             // tokens per tile
-constexpr int HEADS = 16;         // heads per CTA (the MMA M dimension)
+constexpr int HEADS = 64;         // heads per CTA: four MMA row groups of 16 share each staged KV tile
 constexpr int D = 576, DC = 512;
 constexpr int ROW = D + 8;        // bf16 row stride: 1168 B, 16-byte aligned, an odd number of 16 B units
-constexpr int SROW = T + 8;       // fp32 score row stride
-constexpr int WARPS = 4;          // warp w scores tokens [8w, 8w+8) and owns output columns [128w, 128w+128)
+constexpr int SROW = T + 4;       // fp32 score row stride
+constexpr int WARPS = 8;          // warp w: head group g = w & 3, latent half c = w >> 2
 constexpr size_t SMEM = (size_t)HEADS * ROW * 2 + 2 * (size_t)T * ROW * 2 + (size_t)HEADS * SROW * 4;
 }  // namespace mla_mma
 
@@ -272,53 +285,63 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
     return *reinterpret_cast<const uint32_t*>(&v);
 }
 
-__global__ void __launch_bounds__(mla_mma::WARPS * 32) attention_mma_kernel(const AttnArgs a) {
+// One (split, 64-head block, row) per CTA; 8 warps.  Warp (g, c) scores tokens [16c, 16c + 16) of every
+// tile for heads 16g..16g+15 (two 8-token MMA column tiles, four independent accumulators), the scores go
+// through shared memory, both warps of a head group run the same online softmax over the 32-token tile,
+// and warp (g, c) accumulates O[16 heads, 256c .. 256c + 256) = P V.  Q (64 heads x 576) and the
+// double-buffered KV tiles are staged with cp.async; the KV rows come through the block table.
+__global__ void __launch_bounds__(mla_mma::WARPS * 32, 1) attention_mma_kernel(const AttnArgs a) {
+    using namespace mla_mma;
     pdl_trigger();
     pdl_wait();
-    using namespace mla_mma;
     extern __shared__ __align__(16) unsigned char smraw[];
     bf16* qs = reinterpret_cast<bf16*>(smraw);                  // [HEADS][ROW]
     bf16* kvb = qs + HEADS * ROW;                              // [2][T][ROW]
     float* ss = reinterpret_cast<float*>(kvb + 2 * T * ROW);   // [HEADS][SROW]
-    const int s = blockIdx.x, hg = blockIdx.y, r = blockIdx.z;
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane >> 2, tig = lane & 3;
+    const int s = blockIdx.x, hb = blockIdx.y, r = blockIdx.z;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, gq = lane >> 2, tig = lane & 3;
+    const int hgrp = warp & 3, half = warp >> 2;
     const int b = a.row_seq[r], pos = a.row_pos[r], n = pos + 1;
     int chunk = (n + a.splits - 1) / a.splits;
     chunk = (chunk + T - 1) / T * T;
     const int t0 = s * chunk, t1 = min(n, t0 + chunk);
-    const int h0 = hg * HEADS;
+    const int h0 = hb * HEADS;
 
+    // Q: heads h0 .. h0 + 63 of row r (zero rows past n_heads)
     for (int c = tid; c < HEADS * (D / 8); c += WARPS * 32) {
         const int hh = c / (D / 8), q = c % (D / 8), h = h0 + hh;
-        uint4 v = make_uint4(0, 0, 0, 0);
-        if (h < a.nh) v = *reinterpret_cast<const uint4*>(a.qa_bf + ((long)r * a.nh + h) * D + 8 * q);
-        *reinterpret_cast<uint4*>(qs + hh * ROW + 8 * q) = v;
+        bf16* d = qs + hh * ROW + 8 * q;
+        if (h < a.nh) cp_async16(smem_u32(d), a.qa_bf + ((long)r * a.nh + h) * D + 8 * q);
+        else *reinterpret_cast<uint4*>(d) = make_uint4(0, 0, 0, 0);
     }
     const bf16* cache = reinterpret_cast<const bf16*>(a.cache);
     const int* bt = a.block_table + (long)b * a.max_pages;
+    // tile loader: thread t copies row t % T, chunks t / T + k * (threads / T): one block-table lookup per tile
+    constexpr int kChunkStep = WARPS * 32 / T;
     auto load_tile = [&](int buf, int tt) {
-        bf16* dst = kvb + buf * T * ROW;
-        for (int c = tid; c < T * (D / 8); c += WARPS * 32) {
-            const int j = c / (D / 8), q = c % (D / 8), slot = tt + j;
-            bf16* d = dst + j * ROW + 8 * q;
-            const int page = (slot < t1) ? bt[slot / a.page_size] : -1;
-            if (page >= 0 && page < a.num_pages) {
-                cp_async16(smem_u32(d), cache + ((long)page * a.page_size + slot % a.page_size) * D + 8 * q);
-            } else {
-                *reinterpret_cast<uint4*>(d) = make_uint4(0, 0, 0, 0);
-                if (slot < t1 && q == 0) set_err(a.err, 8);
-            }
+        const int j = tid % T, slot = tt + j;
+        bf16* d = kvb + buf * T * ROW + j * ROW;
+        const int page = (slot < t1) ? bt[slot / a.page_size] : -1;
+        if (page >= 0 && page < a.num_pages) {
+            const bf16* src = cache + ((long)page * a.page_size + slot % a.page_size) * D;
+            for (int q = tid / T; q < D / 8; q += kChunkStep) cp_async16(smem_u32(d + 8 * q), src + 8 * q);
+        } else {
+            for (int q = tid / T; q < D / 8; q += kChunkStep) *reinterpret_cast<uint4*>(d + 8 * q) = make_uint4(0, 0, 0, 0);
+            if (slot < t1 && tid < T) set_err(a.err, 8);
         }
         cp_async_commit();
     };
 
     float m_r[2] = {-INFINITY, -INFINITY}, l_r[2] = {0.f, 0.f};
-    float o[16][4];
+    float o[32][4];
 #pragma unroll
-    for (int i = 0; i < 16; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+    for (int i = 0; i < 32; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
 
     if (t0 < t1) load_tile(0, t0);
+    else cp_async_commit();
     int it = 0;
+    // A-fragment rows of this warp's head group; B rows: tokens 16c + (lane & 7) + 8 (lane >> 4)
+    const uint32_t qrow = smem_u32(qs + (16 * hgrp + (lane & 7) + ((lane >> 3) & 1) * 8) * ROW + (lane >> 4) * 8);
     for (int tt = t0; tt < t1; tt += T, ++it) {
         const int cnt = min(T, t1 - tt);
         if (tt + T < t1) {
@@ -329,38 +352,43 @@ __global__ void __launch_bounds__(mla_mma::WARPS * 32) attention_mma_kernel(cons
         }
         __syncthreads();
         const bf16* K = kvb + (it & 1) * T * ROW;
-        // ---- scores of tokens [8w, 8w+8) for the 16 heads: two accumulators split the k-chain
-        float sacc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-        const uint32_t qrow = smem_u32(qs + ((lane & 7) + ((lane >> 3) & 1) * 8) * ROW + (lane >> 4) * 8);
-        const uint32_t krow = smem_u32(K + (8 * warp + (lane & 7)) * ROW + (lane >> 3) * 8);
-#pragma unroll 6
-        for (int ks = 0; ks < D / 16; ks += 2) {
-            uint32_t qa0[4], qa1[4], kb[4];
-            ldsm_x4(qrow + ks * 32, qa0);
-            ldsm_x4(qrow + (ks + 1) * 32, qa1);
-            ldsm_x4(krow + ks * 32, kb);
-            mma_bf16_16816(sacc[0], qa0, kb[0], kb[1]);
-            mma_bf16_16816(sacc[1], qa1, kb[2], kb[3]);
-        }
-        const int col0 = 8 * warp + 2 * tig;
-        float sv[4];
+        // ---- scores: heads 16g.., tokens 16c + [0, 16)
+        float sacc[2][2][4];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) sv[i] = (sacc[0][i] + sacc[1][i]) * a.sigma;
-        if (col0 >= cnt) sv[0] = sv[2] = -INFINITY;
-        if (col0 + 1 >= cnt) sv[1] = sv[3] = -INFINITY;
-        ss[g * SROW + col0] = sv[0];
-        ss[g * SROW + col0 + 1] = sv[1];
-        ss[(g + 8) * SROW + col0] = sv[2];
-        ss[(g + 8) * SROW + col0 + 1] = sv[3];
+        for (int x = 0; x < 2; ++x)
+#pragma unroll
+            for (int y = 0; y < 2; ++y) sacc[x][y][0] = sacc[x][y][1] = sacc[x][y][2] = sacc[x][y][3] = 0.f;
+        const uint32_t krow = smem_u32(K + (16 * half + (lane & 7) + (lane >> 4) * 8) * ROW + ((lane >> 3) & 1) * 8);
+#pragma unroll 4
+        for (int ks = 0; ks < D / 16; ++ks) {
+            uint32_t qa[4], kb[4];
+            ldsm_x4(qrow + ks * 32, qa);
+            ldsm_x4(krow + ks * 32, kb);
+            mma_bf16_16816(sacc[ks & 1][0], qa, kb[0], kb[1]);
+            mma_bf16_16816(sacc[ks & 1][1], qa, kb[2], kb[3]);
+        }
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) {
+            const int col = 16 * half + 8 * nt + 2 * tig;
+            float v[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) v[i] = (sacc[0][nt][i] + sacc[1][nt][i]) * a.sigma;
+            if (col >= cnt) v[0] = v[2] = -INFINITY;
+            if (col + 1 >= cnt) v[1] = v[3] = -INFINITY;
+            float* row0 = ss + (16 * hgrp + gq) * SROW + col;
+            float* row1 = row0 + 8 * SROW;
+            row0[0] = v[0]; row0[1] = v[1];
+            row1[0] = v[2]; row1[1] = v[3];
+        }
         __syncthreads();
-        // ---- online softmax over the tile (every warp, for rows g and g + 8)
+        // ---- online softmax over the tile for rows gq and gq + 8 of the head group
         float p[2][2][4];   // [k-step][row][cols 2tig, 2tig+1, 2tig+8, 2tig+9]
         float mx[2] = {-INFINITY, -INFINITY};
 #pragma unroll
         for (int kk = 0; kk < 2; ++kk)
 #pragma unroll
             for (int rr = 0; rr < 2; ++rr) {
-                const float* row = ss + (g + 8 * rr) * SROW + kk * 16 + 2 * tig;
+                const float* row = ss + (16 * hgrp + gq + 8 * rr) * SROW + kk * 16 + 2 * tig;
                 p[kk][rr][0] = row[0];
                 p[kk][rr][1] = row[1];
                 p[kk][rr][2] = row[8];
@@ -389,11 +417,11 @@ __global__ void __launch_bounds__(mla_mma::WARPS * 32) attention_mma_kernel(cons
             m_r[rr] = mn;
         }
 #pragma unroll
-        for (int nt = 0; nt < 16; ++nt) {
+        for (int nt = 0; nt < 32; ++nt) {
             o[nt][0] *= alpha[0]; o[nt][1] *= alpha[0];
             o[nt][2] *= alpha[1]; o[nt][3] *= alpha[1];
         }
-        // ---- O[:, 128w : 128w+128] += P V
+        // ---- O[:, 256c : 256c + 256) += P V
 #pragma unroll
         for (int kk = 0; kk < 2; ++kk) {
             uint32_t pa[4];
@@ -401,10 +429,10 @@ __global__ void __launch_bounds__(mla_mma::WARPS * 32) attention_mma_kernel(cons
             pa[1] = pack_bf16(p[kk][1][0], p[kk][1][1]);
             pa[2] = pack_bf16(p[kk][0][2], p[kk][0][3]);
             pa[3] = pack_bf16(p[kk][1][2], p[kk][1][3]);
-            const uint32_t vrow = smem_u32(K + (kk * 16 + (lane & 7) + ((lane >> 3) & 1) * 8) * ROW + 128 * warp +
+            const uint32_t vrow = smem_u32(K + (kk * 16 + (lane & 7) + ((lane >> 3) & 1) * 8) * ROW + 256 * half +
                                            (lane >> 4) * 8);
 #pragma unroll
-            for (int nt = 0; nt < 16; nt += 2) {
+            for (int nt = 0; nt < 32; nt += 2) {
                 uint32_t vb[4];
                 ldsm_x4_t(vrow + nt * 16, vb);
                 mma_bf16_16816(o[nt], pa, vb[0], vb[1]);
@@ -413,18 +441,19 @@ __global__ void __launch_bounds__(mla_mma::WARPS * 32) attention_mma_kernel(cons
         }
         __syncthreads();
     }
+    cp_async_wait<0>();
 #pragma unroll
     for (int rr = 0; rr < 2; ++rr) {
-        const int h = h0 + g + 8 * rr;
+        const int h = h0 + 16 * hgrp + gq + 8 * rr;
         if (h >= a.nh) continue;
         const long base = ((long)r * a.nh + h) * a.splits + s;
-        if (warp == 0 && tig == 0) {
+        if (half == 0 && tig == 0) {
             a.part_ml[base * 2] = (t0 < t1) ? m_r[rr] : -FLT_MAX;
             a.part_ml[base * 2 + 1] = l_r[rr];
         }
 #pragma unroll
-        for (int nt = 0; nt < 16; ++nt) {
-            const int col = 128 * warp + nt * 8 + 2 * tig;
+        for (int nt = 0; nt < 32; ++nt) {
+            const int col = 256 * half + nt * 8 + 2 * tig;
             *reinterpret_cast<float2*>(a.part_o + base * DC + col) = make_float2(o[nt][2 * rr], o[nt][2 * rr + 1]);
         }
     }

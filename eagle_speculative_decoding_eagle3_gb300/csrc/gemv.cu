@@ -166,8 +166,9 @@ static void gemv_split(int N, int num_sms, int group, int* rows_per_warp, int* c
     const long warps = (long)num_sms * kGemvCtasPerSm * kGemvWarps;
     int rpw = (int)((N + warps - 1) / warps);
     if (rpw < 1) rpw = 1;
-    *R = rpw == 1 ? 1 : 4;
+    *R = rpw < 4 ? rpw : 4;                              // 16 / R loads per row keep 16 in flight
     if (group && *R > 1) {                               // passes must not straddle a group
+        *R = 4;
         int r = (rpw + 3) / 4 * 4;
         while (r <= group && group % r) r += 4;
         if (r <= group && group % r == 0) rpw = r;
@@ -187,8 +188,12 @@ template <typename TA, typename TW, int MR, int EPI>
 static cudaError_t launch_r(const GemvArgs& g, int R, int rpw, int ctas, cudaStream_t st) {
     dim3 grid((g.M + MR - 1) / MR, ctas);
     dim3 block(kGemvWarps * 32);
-    if (R == 1) return launch_pdl(gemv_kernel<TA, TW, MR, EPI, 1>, grid, block, 0, st, g, rpw);
-    return launch_pdl(gemv_kernel<TA, TW, MR, EPI, 4>, grid, block, 0, st, g, rpw);
+    switch (R) {
+        case 1: return launch_pdl(gemv_kernel<TA, TW, MR, EPI, 1>, grid, block, 0, st, g, rpw);
+        case 2: return launch_pdl(gemv_kernel<TA, TW, MR, EPI, 2>, grid, block, 0, st, g, rpw);
+        case 3: return launch_pdl(gemv_kernel<TA, TW, MR, EPI, 3>, grid, block, 0, st, g, rpw);
+        default: return launch_pdl(gemv_kernel<TA, TW, MR, EPI, 4>, grid, block, 0, st, g, rpw);
+    }
 }
 
 template <typename TA, typename TW, int EPI>

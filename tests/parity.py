@@ -59,7 +59,7 @@ def run_round(w, seqs=None, absorbed=False, with_logits=True, stored=None, d2t_o
         head.close()
 
     seqs = list(range(w.batch)) if seqs is None else list(seqs)
-    W = WL.F32View(stored)
+    W = WL.F64Cache(stored)
     caches = [O.SeqCache(WL.as_f32(WL.cache_rows(w, b, int(lengths[b]))), w.max_ctx) for b in seqs]
     exs = WL.make_extend(w, lengths, seqs=seqs)
     aux = [WL.as_f32(a) for a in exs.aux]

@@ -68,3 +68,26 @@ def test_dsv3_extend_rows_tensor_core():
     w = WL.workload("dsv3_extend", batch=2, t_new=256, gamma=2, accept_p=(0.7, 0.7))
     gpu, orc, seqs, paged = run_round(w, absorbed=True)
     print(check_round(w, gpu, orc, seqs, paged, TOL_BF16))
+
+
+def test_dsv3_b64_full_size_sampled():
+    # batch 64, ragged contexts U[1024, 8192], full 129280-entry vocab without d2t, gamma 5; the GPU runs
+    # the whole batch on the tensor-core path, the oracle checks two sampled sequences (sequences are
+    # independent)
+    w = WL.workload("dsv3_b64")
+    gpu, orc, seqs, paged = run_round(w, seqs=[5, 42], absorbed=True)
+    print(check_round(w, gpu, orc, seqs, paged, TOL_BF16))
+
+
+def test_dsv3_b256_full_size_sampled():
+    # batch 256, contexts U[4096, 16384], gamma 7, 32000-entry draft vocab with d2t
+    w = WL.workload("dsv3_b256")
+    gpu, orc, seqs, paged = run_round(w, seqs=[0, 131], absorbed=True, with_logits=False)
+    print(check_round(w, gpu, orc, seqs, paged, TOL_BF16))
+
+
+def test_dsv3_extend_full_size_sampled():
+    # 8 sequences x 2048 new rows on an empty cache (causal extend at M = 16384 rows)
+    w = WL.workload("dsv3_extend")
+    gpu, orc, seqs, paged = run_round(w, seqs=[3], absorbed=True)
+    print(check_round(w, gpu, orc, seqs, paged, TOL_BF16))

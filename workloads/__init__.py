@@ -290,6 +290,26 @@ class F32View(Mapping):
         return len(self._s)
 
 
+class F64Cache(Mapping):
+    """Read-only mapping that widens stored tensors to fp64 once and keeps them (for repeated oracle
+    calls on large heads; exact, since bf16 and fp32 values are representable in fp64)."""
+
+    def __init__(self, stored: Mapping):
+        self._s = stored
+        self._c = {}
+
+    def __getitem__(self, k):
+        if k not in self._c:
+            self._c[k] = as_f32(self._s[k]).astype(np.float64)
+        return self._c[k]
+
+    def __iter__(self):
+        return iter(self._s)
+
+    def __len__(self):
+        return len(self._s)
+
+
 # ----------------------------------------------------------------------------
 # Weights
 # ----------------------------------------------------------------------------
@@ -365,9 +385,13 @@ def make_cache(w: Workload, lengths=None, fill=True) -> PagedCache:
     dt = np.float32 if w.dtype == "f32" else np.uint16
     data = np.zeros((num_pages, w.page_size, w.latent_dim), dtype=dt)
     if fill:
-        for b in range(w.batch):
-            rows = cache_rows(w, b, int(lengths[b]))
-            write_rows(data, bt[b], 0, rows, w.page_size)
+        def one(b):
+            write_rows(data, bt[b], 0, cache_rows(w, b, int(lengths[b])), w.page_size)
+        if w.batch > 1:
+            with ThreadPoolExecutor(max_workers=min(_threads(), w.batch)) as ex:
+                list(ex.map(one, range(w.batch)))
+        else:
+            one(0)
     return PagedCache(data=data, block_table=bt, lengths=lengths.copy(), page_size=w.page_size)
 
 
