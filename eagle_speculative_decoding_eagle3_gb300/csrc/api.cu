@@ -542,6 +542,7 @@ const char* eagle3_status_string(eagle3_status_t s) {
         case EAGLE3_ERR_OOM: return "out of device memory";
         case EAGLE3_ERR_CUDA: return "CUDA error";
         case EAGLE3_ERR_DEVICE_RANGE: return "device-side range error";
+        case EAGLE3_ERR_SCRATCH_LIMIT: return "M * N exceeds the fixed scratch of eagle3_linear_noalloc";
     }
     return "unknown status";
 }

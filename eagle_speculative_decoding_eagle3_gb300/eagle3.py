@@ -11,7 +11,8 @@ import os
 
 _LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libeagle3.so")
 
-OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_STATE, ERR_OOM, ERR_CUDA, ERR_DEVICE_RANGE = range(7)
+OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_STATE, ERR_OOM, ERR_CUDA, ERR_DEVICE_RANGE, ERR_SCRATCH_LIMIT = range(8)
+NOALLOC_SCRATCH_BYTES = 16 << 20   # EAGLE3_NOALLOC_SCRATCH_BYTES
 F32, BF16 = 0, 1
 DEVERR_TOKEN, DEVERR_POSITION, DEVERR_D2T, DEVERR_PAGE, DEVERR_ROWS = 1, 2, 4, 8, 16
 
@@ -68,6 +69,7 @@ def _lib():
         lib.eagle3_draft_decode.argtypes = [P, C.c_int32, P, C.POINTER(eagle3_kv_t), P, P, P, P]
         lib.eagle3_accept.argtypes = [P, P, C.c_int32, C.c_int32, P, P, P]
         lib.eagle3_linear.argtypes = [P, P, P, P, C.c_int32, C.c_int32, C.c_int32, P]
+        lib.eagle3_linear_noalloc.argtypes = [P, P, P, C.c_int32, C.c_int32, C.c_int32, P]
         lib.eagle3_draft_get_error.argtypes = [P, C.POINTER(C.c_int32)]
         lib.eagle3_draft_clear_error.argtypes = [P, P]
         lib.eagle3_draft_destroy.argtypes = [P]
@@ -77,7 +79,7 @@ def _lib():
         lib.eagle3_draft_profile_reset.argtypes = [P]
         for f in ("eagle3_draft_profile_enable", "eagle3_draft_profile_read", "eagle3_draft_profile_reset",
                   "eagle3_draft_create", "eagle3_draft_workspace_bytes", "eagle3_draft_extend", "eagle3_draft_decode",
-                  "eagle3_accept", "eagle3_linear", "eagle3_draft_get_error", "eagle3_draft_clear_error", "eagle3_draft_destroy"):
+                  "eagle3_accept", "eagle3_linear", "eagle3_linear_noalloc", "eagle3_draft_get_error", "eagle3_draft_clear_error", "eagle3_draft_destroy"):
             getattr(lib, f).restype = C.c_int
         _L = lib
     return _L
@@ -163,6 +165,13 @@ def eagle3_draft_decode(handle, gamma, d2t, cache: eagle3_kv_t, draft_tokens, hi
 def eagle3_linear(handle, x, w, y, M, N, K, stream=None):
     _check("eagle3_linear", _lib().eagle3_linear(handle, _ptr(x), _ptr(w), _ptr(y), int(M), int(N), int(K),
                                                  _stream(stream)))
+
+
+def eagle3_linear_noalloc(x, w, y, M, N, K, stream=None):
+    """eagle3_linear without a handle and without any device allocation, for callers that cannot allocate
+    (its split-K scratch is a fixed array in the library; M * N <= 2^21; overlapping calls race)."""
+    _check("eagle3_linear_noalloc", _lib().eagle3_linear_noalloc(_ptr(x), _ptr(w), _ptr(y), int(M), int(N),
+                                                                 int(K), _stream(stream)))
 
 
 def eagle3_accept(draft, target, batch, gamma, accepted_len, hist=None, stream=None):

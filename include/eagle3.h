@@ -59,7 +59,8 @@ typedef enum {
     EAGLE3_ERR_STATE = 3,         /* decode before any extend, or batch mismatch */
     EAGLE3_ERR_OOM = 4,           /* workspace allocation failed at create */
     EAGLE3_ERR_CUDA = 5,          /* a CUDA runtime call failed (see eagle3_last_cuda_error) */
-    EAGLE3_ERR_DEVICE_RANGE = 6   /* returned by eagle3_draft_get_error when the error word is set */
+    EAGLE3_ERR_DEVICE_RANGE = 6,  /* returned by eagle3_draft_get_error when the error word is set */
+    EAGLE3_ERR_SCRATCH_LIMIT = 7  /* eagle3_linear_noalloc: M * N exceeds what its fixed scratch holds */
 } eagle3_status_t;
 
 typedef enum { EAGLE3_F32 = 0, EAGLE3_BF16 = 1 } eagle3_dtype_t;
@@ -186,6 +187,36 @@ EAGLE3_API eagle3_status_t eagle3_draft_decode(eagle3_draft_t *d, int32_t gamma,
  * Returns EAGLE3_ERR_UNSUPPORTED for an fp32 head. */
 EAGLE3_API eagle3_status_t eagle3_linear(eagle3_draft_t *d, const void *x, const void *w, float *y, int32_t M,
                                          int32_t N, int32_t K, void *stream);
+
+/* ---- Allocation-free linear layer.  The pages have no counterpart: this is an engineering addition
+ * for callers that cannot allocate device memory on their call path.
+ *
+ * Computes the same product as eagle3_linear, y[m, n] = sum_k x[m, k] w[n, k] (x [M, K] and w [N, K]
+ * bf16 row-major, y [M, N] fp32 row-major; device pointers, 16-byte aligned, owned by the caller), always
+ * on the tcgen05 split-K tensor-core GEMM.  It takes no handle.  Its split-K partial sums live in one
+ * fixed scratch array per device (EAGLE3_NOALLOC_SCRATCH_BYTES plus a 256-byte header) that the library
+ * defines statically in device memory: every GPU that loads the library holds it until the process exits.
+ * Neither the call nor its set-up calls cudaMalloc, cudaFree or any allocating library routine.
+ *
+ * Who needs it: a serving runtime that hands nearly all HBM to its own pool up front (weights, KV pages),
+ * so a handle's workspace, sized for the largest batch, does not fit or would fragment that pool; and
+ * latency-critical loops that must not reach cudaMalloc or cudaFree, which can synchronise the device.
+ * Callers that can allocate should use eagle3_linear.
+ *
+ * Limits: M, N >= 1; K a multiple of 64; M * N <= EAGLE3_NOALLOC_SCRATCH_BYTES / 8 (= 2^21: two fp32
+ * partial planes must fit).  A larger M * N returns EAGLE3_ERR_SCRATCH_LIMIT before any work is queued.
+ * Set-up: the first call on each device (made with that device current) looks the scratch array's
+ * address up with cudaGetSymbolAddress; make that first call before any stream capture begins.
+ * Sharing: all calls on one device share the one scratch array, which keeps the last call's contents.
+ * Calls ordered on one stream are safe; calls that can overlap on the GPU (different streams, or host
+ * threads whose streams are not ordered) race on the scratch and corrupt each other's results.
+ * Each call clears the scratch's device error word on `stream` before the GEMM.  A bounded wait that runs
+ * out inside the GEMM (a failing device) leaves zeros in the affected outputs; this call does not report
+ * it.  Returns EAGLE3_ERR_INVALID_ARG for a null or misaligned pointer or M, N, K < 1,
+ * EAGLE3_ERR_UNSUPPORTED when K is not a multiple of 64, EAGLE3_ERR_CUDA when a CUDA call fails. */
+#define EAGLE3_NOALLOC_SCRATCH_BYTES (16u << 20)
+EAGLE3_API eagle3_status_t eagle3_linear_noalloc(const void *x, const void *w, float *y, int32_t M, int32_t N,
+                                                 int32_t K, void *stream);
 
 /* Greedy acceptance ("Eagle3 DeepseekV3 in MAX" §10): accepted_len[b] = number of leading
  * positions i with draft[b, i] == target[b, i] (0..gamma).  hist (optional, [gamma + 1]) is
