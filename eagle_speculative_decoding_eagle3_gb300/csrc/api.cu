@@ -372,8 +372,9 @@ cudaError_t run_linear(eagle3_draft& d, const Lin& L, int kind, cudaStream_t st)
         g.w_grp = L.w_grp; g.w_grp_stride = L.w_grp_stride; g.w_row0 = L.w_row0;
         g.a_grp = L.a_grp; g.a_grp_stride = L.a_grp_stride;
         g.err = d.err;
-        if (L.epi == EPI_ARGMAX) d.npart = gemv_argmax_parts(L.N, d.num_sms);
-        return traced(d, kind, st, [&] { return launch_gemv(g, L.epi, d.num_sms, st); });
+        const cudaError_t e = traced(d, kind, st, [&] { return launch_gemv(g, L.epi, d.num_sms, st); });
+        if (L.epi == EPI_ARGMAX) d.npart = g.npart;   // partials per row that this launch wrote
+        return e;
     }
     TcParams p;
     memset(&p, 0, sizeof(p));
@@ -479,10 +480,11 @@ cudaError_t run_layer(eagle3_draft& d, eagle3_kv_t* kv, int M, const float* fuse
     } else {
         E3_TRY(traced(d, K_ABSORB, st, [&] { return launch_absorb(aa, st); }));
     }
-    E3_TRY(traced(d, K_ATTN, st, [&] { return launch_attention(aa, st); }));
-    // merge the attention splits into o_lat, then o_h = W_UV,h o_lat,h over the value rows of kv_b
+    // o_lat: written by the attention kernel itself for a single split, else by the split merge; then
+    // o_h = W_UV,h o_lat,h over the value rows of kv_b
     if (tc) aa.olat_bf = d.olat_bf; else aa.olat = d.olat;
-    E3_TRY(traced(d, K_COMBINE, st, [&] { return launch_merge(aa, st); }));
+    E3_TRY(traced(d, K_ATTN, st, [&] { return launch_attention(aa, st); }));
+    if (aa.splits > 1) E3_TRY(traced(d, K_COMBINE, st, [&] { return launch_merge(aa, st); }));
     if (tc) {
         E3_TRY(run_batched(d, K_UNABSORB, M, d.olat_bf, (long)nh * dc, dc, w.kv_b, (long)nh * (dn + dv), dn, dn + dv,
                            dv, dc, nullptr, d.o_bf, (long)nh * dv, dv, st));

@@ -234,6 +234,17 @@ __global__ void __launch_bounds__(kAttnWarps * 32) attention_kernel(const AttnAr
     for (int hh = 0; hh < 2; ++hh) {
         const int h = h0 + warp * kHeadsPerWarp + hh;
         if (h >= a.nh) continue;
+        if (a.splits == 1) {   // a single split is already the whole softmax: o_lat = o / l
+            const float inv = l[hh] > 0.f ? 1.f / l[hh] : 0.f;
+            const long ob = ((long)r * a.nh + h) * DC;
+#pragma unroll
+            for (int i = 0; i < NO; ++i) {
+                const float v = o[hh][i] * inv;
+                if (a.olat) a.olat[ob + lane + 32 * i] = v;
+                if (a.olat_bf) a.olat_bf[ob + lane + 32 * i] = __float2bfloat16_rn(v);
+            }
+            continue;
+        }
         const long base = ((long)r * a.nh + h) * a.splits + s;
         if (lane == 0) {
             a.part_ml[base * 2] = any ? m[hh] : -FLT_MAX;
@@ -446,6 +457,18 @@ __global__ void __launch_bounds__(mla_mma::WARPS * 32, 1) attention_mma_kernel(c
     for (int rr = 0; rr < 2; ++rr) {
         const int h = h0 + 16 * hgrp + gq + 8 * rr;
         if (h >= a.nh) continue;
+        if (a.splits == 1) {   // a single split is already the whole softmax: o_lat = o / l
+            const float inv = l_r[rr] > 0.f ? 1.f / l_r[rr] : 0.f;
+            const long ob = ((long)r * a.nh + h) * DC;
+#pragma unroll
+            for (int nt = 0; nt < 32; ++nt) {
+                const int col = 256 * half + nt * 8 + 2 * tig;
+                const float v0 = o[nt][2 * rr] * inv, v1 = o[nt][2 * rr + 1] * inv;
+                if (a.olat) *reinterpret_cast<float2*>(a.olat + ob + col) = make_float2(v0, v1);
+                if (a.olat_bf) *reinterpret_cast<uint32_t*>(a.olat_bf + ob + col) = pack2_bf16(v0, v1);
+            }
+            continue;
+        }
         const long base = ((long)r * a.nh + h) * a.splits + s;
         if (half == 0 && tig == 0) {
             a.part_ml[base * 2] = (t0 < t1) ? m_r[rr] : -FLT_MAX;
@@ -460,63 +483,84 @@ __global__ void __launch_bounds__(mla_mma::WARPS * 32, 1) attention_mma_kernel(c
 }
 
 // Split-K merge: o_lat[r, h] = sum_s e^{m_s - M} o_s / sum_s e^{m_s - M} l_s (fp32 and/or bf16).
-// One CTA per (row, head); thread t owns latent columns [4t, 4t + 4).
-__global__ void __launch_bounds__(128) merge_kernel(const AttnArgs a) {
+// One CTA of C4 x G threads per (head, row), C4 = d_c / 4: thread t owns the four latent columns
+// 4 (t % C4) .. + 4 of the splits s = t / C4 + j G (j < kMergeJ).  It issues all of its partial loads
+// first, so they are in flight while warp 0 turns the (m_s, l_s) pairs into split weights; the G group
+// sums meet in shared memory.  G grows with the split count (about four splits per thread), up to
+// kMergeThreads threads.
+constexpr int kMergeThreads = 512;
+constexpr int kMergeJ = 16;          // splits per thread: G >= 4 covers the 64-split maximum
+template <int J>                     // J splits per thread at most; J < kMergeJ launches one group
+__global__ void __launch_bounds__(kMergeThreads) merge_kernel(const AttnArgs a) {
     pdl_trigger();
     pdl_wait();
     __shared__ float wsp[64];
+    __shared__ float4 red[J == kMergeJ ? kMergeThreads : 1];
     const int h = blockIdx.x, r = blockIdx.y;
     const int S = a.splits;
     const long base = ((long)r * a.nh + h) * S;
-    if (threadIdx.x < 32) {
-        const int lane = threadIdx.x;
-        float mx = -FLT_MAX;
-        for (int s = lane; s < S; s += 32) mx = fmaxf(mx, a.part_ml[(base + s) * 2]);
-        mx = warp_max(mx);
-        float den = 0.f;
-        for (int s = lane; s < S; s += 32) {
-            const float l = a.part_ml[(base + s) * 2 + 1];
-            const float e = l > 0.f ? __expf(a.part_ml[(base + s) * 2] - mx) : 0.f;
-            wsp[s] = e;
-            den += e * l;
-        }
-        den = warp_sum(den);
+    const int C4 = a.dc / 4, G = (J == kMergeJ) ? blockDim.x / C4 : 1;
+    const int t = threadIdx.x, col4 = t % C4, grp = t / C4;
+    const bool active = grp < G;
+    float4 o[J];
+#pragma unroll
+    for (int j = 0; j < J; ++j) {
+        const int sp = grp + j * G;
+        o[j] = (active && sp < S) ? *reinterpret_cast<const float4*>(a.part_o + (base + sp) * a.dc + 4 * col4)
+                                  : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    if (t < 32) {
+        float m0 = -FLT_MAX, m1 = -FLT_MAX, l0 = 0.f, l1 = 0.f;
+        if (t < S) { m0 = a.part_ml[(base + t) * 2]; l0 = a.part_ml[(base + t) * 2 + 1]; }
+        if (t + 32 < S) { m1 = a.part_ml[(base + t + 32) * 2]; l1 = a.part_ml[(base + t + 32) * 2 + 1]; }
+        const float mx = warp_max(fmaxf(m0, m1));
+        const float e0 = l0 > 0.f ? __expf(m0 - mx) : 0.f;
+        const float e1 = l1 > 0.f ? __expf(m1 - mx) : 0.f;
+        const float den = warp_sum(e0 * l0 + e1 * l1);
         const float inv = den > 0.f ? 1.f / den : 0.f;
-        __syncwarp();
-        for (int s = lane; s < S; s += 32) wsp[s] *= inv;
+        wsp[t] = e0 * inv;
+        wsp[t + 32] = e1 * inv;
     }
     __syncthreads();
-    for (int c = 4 * threadIdx.x; c < a.dc; c += 4 * blockDim.x) {
-        float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-        // splits in batches of 8 so their L2 reads are in flight together
-        for (int s0 = 0; s0 < S; s0 += 8) {
-            float4 o[8];
+    float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-            for (int j = 0; j < 8; ++j)
-                o[j] = (s0 + j < S) ? *reinterpret_cast<const float4*>(a.part_o + (base + s0 + j) * a.dc + c)
-                                    : make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                const float w = (s0 + j < S) ? wsp[s0 + j] : 0.f;
-                v.x = fmaf(w, o[j].x, v.x); v.y = fmaf(w, o[j].y, v.y);
-                v.z = fmaf(w, o[j].z, v.z); v.w = fmaf(w, o[j].w, v.w);
-            }
+    for (int j = 0; j < J; ++j) {
+        const int sp = grp + j * G;
+        const float w = (active && sp < S) ? wsp[sp] : 0.f;
+        v.x = fmaf(w, o[j].x, v.x); v.y = fmaf(w, o[j].y, v.y);
+        v.z = fmaf(w, o[j].z, v.z); v.w = fmaf(w, o[j].w, v.w);
+    }
+    if (J == kMergeJ) {
+        red[t] = v;
+        __syncthreads();
+        if (grp != 0) return;
+        for (int g = 1; g < G; ++g) {
+            const float4 u = red[g * C4 + col4];
+            v.x += u.x; v.y += u.y; v.z += u.z; v.w += u.w;
         }
-        const long o = ((long)r * a.nh + h) * a.dc + c;
-        if (a.olat) *reinterpret_cast<float4*>(a.olat + o) = v;
-        if (a.olat_bf) {
-            uint2 u;
-            u.x = pack2_bf16(v.x, v.y);
-            u.y = pack2_bf16(v.z, v.w);
-            *reinterpret_cast<uint2*>(a.olat_bf + o) = u;
-        }
+    } else if (!active) {
+        return;
+    }
+    const long off = ((long)r * a.nh + h) * a.dc + 4 * col4;
+    if (a.olat) *reinterpret_cast<float4*>(a.olat + off) = v;
+    if (a.olat_bf) {
+        uint2 u;
+        u.x = pack2_bf16(v.x, v.y);
+        u.y = pack2_bf16(v.z, v.w);
+        *reinterpret_cast<uint2*>(a.olat_bf + off) = u;
     }
 }
 
 cudaError_t launch_merge(const AttnArgs& a, cudaStream_t st) {
-    if (a.splits > 64 || a.dc % 4) return cudaErrorInvalidValue;
-    return launch_pdl(merge_kernel, dim3(a.nh, a.M), dim3(128), 0, st, a);
-    return cudaGetLastError();
+    if (a.splits < 1 || a.splits > 64 || a.dc % 4 || a.dc > 4 * kMergeThreads) return cudaErrorInvalidValue;
+    const int C4 = a.dc / 4;
+    if (a.splits <= 4)   // one group of four-split threads: no cross-group reduction
+        return launch_pdl(merge_kernel<4>, dim3(a.nh, a.M), dim3((C4 + 31) / 32 * 32), 0, st, a);
+    int G = (a.splits + 3) / 4;
+    if (G > kMergeThreads / C4) G = kMergeThreads / C4;
+    if ((long)G * kMergeJ < a.splits) return cudaErrorInvalidValue;   // G split groups of kMergeJ splits
+    const int threads = (C4 * G + 31) / 32 * 32;
+    return launch_pdl(merge_kernel<kMergeJ>, dim3(a.nh, a.M), dim3(threads), 0, st, a);
 }
 
 // Rotated rope part of the query: qa[r, h, dc:] = RoPE(q_pe[r, h], pos_r) (fp32 and bf16).

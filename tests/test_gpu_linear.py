@@ -22,8 +22,8 @@ def head():
     h.close()
 
 
-@pytest.mark.parametrize("M", [1, 3, 8, 9, 24, 64, 200, 256, 300])
-@pytest.mark.parametrize("N,K", [(448, 1088), (2112, 1024)])
+@pytest.mark.parametrize("M", [1, 2, 3, 5, 8, 9, 24, 64, 200, 256, 300])
+@pytest.mark.parametrize("N,K", [(448, 1088), (2112, 1024), (2112, 14336)])
 def test_linear_matches_oracle(head, M, N, K):
     from eagle_speculative_decoding_eagle3_gb300 import eagle3 as E
     from eagle_speculative_decoding_eagle3_gb300 import harness as HN

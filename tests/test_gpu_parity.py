@@ -36,6 +36,13 @@ def test_tiny_f32_empty_cache_no_d2t():
     print(check_round(w, gpu, orc, seqs, paged, TOL_F32))
 
 
+def test_tiny_f32_single_split():
+    # contexts short enough (max 28 slots) that attention runs one split and writes o_lat itself
+    w = WL.workload("tiny_f32", batch=3, ctx=(3, 20), t_new=5, gamma=3, seed=80)
+    gpu, orc, seqs, paged = run_round(w)
+    print(check_round(w, gpu, orc, seqs, paged, TOL_F32))
+
+
 def test_mla_shaped_bf16_round():
     # bf16 storage with the DeepseekV3 latent geometry (kv_lora 512, rope 64, nope 128, v 128) on a
     # narrow hidden size; several tiles of context with ragged lengths
