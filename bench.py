@@ -14,6 +14,7 @@ Prints ONE JSON line (rank 0).  Under torchrun every rank runs its own replica o
 from __future__ import annotations
 
 import argparse
+import hashlib
 import ctypes
 import json
 import os
@@ -49,6 +50,29 @@ def dist_env():
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
     return ws, rank, local
+
+
+def measured_traffic(kind, workload):
+    """DRAM bytes per launch of kernel kind `kind` on `workload` from the committed ncu summary
+    (profiles/dram_traffic.json), or None when none was taken there or the kernel's source file has
+    changed since."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic.json")
+    try:
+        with open(path) as f:
+            entries = json.load(f)["entries"]
+    except (OSError, ValueError, KeyError):
+        return None
+    for e in entries:
+        if e.get("kind") != kind or workload not in e.get("workloads", []):
+            continue
+        try:
+            with open(os.path.join(ROOT, e["source"]), "rb") as f:
+                if hashlib.sha1(f.read()).hexdigest() != e["source_sha1"]:
+                    return None
+        except OSError:
+            return None
+        return int(e["dram_read_bytes"]) + int(e["dram_write_bytes"])
+    return None
 
 
 def measured_peaks():
@@ -352,7 +376,8 @@ def run_ours(args, ws, rank, local):
                    "l2": f"inputs larger than L2: {round_bytes / 1e9:.2f} GB of weights+KV streamed per step",
                    "parallelism": f"replicas x{ws} (sequence-sharded, no collective)"},
         "roofline": {"bound": "hbm", "kernel": dom, "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
-                     "frac": round(achieved / hbm, 4), "traffic": None, "avg_us": round(dom_avg_s * 1e6, 2),
+                     "frac": round(achieved / hbm, 4), "traffic": measured_traffic(dom, w.name),
+                     "avg_us": round(dom_avg_s * 1e6, 2),
                      "algo_bytes_per_launch": int(dom_bytes),
                      "peak_source": f"{src} ({'MEASURED_PEAKS.json hbm' if src == 'measured' else 'fallback 6.8 TB/s'})"},
         "step_roofline": {"algo_bytes": int(round_bytes), "achieved_gbs": round(round_bytes / step_s / 1e9, 1),
