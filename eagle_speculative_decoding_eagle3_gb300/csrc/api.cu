@@ -395,7 +395,14 @@ cudaError_t run_linear(eagle3_draft& d, const Lin& L, int kind, cudaStream_t st)
     p.pval = d.pval; p.pidx = d.pidx; p.logits = L.logits; p.ldl = L.ldl;
     p.err = d.err;
     p.nbatch = 1;
-    const int splits = L.epi == EPI_ARGMAX ? 1 : tc_splits(d, L.M, L.N, L.K, bn, glu);
+    int splits = L.epi == EPI_ARGMAX ? 1 : tc_splits(d, L.M, L.N, L.K, bn, glu);
+    // Large problems take 256 weight rows per CTA: the staged activation tile then feeds two MMAs,
+    // halving the shared-memory traffic per FLOP, which bounds 128-row tiles on long-K layers.
+    const long pair_tiles = (long)((L.N + 255) / 256) * ((L.M + bn - 1) / bn);
+    if (!glu && L.epi != EPI_ARGMAX && bn == 256 && pair_tiles >= 2L * d.num_sms) {
+        p.pair = 1;
+        splits = 1;
+    }
     cudaError_t e = traced(d, kind, st, [&] { return launch_tc_gemm(p, bn, splits, st); });
     if (L.epi == EPI_ARGMAX) d.npart = p.npart;
     return e;

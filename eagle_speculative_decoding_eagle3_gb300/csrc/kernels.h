@@ -130,6 +130,8 @@ struct TcParams {
     int bw_rows, bq_kb;           // and writes output columns + z*by_col (one X segment, no split)
     long by_col;
     int epi;                      // EPI_STORE / EPI_RESID / EPI_GLU / EPI_ARGMAX
+    int pair;                     // STORE / RESID at 256 tokens per tile: each CTA takes two 128-row
+                                  // weight tiles that share the activation tile (0 = one tile)
     float* y; long ldy;           // fp32 output (optional)
     __nv_bfloat16* ybf; long ldybf;  // bf16 output (optional)
     const float* resid; long ldr;

@@ -98,8 +98,12 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float* v) {
     for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
 }
 
-template <int BN, bool GLU> struct Cfg {
-    static constexpr int NP = GLU ? 2 : 1;
+// MODE: kSingle (one 128-row weight tile), kGlu (gate and up tiles of the same rows, SiLU(gate) * up)
+// or kPair (two consecutive 128-row tiles of one weight matrix sharing the activation tile: the CTA
+// covers 256 output features, so each staged activation tile feeds twice the MMA work).
+constexpr int kSingle = 0, kGlu = 1, kPair = 2;
+template <int BN, int MODE> struct Cfg {
+    static constexpr int NP = MODE == kSingle ? 1 : 2;
     static constexpr int P_BYTES = BM * BK * 2;
     static constexpr int Q_BYTES = BN * BK * 2;
     static constexpr int STAGE = NP * P_BYTES + Q_BYTES;
@@ -110,10 +114,11 @@ template <int BN, bool GLU> struct Cfg {
     static constexpr int SMEM = STAGES * STAGE + 1024 + 256;
 };
 
-template <int BN, bool GLU>
+template <int BN, int MODE>
 __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_constant__ TcParams p) {
     pdl_trigger();
-    using C = Cfg<BN, GLU>;
+    using C = Cfg<BN, MODE>;
+    constexpr bool GLU = MODE == kGlu, PAIR = MODE == kPair;
     extern __shared__ unsigned char smem_raw[];
     unsigned char* base = reinterpret_cast<unsigned char*>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     uint64_t* bars = reinterpret_cast<uint64_t*>(base + C::STAGES * C::STAGE);
@@ -122,7 +127,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int n0 = blockIdx.x * BM, m0 = blockIdx.y * BN;
+    const int n0 = blockIdx.x * (PAIR ? 2 * BM : BM), m0 = blockIdx.y * BN;
     const int split = blockIdx.z % p.splits, batch = blockIdx.z / p.splits;
     const int kb0 = split * p.kb_per_split;
     const int kb1 = min(p.nkb, kb0 + p.kb_per_split);
@@ -165,6 +170,11 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
             const int kb = kb0 + i;
             tma_load_2d(su32(st), mw, full, kb * BK, wrow);
             if (GLU) tma_load_2d(su32(st + C::P_BYTES), &p.mw[1], full, kb * BK, n0 + batch * p.bw_rows);
+            if (PAIR) {   // rows n0 + 128 .. of the same weights (segment chosen per tile)
+                const int n1 = n0 + BM;
+                const bool sec1 = n1 >= p.np0;
+                tma_load_2d(su32(st + C::P_BYTES), sec1 ? &p.mw[1] : &p.mw[0], full, kb * BK, sec1 ? n1 - p.np0 : n1);
+            }
             const int qs = kb >= p.kseg[1] ? 2 : (kb >= p.kseg[0] ? 1 : 0);
             const int kl = kb - (qs == 0 ? 0 : p.kseg[qs - 1]) + batch * p.bq_kb;
             tma_load_2d(su32(st + C::NP * C::P_BYTES), &p.mx[qs], full, kl * BK, m0);
@@ -186,7 +196,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
             for (int kk = 0; kk < BK / 16; ++kk) {
                 const uint32_t acc = (i > 0 || kk > 0) ? 1u : 0u;
                 mma_bf16(tmem, da + 2 * kk, db + 2 * kk, idesc, acc);
-                if (GLU) mma_bf16(tmem + BN, da2 + 2 * kk, db + 2 * kk, idesc, acc);
+                if (GLU || PAIR) mma_bf16(tmem + BN, da2 + 2 * kk, db + 2 * kk, idesc, acc);
             }
             mma_commit(su32(&bars[C::STAGES + s]));
         }
@@ -194,19 +204,22 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
     } else if (warp >= 2) {
         // ---------------- epilogue: TMEM lanes [32q, 32q+32) are readable by warp q = warp % 4
         const int q = warp & 3;
-        const int n = n0 + 32 * q + lane;
-        const long ncol = n + (long)batch * p.by_col;   // output column of feature n
-        const bool nvalid = n < p.N;
+        const int n_base = n0 + 32 * q + lane;
         bool ok = nkb > 0 && mbar_wait(su32(&bars[2 * C::STAGES]), 0);
         ok = __all_sync(0xffffffffu, ok);   // tcgen05.ld is warp-collective
         if (!ok && nkb > 0) *abort_flag = 1;
         tc_fence_after();
         const uint32_t trow = tmem + ((uint32_t)(32 * q) << 16);
         const bool splitk = p.splits > 1;   // write fp32 partials for the reduction kernel
-        for (int c = 0; c < BN; c += 16) {
+        // kPair: columns [0, BN) of the accumulator hold features n, columns [BN, 2 BN) features n + 128
+        for (int cc = 0; cc < (PAIR ? 2 * BN : BN); cc += 16) {
+            const int c = PAIR ? cc % BN : cc;
+            const int n = n_base + (PAIR && cc >= BN ? BM : 0);
+            const long ncol = n + (long)batch * p.by_col;
+            const bool nvalid = n < p.N;
             float v[16], u[16];
             if (ok) {
-                tmem_ld16(trow + c, v);
+                tmem_ld16(trow + cc, v);
                 if (GLU) tmem_ld16(trow + BN + c, u);
             } else {
 #pragma unroll
@@ -235,20 +248,30 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
                 }
                 continue;
             }
+            // residual operands first: all 16 loads are in flight before the first store (the output
+            // may alias nothing, but the compiler cannot know that)
+            float rv16[16];
+            if (p.epi == EPI_RESID && !splitk) {
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                    const int m = m0 + c + j;
+                    rv16[j] = (nvalid && m < p.M) ? p.resid[(long)m * p.ldr + ncol] : 0.f;
+                }
+            }
 #pragma unroll
             for (int j = 0; j < 16; ++j) {
                 const int m = m0 + c + j;
                 if (!nvalid || m >= p.M) continue;
                 if (splitk) {
                     const long plane = (long)p.M * p.N;
-                    float* part = p.part + (long)split * C::NP * plane;
+                    float* part = p.part + (long)split * (GLU ? 2 : 1) * plane;
                     part[(long)m * p.N + n] = v[j];
                     if (GLU) part[plane + (long)m * p.N + n] = u[j];
                     continue;
                 }
                 float out;
                 if (GLU) out = silu(v[j]) * u[j];
-                else if (p.epi == EPI_RESID) out = v[j] + p.resid[(long)m * p.ldr + ncol];
+                else if (p.epi == EPI_RESID) out = v[j] + rv16[j];
                 else out = v[j];
                 if (p.y) p.y[(long)m * p.ldy + ncol] = out;
                 if (p.ybf) p.ybf[(long)m * p.ldybf + ncol] = __float2bfloat16_rn(out);
@@ -338,17 +361,17 @@ bool make_tma_2d(CUtensorMap* map, const void* ptr, long rows, long cols, long l
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int BN, bool GLU>
+template <int BN, int MODE>
 static cudaError_t tc_launch_bn(const TcParams& p, dim3 grid, cudaStream_t st) {
-    using C = tc::Cfg<BN, GLU>;
+    using C = tc::Cfg<BN, MODE>;
     static bool attr = false;
     if (!attr) {
-        cudaError_t e = cudaFuncSetAttribute(tc::tc_gemm_kernel<BN, GLU>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        cudaError_t e = cudaFuncSetAttribute(tc::tc_gemm_kernel<BN, MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              C::SMEM);
         if (e != cudaSuccess) return e;
         attr = true;
     }
-    cudaError_t le = launch_pdl(tc::tc_gemm_kernel<BN, GLU>, grid, dim3(tc::kThreads), (size_t)C::SMEM, st, p);
+    cudaError_t le = launch_pdl(tc::tc_gemm_kernel<BN, MODE>, grid, dim3(tc::kThreads), (size_t)C::SMEM, st, p);
     if (le != cudaSuccess) return le;
     return cudaGetLastError();
 }
@@ -368,15 +391,19 @@ cudaError_t launch_tc_gemm(TcParams& p, int bn, int splits, cudaStream_t st) {
     p.kb_per_split = (p.nkb + splits - 1) / splits;
     splits = (p.nkb + p.kb_per_split - 1) / p.kb_per_split;
     p.splits = splits;
-    dim3 grid((p.N + tc::BM - 1) / tc::BM, (p.M + bn - 1) / bn, splits * p.nbatch);
-    if (p.epi == EPI_ARGMAX) p.npart = grid.x;
     const bool glu = p.epi == EPI_GLU;
+    const bool pair = p.pair && bn == 256 && !glu && p.epi != EPI_ARGMAX && p.nbatch == 1;
+    const int rows_per_cta = pair ? 2 * tc::BM : tc::BM;
+    dim3 grid((p.N + rows_per_cta - 1) / rows_per_cta, (p.M + bn - 1) / bn, splits * p.nbatch);
+    if (p.epi == EPI_ARGMAX) p.npart = grid.x;
     cudaError_t e;
-#define TC_CASE(B)                                                                       \
-    case B:                                                                              \
-        e = glu ? tc_launch_bn<B, true>(p, grid, st) : tc_launch_bn<B, false>(p, grid, st); \
+#define TC_CASE(B)                                                                                       \
+    case B:                                                                                              \
+        e = glu ? tc_launch_bn<B, tc::kGlu>(p, grid, st) : tc_launch_bn<B, tc::kSingle>(p, grid, st);   \
         break;
-    switch (bn) {
+    if (pair) {
+        e = tc_launch_bn<256, tc::kPair>(p, grid, st);
+    } else switch (bn) {
         TC_CASE(16)
         TC_CASE(32)
         TC_CASE(64)

@@ -38,3 +38,22 @@ def test_linear_matches_oracle(head, M, N, K):
     got = y.cpu().numpy().astype(np.float64)
     err = np.abs(got - ref).max() / np.abs(ref).max()
     assert err < 1e-5, err
+
+
+@pytest.mark.parametrize("M", [2048, 2100])
+def test_linear_pair_tiles_match_oracle(head, M):
+    # enough 256 x 256 tiles that the tensor-core engine pairs two 128-row weight tiles per CTA; the
+    # last pair has a partial first tile and an empty second one, and M ends inside a token tile
+    from eagle_speculative_decoding_eagle3_gb300 import eagle3 as E
+    from eagle_speculative_decoding_eagle3_gb300 import harness as HN
+    N, K = 10048, 1024
+    x = WL.f32_to_bf16_bits(WL.normal((M, K), 1.0, 6, f"linp.x.{M}"))
+    w = WL.f32_to_bf16_bits(WL.normal((N, K), 0.02, 6, "linp.w"))
+    y = torch.full((M, N), float("nan"), dtype=torch.float32, device="cuda")
+    E.eagle3_linear(head.handle, HN.to_device(x), HN.to_device(w), y, M, N, K)
+    torch.cuda.synchronize()
+    assert head.error_word() == 0
+    ref = O.linear(WL.bf16_to_f32(x), WL.bf16_to_f32(w))
+    got = y.cpu().numpy().astype(np.float64)
+    err = np.abs(got - ref).max() / np.abs(ref).max()
+    assert err < 1e-5, err
