@@ -215,10 +215,12 @@ def algorithmic_bytes(w, ctx_lengths):
     return out
 
 
-def algorithmic_flops(w, ctx_lengths):
+def algorithmic_flops(w, ctx_lengths, unabsorbed_extend=False):
     """Algorithmic FLOPs (2 per multiply-add) of each contraction kind for one round, in the form of
-    algorithmic_bytes.  Attention counts what the absorbed form computes: per (row, head, visible latent
-    row) a 576-wide score and a 512-wide value accumulation."""
+    algorithmic_bytes.  Attention counts the form that runs: absorbed, per (row, head, visible latent
+    row) a 576-wide score and a 512-wide value accumulation; or, for an extend on the unabsorbed path,
+    a 192-wide score and a 128-wide value accumulation per (row, head, visible slot), plus the key/value
+    expansion of every live slot (kv_expand)."""
     B, T, G, H = w.batch, w.t_new, w.gamma, w.hidden
     nh, dq, dc, dr, dn, dv, I = w.n_heads, w.q_lora_rank, w.kv_lora_rank, w.qk_rope_dim, w.qk_nope_dim, \
         w.v_head_dim, w.intermediate
@@ -244,7 +246,17 @@ def algorithmic_flops(w, ctx_lengths):
         add("lm_head_argmax", 2.0 * B * H * w.draft_vocab, n)
     L = [int(x) for x in ctx_lengths]
     per_tok = 2.0 * nh * (D + dc)
-    add("attention", per_tok * sum(sum(l + j + 1 for j in range(T)) for l in L), 1)
+    visible = sum(sum(l + j + 1 for j in range(T)) for l in L)
+    if unabsorbed_extend:
+        add("attention", 2.0 * nh * (dqk + dv) * visible, 1)
+        add("kv_expand", 2.0 * sum(l + T for l in L) * dc * nh * (dn + dv), 1)
+        for k in ("absorb", "unabsorb"):   # the extend's share of these kinds does not run
+            f, c = out.get(k, (0.0, 0))
+            if c:
+                tot = f * c - 2.0 * Me * nh * dc * (dn if k == "absorb" else dv)
+                out[k] = (tot / (c - 1), c - 1) if c > 1 else (0.0, 0)
+    else:
+        add("attention", per_tok * visible, 1)
     for s in range(1, G):
         add("attention", per_tok * sum(l + T + s for l in L), 1)
     return out
@@ -389,7 +401,7 @@ def run_ours(args, ws, rank, local):
     peaks, src = measured_peaks()
     hbm = peak_hbm(peaks)
     model = algorithmic_bytes(w, lengths)
-    fmodel = algorithmic_flops(w, lengths)
+    fmodel = algorithmic_flops(w, lengths, unabsorbed_extend="kv_expand" in prof_all)
     tpeak, tkey = peak_tensor(peaks)
     kernels = {}
     tot_all = sum(v[0] for v in prof_all.values())

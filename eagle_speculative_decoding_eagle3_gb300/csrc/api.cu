@@ -25,16 +25,18 @@ static thread_local int g_last_cuda_error = 0;
 namespace {
 enum Kind {
     K_FC = 0, K_EMBED, K_QKV_A, K_LATENT, K_Q_B, K_ABSORB, K_ATTN, K_COMBINE, K_O_PROJ, K_POST_NORM,
-    K_GATE_UP, K_DOWN, K_FINAL, K_LM_HEAD, K_ARGMAX, K_EMIT, K_ROPE_Q, K_UNABSORB, K_COUNT
+    K_GATE_UP, K_DOWN, K_FINAL, K_LM_HEAD, K_ARGMAX, K_EMIT, K_ROPE_Q, K_UNABSORB, K_KV_GATHER, K_KV_EXPAND,
+    K_PREFILL_TILES, K_COUNT
 };
 static_assert(K_COUNT <= EAGLE3_PROF_KINDS, "profile kinds");
 const char* kKindNames[EAGLE3_PROF_KINDS] = {
     "fc", "embed_norms", "q_a_kv_a", "latent_rope_append", "q_b", "absorb", "attention", "merge_splits",
     "o_proj", "post_attn_norm", "gate_up_silu", "down", "final_norm", "lm_head_argmax", "argmax_remap",
-    "emit_first", "rope_q", "unabsorb", "", "", "", "", "", ""};
+    "emit_first", "rope_q", "unabsorb", "kv_gather", "kv_expand", "prefill_tiles", "", "", ""};
 constexpr int kProfPairs = 32768;
 constexpr int kGemvMaxRows = 8;          // rows above this take the tensor-core path (bf16 heads)
 constexpr size_t kSplitKBytes = 64u << 20;
+constexpr int kPrefillMinRows = 1024;    // extends of at least this many rows may take the unabsorbed path
 }  // namespace
 
 struct eagle3_draft {
@@ -55,6 +57,10 @@ struct eagle3_draft {
           *rope_sin = nullptr, *tc_part = nullptr, *olat = nullptr;
     bf16_t *qa_bf = nullptr, *x_bf = nullptr, *cqh_bf = nullptr, *q_bf = nullptr, *olat_bf = nullptr,
            *o_bf = nullptr, *y_bf = nullptr, *m_bf = nullptr, *z_bf = nullptr, *wukt = nullptr;
+    // unabsorbed extend attention (allocated when the configuration allows long extends)
+    bf16_t *xc = nullptr, *xpe = nullptr, *kvx = nullptr;
+    int4* tiles = nullptr;
+    int tiles_cap = 0;
     int *pidx = nullptr, *row_seq = nullptr, *row_pos = nullptr, *d0 = nullptr, *tok_in = nullptr,
         *err = nullptr;
     size_t part_rows = 0;   // capacity of the attention partials in (row, split) pairs
@@ -203,10 +209,18 @@ struct Layout {
 struct Offsets {
     size_t f, carry, x, cqkv, cq_hat, q, qa, qa_bf, part_o, part_ml, o, h1, y, mlp, h2, z, pval, pidx, rope_cos,
         rope_sin, row_seq, row_pos, d0, tok_in, err, olat, x_bf, cqh_bf, q_bf, olat_bf, o_bf, y_bf, m_bf, z_bf, wukt,
-        tc_part, total;
+        tc_part, xc, xpe, kvx, tiles, total;
+    int tiles_cap;
     int m_cap, splits_cap, npart;
     size_t part_rows;
 };
+
+// The unabsorbed extend path exists for bf16 heads with the DeepseekV3 head geometry whose
+// configuration allows extends of at least kPrefillMinRows rows.
+bool prefill_allowed(const eagle3_config_t& c) {
+    return tc_supported(c) && c.max_tokens_per_extend >= kPrefillMinRows &&
+           prefill_supported(c.dtype == EAGLE3_BF16 ? BF16 : F32, c.qk_nope_dim, c.qk_rope_dim, c.v_head_dim);
+}
 
 Offsets plan(const eagle3_config_t& c, int num_sms) {
     Offsets o;
@@ -261,6 +275,14 @@ Offsets plan(const eagle3_config_t& c, int num_sms) {
     o.z_bf = L.take((tc ? B : 0) * H * b2);
     o.wukt = L.take(tc ? (size_t)nh * c.kv_lora_rank * c.qk_nope_dim * b2 : 0);
     o.tc_part = L.take(tc ? kSplitKBytes : 0);
+    // unabsorbed extend attention: gathered latent rows, expanded keys/values, query tile map
+    const bool pre = prefill_allowed(c);
+    const size_t slots = pre ? (size_t)B * c.max_ctx : 0;
+    o.tiles_cap = pre ? prefill_tiles_cap((int)M, (int)B) : 0;
+    o.xc = L.take(slots * c.kv_lora_rank * b2);
+    o.xpe = L.take(slots * c.qk_rope_dim * b2);
+    o.kvx = L.take(slots * nh * (c.qk_nope_dim + c.v_head_dim) * b2);
+    o.tiles = L.take((size_t)o.tiles_cap * sizeof(int4));
     o.total = L.off;
     return o;
 }
@@ -444,7 +466,38 @@ cudaError_t run_batched(eagle3_draft& d, int kind, int M, const bf16_t* x, long 
 
 // The decoder chain from the concatenated input x to h2.
 // fused: the residual stream of the rows (fc output in extend, the carried hidden in decode).
-cudaError_t run_layer(eagle3_draft& d, eagle3_kv_t* kv, int M, const float* fused, cudaStream_t st) {
+// Unabsorbed causal attention of a long extend: rotate q_pe in the bf16 query rows, gather and expand
+// every live slot's keys and values once, then flash-attention tiles write o_h per head (bf16).
+cudaError_t run_prefill_attention(eagle3_draft& d, eagle3_kv_t* kv, int M, int batch, const int32_t* row_offsets,
+                                  cudaStream_t st) {
+    const eagle3_config_t& c = d.cfg;
+    const int nh = c.n_heads, dkv = c.qk_nope_dim + c.v_head_dim;
+    PrefillArgs pa;
+    memset(&pa, 0, sizeof(pa));
+    pa.M = M; pa.B = batch; pa.nh = nh; pa.max_ctx = c.max_ctx;
+    pa.page_size = c.page_size; pa.max_pages = c.max_pages_per_seq; pa.num_pages = kv->num_pages;
+    pa.ntiles_cap = prefill_tiles_cap(M, batch);
+    pa.sigma = attention_scale(c);
+    pa.row_offsets = row_offsets; pa.row_pos = d.row_pos; pa.block_table = kv->block_table; pa.cache = kv->data;
+    pa.xc = d.xc; pa.xpe = d.xpe; pa.kv = d.kvx; pa.q = d.q_bf; pa.qf = d.q;
+    pa.rope_cos = d.rope_cos; pa.rope_sin = d.rope_sin;
+    pa.tiles = d.tiles; pa.o_bf = d.o_bf; pa.err = d.err;
+    if (pa.ntiles_cap > d.tiles_cap) return cudaErrorInvalidValue;
+    E3_TRY(traced(d, K_ROPE_Q, st, [&] { return launch_rope_q_rows(pa, st); }));
+    E3_TRY(traced(d, K_KV_GATHER, st, [&] { return launch_kv_gather(pa, st); }));
+    {
+        Lin L = lin1(d, batch * c.max_ctx, nullptr, d.xc, c.kv_lora_rank, d.w.kv_b, nh * dkv);
+        L.ybf = d.kvx; L.ldybf = (long)nh * dkv;
+        E3_TRY(run_linear(d, L, K_KV_EXPAND, st));
+    }
+    E3_TRY(traced(d, K_PREFILL_TILES, st, [&] { return launch_prefill_tiles(pa, st); }));
+    return traced(d, K_ATTN, st, [&] { return launch_prefill_attention(pa, st); });
+}
+
+// One decoder layer over M rows.  row_offsets (extend only) lets a long extend take the unabsorbed
+// attention path.
+cudaError_t run_layer(eagle3_draft& d, eagle3_kv_t* kv, int M, const float* fused, cudaStream_t st, int batch = 0,
+                      const int32_t* row_offsets = nullptr) {
     const eagle3_config_t& c = d.cfg;
     const eagle3_weights_t& w = d.w;
     const int H = c.hidden, dq = c.q_lora_rank, dc = c.kv_lora_rank, dr = c.qk_rope_dim, dn = c.qk_nope_dim;
@@ -468,40 +521,45 @@ cudaError_t run_layer(eagle3_draft& d, eagle3_kv_t* kv, int M, const float* fuse
         if (tc) { L.ybf = d.q_bf; L.ldybf = (long)nh * dqk; }
         E3_TRY(run_linear(d, L, K_Q_B, st));
     }
-    AttnArgs aa;
-    memset(&aa, 0, sizeof(aa));
-    aa.M = M; aa.nh = nh; aa.dn = dn; aa.dr = dr; aa.dc = dc; aa.dv = dv;
-    aa.sigma = attention_scale(c);
-    aa.page_size = c.page_size; aa.max_pages = c.max_pages_per_seq; aa.num_pages = kv->num_pages; aa.err = d.err;
-    aa.splits = attn_splits(d, M);
-    aa.dt = ra.dt;
-    aa.row_seq = d.row_seq; aa.row_pos = d.row_pos; aa.block_table = kv->block_table;
-    aa.cache = kv->data; aa.kv_b = w.kv_b; aa.q = d.q; aa.rope_cos = d.rope_cos; aa.rope_sin = d.rope_sin;
-    aa.qa = d.qa; aa.qa_bf = ra.dt == BF16 ? d.qa_bf : nullptr;
-    aa.part_o = d.part_o; aa.part_ml = d.part_ml; aa.o = d.o;
-    if (tc) {
-        // rope part, then q_lat,h = q_nope,h W_UK,h as a per-head GEMM against the transposed key weights
-        E3_TRY(traced(d, K_ROPE_Q, st, [&] { return launch_rope_q(aa, st); }));
-        E3_TRY(run_batched(d, K_ABSORB, M, d.q_bf, (long)nh * dqk, dqk, d.wukt, (long)nh * dc, 0, dc, dc, dn,
-                           nullptr, d.qa_bf, (long)nh * D, D, st));
+    const bool prefill = d.tiles && row_offsets && M >= kPrefillMinRows && 2L * M >= (long)batch * c.max_ctx;
+    if (prefill) {
+        E3_TRY(run_prefill_attention(d, kv, M, batch, row_offsets, st));
     } else {
-        E3_TRY(traced(d, K_ABSORB, st, [&] { return launch_absorb(aa, st); }));
-    }
-    // o_lat: written by the attention kernel itself for a single split, else by the split merge; then
-    // o_h = W_UV,h o_lat,h over the value rows of kv_b
-    if (tc) aa.olat_bf = d.olat_bf; else aa.olat = d.olat;
-    E3_TRY(traced(d, K_ATTN, st, [&] { return launch_attention(aa, st); }));
-    if (aa.splits > 1) E3_TRY(traced(d, K_COMBINE, st, [&] { return launch_merge(aa, st); }));
-    if (tc) {
-        E3_TRY(run_batched(d, K_UNABSORB, M, d.olat_bf, (long)nh * dc, dc, w.kv_b, (long)nh * (dn + dv), dn, dn + dv,
-                           dv, dc, nullptr, d.o_bf, (long)nh * dv, dv, st));
-    } else {
-        Lin L = lin1(d, M, d.olat, nullptr, dc, w.kv_b, nh * dv);
-        L.lda[0] = (long)nh * dc;
-        L.w_grp = dv; L.w_grp_stride = dn + dv; L.w_row0 = dn;
-        L.a_grp = dv; L.a_grp_stride = dc;
-        L.y = d.o; L.ldy = (long)nh * dv;
-        E3_TRY(run_linear(d, L, K_UNABSORB, st));
+        AttnArgs aa;
+        memset(&aa, 0, sizeof(aa));
+        aa.M = M; aa.nh = nh; aa.dn = dn; aa.dr = dr; aa.dc = dc; aa.dv = dv;
+        aa.sigma = attention_scale(c);
+        aa.page_size = c.page_size; aa.max_pages = c.max_pages_per_seq; aa.num_pages = kv->num_pages; aa.err = d.err;
+        aa.splits = attn_splits(d, M);
+        aa.dt = ra.dt;
+        aa.row_seq = d.row_seq; aa.row_pos = d.row_pos; aa.block_table = kv->block_table;
+        aa.cache = kv->data; aa.kv_b = w.kv_b; aa.q = d.q; aa.rope_cos = d.rope_cos; aa.rope_sin = d.rope_sin;
+        aa.qa = d.qa; aa.qa_bf = ra.dt == BF16 ? d.qa_bf : nullptr;
+        aa.part_o = d.part_o; aa.part_ml = d.part_ml; aa.o = d.o;
+        if (tc) {
+            // rope part, then q_lat,h = q_nope,h W_UK,h as a per-head GEMM against the transposed key weights
+            E3_TRY(traced(d, K_ROPE_Q, st, [&] { return launch_rope_q(aa, st); }));
+            E3_TRY(run_batched(d, K_ABSORB, M, d.q_bf, (long)nh * dqk, dqk, d.wukt, (long)nh * dc, 0, dc, dc, dn,
+                               nullptr, d.qa_bf, (long)nh * D, D, st));
+        } else {
+            E3_TRY(traced(d, K_ABSORB, st, [&] { return launch_absorb(aa, st); }));
+        }
+        // o_lat: written by the attention kernel itself for a single split, else by the split merge; then
+        // o_h = W_UV,h o_lat,h over the value rows of kv_b
+        if (tc) aa.olat_bf = d.olat_bf; else aa.olat = d.olat;
+        E3_TRY(traced(d, K_ATTN, st, [&] { return launch_attention(aa, st); }));
+        if (aa.splits > 1) E3_TRY(traced(d, K_COMBINE, st, [&] { return launch_merge(aa, st); }));
+        if (tc) {
+            E3_TRY(run_batched(d, K_UNABSORB, M, d.olat_bf, (long)nh * dc, dc, w.kv_b, (long)nh * (dn + dv), dn, dn + dv,
+                               dv, dc, nullptr, d.o_bf, (long)nh * dv, dv, st));
+        } else {
+            Lin L = lin1(d, M, d.olat, nullptr, dc, w.kv_b, nh * dv);
+            L.lda[0] = (long)nh * dc;
+            L.w_grp = dv; L.w_grp_stride = dn + dv; L.w_row0 = dn;
+            L.a_grp = dv; L.a_grp_stride = dc;
+            L.y = d.o; L.ldy = (long)nh * dv;
+            E3_TRY(run_linear(d, L, K_UNABSORB, st));
+        }
     }
     // o_proj + residual
     {
@@ -607,6 +665,9 @@ eagle3_status_t eagle3_draft_create(const eagle3_config_t* config, const eagle3_
     d->x_bf = Bf(o.x_bf); d->cqh_bf = Bf(o.cqh_bf); d->q_bf = Bf(o.q_bf); d->olat_bf = Bf(o.olat_bf);
     d->o_bf = Bf(o.o_bf); d->y_bf = Bf(o.y_bf); d->m_bf = Bf(o.m_bf); d->z_bf = Bf(o.z_bf); d->wukt = Bf(o.wukt);
     d->tc_part = F(o.tc_part);
+    d->xc = Bf(o.xc); d->xpe = Bf(o.xpe); d->kvx = Bf(o.kvx);
+    d->tiles = o.tiles_cap ? reinterpret_cast<int4*>(base + o.tiles) : nullptr;
+    d->tiles_cap = o.tiles_cap;
     std::vector<float> cs, sn;
     yarn_table(d->cfg, cs, sn);
     e = cudaMemcpy(d->rope_cos, cs.data(), cs.size() * sizeof(float), cudaMemcpyHostToDevice);
@@ -659,7 +720,7 @@ eagle3_status_t eagle3_draft_extend(eagle3_draft_t* d, const void* const aux_hid
                                   d->w.embed, d->w.input_norm, d->w.hidden_norm, d->x, tc ? d->x_bf : nullptr,
                                   d->row_seq, d->row_pos, st);
     }));
-    E3_CUDA(run_layer(*d, cache, M, d->f, st));
+    E3_CUDA(run_layer(*d, cache, M, d->f, st, batch, row_offsets));
     const bool tch = use_tc(*d, batch);
     E3_CUDA(traced(*d, K_FINAL, st, [&] {
         return launch_final(ra, true, batch, M, row_offsets, d->h2, d->w.final_norm, d->row_pos, d->carry, d->z,

@@ -84,6 +84,34 @@ cudaError_t launch_emit_first(int batch, const int* d0, const int* d2t, int Vt, 
 cudaError_t launch_accept(const int* draft, const int* target, int batch, int gamma, int* acc, int* hist,
                           cudaStream_t st);
 
+// ---------------------------------------------------------------- causal attention of a long extend
+// (unabsorbed; DeepseekV3 geometry d_n 128, d_r 64, d_v 128)
+struct PrefillArgs {
+    int M, B, nh, max_ctx, page_size, max_pages, num_pages;
+    int ntiles_cap;                    // entries of `tiles` (prefill_tiles_cap)
+    float sigma;
+    const int* row_offsets;            // [B + 1] rows of each sequence in this extend
+    const int* row_pos;                // [M] positions
+    const int* block_table;            // [B, max_pages]
+    const void* cache;                 // bf16 [pages, page_size, 576]
+    __nv_bfloat16* xc;                 // [B * max_ctx, 512] gathered latent rows
+    __nv_bfloat16* xpe;                // [B * max_ctx, 64] gathered rotated k_pe
+    const __nv_bfloat16* kv;           // [B * max_ctx, nh * 256] expanded [k_nope | v] per head
+    __nv_bfloat16* q;                  // [M, nh * 192] bf16 query rows (rope part rotated in place)
+    const float* qf;                   // [M, nh * 192] fp32 query rows (source of the rope part)
+    const float* rope_cos;             // [max_ctx, 32]
+    const float* rope_sin;
+    int4* tiles;                       // [ntiles_cap] (sequence, first row, rows) or sequence -1
+    __nv_bfloat16* o_bf;               // [M, nh * 128] attention output per head
+    int* err;
+};
+bool prefill_supported(int dt, int dn, int dr, int dv);
+int prefill_tiles_cap(int M, int B);
+cudaError_t launch_kv_gather(const PrefillArgs& a, cudaStream_t st);
+cudaError_t launch_prefill_tiles(const PrefillArgs& a, cudaStream_t st);
+cudaError_t launch_rope_q_rows(const PrefillArgs& a, cudaStream_t st);
+cudaError_t launch_prefill_attention(const PrefillArgs& a, cudaStream_t st);
+
 // ---------------------------------------------------------------- MLA attention (absorbed)
 struct AttnArgs {
     int M, nh, dn, dr, dc, dv;

@@ -77,6 +77,25 @@ def test_dsv3_extend_rows_tensor_core():
     print(check_round(w, gpu, orc, seqs, paged, TOL_BF16))
 
 
+def test_mla_shaped_long_extend_unabsorbed():
+    # 2 sequences x 600 new rows over ragged cached prefixes (0..50 slots): the extend takes the
+    # unabsorbed path (gathered and expanded keys/values, flash-attention tiles); the last query tile of
+    # each sequence is partial and the last key tile runs past the configured context
+    w = WL.workload("dsv3_b1", hidden=1024, n_heads=8, q_lora_rank=256, intermediate=2048,
+                    target_vocab=8192, draft_vocab=4096, batch=2, ctx=(0, 50), t_new=600, gamma=2,
+                    accept_p=(0.7, 0.7), seed=81)
+    gpu, orc, seqs, paged = run_round(w)
+    print(check_round(w, gpu, orc, seqs, paged, TOL_BF16))
+
+
+def test_dsv3_long_extend_over_prefix_sampled():
+    # full DeepseekV3 dimensions, 2 sequences x 1024 new rows over cached prefixes of 100..300 slots
+    # (unabsorbed extend path); the oracle checks sequence 1
+    w = WL.workload("dsv3_extend", batch=2, t_new=1024, ctx=(100, 300), gamma=2, accept_p=(0.7, 0.7), seed=82)
+    gpu, orc, seqs, paged = run_round(w, seqs=[1], absorbed=True)
+    print(check_round(w, gpu, orc, seqs, paged, TOL_BF16))
+
+
 def test_dsv3_b64_full_size_sampled():
     # batch 64, ragged contexts U[1024, 8192], full 129280-entry vocab without d2t, gamma 5; the GPU runs
     # the whole batch on the tensor-core path, the oracle checks two sampled sequences (sequences are
