@@ -479,7 +479,7 @@ cudaError_t run_prefill_attention(eagle3_draft& d, eagle3_kv_t* kv, int M, int b
     pa.ntiles_cap = prefill_tiles_cap(M, batch);
     pa.sigma = attention_scale(c);
     pa.row_offsets = row_offsets; pa.row_pos = d.row_pos; pa.block_table = kv->block_table; pa.cache = kv->data;
-    pa.xc = d.xc; pa.xpe = d.xpe; pa.kv = d.kvx; pa.q = d.q_bf; pa.qf = d.q;
+    pa.xc = d.xc; pa.xpe = d.xpe; pa.kv = d.kvx; pa.q = d.q_bf; pa.qf = nullptr;
     pa.rope_cos = d.rope_cos; pa.rope_sin = d.rope_sin;
     pa.tiles = d.tiles; pa.o_bf = d.o_bf; pa.err = d.err;
     if (pa.ntiles_cap > d.tiles_cap) return cudaErrorInvalidValue;
@@ -517,8 +517,9 @@ cudaError_t run_layer(eagle3_draft& d, eagle3_kv_t* kv, int M, const float* fuse
     }));
     {
         Lin L = lin1(d, M, d.cq_hat, d.cqh_bf, dq, w.q_b, nh * dqk);
-        L.y = d.q; L.ldy = (long)nh * dqk;
-        if (tc) { L.ybf = d.q_bf; L.ldybf = (long)nh * dqk; }
+        // the tensor-core path keeps only the bf16 rows: every consumer (absorb GEMM, rope, attention)
+        // reads bf16
+        if (tc) { L.ybf = d.q_bf; L.ldybf = (long)nh * dqk; } else { L.y = d.q; L.ldy = (long)nh * dqk; }
         E3_TRY(run_linear(d, L, K_Q_B, st));
     }
     const bool prefill = d.tiles && row_offsets && M >= kPrefillMinRows && 2L * M >= (long)batch * c.max_ctx;
@@ -534,7 +535,8 @@ cudaError_t run_layer(eagle3_draft& d, eagle3_kv_t* kv, int M, const float* fuse
         aa.dt = ra.dt;
         aa.row_seq = d.row_seq; aa.row_pos = d.row_pos; aa.block_table = kv->block_table;
         aa.cache = kv->data; aa.kv_b = w.kv_b; aa.q = d.q; aa.rope_cos = d.rope_cos; aa.rope_sin = d.rope_sin;
-        aa.qa = d.qa; aa.qa_bf = ra.dt == BF16 ? d.qa_bf : nullptr;
+        aa.qa = tc ? nullptr : d.qa; aa.qa_bf = ra.dt == BF16 ? d.qa_bf : nullptr;
+        aa.q_bf = tc ? d.q_bf : nullptr;
         aa.part_o = d.part_o; aa.part_ml = d.part_ml; aa.o = d.o;
         if (tc) {
             // rope part, then q_lat,h = q_nope,h W_UK,h as a per-head GEMM against the transposed key weights

@@ -546,12 +546,21 @@ __global__ void rope_q_kernel(const AttnArgs a) {
     for (int t = threadIdx.x; t < a.nh * half; t += blockDim.x) {
         const int h = t / half, p = t % half;
         const float c = a.rope_cos[(long)pos * half + p], s = a.rope_sin[(long)pos * half + p];
-        const float* qp = a.q + ((long)r * a.nh + h) * dqk + a.dn;
-        const float x0 = qp[2 * p], x1 = qp[2 * p + 1];
+        const long qi = ((long)r * a.nh + h) * dqk + a.dn + 2 * p;
+        float x0, x1;
+        if (a.q_bf) {
+            x0 = __bfloat162float(a.q_bf[qi]);
+            x1 = __bfloat162float(a.q_bf[qi + 1]);
+        } else {
+            x0 = a.q[qi];
+            x1 = a.q[qi + 1];
+        }
         const float y0 = x0 * c - x1 * s, y1 = x0 * s + x1 * c;
         const long o = ((long)r * a.nh + h) * D + a.dc + 2 * p;
-        a.qa[o] = y0;
-        a.qa[o + 1] = y1;
+        if (a.qa) {
+            a.qa[o] = y0;
+            a.qa[o + 1] = y1;
+        }
         if (a.qa_bf) *reinterpret_cast<uint32_t*>(a.qa_bf + o) = pack2_bf16(y0, y1);
     }
 }

@@ -98,7 +98,8 @@ struct PrefillArgs {
     __nv_bfloat16* xpe;                // [B * max_ctx, 64] gathered rotated k_pe
     const __nv_bfloat16* kv;           // [B * max_ctx, nh * 256] expanded [k_nope | v] per head
     __nv_bfloat16* q;                  // [M, nh * 192] bf16 query rows (rope part rotated in place)
-    const float* qf;                   // [M, nh * 192] fp32 query rows (source of the rope part)
+    const float* qf;                   // [M, nh * 192] fp32 query rows (source of the rope part), or
+                                       // null to rotate the bf16 rows of q in place
     const float* rope_cos;             // [max_ctx, 32]
     const float* rope_sin;
     int4* tiles;                       // [ntiles_cap] (sequence, first row, rows) or sequence -1
@@ -123,6 +124,7 @@ struct AttnArgs {
     const void* cache;
     const void* kv_b;
     const float* q;      // [M, nh*(dn+dr)]
+    const __nv_bfloat16* q_bf;   // bf16 copy of q; when set, rope_q reads the rope part from it
     const float* rope_cos; const float* rope_sin;
     float* qa;           // [M, nh, dc+dr]   absorbed latent query | rotated rope query
     __nv_bfloat16* qa_bf;  // bf16 copy of qa for the tensor-core kernel (nullptr: not written)

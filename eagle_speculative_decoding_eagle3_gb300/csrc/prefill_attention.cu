@@ -114,7 +114,8 @@ __global__ void __launch_bounds__(256) rope_q_rows_kernel(const PrefillArgs a) {
         const int h = t / half, p = t % half;
         const float c = a.rope_cos[(long)pos * half + p], s = a.rope_sin[(long)pos * half + p];
         const long o = ((long)r * a.nh + h) * pf::DQK + pf::DN + 2 * p;
-        const float x0 = a.qf[o], x1 = a.qf[o + 1];
+        const float x0 = a.qf ? a.qf[o] : __bfloat162float(a.q[o]);
+        const float x1 = a.qf ? a.qf[o + 1] : __bfloat162float(a.q[o + 1]);
         *reinterpret_cast<uint32_t*>(a.q + o) = pack_bf16(x0 * c - x1 * s, x0 * s + x1 * c);
     }
 }

@@ -102,6 +102,17 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float* v) {
 // or kPair (two consecutive 128-row tiles of one weight matrix sharing the activation tile: the CTA
 // covers 256 output features, so each staged activation tile feeds twice the MMA work).
 constexpr int kSingle = 0, kGlu = 1, kPair = 2;
+// 32 consecutive accumulator columns of the warp's 32 lanes (one column per register).
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float* v) {
+    uint32_t r[32];
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+                 : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
 template <int BN, int MODE> struct Cfg {
     static constexpr int NP = MODE == kSingle ? 1 : 2;
     static constexpr int P_BYTES = BM * BK * 2;
@@ -127,7 +138,18 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int n0 = blockIdx.x * (PAIR ? 2 * BM : BM), m0 = blockIdx.y * BN;
+    // tile order: groups of up to 8 token tiles run back to back on each weight tile, so the CTAs in
+    // flight share weight panels in L2 instead of streaming every weight panel once per token tile
+    int ntile = blockIdx.x, mtile = blockIdx.y;
+    if (gridDim.y > 1) {
+        constexpr int G = 8;
+        const int lin = blockIdx.x + gridDim.x * blockIdx.y;
+        const int g = lin / (G * gridDim.x), in = lin % (G * gridDim.x);
+        const int gsize = min(G, (int)gridDim.y - g * G);
+        mtile = g * G + in % gsize;
+        ntile = in / gsize;
+    }
+    const int n0 = ntile * (PAIR ? 2 * BM : BM), m0 = mtile * BN;
     const int split = blockIdx.z % p.splits, batch = blockIdx.z / p.splits;
     const int kb0 = split * p.kb_per_split;
     const int kb1 = min(p.nkb, kb0 + p.kb_per_split);
@@ -211,24 +233,38 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
         tc_fence_after();
         const uint32_t trow = tmem + ((uint32_t)(32 * q) << 16);
         const bool splitk = p.splits > 1;   // write fp32 partials for the reduction kernel
+        // bf16-only outputs are staged through the (now idle) stage ring as [token][feature] rows and
+        // leave in 16-byte row chunks: output rows are far apart (tens of KB), and one 64-byte piece
+        // per row per store instruction left the writes at a fraction of the bandwidth
+        constexpr int TW = PAIR ? 2 * BM : BM;      // output features of this CTA
+        constexpr int OPITCH = TW + 8;              // staged row pitch (bf16), 16-byte multiple
+        static_assert((size_t)BN * OPITCH * 2 <= (size_t)C::STAGES * C::STAGE, "staged tile fits the ring");
+        const bool staged = !splitk && p.epi != EPI_ARGMAX && p.epi != EPI_RESID && p.y == nullptr && p.ybf != nullptr;
+        __nv_bfloat16* obuf = reinterpret_cast<__nv_bfloat16*>(base);
         // kPair: columns [0, BN) of the accumulator hold features n, columns [BN, 2 BN) features n + 128
-        for (int cc = 0; cc < (PAIR ? 2 * BN : BN); cc += 16) {
+        constexpr int CW = BN >= 32 ? 32 : 16;   // accumulator columns per TMEM load
+        for (int cc = 0; cc < (PAIR ? 2 * BN : BN); cc += CW) {
             const int c = PAIR ? cc % BN : cc;
             const int n = n_base + (PAIR && cc >= BN ? BM : 0);
             const long ncol = n + (long)batch * p.by_col;
             const bool nvalid = n < p.N;
-            float v[16], u[16];
+            float v[CW], u[CW];
             if (ok) {
-                tmem_ld16(trow + cc, v);
-                if (GLU) tmem_ld16(trow + BN + c, u);
+                if (CW == 32) {
+                    tmem_ld32(trow + cc, v);
+                    if (GLU) tmem_ld32(trow + BN + c, u);
+                } else {
+                    tmem_ld16(trow + cc, v);
+                    if (GLU) tmem_ld16(trow + BN + c, u);
+                }
             } else {
 #pragma unroll
-                for (int j = 0; j < 16; ++j) { v[j] = 0.f; u[j] = 0.f; }
+                for (int j = 0; j < CW; ++j) { v[j] = 0.f; u[j] = 0.f; }
             }
             if (p.epi == EPI_ARGMAX) {
                 // per token: (max, argmax) over this warp's 32 features, lowest index on ties
 #pragma unroll
-                for (int j = 0; j < 16; ++j) {
+                for (int j = 0; j < CW; ++j) {
                     float bvv = nvalid ? v[j] : -FLT_MAX;
                     int bi = nvalid ? n : INT_MAX;
                     const int m = m0 + c + j;
@@ -248,18 +284,18 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
                 }
                 continue;
             }
-            // residual operands first: all 16 loads are in flight before the first store (the output
+            // residual operands first: all CW loads are in flight before the first store (the output
             // may alias nothing, but the compiler cannot know that)
-            float rv16[16];
+            float rv16[CW];
             if (p.epi == EPI_RESID && !splitk) {
 #pragma unroll
-                for (int j = 0; j < 16; ++j) {
+                for (int j = 0; j < CW; ++j) {
                     const int m = m0 + c + j;
                     rv16[j] = (nvalid && m < p.M) ? p.resid[(long)m * p.ldr + ncol] : 0.f;
                 }
             }
 #pragma unroll
-            for (int j = 0; j < 16; ++j) {
+            for (int j = 0; j < CW; ++j) {
                 const int m = m0 + c + j;
                 if (!nvalid || m >= p.M) continue;
                 if (splitk) {
@@ -273,8 +309,24 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
                 if (GLU) out = silu(v[j]) * u[j];
                 else if (p.epi == EPI_RESID) out = v[j] + rv16[j];
                 else out = v[j];
+                if (staged) {
+                    obuf[(c + j) * OPITCH + (n - n0)] = __float2bfloat16_rn(out);
+                    continue;
+                }
                 if (p.y) p.y[(long)m * p.ldy + ncol] = out;
                 if (p.ybf) p.ybf[(long)m * p.ldybf + ncol] = __float2bfloat16_rn(out);
+            }
+        }
+        if (staged) {
+            asm volatile("bar.sync 1, 128;" ::: "memory");   // the four epilogue warps
+            constexpr int CPR = TW / 8;                       // 16-byte chunks per staged row
+            const long col0 = (long)batch * p.by_col;
+            for (int i = threadIdx.x - 64; i < BN * CPR; i += 128) {
+                const int row = i / CPR, ch = i % CPR;
+                const int m = m0 + row, nf = n0 + ch * 8;
+                if (m >= p.M || nf >= p.N) continue;
+                *reinterpret_cast<uint4*>(p.ybf + (long)m * p.ldybf + col0 + nf) =
+                    *reinterpret_cast<const uint4*>(obuf + row * OPITCH + ch * 8);
             }
         }
         if (p.epi == EPI_ARGMAX) {
@@ -288,8 +340,8 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
                 int bi = ri[j];
                 for (int w = 1; w < 4; ++w)
                     if (better(rv[w * BN + j], ri[w * BN + j], b, bi)) { b = rv[w * BN + j]; bi = ri[w * BN + j]; }
-                p.pval[(long)m * p.npart + blockIdx.x] = b;
-                p.pidx[(long)m * p.npart + blockIdx.x] = bi;
+                p.pval[(long)m * p.npart + ntile] = b;
+                p.pidx[(long)m * p.npart + ntile] = bi;
             }
         }
     }

@@ -148,6 +148,11 @@ WORKLOADS: dict[str, Workload] = {
     "dsv3_extend": Workload(
         name="dsv3_extend", draft_vocab=32000, batch=8, ctx=(0, 0), t_new=2048, gamma=1, d2t="sorted",
         accept_p=(0.7,), seed=1003, **_DSV3),
+    # one sequence of the extend above (2048 new rows): the same kernels at a size a profiler capture of
+    # every section can hold
+    "dsv3_extend_small": Workload(
+        name="dsv3_extend_small", draft_vocab=32000, batch=1, ctx=(0, 0), t_new=2048, gamma=1, d2t="sorted",
+        accept_p=(0.7,), seed=1006, **_DSV3),
     # batch-256 decode, long ragged contexts, gamma 7, acceptance decaying 0.9 -> 0.5
     "dsv3_b256": Workload(
         name="dsv3_b256", draft_vocab=32000, batch=256, ctx=(4096, 16384), t_new=1, gamma=7, d2t="sorted",
