@@ -35,6 +35,8 @@ const char* kKindNames[EAGLE3_PROF_KINDS] = {
     "emit_first", "rope_q", "unabsorb", "kv_gather", "kv_expand", "prefill_tiles", "", "", ""};
 constexpr int kProfPairs = 32768;
 constexpr int kGemvMaxRows = 8;          // rows above this take the tensor-core path (bf16 heads)
+constexpr int kAttnWaves = 8;            // waves of attention CTAs planned for fixed-chunk splits
+constexpr int kAttnChunkRows = 16;       // rows from which attention splits use fixed chunks
 constexpr size_t kSplitKBytes = 64u << 20;
 constexpr int kPrefillMinRows = 1024;    // extends of at least this many rows may take the unabsorbed path
 }  // namespace
@@ -137,15 +139,34 @@ eagle3_status_t cuda_fail(cudaError_t e) {
 
 bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
 
-int attn_splits(const eagle3_draft& d, int M) {
+// Attention split plan for M rows.  With few rows the context of each row is divided evenly over
+// enough splits for two CTAs per SM.  From kAttnChunkRows rows on, contexts are cut into fixed chunks
+// instead (about kAttnWaves waves of CTAs over the longest possible context), so rows of very different
+// lengths give CTAs of similar work; splits past a row's context exit at once.
+void attn_plan(const eagle3_draft& d, int M, int* splits, int* chunk) {
     const int hpc = attention_heads_per_cta(d.cfg.dtype == EAGLE3_BF16 ? BF16 : F32, d.cfg.kv_lora_rank,
                                             d.cfg.qk_rope_dim);
-    const int hg = (d.cfg.n_heads + hpc - 1) / hpc;
-    const long want = 2L * d.num_sms;
-    long s = (want + (long)M * hg - 1) / ((long)M * hg);
-    if (s < 1) s = 1;
-    if (s > d.splits_cap) s = d.splits_cap;
-    return (int)s;
+    const long hg = (d.cfg.n_heads + hpc - 1) / hpc;
+    const long rows = (long)M * hg, ctx = d.cfg.max_ctx;
+    *chunk = 0;
+    if (M < kAttnChunkRows) {
+        long s = (2L * d.num_sms + rows - 1) / rows;
+        if (s < 1) s = 1;
+        if (s > d.splits_cap) s = d.splits_cap;
+        *splits = (int)s;
+        return;
+    }
+    long ch = (ctx * rows + (long)kAttnWaves * d.num_sms - 1) / ((long)kAttnWaves * d.num_sms);
+    if (ch < 256) ch = 256;
+    ch = (ch + 31) / 32 * 32;
+    long s = (ctx + ch - 1) / ch;
+    // at most splits_cap splits, and the (row, split) partials must fit the workspace
+    while (s > 1 && (s > d.splits_cap || (size_t)M * s > d.part_rows)) {
+        ch *= 2;
+        s = (ctx + ch - 1) / ch;
+    }
+    *splits = (int)s;
+    *chunk = s > 1 ? (int)ch : 0;
 }
 
 eagle3_status_t check_config(const eagle3_config_t* c) {
@@ -235,8 +256,9 @@ Offsets plan(const eagle3_config_t& c, int num_sms) {
     // argmax partials per scored row: the GEMV writes one per CTA, the tensor-core GEMM one per 128 rows
     o.npart = gemv_argmax_parts(c.draft_vocab, num_sms);
     if (tc && (c.draft_vocab + 127) / 128 > o.npart) o.npart = (c.draft_vocab + 127) / 128;
-    // rows x splits never exceeds M + 2 * num_sms (splits = ceil(2 * SMs / (M * groups)) for small M)
-    o.part_rows = (size_t)M + 2 * (size_t)num_sms + 1;
+    // (row, split) partials: few rows use at most M + 2 * num_sms pairs (splits = ceil(2 SMs / (M groups)));
+    // fixed chunks are planned for about kAttnWaves * num_sms pairs and shrunk to fit this capacity
+    o.part_rows = (size_t)M + (size_t)kAttnWaves * num_sms + 1;
     Layout L;
     const size_t f4 = 4, b2 = 2;
     o.f = L.take(M * H * f4);
@@ -531,7 +553,7 @@ cudaError_t run_layer(eagle3_draft& d, eagle3_kv_t* kv, int M, const float* fuse
         aa.M = M; aa.nh = nh; aa.dn = dn; aa.dr = dr; aa.dc = dc; aa.dv = dv;
         aa.sigma = attention_scale(c);
         aa.page_size = c.page_size; aa.max_pages = c.max_pages_per_seq; aa.num_pages = kv->num_pages; aa.err = d.err;
-        aa.splits = attn_splits(d, M);
+        attn_plan(d, M, &aa.splits, &aa.chunk);
         aa.dt = ra.dt;
         aa.row_seq = d.row_seq; aa.row_pos = d.row_pos; aa.block_table = kv->block_table;
         aa.cache = kv->data; aa.kv_b = w.kv_b; aa.q = d.q; aa.rope_cos = d.rope_cos; aa.rope_sin = d.rope_sin;

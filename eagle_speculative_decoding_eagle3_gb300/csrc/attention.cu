@@ -146,10 +146,13 @@ __global__ void __launch_bounds__(kAttnWarps * 32) attention_kernel(const AttnAr
     const int s = blockIdx.x, hg = blockIdx.y, r = blockIdx.z;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int b = a.row_seq[r], pos = a.row_pos[r], n = pos + 1;
-    int chunk = (n + a.splits - 1) / a.splits;
+    int chunk = a.chunk > 0 ? a.chunk : (n + a.splits - 1) / a.splits;
     chunk = (chunk + kTile - 1) / kTile * kTile;
     const int t0 = s * chunk, t1 = min(n, t0 + chunk);
     const int h0 = hg * kHeadsPerCta;
+    if (a.chunk > 0 && t0 >= t1) {   // past this row's context: an empty split that the merge skips
+        return;
+    }
 
     for (int t = threadIdx.x; t < kHeadsPerCta * D; t += blockDim.x) {
         const int hh = t / D, d = t % D, h = h0 + hh;
@@ -286,10 +289,11 @@ __global__ void __launch_bounds__(mla_mma::WARPS * 32, 1) attention_mma_kernel(c
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, gq = lane >> 2, tig = lane & 3;
     const int hgrp = warp & 3, half = warp >> 2;
     const int b = a.row_seq[r], pos = a.row_pos[r], n = pos + 1;
-    int chunk = (n + a.splits - 1) / a.splits;
+    int chunk = a.chunk > 0 ? a.chunk : (n + a.splits - 1) / a.splits;
     chunk = (chunk + T - 1) / T * T;
     const int t0 = s * chunk, t1 = min(n, t0 + chunk);
     const int h0 = hb * HEADS;
+    if (a.chunk > 0 && t0 >= t1) return;   // past this row's context: an empty split that the merge skips
 
     // Q: heads h0 .. h0 + 63 of row r (zero rows past n_heads)
     for (int c = tid; c < HEADS * (D / 8); c += WARPS * 32) {
@@ -456,36 +460,38 @@ __global__ void __launch_bounds__(mla_mma::WARPS * 32, 1) attention_mma_kernel(c
 }
 
 // Split-K merge: o_lat[r, h] = sum_s e^{m_s - M} o_s / sum_s e^{m_s - M} l_s (fp32 and/or bf16).
-// One CTA of C4 x G threads per (head, row), C4 = d_c / 4: thread t owns the four latent columns
-// 4 (t % C4) .. + 4 of the splits s = t / C4 + j G (j < kMergeJ).  It issues all of its partial loads
-// first, so they are in flight while warp 0 turns the (m_s, l_s) pairs into split weights; the G group
-// sums meet in shared memory.  G grows with the split count (about four splits per thread), up to
-// kMergeThreads threads.
+// One CTA per (head, row); thread t owns the four latent columns 4 (t % C4) .. + 4 (C4 = d_c / 4) of the
+// splits s = t / C4 + j G (j < J).  It issues all of its partial loads first, so they are in flight
+// while warp 0 turns the (m_s, l_s) pairs into split weights.  Up to 16 splits one group of C4 threads
+// holds them all; beyond that G groups (about four splits per thread, up to kMergeThreads threads) meet
+// in shared memory.  With fixed-chunk splits only the splits that reach into the row's context are read.
 constexpr int kMergeThreads = 512;
 constexpr int kMergeJ = 16;          // splits per thread: G >= 4 covers the 64-split maximum
-template <int J>                     // J splits per thread at most; J < kMergeJ launches one group
+template <int J, bool MULTI>         // J splits per thread at most; MULTI: several split groups
 __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const AttnArgs a) {
     pdl_trigger();
     pdl_wait();
     __shared__ float wsp[64];
-    __shared__ float4 red[J == kMergeJ ? kMergeThreads : 1];
+    __shared__ float4 red[MULTI ? kMergeThreads : 1];
     const int h = blockIdx.x, r = blockIdx.y;
     const int S = a.splits;
     const long base = ((long)r * a.nh + h) * S;
-    const int C4 = a.dc / 4, G = (J == kMergeJ) ? blockDim.x / C4 : 1;
+    const int C4 = a.dc / 4, G = MULTI ? blockDim.x / C4 : 1;
+    // fixed chunks: only the splits that cover part of this row's context hold partials
+    const int Sv = a.chunk > 0 ? min(S, (a.row_pos[r] + a.chunk) / a.chunk) : S;
     const int t = threadIdx.x, col4 = t % C4, grp = t / C4;
     const bool active = grp < G;
     float4 o[J];
 #pragma unroll
     for (int j = 0; j < J; ++j) {
         const int sp = grp + j * G;
-        o[j] = (active && sp < S) ? *reinterpret_cast<const float4*>(a.part_o + (base + sp) * a.dc + 4 * col4)
-                                  : make_float4(0.f, 0.f, 0.f, 0.f);
+        o[j] = (active && sp < Sv) ? *reinterpret_cast<const float4*>(a.part_o + (base + sp) * a.dc + 4 * col4)
+                                   : make_float4(0.f, 0.f, 0.f, 0.f);
     }
     if (t < 32) {
         float m0 = -FLT_MAX, m1 = -FLT_MAX, l0 = 0.f, l1 = 0.f;
-        if (t < S) { m0 = a.part_ml[(base + t) * 2]; l0 = a.part_ml[(base + t) * 2 + 1]; }
-        if (t + 32 < S) { m1 = a.part_ml[(base + t + 32) * 2]; l1 = a.part_ml[(base + t + 32) * 2 + 1]; }
+        if (t < Sv) { m0 = a.part_ml[(base + t) * 2]; l0 = a.part_ml[(base + t) * 2 + 1]; }
+        if (t + 32 < Sv) { m1 = a.part_ml[(base + t + 32) * 2]; l1 = a.part_ml[(base + t + 32) * 2 + 1]; }
         const float mx = warp_max(fmaxf(m0, m1));
         const float e0 = l0 > 0.f ? __expf(m0 - mx) : 0.f;
         const float e1 = l1 > 0.f ? __expf(m1 - mx) : 0.f;
@@ -499,11 +505,11 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const AttnArgs a) 
 #pragma unroll
     for (int j = 0; j < J; ++j) {
         const int sp = grp + j * G;
-        const float w = (active && sp < S) ? wsp[sp] : 0.f;
+        const float w = (active && sp < Sv) ? wsp[sp] : 0.f;
         v.x = fmaf(w, o[j].x, v.x); v.y = fmaf(w, o[j].y, v.y);
         v.z = fmaf(w, o[j].z, v.z); v.w = fmaf(w, o[j].w, v.w);
     }
-    if (J == kMergeJ) {
+    if (MULTI) {
         red[t] = v;
         __syncthreads();
         if (grp != 0) return;
@@ -527,13 +533,16 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const AttnArgs a) 
 cudaError_t launch_merge(const AttnArgs& a, cudaStream_t st) {
     if (a.splits < 1 || a.splits > 64 || a.dc % 4 || a.dc > 4 * kMergeThreads) return cudaErrorInvalidValue;
     const int C4 = a.dc / 4;
-    if (a.splits <= 4)   // one group of four-split threads: no cross-group reduction
-        return launch_pdl(merge_kernel<4>, dim3(a.nh, a.M), dim3((C4 + 31) / 32 * 32), 0, st, a);
+    // up to 16 splits: one group whose threads hold all of them, no cross-group reduction
+    const dim3 one((C4 + 31) / 32 * 32);
+    if (a.splits <= 4) return launch_pdl(merge_kernel<4, false>, dim3(a.nh, a.M), one, 0, st, a);
+    if (a.splits <= 8) return launch_pdl(merge_kernel<8, false>, dim3(a.nh, a.M), one, 0, st, a);
+    if (a.splits <= 16) return launch_pdl(merge_kernel<16, false>, dim3(a.nh, a.M), one, 0, st, a);
     int G = (a.splits + 3) / 4;
     if (G > kMergeThreads / C4) G = kMergeThreads / C4;
     if ((long)G * kMergeJ < a.splits) return cudaErrorInvalidValue;   // G split groups of kMergeJ splits
     const int threads = (C4 * G + 31) / 32 * 32;
-    return launch_pdl(merge_kernel<kMergeJ>, dim3(a.nh, a.M), dim3(threads), 0, st, a);
+    return launch_pdl(merge_kernel<kMergeJ, true>, dim3(a.nh, a.M), dim3(threads), 0, st, a);
 }
 
 // Rotated rope part of the query: qa[r, h, dc:] = RoPE(q_pe[r, h], pos_r) (fp32 and bf16).

@@ -118,6 +118,8 @@ struct AttnArgs {
     int M, nh, dn, dr, dc, dv;
     float sigma;
     int page_size, max_pages, num_pages, splits;
+    int chunk;                // > 0: split s covers slots [s chunk, (s + 1) chunk) of every row (splits past a
+                              // row's context are empty); 0: a row's context is divided evenly over splits
     int* err;
     DType dt;
     const int* row_seq; const int* row_pos; const int* block_table;
