@@ -262,6 +262,20 @@ def algorithmic_flops(w, ctx_lengths, unabsorbed_extend=False):
     return out
 
 
+def decode_step_entry(decode_ms, steps, ws, B, G, model, hbm):
+    """Decode-step throughput (B tokens per step, all ranks) and its HBM roofline fraction.  A step's
+    algorithmic bytes are one layer pass plus the lm_head: the round's bytes without fc, over gamma."""
+    if decode_ms is None:
+        return None
+    per_step_s = decode_ms * 1e-3 / (steps * (G - 1))
+    step_bytes = (sum(b * n for k, (b, n) in model.items() if k != "fc")) / G
+    return {"ms_per_decode_step": round(per_step_s * 1e3, 4), "tokens_per_s": round(ws * B / per_step_s, 2),
+            "algo_bytes": int(step_bytes), "achieved_gbs": round(step_bytes / per_step_s / 1e9, 1),
+            "hbm_frac": round(step_bytes / per_step_s / 1e9 / hbm, 4),
+            "note": "gamma - 1 decode steps per decode call, replayed from one CUDA graph; includes the "
+                    "first token's remap launch"}
+
+
 # --------------------------------------------------------------------------------------------- our arm
 def run_ours(args, ws, rank, local):
     import numpy as np
@@ -358,6 +372,40 @@ def run_ours(args, ws, rank, local):
     launches += args.steps  # one acceptance launch per round
     assert head.error_word() == 0
     del graph
+
+    # ---------------------------------------------------------------- decode steps alone
+    # The same head after one extend, replaying decode(gamma) calls (gamma - 1 decode steps each, plus
+    # the first token's remap) with the cache length rewound before each call.
+    decode_ms = None
+    if G > 1:
+        cache.lengths.copy_(len0)
+        head.extend(din, cache, stream=stream)
+        torch.cuda.synchronize()
+        len1 = cache.lengths.clone()
+
+        def dstep(st):
+            cache.lengths.copy_(len1)
+            head.decode(G, d2t_dev, cache, toks, stream=st)
+
+        for _ in range(args.warmup):
+            dstep(stream)
+        torch.cuda.synchronize()
+        gd = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gd):
+            cap = torch.cuda.current_stream()
+            for _ in range(args.steps):
+                dstep(cap)
+        gd.replay()
+        torch.cuda.synchronize()
+        barrier(ws)
+        ev0.record(stream)
+        gd.replay()
+        ev1.record(stream)
+        torch.cuda.synchronize()
+        barrier(ws)
+        decode_ms = reduce_max(ev0.elapsed_time(ev1), ws)
+        assert head.error_word() == 0
+        del gd
 
     # ---------------------------------------------------------------- end to end, host buffers
     e2e_steps = args.e2e_steps or max(3, args.steps)
@@ -457,6 +505,7 @@ def run_ours(args, ws, rank, local):
                       "algo_flops_per_launch": int(dom_flops),
                       "tensor_frac": round(achieved_tf / tpeak, 4),
                       "peak_source": f"{src} ({'MEASURED_PEAKS.json hbm_gbs' if src == 'measured' else 'fallback 6.8 TB/s'})"}),
+        "decode_step": decode_step_entry(decode_ms, args.steps, ws, B, G, model, hbm),
         "step_roofline": {"algo_bytes": int(round_bytes), "achieved_gbs": round(round_bytes / step_s / 1e9, 1),
                           "frac": round(round_bytes / step_s / 1e9 / hbm, 4),
                           "algo_flops": int(round_flops),
