@@ -358,3 +358,39 @@ def accept(draft, target):
     for k in acc:
         hist[k] += 1
     return acc, hist
+
+
+def accept_relaxed(draft, topk_ids, topk_logprobs, in_thinking, delta):
+    """Relaxed acceptance inside thinking blocks ([MAX-walkthrough] §10: use_relaxed_acceptance_for_
+    thinking with relaxed_topk and relaxed_delta; §8: the per-row in_thinking_phase flag).
+
+    Reading of the pages: a row in its thinking phase accepts a drafted token when it is one of the
+    target's top-k candidates whose log-probability is at least the best candidate's minus delta; a row
+    outside it accepts only the target's best candidate (the greedy rule; among equal best
+    log-probabilities the first listed wins).  The accepted length counts leading accepted positions.
+    draft [B, G]; topk_ids, topk_logprobs [B, G, k]; in_thinking [B] (bool).  Returns (acc, hist) like
+    ``accept``."""
+    draft = np.asarray(draft)
+    ids = np.asarray(topk_ids)
+    lp = np.asarray(topk_logprobs, dtype=np.float64)
+    think = np.asarray(in_thinking, dtype=bool)
+    B, G = draft.shape
+    K = ids.shape[2]
+
+    def matches(b, i):
+        best = max(lp[b, i, j] for j in range(K))
+        if not think[b]:
+            first = min(j for j in range(K) if lp[b, i, j] == best)
+            return draft[b, i] == ids[b, i, first]
+        return any(ids[b, i, j] == draft[b, i] and lp[b, i, j] >= best - delta for j in range(K))
+
+    acc = np.zeros(B, dtype=np.int32)
+    for b in range(B):
+        k = 0
+        while k < G and matches(b, k):
+            k += 1
+        acc[b] = k
+    hist = np.zeros(G + 1, dtype=np.int32)
+    for k in acc:
+        hist[k] += 1
+    return acc, hist

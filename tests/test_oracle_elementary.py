@@ -264,3 +264,64 @@ def test_accept_cases_and_brute_force():
         k = next((i for i in range(6) if d[b, i] != t[b, i]), 6)
         assert acc[b] == k
     assert list(hist) == [int((acc == k).sum()) for k in range(7)]
+
+
+def _sorted_topk(rng, B, G, K, vocab):
+    """Distinct candidate ids per position with strictly descending log-probabilities."""
+    ids = np.stack([np.stack([rng.choice(vocab, size=K, replace=False) for _ in range(G)]) for _ in range(B)])
+    gaps = rng.uniform(0.05, 0.5, size=(B, G, K))
+    lp = -np.cumsum(gaps, axis=2)
+    return ids.astype(np.int32), lp
+
+
+def test_accept_relaxed_hand_example():
+    # one position, candidates 5, 9, 2 with log-probabilities -0.1, -0.5, -0.8; default delta 0.6
+    ids = np.array([[[5, 9, 2]]])
+    lp = np.array([[[-0.1, -0.5, -0.8]]])
+    for tok, think, want in [(5, False, 1), (9, False, 0), (9, True, 1), (2, True, 0), (7, True, 0), (5, True, 1)]:
+        acc, _ = O.accept_relaxed(np.array([[tok]]), ids, lp, [think], 0.6)
+        assert acc[0] == want, (tok, think)
+
+
+def test_accept_relaxed_reduces_to_greedy():
+    rng = np.random.default_rng(11)
+    B, G, K = 30, 5, 4
+    ids, lp = _sorted_topk(rng, B, G, K, 12)
+    # drafts: mostly the best candidate, sometimes another candidate or an outside token
+    draft = ids[:, :, 0].copy()
+    pick = rng.integers(0, 3, size=(B, G))
+    draft[pick == 1] = ids[:, :, 1][pick == 1]
+    draft[pick == 2] = 99
+    greedy, ghist = O.accept(draft, ids[:, :, 0])
+    # rows outside thinking follow the greedy rule whatever delta is
+    acc, hist = O.accept_relaxed(draft, ids, lp, np.zeros(B, bool), 5.0)
+    np.testing.assert_array_equal(acc, greedy)
+    np.testing.assert_array_equal(hist, ghist)
+    # a delta below every log-probability gap, or a single candidate, is greedy too
+    acc, _ = O.accept_relaxed(draft, ids, lp, np.ones(B, bool), 0.01)
+    np.testing.assert_array_equal(acc, greedy)
+    acc, _ = O.accept_relaxed(draft, ids[:, :, :1], lp[:, :, :1], np.ones(B, bool), 5.0)
+    np.testing.assert_array_equal(acc, greedy)
+    # a delta above every gap accepts any listed candidate
+    acc, _ = O.accept_relaxed(draft, ids, lp, np.ones(B, bool), 100.0)
+    for b in range(B):
+        k = 0
+        while k < G and draft[b, k] != 99:
+            k += 1
+        assert acc[b] == k
+
+
+def test_accept_relaxed_monotone_in_delta():
+    rng = np.random.default_rng(12)
+    B, G, K = 40, 6, 5
+    ids, lp = _sorted_topk(rng, B, G, K, 10)
+    draft = np.where(rng.random((B, G)) < 0.8, ids[np.arange(B)[:, None], np.arange(G)[None, :],
+                                                     rng.integers(0, K, size=(B, G))], 77)
+    think = rng.random(B) < 0.5
+    prev = None
+    for delta in [0.0, 0.1, 0.3, 0.6, 1.0, 3.0]:
+        acc, hist = O.accept_relaxed(draft, ids, lp, think, delta)
+        assert hist.sum() == B
+        if prev is not None:
+            assert np.all(acc >= prev)
+        prev = acc
