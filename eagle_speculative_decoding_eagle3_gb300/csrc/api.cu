@@ -818,6 +818,16 @@ eagle3_status_t eagle3_accept(const int32_t* draft, const int32_t* target, int32
     return EAGLE3_OK;
 }
 
+eagle3_status_t eagle3_accept_relaxed(const int32_t* draft, const int32_t* topk_ids, const float* topk_logprobs,
+                                      const uint8_t* in_thinking, int32_t batch, int32_t gamma, int32_t k, float delta,
+                                      int32_t* accepted_len, int32_t* hist, void* stream) {
+    if (!draft || !topk_ids || !topk_logprobs || !accepted_len) return EAGLE3_ERR_INVALID_ARG;
+    if (batch < 1 || gamma < 1 || gamma > 4096 || k < 1 || k > 1024 || !(delta >= 0.f)) return EAGLE3_ERR_INVALID_ARG;
+    E3_CUDA(launch_accept_relaxed(draft, topk_ids, topk_logprobs, in_thinking, batch, gamma, k, delta, accepted_len,
+                                  hist, (cudaStream_t)stream));
+    return EAGLE3_OK;
+}
+
 eagle3_status_t eagle3_draft_get_error(eagle3_draft_t* d, int32_t* device_error) {
     if (!d || !device_error) return EAGLE3_ERR_INVALID_ARG;
     E3_CUDA(cudaDeviceSynchronize());

@@ -83,6 +83,8 @@ cudaError_t launch_emit_first(int batch, const int* d0, const int* d2t, int Vt, 
 
 cudaError_t launch_accept(const int* draft, const int* target, int batch, int gamma, int* acc, int* hist,
                           cudaStream_t st);
+cudaError_t launch_accept_relaxed(const int* draft, const int* ids, const float* lp, const unsigned char* think,
+                                  int batch, int gamma, int k, float delta, int* acc, int* hist, cudaStream_t st);
 
 // ---------------------------------------------------------------- causal attention of a long extend
 // (unabsorbed; DeepseekV3 geometry d_n 128, d_r 64, d_v 128)

@@ -341,6 +341,47 @@ accept_kernel(const int* draft, const int* target, int batch, int gamma, int* ac
         for (int k = threadIdx.x; k <= gamma; k += blockDim.x) hist[k] = sh[k];
 }
 
+// Relaxed acceptance ("Eagle3 DeepseekV3 in MAX" §10: use_relaxed_acceptance_for_thinking, relaxed_topk,
+// relaxed_delta; §8: the per-row in_thinking_phase flag).  Position i of a thinking row accepts a draft
+// token listed among the target's k candidates with log-probability >= the best candidate's - delta;
+// other rows accept only the best candidate (the first listed among equal best).  One thread per row.
+__global__ void __launch_bounds__(kRowThreads)
+accept_relaxed_kernel(const int* draft, const int* ids, const float* lp, const unsigned char* think, int batch,
+                      int gamma, int k, float delta, int* acc, int* hist) {
+    pdl_trigger();
+    pdl_wait();
+    extern __shared__ int sh[];
+    for (int j = threadIdx.x; j <= gamma; j += blockDim.x) sh[j] = 0;
+    __syncthreads();
+    for (int b = threadIdx.x; b < batch; b += blockDim.x) {
+        const bool relaxed = think != nullptr && think[b] != 0;
+        int n = 0;
+        for (; n < gamma; ++n) {
+            const long pos = (long)b * gamma + n;
+            const int* ci = ids + pos * k;
+            const float* cl = lp + pos * k;
+            const int tok = draft[pos];
+            float best = cl[0];
+            int first = 0;
+            for (int j = 1; j < k; ++j)
+                if (cl[j] > best) { best = cl[j]; first = j; }
+            bool ok;
+            if (!relaxed) {
+                ok = tok == ci[first];
+            } else {
+                ok = false;
+                for (int j = 0; j < k; ++j) ok = ok || (ci[j] == tok && cl[j] >= best - delta);
+            }
+            if (!ok) break;
+        }
+        acc[b] = n;
+        if (hist) atomicAdd(&sh[n], 1);
+    }
+    __syncthreads();
+    if (hist)
+        for (int j = threadIdx.x; j <= gamma; j += blockDim.x) hist[j] = sh[j];
+}
+
 // ------------------------------------------------------------------------------------------ launchers
 cudaError_t launch_embed_norms(const RowArgs& a, bool decode, int M, const int* tokens, const int* positions,
                                const int* row_offsets, int batch, const int* tok_in, const int* lengths,
@@ -403,6 +444,13 @@ cudaError_t launch_emit_first(int batch, const int* d0, const int* d2t, int Vt, 
 cudaError_t launch_accept(const int* draft, const int* target, int batch, int gamma, int* acc, int* hist,
                           cudaStream_t st) {
     launch_pdl(accept_kernel, dim3(1), dim3(kRowThreads), (gamma + 1) * sizeof(int), st, draft, target, batch, gamma, acc, hist);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_accept_relaxed(const int* draft, const int* ids, const float* lp, const unsigned char* think,
+                                  int batch, int gamma, int k, float delta, int* acc, int* hist, cudaStream_t st) {
+    launch_pdl(accept_relaxed_kernel, dim3(1), dim3(kRowThreads), (gamma + 1) * sizeof(int), st, draft, ids, lp, think,
+               batch, gamma, k, delta, acc, hist);
     return cudaGetLastError();
 }
 

@@ -68,6 +68,7 @@ def _lib():
                                             P, P, P]
         lib.eagle3_draft_decode.argtypes = [P, C.c_int32, P, C.POINTER(eagle3_kv_t), P, P, P, P]
         lib.eagle3_accept.argtypes = [P, P, C.c_int32, C.c_int32, P, P, P]
+        lib.eagle3_accept_relaxed.argtypes = [P, P, P, P, C.c_int32, C.c_int32, C.c_int32, C.c_float, P, P, P]
         lib.eagle3_linear.argtypes = [P, P, P, P, C.c_int32, C.c_int32, C.c_int32, P]
         lib.eagle3_linear_noalloc.argtypes = [P, P, P, C.c_int32, C.c_int32, C.c_int32, P]
         lib.eagle3_draft_get_error.argtypes = [P, C.POINTER(C.c_int32)]
@@ -79,7 +80,7 @@ def _lib():
         lib.eagle3_draft_profile_reset.argtypes = [P]
         for f in ("eagle3_draft_profile_enable", "eagle3_draft_profile_read", "eagle3_draft_profile_reset",
                   "eagle3_draft_create", "eagle3_draft_workspace_bytes", "eagle3_draft_extend", "eagle3_draft_decode",
-                  "eagle3_accept", "eagle3_linear", "eagle3_linear_noalloc", "eagle3_draft_get_error", "eagle3_draft_clear_error", "eagle3_draft_destroy"):
+                  "eagle3_accept", "eagle3_accept_relaxed", "eagle3_linear", "eagle3_linear_noalloc", "eagle3_draft_get_error", "eagle3_draft_clear_error", "eagle3_draft_destroy"):
             getattr(lib, f).restype = C.c_int
         _L = lib
     return _L
@@ -177,6 +178,13 @@ def eagle3_linear_noalloc(x, w, y, M, N, K, stream=None):
 def eagle3_accept(draft, target, batch, gamma, accepted_len, hist=None, stream=None):
     _check("eagle3_accept", _lib().eagle3_accept(_ptr(draft), _ptr(target), int(batch), int(gamma),
                                                  _ptr(accepted_len), _ptr(hist), _stream(stream)))
+
+
+def eagle3_accept_relaxed(draft, topk_ids, topk_logprobs, in_thinking, batch, gamma, k, delta, accepted_len,
+                          hist=None, stream=None):
+    _check("eagle3_accept_relaxed", _lib().eagle3_accept_relaxed(
+        _ptr(draft), _ptr(topk_ids), _ptr(topk_logprobs), _ptr(in_thinking), int(batch), int(gamma), int(k),
+        float(delta), _ptr(accepted_len), _ptr(hist), _stream(stream)))
 
 
 def eagle3_draft_get_error(handle) -> int:

@@ -224,6 +224,25 @@ EAGLE3_API eagle3_status_t eagle3_linear_noalloc(const void *x, const void *w, f
 EAGLE3_API eagle3_status_t eagle3_accept(const int32_t *draft, const int32_t *target, int32_t batch,
                               int32_t gamma, int32_t *accepted_len, int32_t *hist, void *stream);
 
+/* Relaxed acceptance inside thinking blocks ("Eagle3 DeepseekV3 in MAX" §10: use_relaxed_acceptance_for_
+ * thinking with relaxed_topk (default 10) and relaxed_delta (default 0.6); §8: the per-row
+ * in_thinking_phase flag).  For each position i of sequence b the target supplies its k candidate
+ * tokens and their log-probabilities.  A row whose in_thinking flag is set accepts the drafted token when
+ * it is one of the candidates with log-probability >= the best candidate's log-probability - delta
+ * (formed in fp32); every other row accepts only the best candidate (the first listed among equal best).
+ * accepted_len[b] = number of leading accepted positions (0..gamma).
+ *   draft           [batch, gamma] int32
+ *   topk_ids        [batch, gamma, k] int32
+ *   topk_logprobs   [batch, gamma, k] fp32
+ *   in_thinking     [batch] uint8 (non-zero = thinking) or NULL (no row is thinking: the greedy rule)
+ *   accepted_len    [batch] int32 out; hist [gamma + 1] int32 out or NULL, as in eagle3_accept
+ * All device pointers; no handle needed.  Returns EAGLE3_ERR_INVALID_ARG for null required pointers,
+ * batch or gamma < 1, k < 1 or k > 1024, or a negative delta. */
+EAGLE3_API eagle3_status_t eagle3_accept_relaxed(const int32_t *draft, const int32_t *topk_ids,
+                                                 const float *topk_logprobs, const uint8_t *in_thinking,
+                                                 int32_t batch, int32_t gamma, int32_t k, float delta,
+                                                 int32_t *accepted_len, int32_t *hist, void *stream);
+
 /* Read the sticky device error word (synchronises the device).  *device_error (host) receives
  * the EAGLE3_DEVERR_* bits; returns EAGLE3_ERR_DEVICE_RANGE when any bit is set. */
 EAGLE3_API eagle3_status_t eagle3_draft_get_error(eagle3_draft_t *d, int32_t *device_error);

@@ -369,10 +369,12 @@ def accept_relaxed(draft, topk_ids, topk_logprobs, in_thinking, delta):
     outside it accepts only the target's best candidate (the greedy rule; among equal best
     log-probabilities the first listed wins).  The accepted length counts leading accepted positions.
     draft [B, G]; topk_ids, topk_logprobs [B, G, k]; in_thinking [B] (bool).  Returns (acc, hist) like
-    ``accept``."""
+    ``accept``.  The log-probabilities arrive in fp32 and the threshold best - delta decides an integer,
+    so it is formed and compared in fp32, as the GPU does."""
     draft = np.asarray(draft)
     ids = np.asarray(topk_ids)
-    lp = np.asarray(topk_logprobs, dtype=np.float64)
+    lp = np.asarray(topk_logprobs, dtype=np.float32)
+    delta = np.float32(delta)
     think = np.asarray(in_thinking, dtype=bool)
     B, G = draft.shape
     K = ids.shape[2]

@@ -76,3 +76,14 @@ def test_null_arguments_are_rejected_without_a_gpu(lib):
     assert lib.eagle3_draft_decode(None, 3, None, C.byref(kv), None, None, None, None) == E.ERR_INVALID_ARG
     assert lib.eagle3_accept(None, None, 1, 1, None, None, None) == E.ERR_INVALID_ARG
     assert lib.eagle3_draft_destroy(None) == E.OK
+
+
+def test_accept_relaxed_rejects_bad_arguments(lib):
+    # argument checks happen on the host before any launch
+    for kw in [dict(draft=None), dict(k=0), dict(k=2000), dict(delta=-0.1), dict(batch=0), dict(gamma=0)]:
+        args = dict(draft=16, ids=16, lp=16, think=None, batch=2, gamma=3, k=4, delta=0.6, acc=16)
+        args.update(kw)
+        with pytest.raises(E.Eagle3Error) as ei:
+            E.eagle3_accept_relaxed(args["draft"], args["ids"], args["lp"], args["think"], args["batch"],
+                                    args["gamma"], args["k"], args["delta"], args["acc"])
+        assert ei.value.status == E.ERR_INVALID_ARG, kw
