@@ -40,4 +40,5 @@ from .head import (  # noqa: F401
     F64, rms_norm, linear, silu, yarn_inv_freq, yarn_mscale, rope_cos_sin, rope_interleaved,
     softmax_scale, split_kv_b, mla_attention, decoder_rows, final_logits, argmax_lowest,
     top2_gap, d2t_remap, SeqCache, draft_extend, draft_decode_step, draft_round, accept, accept_relaxed,
+    sample_filtered, accept_residual,
 )

@@ -396,3 +396,96 @@ def accept_relaxed(draft, topk_ids, topk_logprobs, in_thinking, delta):
     for k in acc:
         hist[k] += 1
     return acc, hist
+
+
+def sample_filtered(logits, temperature, top_k, top_p, u):
+    """Sampled draft token ([MAX-walkthrough] §3.1 and §10: sampling parameters of the drafts; §8: a seed
+    counter feeds the sampler).  The uniform u in [0, 1) is an input, so both sides draw the same number.
+
+    Reading of the pages, which name the parameters but not their composition: temperature 0 is the
+    greedy argmax (lowest index among equal maxima).  Otherwise x = logits / temperature (fp32, as the
+    GPU divides); top_k > 0 keeps the top_k largest x, lower indices first among equal values; top_p < 1
+    then keeps the shortest prefix of those, in the order (x descending, index ascending), whose softmax
+    mass reaches top_p of the kept mass.  The kept tokens' softmax weights are renormalised and u picks
+    the token by inverse CDF over the kept tokens in ascending index order.
+    Returns (token, probs) with probs [V] the final distribution (zero outside the kept set)."""
+    l = np.asarray(logits, dtype=np.float32)
+    V = l.shape[0]
+    probs = np.zeros(V, dtype=np.float64)
+    if temperature == 0.0:
+        t = int(np.flatnonzero(l == l.max())[0])
+        probs[t] = 1.0
+        return t, probs
+    x = (l / np.float32(temperature)).astype(np.float32)
+    order = sorted(range(V), key=lambda i: (-float(x[i]), i))
+    kept = order[:top_k] if top_k > 0 else order
+    m = float(x[kept[0]])
+    w = np.array([math.exp(float(x[i]) - m) for i in kept])
+    if top_p < 1.0:
+        cum, n = 0.0, 0
+        total = w.sum()
+        while n < len(kept):
+            cum += w[n]
+            n += 1
+            if cum >= top_p * total:
+                break
+        kept, w = kept[:n], w[:n]
+    by_index = sorted(range(len(kept)), key=lambda j: kept[j])
+    total = w.sum()
+    cum, token = 0.0, kept[by_index[-1]]
+    for j in by_index:
+        cum += w[j]
+        if u * total < cum:
+            token = kept[j]
+            break
+    for j, i in enumerate(kept):
+        probs[i] = w[j] / total
+    return int(token), probs
+
+
+def accept_residual(draft, draft_probs, target_probs, u_accept, u_resample):
+    """Residual (rejection-sampling) acceptance ([MAX-walkthrough] §10: the residual strategy of
+    --rejection-sampling-strategy).  The speculative-sampling rule: position i accepts its drafted
+    token x with probability min(1, p_i(x) / q_i(x)), tested as u_accept[b, i] * q_i(x) < p_i(x); the
+    first rejected position instead emits a token drawn from the residual max(0, p_i - q_i),
+    renormalised, by inverse CDF in ascending token order with u_resample[b, i]; if every position is
+    accepted the bonus token is drawn from p_gamma with u_resample[b, gamma - 1].
+    draft [B, G] target-vocab ids; draft_probs [B, G, V] (the drafts' final distributions mapped to
+    the target vocabulary); target_probs [B, G + 1, V].  Returns (acc [B], next_token [B], hist)."""
+    draft = np.asarray(draft)
+    q = np.asarray(draft_probs, dtype=np.float64)
+    p = np.asarray(target_probs, dtype=np.float64)
+    ua = np.asarray(u_accept, dtype=np.float64)
+    ur = np.asarray(u_resample, dtype=np.float64)
+    B, G = draft.shape
+    V = p.shape[2]
+
+    def inverse_cdf(w, u):
+        total = w.sum()
+        cum = 0.0
+        last = max(i for i in range(V) if w[i] > 0) if total > 0 else V - 1
+        for i in range(V):
+            cum += w[i]
+            if w[i] > 0 and u * total < cum:
+                return i
+        return last
+
+    acc = np.zeros(B, dtype=np.int32)
+    nxt = np.zeros(B, dtype=np.int32)
+    for b in range(B):
+        k = 0
+        while k < G:
+            x = int(draft[b, k])
+            if ua[b, k] * q[b, k, x] < p[b, k, x]:
+                k += 1
+                continue
+            break
+        acc[b] = k
+        if k < G:
+            nxt[b] = inverse_cdf(np.maximum(p[b, k] - q[b, k], 0.0), ur[b, k])
+        else:
+            nxt[b] = inverse_cdf(p[b, G], ur[b, G - 1])
+    hist = np.zeros(G + 1, dtype=np.int32)
+    for k in acc:
+        hist[k] += 1
+    return acc, nxt, hist

@@ -325,3 +325,72 @@ def test_accept_relaxed_monotone_in_delta():
         if prev is not None:
             assert np.all(acc >= prev)
         prev = acc
+
+
+def test_sample_filtered_greedy_and_top1():
+    l = np.array([0.5, 2.0, 2.0, -1.0], dtype=np.float32)
+    for T in (0.0, 0.7):
+        k = 1 if T > 0 else 0
+        for u in (0.0, 0.5, 0.999):
+            t, probs = O.sample_filtered(l, T, k, 1.0, u)
+            assert t == 1 and probs[1] == 1.0 and probs.sum() == 1.0
+
+
+def test_sample_filtered_frequencies_match_softmax():
+    # inverse-CDF sampling over a fine grid of u reproduces the renormalised softmax of the kept set
+    l = np.array([1.0, 0.2, -0.5, 1.5, 0.0, 0.7], dtype=np.float32)
+    T = 0.8
+    x = (l / np.float32(T)).astype(np.float64)
+    for top_k, top_p, keep in [(0, 1.0, [0, 1, 2, 3, 4, 5]), (3, 1.0, [3, 0, 5]), (6, 0.5, [3, 0])]:
+        w = np.zeros(6)
+        w[keep] = np.exp(x[keep] - x[keep].max())
+        want = w / w.sum()
+        n = 20000
+        counts = np.zeros(6)
+        for i in range(n):
+            t, probs = O.sample_filtered(l, T, top_k, top_p, (i + 0.5) / n)
+            counts[t] += 1
+        np.testing.assert_allclose(probs, want, rtol=1e-12, atol=1e-15)
+        np.testing.assert_allclose(counts / n, want, atol=2e-4)
+
+
+def test_sample_filtered_top_p_and_tie_order_hand_cases():
+    l = np.array([2.0, 1.0, 0.0, -1.0], dtype=np.float32)    # softmax 0.644, 0.237, 0.087, 0.032
+    for u in (0.0, 0.3, 0.99):
+        assert O.sample_filtered(l, 1.0, 4, 0.6, u)[0] == 0
+    _, probs = O.sample_filtered(l, 1.0, 4, 0.7, 0.5)
+    np.testing.assert_array_equal(probs > 0, [True, True, False, False])
+    # equal logits at the top-k boundary: lower indices are kept first
+    _, probs = O.sample_filtered(np.array([1.0, 3.0, 3.0, 3.0, 0.0], np.float32), 1.0, 2, 1.0, 0.5)
+    np.testing.assert_array_equal(probs > 0, [False, True, True, False, False])
+
+
+def test_accept_residual_emits_the_target_distribution():
+    # the speculative-sampling theorem: the token emitted at a position (the accepted draft, or the
+    # residual draw after a rejection) is distributed as the target's p, whatever the draft's q
+    rng = np.random.default_rng(13)
+    V = 5
+    q = rng.dirichlet(np.ones(V))
+    p = rng.dirichlet(np.ones(V))
+    n = 400
+    out = np.zeros(V)
+    for x in range(V):                       # the draft token, drawn from q
+        for ia in range(n):                  # u_accept grid
+            for ir in range(0, n, 8):        # u_resample grid (coarser)
+                ua, ur = (ia + 0.5) / n, (ir + 4) / n
+                acc, nxt, _ = O.accept_residual([[x]], q[None, None, :], np.stack([p, p])[None], [[ua]], [[ur]])
+                tok = x if acc[0] == 1 else nxt[0]
+                out[tok] += q[x] / (n * (n // 8))
+    np.testing.assert_allclose(out, p, atol=4e-3)
+
+
+def test_accept_residual_special_cases():
+    p = np.array([[[0.1, 0.6, 0.3], [0.2, 0.2, 0.6], [0.5, 0.25, 0.25]]])
+    # a draft distribution equal to the target's is always accepted; the bonus comes from p[gamma]
+    acc, nxt, hist = O.accept_residual([[1, 2]], p[:, :2], p, [[0.999, 0.999]], [[0.1, 0.7]])
+    assert acc[0] == 2 and nxt[0] == 1 and hist[2] == 1
+    # a drafted token the target gives no mass is rejected; the residual excludes it
+    q = np.array([[[0.0, 0.0, 1.0], [1.0, 0.0, 0.0]]])
+    p0 = np.array([[[0.5, 0.5, 0.0], [1.0, 0.0, 0.0], [1.0, 0.0, 0.0]]])
+    acc, nxt, _ = O.accept_residual([[2, 0]], q, p0, [[0.0, 0.0]], [[0.75, 0.0]])
+    assert acc[0] == 0 and nxt[0] == 1
