@@ -828,6 +828,49 @@ eagle3_status_t eagle3_accept_relaxed(const int32_t* draft, const int32_t* topk_
     return EAGLE3_OK;
 }
 
+namespace {
+bool sampling_ok(const eagle3_sampling_t* p) {
+    return p && p->temperature >= 0.f && p->top_k >= 0 && p->top_k <= 1024 && p->top_p > 0.f && p->top_p <= 1.f &&
+           !(p->temperature > 0.f && p->top_k == 0 && p->top_p < 1.f);
+}
+}  // namespace
+
+eagle3_status_t eagle3_sample(const float* logits, int32_t rows, int32_t V, int64_t ld,
+                              const eagle3_sampling_t* params, const float* uniforms, const int32_t* d2t,
+                              int32_t target_vocab, int32_t* tokens, float* token_prob, float* probs,
+                              int32_t probs_len, int32_t probs_in_target, void* stream) {
+    if (!logits || !uniforms || !tokens || rows < 1 || V < 1 || ld < V || !sampling_ok(params))
+        return EAGLE3_ERR_INVALID_ARG;
+    if (d2t && target_vocab < 1) return EAGLE3_ERR_INVALID_ARG;
+    if (probs && probs_len < (probs_in_target && d2t ? target_vocab : V)) return EAGLE3_ERR_INVALID_ARG;
+    SampleArgs sa;
+    memset(&sa, 0, sizeof(sa));
+    sa.logits = logits; sa.ldl = ld; sa.rows = rows; sa.V = V;
+    sa.temperature = params->temperature; sa.top_k = params->top_k; sa.top_p = params->top_p;
+    sa.uniforms = uniforms; sa.d2t = d2t; sa.target_vocab = d2t ? target_vocab : V;
+    sa.tokens = tokens; sa.token_prob = token_prob;
+    sa.probs = probs; sa.ldp = probs_len; sa.probs_len = probs_len; sa.probs_target = probs_in_target ? 1 : 0;
+    sa.err = nullptr;
+    E3_CUDA(launch_sample(sa, (cudaStream_t)stream));
+    return EAGLE3_OK;
+}
+
+eagle3_status_t eagle3_accept_residual(const int32_t* draft, const float* draft_probs, const float* target_probs,
+                                       const float* u_accept, const float* u_resample, int32_t batch, int32_t gamma,
+                                       int32_t V, int32_t* accepted_len, int32_t* next_token, int32_t* hist,
+                                       void* stream) {
+    if (!draft || !draft_probs || !target_probs || !u_accept || !u_resample || !accepted_len || !next_token)
+        return EAGLE3_ERR_INVALID_ARG;
+    if (batch < 1 || gamma < 1 || gamma > 4096 || V < 1) return EAGLE3_ERR_INVALID_ARG;
+    ResidualArgs ra;
+    memset(&ra, 0, sizeof(ra));
+    ra.draft = draft; ra.draft_probs = draft_probs; ra.target_probs = target_probs;
+    ra.u_accept = u_accept; ra.u_resample = u_resample; ra.batch = batch; ra.gamma = gamma; ra.V = V;
+    ra.accepted_len = accepted_len; ra.next_token = next_token; ra.hist = hist;
+    E3_CUDA(launch_accept_residual(ra, (cudaStream_t)stream));
+    return EAGLE3_OK;
+}
+
 eagle3_status_t eagle3_draft_get_error(eagle3_draft_t* d, int32_t* device_error) {
     if (!d || !device_error) return EAGLE3_ERR_INVALID_ARG;
     E3_CUDA(cudaDeviceSynchronize());

@@ -86,6 +86,39 @@ cudaError_t launch_accept(const int* draft, const int* target, int batch, int ga
 cudaError_t launch_accept_relaxed(const int* draft, const int* ids, const float* lp, const unsigned char* think,
                                   int batch, int gamma, int k, float delta, int* acc, int* hist, cudaStream_t st);
 
+// ---------------------------------------------------------------- sampled drafts, residual acceptance
+struct SampleArgs {
+    const float* logits; long ldl;     // [rows, V] draft-vocabulary logits
+    int rows, V;
+    float temperature;                 // 0: greedy argmax
+    int top_k;                         // 0: whole vocabulary (top_p must then be 1); else 1..1024
+    float top_p;                       // (0, 1]
+    const float* uniforms;             // [rows] in [0, 1)
+    const int* d2t;                    // [V] additive draft-to-target map or null
+    int target_vocab;
+    int* tokens;                       // [rows] out: target-vocabulary ids
+    int* tokens2; long tok2_stride;    // optional second copy of the ids, row r at r * tok2_stride
+    int* draft_ids;                    // [rows] out (optional): draft-vocabulary ids
+    float* token_prob;                 // [rows] out (optional): the sampled token's final probability
+    float* probs; long ldp;            // [rows, probs_len] out (optional): final distribution
+    int probs_len;
+    int probs_target;                  // probs indexed by target ids (through d2t) instead of draft ids
+    int* err;
+};
+struct ResidualArgs {
+    const int* draft;                  // [B, gamma] target-vocabulary ids
+    const float* draft_probs;          // [B, gamma, V] draft distributions over the target vocabulary
+    const float* target_probs;         // [B, gamma + 1, V]
+    const float* u_accept;             // [B, gamma]
+    const float* u_resample;           // [B, gamma]
+    int batch, gamma, V;
+    int* accepted_len;                 // [B]
+    int* next_token;                   // [B] the token emitted after the accepted prefix
+    int* hist;                         // [gamma + 1] or null
+};
+cudaError_t launch_sample(const SampleArgs& s, cudaStream_t st);
+cudaError_t launch_accept_residual(const ResidualArgs& a, cudaStream_t st);
+
 // ---------------------------------------------------------------- causal attention of a long extend
 // (unabsorbed; DeepseekV3 geometry d_n 128, d_r 64, d_v 128)
 struct PrefillArgs {

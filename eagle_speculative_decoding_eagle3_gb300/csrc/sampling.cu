@@ -1,0 +1,401 @@
+// Sampled drafts and residual (rejection-sampling) acceptance.
+//
+// "Eagle3 DeepseekV3 in MAX" §3.1 and §10 name the sampling parameters of the drafts (temperature,
+// top-k, top-p) and the rejection-sampling strategies (greedy, residual, ...), and §8 a seed counter
+// that feeds the sampler.  Here the uniform random numbers are inputs, so a caller (or a test) draws
+// them once and every consumer uses the same ones.
+//
+// sample_kernel: one CTA of kThreads per row.  x = logits / temperature (fp32 division); top_k keeps the
+// top_k largest x (lower indices first among equal values) found by a radix select on the order-
+// preserving integer image of x; the kept tokens are sorted (x descending, index ascending) by a bitonic
+// sort in shared memory; top_p keeps the shortest prefix whose softmax mass reaches top_p of the kept
+// mass; the kept weights are renormalised and u picks the token by inverse CDF in ascending index order.
+// temperature 0 is the greedy argmax.  Without top_k the whole vocabulary is kept (top_p must be 1) and
+// the inverse CDF runs over it with a block-wide scan.
+//
+// accept_residual_kernel: one CTA per sequence; the speculative-sampling rule (accept x with
+// probability min(1, p(x) / q(x)); at the first rejection draw from max(0, p - q) renormalised; after
+// gamma acceptances draw the bonus token from the target's next distribution).
+#include <float.h>
+#include <math.h>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace e3 {
+
+namespace smp {
+constexpr int kThreads = 1024;
+constexpr int kMaxTopK = 1024;
+}  // namespace smp
+
+// order-preserving image of a float: larger floats give larger unsigned keys
+__device__ __forceinline__ uint32_t fkey(float x) {
+    const uint32_t b = __float_as_uint(x);
+    return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+
+// inclusive block scan of one float per thread (kThreads threads); returns the thread's inclusive sum
+__device__ float block_inclusive_scan(float v, float* warp_tot) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const float n = __shfl_up_sync(0xffffffffu, v, o);
+        if (lane >= o) v += n;
+    }
+    __syncthreads();
+    if (lane == 31) warp_tot[warp] = v;
+    __syncthreads();
+    if (warp == 0) {
+        float t = lane < (int)(blockDim.x >> 5) ? warp_tot[lane] : 0.f;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const float n = __shfl_up_sync(0xffffffffu, t, o);
+            if (lane >= o) t += n;
+        }
+        warp_tot[lane] = t;   // inclusive totals per warp
+    }
+    __syncthreads();
+    return v + (warp > 0 ? warp_tot[warp - 1] : 0.f);
+}
+
+__device__ int block_inclusive_scan_int(int v, int* warp_tot) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int n = __shfl_up_sync(0xffffffffu, v, o);
+        if (lane >= o) v += n;
+    }
+    __syncthreads();
+    if (lane == 31) warp_tot[warp] = v;
+    __syncthreads();
+    if (warp == 0) {
+        int t = lane < (int)(blockDim.x >> 5) ? warp_tot[lane] : 0;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int n = __shfl_up_sync(0xffffffffu, t, o);
+            if (lane >= o) t += n;
+        }
+        warp_tot[lane] = t;
+    }
+    __syncthreads();
+    return v + (warp > 0 ? warp_tot[warp - 1] : 0);
+}
+
+// bitonic sort of kThreads (key, index) pairs in shared memory, ascending by (key, index)
+__device__ void bitonic_sort(unsigned long long* a) {
+    const int t = threadIdx.x;
+    for (int k = 2; k <= smp::kThreads; k <<= 1) {
+        for (int j = k >> 1; j > 0; j >>= 1) {
+            const int p = t ^ j;
+            if (p > t) {
+                const bool up = (t & k) == 0;
+                const unsigned long long x = a[t], y = a[p];
+                if ((x > y) == up) { a[t] = y; a[p] = x; }
+            }
+            __syncthreads();
+        }
+    }
+}
+
+__global__ void __launch_bounds__(smp::kThreads) sample_kernel(SampleArgs s) {
+    using namespace smp;
+    pdl_trigger();
+    pdl_wait();
+    __shared__ unsigned long long sorted[kThreads];   // (key, index) packed; reused
+    __shared__ float wv[kThreads];
+    __shared__ int hist[256];
+    __shared__ float ftot[32];
+    __shared__ int itot[32];
+    __shared__ int sh_int[4];
+    __shared__ float sh_f[2];
+    const int r = blockIdx.x, t = threadIdx.x, V = s.V;
+    const float* l = s.logits + (long)r * s.ldl;
+    float* probs = s.probs ? s.probs + (long)r * s.ldp : nullptr;
+    const float u = s.uniforms[r];
+    int token = 0;
+    float qtok = 1.f;
+
+    if (s.temperature <= 0.f) {
+        // greedy: max with the lowest index
+        float bv = -INFINITY;
+        int bi = INT_MAX;
+        for (int i = t; i < V; i += kThreads)
+            if (l[i] > bv) { bv = l[i]; bi = i; }
+        for (int o = 16; o > 0; o >>= 1) {
+            const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+            const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+            if (ov > bv || (ov == bv && oi < bi)) { bv = ov; bi = oi; }
+        }
+        if ((t & 31) == 0) { wv[t >> 5] = bv; sorted[t >> 5] = (unsigned long long)bi; }
+        __syncthreads();
+        if (t == 0) {
+            float b = wv[0];
+            int bidx = (int)sorted[0];
+            for (int w = 1; w < kThreads / 32; ++w)
+                if (wv[w] > b || (wv[w] == b && (int)sorted[w] < bidx)) { b = wv[w]; bidx = (int)sorted[w]; }
+            sh_int[0] = bidx;
+        }
+        __syncthreads();
+        token = sh_int[0];
+        if (probs) {
+            const int o = s.probs_target && s.d2t ? token + s.d2t[token] : token;
+            for (int i = t; i < s.probs_len; i += kThreads) probs[i] = i == o ? 1.f : 0.f;
+        }
+    } else if (s.top_k <= 0) {
+        // whole vocabulary: softmax and inverse CDF in index order
+        const float T = s.temperature;
+        float m = -INFINITY;
+        for (int i = t; i < V; i += kThreads) m = fmaxf(m, l[i] / T);
+        m = warp_max(m);
+        if ((t & 31) == 0) wv[t >> 5] = m;
+        __syncthreads();
+        if (t < 32) {
+            float mm = wv[t];
+            mm = warp_max(mm);
+            if (t == 0) sh_f[0] = mm;
+        }
+        __syncthreads();
+        m = sh_f[0];
+        // contiguous segment per thread, so the block scan follows the index order
+        const int seg = (V + kThreads - 1) / kThreads, i0 = t * seg, i1 = min(V, i0 + seg);
+        float part = 0.f;
+        for (int i = i0; i < i1; ++i) part += __expf(l[i] / T - m);
+        const float incl = block_inclusive_scan(part, ftot);
+        const float total = ftot[kThreads / 32 - 1];
+        const float target = u * total;
+        float cum = incl - part;
+        int found = -1;
+        if (cum <= target && target < incl) {
+            for (int i = i0; i < i1; ++i) {
+                cum += __expf(l[i] / T - m);
+                if (target < cum) { found = i; break; }
+            }
+            if (found < 0) found = i1 - 1;
+        }
+        if (t == 0) sh_int[0] = V - 1;   // u rounding past the total: the last token
+        __syncthreads();
+        if (found >= 0) sh_int[0] = found;
+        __syncthreads();
+        token = sh_int[0];
+        qtok = __expf(l[token] / T - m) / total;
+        if (probs) {
+            if (s.probs_target && s.d2t) {
+                for (int i = t; i < s.probs_len; i += kThreads) probs[i] = 0.f;
+                __syncthreads();
+            }
+            for (int i = t; i < V; i += kThreads) {
+                const int o = s.probs_target && s.d2t ? i + s.d2t[i] : i;
+                if (o >= 0 && o < s.probs_len) probs[o] = __expf(l[i] / T - m) / total;
+            }
+        }
+    } else {
+        const float T = s.temperature;
+        const int K = min(s.top_k, min(kMaxTopK, V));
+        // radix select of the K-th largest key, 8 bits at a time from the top
+        uint32_t prefix = 0, pmask = 0;
+        int need = K;
+        for (int shift = 24; shift >= 0; shift -= 8) {
+            for (int i = t; i < 256; i += kThreads) hist[i] = 0;
+            __syncthreads();
+            for (int i = t; i < V; i += kThreads) {
+                const uint32_t k = fkey(l[i] / T);
+                if ((k & pmask) == prefix) atomicAdd(&hist[(k >> shift) & 255u], 1);
+            }
+            __syncthreads();
+            if (t == 0) {
+                int acc = 0, d = 255;
+                for (; d > 0; --d) {
+                    if (acc + hist[d] >= need) break;
+                    acc += hist[d];
+                }
+                sh_int[0] = d;
+                sh_int[1] = acc;
+            }
+            __syncthreads();
+            prefix |= (uint32_t)sh_int[0] << shift;
+            pmask |= 255u << shift;
+            need -= sh_int[1];
+            __syncthreads();
+        }
+        const uint32_t kth = prefix;   // keys > kth are all kept; `need` of the keys == kth, lowest index first
+        // gather: keys above the threshold, then the first `need` equal keys in index order
+        if (t == 0) sh_int[2] = 0;
+        sorted[t] = ~0ull;
+        __syncthreads();
+        for (int i = t; i < V; i += kThreads) {
+            const uint32_t k = fkey(l[i] / T);
+            if (k > kth) {
+                const int slot = atomicAdd(&sh_int[2], 1);
+                sorted[slot] = ((unsigned long long)(~k) << 32) | (uint32_t)i;
+            }
+        }
+        __syncthreads();
+        int base = sh_int[2];
+        for (int c0 = 0; c0 < V && need > 0; c0 += kThreads) {
+            const int i = c0 + t;
+            const int eq = (i < V && fkey(l[i] / T) == kth) ? 1 : 0;
+            const int incl = block_inclusive_scan_int(eq, itot);
+            const int rank = incl - eq;
+            if (eq && rank < need) sorted[base + rank] = ((unsigned long long)(~kth) << 32) | (uint32_t)i;
+            const int taken = min(need, itot[kThreads / 32 - 1]);
+            base += taken;
+            need -= taken;
+            __syncthreads();
+        }
+        const int n = K;
+        // (x descending, index ascending) == (~key ascending, index ascending)
+        bitonic_sort(sorted);
+        const bool live = t < n;
+        const int idx = live ? (int)(sorted[t] & 0xffffffffu) : 0;
+        const float x0 = l[(int)(sorted[0] & 0xffffffffu)] / T;
+        const float w = live ? __expf(l[idx] / T - x0) : 0.f;
+        const float cum = block_inclusive_scan(w, ftot);
+        const float total = ftot[kThreads / 32 - 1];
+        // top-p: the shortest prefix whose mass reaches top_p of the total
+        int keep = n;
+        if (s.top_p < 1.f) {
+            if (t == 0) sh_int[3] = n;
+            __syncthreads();
+            const float lim = s.top_p * total;
+            const float prev = cum - w;
+            if (live && cum >= lim && prev < lim) sh_int[3] = t + 1;
+            __syncthreads();
+            keep = sh_int[3];
+        }
+        // inverse CDF over the kept tokens in index order
+        const bool kept = t < keep;
+        __syncthreads();
+        sorted[t] = kept ? (((unsigned long long)(uint32_t)idx << 32) | __float_as_uint(w)) : ~0ull;
+        __syncthreads();
+        bitonic_sort(sorted);
+        const bool k2 = t < keep;
+        const float w2 = k2 ? __uint_as_float((uint32_t)(sorted[t] & 0xffffffffu)) : 0.f;
+        const int i2 = k2 ? (int)(sorted[t] >> 32) : 0;
+        const float c2 = block_inclusive_scan(w2, ftot);
+        const float kept_total = ftot[kThreads / 32 - 1];
+        const float target = u * kept_total;
+        if (t == 0) {   // u rounding past the kept total: the last kept token
+            sh_int[0] = (int)(sorted[keep - 1] >> 32);
+            sh_f[1] = __uint_as_float((uint32_t)(sorted[keep - 1] & 0xffffffffu));
+        }
+        __syncthreads();
+        if (k2 && c2 - w2 <= target && target < c2) { sh_int[0] = i2; sh_f[1] = w2; }
+        __syncthreads();
+        token = sh_int[0];
+        qtok = sh_f[1] / kept_total;
+        if (probs) {
+            for (int i = t; i < s.probs_len; i += kThreads) probs[i] = 0.f;
+            __syncthreads();
+            if (k2) {
+                const int o = s.probs_target && s.d2t ? i2 + s.d2t[i2] : i2;
+                if (o >= 0 && o < s.probs_len) probs[o] = w2 / kept_total;
+            }
+        }
+    }
+    if (t == 0) {
+        int out = token;
+        if (s.d2t) {
+            out = token + s.d2t[token];
+            if (out < 0 || out >= s.target_vocab) {
+                if (s.err) set_err(s.err, 4);
+                out = out < 0 ? 0 : s.target_vocab - 1;
+            }
+        }
+        s.tokens[r] = out;
+        if (s.tokens2) s.tokens2[(long)r * s.tok2_stride] = out;
+        if (s.draft_ids) s.draft_ids[r] = token;
+        if (s.token_prob) s.token_prob[r] = qtok;
+    }
+}
+
+// Residual acceptance; one CTA per sequence.  Thread 0 walks the gamma positions (accept x while
+// u_accept * q(x) < p(x)); then the block draws the emitted token by inverse CDF in index order over the
+// residual max(0, p - q) of the first rejected position, or over p_gamma after gamma acceptances.  p and
+// q are over the target vocabulary: p [B, gamma + 1, V], q [B, gamma, V].
+__global__ void __launch_bounds__(smp::kThreads) accept_residual_kernel(ResidualArgs a) {
+    using namespace smp;
+    pdl_trigger();
+    pdl_wait();
+    __shared__ float ftot[32];
+    __shared__ int sh[2];
+    const int b = blockIdx.x, t = threadIdx.x, V = a.V, G = a.gamma;
+    if (t == 0) {
+        int k = 0;
+        for (; k < G; ++k) {
+            const long pos = (long)b * G + k;
+            const int x = a.draft[pos];
+            if (x < 0 || x >= V) break;   // an id outside the vocabulary is never accepted
+            const float qx = a.draft_probs[pos * V + x];
+            const float px = a.target_probs[((long)b * (G + 1) + k) * V + x];
+            if (!(a.u_accept[pos] * qx < px)) break;
+        }
+        sh[0] = k;
+        sh[1] = -1;
+    }
+    __syncthreads();
+    const int k = sh[0];
+    const float* p = a.target_probs + ((long)b * (G + 1) + k) * V;
+    const float* q = k < G ? a.draft_probs + ((long)b * G + k) * V : nullptr;
+    const float u = a.u_resample[(long)b * G + (k < G ? k : G - 1)];
+    const int seg = (V + kThreads - 1) / kThreads, i0 = t * seg, i1 = min(V, i0 + seg);
+    float part = 0.f;
+    int last = -1;
+    for (int i = i0; i < i1; ++i) {
+        const float w = q ? fmaxf(p[i] - q[i], 0.f) : p[i];
+        part += w;
+        if (w > 0.f) last = i;
+    }
+    const float incl = block_inclusive_scan(part, ftot);
+    const float total = ftot[kThreads / 32 - 1];
+    const float target = u * total;
+    // the last positive weight is the fallback when u * total rounds past the sum
+    if (last >= 0) atomicMax(&sh[1], last);
+    __syncthreads();
+    const int fallback = sh[1] >= 0 ? sh[1] : V - 1;
+    __syncthreads();
+    if (t == 0) sh[1] = fallback;
+    int found = -1;
+    float cum = incl - part;
+    if (cum <= target && target < incl) {
+        for (int i = i0; i < i1; ++i) {
+            const float w = q ? fmaxf(p[i] - q[i], 0.f) : p[i];
+            cum += w;
+            if (w > 0.f && target < cum) { found = i; break; }
+        }
+    }
+    __syncthreads();
+    if (found >= 0) sh[1] = found;
+    __syncthreads();
+    if (t == 0) {
+        a.accepted_len[b] = k;
+        a.next_token[b] = sh[1];
+    }
+}
+
+__global__ void acceptance_hist_kernel(const int* acc, int batch, int gamma, int* hist) {
+    pdl_trigger();
+    pdl_wait();
+    extern __shared__ int hsh[];
+    for (int k = threadIdx.x; k <= gamma; k += blockDim.x) hsh[k] = 0;
+    __syncthreads();
+    for (int b = threadIdx.x; b < batch; b += blockDim.x) atomicAdd(&hsh[min(max(acc[b], 0), gamma)], 1);
+    __syncthreads();
+    for (int k = threadIdx.x; k <= gamma; k += blockDim.x) hist[k] = hsh[k];
+}
+
+cudaError_t launch_sample(const SampleArgs& s, cudaStream_t st) {
+    if (s.V < 1 || s.rows < 1 || (s.top_k > smp::kMaxTopK) || (s.temperature > 0.f && s.top_k <= 0 && s.top_p < 1.f))
+        return cudaErrorInvalidValue;
+    return launch_pdl(sample_kernel, dim3(s.rows), dim3(smp::kThreads), 0, st, s);
+}
+
+cudaError_t launch_accept_residual(const ResidualArgs& a, cudaStream_t st) {
+    if (a.batch < 1 || a.gamma < 1 || a.V < 1) return cudaErrorInvalidValue;
+    cudaError_t e = launch_pdl(accept_residual_kernel, dim3(a.batch), dim3(smp::kThreads), 0, st, a);
+    if (e != cudaSuccess || !a.hist) return e;
+    return launch_pdl(acceptance_hist_kernel, dim3(1), dim3(256), (a.gamma + 1) * sizeof(int), st, a.accepted_len,
+                      a.batch, a.gamma, a.hist);
+}
+
+}  // namespace e3

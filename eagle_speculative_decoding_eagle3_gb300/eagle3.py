@@ -40,6 +40,10 @@ class eagle3_kv_t(C.Structure):
                 ("num_pages", C.c_int32)]
 
 
+class eagle3_sampling_t(C.Structure):
+    _fields_ = [("temperature", C.c_float), ("top_k", C.c_int32), ("top_p", C.c_float)]
+
+
 class Eagle3Error(RuntimeError):
     def __init__(self, fn, status):
         self.status = status
@@ -69,6 +73,9 @@ def _lib():
         lib.eagle3_draft_decode.argtypes = [P, C.c_int32, P, C.POINTER(eagle3_kv_t), P, P, P, P]
         lib.eagle3_accept.argtypes = [P, P, C.c_int32, C.c_int32, P, P, P]
         lib.eagle3_accept_relaxed.argtypes = [P, P, P, P, C.c_int32, C.c_int32, C.c_int32, C.c_float, P, P, P]
+        lib.eagle3_sample.argtypes = [P, C.c_int32, C.c_int32, C.c_int64, C.POINTER(eagle3_sampling_t), P, P,
+                                      C.c_int32, P, P, P, C.c_int32, C.c_int32, P]
+        lib.eagle3_accept_residual.argtypes = [P, P, P, P, P, C.c_int32, C.c_int32, C.c_int32, P, P, P, P]
         lib.eagle3_linear.argtypes = [P, P, P, P, C.c_int32, C.c_int32, C.c_int32, P]
         lib.eagle3_linear_noalloc.argtypes = [P, P, P, C.c_int32, C.c_int32, C.c_int32, P]
         lib.eagle3_draft_get_error.argtypes = [P, C.POINTER(C.c_int32)]
@@ -80,7 +87,7 @@ def _lib():
         lib.eagle3_draft_profile_reset.argtypes = [P]
         for f in ("eagle3_draft_profile_enable", "eagle3_draft_profile_read", "eagle3_draft_profile_reset",
                   "eagle3_draft_create", "eagle3_draft_workspace_bytes", "eagle3_draft_extend", "eagle3_draft_decode",
-                  "eagle3_accept", "eagle3_accept_relaxed", "eagle3_linear", "eagle3_linear_noalloc", "eagle3_draft_get_error", "eagle3_draft_clear_error", "eagle3_draft_destroy"):
+                  "eagle3_accept", "eagle3_accept_relaxed", "eagle3_sample", "eagle3_accept_residual", "eagle3_linear", "eagle3_linear_noalloc", "eagle3_draft_get_error", "eagle3_draft_clear_error", "eagle3_draft_destroy"):
             getattr(lib, f).restype = C.c_int
         _L = lib
     return _L
@@ -185,6 +192,21 @@ def eagle3_accept_relaxed(draft, topk_ids, topk_logprobs, in_thinking, batch, ga
     _check("eagle3_accept_relaxed", _lib().eagle3_accept_relaxed(
         _ptr(draft), _ptr(topk_ids), _ptr(topk_logprobs), _ptr(in_thinking), int(batch), int(gamma), int(k),
         float(delta), _ptr(accepted_len), _ptr(hist), _stream(stream)))
+
+
+def eagle3_sample(logits, rows, V, ld, temperature, top_k, top_p, uniforms, d2t, target_vocab, tokens,
+                  token_prob=None, probs=None, probs_len=0, probs_in_target=False, stream=None):
+    prm = eagle3_sampling_t(float(temperature), int(top_k), float(top_p))
+    _check("eagle3_sample", _lib().eagle3_sample(
+        _ptr(logits), int(rows), int(V), int(ld), C.byref(prm), _ptr(uniforms), _ptr(d2t), int(target_vocab),
+        _ptr(tokens), _ptr(token_prob), _ptr(probs), int(probs_len), int(bool(probs_in_target)), _stream(stream)))
+
+
+def eagle3_accept_residual(draft, draft_probs, target_probs, u_accept, u_resample, batch, gamma, V, accepted_len,
+                           next_token, hist=None, stream=None):
+    _check("eagle3_accept_residual", _lib().eagle3_accept_residual(
+        _ptr(draft), _ptr(draft_probs), _ptr(target_probs), _ptr(u_accept), _ptr(u_resample), int(batch),
+        int(gamma), int(V), _ptr(accepted_len), _ptr(next_token), _ptr(hist), _stream(stream)))
 
 
 def eagle3_draft_get_error(handle) -> int:

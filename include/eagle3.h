@@ -243,6 +243,52 @@ EAGLE3_API eagle3_status_t eagle3_accept_relaxed(const int32_t *draft, const int
                                                  int32_t batch, int32_t gamma, int32_t k, float delta,
                                                  int32_t *accepted_len, int32_t *hist, void *stream);
 
+/* ---- Sampled drafts and residual acceptance ("Eagle3 DeepseekV3 in MAX" §3.1, §10: the sampling
+ * parameters of the drafts and the rejection-sampling strategies; §8: a seed counter feeds the sampler).
+ * The uniform random numbers are inputs (device arrays in [0, 1)), so every consumer of a draw sees the
+ * same number. */
+typedef struct {
+    float temperature;   /* 0: greedy argmax (lowest index among equal maxima) */
+    int32_t top_k;       /* 0: the whole vocabulary (top_p must then be 1); else 1..1024 */
+    float top_p;         /* (0, 1]: keep the shortest prefix of the top_k tokens, by probability, whose mass
+                            reaches top_p of their total */
+} eagle3_sampling_t;
+
+/* Draw one token per row from filtered logits: x = logits / temperature (fp32); keep the top_k largest x
+ * (lower indices first among equal values), then the top_p prefix in the order (x descending, index
+ * ascending); renormalise the kept softmax weights and pick by inverse CDF over the kept tokens in
+ * ascending index order with uniforms[r].
+ *   logits       [rows, ld] fp32, the first V entries of each row are the draft-vocabulary logits
+ *   uniforms     [rows] fp32
+ *   d2t          [V] int32 additive draft-to-target map or NULL (tokens are then draft ids)
+ *   tokens       [rows] int32 out, target-vocabulary ids
+ *   token_prob   [rows] fp32 out or NULL: the drawn token's final probability
+ *   probs        [rows, probs_len] fp32 out or NULL: the final distribution, indexed by target ids when
+ *                probs_in_target is non-zero (zeros elsewhere), else by draft ids
+ * One CTA per row.  Returns EAGLE3_ERR_INVALID_ARG for null required pointers, rows or V < 1, ld < V,
+ * top_k outside 0..1024, top_p outside (0, 1], top_p < 1 without top_k, or a negative temperature. */
+EAGLE3_API eagle3_status_t eagle3_sample(const float *logits, int32_t rows, int32_t V, int64_t ld,
+                                         const eagle3_sampling_t *params, const float *uniforms, const int32_t *d2t,
+                                         int32_t target_vocab, int32_t *tokens, float *token_prob, float *probs,
+                                         int32_t probs_len, int32_t probs_in_target, void *stream);
+
+/* Residual (rejection-sampling) acceptance: position i of sequence b accepts its drafted token x when
+ * u_accept[b, i] * q(x) < p(x) (probability min(1, p(x) / q(x))); the first rejected position emits a
+ * token drawn from max(0, p - q) renormalised, by inverse CDF in ascending token order with
+ * u_resample[b, i]; if all gamma positions are accepted the emitted token is drawn from p_gamma with
+ * u_resample[b, gamma - 1].
+ *   draft         [batch, gamma] int32 target-vocabulary ids
+ *   draft_probs   [batch, gamma, V] fp32: the draft's final distributions over the target vocabulary
+ *   target_probs  [batch, gamma + 1, V] fp32
+ *   u_accept, u_resample  [batch, gamma] fp32
+ *   accepted_len  [batch] int32 out; next_token [batch] int32 out; hist [gamma + 1] int32 out or NULL
+ * One CTA per sequence.  Returns EAGLE3_ERR_INVALID_ARG for null required pointers or sizes < 1. */
+EAGLE3_API eagle3_status_t eagle3_accept_residual(const int32_t *draft, const float *draft_probs,
+                                                  const float *target_probs, const float *u_accept,
+                                                  const float *u_resample, int32_t batch, int32_t gamma, int32_t V,
+                                                  int32_t *accepted_len, int32_t *next_token, int32_t *hist,
+                                                  void *stream);
+
 /* Read the sticky device error word (synchronises the device).  *device_error (host) receives
  * the EAGLE3_DEVERR_* bits; returns EAGLE3_ERR_DEVICE_RANGE when any bit is set. */
 EAGLE3_API eagle3_status_t eagle3_draft_get_error(eagle3_draft_t *d, int32_t *device_error);
