@@ -26,13 +26,13 @@ namespace {
 enum Kind {
     K_FC = 0, K_EMBED, K_QKV_A, K_LATENT, K_Q_B, K_ABSORB, K_ATTN, K_COMBINE, K_O_PROJ, K_POST_NORM,
     K_GATE_UP, K_DOWN, K_FINAL, K_LM_HEAD, K_ARGMAX, K_EMIT, K_ROPE_Q, K_UNABSORB, K_KV_GATHER, K_KV_EXPAND,
-    K_PREFILL_TILES, K_COUNT
+    K_PREFILL_TILES, K_SAMPLE, K_COUNT
 };
 static_assert(K_COUNT <= EAGLE3_PROF_KINDS, "profile kinds");
 const char* kKindNames[EAGLE3_PROF_KINDS] = {
     "fc", "embed_norms", "q_a_kv_a", "latent_rope_append", "q_b", "absorb", "attention", "merge_splits",
     "o_proj", "post_attn_norm", "gate_up_silu", "down", "final_norm", "lm_head_argmax", "argmax_remap",
-    "emit_first", "rope_q", "unabsorb", "kv_gather", "kv_expand", "prefill_tiles", "", "", ""};
+    "emit_first", "rope_q", "unabsorb", "kv_gather", "kv_expand", "prefill_tiles", "sample", "", ""};
 constexpr int kProfPairs = 32768;
 constexpr int kGemvMaxRows = 8;          // rows above this take the tensor-core path (bf16 heads)
 constexpr int kAttnWaves = 8;            // waves of attention CTAs planned for fixed-chunk splits
@@ -56,7 +56,7 @@ struct eagle3_draft {
     float *f = nullptr, *carry = nullptr, *x = nullptr, *cqkv = nullptr, *cq_hat = nullptr, *q = nullptr,
           *qa = nullptr, *part_o = nullptr, *part_ml = nullptr, *o = nullptr, *h1 = nullptr, *y = nullptr,
           *mlp = nullptr, *h2 = nullptr, *z = nullptr, *pval = nullptr, *rope_cos = nullptr,
-          *rope_sin = nullptr, *tc_part = nullptr, *olat = nullptr;
+          *rope_sin = nullptr, *tc_part = nullptr, *olat = nullptr, *logits = nullptr;
     bf16_t *qa_bf = nullptr, *x_bf = nullptr, *cqh_bf = nullptr, *q_bf = nullptr, *olat_bf = nullptr,
            *o_bf = nullptr, *y_bf = nullptr, *m_bf = nullptr, *z_bf = nullptr, *wukt = nullptr;
     // unabsorbed extend attention (allocated when the configuration allows long extends)
@@ -230,7 +230,7 @@ struct Layout {
 struct Offsets {
     size_t f, carry, x, cqkv, cq_hat, q, qa, qa_bf, part_o, part_ml, o, h1, y, mlp, h2, z, pval, pidx, rope_cos,
         rope_sin, row_seq, row_pos, d0, tok_in, err, olat, x_bf, cqh_bf, q_bf, olat_bf, o_bf, y_bf, m_bf, z_bf, wukt,
-        tc_part, xc, xpe, kvx, tiles, total;
+        tc_part, xc, xpe, kvx, tiles, logits, total;
     int tiles_cap;
     int m_cap, splits_cap, npart;
     size_t part_rows;
@@ -297,6 +297,7 @@ Offsets plan(const eagle3_config_t& c, int num_sms) {
     o.z_bf = L.take((tc ? B : 0) * H * b2);
     o.wukt = L.take(tc ? (size_t)nh * c.kv_lora_rank * c.qk_nope_dim * b2 : 0);
     o.tc_part = L.take(tc ? kSplitKBytes : 0);
+    o.logits = L.take(B * (size_t)c.draft_vocab * f4);   // lm_head outputs of a sampled decode step
     // unabsorbed extend attention: gathered latent rows, expanded keys/values, query tile map
     const bool pre = prefill_allowed(c);
     const size_t slots = pre ? (size_t)B * c.max_ctx : 0;
@@ -690,6 +691,7 @@ eagle3_status_t eagle3_draft_create(const eagle3_config_t* config, const eagle3_
     d->o_bf = Bf(o.o_bf); d->y_bf = Bf(o.y_bf); d->m_bf = Bf(o.m_bf); d->z_bf = Bf(o.z_bf); d->wukt = Bf(o.wukt);
     d->tc_part = F(o.tc_part);
     d->xc = Bf(o.xc); d->xpe = Bf(o.xpe); d->kvx = Bf(o.kvx);
+    d->logits = F(o.logits);
     d->tiles = o.tiles_cap ? reinterpret_cast<int4*>(base + o.tiles) : nullptr;
     d->tiles_cap = o.tiles_cap;
     std::vector<float> cs, sn;
@@ -795,6 +797,65 @@ eagle3_status_t eagle3_draft_decode(eagle3_draft_t* d, int32_t gamma, const int3
     return EAGLE3_OK;
 }
 
+namespace {
+bool sampling_ok(const eagle3_sampling_t* p) {
+    return p && p->temperature >= 0.f && p->top_k >= 0 && p->top_k <= 1024 && p->top_p > 0.f && p->top_p <= 1.f &&
+           !(p->temperature > 0.f && p->top_k == 0 && p->top_p < 1.f);
+}
+}  // namespace
+
+eagle3_status_t eagle3_draft_decode_sampled(eagle3_draft_t* d, int32_t gamma, const int32_t* d2t,
+                                            eagle3_kv_t* cache, const eagle3_sampling_t* params,
+                                            const float* first_logits, const float* uniforms, int32_t* draft_tokens,
+                                            float* draft_probs, int32_t probs_len, int32_t probs_in_target,
+                                            float* hidden_out, float* logits_out, void* stream) {
+    if (!d || !draft_tokens || !first_logits || !uniforms || !kv_ok(cache) || !sampling_ok(params))
+        return EAGLE3_ERR_INVALID_ARG;
+    if (gamma < 1 || gamma > 64) return EAGLE3_ERR_INVALID_ARG;
+    if (!d->have_extend) return EAGLE3_ERR_STATE;
+    const eagle3_config_t& c = d->cfg;
+    const int B = d->batch, H = c.hidden, Vd = c.draft_vocab;
+    if (draft_probs && probs_len < (probs_in_target && d2t ? c.target_vocab : Vd)) return EAGLE3_ERR_INVALID_ARG;
+    cudaStream_t st = (cudaStream_t)stream;
+    const bool tc = use_tc(*d, B);
+    RowArgs ra = row_args(*d, cache);
+    // step s draws with uniforms[s] from the step's logits: the extend's for s = 0, else the decode step's
+    auto sample = [&](int s, const float* logits) {
+        SampleArgs sa;
+        memset(&sa, 0, sizeof(sa));
+        sa.logits = logits; sa.ldl = Vd; sa.rows = B; sa.V = Vd;
+        sa.temperature = params->temperature; sa.top_k = params->top_k; sa.top_p = params->top_p;
+        sa.uniforms = uniforms + (size_t)s * B; sa.d2t = d2t; sa.target_vocab = c.target_vocab;
+        sa.tokens = d->tok_in; sa.tokens2 = draft_tokens + s; sa.tok2_stride = gamma;
+        sa.probs = draft_probs ? draft_probs + (size_t)s * B * probs_len : nullptr; sa.ldp = probs_len;
+        sa.probs_len = probs_len; sa.probs_target = probs_in_target ? 1 : 0;
+        sa.err = d->err;
+        return traced(*d, K_SAMPLE, st, [&] { return launch_sample(sa, st); });
+    };
+    E3_CUDA(sample(0, first_logits));
+    for (int s = 1; s < gamma; ++s) {
+        E3_CUDA(traced(*d, K_EMBED, st, [&] {
+            return launch_embed_norms(ra, true, B, nullptr, nullptr, nullptr, B, d->tok_in, cache->lengths, d->carry,
+                                      d->w.embed, d->w.input_norm, d->w.hidden_norm, d->x, tc ? d->x_bf : nullptr,
+                                      d->row_seq, d->row_pos, st);
+        }));
+        E3_CUDA(run_layer(*d, cache, B, d->carry, st));
+        float* ho = hidden_out ? hidden_out + (size_t)(s - 1) * B * H : nullptr;
+        float* lo = logits_out ? logits_out + (size_t)(s - 1) * B * Vd : d->logits;
+        E3_CUDA(traced(*d, K_FINAL, st, [&] {
+            return launch_final(ra, false, B, B, nullptr, d->h2, d->w.final_norm, d->row_pos, d->carry, d->z,
+                                tc ? d->z_bf : nullptr, ho, cache->lengths, st);
+        }));
+        {
+            Lin L = lin1(*d, B, d->z, d->z_bf, H, d->w.lm_head, Vd);
+            L.y = lo; L.ldy = Vd;
+            E3_CUDA(run_linear(*d, L, K_LM_HEAD, st));
+        }
+        E3_CUDA(sample(s, lo));
+    }
+    return EAGLE3_OK;
+}
+
 eagle3_status_t eagle3_linear(eagle3_draft_t* d, const void* x, const void* w, float* y, int32_t M, int32_t N,
                               int32_t K, void* stream) {
     if (!d || !x || !w || !y || M < 1 || N < 1 || K < 8 || K % 8) return EAGLE3_ERR_INVALID_ARG;
@@ -828,12 +889,6 @@ eagle3_status_t eagle3_accept_relaxed(const int32_t* draft, const int32_t* topk_
     return EAGLE3_OK;
 }
 
-namespace {
-bool sampling_ok(const eagle3_sampling_t* p) {
-    return p && p->temperature >= 0.f && p->top_k >= 0 && p->top_k <= 1024 && p->top_p > 0.f && p->top_p <= 1.f &&
-           !(p->temperature > 0.f && p->top_k == 0 && p->top_p < 1.f);
-}
-}  // namespace
 
 eagle3_status_t eagle3_sample(const float* logits, int32_t rows, int32_t V, int64_t ld,
                               const eagle3_sampling_t* params, const float* uniforms, const int32_t* d2t,

@@ -76,6 +76,9 @@ def _lib():
         lib.eagle3_sample.argtypes = [P, C.c_int32, C.c_int32, C.c_int64, C.POINTER(eagle3_sampling_t), P, P,
                                       C.c_int32, P, P, P, C.c_int32, C.c_int32, P]
         lib.eagle3_accept_residual.argtypes = [P, P, P, P, P, C.c_int32, C.c_int32, C.c_int32, P, P, P, P]
+        lib.eagle3_draft_decode_sampled.argtypes = [P, C.c_int32, P, C.POINTER(eagle3_kv_t),
+                                                    C.POINTER(eagle3_sampling_t), P, P, P, P, C.c_int32, C.c_int32,
+                                                    P, P, P]
         lib.eagle3_linear.argtypes = [P, P, P, P, C.c_int32, C.c_int32, C.c_int32, P]
         lib.eagle3_linear_noalloc.argtypes = [P, P, P, C.c_int32, C.c_int32, C.c_int32, P]
         lib.eagle3_draft_get_error.argtypes = [P, C.POINTER(C.c_int32)]
@@ -87,7 +90,7 @@ def _lib():
         lib.eagle3_draft_profile_reset.argtypes = [P]
         for f in ("eagle3_draft_profile_enable", "eagle3_draft_profile_read", "eagle3_draft_profile_reset",
                   "eagle3_draft_create", "eagle3_draft_workspace_bytes", "eagle3_draft_extend", "eagle3_draft_decode",
-                  "eagle3_accept", "eagle3_accept_relaxed", "eagle3_sample", "eagle3_accept_residual", "eagle3_linear", "eagle3_linear_noalloc", "eagle3_draft_get_error", "eagle3_draft_clear_error", "eagle3_draft_destroy"):
+                  "eagle3_accept", "eagle3_accept_relaxed", "eagle3_sample", "eagle3_accept_residual", "eagle3_draft_decode_sampled", "eagle3_linear", "eagle3_linear_noalloc", "eagle3_draft_get_error", "eagle3_draft_clear_error", "eagle3_draft_destroy"):
             getattr(lib, f).restype = C.c_int
         _L = lib
     return _L
@@ -200,6 +203,16 @@ def eagle3_sample(logits, rows, V, ld, temperature, top_k, top_p, uniforms, d2t,
     _check("eagle3_sample", _lib().eagle3_sample(
         _ptr(logits), int(rows), int(V), int(ld), C.byref(prm), _ptr(uniforms), _ptr(d2t), int(target_vocab),
         _ptr(tokens), _ptr(token_prob), _ptr(probs), int(probs_len), int(bool(probs_in_target)), _stream(stream)))
+
+
+def eagle3_draft_decode_sampled(handle, gamma, d2t, kv, temperature, top_k, top_p, first_logits, uniforms,
+                                draft_tokens, draft_probs=None, probs_len=0, probs_in_target=False, hidden_out=None,
+                                logits_out=None, stream=None):
+    prm = eagle3_sampling_t(float(temperature), int(top_k), float(top_p))
+    _check("eagle3_draft_decode_sampled", _lib().eagle3_draft_decode_sampled(
+        handle, int(gamma), _ptr(d2t), C.byref(kv), C.byref(prm), _ptr(first_logits), _ptr(uniforms),
+        _ptr(draft_tokens), _ptr(draft_probs), int(probs_len), int(bool(probs_in_target)), _ptr(hidden_out),
+        _ptr(logits_out), _stream(stream)))
 
 
 def eagle3_accept_residual(draft, draft_probs, target_probs, u_accept, u_resample, batch, gamma, V, accepted_len,

@@ -89,5 +89,12 @@ class DeviceHead:
     def decode(self, gamma, d2t, cache: DeviceCache, draft_tokens, hidden_out=None, logits_out=None, stream=None):
         E.eagle3_draft_decode(self.handle, gamma, d2t, cache.kv(), draft_tokens, hidden_out, logits_out, stream)
 
+    def decode_sampled(self, gamma, d2t, cache: DeviceCache, temperature, top_k, top_p, first_logits, uniforms,
+                       draft_tokens, draft_probs=None, probs_len=0, probs_in_target=False, hidden_out=None,
+                       logits_out=None, stream=None):
+        E.eagle3_draft_decode_sampled(self.handle, gamma, d2t, cache.kv(), temperature, top_k, top_p, first_logits,
+                                      uniforms, draft_tokens, draft_probs, probs_len, probs_in_target, hidden_out,
+                                      logits_out, stream)
+
     def error_word(self) -> int:
         return E.eagle3_draft_get_error(self.handle)

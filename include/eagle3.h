@@ -272,6 +272,25 @@ EAGLE3_API eagle3_status_t eagle3_sample(const float *logits, int32_t rows, int3
                                          int32_t target_vocab, int32_t *tokens, float *token_prob, float *probs,
                                          int32_t probs_len, int32_t probs_in_target, void *stream);
 
+/* The decode of a sampled round: like eagle3_draft_decode, but every draft token is drawn with
+ * eagle3_sample's rule instead of the argmax.  Token 0 is drawn from first_logits (the extend's logits of
+ * the scored rows, [batch, V_d], from eagle3_draft_extend's logits_out) with uniforms[0, :]; decode step
+ * s (1 <= s < gamma) draws from its own logits with uniforms[s, :] and feeds the drawn token (target id,
+ * through d2t) to the next step.
+ *   uniforms     [gamma, batch] fp32 in [0, 1)
+ *   draft_tokens [batch, gamma] int32 out, target-vocabulary ids
+ *   draft_probs  [gamma, batch, probs_len] fp32 out or NULL: each step's final distribution, indexed by
+ *                target ids when probs_in_target is non-zero (the layout eagle3_accept_residual reads)
+ *   hidden_out, logits_out: as in eagle3_draft_decode (logits of decode steps 1..gamma-1)
+ * Returns EAGLE3_ERR_STATE before any extend, EAGLE3_ERR_INVALID_ARG as eagle3_sample and
+ * eagle3_draft_decode do. */
+EAGLE3_API eagle3_status_t eagle3_draft_decode_sampled(eagle3_draft_t *d, int32_t gamma, const int32_t *d2t,
+                                                       eagle3_kv_t *cache, const eagle3_sampling_t *params,
+                                                       const float *first_logits, const float *uniforms,
+                                                       int32_t *draft_tokens, float *draft_probs, int32_t probs_len,
+                                                       int32_t probs_in_target, float *hidden_out, float *logits_out,
+                                                       void *stream);
+
 /* Residual (rejection-sampling) acceptance: position i of sequence b accepts its drafted token x when
  * u_accept[b, i] * q(x) < p(x) (probability min(1, p(x) / q(x))); the first rejected position emits a
  * token drawn from max(0, p - q) renormalised, by inverse CDF in ascending token order with
