@@ -43,6 +43,8 @@ def parse_args(argv=None):
     p.add_argument("--workload", default="dsv3_b1")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--e2e-steps", type=int, default=None)
+    p.add_argument("--sampling", default=None,
+                   help="T,top_k,top_p: sampled drafts and residual acceptance instead of greedy rounds")
     return p.parse_args(argv)
 
 
@@ -313,11 +315,36 @@ def run_ours(args, ws, rank, local):
     tgt = torch.from_numpy(WL.synthetic_targets(w, toks.cpu().numpy())).cuda()
     assert head.error_word() == 0
 
-    def step(st):
+    sampling = None
+    if args.sampling:
+        T_s, k_s, p_s = args.sampling.split(",")
+        sampling = (float(T_s), int(k_s), float(p_s))
+        Vt = w.target_vocab if d2t is not None else w.draft_vocab
+        gen = torch.Generator(device="cuda").manual_seed(1234)
+        lg0 = torch.empty((B, w.draft_vocab), dtype=torch.float32, device="cuda")
+        u_draw = torch.rand((G, B), generator=gen, device="cuda")
+        q_probs = torch.empty((B, G, Vt), dtype=torch.float32, device="cuda")
+        tprobs = torch.rand((B, G + 1, Vt), generator=gen, device="cuda") ** 4
+        tprobs /= tprobs.sum(dim=2, keepdim=True)
+        u_acc = torch.rand((B, G), generator=gen, device="cuda")
+        u_res = torch.rand((B, G), generator=gen, device="cuda")
+        nxt = torch.zeros(B, dtype=torch.int32, device="cuda")
+
+    def run_round(st, dev_in):
         cache.lengths.copy_(len0)
-        head.extend(din, cache, stream=st)
-        head.decode(G, d2t_dev, cache, toks, stream=st)
-        E.eagle3_accept(toks, tgt, B, G, acc, hist, stream=st)
+        if sampling is None:
+            head.extend(dev_in, cache, stream=st)
+            head.decode(G, d2t_dev, cache, toks, stream=st)
+            E.eagle3_accept(toks, tgt, B, G, acc, hist, stream=st)
+            return
+        head.extend(dev_in, cache, logits_out=lg0, stream=st)
+        head.decode_sampled(G, d2t_dev, cache, sampling[0], sampling[1], sampling[2], lg0, u_draw, toks, q_probs,
+                            q_probs.shape[2], d2t is not None, stream=st)
+        E.eagle3_accept_residual(toks, q_probs, tprobs, u_acc, u_res, B, G, q_probs.shape[2], acc, nxt, hist,
+                                 stream=st)
+
+    def step(st):
+        run_round(st, din)
 
     for _ in range(args.warmup):
         step(stream)
@@ -385,7 +412,11 @@ def run_ours(args, ws, rank, local):
 
         def dstep(st):
             cache.lengths.copy_(len1)
-            head.decode(G, d2t_dev, cache, toks, stream=st)
+            if sampling is None:
+                head.decode(G, d2t_dev, cache, toks, stream=st)
+            else:
+                head.decode_sampled(G, d2t_dev, cache, sampling[0], sampling[1], sampling[2], lg0, u_draw, toks,
+                                    q_probs, q_probs.shape[2], d2t is not None, stream=st)
 
         for _ in range(args.warmup):
             dstep(stream)
@@ -417,8 +448,11 @@ def run_ours(args, ws, rank, local):
     o_acc = torch.empty(B, dtype=torch.int32).pin_memory()
     o_hist = torch.empty(G + 1, dtype=torch.int32).pin_memory()
     d_in = {k: (v if k != "aux" else list(v)) for k, v in din.items()}
+    # sampled rounds also bring the uniforms and the target distributions from the host
+    h_samp = [] if sampling is None else [(t, pin(t)) for t in (u_draw, tprobs, u_acc, u_res)]
     h2d = sum(a.numel() * a.element_size() for a in h_aux) + sum(
-        t.numel() * t.element_size() for t in (h_tok, h_pos, h_ro, h_tgt))
+        t.numel() * t.element_size() for t in (h_tok, h_pos, h_ro, h_tgt)) + sum(
+        h.numel() * h.element_size() for _, h in h_samp)
     d2h = sum(t.numel() * t.element_size() for t in (o_toks, o_acc, o_hist))
 
     def e2e_step():
@@ -428,10 +462,9 @@ def run_ours(args, ws, rank, local):
         d_in["positions"].copy_(h_pos, non_blocking=True)
         d_in["row_offsets"].copy_(h_ro, non_blocking=True)
         tgt.copy_(h_tgt, non_blocking=True)
-        cache.lengths.copy_(len0)
-        head.extend(d_in, cache, stream=stream)
-        head.decode(G, d2t_dev, cache, toks, stream=stream)
-        E.eagle3_accept(toks, tgt, B, G, acc, hist, stream=stream)
+        for dv, hv in h_samp:
+            dv.copy_(hv, non_blocking=True)
+        run_round(stream, d_in)
         o_toks.copy_(toks, non_blocking=True)
         o_acc.copy_(acc, non_blocking=True)
         o_hist.copy_(hist, non_blocking=True)
@@ -489,7 +522,9 @@ def run_ours(args, ws, rank, local):
                                f"T_new {w.t_new}, gamma {G}, draft vocab {w.draft_vocab}"
                                + (" with d2t" if w.d2t else ""),
                    "batch": B, "gamma": G, "ctx": list(w.ctx), "draft_vocab": w.draft_vocab,
-                   "step": "extend + (gamma-1) decode steps + acceptance",
+                   "step": "extend + (gamma-1) decode steps + acceptance" if sampling is None else
+                           f"extend + (gamma-1) sampled decode steps (T {sampling[0]}, top_k {sampling[1]}, "
+                           f"top_p {sampling[2]}) + residual acceptance",
                    "l2": f"inputs larger than L2: {round_bytes / 1e9:.2f} GB of weights+KV streamed per step",
                    "parallelism": f"replicas x{ws} (sequence-sharded, no collective)"},
         "roofline": ({"bound": "tensor", "kernel": dom, "achieved": round(achieved_tf, 1), "peak": tpeak,

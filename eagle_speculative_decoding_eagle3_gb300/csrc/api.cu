@@ -827,7 +827,8 @@ eagle3_status_t eagle3_draft_decode_sampled(eagle3_draft_t* d, int32_t gamma, co
         sa.temperature = params->temperature; sa.top_k = params->top_k; sa.top_p = params->top_p;
         sa.uniforms = uniforms + (size_t)s * B; sa.d2t = d2t; sa.target_vocab = c.target_vocab;
         sa.tokens = d->tok_in; sa.tokens2 = draft_tokens + s; sa.tok2_stride = gamma;
-        sa.probs = draft_probs ? draft_probs + (size_t)s * B * probs_len : nullptr; sa.ldp = probs_len;
+        // [batch, gamma, probs_len]: the layout eagle3_accept_residual reads
+        sa.probs = draft_probs ? draft_probs + (size_t)s * probs_len : nullptr; sa.ldp = (long)gamma * probs_len;
         sa.probs_len = probs_len; sa.probs_target = probs_in_target ? 1 : 0;
         sa.err = d->err;
         return traced(*d, K_SAMPLE, st, [&] { return launch_sample(sa, st); });
@@ -894,7 +895,7 @@ eagle3_status_t eagle3_sample(const float* logits, int32_t rows, int32_t V, int6
                               const eagle3_sampling_t* params, const float* uniforms, const int32_t* d2t,
                               int32_t target_vocab, int32_t* tokens, float* token_prob, float* probs,
                               int32_t probs_len, int32_t probs_in_target, void* stream) {
-    if (!logits || !uniforms || !tokens || rows < 1 || V < 1 || ld < V || !sampling_ok(params))
+    if (!logits || !uniforms || !tokens || rows < 1 || V < 1 || V > 131072 || ld < V || !sampling_ok(params))
         return EAGLE3_ERR_INVALID_ARG;
     if (d2t && target_vocab < 1) return EAGLE3_ERR_INVALID_ARG;
     if (probs && probs_len < (probs_in_target && d2t ? target_vocab : V)) return EAGLE3_ERR_INVALID_ARG;

@@ -5,7 +5,7 @@
 // that feeds the sampler.  Here the uniform random numbers are inputs, so a caller (or a test) draws
 // them once and every consumer uses the same ones.
 //
-// sample_kernel: one CTA of kThreads per row.  x = logits / temperature (fp32 division); top_k keeps the
+// sample_kernel: one CTA of kThreads per row.  x = logits * (1 / temperature) in fp32; top_k keeps the
 // top_k largest x (lower indices first among equal values) found by a radix select on the order-
 // preserving integer image of x; the kept tokens are sorted (x descending, index ascending) by a bitonic
 // sort in shared memory; top_p keeps the shortest prefix whose softmax mass reaches top_p of the kept
@@ -27,6 +27,8 @@ namespace e3 {
 namespace smp {
 constexpr int kThreads = 1024;
 constexpr int kMaxTopK = 1024;
+constexpr int kKeyCache = 40960;   // rows up to this many logits keep their sort keys in shared memory
+constexpr int kMaxChunks = 4096;   // rows of at most 131072 logits
 }  // namespace smp
 
 // order-preserving image of a float: larger floats give larger unsigned keys
@@ -82,13 +84,14 @@ __device__ int block_inclusive_scan_int(int v, int* warp_tot) {
     return v + (warp > 0 ? warp_tot[warp - 1] : 0);
 }
 
-// bitonic sort of kThreads (key, index) pairs in shared memory, ascending by (key, index)
-__device__ void bitonic_sort(unsigned long long* a) {
+// bitonic sort of the first n (a power of two <= kThreads) packed (key, index) pairs in shared memory,
+// ascending
+__device__ void bitonic_sort(unsigned long long* a, int n) {
     const int t = threadIdx.x;
-    for (int k = 2; k <= smp::kThreads; k <<= 1) {
+    for (int k = 2; k <= n; k <<= 1) {
         for (int j = k >> 1; j > 0; j >>= 1) {
             const int p = t ^ j;
-            if (p > t) {
+            if (t < n && p > t) {
                 const bool up = (t & k) == 0;
                 const unsigned long long x = a[t], y = a[p];
                 if ((x > y) == up) { a[t] = y; a[p] = x; }
@@ -105,10 +108,13 @@ __global__ void __launch_bounds__(smp::kThreads) sample_kernel(SampleArgs s) {
     __shared__ unsigned long long sorted[kThreads];   // (key, index) packed; reused
     __shared__ float wv[kThreads];
     __shared__ int hist[256];
+    __shared__ int whist[kThreads / 32][256];         // per-warp radix histograms
+    __shared__ int ccount[kMaxChunks];                // equal-key counts, then prefixes, per 32 indices
     __shared__ float ftot[32];
     __shared__ int itot[32];
     __shared__ int sh_int[4];
     __shared__ float sh_f[2];
+    extern __shared__ uint32_t keycache[];             // [V] keys of x = logits * (1 / T) when V fits
     const int r = blockIdx.x, t = threadIdx.x, V = s.V;
     const float* l = s.logits + (long)r * s.ldl;
     float* probs = s.probs ? s.probs + (long)r * s.ldp : nullptr;
@@ -144,9 +150,9 @@ __global__ void __launch_bounds__(smp::kThreads) sample_kernel(SampleArgs s) {
         }
     } else if (s.top_k <= 0) {
         // whole vocabulary: softmax and inverse CDF in index order
-        const float T = s.temperature;
+        const float T = 1.f / s.temperature;   // x = logits * (1 / temperature), both rounded to fp32
         float m = -INFINITY;
-        for (int i = t; i < V; i += kThreads) m = fmaxf(m, l[i] / T);
+        for (int i = t; i < V; i += kThreads) m = fmaxf(m, l[i] * T);
         m = warp_max(m);
         if ((t & 31) == 0) wv[t >> 5] = m;
         __syncthreads();
@@ -160,7 +166,7 @@ __global__ void __launch_bounds__(smp::kThreads) sample_kernel(SampleArgs s) {
         // contiguous segment per thread, so the block scan follows the index order
         const int seg = (V + kThreads - 1) / kThreads, i0 = t * seg, i1 = min(V, i0 + seg);
         float part = 0.f;
-        for (int i = i0; i < i1; ++i) part += __expf(l[i] / T - m);
+        for (int i = i0; i < i1; ++i) part += __expf(l[i] * T - m);
         const float incl = block_inclusive_scan(part, ftot);
         const float total = ftot[kThreads / 32 - 1];
         const float target = u * total;
@@ -168,7 +174,7 @@ __global__ void __launch_bounds__(smp::kThreads) sample_kernel(SampleArgs s) {
         int found = -1;
         if (cum <= target && target < incl) {
             for (int i = i0; i < i1; ++i) {
-                cum += __expf(l[i] / T - m);
+                cum += __expf(l[i] * T - m);
                 if (target < cum) { found = i; break; }
             }
             if (found < 0) found = i1 - 1;
@@ -178,7 +184,7 @@ __global__ void __launch_bounds__(smp::kThreads) sample_kernel(SampleArgs s) {
         if (found >= 0) sh_int[0] = found;
         __syncthreads();
         token = sh_int[0];
-        qtok = __expf(l[token] / T - m) / total;
+        qtok = __expf(l[token] * T - m) / total;
         if (probs) {
             if (s.probs_target && s.d2t) {
                 for (int i = t; i < s.probs_len; i += kThreads) probs[i] = 0.f;
@@ -186,21 +192,47 @@ __global__ void __launch_bounds__(smp::kThreads) sample_kernel(SampleArgs s) {
             }
             for (int i = t; i < V; i += kThreads) {
                 const int o = s.probs_target && s.d2t ? i + s.d2t[i] : i;
-                if (o >= 0 && o < s.probs_len) probs[o] = __expf(l[i] / T - m) / total;
+                if (o >= 0 && o < s.probs_len) probs[o] = __expf(l[i] * T - m) / total;
             }
         }
     } else {
-        const float T = s.temperature;
+        const float T = 1.f / s.temperature;   // x = logits * (1 / temperature), both rounded to fp32
         const int K = min(s.top_k, min(kMaxTopK, V));
+        const bool cached = V <= kKeyCache;
+        if (cached) {
+            for (int i = t; i < V; i += kThreads) keycache[i] = fkey(l[i] * T);
+            __syncthreads();
+        }
+        auto key_of = [&](int i) { return cached ? keycache[i] : fkey(l[i] * T); };
         // radix select of the K-th largest key, 8 bits at a time from the top
         uint32_t prefix = 0, pmask = 0;
         int need = K;
+        const int warp = t >> 5;
         for (int shift = 24; shift >= 0; shift -= 8) {
-            for (int i = t; i < 256; i += kThreads) hist[i] = 0;
+            for (int i = t; i < (kThreads / 32) * 256; i += kThreads) (&whist[0][0])[i] = 0;
             __syncthreads();
-            for (int i = t; i < V; i += kThreads) {
-                const uint32_t k = fkey(l[i] / T);
-                if ((k & pmask) == prefix) atomicAdd(&hist[(k >> shift) & 255u], 1);
+            // logits cluster in a few exponents, so most keys share a bin: every warp counts into its own
+            // histogram, which keeps the atomics of different warps apart
+            for (int i0 = 0; i0 < V; i0 += kThreads) {
+                const int i = i0 + t;
+                int bin = 256;
+                if (i < V) {
+                    const uint32_t k = key_of(i);
+                    if ((k & pmask) == prefix) bin = (int)((k >> shift) & 255u);
+                }
+                // lanes sharing lane 0's bin add once through lane 0; the others add one by one
+                const int b0 = __shfl_sync(0xffffffffu, bin, 0);
+                const unsigned same = __ballot_sync(0xffffffffu, bin == b0);
+                if (bin < 256) {
+                    if (bin != b0) atomicAdd(&whist[warp][bin], 1);
+                    else if ((t & 31) == 0) atomicAdd(&whist[warp][b0], __popc(same));
+                }
+            }
+            __syncthreads();
+            for (int b = t; b < 256; b += kThreads) {
+                int c = 0;
+                for (int w = 0; w < kThreads / 32; ++w) c += whist[w][b];
+                hist[b] = c;
             }
             __syncthreads();
             if (t == 0) {
@@ -211,6 +243,7 @@ __global__ void __launch_bounds__(smp::kThreads) sample_kernel(SampleArgs s) {
                 }
                 sh_int[0] = d;
                 sh_int[1] = acc;
+                sh_int[3] = hist[d];   // after the last pass: the number of keys equal to the threshold
             }
             __syncthreads();
             prefix |= (uint32_t)sh_int[0] << shift;
@@ -223,33 +256,58 @@ __global__ void __launch_bounds__(smp::kThreads) sample_kernel(SampleArgs s) {
         if (t == 0) sh_int[2] = 0;
         sorted[t] = ~0ull;
         __syncthreads();
+        // when every key equal to the threshold is kept (the usual case) one pass gathers them all
+        const bool all_eq = sh_int[3] == need;
         for (int i = t; i < V; i += kThreads) {
-            const uint32_t k = fkey(l[i] / T);
-            if (k > kth) {
+            const uint32_t k = key_of(i);
+            if (k > kth || (all_eq && k == kth)) {
                 const int slot = atomicAdd(&sh_int[2], 1);
                 sorted[slot] = ((unsigned long long)(~k) << 32) | (uint32_t)i;
             }
         }
         __syncthreads();
-        int base = sh_int[2];
-        for (int c0 = 0; c0 < V && need > 0; c0 += kThreads) {
-            const int i = c0 + t;
-            const int eq = (i < V && fkey(l[i] / T) == kth) ? 1 : 0;
-            const int incl = block_inclusive_scan_int(eq, itot);
-            const int rank = incl - eq;
-            if (eq && rank < need) sorted[base + rank] = ((unsigned long long)(~kth) << 32) | (uint32_t)i;
-            const int taken = min(need, itot[kThreads / 32 - 1]);
-            base += taken;
-            need -= taken;
+        if (!all_eq)
+        {
+            // equal keys in index order: per 32-index chunk counts by ballot, one scan over the chunk counts,
+            // then ranks inside the chunks that hold any of the `need` first equal keys
+            const int base = sh_int[2];
+            const int nchunk = (V + 31) / 32;
+            for (int c = warp; c < nchunk; c += kThreads / 32) {
+                const int i = c * 32 + (t & 31);
+                const unsigned bal = __ballot_sync(0xffffffffu, i < V && key_of(i) == kth);
+                if ((t & 31) == 0) ccount[c] = __popc(bal);
+            }
+            __syncthreads();
+            const int per = (nchunk + kThreads - 1) / kThreads, c0 = t * per, c1 = min(nchunk, c0 + per);
+            int mine = 0;
+            for (int c = c0; c < c1; ++c) mine += ccount[c];
+            int run = block_inclusive_scan_int(mine, itot) - mine;
+            for (int c = c0; c < c1; ++c) {
+                const int cn = ccount[c];
+                ccount[c] = run;
+                run += cn;
+            }
+            __syncthreads();
+            for (int c = warp; c < nchunk; c += kThreads / 32) {
+                const int start = ccount[c];
+                if (start >= need) continue;   // warp-uniform
+                const int i = c * 32 + (t & 31);
+                const bool eq = i < V && key_of(i) == kth;
+                const unsigned bal = __ballot_sync(0xffffffffu, eq);
+                const int rank = start + __popc(bal & ((1u << (t & 31)) - 1u));
+                if (eq && rank < need) sorted[base + rank] = ((unsigned long long)(~kth) << 32) | (uint32_t)i;
+            }
             __syncthreads();
         }
         const int n = K;
         // (x descending, index ascending) == (~key ascending, index ascending)
-        bitonic_sort(sorted);
+        int np2 = 2;
+        while (np2 < n) np2 <<= 1;
+        bitonic_sort(sorted, np2);
         const bool live = t < n;
         const int idx = live ? (int)(sorted[t] & 0xffffffffu) : 0;
-        const float x0 = l[(int)(sorted[0] & 0xffffffffu)] / T;
-        const float w = live ? __expf(l[idx] / T - x0) : 0.f;
+        const float x0 = l[(int)(sorted[0] & 0xffffffffu)] * T;
+        const float w = live ? __expf(l[idx] * T - x0) : 0.f;
         const float cum = block_inclusive_scan(w, ftot);
         const float total = ftot[kThreads / 32 - 1];
         // top-p: the shortest prefix whose mass reaches top_p of the total
@@ -268,7 +326,7 @@ __global__ void __launch_bounds__(smp::kThreads) sample_kernel(SampleArgs s) {
         __syncthreads();
         sorted[t] = kept ? (((unsigned long long)(uint32_t)idx << 32) | __float_as_uint(w)) : ~0ull;
         __syncthreads();
-        bitonic_sort(sorted);
+        bitonic_sort(sorted, np2);
         const bool k2 = t < keep;
         const float w2 = k2 ? __uint_as_float((uint32_t)(sorted[t] & 0xffffffffu)) : 0.f;
         const int i2 = k2 ? (int)(sorted[t] >> 32) : 0;
@@ -385,9 +443,19 @@ __global__ void acceptance_hist_kernel(const int* acc, int batch, int gamma, int
 }
 
 cudaError_t launch_sample(const SampleArgs& s, cudaStream_t st) {
-    if (s.V < 1 || s.rows < 1 || (s.top_k > smp::kMaxTopK) || (s.temperature > 0.f && s.top_k <= 0 && s.top_p < 1.f))
+    if (s.V < 1 || s.V > 32 * smp::kMaxChunks || s.rows < 1 || (s.top_k > smp::kMaxTopK) ||
+        (s.temperature > 0.f && s.top_k <= 0 && s.top_p < 1.f))
         return cudaErrorInvalidValue;
-    return launch_pdl(sample_kernel, dim3(s.rows), dim3(smp::kThreads), 0, st, s);
+    static bool attr_set = false;
+    if (!attr_set) {
+        cudaError_t e = cudaFuncSetAttribute(sample_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)(smp::kKeyCache * sizeof(uint32_t)));
+        if (e != cudaSuccess) return e;
+        attr_set = true;
+    }
+    const bool cached = s.temperature > 0.f && s.top_k > 0 && s.V <= smp::kKeyCache;
+    const size_t smem = cached ? (size_t)s.V * sizeof(uint32_t) : 0;
+    return launch_pdl(sample_kernel, dim3(s.rows), dim3(smp::kThreads), smem, st, s);
 }
 
 cudaError_t launch_accept_residual(const ResidualArgs& a, cudaStream_t st) {

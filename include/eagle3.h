@@ -254,7 +254,7 @@ typedef struct {
                             reaches top_p of their total */
 } eagle3_sampling_t;
 
-/* Draw one token per row from filtered logits: x = logits / temperature (fp32); keep the top_k largest x
+/* Draw one token per row from filtered logits: x = logits * (1 / temperature) (fp32); keep the top_k largest x
  * (lower indices first among equal values), then the top_p prefix in the order (x descending, index
  * ascending); renormalise the kept softmax weights and pick by inverse CDF over the kept tokens in
  * ascending index order with uniforms[r].
@@ -265,7 +265,7 @@ typedef struct {
  *   token_prob   [rows] fp32 out or NULL: the drawn token's final probability
  *   probs        [rows, probs_len] fp32 out or NULL: the final distribution, indexed by target ids when
  *                probs_in_target is non-zero (zeros elsewhere), else by draft ids
- * One CTA per row.  Returns EAGLE3_ERR_INVALID_ARG for null required pointers, rows or V < 1, ld < V,
+ * One CTA per row.  Returns EAGLE3_ERR_INVALID_ARG for null required pointers, rows or V < 1, V > 131072, ld < V,
  * top_k outside 0..1024, top_p outside (0, 1], top_p < 1 without top_k, or a negative temperature. */
 EAGLE3_API eagle3_status_t eagle3_sample(const float *logits, int32_t rows, int32_t V, int64_t ld,
                                          const eagle3_sampling_t *params, const float *uniforms, const int32_t *d2t,
@@ -279,7 +279,7 @@ EAGLE3_API eagle3_status_t eagle3_sample(const float *logits, int32_t rows, int3
  * through d2t) to the next step.
  *   uniforms     [gamma, batch] fp32 in [0, 1)
  *   draft_tokens [batch, gamma] int32 out, target-vocabulary ids
- *   draft_probs  [gamma, batch, probs_len] fp32 out or NULL: each step's final distribution, indexed by
+ *   draft_probs  [batch, gamma, probs_len] fp32 out or NULL: each step's final distribution, indexed by
  *                target ids when probs_in_target is non-zero (the layout eagle3_accept_residual reads)
  *   hidden_out, logits_out: as in eagle3_draft_decode (logits of decode steps 1..gamma-1)
  * Returns EAGLE3_ERR_STATE before any extend, EAGLE3_ERR_INVALID_ARG as eagle3_sample and

@@ -403,8 +403,10 @@ def sample_filtered(logits, temperature, top_k, top_p, u):
     counter feeds the sampler).  The uniform u in [0, 1) is an input, so both sides draw the same number.
 
     Reading of the pages, which name the parameters but not their composition: temperature 0 is the
-    greedy argmax (lowest index among equal maxima).  Otherwise x = logits / temperature (fp32, as the
-    GPU divides); top_k > 0 keeps the top_k largest x, lower indices first among equal values; top_p < 1
+    greedy argmax (lowest index among equal maxima).  Otherwise x = logits * (1 / temperature), the
+    reciprocal and the product rounded to fp32 as the GPU forms them (x decides which tokens are kept, so
+    both sides use the same fp32 values); top_k > 0 keeps the top_k largest x, lower indices first among
+    equal values; top_p < 1
     then keeps the shortest prefix of those, in the order (x descending, index ascending), whose softmax
     mass reaches top_p of the kept mass.  The kept tokens' softmax weights are renormalised and u picks
     the token by inverse CDF over the kept tokens in ascending index order.
@@ -416,7 +418,7 @@ def sample_filtered(logits, temperature, top_k, top_p, u):
         t = int(np.flatnonzero(l == l.max())[0])
         probs[t] = 1.0
         return t, probs
-    x = (l / np.float32(temperature)).astype(np.float32)
+    x = (l * (np.float32(1.0) / np.float32(temperature))).astype(np.float32)
     order = sorted(range(V), key=lambda i: (-float(x[i]), i))
     kept = order[:top_k] if top_k > 0 else order
     m = float(x[kept[0]])

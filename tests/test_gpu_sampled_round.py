@@ -38,7 +38,7 @@ def _sampled_round(w, T, k, p, seed, tol):
         hid = torch.zeros((G, B, H), dtype=torch.float32, device="cuda")
         lg = torch.zeros((G, B, Vd), dtype=torch.float32, device="cuda")
         toks = torch.zeros((B, G), dtype=torch.int32, device="cuda")
-        probs = torch.zeros((G, B, Vt), dtype=torch.float32, device="cuda")
+        probs = torch.zeros((B, G, Vt), dtype=torch.float32, device="cuda")
         d2t_dev = HN.to_device(d2t) if d2t is not None else None
         head.extend(din, dc, hidden_out=hid[0], logits_out=lg[0])
         head.decode_sampled(G, d2t_dev, dc, T, k, p, lg[0], torch.from_numpy(u).cuda(), toks, probs, Vt, True,
@@ -48,7 +48,7 @@ def _sampled_round(w, T, k, p, seed, tol):
         g_tok, g_hid, g_lg, g_probs = toks.cpu().numpy(), hid.cpu().numpy(), lg.cpu().numpy(), probs.cpu().numpy()
         # residual acceptance against synthetic target distributions over the target vocabulary
         tp = rng.dirichlet(np.ones(Vt) * 0.5, size=(B, G + 1)).astype(np.float32)
-        q = np.ascontiguousarray(g_probs.transpose(1, 0, 2))
+        q = g_probs
         for b in range(B):                              # some positions where the target agrees with the draft
             tp[b, 0] = q[b, 0]
         ua = rng.random((B, G)).astype(np.float32)

@@ -112,3 +112,27 @@ def test_accept_residual_matches_oracle():
             u2[b, min(k, G - 1)] = np.clip(u2[b, min(k, G - 1)] + du, 0.0, 1.0 - 1e-9)
             near.add(int(O.accept_residual(draft[b:b + 1], q[b:b + 1], p[b:b + 1], ua[b:b + 1], u2[b:b + 1])[1][0]))
         assert nxt[b] in near, (b, nxt[b], o_nxt[b])
+
+
+@pytest.mark.parametrize("k", [5, 50, 1000])
+def test_sample_top_k_boundary_on_ties(k):
+    # integer-valued logits: the top_k boundary falls inside a group of equal values, where the lower
+    # indices must be the ones kept
+    from eagle_speculative_decoding_eagle3_gb300 import build
+    from eagle_speculative_decoding_eagle3_gb300 import eagle3 as E
+    build.build()
+    rows, V = 4, 4096
+    rng = np.random.default_rng(k)
+    l = np.round(rng.normal(0.0, 1.5, size=(rows, V))).astype(np.float32)
+    u = rng.random(rows).astype(np.float32)
+    tok = torch.zeros(rows, dtype=torch.int32, device="cuda")
+    probs = torch.zeros((rows, V), dtype=torch.float32, device="cuda")
+    E.eagle3_sample(torch.from_numpy(l).cuda(), rows, V, V, 1.0, k, 1.0, torch.from_numpy(u).cuda(), None, 0, tok,
+                    None, probs, V, False)
+    torch.cuda.synchronize()
+    tok, probs = tok.cpu().numpy(), probs.cpu().numpy()
+    for r in range(rows):
+        t_o, pr_o = O.sample_filtered(l[r], 1.0, k, 1.0, float(u[r]))
+        np.testing.assert_array_equal(probs[r] > 0, pr_o > 0)      # the same kept set, ties included
+        if tok[r] != t_o:
+            assert tok[r] in _allowed(l[r], 1.0, k, 1.0, float(u[r])), (r, tok[r], t_o)
