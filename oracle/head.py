@@ -491,3 +491,53 @@ def accept_residual(draft, draft_probs, target_probs, u_accept, u_resample):
     for k in acc:
         hist[k] += 1
     return acc, nxt, hist
+
+
+# --------------------------------------------------------------------------- FP8 draft weights
+def e4m3_decode(code):
+    """Value of an FP8 E4M3 code (OCP 8-bit floating point, E4M3: sign, 4 exponent bits with bias 7, 3
+    mantissa bits, subnormals at exponent 0, no infinities, S.1111.111 is NaN, largest finite 448)."""
+    code = int(code) & 0xFF
+    sign = -1.0 if code & 0x80 else 1.0
+    e, m = (code >> 3) & 0xF, code & 7
+    if e == 0xF and m == 7:
+        return float("nan")
+    if e == 0:
+        return sign * (m / 8.0) * 2.0 ** -6
+    return sign * (1.0 + m / 8.0) * 2.0 ** (e - 7)
+
+
+_E4M3_POS = np.array([e4m3_decode(c) for c in range(0x7F)])      # codes 0 .. 126, ascending values
+
+
+def e4m3_encode(x):
+    """Nearest E4M3 code of x, ties to the even code, saturating at +-448 (the satfinite conversion)."""
+    x = float(x)
+    sign = 0x80 if (x < 0 or (x == 0 and math.copysign(1.0, x) < 0)) else 0
+    a = min(abs(x), 448.0)
+    i = int(np.searchsorted(_E4M3_POS, a))          # first code with value >= a
+    if i == 0:
+        return sign
+    lo, hi = i - 1, min(i, 0x7E)
+    dl, dh = a - _E4M3_POS[lo], _E4M3_POS[hi] - a
+    if dl < dh or (dl == dh and lo % 2 == 0):
+        return sign | lo
+    return sign | hi
+
+
+def quantize_rows_e4m3(W):
+    """Per-output-row FP8 weights ("EAGLE head deep dive", deployment: the drafter quantized to FP8 by
+    post-training quantization with weight scales).  Reading: scale_n = max_k |W[n, k]| / 448 (1 for an
+    all-zero row), q[n, k] = E4M3(W[n, k] / scale_n), both in fp32 as the GPU forms them; the weight the
+    head then uses is decode(q) * scale_n.  Returns (codes uint8 [N, K], scales fp32 [N], dequantized
+    fp64 [N, K])."""
+    W = np.asarray(W, dtype=np.float32)
+    N, K = W.shape
+    amax = np.abs(W).max(axis=1)
+    scales = np.where(amax > 0, amax / np.float32(448.0), np.float32(1.0)).astype(np.float32)
+    codes = np.zeros((N, K), dtype=np.uint8)
+    for n in range(N):
+        inv = W[n] / scales[n]                       # fp32 division, as the GPU divides
+        codes[n] = [e4m3_encode(v) for v in inv.astype(np.float32)]
+    deq = np.vectorize(e4m3_decode)(codes).astype(np.float64) * scales[:, None].astype(np.float64)
+    return codes, scales, deq

@@ -394,3 +394,38 @@ def test_accept_residual_special_cases():
     p0 = np.array([[[0.5, 0.5, 0.0], [1.0, 0.0, 0.0], [1.0, 0.0, 0.0]]])
     acc, nxt, _ = O.accept_residual([[2, 0]], q, p0, [[0.0, 0.0]], [[0.75, 0.0]])
     assert acc[0] == 0 and nxt[0] == 1
+
+
+def test_e4m3_table_and_round_trip():
+    # published E4M3 facts: largest finite 448, smallest subnormal 2^-9, smallest normal 2^-6, one NaN code
+    assert O.e4m3_decode(0x7E) == 448.0 and O.e4m3_decode(0xFE) == -448.0
+    assert O.e4m3_decode(0x01) == 2.0 ** -9 and O.e4m3_decode(0x08) == 2.0 ** -6
+    assert np.isnan(O.e4m3_decode(0x7F)) and np.isnan(O.e4m3_decode(0xFF))
+    assert O.e4m3_decode(0x38) == 1.0 and O.e4m3_decode(0x40) == 2.0 and O.e4m3_decode(0x3C) == 1.5
+    for c in list(range(0x7F)) + list(range(0x81, 0xFF)):
+        assert O.e4m3_encode(O.e4m3_decode(c)) == c, hex(c)
+
+
+def test_e4m3_rounding_ties_and_saturation():
+    assert O.e4m3_encode(1.0625) == 0x38          # midpoint of 1.0 (even code 0x38) and 1.125 -> even
+    assert O.e4m3_encode(1.1875) == 0x3A          # midpoint of 1.125 (0x39) and 1.25 (0x3A) -> even
+    assert O.e4m3_encode(1.07) == 0x39
+    assert O.e4m3_encode(1e6) == 0x7E and O.e4m3_encode(-1e6) == 0xFE
+    assert O.e4m3_encode(2.0 ** -11) == 0x00     # below half the smallest subnormal
+
+
+def test_quantize_rows_e4m3_error_bound():
+    rng = np.random.default_rng(14)
+    W = (rng.normal(0, 0.02, size=(9, 40))).astype(np.float32)
+    W[3] = 0.0
+    codes, scales, deq = O.quantize_rows_e4m3(W)
+    assert codes.dtype == np.uint8 and scales.shape == (9,)
+    amax = np.abs(W).max(axis=1)
+    # each row's largest magnitude maps to 448 exactly; relative error of E4M3 <= 2^-4 per element
+    for n in range(9):
+        if amax[n] == 0:
+            assert scales[n] == 1.0 and np.all(deq[n] == 0)
+            continue
+        assert np.max(np.abs(deq[n])) == pytest.approx(amax[n], rel=1e-6)
+        err = np.abs(deq[n] - W[n])
+        assert np.all(err <= np.maximum(np.abs(W[n]) * 2.0 ** -4, scales[n] * 2.0 ** -10) * (1 + 1e-6))
