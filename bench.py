@@ -45,6 +45,8 @@ def parse_args(argv=None):
     p.add_argument("--e2e-steps", type=int, default=None)
     p.add_argument("--sampling", default=None,
                    help="T,top_k,top_p: sampled drafts and residual acceptance instead of greedy rounds")
+    p.add_argument("--weights", choices=["bf16", "fp8"], default="bf16",
+                   help="fp8: the nine projection matrices as FP8 E4M3 codes with per-row fp32 scales")
     return p.parse_args(argv)
 
 
@@ -177,12 +179,15 @@ class ClockSampler:
 
 
 # --------------------------------------------------------------------------------------------- bytes model
-def algorithmic_bytes(w, ctx_lengths):
+def algorithmic_bytes(w, ctx_lengths, fp8=False):
     """Algorithmic HBM bytes of each kernel launch kind for one round (weights + KV + activations).
 
     Returns {kind: (bytes_per_launch, launches_per_round)}; activations are fp32 in the workspace.
+    fp8: the projection matrices (all but kv_b) take one byte per weight plus a 4-byte scale per row.
     """
     ws = 2 if w.dtype == "bf16" else 4
+    wp = 1 if fp8 else ws                      # bytes per projection weight
+    sc = 4 if fp8 else 0                       # bytes per projection row (its scale)
     B, T, G, H = w.batch, w.t_new, w.gamma, w.hidden
     nh, dq, dc, dr, dn, dv, I = w.n_heads, w.q_lora_rank, w.kv_lora_rank, w.qk_rope_dim, w.qk_nope_dim, \
         w.v_head_dim, w.intermediate
@@ -196,18 +201,18 @@ def algorithmic_bytes(w, ctx_lengths):
         # average bytes per launch over the round
         out[kind] = ((b * c + per_launch * n) / (c + n) if c + n else 0.0, c + n)
 
-    add("fc", H * 3 * H * ws + Me * 3 * H * ws + Me * H * 4, 1)
+    add("fc", H * (3 * H * wp + sc) + Me * 3 * H * ws + Me * H * 4, 1)
     for M, n in ((Me, 1), (Md, steps)):
         if n == 0:
             continue
-        add("q_a_kv_a", (dq + D) * 2 * H * ws + M * 2 * H * 4 + M * (dq + D) * 4, n)
-        add("q_b", nh * dqk * dq * ws + M * dq * 4 + M * nh * dqk * 4, n)
+        add("q_a_kv_a", (dq + D) * (2 * H * wp + sc) + M * 2 * H * 4 + M * (dq + D) * 4, n)
+        add("q_b", nh * dqk * (dq * wp + sc) + M * dq * 4 + M * nh * dqk * 4, n)
         add("absorb", nh * dn * dc * ws + M * nh * dqk * 4 + M * nh * D * 4, n)
         add("unabsorb", nh * dv * dc * ws + M * nh * dc * 4 + M * nh * dv * 4, n)
-        add("o_proj", H * nh * dv * ws + M * nh * dv * 4 + 2 * M * H * 4, n)
-        add("gate_up_silu", 2 * I * H * ws + M * H * 4 + M * I * 4, n)
-        add("down", H * I * ws + M * I * 4 + 2 * M * H * 4, n)
-        add("lm_head_argmax", w.draft_vocab * H * ws + B * H * 4, n)
+        add("o_proj", H * (nh * dv * wp + sc) + M * nh * dv * 4 + 2 * M * H * 4, n)
+        add("gate_up_silu", 2 * I * (H * wp + sc) + M * H * 4 + M * I * 4, n)
+        add("down", H * (I * wp + sc) + M * I * 4 + 2 * M * H * 4, n)
+        add("lm_head_argmax", w.draft_vocab * (H * wp + sc) + B * H * 4, n)
     # attention must read each sequence's live latent rows once (the cached prefix plus the new rows);
     # the causal re-reads of an extend's rows by later rows are served on chip
     L = [int(x) for x in ctx_lengths]
@@ -298,7 +303,8 @@ def run_ours(args, ws, rank, local):
     ex = WL.make_extend(w, lengths)
     d2t = WL.make_d2t(w)
 
-    head = HN.DeviceHead(w, stored)
+    fp8 = args.weights == "fp8"
+    head = HN.DeviceHead(w, stored, fp8=fp8)
     cache = head.cache(paged)
     len0 = cache.lengths.clone()
     din = head.extend_inputs(ex)
@@ -481,7 +487,8 @@ def run_ours(args, ws, rank, local):
     # ---------------------------------------------------------------- roofline of the dominant kernel
     peaks, src = measured_peaks()
     hbm = peak_hbm(peaks)
-    model = algorithmic_bytes(w, lengths)
+    model = algorithmic_bytes(w, lengths, fp8=fp8)
+    traffic_key = w.name + ("+fp8" if fp8 else "")
     fmodel = algorithmic_flops(w, lengths, unabsorbed_extend="kv_expand" in prof_all)
     tpeak, tkey = peak_tensor(peaks)
     kernels = {}
@@ -517,11 +524,14 @@ def run_ours(args, ws, rank, local):
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": ws, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms_max / args.steps, 4), "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "data": "synthetic (seeded; random-init weights)",
+        "scaling": "weak", "vs_baseline": None,
+        "dtype": "fp8_e4m3 weights, bf16 activations and cache, fp32 accumulate" if fp8 else w.dtype, "data": "synthetic (seeded; random-init weights)",
         "config": {"workload": f"{w.name}: DSV3-shaped EAGLE-3 head, batch {B}, context {w.ctx[0]}-{w.ctx[1]}, "
                                f"T_new {w.t_new}, gamma {G}, draft vocab {w.draft_vocab}"
                                + (" with d2t" if w.d2t else ""),
                    "batch": B, "gamma": G, "ctx": list(w.ctx), "draft_vocab": w.draft_vocab,
+                   "weights": ("FP8 E4M3 projection matrices with per-row fp32 scales (quantized on the GPU "
+                               "from the bf16 weights); kv_b, embedding and norms bf16") if fp8 else w.dtype,
                    "step": "extend + (gamma-1) decode steps + acceptance" if sampling is None else
                            f"extend + (gamma-1) sampled decode steps (T {sampling[0]}, top_k {sampling[1]}, "
                            f"top_p {sampling[2]}) + residual acceptance",
@@ -529,13 +539,13 @@ def run_ours(args, ws, rank, local):
                    "parallelism": f"replicas x{ws} (sequence-sharded, no collective)"},
         "roofline": ({"bound": "tensor", "kernel": dom, "achieved": round(achieved_tf, 1), "peak": tpeak,
                       "unit": "TFLOP/s", "frac": round(achieved_tf / tpeak, 4),
-                      "traffic": measured_traffic(dom, w.name), "avg_us": round(dom_avg_s * 1e6, 2),
+                      "traffic": measured_traffic(dom, traffic_key), "avg_us": round(dom_avg_s * 1e6, 2),
                       "algo_flops_per_launch": int(dom_flops), "algo_bytes_per_launch": int(dom_bytes),
                       "hbm_frac": round(achieved / hbm, 4),
                       "peak_source": f"{src} ({tkey if src == 'measured' else 'fallback 1.7 PFLOP/s sustained'})"}
                      if tensor_bound else
                      {"bound": "hbm", "kernel": dom, "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
-                      "frac": round(achieved / hbm, 4), "traffic": measured_traffic(dom, w.name),
+                      "frac": round(achieved / hbm, 4), "traffic": measured_traffic(dom, traffic_key),
                       "avg_us": round(dom_avg_s * 1e6, 2), "algo_bytes_per_launch": int(dom_bytes),
                       "algo_flops_per_launch": int(dom_flops),
                       "tensor_frac": round(achieved_tf / tpeak, 4),

@@ -26,13 +26,13 @@ namespace {
 enum Kind {
     K_FC = 0, K_EMBED, K_QKV_A, K_LATENT, K_Q_B, K_ABSORB, K_ATTN, K_COMBINE, K_O_PROJ, K_POST_NORM,
     K_GATE_UP, K_DOWN, K_FINAL, K_LM_HEAD, K_ARGMAX, K_EMIT, K_ROPE_Q, K_UNABSORB, K_KV_GATHER, K_KV_EXPAND,
-    K_PREFILL_TILES, K_SAMPLE, K_COUNT
+    K_PREFILL_TILES, K_SAMPLE, K_DEQUANT, K_COUNT
 };
 static_assert(K_COUNT <= EAGLE3_PROF_KINDS, "profile kinds");
 const char* kKindNames[EAGLE3_PROF_KINDS] = {
     "fc", "embed_norms", "q_a_kv_a", "latent_rope_append", "q_b", "absorb", "attention", "merge_splits",
     "o_proj", "post_attn_norm", "gate_up_silu", "down", "final_norm", "lm_head_argmax", "argmax_remap",
-    "emit_first", "rope_q", "unabsorb", "kv_gather", "kv_expand", "prefill_tiles", "sample", "", ""};
+    "emit_first", "rope_q", "unabsorb", "kv_gather", "kv_expand", "prefill_tiles", "sample", "dequant_fp8", ""};
 constexpr int kProfPairs = 32768;
 constexpr int kGemvMaxRows = 8;          // rows above this take the tensor-core path (bf16 heads)
 constexpr int kAttnWaves = 8;            // waves of attention CTAs planned for fixed-chunk splits
@@ -63,6 +63,8 @@ struct eagle3_draft {
     bf16_t *xc = nullptr, *xpe = nullptr, *kvx = nullptr;
     int4* tiles = nullptr;
     int tiles_cap = 0;
+    // FP8 heads on the tensor-core path: the bf16 expansion of the matrix being multiplied
+    bf16_t* wdq = nullptr;
     int *pidx = nullptr, *row_seq = nullptr, *row_pos = nullptr, *d0 = nullptr, *tok_in = nullptr,
         *err = nullptr;
     size_t part_rows = 0;   // capacity of the attention partials in (row, split) pairs
@@ -179,6 +181,9 @@ eagle3_status_t check_config(const eagle3_config_t* c) {
     if (c->qk_rope_dim % 2) return EAGLE3_ERR_INVALID_ARG;
     if (c->rope_interleave != 1) return EAGLE3_ERR_UNSUPPORTED;
     if (c->dtype != EAGLE3_F32 && c->dtype != EAGLE3_BF16) return EAGLE3_ERR_INVALID_ARG;
+    if (c->weight_format != EAGLE3_WEIGHTS_DTYPE && c->weight_format != EAGLE3_WEIGHTS_FP8)
+        return EAGLE3_ERR_INVALID_ARG;
+    if (c->weight_format == EAGLE3_WEIGHTS_FP8 && c->dtype != EAGLE3_BF16) return EAGLE3_ERR_UNSUPPORTED;
     // inner (K) dimensions of every linear layer stream in 8-element chunks
     const long inner[] = {c->hidden, c->q_lora_rank, c->kv_lora_rank, (long)c->n_heads * c->v_head_dim,
                           c->intermediate, c->kv_lora_rank + c->qk_rope_dim};
@@ -196,14 +201,36 @@ eagle3_status_t check_config(const eagle3_config_t* c) {
     return EAGLE3_OK;
 }
 
-eagle3_status_t check_weights(const eagle3_weights_t* w) {
+eagle3_status_t check_weights(const eagle3_config_t& c, const eagle3_weights_t* w) {
     if (!w) return EAGLE3_ERR_INVALID_ARG;
     const void* p[] = {w->embed, w->fc, w->input_norm, w->hidden_norm, w->q_a, w->q_a_norm, w->q_b,
                        w->kv_a, w->kv_a_norm, w->kv_b, w->o, w->post_attn_norm, w->gate, w->up, w->down,
                        w->final_norm, w->lm_head};
     for (const void* v : p)
         if (!v || !aligned16(v)) return EAGLE3_ERR_INVALID_ARG;
+    if (c.weight_format == EAGLE3_WEIGHTS_FP8) {
+        const float* s[] = {w->fc_scale, w->q_a_scale, w->kv_a_scale, w->q_b_scale, w->o_scale, w->gate_scale,
+                            w->up_scale, w->down_scale, w->lm_head_scale};
+        for (const float* v : s)
+            if (!v || ((uintptr_t)v & 3u)) return EAGLE3_ERR_INVALID_ARG;
+    }
     return EAGLE3_OK;
+}
+
+bool fp8_head(const eagle3_config_t& c) { return c.weight_format == EAGLE3_WEIGHTS_FP8; }
+// A projection matrix's row scales when the head stores the matrix as FP8, else null (dtype weights).
+const float* fp8_scale(const eagle3_config_t& c, const float* s) { return fp8_head(c) ? s : nullptr; }
+
+// Elements of the largest FP8 matrix pair one tensor-core GEMM reads (q_a | kv_a and gate | up are
+// expanded together).
+size_t fp8_max_matrix(const eagle3_config_t& c) {
+    const size_t H = c.hidden, nh = c.n_heads, D = c.kv_lora_rank + c.qk_rope_dim;
+    const size_t m[] = {H * 3 * H, (c.q_lora_rank + D) * 2 * H, nh * (c.qk_nope_dim + c.qk_rope_dim) * c.q_lora_rank,
+                        H * nh * c.v_head_dim, 2 * (size_t)c.intermediate * H, H * c.intermediate,
+                        (size_t)c.draft_vocab * H};
+    size_t best = 0;
+    for (size_t v : m) best = v > best ? v : best;
+    return best;
 }
 
 // The tensor-core path needs bf16 weights, every GEMM K a multiple of 64 and the q_a | kv_a split on a
@@ -230,7 +257,7 @@ struct Layout {
 struct Offsets {
     size_t f, carry, x, cqkv, cq_hat, q, qa, qa_bf, part_o, part_ml, o, h1, y, mlp, h2, z, pval, pidx, rope_cos,
         rope_sin, row_seq, row_pos, d0, tok_in, err, olat, x_bf, cqh_bf, q_bf, olat_bf, o_bf, y_bf, m_bf, z_bf, wukt,
-        tc_part, xc, xpe, kvx, tiles, logits, total;
+        tc_part, xc, xpe, kvx, tiles, logits, wdq, total;
     int tiles_cap;
     int m_cap, splits_cap, npart;
     size_t part_rows;
@@ -306,6 +333,7 @@ Offsets plan(const eagle3_config_t& c, int num_sms) {
     o.xpe = L.take(slots * c.qk_rope_dim * b2);
     o.kvx = L.take(slots * nh * (c.qk_nope_dim + c.v_head_dim) * b2);
     o.tiles = L.take((size_t)o.tiles_cap * sizeof(int4));
+    o.wdq = L.take(tc && fp8_head(c) && M > kGemvMaxRows ? fp8_max_matrix(c) * b2 : 0);
     o.total = L.off;
     return o;
 }
@@ -376,6 +404,8 @@ struct Lin {
     const void* w0 = nullptr;
     const void* w1 = nullptr;
     int n0rows = 0, n1rows = 0;
+    const float* s0 = nullptr;                 // FP8 heads: per-row scales of w0 / w1 (the codes' format)
+    const float* s1 = nullptr;
     float* y = nullptr; long ldy = 0;          // fp32 output (GEMV path always; tensor path when set)
     bf16_t* ybf = nullptr; long ldybf = 0;     // bf16 output for the next tensor-core GEMM
     const float* resid = nullptr; long ldr = 0;
@@ -410,7 +440,8 @@ cudaError_t run_linear(eagle3_draft& d, const Lin& L, int kind, cudaStream_t st)
         g.nseg_w = (L.epi != EPI_GLU && L.w1) ? 2 : 1;
         g.M = L.M; g.N = L.N; g.K = L.K;
         g.a_type = L.a32_is_bf16 ? BF16 : F32;
-        g.w_type = d.cfg.dtype == EAGLE3_BF16 ? BF16 : F32;
+        g.w_type = L.s0 ? FP8 : (d.cfg.dtype == EAGLE3_BF16 ? BF16 : F32);
+        g.wscale[0] = L.s0; g.wscale[1] = L.s1;
         g.y = L.y; g.ldy = L.ldy;
         g.resid = L.resid; g.ldr = L.ldr;
         g.pval = d.pval; g.pidx = d.pidx; g.logits = L.logits; g.ldl = L.ldl;
@@ -425,8 +456,28 @@ cudaError_t run_linear(eagle3_draft& d, const Lin& L, int kind, cudaStream_t st)
     memset(&p, 0, sizeof(p));
     const int bn = tc_pick_bn(L.M);
     const bool glu = L.epi == EPI_GLU;
-    if (!make_tma_2d(&p.mw[0], L.w0, glu ? L.N : L.n0rows, L.K, L.K, 128)) return cudaErrorInvalidValue;
-    if (L.w1 && !make_tma_2d(&p.mw[1], L.w1, glu ? L.N : L.n1rows, L.K, L.K, 128)) return cudaErrorInvalidValue;
+    const void* w0 = L.w0;
+    const void* w1 = L.w1;
+    const long r0 = glu ? L.N : L.n0rows, r1 = glu ? L.N : L.n1rows;
+    if (L.s0) {
+        // FP8 weights: expand the codes to bf16 (decode(code) * scale, rounded) in the workspace; the
+        // GEMM then runs as for a bf16 head
+        if (!d.wdq || (size_t)(r0 + (L.w1 ? r1 : 0)) * L.K > fp8_max_matrix(d.cfg) || (L.w1 && !L.s1))
+            return cudaErrorInvalidValue;
+        E3_TRY(traced(d, K_DEQUANT, st, [&] {
+            return launch_dequant_e4m3(static_cast<const uint8_t*>(L.w0), L.s0, r0, L.K, d.wdq, d.num_sms, st);
+        }));
+        w0 = d.wdq;
+        if (L.w1) {
+            E3_TRY(traced(d, K_DEQUANT, st, [&] {
+                return launch_dequant_e4m3(static_cast<const uint8_t*>(L.w1), L.s1, r1, L.K, d.wdq + r0 * L.K,
+                                           d.num_sms, st);
+            }));
+            w1 = d.wdq + r0 * L.K;
+        }
+    }
+    if (!make_tma_2d(&p.mw[0], w0, r0, L.K, L.K, 128)) return cudaErrorInvalidValue;
+    if (w1 && !make_tma_2d(&p.mw[1], w1, r1, L.K, L.K, 128)) return cudaErrorInvalidValue;
     for (int i = 0; i < L.na; ++i)
         if (!make_tma_2d(&p.mx[i], L.a16[i], L.M, L.ka[i], L.lda[i], bn)) return cudaErrorInvalidValue;
     p.np0 = L.w1 && !glu ? L.n0rows : 1 << 30;
@@ -531,6 +582,7 @@ cudaError_t run_layer(eagle3_draft& d, eagle3_kv_t* kv, int M, const float* fuse
     {
         Lin L = lin1(d, M, d.x, d.x_bf, 2 * H, w.q_a, dq + D);
         L.w1 = w.kv_a; L.n0rows = dq; L.n1rows = D;
+        L.s0 = fp8_scale(c, w.q_a_scale); L.s1 = fp8_scale(c, w.kv_a_scale);
         L.y = d.cqkv; L.ldy = dq + D;
         E3_TRY(run_linear(d, L, K_QKV_A, st));
     }
@@ -540,6 +592,7 @@ cudaError_t run_layer(eagle3_draft& d, eagle3_kv_t* kv, int M, const float* fuse
     }));
     {
         Lin L = lin1(d, M, d.cq_hat, d.cqh_bf, dq, w.q_b, nh * dqk);
+        L.s0 = fp8_scale(c, w.q_b_scale);
         // the tensor-core path keeps only the bf16 rows: every consumer (absorb GEMM, rope, attention)
         // reads bf16
         if (tc) { L.ybf = d.q_bf; L.ldybf = (long)nh * dqk; } else { L.y = d.q; L.ldy = (long)nh * dqk; }
@@ -589,6 +642,7 @@ cudaError_t run_layer(eagle3_draft& d, eagle3_kv_t* kv, int M, const float* fuse
     // o_proj + residual
     {
         Lin L = lin1(d, M, d.o, d.o_bf, nh * dv, w.o, H);
+        L.s0 = fp8_scale(c, w.o_scale);
         L.epi = EPI_RESID; L.resid = fused; L.ldr = H;
         L.y = d.h1; L.ldy = H;
         E3_TRY(run_linear(d, L, K_O_PROJ, st));
@@ -599,11 +653,13 @@ cudaError_t run_layer(eagle3_draft& d, eagle3_kv_t* kv, int M, const float* fuse
     {
         Lin L = lin1(d, M, d.y, d.y_bf, H, w.gate, I);
         L.epi = EPI_GLU; L.w1 = w.up; L.n1rows = I;
+        L.s0 = fp8_scale(c, w.gate_scale); L.s1 = fp8_scale(c, w.up_scale);
         if (tc) { L.ybf = d.m_bf; L.ldybf = I; } else { L.y = d.mlp; L.ldy = I; }
         E3_TRY(run_linear(d, L, K_GATE_UP, st));
     }
     {
         Lin L = lin1(d, M, d.mlp, d.m_bf, I, w.down, H);
+        L.s0 = fp8_scale(c, w.down_scale);
         L.epi = EPI_RESID; L.resid = d.h1; L.ldr = H;
         L.y = d.h2; L.ldy = H;
         E3_TRY(run_linear(d, L, K_DOWN, st));
@@ -613,6 +669,7 @@ cudaError_t run_layer(eagle3_draft& d, eagle3_kv_t* kv, int M, const float* fuse
 
 cudaError_t run_head(eagle3_draft& d, int batch, float* logits_out, cudaStream_t st) {
     Lin L = lin1(d, batch, d.z, d.z_bf, d.cfg.hidden, d.w.lm_head, d.cfg.draft_vocab);
+    L.s0 = fp8_scale(d.cfg, d.w.lm_head_scale);
     L.epi = EPI_ARGMAX; L.logits = logits_out; L.ldl = d.cfg.draft_vocab;
     return run_linear(d, L, K_LM_HEAD, st);
 }
@@ -655,7 +712,7 @@ eagle3_status_t eagle3_draft_create(const eagle3_config_t* config, const eagle3_
     *out = nullptr;
     eagle3_status_t s = check_config(config);
     if (s != EAGLE3_OK) return s;
-    if ((s = check_weights(weights)) != EAGLE3_OK) return s;
+    if ((s = check_weights(*config, weights)) != EAGLE3_OK) return s;
     eagle3_draft* d = new (std::nothrow) eagle3_draft();
     if (!d) return EAGLE3_ERR_OOM;
     d->cfg = *config;
@@ -694,6 +751,7 @@ eagle3_status_t eagle3_draft_create(const eagle3_config_t* config, const eagle3_
     d->logits = F(o.logits);
     d->tiles = o.tiles_cap ? reinterpret_cast<int4*>(base + o.tiles) : nullptr;
     d->tiles_cap = o.tiles_cap;
+    d->wdq = fp8_head(d->cfg) && d->tc_ok && o.m_cap > kGemvMaxRows ? Bf(o.wdq) : nullptr;
     std::vector<float> cs, sn;
     yarn_table(d->cfg, cs, sn);
     e = cudaMemcpy(d->rope_cos, cs.data(), cs.size() * sizeof(float), cudaMemcpyHostToDevice);
@@ -738,6 +796,7 @@ eagle3_status_t eagle3_draft_extend(eagle3_draft_t* d, const void* const aux_hid
         }
         L.a32_is_bf16 = ra.dt == BF16;
         L.w0 = d->w.fc; L.n0rows = H;
+        L.s0 = fp8_scale(d->cfg, d->w.fc_scale);
         L.y = d->f; L.ldy = H;
         E3_CUDA(run_linear(*d, L, K_FC, st));
     }
@@ -849,6 +908,7 @@ eagle3_status_t eagle3_draft_decode_sampled(eagle3_draft_t* d, int32_t gamma, co
         }));
         {
             Lin L = lin1(*d, B, d->z, d->z_bf, H, d->w.lm_head, Vd);
+            L.s0 = fp8_scale(d->cfg, d->w.lm_head_scale);
             L.y = lo; L.ldy = Vd;
             E3_CUDA(run_linear(*d, L, K_LM_HEAD, st));
         }

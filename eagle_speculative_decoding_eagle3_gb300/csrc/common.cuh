@@ -2,6 +2,7 @@
 #pragma once
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <stdint.h>
 
 #include <utility>
@@ -66,6 +67,33 @@ __device__ __forceinline__ void widen(const Raw8<float>& r, float* v) {
 }
 __device__ __forceinline__ Raw8<bf16> zero8(bf16*) { return {make_uint4(0, 0, 0, 0)}; }
 __device__ __forceinline__ Raw8<float> zero8(float*) { return {make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0)}; }
+
+// One FP8 E4M3 code (OCP 8-bit floating point: sign, 4 exponent bits with bias 7, 3 mantissa bits).
+struct fp8e4 { uint8_t v; };
+template <> struct Raw8<fp8e4> { uint2 a; };
+template <> __device__ __forceinline__ Raw8<fp8e4> ld8<true, fp8e4>(const fp8e4* p) {
+    uint2 r;
+    asm volatile("ld.global.nc.L1::no_allocate.v2.u32 {%0,%1}, [%2];" : "=r"(r.x), "=r"(r.y) : "l"(p));
+    return {r};
+}
+template <> __device__ __forceinline__ Raw8<fp8e4> ld8<false, fp8e4>(const fp8e4* p) {
+    return {__ldg(reinterpret_cast<const uint2*>(p))};
+}
+// Four E4M3 codes (byte i = element i) to fp32.  Every E4M3 value is exact in fp16 (and so in fp32):
+// the hardware conversion e4m3x2 -> f16x2 puts the low byte in the low half.
+__device__ __forceinline__ void e4m3x4_to_f32(uint32_t w, float* v) {
+    uint32_t h01, h23;
+    asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %2;\n\t"
+        "cvt.rn.f16x2.e4m3x2 %0, lo;\n\tcvt.rn.f16x2.e4m3x2 %1, hi;\n\t}"
+        : "=r"(h01), "=r"(h23) : "r"(w));
+    const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&h01));
+    const float2 b = __half22float2(*reinterpret_cast<const __half2*>(&h23));
+    v[0] = a.x; v[1] = a.y; v[2] = b.x; v[3] = b.y;
+}
+__device__ __forceinline__ void widen(const Raw8<fp8e4>& r, float* v) {
+    e4m3x4_to_f32(r.a.x, v); e4m3x4_to_f32(r.a.y, v + 4);
+}
+__device__ __forceinline__ Raw8<fp8e4> zero8(fp8e4*) { return {make_uint2(0, 0)}; }
 
 // --------------------------------------------------------------------------------------------
 // reductions

@@ -1,361 +1,8 @@
-// Weight-streaming GEMM for few activation rows (decode and small extends).
-//
-// y[m, n] = sum_k A[m, k] W[n, k] — the bias-free linear layers of the draft head (fc, q_a | kv_a,
-// q_b, o_proj, gate | up, down, lm_head, the per-head value up-projection; "Eagle3 DeepseekV3 in MAX"
-// §4).  At a handful of rows a layer is bound by streaming W from HBM once, so the kernel is laid out
-// for HBM:
-//  * one balanced wave: the grid holds kGemvCtasPerSm CTAs per SM and every warp owns an equal range of
-//    weight rows (rows_per_warp), so no SM idles in a half-empty last wave;
-//  * a warp streams R of its rows at once (R = 1 or 4), each with U 16-byte non-allocating loads per
-//    lane (lane l reads elements [8l + 256c, +8) of a row), so about 16 loads of 16 B are in flight per
-//    lane and ~128 KB per SM whatever the row length;
-//  * the activation rows (up to MR) stay L1/L2 resident and are loaded once per chunk for all R rows;
-//  * at the end of each pass the warp reduces its partial dot products and applies the fused epilogue:
-//    store, residual add, SiLU(gate) * up (two weight rows per output), or a running row argmax with
-//    the lowest index winning ties (the logits never round-trip through HBM unless a debug buffer asks
-//    for them).
-// Two kernels share this layout: gemv_kernel gives each warp whole rows; gemv_ks_kernel splits every row
-// across the warps of a row group, for layers whose rows are long and few per warp.
-#include <float.h>
-#include <limits.h>
-
-#include "common.cuh"
-#include "kernels.h"
+// Weight-streaming GEMM for few activation rows: the fp32 and bf16 weight instantiations (the
+// kernels and their launch logic are in gemv.cuh).
+#include "gemv.cuh"
 
 namespace e3 {
-
-constexpr int kGemvWarps = 8;
-constexpr int kGemvCtasPerSm = 2;
-constexpr int kLoadsInFlight = 16;     // 16-byte weight loads per lane per iteration
-
-template <typename TA, typename TW, int MR, int EPI, int R>
-__global__ void __launch_bounds__(kGemvWarps * 32, kGemvCtasPerSm) gemv_kernel(const GemvArgs g, int rows_per_warp) {
-    constexpr int NW = (EPI == EPI_GLU) ? 2 : 1;   // weight rows read per output column
-    constexpr int U0 = kLoadsInFlight / (R * NW) * 2 / (int)sizeof(TW);
-    constexpr int U = U0 < 1 ? 1 : U0;
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int m0 = blockIdx.x * MR;
-    const int mcount = min(MR, g.M - m0);
-    const int K = g.K;
-    const int r_begin = (blockIdx.y * kGemvWarps + warp) * rows_per_warp;
-    const int r_end = min(g.N, r_begin + rows_per_warp);
-    const int ka0 = g.ka[0], ka01 = g.ka[0] + g.ka[1];
-
-    auto wrow = [&](int n, int q) -> const TW* {
-        if (EPI == EPI_GLU) return reinterpret_cast<const TW*>(g.w[q]) + (long)n * K;
-        if (g.w_grp)
-            return reinterpret_cast<const TW*>(g.w[0]) +
-                   ((long)(n / g.w_grp) * g.w_grp_stride + g.w_row0 + n % g.w_grp) * K;
-        const int seg = (g.nseg_w > 1 && n >= g.nw[0]) ? 1 : 0;
-        return reinterpret_cast<const TW*>(g.w[seg]) + (long)(seg ? n - g.nw[0] : n) * K;
-    };
-
-    float best_v[MR];
-    int best_i[MR];
-#pragma unroll
-    for (int i = 0; i < MR; ++i) { best_v[i] = -FLT_MAX; best_i[i] = INT_MAX; }
-
-    // The first batch of weight loads does not depend on the previous kernel: issue it, then wait.
-    pdl_trigger();
-    bool waited = false;
-    for (int p0 = r_begin; p0 < r_end; p0 += R) {
-        const int nr = min(R, r_end - p0);
-        const TW* wp[R][NW];
-#pragma unroll
-        for (int j = 0; j < R; ++j)
-#pragma unroll
-            for (int q = 0; q < NW; ++q) wp[j][q] = wrow(p0 + (j < nr ? j : 0), q);
-        // the per-head GEMVs use one activation slice per row group; all rows of a pass share it
-        const long aoff = g.a_grp ? (long)(p0 / g.a_grp) * g.a_grp_stride : 0;
-        float acc[MR][R][NW];
-#pragma unroll
-        for (int i = 0; i < MR; ++i)
-#pragma unroll
-            for (int j = 0; j < R; ++j)
-#pragma unroll
-                for (int q = 0; q < NW; ++q) acc[i][j][q] = 0.f;
-
-        for (int k0 = lane * 8; k0 < K; k0 += 256 * U) {
-            Raw8<TW> wr[U][R][NW];
-#pragma unroll
-            for (int u = 0; u < U; ++u) {
-                const int k = k0 + u * 256;
-#pragma unroll
-                for (int j = 0; j < R; ++j)
-#pragma unroll
-                    for (int q = 0; q < NW; ++q)
-                        wr[u][j][q] = (k < K && j < nr) ? ld8<true>(wp[j][q] + k) : zero8((TW*)nullptr);
-            }
-            if (!waited) { pdl_wait(); waited = true; }
-#pragma unroll
-            for (int u = 0; u < U; ++u) {
-                const int k = k0 + u * 256;
-                if (k < K) {
-                    const int s = (k >= ka0) + (k >= ka01);
-                    const int kl = k - (s == 0 ? 0 : (s == 1 ? ka0 : ka01));
-                    const TA* ap = reinterpret_cast<const TA*>(g.a[s]) + (long)m0 * g.lda[s] + aoff + kl;
-#pragma unroll
-                    for (int i = 0; i < MR; ++i) {
-                        if (i < mcount) {
-                            float av[8];
-                            widen(ld8<false>(ap + i * g.lda[s]), av);
-#pragma unroll
-                            for (int j = 0; j < R; ++j)
-#pragma unroll
-                                for (int q = 0; q < NW; ++q) {
-                                    float wv[8];
-                                    widen(wr[u][j][q], wv);
-#pragma unroll
-                                    for (int e = 0; e < 8; ++e) acc[i][j][q] = fmaf(wv[e], av[e], acc[i][j][q]);
-                                }
-                        }
-                    }
-                }
-            }
-        }
-#pragma unroll
-        for (int i = 0; i < MR; ++i)
-#pragma unroll
-            for (int j = 0; j < R; ++j)
-#pragma unroll
-                for (int q = 0; q < NW; ++q) acc[i][j][q] = warp_sum(acc[i][j][q]);
-#pragma unroll
-        for (int i = 0; i < MR; ++i) {
-            if (i >= mcount) continue;
-            const long m = m0 + i;
-#pragma unroll
-            for (int j = 0; j < R; ++j) {
-                if (j >= nr) continue;
-                const int n = p0 + j;
-                if (EPI == EPI_ARGMAX) {
-                    if (better(acc[i][j][0], n, best_v[i], best_i[i])) { best_v[i] = acc[i][j][0]; best_i[i] = n; }
-                    if (g.logits != nullptr && lane == (i * R + j) % 32) g.logits[m * g.ldl + n] = acc[i][j][0];
-                } else if (lane == (i * R + j) % 32) {
-                    float v;
-                    if (EPI == EPI_GLU) v = silu(acc[i][j][0]) * acc[i][j][NW - 1];
-                    else if (EPI == EPI_RESID) v = acc[i][j][0] + g.resid[m * g.ldr + n];
-                    else v = acc[i][j][0];
-                    g.y[m * g.ldy + n] = v;
-                }
-            }
-        }
-    }
-
-    if (!waited) pdl_wait();
-    if (EPI == EPI_ARGMAX) {
-        __shared__ float sv[kGemvWarps][MR];
-        __shared__ int si[kGemvWarps][MR];
-        if (lane == 0) {
-#pragma unroll
-            for (int i = 0; i < MR; ++i) { sv[warp][i] = best_v[i]; si[warp][i] = best_i[i]; }
-        }
-        __syncthreads();
-        if (threadIdx.x < MR && (int)threadIdx.x < mcount) {
-            const int i = threadIdx.x;
-            float bv = sv[0][i];
-            int bi = si[0][i];
-            for (int w = 1; w < kGemvWarps; ++w)
-                if (better(sv[w][i], si[w][i], bv, bi)) { bv = sv[w][i]; bi = si[w][i]; }
-            g.pval[(long)(m0 + i) * g.npart + blockIdx.y] = bv;
-            g.pidx[(long)(m0 + i) * g.npart + blockIdx.y] = bi;
-        }
-    }
-}
-
-// K-split variant for long rows (bf16 weights, no row grouping).  A CTA owns `rpc` consecutive output
-// columns; its 8 warps form RG = 8 / KS row groups of KS warps, and the KS warps of a group split K
-// (warp k of a group reads the 256-element chunks [k nch / KS, (k + 1) nch / KS) of every row).  A group
-// streams R rows at once (U chunks each, 16 loads of 16 B in flight per lane), so one activation load
-// feeds R rows instead of the whole-row kernel's few, and a layer with few rows per warp (q_a | kv_a:
-// 2112 rows for 2432 warps) still keeps every warp busy.  Each round the RG groups take one pass of R
-// rows each; the KS partial sums of every output meet in shared memory, where the epilogue is applied.
-template <typename TA, int MR, int EPI, int R>
-__global__ void __launch_bounds__(kGemvWarps * 32, kGemvCtasPerSm) gemv_ks_kernel(const GemvArgs g, int rpc, int KS) {
-    constexpr int NW = (EPI == EPI_GLU) ? 2 : 1;
-    constexpr int U0 = kLoadsInFlight / (R * NW);
-    constexpr int U = U0 < 1 ? 1 : U0;
-    constexpr int OUT = MR * R * NW;                 // partial sums per warp and pass
-    __shared__ float red[kGemvWarps][OUT];
-    __shared__ float fin[kGemvWarps * R * MR];       // ARGMAX: the round's reduced scores
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int RG = kGemvWarps / KS, ks = warp % KS, rg = warp / KS;
-    const int m0 = blockIdx.x * MR, mcount = min(MR, g.M - m0);
-    const int K = g.K, nch = (K + 255) / 256;
-    const int c0 = ks * nch / KS, c1 = (ks + 1) * nch / KS;
-    const int row0 = blockIdx.y * rpc, row1 = min(g.N, row0 + rpc);
-    const int npass = (row1 - row0 + R - 1) / R, nround = (npass + RG - 1) / RG;
-    const int ka0 = g.ka[0], ka01 = g.ka[0] + g.ka[1];
-
-    auto wrow = [&](int n, int q) -> const bf16* {
-        if (EPI == EPI_GLU) return reinterpret_cast<const bf16*>(g.w[q]) + (long)n * K;
-        const int seg = (g.nseg_w > 1 && n >= g.nw[0]) ? 1 : 0;
-        return reinterpret_cast<const bf16*>(g.w[seg]) + (long)(seg ? n - g.nw[0] : n) * K;
-    };
-
-    float best_v[MR];
-    int best_i[MR];
-#pragma unroll
-    for (int i = 0; i < MR; ++i) { best_v[i] = -FLT_MAX; best_i[i] = INT_MAX; }
-
-    pdl_trigger();
-    bool waited = false;
-    for (int q = 0; q < nround; ++q) {
-        const int p0 = row0 + (q * RG + rg) * R;
-        const int nr = max(0, min(R, row1 - p0));
-        float acc[MR][R][NW];
-#pragma unroll
-        for (int i = 0; i < MR; ++i)
-#pragma unroll
-            for (int j = 0; j < R; ++j)
-#pragma unroll
-                for (int w = 0; w < NW; ++w) acc[i][j][w] = 0.f;
-        if (nr > 0) {
-            const bf16* wp[R][NW];
-#pragma unroll
-            for (int j = 0; j < R; ++j)
-#pragma unroll
-                for (int w = 0; w < NW; ++w) wp[j][w] = wrow(p0 + (j < nr ? j : 0), w);
-            for (int c = c0; c < c1; c += U) {
-                Raw8<bf16> wr[U][R][NW];
-#pragma unroll
-                for (int u = 0; u < U; ++u) {
-                    const int k = (c + u) * 256 + lane * 8;
-                    const bool ok = c + u < c1 && k < K;
-#pragma unroll
-                    for (int j = 0; j < R; ++j)
-#pragma unroll
-                        for (int w = 0; w < NW; ++w)
-                            wr[u][j][w] = (ok && j < nr) ? ld8<true>(wp[j][w] + k) : zero8((bf16*)nullptr);
-                }
-                if (!waited) { pdl_wait(); waited = true; }
-#pragma unroll
-                for (int u = 0; u < U; ++u) {
-                    const int k = (c + u) * 256 + lane * 8;
-                    if (c + u < c1 && k < K) {
-                        const int s = (k >= ka0) + (k >= ka01);
-                        const int kl = k - (s == 0 ? 0 : (s == 1 ? ka0 : ka01));
-                        const TA* ap = reinterpret_cast<const TA*>(g.a[s]) + (long)m0 * g.lda[s] + kl;
-#pragma unroll
-                        for (int i = 0; i < MR; ++i) {
-                            if (i < mcount) {
-                                float av[8];
-                                widen(ld8<false>(ap + i * g.lda[s]), av);
-#pragma unroll
-                                for (int j = 0; j < R; ++j)
-#pragma unroll
-                                    for (int w = 0; w < NW; ++w) {
-                                        float wv[8];
-                                        widen(wr[u][j][w], wv);
-#pragma unroll
-                                        for (int e = 0; e < 8; ++e) acc[i][j][w] = fmaf(wv[e], av[e], acc[i][j][w]);
-                                    }
-                            }
-                        }
-                    }
-                }
-            }
-        }
-        if (!waited) { pdl_wait(); waited = true; }
-#pragma unroll
-        for (int i = 0; i < MR; ++i)
-#pragma unroll
-            for (int j = 0; j < R; ++j)
-#pragma unroll
-                for (int w = 0; w < NW; ++w) {
-                    const float v = warp_sum(acc[i][j][w]);
-                    if (lane == 0) red[warp][(i * R + j) * NW + w] = v;
-                }
-        __syncthreads();
-        // one thread per (row group, row of the pass, activation row)
-        for (int t = threadIdx.x; t < RG * R * MR; t += blockDim.x) {
-            const int grp = t / (R * MR), rem = t % (R * MR), j = rem / MR, i = rem % MR;
-            const int pj = row0 + (q * RG + grp) * R;
-            const int n = pj + j;
-            float v0 = 0.f, v1 = 0.f;
-            for (int k = 0; k < KS; ++k) {
-                v0 += red[grp * KS + k][(i * R + j) * NW];
-                if (NW == 2) v1 += red[grp * KS + k][(i * R + j) * NW + NW - 1];
-            }
-            const bool valid = i < mcount && n < row1;
-            const long m = m0 + i;
-            if (EPI == EPI_ARGMAX) {
-                fin[t] = valid ? v0 : -FLT_MAX;
-                if (valid && g.logits != nullptr) g.logits[m * g.ldl + n] = v0;
-            } else if (valid) {
-                float v;
-                if (EPI == EPI_GLU) v = silu(v0) * v1;
-                else if (EPI == EPI_RESID) v = v0 + g.resid[m * g.ldr + n];
-                else v = v0;
-                g.y[m * g.ldy + n] = v;
-            }
-        }
-        if (EPI == EPI_ARGMAX) {
-            __syncthreads();
-            const int t = threadIdx.x;
-            if (t < MR) {
-                // ascending column order; better() keeps the lowest index on ties
-                for (int grp = 0; grp < RG; ++grp)
-                    for (int j = 0; j < R; ++j) {
-                        const int n = row0 + (q * RG + grp) * R + j;
-                        const float v = fin[(grp * R + j) * MR + t];
-                        if (n < row1 && better(v, n, best_v[t], best_i[t])) { best_v[t] = v; best_i[t] = n; }
-                    }
-            }
-        }
-        __syncthreads();
-    }
-    if (!waited) pdl_wait();
-    if (EPI == EPI_ARGMAX && (int)threadIdx.x < mcount) {
-        const int i = threadIdx.x;
-        g.pval[(long)(m0 + i) * g.npart + blockIdx.y] = best_v[i];
-        g.pidx[(long)(m0 + i) * g.npart + blockIdx.y] = best_i[i];
-    }
-}
-
-// K slices per row group: 8 when the row's 256-element chunks split evenly into at least two per warp
-// or are many enough (>= 64) that an uneven split costs under an eighth; else the largest of {4, 2} that
-// splits them evenly into at least two per warp; else 1 (whole rows, as in gemv_kernel).
-static int gemv_ks_slices(int K) {
-    const int nch = (K + 255) / 256;
-    if ((nch % 8 == 0 && nch >= 16) || nch >= 64) return 8;
-    for (int ks = 4; ks >= 2; ks >>= 1)
-        if (nch % ks == 0 && nch / ks >= 2) return ks;
-    return 1;
-}
-
-// Rows per pass of the K-split kernel: 16 loads of 16 B in flight per lane and the accumulators within
-// the register budget of two CTAs per SM.
-template <int MR, int EPI>
-constexpr int gemv_ks_rows() {
-    return (EPI == EPI_GLU ? 4 : 8) / (MR >= 8 ? 4 : (MR >= 4 ? 2 : 1));
-}
-
-// Columns per CTA of the K-split kernel: one balanced wave of kGemvCtasPerSm CTAs per SM, whole passes.
-static void gemv_ks_split(int N, int num_sms, int R, int* rpc, int* ctas) {
-    const long slots = (long)num_sms * kGemvCtasPerSm;
-    int r = (int)((N + slots - 1) / slots);
-    r = (r + R - 1) / R * R;
-    *rpc = r;
-    *ctas = (N + r - 1) / r;
-}
-
-// Rows per warp and CTAs along N for one balanced wave of kGemvCtasPerSm CTAs per SM.  A grouped GEMV
-// keeps every pass of R rows inside one activation group.
-static void gemv_split(int N, int num_sms, int group, int* rows_per_warp, int* ctas, int* R) {
-    const long warps = (long)num_sms * kGemvCtasPerSm * kGemvWarps;
-    int rpw = (int)((N + warps - 1) / warps);
-    if (rpw < 1) rpw = 1;
-    *R = rpw < 4 ? rpw : 4;                              // 16 / R loads per row keep 16 in flight
-    if (group && *R > 1) {                               // passes must not straddle a group
-        *R = 4;
-        int r = (rpw + 3) / 4 * 4;
-        while (r <= group && group % r) r += 4;
-        if (r <= group && group % r == 0) rpw = r;
-        else *R = 1;                                     // one-row passes never straddle
-    }
-    *rows_per_warp = rpw;
-    *ctas = (N + kGemvWarps * rpw - 1) / (kGemvWarps * rpw);
-}
 
 // Upper bound of the ARGMAX partials per row (one per CTA): both kernels run one wave of at most
 // kGemvCtasPerSm CTAs per SM.  The launch reports the count it used in GemvArgs::npart.
@@ -364,65 +11,8 @@ int gemv_argmax_parts(int N, int num_sms) {
     return (int)(N < slots ? N : slots);
 }
 
-template <typename TA, typename TW, int MR, int EPI>
-static cudaError_t launch_r(const GemvArgs& g, int R, int rpw, int ctas, cudaStream_t st) {
-    dim3 grid((g.M + MR - 1) / MR, ctas);
-    dim3 block(kGemvWarps * 32);
-    switch (R) {
-        case 1: return launch_pdl(gemv_kernel<TA, TW, MR, EPI, 1>, grid, block, 0, st, g, rpw);
-        case 2: return launch_pdl(gemv_kernel<TA, TW, MR, EPI, 2>, grid, block, 0, st, g, rpw);
-        case 3: return launch_pdl(gemv_kernel<TA, TW, MR, EPI, 3>, grid, block, 0, st, g, rpw);
-        default: return launch_pdl(gemv_kernel<TA, TW, MR, EPI, 4>, grid, block, 0, st, g, rpw);
-    }
-}
-
-template <typename TA, int MR, int EPI>
-static cudaError_t launch_ks(GemvArgs& g, int KS, int num_sms, cudaStream_t st) {
-    constexpr int R = gemv_ks_rows<MR, EPI>();
-    int rpc, ctas;
-    gemv_ks_split(g.N, num_sms, R, &rpc, &ctas);
-    if (EPI == EPI_ARGMAX) g.npart = ctas;
-    dim3 grid((g.M + MR - 1) / MR, ctas);
-    return launch_pdl(gemv_ks_kernel<TA, MR, EPI, R>, grid, dim3(kGemvWarps * 32), 0, st, g, rpc, KS);
-}
-
-template <typename TA, typename TW, int EPI>
-static cudaError_t launch_mr(GemvArgs& g, int num_sms, cudaStream_t st) {
-    const int MR = g.M >= 5 ? 8 : (g.M >= 3 ? 4 : (g.M == 2 ? 2 : 1));
-    // The K-split kernel wins where the whole-row kernel has few rows per warp (long rows: fc, q_a | kv_a,
-    // o_proj, down); with four or more rows per pass the whole-row kernel already reuses each activation
-    // load and streams slightly faster (gate | up, lm_head, q_b on a GB300).
-    const int KS = gemv_ks_slices(g.K);
-    int rpw, ctas, R;
-    gemv_split(g.N, num_sms, g.a_grp, &rpw, &ctas, &R);
-    if (sizeof(TW) == 2 && KS > 1 && rpw <= 4 && !g.w_grp && !g.a_grp) {
-        switch (MR) {
-            case 1: return launch_ks<TA, 1, EPI>(g, KS, num_sms, st);
-            case 2: return launch_ks<TA, 2, EPI>(g, KS, num_sms, st);
-            case 4: return launch_ks<TA, 4, EPI>(g, KS, num_sms, st);
-            default: return launch_ks<TA, 8, EPI>(g, KS, num_sms, st);
-        }
-    }
-    if (EPI == EPI_ARGMAX) g.npart = ctas;
-    switch (MR) {
-        case 1: return launch_r<TA, TW, 1, EPI>(g, R, rpw, ctas, st);
-        case 2: return launch_r<TA, TW, 2, EPI>(g, R, rpw, ctas, st);
-        case 4: return launch_r<TA, TW, 4, EPI>(g, R, rpw, ctas, st);
-        default: return launch_r<TA, TW, 8, EPI>(g, R, rpw, ctas, st);
-    }
-}
-
-template <typename TA, typename TW>
-static cudaError_t launch_epi(GemvArgs& g, int epi, int num_sms, cudaStream_t st) {
-    switch (epi) {
-        case EPI_STORE: return launch_mr<TA, TW, EPI_STORE>(g, num_sms, st);
-        case EPI_RESID: return launch_mr<TA, TW, EPI_RESID>(g, num_sms, st);
-        case EPI_GLU: return launch_mr<TA, TW, EPI_GLU>(g, num_sms, st);
-        default: return launch_mr<TA, TW, EPI_ARGMAX>(g, num_sms, st);
-    }
-}
-
 cudaError_t launch_gemv(GemvArgs& g, int epi, int num_sms, cudaStream_t st) {
+    if (g.w_type == FP8) return launch_gemv_fp8(g, epi, num_sms, st);
     if (g.M <= 0 || g.N <= 0) return cudaSuccess;
     for (int s = g.na; s < 3; ++s) g.ka[s] = 1 << 30;   // unused K segments never match
     if (g.w_type == F32) {

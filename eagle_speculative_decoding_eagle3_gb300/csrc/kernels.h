@@ -8,7 +8,7 @@
 
 namespace e3 {
 
-enum DType { F32 = 0, BF16 = 1 };
+enum DType { F32 = 0, BF16 = 1, FP8 = 2 };   // FP8: E4M3 codes with per-row fp32 scales (GEMV weights)
 
 // ---------------------------------------------------------------- weight-streaming GEMM
 // y[m, n] = sum_k A[m, k] * W[n, k] for m < M, n < N, with
@@ -37,8 +37,14 @@ struct GemvArgs {
     int w_grp; long w_grp_stride; int w_row0;
     int a_grp; long a_grp_stride;
     int* err;                         // device error word (bounded waits that ran out)
+    // w_type FP8: per-output-row scales of w[0] / w[1] (y[m, n] = scale[n] * sum_k A[m, k] code[n, k])
+    const float* wscale[2];
 };
 cudaError_t launch_gemv(GemvArgs& g, int epi, int num_sms, cudaStream_t st);
+cudaError_t launch_gemv_fp8(GemvArgs& g, int epi, int num_sms, cudaStream_t st);   // w_type FP8
+// bf16 expansion of an FP8 E4M3 matrix with per-row scales (K a multiple of 8)
+cudaError_t launch_dequant_e4m3(const uint8_t* codes, const float* scales, long rows, int K, __nv_bfloat16* out,
+                                int num_sms, cudaStream_t st);
 int gemv_argmax_parts(int N, int num_sms);   // partial count of an ARGMAX launch over N columns
 
 // ---------------------------------------------------------------- row kernels

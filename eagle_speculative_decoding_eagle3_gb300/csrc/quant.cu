@@ -1,0 +1,95 @@
+// FP8 E4M3 draft weights: the per-row quantizer (eagle3_quantize_e4m3) and the expansion of an FP8
+// matrix to bf16 that the tensor-core GEMM reads when a call has more rows than the GEMV path serves.
+//
+// The drafter's post-training quantization to FP8 ("EAGLE head deep dive", deployment) stores each
+// projection matrix as E4M3 codes with one fp32 scale per output row:
+//   scale[n] = max_k |W[n, k]| / 448 (1 for an all-zero row), code[n, k] = E4M3(W[n, k] / scale[n]),
+// with the quotient rounded to nearest (ties to the even code) and saturated at +-448 by the hardware
+// conversion cvt.rn.satfinite.e4m3x2.f32, and the head then uses decode(code) * scale.
+#include "common.cuh"
+#include "eagle3.h"
+#include "kernels.h"
+
+namespace e3 {
+
+constexpr int kQuantThreads = 256;
+
+// One CTA per row: the row's absolute maximum, then the codes, two per conversion.
+template <typename T>
+__global__ void __launch_bounds__(kQuantThreads) quantize_e4m3_kernel(const T* __restrict__ w, int K,
+                                                                       uint8_t* __restrict__ codes,
+                                                                       float* __restrict__ scales) {
+    __shared__ float red[kQuantThreads / kWarp];
+    const long n = blockIdx.x;
+    const T* row = w + n * K;
+    float amax = 0.f;
+    for (int k = threadIdx.x; k < K; k += kQuantThreads) amax = fmaxf(amax, fabsf(to_f(row[k])));
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = amax;
+    __syncthreads();
+    amax = red[0];
+#pragma unroll
+    for (int i = 1; i < kQuantThreads / kWarp; ++i) amax = fmaxf(amax, red[i]);
+    const float scale = amax > 0.f ? amax / 448.f : 1.f;     // IEEE fp32 division
+    if (threadIdx.x == 0) scales[n] = scale;
+    uint8_t* out = codes + n * K;
+    for (int k = 2 * threadIdx.x; k < K; k += 2 * kQuantThreads) {
+        const float a = to_f(row[k]) / scale;
+        const float b = k + 1 < K ? to_f(row[k + 1]) / scale : 0.f;
+        uint16_t pair;
+        // the first source operand lands in the upper byte: b, then a, puts element k in the low byte
+        asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(pair) : "f"(b), "f"(a));
+        out[k] = (uint8_t)(pair & 0xFF);
+        if (k + 1 < K) out[k + 1] = (uint8_t)(pair >> 8);
+    }
+}
+
+// out[n, k] = bf16(decode(code[n, k]) * scale[n]) for rows [0, rows), K a multiple of 8: one thread per
+// 8 codes (an 8-byte load, a 16-byte store), a grid-stride loop over one wave.
+__global__ void __launch_bounds__(256) dequant_e4m3_kernel(const uint8_t* __restrict__ codes,
+                                                           const float* __restrict__ scales, long rows, int K,
+                                                           bf16* __restrict__ out) {
+    const long chunks_per_row = K / 8, total = rows * chunks_per_row;
+    for (long c = (long)blockIdx.x * blockDim.x + threadIdx.x; c < total; c += (long)gridDim.x * blockDim.x) {
+        const long n = c / chunks_per_row;
+        const Raw8<fp8e4> r = ld8<true>(reinterpret_cast<const fp8e4*>(codes) + c * 8);
+        float v[8];
+        widen(r, v);
+        const float s = __ldg(scales + n);
+        uint32_t p[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const __nv_bfloat162 h = __floats2bfloat162_rn(v[2 * i] * s, v[2 * i + 1] * s);
+            p[i] = *reinterpret_cast<const uint32_t*>(&h);
+        }
+        *reinterpret_cast<uint4*>(out + c * 8) = make_uint4(p[0], p[1], p[2], p[3]);
+    }
+}
+
+cudaError_t launch_dequant_e4m3(const uint8_t* codes, const float* scales, long rows, int K, bf16* out,
+                                int num_sms, cudaStream_t st) {
+    if (rows <= 0) return cudaSuccess;
+    if (K % 8) return cudaErrorInvalidValue;
+    const long chunks = rows * (K / 8);
+    long ctas = (chunks + 255) / 256;
+    if (ctas > 8L * num_sms) ctas = 8L * num_sms;
+    dequant_e4m3_kernel<<<(int)ctas, 256, 0, st>>>(codes, scales, rows, K, out);
+    return cudaGetLastError();
+}
+
+}  // namespace e3
+
+extern "C" eagle3_status_t eagle3_quantize_e4m3(const void* w, eagle3_dtype_t dtype, int32_t N, int32_t K,
+                                                uint8_t* codes, float* scales, void* stream) {
+    using namespace e3;
+    if (!w || !codes || !scales || N < 1 || K < 1) return EAGLE3_ERR_INVALID_ARG;
+    const cudaStream_t st = (cudaStream_t)stream;
+    if (dtype == EAGLE3_BF16)
+        quantize_e4m3_kernel<bf16><<<N, kQuantThreads, 0, st>>>(static_cast<const bf16*>(w), K, codes, scales);
+    else if (dtype == EAGLE3_F32)
+        quantize_e4m3_kernel<float><<<N, kQuantThreads, 0, st>>>(static_cast<const float*>(w), K, codes, scales);
+    else
+        return EAGLE3_ERR_UNSUPPORTED;
+    return cudaGetLastError() == cudaSuccess ? EAGLE3_OK : EAGLE3_ERR_CUDA;
+}

@@ -14,6 +14,7 @@ _LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libeagle3.
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_STATE, ERR_OOM, ERR_CUDA, ERR_DEVICE_RANGE, ERR_SCRATCH_LIMIT = range(8)
 NOALLOC_SCRATCH_BYTES = 16 << 20   # EAGLE3_NOALLOC_SCRATCH_BYTES
 F32, BF16 = 0, 1
+WEIGHTS_DTYPE, WEIGHTS_FP8 = 0, 1   # eagle3_weight_format_t
 DEVERR_TOKEN, DEVERR_POSITION, DEVERR_D2T, DEVERR_PAGE, DEVERR_ROWS = 1, 2, 4, 8, 16
 
 
@@ -24,15 +25,19 @@ class eagle3_config_t(C.Structure):
         "page_size", "max_pages_per_seq")] + [(n, C.c_float) for n in (
             "rms_eps", "rope_theta", "yarn_factor", "yarn_beta_fast", "yarn_beta_slow", "yarn_mscale",
             "yarn_mscale_all_dim")] + [("yarn_original_max_pos", C.c_int32), ("rope_interleave", C.c_int32),
-                                       ("dtype", C.c_int32)]
+                                       ("dtype", C.c_int32), ("weight_format", C.c_int32)]
 
 
 WEIGHT_NAMES = ("embed", "fc", "input_norm", "hidden_norm", "q_a", "q_a_norm", "q_b", "kv_a", "kv_a_norm", "kv_b",
                 "o", "post_attn_norm", "gate", "up", "down", "final_norm", "lm_head")
 
 
+# the projection matrices that EAGLE3_WEIGHTS_FP8 stores as E4M3 codes with per-row scales
+FP8_WEIGHT_NAMES = ("fc", "q_a", "kv_a", "q_b", "o", "gate", "up", "down", "lm_head")
+
+
 class eagle3_weights_t(C.Structure):
-    _fields_ = [(n, C.c_void_p) for n in WEIGHT_NAMES]
+    _fields_ = [(n, C.c_void_p) for n in WEIGHT_NAMES] + [(n + "_scale", C.c_void_p) for n in FP8_WEIGHT_NAMES]
 
 
 class eagle3_kv_t(C.Structure):
@@ -81,6 +86,7 @@ def _lib():
                                                     P, P, P]
         lib.eagle3_linear.argtypes = [P, P, P, P, C.c_int32, C.c_int32, C.c_int32, P]
         lib.eagle3_linear_noalloc.argtypes = [P, P, P, C.c_int32, C.c_int32, C.c_int32, P]
+        lib.eagle3_quantize_e4m3.argtypes = [P, C.c_int32, C.c_int32, C.c_int32, P, P, P]
         lib.eagle3_draft_get_error.argtypes = [P, C.POINTER(C.c_int32)]
         lib.eagle3_draft_clear_error.argtypes = [P, P]
         lib.eagle3_draft_destroy.argtypes = [P]
@@ -131,10 +137,13 @@ def make_config(**fields) -> eagle3_config_t:
     return c
 
 
-def make_weights(tensors) -> eagle3_weights_t:
+def make_weights(tensors, scales=None) -> eagle3_weights_t:
+    """Weight pointers; `scales` (FP8 heads) maps each of FP8_WEIGHT_NAMES to its row scales."""
     w = eagle3_weights_t()
     for n in WEIGHT_NAMES:
         setattr(w, n, _ptr(tensors[n]))
+    for n in FP8_WEIGHT_NAMES if scales else ():
+        setattr(w, n + "_scale", _ptr(scales[n]))
     return w
 
 
@@ -183,6 +192,12 @@ def eagle3_linear_noalloc(x, w, y, M, N, K, stream=None):
     (its split-K scratch is a fixed array in the library; M * N <= 2^21; overlapping calls race)."""
     _check("eagle3_linear_noalloc", _lib().eagle3_linear_noalloc(_ptr(x), _ptr(w), _ptr(y), int(M), int(N),
                                                                  int(K), _stream(stream)))
+
+
+def eagle3_quantize_e4m3(w, dtype, N, K, codes, scales, stream=None):
+    """Per-row FP8 E4M3 codes [N, K] (uint8) and fp32 scales [N] of the bf16 / fp32 matrix w [N, K]."""
+    _check("eagle3_quantize_e4m3", _lib().eagle3_quantize_e4m3(_ptr(w), int(dtype), int(N), int(K), _ptr(codes),
+                                                               _ptr(scales), _stream(stream)))
 
 
 def eagle3_accept(draft, target, batch, gamma, accepted_len, hist=None, stream=None):

@@ -22,7 +22,7 @@ def to_device(arr: np.ndarray, device="cuda") -> torch.Tensor:
     return torch.from_numpy(arr).to(device)
 
 
-def config_for(w, max_batch=None, max_tokens=None) -> E.eagle3_config_t:
+def config_for(w, max_batch=None, max_tokens=None, fp8=False) -> E.eagle3_config_t:
     return E.make_config(
         hidden=w.hidden, n_heads=w.n_heads, q_lora_rank=w.q_lora_rank, kv_lora_rank=w.kv_lora_rank,
         qk_nope_dim=w.qk_nope_dim, qk_rope_dim=w.qk_rope_dim, v_head_dim=w.v_head_dim,
@@ -32,7 +32,7 @@ def config_for(w, max_batch=None, max_tokens=None) -> E.eagle3_config_t:
         rms_eps=w.rms_eps, rope_theta=w.rope_theta, yarn_factor=w.yarn_factor, yarn_beta_fast=w.yarn_beta_fast,
         yarn_beta_slow=w.yarn_beta_slow, yarn_mscale=w.yarn_mscale, yarn_mscale_all_dim=w.yarn_mscale_all_dim,
         yarn_original_max_pos=w.yarn_original_max_pos, rope_interleave=1,
-        dtype=E.BF16 if w.dtype == "bf16" else E.F32)
+        dtype=E.BF16 if w.dtype == "bf16" else E.F32, weight_format=E.WEIGHTS_FP8 if fp8 else E.WEIGHTS_DTYPE)
 
 
 @dataclass
@@ -46,15 +46,33 @@ class DeviceCache:
         return E.make_kv(self.data, self.block_table, self.lengths, self.num_pages)
 
 
-class DeviceHead:
-    """A created draft head whose weights live in device tensors owned by this object."""
+def quantize_fp8(t: torch.Tensor):
+    """Device FP8 E4M3 codes and row scales of a bf16 / fp32 device matrix, by eagle3_quantize_e4m3."""
+    N, K = t.shape
+    codes = torch.empty((N, K), dtype=torch.uint8, device=t.device)
+    scales = torch.empty((N,), dtype=torch.float32, device=t.device)
+    E.eagle3_quantize_e4m3(t, E.BF16 if t.dtype == torch.bfloat16 else E.F32, N, K, codes, scales)
+    return codes, scales
 
-    def __init__(self, w, stored_weights, device="cuda", max_batch=None, max_tokens=None):
+
+class DeviceHead:
+    """A created draft head whose weights live in device tensors owned by this object.
+
+    fp8=True stores the projection matrices as FP8 E4M3 codes with per-row scales, quantized on the
+    device from the given weights (the bf16 copies of those matrices are released)."""
+
+    def __init__(self, w, stored_weights, device="cuda", max_batch=None, max_tokens=None, fp8=False):
         self.w = w
         self.device = device
-        self.tensors = {n: to_device(stored_weights[n], device) for n in E.WEIGHT_NAMES}
-        self.config = config_for(w, max_batch, max_tokens)
-        self.handle = E.eagle3_draft_create(self.config, E.make_weights(self.tensors))
+        self.tensors = {}
+        self.scales = {}
+        for n in E.WEIGHT_NAMES:
+            t = to_device(stored_weights[n], device)
+            if fp8 and n in E.FP8_WEIGHT_NAMES:
+                t, self.scales[n] = quantize_fp8(t)
+            self.tensors[n] = t
+        self.config = config_for(w, max_batch, max_tokens, fp8)
+        self.handle = E.eagle3_draft_create(self.config, E.make_weights(self.tensors, self.scales or None))
 
     def close(self):
         if self.handle:

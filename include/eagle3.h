@@ -65,6 +65,17 @@ typedef enum {
 
 typedef enum { EAGLE3_F32 = 0, EAGLE3_BF16 = 1 } eagle3_dtype_t;
 
+/* Storage of the nine projection matrices (fc, q_a, kv_a, q_b, o, gate, up, down, lm_head).
+ *   EAGLE3_WEIGHTS_DTYPE  the configured dtype, like every other weight;
+ *   EAGLE3_WEIGHTS_FP8    FP8 E4M3 codes (OCP 8-bit floating point: sign, 4 exponent bits with bias 7,
+ *                         3 mantissa bits, largest finite 448) [rows, cols] row-major, one byte each, with
+ *                         one fp32 scale per output row: weight[n, k] = decode(code[n, k]) * scale[n].
+ *                         The post-training FP8 quantization of the drafter ("EAGLE head deep dive",
+ *                         deployment); eagle3_quantize_e4m3 produces this form from bf16 / fp32 weights.
+ *                         Requires dtype == EAGLE3_BF16.  kv_b, the embedding and the norm weights keep
+ *                         the configured dtype. */
+typedef enum { EAGLE3_WEIGHTS_DTYPE = 0, EAGLE3_WEIGHTS_FP8 = 1 } eagle3_weight_format_t;
+
 /* Device error word bits (eagle3_draft_get_error). */
 #define EAGLE3_DEVERR_TOKEN    1   /* an input token id was outside [0, target_vocab) */
 #define EAGLE3_DEVERR_POSITION 2   /* a position was >= max_ctx */
@@ -101,6 +112,7 @@ typedef struct {
     int32_t yarn_original_max_pos;/* 4096 */
     int32_t rope_interleave;      /* must be 1: pairs (2i, 2i+1) rotate together */
     eagle3_dtype_t dtype;         /* storage type of weights, aux states and cache */
+    eagle3_weight_format_t weight_format; /* storage of the projection matrices (0 = dtype) */
 } eagle3_config_t;
 
 /* Device pointers to the head's weights (BORROWED).  Shapes [rows, cols], row-major. */
@@ -122,6 +134,10 @@ typedef struct {
     const void *down;           /* [H, I] */
     const void *final_norm;     /* [H] */
     const void *lm_head;        /* [V_d, H] */
+    /* EAGLE3_WEIGHTS_FP8 only (ignored otherwise): the per-output-row fp32 scales of the E4M3
+     * matrices above, one per row of the matrix of the same name. */
+    const float *fc_scale, *q_a_scale, *kv_a_scale, *q_b_scale, *o_scale, *gate_scale, *up_scale,
+        *down_scale, *lm_head_scale;
 } eagle3_weights_t;
 
 /* The one-layer latent cache (BORROWED).  Slot p of sequence b is row (p % page_size) of page
@@ -307,6 +323,18 @@ EAGLE3_API eagle3_status_t eagle3_accept_residual(const int32_t *draft, const fl
                                                   const float *u_resample, int32_t batch, int32_t gamma, int32_t V,
                                                   int32_t *accepted_len, int32_t *next_token, int32_t *hist,
                                                   void *stream);
+
+/* Per-row FP8 E4M3 quantization of one weight matrix (the drafter's post-training FP8 quantization,
+ * "EAGLE head deep dive", deployment; the form EAGLE3_WEIGHTS_FP8 reads).  For every row n of w:
+ *   scale[n] = max_k |w[n, k]| / 448 in fp32 (1 for an all-zero row),
+ *   code[n, k] = E4M3(w[n, k] / scale[n]): the fp32 quotient rounded to the nearest E4M3 value, ties to
+ *   the even code, magnitudes above 448 saturating to 448.
+ *   w       [N, K] of `dtype` (bf16 or fp32), row-major
+ *   codes   [N, K] uint8 out; scales [N] fp32 out (both caller-owned device memory)
+ * One CTA per row.  Returns EAGLE3_ERR_INVALID_ARG for null pointers or sizes < 1, _UNSUPPORTED for
+ * another dtype. */
+EAGLE3_API eagle3_status_t eagle3_quantize_e4m3(const void *w, eagle3_dtype_t dtype, int32_t N, int32_t K,
+                                                uint8_t *codes, float *scales, void *stream);
 
 /* Read the sticky device error word (synchronises the device).  *device_error (host) receives
  * the EAGLE3_DEVERR_* bits; returns EAGLE3_ERR_DEVICE_RANGE when any bit is set. */

@@ -28,7 +28,8 @@ fusion or reordering).  Pins (``tests/test_oracle_*.py``):
   d2t_remap         zero offsets give identity; brute force
   accept            full match gives gamma; first mismatch gives 0; brute force
   e4m3_*            every code decodes per the OCP E4M3 table (max 448, one NaN pattern); encode(decode(c)) ==
-                    c; midpoints round to the even code; values saturate at 448
+                    c; midpoints round to the even code; values saturate at 448; the array
+                    encoder equals the scalar one on every code, midpoint and a random sweep
   accept_relaxed    rows outside thinking == greedy accept; k = 1 or delta below every gap ==
                     greedy; hand example with the default delta 0.6; monotone in delta
   draft_extend /    composition invariants: one T-row extend == T one-row extends
@@ -42,5 +43,5 @@ from .head import (  # noqa: F401
     F64, rms_norm, linear, silu, yarn_inv_freq, yarn_mscale, rope_cos_sin, rope_interleaved,
     softmax_scale, split_kv_b, mla_attention, decoder_rows, final_logits, argmax_lowest,
     top2_gap, d2t_remap, SeqCache, draft_extend, draft_decode_step, draft_round, accept, accept_relaxed,
-    sample_filtered, accept_residual, e4m3_decode, e4m3_encode, quantize_rows_e4m3,
+    sample_filtered, accept_residual, e4m3_decode, e4m3_encode, e4m3_encode_array, quantize_rows_e4m3,
 )

@@ -508,6 +508,7 @@ def e4m3_decode(code):
 
 
 _E4M3_POS = np.array([e4m3_decode(c) for c in range(0x7F)])      # codes 0 .. 126, ascending values
+_E4M3_ALL = np.array([e4m3_decode(c) for c in range(256)])       # value of every code (NaN at 0x7F, 0xFF)
 
 
 def e4m3_encode(x):
@@ -525,6 +526,22 @@ def e4m3_encode(x):
     return sign | hi
 
 
+def e4m3_encode_array(x):
+    """e4m3_encode over an array (the same nearest-code rule, ties to the even code, saturation at
+    +-448), for matrices too large for the scalar loop.  Returns uint8 codes of x's shape."""
+    x = np.asarray(x, dtype=np.float64)
+    sign = np.where(np.signbit(x), 0x80, 0).astype(np.uint8)
+    a = np.minimum(np.abs(x), 448.0)
+    i = np.searchsorted(_E4M3_POS, a)               # first code with value >= a
+    lo = np.maximum(i - 1, 0)
+    hi = np.minimum(i, 0x7E)
+    dl = a - _E4M3_POS[lo]
+    dh = _E4M3_POS[hi] - a
+    pick_lo = (dl < dh) | ((dl == dh) & (lo % 2 == 0))
+    code = np.where(i == 0, 0, np.where(pick_lo, lo, hi)).astype(np.uint8)
+    return code | sign
+
+
 def quantize_rows_e4m3(W):
     """Per-output-row FP8 weights ("EAGLE head deep dive", deployment: the drafter quantized to FP8 by
     post-training quantization with weight scales).  Reading: scale_n = max_k |W[n, k]| / 448 (1 for an
@@ -535,9 +552,7 @@ def quantize_rows_e4m3(W):
     N, K = W.shape
     amax = np.abs(W).max(axis=1)
     scales = np.where(amax > 0, amax / np.float32(448.0), np.float32(1.0)).astype(np.float32)
-    codes = np.zeros((N, K), dtype=np.uint8)
-    for n in range(N):
-        inv = W[n] / scales[n]                       # fp32 division, as the GPU divides
-        codes[n] = [e4m3_encode(v) for v in inv.astype(np.float32)]
-    deq = np.vectorize(e4m3_decode)(codes).astype(np.float64) * scales[:, None].astype(np.float64)
+    inv = (W / scales[:, None]).astype(np.float32)   # fp32 division, as the GPU divides
+    codes = e4m3_encode_array(inv)
+    deq = _E4M3_ALL[codes] * scales[:, None].astype(np.float64)
     return codes, scales, deq

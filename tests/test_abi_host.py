@@ -87,3 +87,30 @@ def test_accept_relaxed_rejects_bad_arguments(lib):
             E.eagle3_accept_relaxed(args["draft"], args["ids"], args["lp"], args["think"], args["batch"],
                                     args["gamma"], args["k"], args["delta"], args["acc"])
         assert ei.value.status == E.ERR_INVALID_ARG, kw
+
+
+def test_fp8_weight_format_checks_without_a_gpu(lib):
+    # the format must be known, FP8 needs bf16 storage, and extends above the GEMV rows reserve the
+    # bf16 expansion of the largest FP8 matrix pair (gate | up: 2 x 18432 x 7168 elements)
+    for kw in [dict(weight_format=2), dict(weight_format=E.WEIGHTS_FP8, dtype=E.F32)]:
+        with pytest.raises(E.Eagle3Error) as ei:
+            E.eagle3_draft_workspace_bytes(_dsv3_config(**kw))
+        assert ei.value.status in (E.ERR_INVALID_ARG, E.ERR_UNSUPPORTED), kw
+    small = E.eagle3_draft_workspace_bytes(_dsv3_config(weight_format=E.WEIGHTS_FP8))
+    assert small == E.eagle3_draft_workspace_bytes(_dsv3_config())
+    big = dict(max_batch=64, max_tokens_per_extend=64)
+    extra = E.eagle3_draft_workspace_bytes(_dsv3_config(weight_format=E.WEIGHTS_FP8, **big)) - \
+        E.eagle3_draft_workspace_bytes(_dsv3_config(**big))
+    assert 0 <= extra - 2 * 18432 * 7168 * 2 < 256
+    # an FP8 head without its row scales is rejected before any CUDA call
+    h = C.c_void_p()
+    cfg = _dsv3_config(weight_format=E.WEIGHTS_FP8)
+    w = E.eagle3_weights_t()
+    for n in E.WEIGHT_NAMES:
+        setattr(w, n, 256)
+    assert lib.eagle3_draft_create(C.byref(cfg), C.byref(w), C.byref(h)) == E.ERR_INVALID_ARG
+    assert h.value is None
+    # the quantizer checks its arguments on the host
+    assert lib.eagle3_quantize_e4m3(None, E.BF16, 4, 8, None, None, None) == E.ERR_INVALID_ARG
+    assert lib.eagle3_quantize_e4m3(256, E.BF16, 0, 8, 256, 256, None) == E.ERR_INVALID_ARG
+    assert lib.eagle3_quantize_e4m3(256, 7, 4, 8, 256, 256, None) == E.ERR_UNSUPPORTED

@@ -414,12 +414,30 @@ def test_e4m3_rounding_ties_and_saturation():
     assert O.e4m3_encode(2.0 ** -11) == 0x00     # below half the smallest subnormal
 
 
+def test_e4m3_array_encoder_matches_the_scalar_rule():
+    # every code value, every midpoint between neighbours (and a hair to each side), zeros, tiny and
+    # saturating magnitudes, a random sweep over 2^-12 .. 2^10; both signs
+    pos = np.array([O.e4m3_decode(c) for c in range(0x7F)])
+    mids = (pos[1:] + pos[:-1]) / 2
+    xs = np.concatenate([pos, mids, mids * (1 + 1e-9), mids * (1 - 1e-9), [0.0, 2.0 ** -11, 2.0 ** -10, 449.0,
+                         464.0, 480.0, 1e6], np.exp2(np.random.default_rng(15).uniform(-12, 10, 3000))])
+    xs = np.concatenate([xs, -xs])
+    got = O.e4m3_encode_array(xs)
+    ref = np.array([O.e4m3_encode(v) for v in xs], dtype=np.uint8)
+    np.testing.assert_array_equal(got, ref)
+    assert O.e4m3_encode_array(np.array([-0.0]))[0] == O.e4m3_encode(-0.0) == 0x80
+
+
 def test_quantize_rows_e4m3_error_bound():
     rng = np.random.default_rng(14)
     W = (rng.normal(0, 0.02, size=(9, 40))).astype(np.float32)
     W[3] = 0.0
     codes, scales, deq = O.quantize_rows_e4m3(W)
     assert codes.dtype == np.uint8 and scales.shape == (9,)
+    # the per-element rule, written out with the scalar encoder and fp32 quotients
+    for n in range(9):
+        assert [O.e4m3_encode(np.float32(v) / scales[n]) for v in W[n]] == codes[n].tolist()
+        assert np.all(deq[n] == np.array([O.e4m3_decode(c) for c in codes[n]]) * np.float64(scales[n]))
     amax = np.abs(W).max(axis=1)
     # each row's largest magnitude maps to 448 exactly; relative error of E4M3 <= 2^-4 per element
     for n in range(9):
