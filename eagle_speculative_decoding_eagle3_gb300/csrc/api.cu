@@ -183,7 +183,12 @@ eagle3_status_t check_config(const eagle3_config_t* c) {
     if (c->dtype != EAGLE3_F32 && c->dtype != EAGLE3_BF16) return EAGLE3_ERR_INVALID_ARG;
     if (c->weight_format != EAGLE3_WEIGHTS_DTYPE && c->weight_format != EAGLE3_WEIGHTS_FP8)
         return EAGLE3_ERR_INVALID_ARG;
-    if (c->weight_format == EAGLE3_WEIGHTS_FP8 && c->dtype != EAGLE3_BF16) return EAGLE3_ERR_UNSUPPORTED;
+    if (c->weight_format == EAGLE3_WEIGHTS_FP8) {
+        // the FP8 kernels load 16 codes per lane: every FP8 matrix's K is a multiple of 16
+        if (c->dtype != EAGLE3_BF16) return EAGLE3_ERR_UNSUPPORTED;
+        if (c->hidden % 16 || c->q_lora_rank % 16 || (c->n_heads * c->v_head_dim) % 16 || c->intermediate % 16)
+            return EAGLE3_ERR_UNSUPPORTED;
+    }
     // inner (K) dimensions of every linear layer stream in 8-element chunks
     const long inner[] = {c->hidden, c->q_lora_rank, c->kv_lora_rank, (long)c->n_heads * c->v_head_dim,
                           c->intermediate, c->kv_lora_rank + c->qk_rope_dim};

@@ -94,6 +94,11 @@ __device__ __forceinline__ void widen(const Raw8<fp8e4>& r, float* v) {
     e4m3x4_to_f32(r.a.x, v); e4m3x4_to_f32(r.a.y, v + 4);
 }
 __device__ __forceinline__ Raw8<fp8e4> zero8(fp8e4*) { return {make_uint2(0, 0)}; }
+// Sixteen E4M3 codes: one 16-byte load, the streaming unit of the FP8 weight kernels.
+struct Raw16e4 { uint4 a; };
+__device__ __forceinline__ void widen(const Raw16e4& r, float* v) {
+    e4m3x4_to_f32(r.a.x, v); e4m3x4_to_f32(r.a.y, v + 4); e4m3x4_to_f32(r.a.z, v + 8); e4m3x4_to_f32(r.a.w, v + 12);
+}
 
 // --------------------------------------------------------------------------------------------
 // reductions

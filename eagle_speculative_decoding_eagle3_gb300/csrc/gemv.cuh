@@ -7,8 +7,8 @@
 //  * one balanced wave: the grid holds kGemvCtasPerSm CTAs per SM and every warp owns an equal range of
 //    weight rows (rows_per_warp), so no SM idles in a half-empty last wave;
 //  * a warp streams R of its rows at once (R = 1 or 4), each with U 16-byte non-allocating loads per
-//    lane (lane l reads elements [8l + 256c, +8) of a row), so about 16 loads of 16 B are in flight per
-//    lane and ~128 KB per SM whatever the row length;
+//    lane (lane l reads elements [8l + 256c, +8) of a row; FP8: [16l + 512c, +16)), so about 16 loads of
+//    16 B are in flight per lane and ~128 KB per SM whatever the row length;
 //  * the activation rows (up to MR) stay L1/L2 resident and are loaded once per chunk for all R rows;
 //  * at the end of each pass the warp reduces its partial dot products and applies the fused epilogue:
 //    store, residual add, SiLU(gate) * up (two weight rows per output), or a running row argmax with
@@ -36,6 +36,23 @@ constexpr int kLoadsInFlight = 16;     // 16-byte weight loads per lane per iter
 template <typename T> constexpr bool kIsFp8 = false;
 template <> constexpr bool kIsFp8<fp8e4> = true;
 
+// The unit a lane loads from a weight row: 8 elements (fp32: two 16-byte loads, bf16: one), or 16 E4M3
+// codes (one 16-byte load).  A warp covers kChunk<TW> = 32 units' elements per row and step.
+template <typename TW> struct WUnit { static constexpr int EL = 8; using Raw = Raw8<TW>; };
+template <> struct WUnit<fp8e4> { static constexpr int EL = 16; using Raw = Raw16e4; };
+template <typename TW> constexpr int kChunk = 32 * WUnit<TW>::EL;
+template <typename TW> __device__ __forceinline__ typename WUnit<TW>::Raw ldw(const TW* p) {
+    if constexpr (kIsFp8<TW>) return Raw16e4{ld_stream16(p)}; else return ld8<true>(p);
+}
+template <typename TW> __device__ __forceinline__ typename WUnit<TW>::Raw zerow() {
+    if constexpr (kIsFp8<TW>) return Raw16e4{make_uint4(0, 0, 0, 0)}; else return zero8((TW*)nullptr);
+}
+// EL activations of row `p` (fp32 or bf16) widened to fp32
+template <int EL, typename TA> __device__ __forceinline__ void ld_act(const TA* p, float* v) {
+#pragma unroll
+    for (int h = 0; h < EL / 8; ++h) widen(ld8<false>(p + 8 * h), v + 8 * h);
+}
+
 // Scale of output column n of an FP8 GEMV (GLU: q selects the gate or up matrix; else the segment).
 __device__ __forceinline__ float row_scale(const GemvArgs& g, bool glu, int n, int q) {
     if (glu) return __ldg(g.wscale[q] + n);
@@ -46,7 +63,8 @@ __device__ __forceinline__ float row_scale(const GemvArgs& g, bool glu, int n, i
 template <typename TA, typename TW, int MR, int EPI, int R>
 __global__ void __launch_bounds__(kGemvWarps * 32, kGemvCtasPerSm) gemv_kernel(const GemvArgs g, int rows_per_warp) {
     constexpr int NW = (EPI == EPI_GLU) ? 2 : 1;   // weight rows read per output column
-    constexpr int U0 = kLoadsInFlight / (R * NW) * 2 / (int)sizeof(TW);
+    constexpr int EL = WUnit<TW>::EL, CW = kChunk<TW>;
+    constexpr int U0 = kLoadsInFlight / (R * NW) * 16 / ((int)sizeof(TW) * EL);
     constexpr int U = U0 < 1 ? 1 : U0;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int m0 = blockIdx.x * MR;
@@ -95,21 +113,21 @@ __global__ void __launch_bounds__(kGemvWarps * 32, kGemvCtasPerSm) gemv_kernel(c
 #pragma unroll
                 for (int q = 0; q < NW; ++q) acc[i][j][q] = 0.f;
 
-        for (int k0 = lane * 8; k0 < K; k0 += 256 * U) {
-            Raw8<TW> wr[U][R][NW];
+        for (int k0 = lane * EL; k0 < K; k0 += CW * U) {
+            typename WUnit<TW>::Raw wr[U][R][NW];
 #pragma unroll
             for (int u = 0; u < U; ++u) {
-                const int k = k0 + u * 256;
+                const int k = k0 + u * CW;
 #pragma unroll
                 for (int j = 0; j < R; ++j)
 #pragma unroll
                     for (int q = 0; q < NW; ++q)
-                        wr[u][j][q] = (k < K && j < nr) ? ld8<true>(wp[j][q] + k) : zero8((TW*)nullptr);
+                        wr[u][j][q] = (k < K && j < nr) ? ldw(wp[j][q] + k) : zerow<TW>();
             }
             if (!waited) { pdl_wait(); waited = true; }
 #pragma unroll
             for (int u = 0; u < U; ++u) {
-                const int k = k0 + u * 256;
+                const int k = k0 + u * CW;
                 if (k < K) {
                     const int s = (k >= ka0) + (k >= ka01);
                     const int kl = k - (s == 0 ? 0 : (s == 1 ? ka0 : ka01));
@@ -117,16 +135,16 @@ __global__ void __launch_bounds__(kGemvWarps * 32, kGemvCtasPerSm) gemv_kernel(c
 #pragma unroll
                     for (int i = 0; i < MR; ++i) {
                         if (i < mcount) {
-                            float av[8];
-                            widen(ld8<false>(ap + i * g.lda[s]), av);
+                            float av[EL];
+                            ld_act<EL>(ap + i * g.lda[s], av);
 #pragma unroll
                             for (int j = 0; j < R; ++j)
 #pragma unroll
                                 for (int q = 0; q < NW; ++q) {
-                                    float wv[8];
+                                    float wv[EL];
                                     widen(wr[u][j][q], wv);
 #pragma unroll
-                                    for (int e = 0; e < 8; ++e) acc[i][j][q] = fmaf(wv[e], av[e], acc[i][j][q]);
+                                    for (int e = 0; e < EL; ++e) acc[i][j][q] = fmaf(wv[e], av[e], acc[i][j][q]);
                                 }
                         }
                     }
@@ -184,7 +202,7 @@ __global__ void __launch_bounds__(kGemvWarps * 32, kGemvCtasPerSm) gemv_kernel(c
 
 // K-split variant for long rows (bf16 or FP8 weights, no row grouping).  A CTA owns `rpc` consecutive output
 // columns; its 8 warps form RG = 8 / KS row groups of KS warps, and the KS warps of a group split K
-// (warp k of a group reads the 256-element chunks [k nch / KS, (k + 1) nch / KS) of every row).  A group
+// (warp k of a group reads the warp chunks [k nch / KS, (k + 1) nch / KS) of every row).  A group
 // streams R rows at once (U chunks each, 16 loads of 16 B in flight per lane), so one activation load
 // feeds R rows instead of the whole-row kernel's few, and a layer with few rows per warp (q_a | kv_a:
 // 2112 rows for 2432 warps) still keeps every warp busy.  Each round the RG groups take one pass of R
@@ -192,7 +210,8 @@ __global__ void __launch_bounds__(kGemvWarps * 32, kGemvCtasPerSm) gemv_kernel(c
 template <typename TA, typename TW, int MR, int EPI, int R>
 __global__ void __launch_bounds__(kGemvWarps * 32, kGemvCtasPerSm) gemv_ks_kernel(const GemvArgs g, int rpc, int KS) {
     constexpr int NW = (EPI == EPI_GLU) ? 2 : 1;
-    constexpr int U0 = kLoadsInFlight / (R * NW) * 2 / (int)sizeof(TW);
+    constexpr int EL = WUnit<TW>::EL, CW = kChunk<TW>;
+    constexpr int U0 = kLoadsInFlight / (R * NW) * 16 / ((int)sizeof(TW) * EL);
     static_assert(R * MR <= 32, "one epilogue thread per (row group, row, activation row)");
     constexpr int U = U0 < 1 ? 1 : U0;
     constexpr int OUT = MR * R * NW;                 // partial sums per warp and pass
@@ -201,7 +220,7 @@ __global__ void __launch_bounds__(kGemvWarps * 32, kGemvCtasPerSm) gemv_ks_kerne
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int RG = kGemvWarps / KS, ks = warp % KS, rg = warp / KS;
     const int m0 = blockIdx.x * MR, mcount = min(MR, g.M - m0);
-    const int K = g.K, nch = (K + 255) / 256;
+    const int K = g.K, nch = (K + CW - 1) / CW;
     const int c0 = ks * nch / KS, c1 = (ks + 1) * nch / KS;
     const int row0 = blockIdx.y * rpc, row1 = min(g.N, row0 + rpc);
     const int npass = (row1 - row0 + R - 1) / R, nround = (npass + RG - 1) / RG;
@@ -247,21 +266,21 @@ __global__ void __launch_bounds__(kGemvWarps * 32, kGemvCtasPerSm) gemv_ks_kerne
 #pragma unroll
                 for (int w = 0; w < NW; ++w) wp[j][w] = wrow(p0 + (j < nr ? j : 0), w);
             for (int c = c0; c < c1; c += U) {
-                Raw8<TW> wr[U][R][NW];
+                typename WUnit<TW>::Raw wr[U][R][NW];
 #pragma unroll
                 for (int u = 0; u < U; ++u) {
-                    const int k = (c + u) * 256 + lane * 8;
+                    const int k = (c + u) * CW + lane * EL;
                     const bool ok = c + u < c1 && k < K;
 #pragma unroll
                     for (int j = 0; j < R; ++j)
 #pragma unroll
                         for (int w = 0; w < NW; ++w)
-                            wr[u][j][w] = (ok && j < nr) ? ld8<true>(wp[j][w] + k) : zero8((TW*)nullptr);
+                            wr[u][j][w] = (ok && j < nr) ? ldw(wp[j][w] + k) : zerow<TW>();
                 }
                 if (!waited) { pdl_wait(); waited = true; }
 #pragma unroll
                 for (int u = 0; u < U; ++u) {
-                    const int k = (c + u) * 256 + lane * 8;
+                    const int k = (c + u) * CW + lane * EL;
                     if (c + u < c1 && k < K) {
                         const int s = (k >= ka0) + (k >= ka01);
                         const int kl = k - (s == 0 ? 0 : (s == 1 ? ka0 : ka01));
@@ -269,16 +288,16 @@ __global__ void __launch_bounds__(kGemvWarps * 32, kGemvCtasPerSm) gemv_ks_kerne
 #pragma unroll
                         for (int i = 0; i < MR; ++i) {
                             if (i < mcount) {
-                                float av[8];
-                                widen(ld8<false>(ap + i * g.lda[s]), av);
+                                float av[EL];
+                                ld_act<EL>(ap + i * g.lda[s], av);
 #pragma unroll
                                 for (int j = 0; j < R; ++j)
 #pragma unroll
                                     for (int w = 0; w < NW; ++w) {
-                                        float wv[8];
+                                        float wv[EL];
                                         widen(wr[u][j][w], wv);
 #pragma unroll
-                                        for (int e = 0; e < 8; ++e) acc[i][j][w] = fmaf(wv[e], av[e], acc[i][j][w]);
+                                        for (int e = 0; e < EL; ++e) acc[i][j][w] = fmaf(wv[e], av[e], acc[i][j][w]);
                                     }
                             }
                         }
@@ -343,11 +362,11 @@ __global__ void __launch_bounds__(kGemvWarps * 32, kGemvCtasPerSm) gemv_ks_kerne
     }
 }
 
-// K slices per row group: 8 when the row's 256-element chunks split evenly into at least two per warp
-// or are many enough (>= 64) that an uneven split costs under an eighth; else the largest of {4, 2} that
-// splits them evenly into at least two per warp; else 1 (whole rows, as in gemv_kernel).
-static int gemv_ks_slices(int K) {
-    const int nch = (K + 255) / 256;
+// K slices per row group, from the row's nch warp chunks (kChunk elements each): 8 when they split evenly
+// into at least two per warp or are many enough (>= 64) that an uneven split costs under an eighth; else
+// the largest of {4, 2} that splits them evenly into at least two per warp; else 1 (whole rows, as in
+// gemv_kernel).
+static int gemv_ks_slices(int nch) {
     if ((nch % 8 == 0 && nch >= 16) || nch >= 64) return 8;
     for (int ks = 4; ks >= 2; ks >>= 1)
         if (nch % ks == 0 && nch / ks >= 2) return ks;
@@ -416,7 +435,7 @@ static cudaError_t launch_mr(GemvArgs& g, int num_sms, cudaStream_t st) {
     // The K-split kernel wins where the whole-row kernel has few rows per warp (long rows: fc, q_a | kv_a,
     // o_proj, down); with four or more rows per pass the whole-row kernel already reuses each activation
     // load and streams slightly faster (gate | up, lm_head, q_b on a GB300).
-    const int KS = gemv_ks_slices(g.K);
+    const int KS = gemv_ks_slices((g.K + kChunk<TW> - 1) / kChunk<TW>);
     int rpw, ctas, R;
     gemv_split(g.N, num_sms, g.a_grp, &rpw, &ctas, &R);
     if (sizeof(TW) <= 2 && KS > 1 && rpw <= 4 && !g.w_grp && !g.a_grp) {

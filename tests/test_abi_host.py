@@ -92,7 +92,8 @@ def test_accept_relaxed_rejects_bad_arguments(lib):
 def test_fp8_weight_format_checks_without_a_gpu(lib):
     # the format must be known, FP8 needs bf16 storage, and extends above the GEMV rows reserve the
     # bf16 expansion of the largest FP8 matrix pair (gate | up: 2 x 18432 x 7168 elements)
-    for kw in [dict(weight_format=2), dict(weight_format=E.WEIGHTS_FP8, dtype=E.F32)]:
+    for kw in [dict(weight_format=2), dict(weight_format=E.WEIGHTS_FP8, dtype=E.F32),
+               dict(weight_format=E.WEIGHTS_FP8, hidden=7160)]:          # FP8 rows: K a multiple of 16
         with pytest.raises(E.Eagle3Error) as ei:
             E.eagle3_draft_workspace_bytes(_dsv3_config(**kw))
         assert ei.value.status in (E.ERR_INVALID_ARG, E.ERR_UNSUPPORTED), kw
