@@ -24,6 +24,10 @@ fusion or reordering).  Pins (``tests/test_oracle_*.py``):
   mla_attention     torch scaled_dot_product_attention (fp64) on explicit K/V; single key
                     returns its value; equal keys return the mean; causal first row;
                     absorbed == unabsorbed to fp64 round-off
+  rope_half         (MHA head) hand quarter turn and the (i, i + d/2) pairing; complex multiplication;
+                    identity at 0, relative-position invariance
+  mha_attention     torch SDPA in fp64 with key/value heads repeated per group and the causal mask;
+                    single visible slot; equal keys give the mean value
   argmax_lowest     brute force with planted ties
   d2t_remap         zero offsets give identity; brute force
   accept            full match gives gamma; first mismatch gives 0; brute force
@@ -40,8 +44,8 @@ above its parity is unpinned (the 2H concat order is a reading that only permute
 weight columns and cannot be pinned).
 """
 from .head import (  # noqa: F401
-    F64, rms_norm, linear, silu, yarn_inv_freq, yarn_mscale, rope_cos_sin, rope_interleaved,
-    softmax_scale, split_kv_b, mla_attention, decoder_rows, final_logits, argmax_lowest,
+    F64, rms_norm, linear, silu, yarn_inv_freq, yarn_mscale, rope_cos_sin, rope_interleaved, rope_half, rope_dim,
+    softmax_scale, split_kv_b, mla_attention, mha_attention, decoder_rows, final_logits, argmax_lowest,
     top2_gap, d2t_remap, SeqCache, draft_extend, draft_decode_step, draft_round, accept, accept_relaxed,
     sample_filtered, accept_residual, e4m3_decode, e4m3_encode, e4m3_encode_array, quantize_rows_e4m3,
 )

@@ -1,7 +1,8 @@
-"""fp64 oracle of the EAGLE-3 MLA draft head — test infrastructure only (see package docstring).
+"""fp64 oracle of the EAGLE-3 draft heads (MLA, and the Llama-style MHA variant) — test
+infrastructure only (see package docstring).
 
 Notation: H hidden, n_h heads, d_q q_lora_rank, d_c kv_lora_rank, d_n qk_nope, d_r qk_rope,
-d_v v_head, I intermediate, V_t target vocab, V_d draft vocab.  Weights follow nn.Linear:
+d_v v_head, I intermediate, V_t target vocab, V_d draft vocab; MHA: n_kv key/value heads, d head_dim.  Weights follow nn.Linear:
 W[out, in], y = x W^T.  ``hyper`` is a plain dict with those sizes and the YaRN / norm
 constants; ``W`` maps weight names to arrays (any float dtype, widened to fp64 on use).
 """
@@ -83,10 +84,15 @@ def yarn_mscale(factor, mscale):
     return 0.1 * mscale * math.log(factor) + 1.0
 
 
+def rope_dim(hyper):
+    """Rotated width: d_r of the MLA head; the whole head_dim d of the MHA head."""
+    return hyper["head_dim"] if hyper.get("attention", "mla") == "mha" else hyper["qk_rope_dim"]
+
+
 def rope_cos_sin(positions, hyper):
-    """cos/sin [len(positions), d_r/2] of angle p * omega_i, scaled by
+    """cos/sin [len(positions), d/2] (d = rope_dim) of angle p * omega_i, scaled by
     m(f, mscale) / m(f, mscale_all_dim) (reading)."""
-    d = hyper["qk_rope_dim"]
+    d = rope_dim(hyper)
     inv = yarn_inv_freq(d, hyper["rope_theta"], hyper["yarn_factor"], hyper["yarn_original_max_pos"],
                         hyper["yarn_beta_fast"], hyper["yarn_beta_slow"])
     ang = _f64(positions)[:, None] * inv[None, :]
@@ -114,10 +120,30 @@ def rope_interleaved(x, positions, hyper):
     return out
 
 
+def rope_half(x, positions, hyper):
+    """Llama-style rotary embedding of the MHA head (LlamaForCausalLMEagle3, "Eagle3 DeepseekV3 in
+    MAX" §11): dimension i pairs with i + d/2 (reading: the Llama "rotate half" layout), both rotated
+    by angle p * omega_i counter-clockwise:
+        x'_i       = x_i cos - x_{i+d/2} sin
+        x'_{i+d/2} = x_i sin + x_{i+d/2} cos.
+    ``x`` is [T, ..., d] with one position per leading row."""
+    x = _f64(x)
+    cos, sin = rope_cos_sin(positions, hyper)
+    shape = (x.shape[0],) + (1,) * (x.ndim - 2) + (cos.shape[1],)
+    cos = cos.reshape(shape)
+    sin = sin.reshape(shape)
+    h = x.shape[-1] // 2
+    a = x[..., :h]
+    b = x[..., h:]
+    return np.concatenate([a * cos - b * sin, a * sin + b * cos], axis=-1)
+
+
 def softmax_scale(hyper):
-    """sigma = (d_n + d_r)^(-1/2) * m(f, mscale_all_dim)^2 (reading: YaRN attention scaling
-    folded into the softmax scale, as DeepSeek's MLA does)."""
+    """sigma = d_qk^(-1/2) * m(f, mscale_all_dim)^2 with d_qk = d_n + d_r (MLA) or head_dim (MHA)
+    (reading: YaRN attention scaling folded into the softmax scale, as DeepSeek's MLA does)."""
     m = yarn_mscale(hyper["yarn_factor"], hyper["yarn_mscale_all_dim"])
+    if hyper.get("attention", "mla") == "mha":
+        return hyper["head_dim"] ** -0.5 * m * m
     return (hyper["qk_nope_dim"] + hyper["qk_rope_dim"]) ** -0.5 * m * m
 
 
@@ -182,6 +208,40 @@ def mla_attention(q, positions, cache, kv_b, hyper, absorbed=False):
     return out
 
 
+def mha_attention(q, positions, cache, hyper):
+    """Grouped-query attention of the MHA head over its own one-layer cache ("Eagle3 DeepseekV3 in
+    MAX" §11: the Llama-style Eagle3 head; [MAX-API] Eagle3MHADeepseekV3DraftArchConfig: its own KV,
+    one layer, bf16).
+
+    q        [T, n_h, d]          (rotated)
+    cache    [L, 2 n_kv d]        rows [k_rot (n_kv x d) | v (n_kv x d)] indexed by position
+    returns  o [T, n_h, d]
+
+    Query head h reads key/value head h // (n_h / n_kv) (reading: consecutive query heads share a
+    key/value head, as Llama's grouped-query attention repeats them).  Row i at position p attends
+    to slots 0..p: s_t = sigma q_h . k_g,t, o_h = sum_t softmax(s)_t v_g,t.
+    """
+    q = _f64(q)
+    cache = _f64(cache)
+    nh, nkv, d = hyper["n_heads"], hyper["n_kv_heads"], hyper["head_dim"]
+    G = nh // nkv
+    sigma = softmax_scale(hyper)
+    T = q.shape[0]
+    k = cache[:, :nkv * d].reshape(-1, nkv, d)
+    v = cache[:, nkv * d:].reshape(-1, nkv, d)
+    out = np.empty((T, nh, d), dtype=F64)
+    for i in range(T):
+        n = int(positions[i]) + 1
+        for h in range(nh):
+            g = h // G
+            s = sigma * (k[:n, g] @ q[i, h])
+            s = s - s.max()
+            p = np.exp(s)
+            p /= p.sum()
+            out[i, h] = p @ v[:n, g]
+    return out
+
+
 # ----------------------------------------------------------------------------
 # The decoder chain
 # ----------------------------------------------------------------------------
@@ -218,6 +278,27 @@ def decoder_rows(hyper, W, f, tokens, positions, cache: SeqCache, absorbed=False
     # two streams normalised separately, then concatenated to 2H: [norm(embed) | norm(fused)]
     # ([ModelOpt-EAGLE] part 3; [MAX-walkthrough] §4; the order is a reading)
     x = np.concatenate([rms_norm(e, W["input_norm"], eps), rms_norm(f, W["hidden_norm"], eps)], axis=1)
+    need = int(positions.max()) + 1
+    if need > cache.data.shape[0]:
+        grow = np.zeros((need - cache.data.shape[0], cache.data.shape[1]), dtype=F64)
+        cache.data = np.concatenate([cache.data, grow], axis=0)
+    if hyper.get("attention", "mla") == "mha":
+        # Llama-style attention at 2H input ("Eagle3 DeepseekV3 in MAX" §11; [ModelOpt-EAGLE] part 3):
+        # q, k, v projections, rotary on q and k, own cache append, grouped-query attention
+        nkv, d = hyper["n_kv_heads"], hyper["head_dim"]
+        q = rope_half(linear(x, W["q_proj"]).reshape(T, nh, d), positions, hyper)
+        k = rope_half(linear(x, W["k_proj"]).reshape(T, nkv, d), positions, hyper)
+        v = linear(x, W["v_proj"])
+        cache.data[positions] = np.concatenate([k.reshape(T, nkv * d), v], axis=1)
+        cache.length = max(cache.length, need)
+        o = mha_attention(q, positions, cache.data, hyper)
+        h1 = linear(o.reshape(T, -1), W["o"]) + f
+        y = rms_norm(h1, W["post_attn_norm"], eps)
+        m = silu(linear(y, W["gate"])) * linear(y, W["up"])
+        h2 = linear(m, W["down"]) + h1
+        if trace is not None:
+            trace.update(x=x, q=q, k=k, v=v, o=o, h1=h1, y=y, m=m, h2=h2)
+        return h2
     # MLA projections at 2H input ([ModelOpt-EAGLE] part 3: first-layer q/k/v input doubled)
     c_q = rms_norm(linear(x, W["q_a"]), W["q_a_norm"], eps)
     kv = linear(x, W["kv_a"])
@@ -226,10 +307,6 @@ def decoder_rows(hyper, W, f, tokens, positions, cache: SeqCache, absorbed=False
     q = linear(c_q, W["q_b"]).reshape(T, nh, dn + dr)
     q[:, :, dn:] = rope_interleaved(q[:, :, dn:], positions, hyper)
     # latent KV append: slot = position
-    need = int(positions.max()) + 1
-    if need > cache.data.shape[0]:
-        grow = np.zeros((need - cache.data.shape[0], cache.data.shape[1]), dtype=F64)
-        cache.data = np.concatenate([cache.data, grow], axis=0)
     cache.data[positions] = np.concatenate([c_kv, k_r], axis=1)
     cache.length = max(cache.length, need)
     o = mla_attention(q, positions, cache.data, W["kv_b"], hyper, absorbed=absorbed)
@@ -275,17 +352,18 @@ def d2t_remap(d, d2t):
 # Head calls
 # ----------------------------------------------------------------------------
 def draft_extend(hyper, W, aux, tokens, positions, row_offsets, caches, absorbed=False):
-    """Extend: fc fuses the three aux states (early, middle, late) from 3H to H with no bias
+    """Extend: fc fuses the aux states (three for the MLA head: early, middle, late; two or three for
+    the MHA head, as fc's width says, "Eagle3 DeepseekV3 in MAX" §11) to H with no bias
     ([MAX-walkthrough] §4; [ModelOpt-EAGLE] part 2), then the decoder chain over each
     sequence's new rows; the last row of each sequence is scored ([MAX-walkthrough] §4:
     last-token gather by input_row_offsets).
 
-    aux: three arrays [N, H]; caches: list of SeqCache (mutated).
+    aux: fc_inputs arrays [N, H] (3 unless hyper says otherwise); caches: list of SeqCache (mutated).
     Returns dict(h2 [B, H], logits [B, V_d], d [B]).
     """
     B = len(row_offsets) - 1
-    fused_in = np.concatenate([_f64(a) for a in aux], axis=1)        # [N, 3H]
-    assert fused_in.shape[1] == 3 * hyper["hidden"], "fc applies only to a 3H-wide input"
+    fused_in = np.concatenate([_f64(a) for a in aux], axis=1)        # [N, fc_inputs H]
+    assert fused_in.shape[1] == hyper.get("fc_inputs", 3) * hyper["hidden"], "fc's input width"
     h2_last, logits = [], []
     for b in range(B):
         r0, r1 = int(row_offsets[b]), int(row_offsets[b + 1])

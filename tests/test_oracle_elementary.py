@@ -447,3 +447,74 @@ def test_quantize_rows_e4m3_error_bound():
         assert np.max(np.abs(deq[n])) == pytest.approx(amax[n], rel=1e-6)
         err = np.abs(deq[n] - W[n])
         assert np.all(err <= np.maximum(np.abs(W[n]) * 2.0 ** -4, scales[n] * 2.0 ** -10) * (1 + 1e-6))
+
+
+# ---------------------------------------------------------------- MHA head: rotate-half RoPE, GQA attention
+def _mha_hyper(nh=4, nkv=2, d=8, factor=1.0, L0=16):
+    h = _hyper(d=d, factor=factor, L0=L0)
+    h.update(attention="mha", n_heads=nh, n_kv_heads=nkv, head_dim=d)
+    return h
+
+
+def test_rope_half_hand_quarter_turn_and_pairing():
+    # d = 2: the only pair is (x_0, x_1) with omega = 1 rad per position, as in the interleaved layout
+    h = _mha_hyper(d=2)
+    np.testing.assert_allclose(O.rope_half(np.array([[1.0, 0.0]]), np.array([math.pi / 2]), h), [[0.0, 1.0]],
+                               atol=1e-15)
+    # d = 4: dimension 0 pairs with 2 (omega 1) and dimension 1 with 3 (omega theta^-1/2); the interleaved
+    # layout would pair 0 with 1 instead
+    h = _mha_hyper(d=4)
+    y = O.rope_half(np.array([[1.0, 0.0, 0.0, 0.0]]), np.array([math.pi / 2]), h)
+    np.testing.assert_allclose(y, [[0.0, 0.0, 1.0, 0.0]], atol=1e-15)
+
+
+def test_rope_half_matches_complex_multiplication_and_invariants():
+    h = _mha_hyper(d=64, factor=40.0, L0=4096)
+    rng = np.random.default_rng(21)
+    x = rng.standard_normal((7, 3, 64))
+    pos = rng.integers(0, 100000, size=7)
+    y = O.rope_half(x, pos, h)
+    inv = O.yarn_inv_freq(64, 1e4, 40.0, 4096, 32.0, 1.0)
+    z = (x[..., :32] + 1j * x[..., 32:]) * np.exp(1j * pos[:, None, None] * inv[None, None, :])
+    np.testing.assert_allclose(y[..., :32], z.real, rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(y[..., 32:], z.imag, rtol=1e-12, atol=1e-12)
+    q, k = rng.standard_normal((1, 64)), rng.standard_normal((1, 64))
+    np.testing.assert_allclose(O.rope_half(q, np.array([0]), h), q, rtol=0, atol=0)
+
+    def dot(pq, pk):
+        return float((O.rope_half(q, np.array([pq]), h) @ O.rope_half(k, np.array([pk]), h).T)[0, 0])
+    assert dot(100, 37) == pytest.approx(dot(1063, 1000), rel=1e-9)
+
+
+def test_mha_attention_matches_torch_sdpa_with_grouped_heads():
+    h = _mha_hyper(nh=6, nkv=2, d=8, factor=4.0)
+    rng = np.random.default_rng(22)
+    T, L = 3, 11
+    q = rng.standard_normal((T, 6, 8))
+    cache = rng.standard_normal((L, 2 * 2 * 8))
+    pos = np.arange(L - T, L)
+    o = O.mha_attention(q, pos, cache, h)
+    k = torch.tensor(cache[:, :16].reshape(L, 2, 8)).permute(1, 0, 2)        # [n_kv, L, d]
+    v = torch.tensor(cache[:, 16:].reshape(L, 2, 8)).permute(1, 0, 2)
+    kk, vv = k.repeat_interleave(3, dim=0), v.repeat_interleave(3, dim=0)     # query heads 3g..3g+2 -> g
+    mask = torch.tensor(np.arange(L)[None, :] <= pos[:, None])                  # [T, L]: slot <= position
+    ref = torch.nn.functional.scaled_dot_product_attention(
+        torch.tensor(q).permute(1, 0, 2), kk, vv, attn_mask=mask, scale=O.softmax_scale(h)).permute(1, 0, 2)
+    np.testing.assert_allclose(o, ref.numpy(), rtol=1e-12, atol=1e-13)
+    # the softmax scale of the MHA head: d^-1/2 times the squared YaRN attention factor
+    m = 0.1 * math.log(4.0) + 1.0
+    assert O.softmax_scale(h) == pytest.approx(8 ** -0.5 * m * m, rel=1e-15)
+
+
+def test_mha_attention_single_slot_and_equal_keys():
+    h = _mha_hyper(nh=4, nkv=1, d=8)
+    rng = np.random.default_rng(23)
+    q = rng.standard_normal((1, 4, 8))
+    cache = rng.standard_normal((5, 16))
+    # position 0 sees one slot: every head returns that slot's value row
+    o = O.mha_attention(q, np.array([0]), cache, h)
+    np.testing.assert_allclose(o[0], np.repeat(cache[0:1, 8:], 4, axis=0), rtol=1e-14)
+    # equal keys give the mean of the visible values
+    cache[:, :8] = cache[0, :8]
+    o = O.mha_attention(q, np.array([4]), cache, h)
+    np.testing.assert_allclose(o[0], np.repeat(cache[:, 8:].mean(axis=0, keepdims=True), 4, axis=0), rtol=1e-12)

@@ -6,9 +6,9 @@ import oracle as O
 import workloads as WL
 
 
-@pytest.fixture(scope="module")
-def tiny():
-    w = WL.workload("tiny_f32")
+@pytest.fixture(scope="module", params=["tiny_f32", "mha_tiny_f32"])
+def tiny(request):
+    w = WL.workload(request.param)
     W = WL.F32View(WL.make_weights(w))
     return w, W
 
@@ -60,17 +60,19 @@ def test_residual_pass_through(tiny):
     L = WL.context_lengths(w)
     ex = WL.make_extend(w, L)
     out = O.draft_extend(hy, W0, ex.aux, ex.tokens, ex.positions, ex.row_offsets, _caches(w, L))
-    fused = O.linear(np.concatenate([ex.aux[0], ex.aux[1], ex.aux[2]], axis=1), W["fc"])
+    fused = O.linear(np.concatenate(list(ex.aux), axis=1), W["fc"])
     last = ex.row_offsets[1:] - 1
-    np.testing.assert_allclose(out["h2"], fused[last], rtol=1e-13)
-    # a zero value projection makes the attention output vanish: h1 == fused
-    W1 = dict(W)
-    kvb = np.array(W["kv_b"]).reshape(w.n_heads, w.qk_nope_dim + w.v_head_dim, w.kv_lora_rank).copy()
-    kvb[:, w.qk_nope_dim:] = 0
-    W1["kv_b"] = kvb.reshape(-1, w.kv_lora_rank)
-    W1["down"] = np.zeros_like(W["down"])
-    out = O.draft_extend(hy, W1, ex.aux, ex.tokens, ex.positions, ex.row_offsets, _caches(w, L))
-    np.testing.assert_allclose(out["h2"], fused[last], rtol=1e-13)
+    np.testing.assert_allclose(out["h2"], fused[last], rtol=1e-13, atol=1e-15)
+    # a zero value projection makes the attention output vanish: h1 == fused (the MHA head's new
+    # value rows are zero, but its cached prefix is not, so only the MLA head's kv_b zeroes them all)
+    if w.attention == "mla":
+        W1 = dict(W)
+        kvb = np.array(W["kv_b"]).reshape(w.n_heads, w.qk_nope_dim + w.v_head_dim, w.kv_lora_rank).copy()
+        kvb[:, w.qk_nope_dim:] = 0
+        W1["kv_b"] = kvb.reshape(-1, w.kv_lora_rank)
+        W1["down"] = np.zeros_like(W["down"])
+        out = O.draft_extend(hy, W1, ex.aux, ex.tokens, ex.positions, ex.row_offsets, _caches(w, L))
+        np.testing.assert_allclose(out["h2"], fused[last], rtol=1e-13, atol=1e-15)
 
 
 def test_decode_carries_previous_hidden(tiny):
@@ -87,12 +89,14 @@ def test_decode_carries_previous_hidden(tiny):
     np.testing.assert_allclose(st["h2"], h_prev, rtol=1e-14)
 
 
-def test_fc_only_on_3h_input(tiny):
+def test_fc_only_on_its_input_width(tiny):
+    # fc takes exactly fc_inputs aux states (3 for the MLA head; 2 for the tiny MHA head)
     w, W = tiny
     L = WL.context_lengths(w)
     ex = WL.make_extend(w, L)
+    assert len(ex.aux) == w.fc_inputs
     with pytest.raises(AssertionError):
-        O.draft_extend(w.hyper(), W, ex.aux[:2], ex.tokens, ex.positions, ex.row_offsets, _caches(w, L))
+        O.draft_extend(w.hyper(), W, ex.aux[:-1], ex.tokens, ex.positions, ex.row_offsets, _caches(w, L))
 
 
 def test_decode_step_equals_one_row_extend_with_given_hidden(tiny):
@@ -106,8 +110,8 @@ def test_decode_step_equals_one_row_extend_with_given_hidden(tiny):
     toks = np.array([17, 1999])
     st = O.draft_decode_step(hy, W, h_prev, toks, _caches(w, L))
     Wi = dict(W)
-    Wi["fc"] = np.concatenate([np.eye(w.hidden), np.zeros((w.hidden, 2 * w.hidden))], axis=1)
-    aux = [h_prev, np.zeros_like(h_prev), np.zeros_like(h_prev)]
+    Wi["fc"] = np.concatenate([np.eye(w.hidden), np.zeros((w.hidden, (w.fc_inputs - 1) * w.hidden))], axis=1)
+    aux = [h_prev] + [np.zeros_like(h_prev)] * (w.fc_inputs - 1)
     ex = O.draft_extend(hy, Wi, aux, toks, L.astype(np.int64), np.arange(w.batch + 1), _caches(w, L))
     np.testing.assert_allclose(ex["h2"], st["h2"], rtol=1e-12)
     np.testing.assert_allclose(ex["logits"], st["logits"], rtol=1e-11, atol=1e-12)
@@ -134,7 +138,7 @@ def test_round_structure_and_forced_continuation(tiny):
 
 
 def test_workload_generators_are_valid():
-    for name in ("tiny_f32", "dsv3_b1"):
+    for name in ("tiny_f32", "dsv3_b1", "mha_tiny_f32", "mha_b1"):
         w = WL.workload(name)
         d2t = WL.make_d2t(w)
         t = np.arange(w.draft_vocab) + d2t

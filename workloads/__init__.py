@@ -1,4 +1,4 @@
-"""Seeded synthetic workloads for the EAGLE-3 MLA draft head.
+"""Seeded synthetic workloads for the EAGLE-3 draft heads (MLA, and the Llama-style MHA variant).
 
 This module is the ONLY code shared by the fp64 oracle side (``oracle/``) and the
 CUDA side (the ``eagle_speculative_decoding_eagle3_gb300`` package).  It holds no
@@ -70,6 +70,11 @@ class Workload:
     seed: int = 1000
     weight_std: float = 0.02
     norm_std: float = 0.01
+    # the Llama-style MHA head ("Eagle3 DeepseekV3 in MAX" §11); the MLA sizes above are unused by it
+    attention: str = "mla"          # "mla" or "mha"
+    n_kv_heads: int = 0
+    head_dim: int = 0
+    fc_inputs: int = 3              # aux states fused by fc (the MLA head always takes 3)
 
     # derived sizes ----------------------------------------------------------
     @property
@@ -79,6 +84,11 @@ class Workload:
     @property
     def latent_dim(self) -> int:
         return self.kv_lora_rank + self.qk_rope_dim
+
+    @property
+    def cache_dim(self) -> int:
+        """Width of one cache row: [c_kv | k_rope] (MLA) or [k (n_kv x d) | v (n_kv x d)] (MHA)."""
+        return 2 * self.n_kv_heads * self.head_dim if self.attention == "mha" else self.latent_dim
 
     @property
     def max_ctx(self) -> int:
@@ -93,11 +103,30 @@ class Workload:
         keys = ("hidden", "n_heads", "q_lora_rank", "kv_lora_rank", "qk_nope_dim", "qk_rope_dim",
                 "v_head_dim", "intermediate", "target_vocab", "draft_vocab", "rope_theta",
                 "yarn_factor", "yarn_original_max_pos", "yarn_beta_fast", "yarn_beta_slow",
-                "yarn_mscale", "yarn_mscale_all_dim", "rms_eps")
+                "yarn_mscale", "yarn_mscale_all_dim", "rms_eps", "attention", "n_kv_heads", "head_dim",
+                "fc_inputs")
         return {k: getattr(self, k) for k in keys}
 
     def weight_shapes(self) -> dict:
         H, nh = self.hidden, self.n_heads
+        if self.attention == "mha":
+            d, nkv = self.head_dim, self.n_kv_heads
+            return {
+                "embed": (self.target_vocab, H),
+                "fc": (H, self.fc_inputs * H),
+                "input_norm": (H,),
+                "hidden_norm": (H,),
+                "q_proj": (nh * d, 2 * H),
+                "k_proj": (nkv * d, 2 * H),
+                "v_proj": (nkv * d, 2 * H),
+                "o": (H, nh * d),
+                "post_attn_norm": (H,),
+                "gate": (self.intermediate, H),
+                "up": (self.intermediate, H),
+                "down": (H, self.intermediate),
+                "final_norm": (H,),
+                "lm_head": (self.draft_vocab, H),
+            }
         return {
             "embed": (self.target_vocab, H),
             "fc": (H, 3 * H),
@@ -157,6 +186,19 @@ WORKLOADS: dict[str, Workload] = {
     "dsv3_b256": Workload(
         name="dsv3_b256", draft_vocab=32000, batch=256, ctx=(4096, 16384), t_new=1, gamma=7, d2t="sorted",
         accept_p=tuple(0.9 * (0.5 / 0.9) ** (i / 6) for i in range(7)), seed=1004, **_DSV3),
+    # the Llama-style MHA head on the same target: tiny fp32 head (2-way fc, 4 query heads per key/value
+    # head) and a DeepseekV3-width head (hidden 7168 = 56 heads x 128, 8 key/value heads, 3-way fc) at
+    # batch 1; no MHA head configuration is printed on the pages, these sizes are a reading
+    "mha_tiny_f32": Workload(
+        name="mha_tiny_f32", hidden=256, n_heads=8, q_lora_rank=0, kv_lora_rank=0, qk_nope_dim=0, qk_rope_dim=0,
+        v_head_dim=0, intermediate=512, target_vocab=2048, draft_vocab=1024, dtype="f32", batch=2, ctx=(64, 64),
+        t_new=4, gamma=3, d2t="uniform", accept_p=(0.7, 0.7, 0.7), yarn_factor=4.0, yarn_original_max_pos=32,
+        page_size=16, seed=1010, attention="mha", n_kv_heads=2, head_dim=32, fc_inputs=2),
+    "mha_b1": Workload(
+        name="mha_b1", hidden=7168, n_heads=56, q_lora_rank=0, kv_lora_rank=0, qk_nope_dim=0, qk_rope_dim=0,
+        v_head_dim=0, intermediate=18432, target_vocab=129280, draft_vocab=32000, dtype="bf16", batch=1,
+        ctx=(4096, 4096), t_new=1, gamma=3, d2t="sorted", accept_p=(0.7, 0.7, 0.7), yarn_factor=40.0,
+        yarn_original_max_pos=4096, seed=1011, attention="mha", n_kv_heads=8, head_dim=128, fc_inputs=3),
 }
 
 
@@ -363,7 +405,7 @@ def context_lengths(w: Workload) -> np.ndarray:
 
 def cache_rows(w: Workload, b: int, length: int) -> np.ndarray:
     """Stored cache rows [length, d_c + d_r] of sequence b (taken as already normalised/rotated)."""
-    v = normal((length, w.latent_dim), 1.0, w.seed, f"cache.{b}")
+    v = normal((length, w.cache_dim), 1.0, w.seed, f"cache.{b}")
     return _store(v, w.dtype)
 
 
@@ -388,7 +430,7 @@ def make_cache(w: Workload, lengths=None, fill=True) -> PagedCache:
     bt = page_assignment(w)
     num_pages = w.batch * w.max_pages_per_seq
     dt = np.float32 if w.dtype == "f32" else np.uint16
-    data = np.zeros((num_pages, w.page_size, w.latent_dim), dtype=dt)
+    data = np.zeros((num_pages, w.page_size, w.cache_dim), dtype=dt)
     if fill:
         def one(b):
             write_rows(data, bt[b], 0, cache_rows(w, b, int(lengths[b])), w.page_size)
@@ -427,7 +469,7 @@ def read_rows(data, bt_row, start, n, page_size):
 
 @dataclass
 class ExtendInputs:
-    aux: list                 # 3 stored arrays [N, H] (early, middle, late)
+    aux: list                 # fc_inputs stored arrays [N, H] (early, (middle,) late)
     tokens: np.ndarray        # int32 [N]
     positions: np.ndarray     # int32 [N]
     row_offsets: np.ndarray   # int32 [B+1]
@@ -441,10 +483,10 @@ def make_extend(w: Workload, lengths: np.ndarray, seqs=None) -> ExtendInputs:
     """
     seqs = list(range(w.batch)) if seqs is None else list(seqs)
     T, H = w.t_new, w.hidden
-    aux = [[], [], []]
+    aux = [[] for _ in range(w.fc_inputs)]
     toks, pos = [], []
     for b in seqs:
-        for j in range(3):
+        for j in range(w.fc_inputs):
             aux[j].append(_store(normal((T, H), 1.0, w.seed, f"aux{j}.{b}"), w.dtype))
         g = _chunk_gen(w.seed, f"tok.{b}", 0)
         toks.append(g.integers(0, w.target_vocab, size=T, dtype=np.int64).astype(np.int32))
