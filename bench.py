@@ -201,6 +201,25 @@ def algorithmic_bytes(w, ctx_lengths, fp8=False):
         # average bytes per launch over the round
         out[kind] = ((b * c + per_launch * n) / (c + n) if c + n else 0.0, c + n)
 
+    if w.attention == "mha":
+        # the Llama-style head: q_proj under "q_b", k | v under "q_a_kv_a", its own [k | v] cache rows
+        nkv, hd, F = w.n_kv_heads, w.head_dim, w.fc_inputs
+        add("fc", H * F * H * ws + Me * F * H * ws + Me * H * 4, 1)
+        for M, n in ((Me, 1), (Md, steps)):
+            if n == 0:
+                continue
+            add("q_a_kv_a", 2 * nkv * hd * 2 * H * ws + M * 2 * H * 4 + M * 2 * nkv * hd * 4, n)
+            add("q_b", nh * hd * 2 * H * ws + M * 2 * H * 4 + M * nh * hd * 4, n)
+            add("o_proj", H * nh * hd * ws + M * nh * hd * 4 + 2 * M * H * 4, n)
+            add("gate_up_silu", 2 * I * H * ws + M * H * 4 + M * I * 4, n)
+            add("down", H * I * ws + M * I * 4 + 2 * M * H * 4, n)
+            add("lm_head_argmax", w.draft_vocab * H * ws + B * H * 4, n)
+        L = [int(x) for x in ctx_lengths]
+        row = 2 * nkv * hd * ws
+        add("attention", sum(l + T for l in L) * row, 1)
+        for s in range(1, G):
+            add("attention", sum(l + T + s for l in L) * row, 1)
+        return out
     add("fc", H * (3 * H * wp + sc) + Me * 3 * H * ws + Me * H * 4, 1)
     for M, n in ((Me, 1), (Md, steps)):
         if n == 0:
@@ -239,6 +258,24 @@ def algorithmic_flops(w, ctx_lengths, unabsorbed_extend=False):
         f, c = out.get(kind, (0.0, 0))
         out[kind] = ((f * c + per_launch * n) / (c + n) if c + n else 0.0, c + n)
 
+    if w.attention == "mha":
+        nkv, hd, F = w.n_kv_heads, w.head_dim, w.fc_inputs
+        add("fc", 2.0 * Me * F * H * H, 1)
+        for M, n in ((Me, 1), (Md, G - 1)):
+            if n == 0:
+                continue
+            add("q_a_kv_a", 2.0 * M * 2 * H * 2 * nkv * hd, n)
+            add("q_b", 2.0 * M * 2 * H * nh * hd, n)
+            add("o_proj", 2.0 * M * nh * hd * H, n)
+            add("gate_up_silu", 2.0 * M * H * 2 * I, n)
+            add("down", 2.0 * M * I * H, n)
+            add("lm_head_argmax", 2.0 * B * H * w.draft_vocab, n)
+        L = [int(x) for x in ctx_lengths]
+        per_tok = 2.0 * nh * 2 * hd                  # score and value accumulation per (row, head, slot)
+        add("attention", per_tok * sum(sum(l + j + 1 for j in range(T)) for l in L), 1)
+        for s in range(1, G):
+            add("attention", per_tok * sum(l + T + s for l in L), 1)
+        return out
     add("fc", 2.0 * Me * 3 * H * H, 1)
     for M, n in ((Me, 1), (Md, G - 1)):
         if n == 0:
@@ -526,7 +563,11 @@ def run_ours(args, ws, rank, local):
         "warmup": args.warmup, "ms_per_step": round(ms_max / args.steps, 4), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None,
         "dtype": "fp8_e4m3 weights, bf16 activations and cache, fp32 accumulate" if fp8 else w.dtype, "data": "synthetic (seeded; random-init weights)",
-        "config": {"workload": f"{w.name}: DSV3-shaped EAGLE-3 head, batch {B}, context {w.ctx[0]}-{w.ctx[1]}, "
+        "config": {"workload": f"{w.name}: "
+                               + (f"Llama-style MHA EAGLE-3 head ({w.n_heads} heads, {w.n_kv_heads} key/value heads, "
+                                  f"head_dim {w.head_dim}, {w.fc_inputs}-way fc) on a DSV3 target"
+                                  if w.attention == "mha" else "DSV3-shaped EAGLE-3 head")
+                               + f", batch {B}, context {w.ctx[0]}-{w.ctx[1]}, "
                                f"T_new {w.t_new}, gamma {G}, draft vocab {w.draft_vocab}"
                                + (" with d2t" if w.d2t else ""),
                    "batch": B, "gamma": G, "ctx": list(w.ctx), "draft_vocab": w.draft_vocab,

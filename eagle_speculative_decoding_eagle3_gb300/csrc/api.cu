@@ -171,8 +171,37 @@ void attn_plan(const eagle3_draft& d, int M, int* splits, int* chunk) {
     *chunk = s > 1 ? (int)ch : 0;
 }
 
+bool mha_head(const eagle3_config_t& c) { return c.attention == EAGLE3_ATTN_MHA; }
+int fc_inputs(const eagle3_config_t& c) { return c.fc_inputs == 0 ? 3 : c.fc_inputs; }
+// width rotated by RoPE: d_r (MLA) or the whole head_dim (MHA)
+int rope_dim(const eagle3_config_t& c) { return mha_head(c) ? c.head_dim : c.qk_rope_dim; }
+
+// The Llama-style MHA head's configuration (its MLA sizes are not read).
+eagle3_status_t check_config_mha(const eagle3_config_t* c) {
+    const int dims[] = {c->hidden, c->n_heads, c->n_kv_heads, c->head_dim, c->intermediate, c->target_vocab,
+                        c->draft_vocab, c->max_batch, c->max_tokens_per_extend, c->max_ctx, c->page_size,
+                        c->max_pages_per_seq};
+    for (int v : dims)
+        if (v <= 0) return EAGLE3_ERR_INVALID_ARG;
+    if (c->n_heads % c->n_kv_heads) return EAGLE3_ERR_INVALID_ARG;
+    if (!mha_supported(c->n_heads, c->n_kv_heads, c->head_dim)) return EAGLE3_ERR_UNSUPPORTED;
+    if (c->dtype != EAGLE3_F32 && c->dtype != EAGLE3_BF16) return EAGLE3_ERR_INVALID_ARG;
+    if (c->weight_format != EAGLE3_WEIGHTS_DTYPE) return EAGLE3_ERR_UNSUPPORTED;
+    if (c->hidden % 8 || c->intermediate % 8) return EAGLE3_ERR_UNSUPPORTED;
+    if (c->draft_vocab > c->target_vocab) return EAGLE3_ERR_INVALID_ARG;
+    if (c->hidden > 16384) return EAGLE3_ERR_UNSUPPORTED;
+    if (!(c->rms_eps > 0.f) || !(c->rope_theta > 1.f) || !(c->yarn_factor >= 1.f) ||
+        c->yarn_original_max_pos <= 0)
+        return EAGLE3_ERR_INVALID_ARG;
+    if ((long)c->max_ctx > (long)c->max_pages_per_seq * c->page_size) return EAGLE3_ERR_INVALID_ARG;
+    return EAGLE3_OK;
+}
+
 eagle3_status_t check_config(const eagle3_config_t* c) {
     if (!c) return EAGLE3_ERR_INVALID_ARG;
+    if (c->attention != EAGLE3_ATTN_MLA && c->attention != EAGLE3_ATTN_MHA) return EAGLE3_ERR_INVALID_ARG;
+    if (fc_inputs(*c) != 3 && !(mha_head(*c) && fc_inputs(*c) == 2)) return EAGLE3_ERR_INVALID_ARG;
+    if (mha_head(*c)) return check_config_mha(c);
     const int dims[] = {c->hidden, c->n_heads, c->q_lora_rank, c->kv_lora_rank, c->qk_nope_dim, c->qk_rope_dim,
                         c->v_head_dim, c->intermediate, c->target_vocab, c->draft_vocab, c->max_batch,
                         c->max_tokens_per_extend, c->max_ctx, c->page_size, c->max_pages_per_seq};
@@ -208,6 +237,13 @@ eagle3_status_t check_config(const eagle3_config_t* c) {
 
 eagle3_status_t check_weights(const eagle3_config_t& c, const eagle3_weights_t* w) {
     if (!w) return EAGLE3_ERR_INVALID_ARG;
+    if (mha_head(c)) {
+        const void* p[] = {w->embed, w->fc, w->input_norm, w->hidden_norm, w->q_proj, w->k_proj, w->v_proj, w->o,
+                           w->post_attn_norm, w->gate, w->up, w->down, w->final_norm, w->lm_head};
+        for (const void* v : p)
+            if (!v || !aligned16(v)) return EAGLE3_ERR_INVALID_ARG;
+        return EAGLE3_OK;
+    }
     const void* p[] = {w->embed, w->fc, w->input_norm, w->hidden_norm, w->q_a, w->q_a_norm, w->q_b,
                        w->kv_a, w->kv_a_norm, w->kv_b, w->o, w->post_attn_norm, w->gate, w->up, w->down,
                        w->final_norm, w->lm_head};
@@ -242,6 +278,13 @@ size_t fp8_max_matrix(const eagle3_config_t& c) {
 // 128-row tile boundary; otherwise large calls stay on the GEMV path.
 bool tc_supported(const eagle3_config_t& c) {
     if (c.dtype != EAGLE3_BF16) return false;
+    if (mha_head(c)) {
+        // K of every GEMM a multiple of 64, the k | v split on a 128-row tile boundary
+        const long ks[] = {c.hidden, (long)c.n_heads * c.head_dim, c.intermediate};
+        for (long k : ks)
+            if (k % 64) return false;
+        return ((long)c.n_kv_heads * c.head_dim) % 128 == 0;
+    }
     const long ks[] = {c.hidden, c.q_lora_rank, c.kv_lora_rank, c.qk_nope_dim, (long)c.n_heads * c.v_head_dim,
                        c.intermediate, c.qk_nope_dim + c.qk_rope_dim};
     for (long k : ks)
@@ -271,7 +314,7 @@ struct Offsets {
 // The unabsorbed extend path exists for bf16 heads with the DeepseekV3 head geometry whose
 // configuration allows extends of at least kPrefillMinRows rows.
 bool prefill_allowed(const eagle3_config_t& c) {
-    return tc_supported(c) && c.max_tokens_per_extend >= kPrefillMinRows &&
+    return !mha_head(c) && tc_supported(c) && c.max_tokens_per_extend >= kPrefillMinRows &&
            prefill_supported(c.dtype == EAGLE3_BF16 ? BF16 : F32, c.qk_nope_dim, c.qk_rope_dim, c.v_head_dim);
 }
 
@@ -281,6 +324,14 @@ Offsets plan(const eagle3_config_t& c, int num_sms) {
     const long H = c.hidden, nh = c.n_heads, dqk = c.qk_nope_dim + c.qk_rope_dim;
     const long D = c.kv_lora_rank + c.qk_rope_dim, B = c.max_batch;
     const bool tc = tc_supported(c);
+    const bool mha = mha_head(c);
+    const long hd = c.head_dim, nkv = c.n_kv_heads;
+    // per-row widths: projections into cqkv ([q_a | kv_a] or [k | v]), queries, attention output; the
+    // attention partials' width per head; MLA-only buffers are empty for an MHA head
+    const long w_cqkv = mha ? 2 * nkv * hd : c.q_lora_rank + D;
+    const long w_q = mha ? nh * hd : nh * dqk, w_o = mha ? nh * hd : nh * c.v_head_dim;
+    const long w_part = mha ? hd : c.kv_lora_rank;
+    const long mla = mha ? 0 : 1;
     const long Mt = tc ? M : 0;       // rows of the bf16 activation copies
     o.m_cap = (int)M;
     o.splits_cap = (c.max_ctx + 31) / 32;
@@ -296,14 +347,14 @@ Offsets plan(const eagle3_config_t& c, int num_sms) {
     o.f = L.take(M * H * f4);
     o.carry = L.take(B * H * f4);
     o.x = L.take(M * 2 * H * f4);
-    o.cqkv = L.take(M * (c.q_lora_rank + D) * f4);
-    o.cq_hat = L.take(M * c.q_lora_rank * f4);
-    o.q = L.take(M * nh * dqk * f4);
-    o.qa = L.take(M * nh * D * f4);
-    o.qa_bf = L.take(M * nh * D * b2);
-    o.part_o = L.take(o.part_rows * nh * c.kv_lora_rank * f4);
+    o.cqkv = L.take(M * w_cqkv * f4);
+    o.cq_hat = L.take(mla * M * c.q_lora_rank * f4);
+    o.q = L.take(M * w_q * f4);
+    o.qa = L.take(mla * M * nh * D * f4);
+    o.qa_bf = L.take(mla * M * nh * D * b2);
+    o.part_o = L.take(o.part_rows * nh * w_part * f4);
     o.part_ml = L.take(o.part_rows * nh * 2 * f4);
-    o.o = L.take(M * nh * c.v_head_dim * f4);
+    o.o = L.take(M * w_o * f4);
     o.h1 = L.take(M * H * f4);
     o.y = L.take(M * H * f4);
     o.mlp = L.take(M * (size_t)c.intermediate * f4);
@@ -311,23 +362,23 @@ Offsets plan(const eagle3_config_t& c, int num_sms) {
     o.z = L.take(B * H * f4);
     o.pval = L.take(B * o.npart * f4);
     o.pidx = L.take(B * o.npart * 4);
-    o.rope_cos = L.take((size_t)c.max_ctx * (c.qk_rope_dim / 2) * f4);
-    o.rope_sin = L.take((size_t)c.max_ctx * (c.qk_rope_dim / 2) * f4);
+    o.rope_cos = L.take((size_t)c.max_ctx * (rope_dim(c) / 2) * f4);
+    o.rope_sin = L.take((size_t)c.max_ctx * (rope_dim(c) / 2) * f4);
     o.row_seq = L.take(M * 4);
     o.row_pos = L.take(M * 4);
     o.d0 = L.take(B * 4);
     o.tok_in = L.take(B * 4);
     o.err = L.take(4);
-    o.olat = L.take((tc && M > 8 ? 8 : M) * nh * c.kv_lora_rank * f4);
+    o.olat = L.take(mla * (tc && M > 8 ? 8 : M) * nh * c.kv_lora_rank * f4);
     o.x_bf = L.take(Mt * 2 * H * b2);
-    o.cqh_bf = L.take(Mt * c.q_lora_rank * b2);
-    o.q_bf = L.take(Mt * nh * dqk * b2);
-    o.olat_bf = L.take(Mt * nh * c.kv_lora_rank * b2);
-    o.o_bf = L.take(Mt * nh * c.v_head_dim * b2);
+    o.cqh_bf = L.take(mla * Mt * c.q_lora_rank * b2);
+    o.q_bf = L.take(mla * Mt * nh * dqk * b2);
+    o.olat_bf = L.take(mla * Mt * nh * c.kv_lora_rank * b2);
+    o.o_bf = L.take(Mt * w_o * b2);
     o.y_bf = L.take(Mt * H * b2);
     o.m_bf = L.take(Mt * (size_t)c.intermediate * b2);
     o.z_bf = L.take((tc ? B : 0) * H * b2);
-    o.wukt = L.take(tc ? (size_t)nh * c.kv_lora_rank * c.qk_nope_dim * b2 : 0);
+    o.wukt = L.take(tc && !mha ? (size_t)nh * c.kv_lora_rank * c.qk_nope_dim * b2 : 0);
     o.tc_part = L.take(tc ? kSplitKBytes : 0);
     o.logits = L.take(B * (size_t)c.draft_vocab * f4);   // lm_head outputs of a sampled decode step
     // unabsorbed extend attention: gathered latent rows, expanded keys/values, query tile map
@@ -348,7 +399,7 @@ Offsets plan(const eagle3_config_t& c, int num_sms) {
 // wavelength fits >= beta_fast times in the original window, is divided by the factor where it fits
 // < beta_slow times, and is blended linearly in between.
 void yarn_table(const eagle3_config_t& c, std::vector<float>& cs, std::vector<float>& sn) {
-    const int d = c.qk_rope_dim, half = d / 2;
+    const int d = rope_dim(c), half = d / 2;
     const double theta = c.rope_theta, f = c.yarn_factor, L0 = c.yarn_original_max_pos;
     auto band = [&](double beta) { return d * log(L0 / (2.0 * M_PI * beta)) / (2.0 * log(theta)); };
     double lo = floor(band(c.yarn_beta_fast));
@@ -378,7 +429,8 @@ void yarn_table(const eagle3_config_t& c, std::vector<float>& cs, std::vector<fl
 float attention_scale(const eagle3_config_t& c) {
     const double f = c.yarn_factor;
     const double m = f <= 1.0 ? 1.0 : 0.1 * c.yarn_mscale_all_dim * log(f) + 1.0;
-    return (float)(m * m / sqrt((double)(c.qk_nope_dim + c.qk_rope_dim)));
+    const int dqk = mha_head(c) ? c.head_dim : c.qk_nope_dim + c.qk_rope_dim;
+    return (float)(m * m / sqrt((double)dqk));
 }
 
 RowArgs row_args(const eagle3_draft& d, const eagle3_kv_t* kv) {
@@ -573,14 +625,14 @@ cudaError_t run_prefill_attention(eagle3_draft& d, eagle3_kv_t* kv, int M, int b
     return traced(d, K_ATTN, st, [&] { return launch_prefill_attention(pa, st); });
 }
 
-// One decoder layer over M rows.  row_offsets (extend only) lets a long extend take the unabsorbed
-// attention path.
-cudaError_t run_layer(eagle3_draft& d, eagle3_kv_t* kv, int M, const float* fused, cudaStream_t st, int batch = 0,
-                      const int32_t* row_offsets = nullptr) {
+// The MLA attention block of a layer: q_a | kv_a, latent norms and cache append, q_b, then absorbed
+// attention (or, for a long extend, the unabsorbed path); leaves o (GEMV path) or o_bf (tensor-core path).
+cudaError_t run_attention_mla(eagle3_draft& d, eagle3_kv_t* kv, int M, cudaStream_t st, int batch,
+                              const int32_t* row_offsets) {
     const eagle3_config_t& c = d.cfg;
     const eagle3_weights_t& w = d.w;
     const int H = c.hidden, dq = c.q_lora_rank, dc = c.kv_lora_rank, dr = c.qk_rope_dim, dn = c.qk_nope_dim;
-    const int nh = c.n_heads, dqk = dn + dr, D = dc + dr, dv = c.v_head_dim, I = c.intermediate;
+    const int nh = c.n_heads, dqk = dn + dr, D = dc + dr, dv = c.v_head_dim;
     const bool tc = use_tc(d, M);
     RowArgs ra = row_args(d, kv);
     // q_a | kv_a over the 2H input
@@ -644,9 +696,74 @@ cudaError_t run_layer(eagle3_draft& d, eagle3_kv_t* kv, int M, const float* fuse
             E3_TRY(run_linear(d, L, K_UNABSORB, st));
         }
     }
+    return cudaSuccess;
+}
+
+// Split plan of the MHA attention: 128-slot chunks (one 32-slot tile per warp), doubled while the
+// (row, key/value head, split) CTAs exceed about 8 per SM or the rows' splits exceed the partials.
+void mha_plan(const eagle3_draft& d, int M, int* splits, int* chunk) {
+    const int ctx = d.cfg.max_ctx;
+    auto ns = [&](int ch) { return (ctx + ch - 1) / ch; };
+    int ch = 128;
+    while (ns(ch) > 1 && ((long)M * d.cfg.n_kv_heads * ns(ch) > 8L * d.num_sms || (size_t)M * ns(ch) > d.part_rows))
+        ch *= 2;
+    *chunk = ch;
+    *splits = ns(ch);
+}
+
+// The MHA attention block ("Eagle3 DeepseekV3 in MAX" §11): q and k | v projections at 2H input, rotate-
+// half RoPE with the cache append, grouped-query attention over the head's own cache and the split
+// merge; leaves o (GEMV path) or o_bf (tensor-core path).
+cudaError_t run_attention_mha(eagle3_draft& d, eagle3_kv_t* kv, int M, cudaStream_t st) {
+    const eagle3_config_t& c = d.cfg;
+    const eagle3_weights_t& w = d.w;
+    const int H = c.hidden, nh = c.n_heads, nkv = c.n_kv_heads, hd = c.head_dim;
+    const bool tc = use_tc(d, M);
+    {
+        Lin L = lin1(d, M, d.x, d.x_bf, 2 * H, w.q_proj, nh * hd);
+        L.y = d.q; L.ldy = (long)nh * hd;
+        E3_TRY(run_linear(d, L, K_Q_B, st));
+    }
+    {
+        Lin L = lin1(d, M, d.x, d.x_bf, 2 * H, w.k_proj, 2 * nkv * hd);
+        L.w1 = w.v_proj; L.n0rows = nkv * hd; L.n1rows = nkv * hd;
+        L.y = d.cqkv; L.ldy = 2L * nkv * hd;
+        E3_TRY(run_linear(d, L, K_QKV_A, st));
+    }
+    MhaArgs ma;
+    memset(&ma, 0, sizeof(ma));
+    ma.M = M; ma.nh = nh; ma.nkv = nkv; ma.d = hd;
+    ma.sigma = attention_scale(c);
+    ma.page_size = c.page_size; ma.max_pages = c.max_pages_per_seq; ma.num_pages = kv->num_pages;
+    ma.dt = c.dtype == EAGLE3_BF16 ? BF16 : F32;
+    ma.row_seq = d.row_seq; ma.row_pos = d.row_pos; ma.block_table = kv->block_table; ma.cache = kv->data;
+    ma.q = d.q; ma.kv = d.cqkv; ma.rope_cos = d.rope_cos; ma.rope_sin = d.rope_sin;
+    ma.part_o = d.part_o; ma.part_ml = d.part_ml;
+    if (tc) ma.o_bf = d.o_bf; else ma.o = d.o;
+    ma.err = d.err;
+    mha_plan(d, M, &ma.splits, &ma.chunk);
+    E3_TRY(traced(d, K_LATENT, st, [&] { return launch_mha_rope_append(ma, st); }));
+    E3_TRY(traced(d, K_ATTN, st, [&] { return launch_mha_attention(ma, st); }));
+    if (ma.splits > 1) E3_TRY(traced(d, K_COMBINE, st, [&] { return launch_mha_merge(ma, st); }));
+    return cudaSuccess;
+}
+
+// One decoder layer over M rows: the attention block of the head's kind, then o_proj with the residual,
+// the post-attention norm and the dense SiLU MLP.  row_offsets (extend only) lets a long extend of an
+// MLA head take the unabsorbed attention path.
+cudaError_t run_layer(eagle3_draft& d, eagle3_kv_t* kv, int M, const float* fused, cudaStream_t st, int batch = 0,
+                      const int32_t* row_offsets = nullptr) {
+    const eagle3_config_t& c = d.cfg;
+    const eagle3_weights_t& w = d.w;
+    const int H = c.hidden, I = c.intermediate;
+    const int w_o = mha_head(c) ? c.n_heads * c.head_dim : c.n_heads * c.v_head_dim;
+    const bool tc = use_tc(d, M);
+    RowArgs ra = row_args(d, kv);
+    if (mha_head(c)) E3_TRY(run_attention_mha(d, kv, M, st));
+    else E3_TRY(run_attention_mla(d, kv, M, st, batch, row_offsets));
     // o_proj + residual
     {
-        Lin L = lin1(d, M, d.o, d.o_bf, nh * dv, w.o, H);
+        Lin L = lin1(d, M, d.o, d.o_bf, w_o, w.o, H);
         L.s0 = fp8_scale(c, w.o_scale);
         L.epi = EPI_RESID; L.resid = fused; L.ldr = H;
         L.y = d.h1; L.ldy = H;
@@ -763,7 +880,7 @@ eagle3_status_t eagle3_draft_create(const eagle3_config_t* config, const eagle3_
     if (e == cudaSuccess) e = cudaMemcpy(d->rope_sin, sn.data(), sn.size() * sizeof(float), cudaMemcpyHostToDevice);
     if (e == cudaSuccess) e = cudaMemset(d->err, 0, sizeof(int));
     if (e == cudaSuccess) e = cudaMemset(d->carry, 0, (size_t)d->cfg.max_batch * d->cfg.hidden * sizeof(float));
-    if (e == cudaSuccess && d->tc_ok)
+    if (e == cudaSuccess && d->tc_ok && !mha_head(d->cfg))
         e = launch_transpose_wuk(d->w.kv_b, d->cfg.n_heads, d->cfg.qk_nope_dim, d->cfg.v_head_dim,
                                  d->cfg.kv_lora_rank, d->wukt, 0);
     if (e == cudaSuccess) e = cudaDeviceSynchronize();
@@ -781,20 +898,21 @@ eagle3_status_t eagle3_draft_extend(eagle3_draft_t* d, const void* const aux_hid
                                     int32_t num_tokens, eagle3_kv_t* cache, float* hidden_out, float* logits_out,
                                     void* stream) {
     if (!d || !aux_hidden || !tokens || !positions || !row_offsets || !kv_ok(cache)) return EAGLE3_ERR_INVALID_ARG;
-    for (int i = 0; i < 3; ++i)
-        if (!aux_hidden[i] || !aligned16(aux_hidden[i])) return EAGLE3_ERR_INVALID_ARG;
     const eagle3_config_t& c = d->cfg;
+    const int nfc = fc_inputs(c);
+    for (int i = 0; i < nfc; ++i)
+        if (!aux_hidden[i] || !aligned16(aux_hidden[i])) return EAGLE3_ERR_INVALID_ARG;
     if (batch < 1 || batch > c.max_batch || num_tokens < batch || num_tokens > c.max_tokens_per_extend)
         return EAGLE3_ERR_INVALID_ARG;
     cudaStream_t st = (cudaStream_t)stream;
     const int H = c.hidden, M = num_tokens;
     const bool tc = use_tc(*d, M);
     RowArgs ra = row_args(*d, cache);
-    // fc: f = [a_early | a_mid | a_late] W_fc^T  (3H -> H, no bias)
+    // fc: f = [a_early | a_mid | a_late] W_fc^T  (3H -> H, no bias; an MHA head may fuse two states)
     {
         Lin L;
-        L.M = M; L.N = H; L.K = 3 * H; L.na = 3;
-        for (int i = 0; i < 3; ++i) {
+        L.M = M; L.N = H; L.K = nfc * H; L.na = nfc;
+        for (int i = 0; i < nfc; ++i) {
             L.a32[i] = aux_hidden[i];
             L.a16[i] = (const bf16_t*)aux_hidden[i];
             L.lda[i] = H; L.ka[i] = H;

@@ -154,6 +154,32 @@ cudaError_t launch_prefill_tiles(const PrefillArgs& a, cudaStream_t st);
 cudaError_t launch_rope_q_rows(const PrefillArgs& a, cudaStream_t st);
 cudaError_t launch_prefill_attention(const PrefillArgs& a, cudaStream_t st);
 
+// ---------------------------------------------------------------- MHA attention (Llama-style head)
+struct MhaArgs {
+    int M, nh, nkv, d;
+    float sigma;
+    int page_size, max_pages, num_pages;
+    int splits, chunk;        // split s of a row covers slots [s chunk, (s + 1) chunk) of its context
+    DType dt;                 // cache storage
+    const int* row_seq;
+    const int* row_pos;
+    const int* block_table;
+    void* cache;              // [num_pages, page_size, 2 nkv d]
+    float* q;                 // [M, nh d], rotated in place by the append kernel
+    const float* kv;          // [M, 2 nkv d] k then v projections
+    const float* rope_cos;    // [max_ctx, d / 2]
+    const float* rope_sin;
+    float* part_o;            // [M splits, nh, d] (splits > 1)
+    float* part_ml;           // [M splits, nh, 2]
+    float* o;                 // [M, nh d] fp32 output (or null)
+    __nv_bfloat16* o_bf;      // [M, nh d] bf16 output (or null)
+    int* err;
+};
+bool mha_supported(int nh, int nkv, int d);
+cudaError_t launch_mha_rope_append(const MhaArgs& a, cudaStream_t st);
+cudaError_t launch_mha_attention(const MhaArgs& a, cudaStream_t st);
+cudaError_t launch_mha_merge(const MhaArgs& a, cudaStream_t st);
+
 // ---------------------------------------------------------------- MLA attention (absorbed)
 struct AttnArgs {
     int M, nh, dn, dr, dc, dv;

@@ -1,0 +1,272 @@
+// Attention of the Llama-style MHA draft head ("Eagle3 DeepseekV3 in MAX" §11: LlamaForCausalLMEagle3 on a
+// DeepseekV3 target; "max.pipelines.architectures.eagle3_deepseekV3", Eagle3MHADeepseekV3DraftArchConfig:
+// the head keeps its own one-layer key/value cache).
+//
+//   mha_rope_append_kernel   rotate q (in place) and k by the rotate-half RoPE (dimension i pairs with
+//                            i + d/2), write the row's [k | v] entry into the paged cache at its position
+//   mha_attention_kernel     grouped-query attention, split over the context: a CTA takes one row, one
+//                            key/value head (the G query heads that share it) and one chunk of slots
+//   mha_merge_kernel         combines the splits' (max, sum, unnormalised output) of every row and head
+//
+// Cache row of slot p: [k_rot (n_kv x d) | v (n_kv x d)] in the configured dtype.  A row at position p
+// attends to slots 0..p of its sequence (causal; a decode row sees itself, after its own append).
+#include <float.h>
+#include <math.h>
+
+#include "common.cuh"
+#include "kernels.h"
+#include "../../include/eagle3.h"
+
+namespace e3 {
+
+constexpr int kMhaThreads = 128;          // 4 warps; each takes 32-slot tiles of the chunk in turn
+constexpr int kMhaWarps = kMhaThreads / 32;
+
+template <typename T>
+__global__ void __launch_bounds__(256) mha_rope_append_kernel(const MhaArgs a) {
+    pdl_trigger();
+    pdl_wait();
+    const int r = blockIdx.x;
+    const int nh = a.nh, nkv = a.nkv, d = a.d, half = d / 2;
+    const int b = a.row_seq[r], pos = a.row_pos[r];
+    const float* cs = a.rope_cos + (long)pos * half;
+    const float* sn = a.rope_sin + (long)pos * half;
+    float* q = a.q + (long)r * nh * d;
+    for (int i = threadIdx.x; i < nh * half; i += blockDim.x) {
+        const int h = i / half, j = i % half;
+        const float x0 = q[h * d + j], x1 = q[h * d + j + half];
+        q[h * d + j] = x0 * cs[j] - x1 * sn[j];
+        q[h * d + j + half] = x0 * sn[j] + x1 * cs[j];
+    }
+    const int pi = pos / a.page_size;
+    int page = -1;
+    if (pi < a.max_pages) page = a.block_table[(long)b * a.max_pages + pi];
+    if (page < 0 || page >= a.num_pages) {
+        if (threadIdx.x == 0) set_err(a.err, EAGLE3_DEVERR_PAGE);
+        return;
+    }
+    const float* kv = a.kv + (long)r * 2 * nkv * d;
+    T* dst = static_cast<T*>(a.cache) + ((long)page * a.page_size + pos % a.page_size) * (2L * nkv * d);
+    for (int i = threadIdx.x; i < nkv * half; i += blockDim.x) {
+        const int h = i / half, j = i % half;
+        const float x0 = kv[h * d + j], x1 = kv[h * d + j + half];
+        dst[h * d + j] = from_f<T>(x0 * cs[j] - x1 * sn[j]);
+        dst[h * d + j + half] = from_f<T>(x0 * sn[j] + x1 * cs[j]);
+    }
+    for (int i = threadIdx.x; i < nkv * d; i += blockDim.x) dst[nkv * d + i] = from_f<T>(kv[nkv * d + i]);
+}
+
+// One CTA: row r, key/value head g, slots [s chunk, min((s + 1) chunk, pos + 1)).  Scores: each lane
+// takes one slot of a 32-slot tile and forms the G dot products over the whole key row (the G query
+// rows sit in shared memory and are read as broadcasts).  Values: each lane owns d/32 output dimensions
+// of every head and walks the tile's slots, with each slot's probabilities shuffled from its lane.
+template <typename T, int D, int G>
+__global__ void __launch_bounds__(kMhaThreads) mha_attention_kernel(const MhaArgs a) {
+    constexpr int DL = D / 32;                       // output dimensions per lane
+    __shared__ float qs[G][D];
+    __shared__ float wm[kMhaWarps][G], wl[kMhaWarps][G];
+    __shared__ float so[G][D];
+    pdl_trigger();
+    pdl_wait();
+    const int r = blockIdx.x, g = blockIdx.y, s = blockIdx.z;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int b = a.row_seq[r], pos = a.row_pos[r];
+    const int start = s * a.chunk, end = min(pos + 1, start + a.chunk);
+    if (start >= end) return;                       // past this row's context: the merge skips it
+    const long rowlen = 2L * a.nkv * D;
+    for (int i = threadIdx.x; i < G * D; i += kMhaThreads) {
+        qs[i / D][i % D] = a.q[(long)r * a.nh * D + (long)g * G * D + i] * a.sigma;
+        so[i / D][i % D] = 0.f;
+    }
+    __syncthreads();
+    const T* cache = static_cast<const T*>(a.cache);
+    const int* bt = a.block_table + (long)b * a.max_pages;
+
+    float m[G], l[G], o[G][DL];
+#pragma unroll
+    for (int h = 0; h < G; ++h) {
+        m[h] = -INFINITY;
+        l[h] = 0.f;
+#pragma unroll
+        for (int e = 0; e < DL; ++e) o[h][e] = 0.f;
+    }
+    for (int tb = start + 32 * warp; tb < end; tb += 32 * kMhaWarps) {
+        const int j = tb + lane;
+        bool valid = j < end;
+        long off = 0;                                // this lane's slot row, in elements
+        if (valid) {
+            const int pi = j / a.page_size;
+            const int page = pi < a.max_pages ? bt[pi] : -1;
+            if (page < 0 || page >= a.num_pages) {
+                set_err(a.err, EAGLE3_DEVERR_PAGE);
+                valid = false;
+            } else {
+                off = ((long)page * a.page_size + j % a.page_size) * rowlen;
+            }
+        }
+        float sc[G];
+#pragma unroll
+        for (int h = 0; h < G; ++h) sc[h] = 0.f;
+        if (valid) {
+            const T* kr = cache + off + (long)g * D;
+#pragma unroll 4
+            for (int c = 0; c < D / 8; ++c) {
+                float kv8[8];
+                widen(ld8<false>(kr + 8 * c), kv8);
+#pragma unroll
+                for (int h = 0; h < G; ++h)
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) sc[h] = fmaf(qs[h][8 * c + e], kv8[e], sc[h]);
+            }
+        }
+        float p[G];
+#pragma unroll
+        for (int h = 0; h < G; ++h) {
+            const float x = valid ? sc[h] : -INFINITY;
+            const float mt = warp_max(x);
+            const float mn = fmaxf(m[h], mt);        // finite: lane 0's slot is always valid or flagged
+            const float mref = mn == -INFINITY ? 0.f : mn;
+            p[h] = valid ? __expf(x - mref) : 0.f;
+            const float corr = __expf(m[h] - mref);  // 0 while m is still -inf
+            l[h] = l[h] * corr + warp_sum(p[h]);
+#pragma unroll
+            for (int e = 0; e < DL; ++e) o[h][e] *= corr;
+            m[h] = mn;
+        }
+        const int nt = min(32, end - tb);
+        for (int jj = 0; jj < nt; ++jj) {
+            const long voff = __shfl_sync(0xffffffffu, off, jj);
+            const bool vval = __shfl_sync(0xffffffffu, valid ? 1 : 0, jj) != 0;
+            if (!vval) continue;
+            const T* vr = cache + voff + (long)a.nkv * D + (long)g * D + lane * DL;
+            float v[DL];
+#pragma unroll
+            for (int e = 0; e < DL; ++e) v[e] = to_f(vr[e]);
+#pragma unroll
+            for (int h = 0; h < G; ++h) {
+                const float ph = __shfl_sync(0xffffffffu, p[h], jj);
+#pragma unroll
+                for (int e = 0; e < DL; ++e) o[h][e] = fmaf(ph, v[e], o[h][e]);
+            }
+        }
+    }
+    // combine the warps: common maximum per head, rescaled sums
+    if (lane == 0) {
+#pragma unroll
+        for (int h = 0; h < G; ++h) { wm[warp][h] = m[h]; wl[warp][h] = l[h]; }
+    }
+    __syncthreads();
+    float M[G], L[G];
+#pragma unroll
+    for (int h = 0; h < G; ++h) {
+        M[h] = wm[0][h];
+        for (int w = 1; w < kMhaWarps; ++w) M[h] = fmaxf(M[h], wm[w][h]);
+        L[h] = 0.f;
+        for (int w = 0; w < kMhaWarps; ++w)
+            if (wm[w][h] != -INFINITY) L[h] += wl[w][h] * __expf(wm[w][h] - M[h]);
+    }
+    for (int w = 0; w < kMhaWarps; ++w) {
+        if (warp == w && m[0] != -INFINITY) {
+#pragma unroll
+            for (int h = 0; h < G; ++h) {
+                const float f = __expf(m[h] - M[h]);
+#pragma unroll
+                for (int e = 0; e < DL; ++e) so[h][lane * DL + e] += o[h][e] * f;
+            }
+        }
+        __syncthreads();
+    }
+    const int head0 = g * G;
+    if (a.splits == 1) {
+        for (int i = threadIdx.x; i < G * D; i += kMhaThreads) {
+            const int h = i / D, e = i % D;
+            const float v = so[h][e] / L[h];
+            const long idx = (long)r * a.nh * D + (long)(head0 + h) * D + e;
+            if (a.o) a.o[idx] = v;
+            if (a.o_bf) a.o_bf[idx] = __float2bfloat16_rn(v);
+        }
+    } else {
+        const long pr = (long)r * a.splits + s;
+        for (int i = threadIdx.x; i < G * D; i += kMhaThreads) {
+            const int h = i / D, e = i % D;
+            a.part_o[(pr * a.nh + head0 + h) * D + e] = so[h][e];
+        }
+        if (threadIdx.x < G) {
+            const int h = threadIdx.x;
+            a.part_ml[(pr * a.nh + head0 + h) * 2] = M[h];
+            a.part_ml[(pr * a.nh + head0 + h) * 2 + 1] = L[h];
+        }
+    }
+}
+
+// One CTA per (row, head), one thread per output dimension: o = sum_s e^(m_s - M) o_s / sum_s e^(m_s - M) l_s
+// over the splits that hold any of the row's slots.
+__global__ void __launch_bounds__(256) mha_merge_kernel(const MhaArgs a) {
+    pdl_trigger();
+    pdl_wait();
+    const int r = blockIdx.x, h = blockIdx.y, e = threadIdx.x;
+    const int pos = a.row_pos[r];
+    const int nvalid = min(a.splits, (pos + a.chunk) / a.chunk);
+    const long pr0 = (long)r * a.splits;
+    float M = -INFINITY;
+    for (int s = 0; s < nvalid; ++s) M = fmaxf(M, a.part_ml[((pr0 + s) * a.nh + h) * 2]);
+    float L = 0.f, acc = 0.f;
+    for (int s = 0; s < nvalid; ++s) {
+        const float ms = a.part_ml[((pr0 + s) * a.nh + h) * 2];
+        const float f = ms == -INFINITY ? 0.f : __expf(ms - M);
+        L += f * a.part_ml[((pr0 + s) * a.nh + h) * 2 + 1];
+        if (e < a.d) acc += f * a.part_o[((pr0 + s) * a.nh + h) * a.d + e];
+    }
+    if (e < a.d) {
+        const float v = acc / L;
+        const long idx = (long)r * a.nh * a.d + (long)h * a.d + e;
+        if (a.o) a.o[idx] = v;
+        if (a.o_bf) a.o_bf[idx] = __float2bfloat16_rn(v);
+    }
+}
+
+bool mha_supported(int nh, int nkv, int d) {
+    if (nkv < 1 || nh % nkv) return false;
+    const int G = nh / nkv;
+    return (d == 32 || d == 64 || d == 128) && (G == 1 || G == 2 || G == 4 || G == 7 || G == 8);
+}
+
+cudaError_t launch_mha_rope_append(const MhaArgs& a, cudaStream_t st) {
+    if (a.dt == BF16) return launch_pdl(mha_rope_append_kernel<bf16>, dim3(a.M), dim3(256), 0, st, a);
+    return launch_pdl(mha_rope_append_kernel<float>, dim3(a.M), dim3(256), 0, st, a);
+}
+
+template <typename T, int D>
+static cudaError_t launch_attn_g(const MhaArgs& a, dim3 grid, cudaStream_t st) {
+    switch (a.nh / a.nkv) {
+        case 1: return launch_pdl(mha_attention_kernel<T, D, 1>, grid, dim3(kMhaThreads), 0, st, a);
+        case 2: return launch_pdl(mha_attention_kernel<T, D, 2>, grid, dim3(kMhaThreads), 0, st, a);
+        case 4: return launch_pdl(mha_attention_kernel<T, D, 4>, grid, dim3(kMhaThreads), 0, st, a);
+        case 7: return launch_pdl(mha_attention_kernel<T, D, 7>, grid, dim3(kMhaThreads), 0, st, a);
+        case 8: return launch_pdl(mha_attention_kernel<T, D, 8>, grid, dim3(kMhaThreads), 0, st, a);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+template <typename T>
+static cudaError_t launch_attn_t(const MhaArgs& a, dim3 grid, cudaStream_t st) {
+    switch (a.d) {
+        case 32: return launch_attn_g<T, 32>(a, grid, st);
+        case 64: return launch_attn_g<T, 64>(a, grid, st);
+        case 128: return launch_attn_g<T, 128>(a, grid, st);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+cudaError_t launch_mha_attention(const MhaArgs& a, cudaStream_t st) {
+    if (!mha_supported(a.nh, a.nkv, a.d) || a.chunk < 1 || a.splits < 1) return cudaErrorInvalidValue;
+    const dim3 grid(a.M, a.nkv, a.splits);
+    return a.dt == BF16 ? launch_attn_t<bf16>(a, grid, st) : launch_attn_t<float>(a, grid, st);
+}
+
+cudaError_t launch_mha_merge(const MhaArgs& a, cudaStream_t st) {
+    const int threads = (a.d + 31) / 32 * 32;
+    return launch_pdl(mha_merge_kernel, dim3(a.M, a.nh), dim3(threads), 0, st, a);
+}
+
+}  // namespace e3

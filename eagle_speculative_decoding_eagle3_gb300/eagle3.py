@@ -15,6 +15,7 @@ OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_STATE, ERR_OOM, ERR_CUDA, ERR_DEVICE_R
 NOALLOC_SCRATCH_BYTES = 16 << 20   # EAGLE3_NOALLOC_SCRATCH_BYTES
 F32, BF16 = 0, 1
 WEIGHTS_DTYPE, WEIGHTS_FP8 = 0, 1   # eagle3_weight_format_t
+ATTN_MLA, ATTN_MHA = 0, 1           # eagle3_attention_t
 DEVERR_TOKEN, DEVERR_POSITION, DEVERR_D2T, DEVERR_PAGE, DEVERR_ROWS = 1, 2, 4, 8, 16
 
 
@@ -25,7 +26,9 @@ class eagle3_config_t(C.Structure):
         "page_size", "max_pages_per_seq")] + [(n, C.c_float) for n in (
             "rms_eps", "rope_theta", "yarn_factor", "yarn_beta_fast", "yarn_beta_slow", "yarn_mscale",
             "yarn_mscale_all_dim")] + [("yarn_original_max_pos", C.c_int32), ("rope_interleave", C.c_int32),
-                                       ("dtype", C.c_int32), ("weight_format", C.c_int32)]
+                                       ("dtype", C.c_int32), ("weight_format", C.c_int32),
+                                       ("attention", C.c_int32), ("n_kv_heads", C.c_int32),
+                                       ("head_dim", C.c_int32), ("fc_inputs", C.c_int32)]
 
 
 WEIGHT_NAMES = ("embed", "fc", "input_norm", "hidden_norm", "q_a", "q_a_norm", "q_b", "kv_a", "kv_a_norm", "kv_b",
@@ -34,10 +37,13 @@ WEIGHT_NAMES = ("embed", "fc", "input_norm", "hidden_norm", "q_a", "q_a_norm", "
 
 # the projection matrices that EAGLE3_WEIGHTS_FP8 stores as E4M3 codes with per-row scales
 FP8_WEIGHT_NAMES = ("fc", "q_a", "kv_a", "q_b", "o", "gate", "up", "down", "lm_head")
+# the MHA head's own projections (its unused MLA fields stay NULL)
+MHA_WEIGHT_NAMES = ("q_proj", "k_proj", "v_proj")
 
 
 class eagle3_weights_t(C.Structure):
-    _fields_ = [(n, C.c_void_p) for n in WEIGHT_NAMES] + [(n + "_scale", C.c_void_p) for n in FP8_WEIGHT_NAMES]
+    _fields_ = ([(n, C.c_void_p) for n in WEIGHT_NAMES] + [(n + "_scale", C.c_void_p) for n in FP8_WEIGHT_NAMES]
+                + [(n, C.c_void_p) for n in MHA_WEIGHT_NAMES])
 
 
 class eagle3_kv_t(C.Structure):
@@ -140,8 +146,8 @@ def make_config(**fields) -> eagle3_config_t:
 def make_weights(tensors, scales=None) -> eagle3_weights_t:
     """Weight pointers; `scales` (FP8 heads) maps each of FP8_WEIGHT_NAMES to its row scales."""
     w = eagle3_weights_t()
-    for n in WEIGHT_NAMES:
-        setattr(w, n, _ptr(tensors[n]))
+    for n in WEIGHT_NAMES + MHA_WEIGHT_NAMES:
+        setattr(w, n, _ptr(tensors.get(n)))
     for n in FP8_WEIGHT_NAMES if scales else ():
         setattr(w, n + "_scale", _ptr(scales[n]))
     return w
@@ -169,7 +175,7 @@ def eagle3_draft_create(config: eagle3_config_t, weights: eagle3_weights_t) -> i
 
 def eagle3_draft_extend(handle, aux_hidden, tokens, positions, row_offsets, batch, num_tokens, cache: eagle3_kv_t,
                         hidden_out=None, logits_out=None, stream=None):
-    aux = (C.c_void_p * 3)(*[_ptr(a) for a in aux_hidden])
+    aux = (C.c_void_p * 3)(*[_ptr(a) for a in aux_hidden] + [None] * (3 - len(aux_hidden)))
     _check("eagle3_draft_extend", _lib().eagle3_draft_extend(
         handle, aux, _ptr(tokens), _ptr(positions), _ptr(row_offsets), int(batch), int(num_tokens), C.byref(cache),
         _ptr(hidden_out), _ptr(logits_out), _stream(stream)))

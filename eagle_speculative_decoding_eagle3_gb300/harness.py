@@ -32,7 +32,9 @@ def config_for(w, max_batch=None, max_tokens=None, fp8=False) -> E.eagle3_config
         rms_eps=w.rms_eps, rope_theta=w.rope_theta, yarn_factor=w.yarn_factor, yarn_beta_fast=w.yarn_beta_fast,
         yarn_beta_slow=w.yarn_beta_slow, yarn_mscale=w.yarn_mscale, yarn_mscale_all_dim=w.yarn_mscale_all_dim,
         yarn_original_max_pos=w.yarn_original_max_pos, rope_interleave=1,
-        dtype=E.BF16 if w.dtype == "bf16" else E.F32, weight_format=E.WEIGHTS_FP8 if fp8 else E.WEIGHTS_DTYPE)
+        dtype=E.BF16 if w.dtype == "bf16" else E.F32, weight_format=E.WEIGHTS_FP8 if fp8 else E.WEIGHTS_DTYPE,
+        attention=E.ATTN_MHA if w.attention == "mha" else E.ATTN_MLA, n_kv_heads=w.n_kv_heads,
+        head_dim=w.head_dim, fc_inputs=w.fc_inputs)
 
 
 @dataclass
@@ -66,7 +68,9 @@ class DeviceHead:
         self.device = device
         self.tensors = {}
         self.scales = {}
-        for n in E.WEIGHT_NAMES:
+        for n in E.WEIGHT_NAMES + E.MHA_WEIGHT_NAMES:
+            if n not in stored_weights:
+                continue                       # the other head kind's weights
             t = to_device(stored_weights[n], device)
             if fp8 and n in E.FP8_WEIGHT_NAMES:
                 t, self.scales[n] = quantize_fp8(t)

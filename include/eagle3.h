@@ -76,6 +76,19 @@ typedef enum { EAGLE3_F32 = 0, EAGLE3_BF16 = 1 } eagle3_dtype_t;
  *                         the configured dtype. */
 typedef enum { EAGLE3_WEIGHTS_DTYPE = 0, EAGLE3_WEIGHTS_FP8 = 1 } eagle3_weight_format_t;
 
+/* Attention of the head's decoder layer.
+ *   EAGLE3_ATTN_MLA  the DeepseekV3 draft (Eagle3DeepseekV2ForCausalLM): latent q/kv projections, one
+ *                    latent cache row [c_kv_hat | k_rope] per token ("Eagle3 DeepseekV3 in MAX" §4, §7);
+ *   EAGLE3_ATTN_MHA  the Llama-style draft (LlamaForCausalLMEagle3, "Eagle3 DeepseekV3 in MAX" §11):
+ *                    q/k/v projections at 2H input, rotate-half RoPE on q and k (dimension i pairs with
+ *                    i + head_dim/2), grouped-query attention (query head h reads key/value head
+ *                    h / (n_heads / n_kv_heads)) over the head's own cache, whose row per token is
+ *                    [k_rot (n_kv_heads x head_dim) | v (n_kv_heads x head_dim)]; softmax scale
+ *                    head_dim^-1/2 times the squared YaRN attention factor.  The MLA sizes of the config
+ *                    (q_lora_rank, kv_lora_rank, qk_nope_dim, qk_rope_dim, v_head_dim, rope_interleave) are
+ *                    not used. */
+typedef enum { EAGLE3_ATTN_MLA = 0, EAGLE3_ATTN_MHA = 1 } eagle3_attention_t;
+
 /* Device error word bits (eagle3_draft_get_error). */
 #define EAGLE3_DEVERR_TOKEN    1   /* an input token id was outside [0, target_vocab) */
 #define EAGLE3_DEVERR_POSITION 2   /* a position was >= max_ctx */
@@ -113,6 +126,12 @@ typedef struct {
     int32_t rope_interleave;      /* must be 1: pairs (2i, 2i+1) rotate together */
     eagle3_dtype_t dtype;         /* storage type of weights, aux states and cache */
     eagle3_weight_format_t weight_format; /* storage of the projection matrices (0 = dtype) */
+    eagle3_attention_t attention; /* 0 = MLA (the fields above), 1 = MHA (the fields below) */
+    int32_t n_kv_heads;           /* MHA: key/value heads; n_heads a multiple of it (n_heads / n_kv_heads
+                                   * in {1, 2, 4, 7, 8}) */
+    int32_t head_dim;             /* MHA: d in {32, 64, 128} */
+    int32_t fc_inputs;            /* aux states fc fuses: 3 (0 means 3), or 2 for an MHA head whose fc is
+                                   * [H, 2H] (§11: the width is read from fc.weight) */
 } eagle3_config_t;
 
 /* Device pointers to the head's weights (BORROWED).  Shapes [rows, cols], row-major. */
@@ -138,6 +157,11 @@ typedef struct {
      * matrices above, one per row of the matrix of the same name. */
     const float *fc_scale, *q_a_scale, *kv_a_scale, *q_b_scale, *o_scale, *gate_scale, *up_scale,
         *down_scale, *lm_head_scale;
+    /* EAGLE3_ATTN_MHA only (its q_a, q_a_norm, q_b, kv_a, kv_a_norm and kv_b are unused and may be NULL;
+     * its fc is [H, fc_inputs H] and its o [H, n_heads head_dim]): */
+    const void *q_proj;         /* [n_heads head_dim, 2H] */
+    const void *k_proj;         /* [n_kv_heads head_dim, 2H] */
+    const void *v_proj;         /* [n_kv_heads head_dim, 2H] */
 } eagle3_weights_t;
 
 /* The one-layer latent cache (BORROWED).  Slot p of sequence b is row (p % page_size) of page
@@ -164,7 +188,8 @@ EAGLE3_API eagle3_status_t eagle3_draft_workspace_bytes(const eagle3_config_t *c
 
 /* Extend (draft step 0, "Eagle3 DeepseekV3 in MAX" §4 and §9): runs the whole head over
  * `num_tokens` new rows of `batch` sequences.
- *   aux_hidden  host array of 3 device pointers, each [num_tokens, H] (early, middle, late)
+ *   aux_hidden  host array of 3 device pointers, each [num_tokens, H] (early, middle, late); with
+ *               fc_inputs 2 only the first two are read (early, late) and the third may be NULL
  *   tokens      [num_tokens] target-vocab ids paired with the aux rows
  *   positions   [num_tokens] slot of each row; within a sequence strictly increasing, and every
  *               slot below a row's position must already hold that sequence's cache entry

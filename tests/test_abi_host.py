@@ -115,3 +115,37 @@ def test_fp8_weight_format_checks_without_a_gpu(lib):
     assert lib.eagle3_quantize_e4m3(None, E.BF16, 4, 8, None, None, None) == E.ERR_INVALID_ARG
     assert lib.eagle3_quantize_e4m3(256, E.BF16, 0, 8, 256, 256, None) == E.ERR_INVALID_ARG
     assert lib.eagle3_quantize_e4m3(256, 7, 4, 8, 256, 256, None) == E.ERR_UNSUPPORTED
+
+
+def _mha_config(**kw):
+    base = dict(hidden=7168, n_heads=56, n_kv_heads=8, head_dim=128, intermediate=18432, target_vocab=129280,
+                draft_vocab=32000, max_batch=1, max_tokens_per_extend=1, max_ctx=4100, page_size=64,
+                max_pages_per_seq=65, yarn_factor=40.0, dtype=E.BF16, attention=E.ATTN_MHA, fc_inputs=3)
+    base.update(kw)
+    return E.make_config(**base)
+
+
+def test_mha_config_checks_without_a_gpu(lib):
+    # the MHA head ignores the MLA sizes (zero here) and checks its own
+    n = E.eagle3_draft_workspace_bytes(_mha_config())
+    assert 0 < n < 1 << 30
+    assert E.eagle3_draft_workspace_bytes(_mha_config(fc_inputs=2)) > 0
+    bad = [dict(attention=2), dict(n_kv_heads=0), dict(n_kv_heads=5), dict(n_heads=12, n_kv_heads=4),
+           dict(head_dim=96), dict(weight_format=E.WEIGHTS_FP8), dict(fc_inputs=1), dict(hidden=7164),
+           dict(max_ctx=10_000)]
+    for kw in bad:
+        with pytest.raises(E.Eagle3Error) as ei:
+            E.eagle3_draft_workspace_bytes(_mha_config(**kw))
+        assert ei.value.status in (E.ERR_INVALID_ARG, E.ERR_UNSUPPORTED), kw
+    # a 2-way fc belongs to the MHA head only
+    with pytest.raises(E.Eagle3Error):
+        E.eagle3_draft_workspace_bytes(_dsv3_config(fc_inputs=2))
+    # an MHA head without its q/k/v projections is rejected before any CUDA call, whatever its MLA
+    # fields hold
+    h = C.c_void_p()
+    cfg = _mha_config()
+    w = E.eagle3_weights_t()
+    for nm in E.WEIGHT_NAMES:
+        setattr(w, nm, 256)
+    assert lib.eagle3_draft_create(C.byref(cfg), C.byref(w), C.byref(h)) == E.ERR_INVALID_ARG
+    assert h.value is None
