@@ -34,6 +34,8 @@ fusion or reordering).  Pins (``tests/test_oracle_*.py``):
   e4m3_*            every code decodes per the OCP E4M3 table (max 448, one NaN pattern); encode(decode(c)) ==
                     c; midpoints round to the even code; values saturate at 448; the array
                     encoder equals the scalar one on every code, midpoint and a random sweep
+  e2m1_* / nvfp4    the eight E2M1 magnitudes and their signs; every midpoint rounds to the even code;
+                    saturation at 6; the NVFP4 rule restated element by element; the block error bound
   accept_relaxed    rows outside thinking == greedy accept; k = 1 or delta below every gap ==
                     greedy; hand example with the default delta 0.6; monotone in delta
   draft_extend /    composition invariants: one T-row extend == T one-row extends
@@ -48,4 +50,5 @@ from .head import (  # noqa: F401
     softmax_scale, split_kv_b, mla_attention, mha_attention, decoder_rows, final_logits, argmax_lowest,
     top2_gap, d2t_remap, SeqCache, draft_extend, draft_decode_step, draft_round, accept, accept_relaxed,
     sample_filtered, accept_residual, e4m3_decode, e4m3_encode, e4m3_encode_array, quantize_rows_e4m3,
+    e2m1_decode, e2m1_encode_array, quantize_nvfp4,
 )

@@ -634,3 +634,59 @@ def quantize_rows_e4m3(W):
     codes = e4m3_encode_array(inv)
     deq = _E4M3_ALL[codes] * scales[:, None].astype(np.float64)
     return codes, scales, deq
+
+
+# --------------------------------------------------------------------------- NVFP4 draft weights
+_E2M1_POS = np.array([0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0])     # codes 0..7 (sign in bit 3)
+
+
+def e2m1_decode(code):
+    """Value of a 4-bit E2M1 code (OCP FP4: sign bit 3, 2 exponent bits with bias 1, 1 mantissa bit,
+    subnormal 0.5 at exponent 0, largest 6, no infinities or NaN)."""
+    code = int(code) & 0xF
+    v = _E2M1_POS[code & 7]
+    return -v if code & 8 else v
+
+
+def e2m1_encode_array(x):
+    """Nearest E2M1 code of each x, ties to the even code, magnitudes above 6 saturating to 6."""
+    x = np.asarray(x, dtype=np.float64)
+    sign = np.where(np.signbit(x), 8, 0).astype(np.uint8)
+    a = np.minimum(np.abs(x), 6.0)
+    i = np.searchsorted(_E2M1_POS, a)
+    lo = np.maximum(i - 1, 0)
+    hi = np.minimum(i, 7)
+    dl = a - _E2M1_POS[lo]
+    dh = _E2M1_POS[hi] - a
+    pick_lo = (dl < dh) | ((dl == dh) & (lo % 2 == 0))
+    code = np.where(i == 0, 0, np.where(pick_lo, lo, hi)).astype(np.uint8)
+    return code | sign
+
+
+def quantize_nvfp4(W):
+    """NVFP4 weights ("EAGLE head deep dive", deployment: the drafter quantized to NVFP4 by post-training
+    quantization; the format is not printed).  Reading, the published NVFP4 layout: E2M1 values, one
+    E4M3 scale per 16 consecutive weights of a row, one fp32 scale per matrix, all formed in fp32 as the
+    GPU forms them:
+        g   = max |W| / (448 * 6)                           (1 for an all-zero matrix)
+        s_b = E4M3(max_{k in b} |W[n, k]| / (6 g))          (6 g rounded first)
+        e_b = decode(s_b) * g                               (the block's effective scale, fp32)
+        q   = E2M1(W / e_b), or 0 where e_b == 0
+    and the head uses decode(q) * decode(s_b) * g.  Returns (codes uint8 [N, K] (one code per element,
+    0..15), block scale codes uint8 [N, K/16], g fp32, dequantized fp64 [N, K])."""
+    W = np.asarray(W, dtype=np.float32)
+    N, K = W.shape
+    assert K % 16 == 0
+    amax = np.float32(np.abs(W).max())
+    g = np.float32(amax / np.float32(2688.0)) if amax > 0 else np.float32(1.0)
+    six_g = np.float32(np.float32(6.0) * g)
+    blocks = W.reshape(N, K // 16, 16)
+    bmax = np.abs(blocks).max(axis=2)
+    sb = e4m3_encode_array((bmax / six_g).astype(np.float32))                 # fp32 quotient
+    eff = (_E4M3_ALL[sb].astype(np.float32) * g).astype(np.float32)          # fp32 product
+    with np.errstate(divide="ignore", invalid="ignore"):
+        quot = np.where(eff[:, :, None] > 0, blocks / eff[:, :, None], np.float32(0.0)).astype(np.float32)
+    codes = e2m1_encode_array(quot).reshape(N, K)
+    vals = np.where(codes & 8, -1.0, 1.0) * _E2M1_POS[codes & 7]
+    deq = vals.reshape(N, K // 16, 16) * _E4M3_ALL[sb][:, :, None] * np.float64(g)
+    return codes, sb, g, deq.reshape(N, K)

@@ -518,3 +518,50 @@ def test_mha_attention_single_slot_and_equal_keys():
     cache[:, :8] = cache[0, :8]
     o = O.mha_attention(q, np.array([4]), cache, h)
     np.testing.assert_allclose(o[0], np.repeat(cache[:, 8:].mean(axis=0, keepdims=True), 4, axis=0), rtol=1e-12)
+
+
+# ---------------------------------------------------------------- NVFP4 (E2M1 codes, E4M3 block scales)
+def test_e2m1_table_ties_and_saturation():
+    # OCP FP4 E2M1: magnitudes 0, 0.5, 1, 1.5, 2, 3, 4, 6; bit 3 is the sign
+    assert [O.e2m1_decode(c) for c in range(8)] == [0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0]
+    assert [O.e2m1_decode(c) for c in range(8, 16)] == [-0.0, -0.5, -1.0, -1.5, -2.0, -3.0, -4.0, -6.0]
+    # every code round-trips; midpoints go to the even code: 0.25 -> 0, 0.75 -> 1, 1.25 -> 1, 1.75 -> 2,
+    # 2.5 -> 2, 3.5 -> 4, 5 -> 4; above 6 saturates
+    vals = np.array([O.e2m1_decode(c) for c in range(16)])
+    np.testing.assert_array_equal(O.e2m1_encode_array(vals)[[c for c in range(16) if c != 8]],
+                                  [c for c in range(16) if c != 8])
+    got = O.e2m1_encode_array(np.array([0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0, 7.0, 1e9, -5.0, 0.26, -0.1]))
+    np.testing.assert_array_equal(got, [0, 2, 2, 4, 4, 6, 6, 7, 7, 14, 1, 8])
+
+
+def test_quantize_nvfp4_rule_and_error_bound():
+    rng = np.random.default_rng(31)
+    W = rng.normal(0, 0.02, size=(5, 64)).astype(np.float32)
+    W[2, 16:32] = 0.0                                       # an all-zero block: scale code 0, codes 0
+    W[4, :16] = np.float32(1e-9)                            # a block whose scale underflows E4M3
+    codes, sb, g, deq = O.quantize_nvfp4(W)
+    assert codes.shape == (5, 64) and sb.shape == (5, 4) and codes.max() <= 15
+    amax = np.float32(np.abs(W).max())
+    assert g == np.float32(amax / np.float32(2688.0))
+    # the rule written out for every block, with the scalar E4M3 encoder
+    six_g = np.float32(np.float32(6.0) * g)
+    for n in range(5):
+        for b in range(4):
+            blk = W[n, 16 * b:16 * b + 16]
+            s = O.e4m3_encode(np.float32(np.abs(blk).max()) / six_g)
+            assert s == sb[n, b]
+            eff = np.float32(np.float32(O.e4m3_decode(s)) * g)
+            for k in range(16):
+                q = np.float32(blk[k]) / eff if eff > 0 else 0.0
+                assert O.e2m1_encode_array(np.array([q]))[0] == codes[n, 16 * b + k]
+    assert np.all(sb[2, 1] == 0) and np.all(codes[2, 16:32] == 0)
+    # error bound: within half a step of the E2M1 grid (<= 1 at the top of the range) times the block's
+    # effective scale, plus the scale's own E4M3 rounding (the largest element maps to 6 * (1 +- 2^-4))
+    for n in range(5):
+        for b in range(4):
+            blk = W[n, 16 * b:16 * b + 16].astype(np.float64)
+            eff = O.e4m3_decode(sb[n, b]) * float(g)
+            if eff == 0:
+                continue
+            err = np.abs(deq[n, 16 * b:16 * b + 16] - blk)
+            assert np.all(err <= np.maximum(np.abs(blk) * 0.25, 0.25 * eff) * (1 + 1e-6) + 1e-12)
