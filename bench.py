@@ -45,8 +45,9 @@ def parse_args(argv=None):
     p.add_argument("--e2e-steps", type=int, default=None)
     p.add_argument("--sampling", default=None,
                    help="T,top_k,top_p: sampled drafts and residual acceptance instead of greedy rounds")
-    p.add_argument("--weights", choices=["bf16", "fp8"], default="bf16",
-                   help="fp8: the nine projection matrices as FP8 E4M3 codes with per-row fp32 scales")
+    p.add_argument("--weights", choices=["bf16", "fp8", "nvfp4"], default="bf16",
+                   help="fp8: the nine projection matrices as FP8 E4M3 codes with per-row fp32 scales; nvfp4: "
+                        "as E2M1 codes with E4M3 scales per 16 weights and an fp32 scale per matrix")
     return p.parse_args(argv)
 
 
@@ -179,15 +180,16 @@ class ClockSampler:
 
 
 # --------------------------------------------------------------------------------------------- bytes model
-def algorithmic_bytes(w, ctx_lengths, fp8=False):
+def algorithmic_bytes(w, ctx_lengths, fp8=False, nvfp4=False):
     """Algorithmic HBM bytes of each kernel launch kind for one round (weights + KV + activations).
 
     Returns {kind: (bytes_per_launch, launches_per_round)}; activations are fp32 in the workspace.
-    fp8: the projection matrices (all but kv_b) take one byte per weight plus a 4-byte scale per row.
+    fp8: the projection matrices (all but kv_b) take one byte per weight plus a 4-byte scale per row;
+    nvfp4: half a byte per weight plus a one-byte scale per 16 weights (the matrix scale is negligible).
     """
     ws = 2 if w.dtype == "bf16" else 4
-    wp = 1 if fp8 else ws                      # bytes per projection weight
-    sc = 4 if fp8 else 0                       # bytes per projection row (its scale)
+    wp = 1 if fp8 else (0.5 + 1 / 16 if nvfp4 else ws)   # bytes per projection weight
+    sc = 4 if fp8 else 0                                  # bytes per projection row (its scale)
     B, T, G, H = w.batch, w.t_new, w.gamma, w.hidden
     nh, dq, dc, dr, dn, dv, I = w.n_heads, w.q_lora_rank, w.kv_lora_rank, w.qk_rope_dim, w.qk_nope_dim, \
         w.v_head_dim, w.intermediate
@@ -340,8 +342,8 @@ def run_ours(args, ws, rank, local):
     ex = WL.make_extend(w, lengths)
     d2t = WL.make_d2t(w)
 
-    fp8 = args.weights == "fp8"
-    head = HN.DeviceHead(w, stored, fp8=fp8)
+    fp8, nvfp4 = args.weights == "fp8", args.weights == "nvfp4"
+    head = HN.DeviceHead(w, stored, fp8=fp8, nvfp4=nvfp4)
     cache = head.cache(paged)
     len0 = cache.lengths.clone()
     din = head.extend_inputs(ex)
@@ -524,8 +526,8 @@ def run_ours(args, ws, rank, local):
     # ---------------------------------------------------------------- roofline of the dominant kernel
     peaks, src = measured_peaks()
     hbm = peak_hbm(peaks)
-    model = algorithmic_bytes(w, lengths, fp8=fp8)
-    traffic_key = w.name + ("+fp8" if fp8 else "")
+    model = algorithmic_bytes(w, lengths, fp8=fp8, nvfp4=nvfp4)
+    traffic_key = w.name + ("+" + args.weights if args.weights != "bf16" else "")
     fmodel = algorithmic_flops(w, lengths, unabsorbed_extend="kv_expand" in prof_all)
     tpeak, tkey = peak_tensor(peaks)
     kernels = {}
@@ -562,7 +564,8 @@ def run_ours(args, ws, rank, local):
         "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": ws, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms_max / args.steps, 4), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None,
-        "dtype": "fp8_e4m3 weights, bf16 activations and cache, fp32 accumulate" if fp8 else w.dtype, "data": "synthetic (seeded; random-init weights)",
+        "dtype": (f"{'fp8_e4m3' if fp8 else 'nvfp4'} weights, bf16 activations and cache, fp32 accumulate"
+                  if fp8 or nvfp4 else w.dtype), "data": "synthetic (seeded; random-init weights)",
         "config": {"workload": f"{w.name}: "
                                + (f"Llama-style MHA EAGLE-3 head ({w.n_heads} heads, {w.n_kv_heads} key/value heads, "
                                   f"head_dim {w.head_dim}, {w.fc_inputs}-way fc) on a DSV3 target"
@@ -572,7 +575,10 @@ def run_ours(args, ws, rank, local):
                                + (" with d2t" if w.d2t else ""),
                    "batch": B, "gamma": G, "ctx": list(w.ctx), "draft_vocab": w.draft_vocab,
                    "weights": ("FP8 E4M3 projection matrices with per-row fp32 scales (quantized on the GPU "
-                               "from the bf16 weights); kv_b, embedding and norms bf16") if fp8 else w.dtype,
+                               "from the bf16 weights); kv_b, embedding and norms bf16") if fp8 else
+                              ("NVFP4 projection matrices: E2M1 codes, E4M3 scales per 16 weights, an fp32 scale "
+                               "per matrix (quantized on the GPU from the bf16 weights); kv_b, embedding and norms "
+                               "bf16") if nvfp4 else w.dtype,
                    "step": "extend + (gamma-1) decode steps + acceptance" if sampling is None else
                            f"extend + (gamma-1) sampled decode steps (T {sampling[0]}, top_k {sampling[1]}, "
                            f"top_p {sampling[2]}) + residual acceptance",

@@ -210,12 +210,15 @@ eagle3_status_t check_config(const eagle3_config_t* c) {
     if (c->qk_rope_dim % 2) return EAGLE3_ERR_INVALID_ARG;
     if (c->rope_interleave != 1) return EAGLE3_ERR_UNSUPPORTED;
     if (c->dtype != EAGLE3_F32 && c->dtype != EAGLE3_BF16) return EAGLE3_ERR_INVALID_ARG;
-    if (c->weight_format != EAGLE3_WEIGHTS_DTYPE && c->weight_format != EAGLE3_WEIGHTS_FP8)
+    if (c->weight_format != EAGLE3_WEIGHTS_DTYPE && c->weight_format != EAGLE3_WEIGHTS_FP8 &&
+        c->weight_format != EAGLE3_WEIGHTS_NVFP4)
         return EAGLE3_ERR_INVALID_ARG;
-    if (c->weight_format == EAGLE3_WEIGHTS_FP8) {
-        // the FP8 kernels load 16 codes per lane: every FP8 matrix's K is a multiple of 16
+    if (c->weight_format != EAGLE3_WEIGHTS_DTYPE) {
+        // the FP8 kernels load 16 codes per lane, the NVFP4 kernels 32: every quantized matrix's K is a
+        // multiple of that
+        const int u = c->weight_format == EAGLE3_WEIGHTS_FP8 ? 16 : 32;
         if (c->dtype != EAGLE3_BF16) return EAGLE3_ERR_UNSUPPORTED;
-        if (c->hidden % 16 || c->q_lora_rank % 16 || (c->n_heads * c->v_head_dim) % 16 || c->intermediate % 16)
+        if (c->hidden % u || c->q_lora_rank % u || (c->n_heads * c->v_head_dim) % u || c->intermediate % u)
             return EAGLE3_ERR_UNSUPPORTED;
     }
     // inner (K) dimensions of every linear layer stream in 8-element chunks
@@ -249,20 +252,25 @@ eagle3_status_t check_weights(const eagle3_config_t& c, const eagle3_weights_t* 
                        w->final_norm, w->lm_head};
     for (const void* v : p)
         if (!v || !aligned16(v)) return EAGLE3_ERR_INVALID_ARG;
-    if (c.weight_format == EAGLE3_WEIGHTS_FP8) {
-        const float* s[] = {w->fc_scale, w->q_a_scale, w->kv_a_scale, w->q_b_scale, w->o_scale, w->gate_scale,
-                            w->up_scale, w->down_scale, w->lm_head_scale};
-        for (const float* v : s)
-            if (!v || ((uintptr_t)v & 3u)) return EAGLE3_ERR_INVALID_ARG;
+    if (c.weight_format != EAGLE3_WEIGHTS_DTYPE) {
+        // FP8 row scales are fp32; NVFP4 block scales are read two bytes at a time
+        const uintptr_t align = c.weight_format == EAGLE3_WEIGHTS_FP8 ? 3u : 1u;
+        const void* s[] = {w->fc_scale, w->q_a_scale, w->kv_a_scale, w->q_b_scale, w->o_scale, w->gate_scale,
+                           w->up_scale, w->down_scale, w->lm_head_scale};
+        for (const void* v : s)
+            if (!v || ((uintptr_t)v & align)) return EAGLE3_ERR_INVALID_ARG;
+        if (c.weight_format == EAGLE3_WEIGHTS_NVFP4 && (!w->matrix_scales || ((uintptr_t)w->matrix_scales & 3u)))
+            return EAGLE3_ERR_INVALID_ARG;
     }
     return EAGLE3_OK;
 }
 
-bool fp8_head(const eagle3_config_t& c) { return c.weight_format == EAGLE3_WEIGHTS_FP8; }
-// A projection matrix's row scales when the head stores the matrix as FP8, else null (dtype weights).
-const float* fp8_scale(const eagle3_config_t& c, const float* s) { return fp8_head(c) ? s : nullptr; }
+// The head stores its projection matrices quantized (FP8 or NVFP4).
+bool quant_head(const eagle3_config_t& c) { return c.weight_format != EAGLE3_WEIGHTS_DTYPE; }
+// Index of each quantized matrix in eagle3_weights_t::matrix_scales.
+enum QMat { QM_FC = 0, QM_QA, QM_KVA, QM_QB, QM_O, QM_GATE, QM_UP, QM_DOWN, QM_LM };
 
-// Elements of the largest FP8 matrix pair one tensor-core GEMM reads (q_a | kv_a and gate | up are
+// Elements of the largest quantized matrix pair one tensor-core GEMM reads (q_a | kv_a and gate | up are
 // expanded together).
 size_t fp8_max_matrix(const eagle3_config_t& c) {
     const size_t H = c.hidden, nh = c.n_heads, D = c.kv_lora_rank + c.qk_rope_dim;
@@ -389,7 +397,7 @@ Offsets plan(const eagle3_config_t& c, int num_sms) {
     o.xpe = L.take(slots * c.qk_rope_dim * b2);
     o.kvx = L.take(slots * nh * (c.qk_nope_dim + c.v_head_dim) * b2);
     o.tiles = L.take((size_t)o.tiles_cap * sizeof(int4));
-    o.wdq = L.take(tc && fp8_head(c) && M > kGemvMaxRows ? fp8_max_matrix(c) * b2 : 0);
+    o.wdq = L.take(tc && quant_head(c) && M > kGemvMaxRows ? fp8_max_matrix(c) * b2 : 0);
     o.total = L.off;
     return o;
 }
@@ -461,8 +469,13 @@ struct Lin {
     const void* w0 = nullptr;
     const void* w1 = nullptr;
     int n0rows = 0, n1rows = 0;
-    const float* s0 = nullptr;                 // FP8 heads: per-row scales of w0 / w1 (the codes' format)
-    const float* s1 = nullptr;
+    // quantized weights (set by quant()): the format, the scales of w0 / w1 (FP8 fp32 row scales or
+    // NVFP4 E4M3 block scales) and, for NVFP4, the two matrices' fp32 scales
+    int wq = EAGLE3_WEIGHTS_DTYPE;
+    const void* s0 = nullptr;
+    const void* s1 = nullptr;
+    const float* g0 = nullptr;
+    const float* g1 = nullptr;
     float* y = nullptr; long ldy = 0;          // fp32 output (GEMV path always; tensor path when set)
     bf16_t* ybf = nullptr; long ldybf = 0;     // bf16 output for the next tensor-core GEMM
     const float* resid = nullptr; long ldr = 0;
@@ -497,8 +510,15 @@ cudaError_t run_linear(eagle3_draft& d, const Lin& L, int kind, cudaStream_t st)
         g.nseg_w = (L.epi != EPI_GLU && L.w1) ? 2 : 1;
         g.M = L.M; g.N = L.N; g.K = L.K;
         g.a_type = L.a32_is_bf16 ? BF16 : F32;
-        g.w_type = L.s0 ? FP8 : (d.cfg.dtype == EAGLE3_BF16 ? BF16 : F32);
-        g.wscale[0] = L.s0; g.wscale[1] = L.s1;
+        g.w_type = d.cfg.dtype == EAGLE3_BF16 ? BF16 : F32;
+        if (L.wq == EAGLE3_WEIGHTS_FP8) {
+            g.w_type = FP8;
+            g.wscale[0] = static_cast<const float*>(L.s0); g.wscale[1] = static_cast<const float*>(L.s1);
+        } else if (L.wq == EAGLE3_WEIGHTS_NVFP4) {
+            g.w_type = FP4;
+            g.wscale[0] = L.g0; g.wscale[1] = L.g1;
+            g.wbs[0] = static_cast<const uint8_t*>(L.s0); g.wbs[1] = static_cast<const uint8_t*>(L.s1);
+        }
         g.y = L.y; g.ldy = L.ldy;
         g.resid = L.resid; g.ldr = L.ldr;
         g.pval = d.pval; g.pidx = d.pidx; g.logits = L.logits; g.ldl = L.ldl;
@@ -516,20 +536,24 @@ cudaError_t run_linear(eagle3_draft& d, const Lin& L, int kind, cudaStream_t st)
     const void* w0 = L.w0;
     const void* w1 = L.w1;
     const long r0 = glu ? L.N : L.n0rows, r1 = glu ? L.N : L.n1rows;
-    if (L.s0) {
-        // FP8 weights: expand the codes to bf16 (decode(code) * scale, rounded) in the workspace; the
-        // GEMM then runs as for a bf16 head
+    if (L.wq != EAGLE3_WEIGHTS_DTYPE) {
+        // quantized weights: expand the codes to bf16 (decoded value times its scales, rounded) in the
+        // workspace; the GEMM then runs as for a bf16 head
         if (!d.wdq || (size_t)(r0 + (L.w1 ? r1 : 0)) * L.K > fp8_max_matrix(d.cfg) || (L.w1 && !L.s1))
             return cudaErrorInvalidValue;
-        E3_TRY(traced(d, K_DEQUANT, st, [&] {
-            return launch_dequant_e4m3(static_cast<const uint8_t*>(L.w0), L.s0, r0, L.K, d.wdq, d.num_sms, st);
-        }));
+        auto expand = [&](const void* codes, const void* sc, const float* gs, long rows, bf16_t* out) {
+            return traced(d, K_DEQUANT, st, [&] {
+                if (L.wq == EAGLE3_WEIGHTS_FP8)
+                    return launch_dequant_e4m3(static_cast<const uint8_t*>(codes), static_cast<const float*>(sc),
+                                               rows, L.K, out, d.num_sms, st);
+                return launch_dequant_nvfp4(static_cast<const uint8_t*>(codes), static_cast<const uint8_t*>(sc), gs,
+                                            rows, L.K, out, d.num_sms, st);
+            });
+        };
+        E3_TRY(expand(L.w0, L.s0, L.g0, r0, d.wdq));
         w0 = d.wdq;
         if (L.w1) {
-            E3_TRY(traced(d, K_DEQUANT, st, [&] {
-                return launch_dequant_e4m3(static_cast<const uint8_t*>(L.w1), L.s1, r1, L.K, d.wdq + r0 * L.K,
-                                           d.num_sms, st);
-            }));
+            E3_TRY(expand(L.w1, L.s1, L.g1, r1, d.wdq + r0 * L.K));
             w1 = d.wdq + r0 * L.K;
         }
     }
@@ -559,6 +583,18 @@ cudaError_t run_linear(eagle3_draft& d, const Lin& L, int kind, cudaStream_t st)
     cudaError_t e = traced(d, kind, st, [&] { return launch_tc_gemm(p, bn, splits, st); });
     if (L.epi == EPI_ARGMAX) d.npart = p.npart;
     return e;
+}
+
+// Marks L's weights as the head's quantized matrices m0 (and m1, the second segment or the up matrix) with
+// scales s0 / s1; nothing for a head with dtype weights.
+void quant(const eagle3_draft& d, Lin& L, int m0, const void* s0, int m1 = -1, const void* s1 = nullptr) {
+    if (!quant_head(d.cfg)) return;
+    L.wq = d.cfg.weight_format;
+    L.s0 = s0; L.s1 = s1;
+    if (L.wq == EAGLE3_WEIGHTS_NVFP4) {
+        L.g0 = d.w.matrix_scales + m0;
+        L.g1 = m1 >= 0 ? d.w.matrix_scales + m1 : nullptr;
+    }
 }
 
 Lin lin1(const eagle3_draft& d, int M, const float* a32, const bf16_t* a16, int K, const void* w, int N) {
@@ -639,7 +675,7 @@ cudaError_t run_attention_mla(eagle3_draft& d, eagle3_kv_t* kv, int M, cudaStrea
     {
         Lin L = lin1(d, M, d.x, d.x_bf, 2 * H, w.q_a, dq + D);
         L.w1 = w.kv_a; L.n0rows = dq; L.n1rows = D;
-        L.s0 = fp8_scale(c, w.q_a_scale); L.s1 = fp8_scale(c, w.kv_a_scale);
+        quant(d, L, QM_QA, w.q_a_scale, QM_KVA, w.kv_a_scale);
         L.y = d.cqkv; L.ldy = dq + D;
         E3_TRY(run_linear(d, L, K_QKV_A, st));
     }
@@ -649,7 +685,7 @@ cudaError_t run_attention_mla(eagle3_draft& d, eagle3_kv_t* kv, int M, cudaStrea
     }));
     {
         Lin L = lin1(d, M, d.cq_hat, d.cqh_bf, dq, w.q_b, nh * dqk);
-        L.s0 = fp8_scale(c, w.q_b_scale);
+        quant(d, L, QM_QB, w.q_b_scale);
         // the tensor-core path keeps only the bf16 rows: every consumer (absorb GEMM, rope, attention)
         // reads bf16
         if (tc) { L.ybf = d.q_bf; L.ldybf = (long)nh * dqk; } else { L.y = d.q; L.ldy = (long)nh * dqk; }
@@ -764,7 +800,7 @@ cudaError_t run_layer(eagle3_draft& d, eagle3_kv_t* kv, int M, const float* fuse
     // o_proj + residual
     {
         Lin L = lin1(d, M, d.o, d.o_bf, w_o, w.o, H);
-        L.s0 = fp8_scale(c, w.o_scale);
+        quant(d, L, QM_O, w.o_scale);
         L.epi = EPI_RESID; L.resid = fused; L.ldr = H;
         L.y = d.h1; L.ldy = H;
         E3_TRY(run_linear(d, L, K_O_PROJ, st));
@@ -775,13 +811,13 @@ cudaError_t run_layer(eagle3_draft& d, eagle3_kv_t* kv, int M, const float* fuse
     {
         Lin L = lin1(d, M, d.y, d.y_bf, H, w.gate, I);
         L.epi = EPI_GLU; L.w1 = w.up; L.n1rows = I;
-        L.s0 = fp8_scale(c, w.gate_scale); L.s1 = fp8_scale(c, w.up_scale);
+        quant(d, L, QM_GATE, w.gate_scale, QM_UP, w.up_scale);
         if (tc) { L.ybf = d.m_bf; L.ldybf = I; } else { L.y = d.mlp; L.ldy = I; }
         E3_TRY(run_linear(d, L, K_GATE_UP, st));
     }
     {
         Lin L = lin1(d, M, d.mlp, d.m_bf, I, w.down, H);
-        L.s0 = fp8_scale(c, w.down_scale);
+        quant(d, L, QM_DOWN, w.down_scale);
         L.epi = EPI_RESID; L.resid = d.h1; L.ldr = H;
         L.y = d.h2; L.ldy = H;
         E3_TRY(run_linear(d, L, K_DOWN, st));
@@ -791,7 +827,7 @@ cudaError_t run_layer(eagle3_draft& d, eagle3_kv_t* kv, int M, const float* fuse
 
 cudaError_t run_head(eagle3_draft& d, int batch, float* logits_out, cudaStream_t st) {
     Lin L = lin1(d, batch, d.z, d.z_bf, d.cfg.hidden, d.w.lm_head, d.cfg.draft_vocab);
-    L.s0 = fp8_scale(d.cfg, d.w.lm_head_scale);
+    quant(d, L, QM_LM, d.w.lm_head_scale);
     L.epi = EPI_ARGMAX; L.logits = logits_out; L.ldl = d.cfg.draft_vocab;
     return run_linear(d, L, K_LM_HEAD, st);
 }
@@ -873,7 +909,7 @@ eagle3_status_t eagle3_draft_create(const eagle3_config_t* config, const eagle3_
     d->logits = F(o.logits);
     d->tiles = o.tiles_cap ? reinterpret_cast<int4*>(base + o.tiles) : nullptr;
     d->tiles_cap = o.tiles_cap;
-    d->wdq = fp8_head(d->cfg) && d->tc_ok && o.m_cap > kGemvMaxRows ? Bf(o.wdq) : nullptr;
+    d->wdq = quant_head(d->cfg) && d->tc_ok && o.m_cap > kGemvMaxRows ? Bf(o.wdq) : nullptr;
     std::vector<float> cs, sn;
     yarn_table(d->cfg, cs, sn);
     e = cudaMemcpy(d->rope_cos, cs.data(), cs.size() * sizeof(float), cudaMemcpyHostToDevice);
@@ -919,7 +955,7 @@ eagle3_status_t eagle3_draft_extend(eagle3_draft_t* d, const void* const aux_hid
         }
         L.a32_is_bf16 = ra.dt == BF16;
         L.w0 = d->w.fc; L.n0rows = H;
-        L.s0 = fp8_scale(d->cfg, d->w.fc_scale);
+        quant(*d, L, QM_FC, d->w.fc_scale);
         L.y = d->f; L.ldy = H;
         E3_CUDA(run_linear(*d, L, K_FC, st));
     }
@@ -1031,7 +1067,7 @@ eagle3_status_t eagle3_draft_decode_sampled(eagle3_draft_t* d, int32_t gamma, co
         }));
         {
             Lin L = lin1(*d, B, d->z, d->z_bf, H, d->w.lm_head, Vd);
-            L.s0 = fp8_scale(d->cfg, d->w.lm_head_scale);
+            quant(*d, L, QM_LM, d->w.lm_head_scale);
             L.y = lo; L.ldy = Vd;
             E3_CUDA(run_linear(*d, L, K_LM_HEAD, st));
         }

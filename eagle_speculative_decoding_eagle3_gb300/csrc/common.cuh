@@ -94,8 +94,35 @@ __device__ __forceinline__ void widen(const Raw8<fp8e4>& r, float* v) {
     e4m3x4_to_f32(r.a.x, v); e4m3x4_to_f32(r.a.y, v + 4);
 }
 __device__ __forceinline__ Raw8<fp8e4> zero8(fp8e4*) { return {make_uint2(0, 0)}; }
-// Sixteen E4M3 codes: one 16-byte load, the streaming unit of the FP8 weight kernels.
+// One byte holding two E2M1 codes (OCP FP4: sign, 2 exponent bits with bias 1, 1 mantissa bit): the
+// element at the even index in the low nibble.
+struct fp4x2 { uint8_t v; };
+// Sixteen E4M3 codes, or 32 E2M1 codes: one 16-byte load, the streaming unit of the FP8 / NVFP4 kernels.
 struct Raw16e4 { uint4 a; };
+// Sixteen E2M1 codes (8 bytes) to fp32; every E2M1 value is exact in fp16.
+__device__ __forceinline__ void e2m1x16_to_f32(uint32_t w0, uint32_t w1, float* v) {
+    const uint32_t w[2] = {w0, w1};
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+        uint32_t h[4];
+        asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\tmov.b32 {b0, b1, b2, b3}, %4;\n\t"
+            "cvt.rn.f16x2.e2m1x2 %0, b0;\n\tcvt.rn.f16x2.e2m1x2 %1, b1;\n\t"
+            "cvt.rn.f16x2.e2m1x2 %2, b2;\n\tcvt.rn.f16x2.e2m1x2 %3, b3;\n\t}"
+            : "=r"(h[0]), "=r"(h[1]), "=r"(h[2]), "=r"(h[3]) : "r"(w[i]));
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&h[k]));
+            v[8 * i + 2 * k] = f.x;
+            v[8 * i + 2 * k + 1] = f.y;
+        }
+    }
+}
+// The E4M3 code in the low byte of b, as fp32.
+__device__ __forceinline__ float e4m3_to_f32(uint32_t b) {
+    uint32_t h;
+    asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, lo;\n\t}" : "=r"(h) : "r"(b & 0xFFu));
+    return __half2float(__ushort_as_half((unsigned short)(h & 0xFFFFu)));
+}
 __device__ __forceinline__ void widen(const Raw16e4& r, float* v) {
     e4m3x4_to_f32(r.a.x, v); e4m3x4_to_f32(r.a.y, v + 4); e4m3x4_to_f32(r.a.z, v + 8); e4m3x4_to_f32(r.a.w, v + 12);
 }

@@ -13,6 +13,7 @@ int gemv_argmax_parts(int N, int num_sms) {
 
 cudaError_t launch_gemv(GemvArgs& g, int epi, int num_sms, cudaStream_t st) {
     if (g.w_type == FP8) return launch_gemv_fp8(g, epi, num_sms, st);
+    if (g.w_type == FP4) return launch_gemv_fp4(g, epi, num_sms, st);
     if (g.M <= 0 || g.N <= 0) return cudaSuccess;
     for (int s = g.na; s < 3; ++s) g.ka[s] = 1 << 30;   // unused K segments never match
     if (g.w_type == F32) {

@@ -35,17 +35,30 @@ constexpr int kLoadsInFlight = 16;     // 16-byte weight loads per lane per iter
 
 template <typename T> constexpr bool kIsFp8 = false;
 template <> constexpr bool kIsFp8<fp8e4> = true;
+template <typename T> constexpr bool kIsFp4 = false;
+template <> constexpr bool kIsFp4<fp4x2> = true;
 
-// The unit a lane loads from a weight row: 8 elements (fp32: two 16-byte loads, bf16: one), or 16 E4M3
-// codes (one 16-byte load).  A warp covers kChunk<TW> = 32 units' elements per row and step.
-template <typename TW> struct WUnit { static constexpr int EL = 8; using Raw = Raw8<TW>; };
-template <> struct WUnit<fp8e4> { static constexpr int EL = 16; using Raw = Raw16e4; };
+// The unit a lane loads from a weight row: 8 elements (fp32: two 16-byte loads, bf16: one), 16 E4M3
+// codes or 32 E2M1 codes (one 16-byte load).  A warp covers kChunk<TW> = 32 units' elements per row and
+// step.  PK elements share one TW (two E2M1 codes per byte).
+template <typename TW> struct WUnit {
+    static constexpr int EL = 8, BYTES = 8 * (int)sizeof(TW), PK = 1;
+    using Raw = Raw8<TW>;
+};
+template <> struct WUnit<fp8e4> { static constexpr int EL = 16, BYTES = 16, PK = 1; using Raw = Raw16e4; };
+template <> struct WUnit<fp4x2> { static constexpr int EL = 32, BYTES = 16, PK = 2; using Raw = Raw16e4; };
 template <typename TW> constexpr int kChunk = 32 * WUnit<TW>::EL;
 template <typename TW> __device__ __forceinline__ typename WUnit<TW>::Raw ldw(const TW* p) {
-    if constexpr (kIsFp8<TW>) return Raw16e4{ld_stream16(p)}; else return ld8<true>(p);
+    if constexpr (kIsFp8<TW> || kIsFp4<TW>) return Raw16e4{ld_stream16(p)}; else return ld8<true>(p);
 }
 template <typename TW> __device__ __forceinline__ typename WUnit<TW>::Raw zerow() {
-    if constexpr (kIsFp8<TW>) return Raw16e4{make_uint4(0, 0, 0, 0)}; else return zero8((TW*)nullptr);
+    if constexpr (kIsFp8<TW> || kIsFp4<TW>) return Raw16e4{make_uint4(0, 0, 0, 0)}; else return zero8((TW*)nullptr);
+}
+// The two E4M3 block scales of an NVFP4 unit (32 codes = 2 blocks of 16), as a 16-bit load.
+__device__ __forceinline__ uint32_t ld_scale_pair(const uint8_t* p) {
+    unsigned short v;
+    asm volatile("ld.global.nc.u16 %0, [%1];" : "=h"(v) : "l"(p));
+    return v;
 }
 // EL activations of row `p` (fp32 or bf16) widened to fp32
 template <int EL, typename TA> __device__ __forceinline__ void ld_act(const TA* p, float* v) {
@@ -59,12 +72,18 @@ __device__ __forceinline__ float row_scale(const GemvArgs& g, bool glu, int n, i
     const int seg = (g.nseg_w > 1 && n >= g.nw[0]) ? 1 : 0;
     return __ldg(g.wscale[seg] + (seg ? n - g.nw[0] : n));
 }
+// The NVFP4 matrix scale of output column n's matrix.
+__device__ __forceinline__ float matrix_scale(const GemvArgs& g, bool glu, int n, int q) {
+    const int seg = glu ? q : ((g.nseg_w > 1 && n >= g.nw[0]) ? 1 : 0);
+    return __ldg(g.wscale[seg]);
+}
 
 template <typename TA, typename TW, int MR, int EPI, int R>
 __global__ void __launch_bounds__(kGemvWarps * 32, kGemvCtasPerSm) gemv_kernel(const GemvArgs g, int rows_per_warp) {
     constexpr int NW = (EPI == EPI_GLU) ? 2 : 1;   // weight rows read per output column
-    constexpr int EL = WUnit<TW>::EL, CW = kChunk<TW>;
-    constexpr int U0 = kLoadsInFlight / (R * NW) * 16 / ((int)sizeof(TW) * EL);
+    constexpr int EL = WUnit<TW>::EL, CW = kChunk<TW>, PK = WUnit<TW>::PK;
+    constexpr bool F4 = kIsFp4<TW>;
+    constexpr int U0 = kLoadsInFlight / (R * NW) * 16 / WUnit<TW>::BYTES;
     constexpr int U = U0 < 1 ? 1 : U0;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int m0 = blockIdx.x * MR;
@@ -74,13 +93,19 @@ __global__ void __launch_bounds__(kGemvWarps * 32, kGemvCtasPerSm) gemv_kernel(c
     const int r_end = min(g.N, r_begin + rows_per_warp);
     const int ka0 = g.ka[0], ka01 = g.ka[0] + g.ka[1];
 
+    const long KW = K / PK;                          // TW per weight row
     auto wrow = [&](int n, int q) -> const TW* {
-        if (EPI == EPI_GLU) return reinterpret_cast<const TW*>(g.w[q]) + (long)n * K;
+        if (EPI == EPI_GLU) return reinterpret_cast<const TW*>(g.w[q]) + (long)n * KW;
         if (g.w_grp)
             return reinterpret_cast<const TW*>(g.w[0]) +
-                   ((long)(n / g.w_grp) * g.w_grp_stride + g.w_row0 + n % g.w_grp) * K;
+                   ((long)(n / g.w_grp) * g.w_grp_stride + g.w_row0 + n % g.w_grp) * KW;
         const int seg = (g.nseg_w > 1 && n >= g.nw[0]) ? 1 : 0;
-        return reinterpret_cast<const TW*>(g.w[seg]) + (long)(seg ? n - g.nw[0] : n) * K;
+        return reinterpret_cast<const TW*>(g.w[seg]) + (long)(seg ? n - g.nw[0] : n) * KW;
+    };
+    // NVFP4 block scales of row n: K / 16 bytes
+    auto bsrow = [&](int n, int q) -> const uint8_t* {
+        const int seg = EPI == EPI_GLU ? q : ((g.nseg_w > 1 && n >= g.nw[0]) ? 1 : 0);
+        return g.wbs[seg] + (long)(seg && EPI != EPI_GLU ? n - g.nw[0] : n) * (K / 16);
     };
 
     float best_v[MR];
@@ -94,17 +119,23 @@ __global__ void __launch_bounds__(kGemvWarps * 32, kGemvCtasPerSm) gemv_kernel(c
     for (int p0 = r_begin; p0 < r_end; p0 += R) {
         const int nr = min(R, r_end - p0);
         const TW* wp[R][NW];
+        const uint8_t* bp[R][NW];
 #pragma unroll
         for (int j = 0; j < R; ++j)
 #pragma unroll
-            for (int q = 0; q < NW; ++q) wp[j][q] = wrow(p0 + (j < nr ? j : 0), q);
+            for (int q = 0; q < NW; ++q) {
+                wp[j][q] = wrow(p0 + (j < nr ? j : 0), q);
+                if constexpr (F4) bp[j][q] = bsrow(p0 + (j < nr ? j : 0), q);
+            }
         // the per-head GEMVs use one activation slice per row group; all rows of a pass share it
         const long aoff = g.a_grp ? (long)(p0 / g.a_grp) * g.a_grp_stride : 0;
-        float sc[R][NW];                      // FP8 row scales, loaded with the pass's first weights
+        float sc[R][NW];                      // FP8 row / NVFP4 matrix scales, loaded with the first weights
 #pragma unroll
         for (int j = 0; j < R; ++j)
 #pragma unroll
-            for (int q = 0; q < NW; ++q) sc[j][q] = kIsFp8<TW> ? row_scale(g, EPI == EPI_GLU, p0 + (j < nr ? j : 0), q) : 1.f;
+            for (int q = 0; q < NW; ++q)
+                sc[j][q] = kIsFp8<TW> ? row_scale(g, EPI == EPI_GLU, p0 + (j < nr ? j : 0), q)
+                                      : (F4 ? matrix_scale(g, EPI == EPI_GLU, p0 + (j < nr ? j : 0), q) : 1.f);
         float acc[MR][R][NW];
 #pragma unroll
         for (int i = 0; i < MR; ++i)
@@ -115,14 +146,17 @@ __global__ void __launch_bounds__(kGemvWarps * 32, kGemvCtasPerSm) gemv_kernel(c
 
         for (int k0 = lane * EL; k0 < K; k0 += CW * U) {
             typename WUnit<TW>::Raw wr[U][R][NW];
+            uint32_t bs[U][R][NW];                   // NVFP4: the unit's two block scales
 #pragma unroll
             for (int u = 0; u < U; ++u) {
                 const int k = k0 + u * CW;
 #pragma unroll
                 for (int j = 0; j < R; ++j)
 #pragma unroll
-                    for (int q = 0; q < NW; ++q)
-                        wr[u][j][q] = (k < K && j < nr) ? ldw(wp[j][q] + k) : zerow<TW>();
+                    for (int q = 0; q < NW; ++q) {
+                        wr[u][j][q] = (k < K && j < nr) ? ldw(wp[j][q] + k / PK) : zerow<TW>();
+                        if constexpr (F4) bs[u][j][q] = (k < K && j < nr) ? ld_scale_pair(bp[j][q] + k / 16) : 0u;
+                    }
             }
             if (!waited) { pdl_wait(); waited = true; }
 #pragma unroll
@@ -135,17 +169,38 @@ __global__ void __launch_bounds__(kGemvWarps * 32, kGemvCtasPerSm) gemv_kernel(c
 #pragma unroll
                     for (int i = 0; i < MR; ++i) {
                         if (i < mcount) {
-                            float av[EL];
-                            ld_act<EL>(ap + i * g.lda[s], av);
+                            if constexpr (F4) {
+                                // two blocks of 16: sum code x activation, then times the block's scale
 #pragma unroll
-                            for (int j = 0; j < R; ++j)
+                                for (int h = 0; h < 2; ++h) {
+                                    float av[16];
+                                    ld_act<16>(ap + i * g.lda[s] + 16 * h, av);
 #pragma unroll
-                                for (int q = 0; q < NW; ++q) {
-                                    float wv[EL];
-                                    widen(wr[u][j][q], wv);
+                                    for (int j = 0; j < R; ++j)
 #pragma unroll
-                                    for (int e = 0; e < EL; ++e) acc[i][j][q] = fmaf(wv[e], av[e], acc[i][j][q]);
+                                        for (int q = 0; q < NW; ++q) {
+                                            float wv[16];
+                                            const uint4 w4 = wr[u][j][q].a;
+                                            e2m1x16_to_f32(h ? w4.z : w4.x, h ? w4.w : w4.y, wv);
+                                            float p = 0.f;
+#pragma unroll
+                                            for (int e = 0; e < 16; ++e) p = fmaf(wv[e], av[e], p);
+                                            acc[i][j][q] = fmaf(p, e4m3_to_f32(bs[u][j][q] >> (8 * h)), acc[i][j][q]);
+                                        }
                                 }
+                            } else {
+                                float av[EL];
+                                ld_act<EL>(ap + i * g.lda[s], av);
+#pragma unroll
+                                for (int j = 0; j < R; ++j)
+#pragma unroll
+                                    for (int q = 0; q < NW; ++q) {
+                                        float wv[EL];
+                                        widen(wr[u][j][q], wv);
+#pragma unroll
+                                        for (int e = 0; e < EL; ++e) acc[i][j][q] = fmaf(wv[e], av[e], acc[i][j][q]);
+                                    }
+                            }
                         }
                     }
                 }
@@ -211,7 +266,8 @@ template <typename TA, typename TW, int MR, int EPI, int R>
 __global__ void __launch_bounds__(kGemvWarps * 32, kGemvCtasPerSm) gemv_ks_kernel(const GemvArgs g, int rpc, int KS) {
     constexpr int NW = (EPI == EPI_GLU) ? 2 : 1;
     constexpr int EL = WUnit<TW>::EL, CW = kChunk<TW>;
-    constexpr int U0 = kLoadsInFlight / (R * NW) * 16 / ((int)sizeof(TW) * EL);
+    static_assert(!kIsFp4<TW>, "NVFP4 weights stream through the whole-row kernel");
+    constexpr int U0 = kLoadsInFlight / (R * NW) * 16 / WUnit<TW>::BYTES;
     static_assert(R * MR <= 32, "one epilogue thread per (row group, row, activation row)");
     constexpr int U = U0 < 1 ? 1 : U0;
     constexpr int OUT = MR * R * NW;                 // partial sums per warp and pass
@@ -438,12 +494,14 @@ static cudaError_t launch_mr(GemvArgs& g, int num_sms, cudaStream_t st) {
     const int KS = gemv_ks_slices((g.K + kChunk<TW> - 1) / kChunk<TW>);
     int rpw, ctas, R;
     gemv_split(g.N, num_sms, g.a_grp, &rpw, &ctas, &R);
-    if (sizeof(TW) <= 2 && KS > 1 && rpw <= 4 && !g.w_grp && !g.a_grp) {
-        switch (MR) {
-            case 1: return launch_ks<TA, TW, 1, EPI>(g, KS, num_sms, st);
-            case 2: return launch_ks<TA, TW, 2, EPI>(g, KS, num_sms, st);
-            case 4: return launch_ks<TA, TW, 4, EPI>(g, KS, num_sms, st);
-            default: return launch_ks<TA, TW, 8, EPI>(g, KS, num_sms, st);
+    if constexpr (!kIsFp4<TW>) {
+        if (sizeof(TW) <= 2 && KS > 1 && rpw <= 4 && !g.w_grp && !g.a_grp) {
+            switch (MR) {
+                case 1: return launch_ks<TA, TW, 1, EPI>(g, KS, num_sms, st);
+                case 2: return launch_ks<TA, TW, 2, EPI>(g, KS, num_sms, st);
+                case 4: return launch_ks<TA, TW, 4, EPI>(g, KS, num_sms, st);
+                default: return launch_ks<TA, TW, 8, EPI>(g, KS, num_sms, st);
+            }
         }
     }
     if (EPI == EPI_ARGMAX) g.npart = ctas;

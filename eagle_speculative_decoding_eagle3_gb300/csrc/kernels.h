@@ -8,7 +8,8 @@
 
 namespace e3 {
 
-enum DType { F32 = 0, BF16 = 1, FP8 = 2 };   // FP8: E4M3 codes with per-row fp32 scales (GEMV weights)
+// FP8: E4M3 codes with per-row fp32 scales; FP4: NVFP4 (E2M1 codes, E4M3 scales per 16, fp32 per matrix)
+enum DType { F32 = 0, BF16 = 1, FP8 = 2, FP4 = 3 };
 
 // ---------------------------------------------------------------- weight-streaming GEMM
 // y[m, n] = sum_k A[m, k] * W[n, k] for m < M, n < N, with
@@ -37,11 +38,17 @@ struct GemvArgs {
     int w_grp; long w_grp_stride; int w_row0;
     int a_grp; long a_grp_stride;
     int* err;                         // device error word (bounded waits that ran out)
-    // w_type FP8: per-output-row scales of w[0] / w[1] (y[m, n] = scale[n] * sum_k A[m, k] code[n, k])
+    // w_type FP8: per-output-row scales of w[0] / w[1] (y[m, n] = scale[n] * sum_k A[m, k] code[n, k]);
+    // w_type FP4: each matrix's one fp32 scale, with its E4M3 block scales [rows, K / 16] in wbs
     const float* wscale[2];
+    const uint8_t* wbs[2];
 };
 cudaError_t launch_gemv(GemvArgs& g, int epi, int num_sms, cudaStream_t st);
 cudaError_t launch_gemv_fp8(GemvArgs& g, int epi, int num_sms, cudaStream_t st);   // w_type FP8
+cudaError_t launch_gemv_fp4(GemvArgs& g, int epi, int num_sms, cudaStream_t st);   // w_type FP4
+// bf16 expansion of an NVFP4 matrix (K a multiple of 32)
+cudaError_t launch_dequant_nvfp4(const uint8_t* codes, const uint8_t* block_scales, const float* global, long rows,
+                                 int K, __nv_bfloat16* out, int num_sms, cudaStream_t st);
 // bf16 expansion of an FP8 E4M3 matrix with per-row scales (K a multiple of 8)
 cudaError_t launch_dequant_e4m3(const uint8_t* codes, const float* scales, long rows, int K, __nv_bfloat16* out,
                                 int num_sms, cudaStream_t st);

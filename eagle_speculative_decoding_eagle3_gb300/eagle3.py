@@ -14,7 +14,7 @@ _LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libeagle3.
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_STATE, ERR_OOM, ERR_CUDA, ERR_DEVICE_RANGE, ERR_SCRATCH_LIMIT = range(8)
 NOALLOC_SCRATCH_BYTES = 16 << 20   # EAGLE3_NOALLOC_SCRATCH_BYTES
 F32, BF16 = 0, 1
-WEIGHTS_DTYPE, WEIGHTS_FP8 = 0, 1   # eagle3_weight_format_t
+WEIGHTS_DTYPE, WEIGHTS_FP8, WEIGHTS_NVFP4 = 0, 1, 2   # eagle3_weight_format_t
 ATTN_MLA, ATTN_MHA = 0, 1           # eagle3_attention_t
 DEVERR_TOKEN, DEVERR_POSITION, DEVERR_D2T, DEVERR_PAGE, DEVERR_ROWS = 1, 2, 4, 8, 16
 
@@ -43,7 +43,7 @@ MHA_WEIGHT_NAMES = ("q_proj", "k_proj", "v_proj")
 
 class eagle3_weights_t(C.Structure):
     _fields_ = ([(n, C.c_void_p) for n in WEIGHT_NAMES] + [(n + "_scale", C.c_void_p) for n in FP8_WEIGHT_NAMES]
-                + [(n, C.c_void_p) for n in MHA_WEIGHT_NAMES])
+                + [(n, C.c_void_p) for n in MHA_WEIGHT_NAMES] + [("matrix_scales", C.c_void_p)])
 
 
 class eagle3_kv_t(C.Structure):
@@ -93,6 +93,7 @@ def _lib():
         lib.eagle3_linear.argtypes = [P, P, P, P, C.c_int32, C.c_int32, C.c_int32, P]
         lib.eagle3_linear_noalloc.argtypes = [P, P, P, C.c_int32, C.c_int32, C.c_int32, P]
         lib.eagle3_quantize_e4m3.argtypes = [P, C.c_int32, C.c_int32, C.c_int32, P, P, P]
+        lib.eagle3_quantize_nvfp4.argtypes = [P, C.c_int32, C.c_int32, C.c_int32, P, P, P, P]
         lib.eagle3_draft_get_error.argtypes = [P, C.POINTER(C.c_int32)]
         lib.eagle3_draft_clear_error.argtypes = [P, P]
         lib.eagle3_draft_destroy.argtypes = [P]
@@ -143,13 +144,15 @@ def make_config(**fields) -> eagle3_config_t:
     return c
 
 
-def make_weights(tensors, scales=None) -> eagle3_weights_t:
-    """Weight pointers; `scales` (FP8 heads) maps each of FP8_WEIGHT_NAMES to its row scales."""
+def make_weights(tensors, scales=None, matrix_scales=None) -> eagle3_weights_t:
+    """Weight pointers; `scales` (quantized heads) maps each of FP8_WEIGHT_NAMES to its FP8 row scales or
+    NVFP4 block scales; `matrix_scales` (NVFP4) is the fp32 [9] tensor of the matrices' scales."""
     w = eagle3_weights_t()
     for n in WEIGHT_NAMES + MHA_WEIGHT_NAMES:
         setattr(w, n, _ptr(tensors.get(n)))
     for n in FP8_WEIGHT_NAMES if scales else ():
         setattr(w, n + "_scale", _ptr(scales[n]))
+    w.matrix_scales = _ptr(matrix_scales)
     return w
 
 
@@ -204,6 +207,14 @@ def eagle3_quantize_e4m3(w, dtype, N, K, codes, scales, stream=None):
     """Per-row FP8 E4M3 codes [N, K] (uint8) and fp32 scales [N] of the bf16 / fp32 matrix w [N, K]."""
     _check("eagle3_quantize_e4m3", _lib().eagle3_quantize_e4m3(_ptr(w), int(dtype), int(N), int(K), _ptr(codes),
                                                                _ptr(scales), _stream(stream)))
+
+
+def eagle3_quantize_nvfp4(w, dtype, N, K, codes, block_scales, global_scale, stream=None):
+    """NVFP4 codes [N, K/2] (uint8, two per byte), E4M3 block scales [N, K/16] (uint8) and the fp32 matrix
+    scale [1] of the bf16 / fp32 matrix w [N, K]."""
+    _check("eagle3_quantize_nvfp4", _lib().eagle3_quantize_nvfp4(_ptr(w), int(dtype), int(N), int(K), _ptr(codes),
+                                                                 _ptr(block_scales), _ptr(global_scale),
+                                                                 _stream(stream)))
 
 
 def eagle3_accept(draft, target, batch, gamma, accepted_len, hist=None, stream=None):

@@ -22,7 +22,7 @@ def to_device(arr: np.ndarray, device="cuda") -> torch.Tensor:
     return torch.from_numpy(arr).to(device)
 
 
-def config_for(w, max_batch=None, max_tokens=None, fp8=False) -> E.eagle3_config_t:
+def config_for(w, max_batch=None, max_tokens=None, fp8=False, nvfp4=False) -> E.eagle3_config_t:
     return E.make_config(
         hidden=w.hidden, n_heads=w.n_heads, q_lora_rank=w.q_lora_rank, kv_lora_rank=w.kv_lora_rank,
         qk_nope_dim=w.qk_nope_dim, qk_rope_dim=w.qk_rope_dim, v_head_dim=w.v_head_dim,
@@ -32,7 +32,7 @@ def config_for(w, max_batch=None, max_tokens=None, fp8=False) -> E.eagle3_config
         rms_eps=w.rms_eps, rope_theta=w.rope_theta, yarn_factor=w.yarn_factor, yarn_beta_fast=w.yarn_beta_fast,
         yarn_beta_slow=w.yarn_beta_slow, yarn_mscale=w.yarn_mscale, yarn_mscale_all_dim=w.yarn_mscale_all_dim,
         yarn_original_max_pos=w.yarn_original_max_pos, rope_interleave=1,
-        dtype=E.BF16 if w.dtype == "bf16" else E.F32, weight_format=E.WEIGHTS_FP8 if fp8 else E.WEIGHTS_DTYPE,
+        dtype=E.BF16 if w.dtype == "bf16" else E.F32, weight_format=E.WEIGHTS_NVFP4 if nvfp4 else (E.WEIGHTS_FP8 if fp8 else E.WEIGHTS_DTYPE),
         attention=E.ATTN_MHA if w.attention == "mha" else E.ATTN_MLA, n_kv_heads=w.n_kv_heads,
         head_dim=w.head_dim, fc_inputs=w.fc_inputs)
 
@@ -57,26 +57,43 @@ def quantize_fp8(t: torch.Tensor):
     return codes, scales
 
 
+def quantize_nvfp4(t: torch.Tensor):
+    """Device NVFP4 codes, E4M3 block scales and fp32 matrix scale of a bf16 / fp32 device matrix, by
+    eagle3_quantize_nvfp4."""
+    N, K = t.shape
+    codes = torch.empty((N, K // 2), dtype=torch.uint8, device=t.device)
+    block = torch.empty((N, K // 16), dtype=torch.uint8, device=t.device)
+    g = torch.empty((1,), dtype=torch.float32, device=t.device)
+    E.eagle3_quantize_nvfp4(t, E.BF16 if t.dtype == torch.bfloat16 else E.F32, N, K, codes, block, g)
+    return codes, block, g
+
+
 class DeviceHead:
     """A created draft head whose weights live in device tensors owned by this object.
 
-    fp8=True stores the projection matrices as FP8 E4M3 codes with per-row scales, quantized on the
-    device from the given weights (the bf16 copies of those matrices are released)."""
+    fp8=True (nvfp4=True) stores the projection matrices as FP8 E4M3 codes with per-row scales (NVFP4
+    codes with block and matrix scales), quantized on the device from the given weights (the bf16 copies
+    of those matrices are released)."""
 
-    def __init__(self, w, stored_weights, device="cuda", max_batch=None, max_tokens=None, fp8=False):
+    def __init__(self, w, stored_weights, device="cuda", max_batch=None, max_tokens=None, fp8=False, nvfp4=False):
         self.w = w
         self.device = device
         self.tensors = {}
         self.scales = {}
+        self.matrix_scales = torch.ones(len(E.FP8_WEIGHT_NAMES), dtype=torch.float32, device=device) if nvfp4 else None
         for n in E.WEIGHT_NAMES + E.MHA_WEIGHT_NAMES:
             if n not in stored_weights:
                 continue                       # the other head kind's weights
             t = to_device(stored_weights[n], device)
             if fp8 and n in E.FP8_WEIGHT_NAMES:
                 t, self.scales[n] = quantize_fp8(t)
+            elif nvfp4 and n in E.FP8_WEIGHT_NAMES:
+                t, self.scales[n], g = quantize_nvfp4(t)
+                self.matrix_scales[E.FP8_WEIGHT_NAMES.index(n)] = g[0]
             self.tensors[n] = t
-        self.config = config_for(w, max_batch, max_tokens, fp8)
-        self.handle = E.eagle3_draft_create(self.config, E.make_weights(self.tensors, self.scales or None))
+        self.config = config_for(w, max_batch, max_tokens, fp8, nvfp4)
+        self.handle = E.eagle3_draft_create(self.config, E.make_weights(self.tensors, self.scales or None,
+                                                                        self.matrix_scales))
 
     def close(self):
         if self.handle:

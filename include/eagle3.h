@@ -73,8 +73,15 @@ typedef enum { EAGLE3_F32 = 0, EAGLE3_BF16 = 1 } eagle3_dtype_t;
  *                         The post-training FP8 quantization of the drafter ("EAGLE head deep dive",
  *                         deployment); eagle3_quantize_e4m3 produces this form from bf16 / fp32 weights.
  *                         Requires dtype == EAGLE3_BF16.  kv_b, the embedding and the norm weights keep
- *                         the configured dtype. */
-typedef enum { EAGLE3_WEIGHTS_DTYPE = 0, EAGLE3_WEIGHTS_FP8 = 1 } eagle3_weight_format_t;
+ *                         the configured dtype.
+ *   EAGLE3_WEIGHTS_NVFP4  NVFP4: E2M1 codes (OCP FP4: sign, 2 exponent bits with bias 1, 1 mantissa bit,
+ *                         largest 6), two per byte with the even element in the low nibble, [rows, cols/2];
+ *                         one E4M3 scale per 16 consecutive weights of a row, [rows, cols/16] bytes; one
+ *                         fp32 scale per matrix: weight = decode(code) * decode(block scale) * matrix
+ *                         scale (the drafter's NVFP4 post-training quantization, same page and section;
+ *                         eagle3_quantize_nvfp4 produces this form).  Requires dtype == EAGLE3_BF16, an MLA
+ *                         head, and every quantized matrix's cols a multiple of 32. */
+typedef enum { EAGLE3_WEIGHTS_DTYPE = 0, EAGLE3_WEIGHTS_FP8 = 1, EAGLE3_WEIGHTS_NVFP4 = 2 } eagle3_weight_format_t;
 
 /* Attention of the head's decoder layer.
  *   EAGLE3_ATTN_MLA  the DeepseekV3 draft (Eagle3DeepseekV2ForCausalLM): latent q/kv projections, one
@@ -153,15 +160,19 @@ typedef struct {
     const void *down;           /* [H, I] */
     const void *final_norm;     /* [H] */
     const void *lm_head;        /* [V_d, H] */
-    /* EAGLE3_WEIGHTS_FP8 only (ignored otherwise): the per-output-row fp32 scales of the E4M3
-     * matrices above, one per row of the matrix of the same name. */
-    const float *fc_scale, *q_a_scale, *kv_a_scale, *q_b_scale, *o_scale, *gate_scale, *up_scale,
+    /* Scales of the quantized matrices above (ignored for EAGLE3_WEIGHTS_DTYPE), for the matrix of the
+     * same name: EAGLE3_WEIGHTS_FP8, the fp32 per-output-row scales [rows]; EAGLE3_WEIGHTS_NVFP4, the
+     * E4M3 block scales [rows, cols/16] (bytes). */
+    const void *fc_scale, *q_a_scale, *kv_a_scale, *q_b_scale, *o_scale, *gate_scale, *up_scale,
         *down_scale, *lm_head_scale;
     /* EAGLE3_ATTN_MHA only (its q_a, q_a_norm, q_b, kv_a, kv_a_norm and kv_b are unused and may be NULL;
      * its fc is [H, fc_inputs H] and its o [H, n_heads head_dim]): */
     const void *q_proj;         /* [n_heads head_dim, 2H] */
     const void *k_proj;         /* [n_kv_heads head_dim, 2H] */
     const void *v_proj;         /* [n_kv_heads head_dim, 2H] */
+    /* EAGLE3_WEIGHTS_NVFP4 only: the nine matrix scales, fp32 [9], in the order fc, q_a, kv_a, q_b, o,
+     * gate, up, down, lm_head. */
+    const float *matrix_scales;
 } eagle3_weights_t;
 
 /* The one-layer latent cache (BORROWED).  Slot p of sequence b is row (p % page_size) of page
@@ -360,6 +371,22 @@ EAGLE3_API eagle3_status_t eagle3_accept_residual(const int32_t *draft, const fl
  * another dtype. */
 EAGLE3_API eagle3_status_t eagle3_quantize_e4m3(const void *w, eagle3_dtype_t dtype, int32_t N, int32_t K,
                                                 uint8_t *codes, float *scales, void *stream);
+
+/* NVFP4 quantization of one weight matrix (the drafter's post-training NVFP4 quantization, "EAGLE head
+ * deep dive", deployment; the form EAGLE3_WEIGHTS_NVFP4 reads), all in fp32:
+ *   g = max |w| / 2688 (= 448 * 6; 1 for an all-zero matrix),
+ *   s_b = E4M3(max_{k in block b} |w[n, k]| / (6 g)) for each 16 consecutive weights of a row (6 g rounded
+ *   first; nearest, ties to even, saturating),
+ *   e_b = decode(s_b) * g, code = E2M1(w / e_b) (nearest, ties to the even code, saturating at 6; 0 where
+ *   e_b is 0).
+ *   w             [N, K] of `dtype` (bf16 or fp32), K a multiple of 32
+ *   codes         [N, K/2] uint8 out, two codes per byte, the even element in the low nibble
+ *   block_scales  [N, K/16] uint8 out (E4M3); global_scale [1] fp32 out (g)
+ * Four launches (matrix maximum, codes, scale).  Returns EAGLE3_ERR_INVALID_ARG for null pointers or
+ * sizes < 1, _UNSUPPORTED for K not a multiple of 32 or another dtype. */
+EAGLE3_API eagle3_status_t eagle3_quantize_nvfp4(const void *w, eagle3_dtype_t dtype, int32_t N, int32_t K,
+                                                 uint8_t *codes, uint8_t *block_scales, float *global_scale,
+                                                 void *stream);
 
 /* Read the sticky device error word (synchronises the device).  *device_error (host) receives
  * the EAGLE3_DEVERR_* bits; returns EAGLE3_ERR_DEVICE_RANGE when any bit is set. */

@@ -26,13 +26,15 @@ def row_rel_err(g, o):
 FP8_NAMES = ("fc", "q_a", "kv_a", "q_b", "o", "gate", "up", "down", "lm_head")
 
 
-class Fp8OracleWeights(Mapping):
-    """The oracle's view of an FP8 head: the nine projection matrices replaced by the oracle's own
-    per-row E4M3 quantization of the stored weights (decode(code) * scale, fp64), every other tensor
-    widened as stored.  Quantized in blocks of rows (the rule is per row), once per matrix."""
+class QuantOracleWeights(Mapping):
+    """The oracle's view of a quantized head: the nine projection matrices replaced by the oracle's own
+    quantization of the stored weights (dequantized, fp64), every other tensor widened as stored.  FP8
+    matrices are quantized in blocks of rows (the rule is per row); NVFP4 matrices whole (one scale per
+    matrix); each once."""
 
-    def __init__(self, stored):
+    def __init__(self, stored, fmt):
         self._s = stored
+        self._fmt = fmt
         self._f = WL.F64Cache(stored)
         self._q = {}
 
@@ -41,7 +43,10 @@ class Fp8OracleWeights(Mapping):
             return self._f[k]
         if k not in self._q:
             W = WL.as_f32(self._s[k])
-            self._q[k] = np.concatenate([O.quantize_rows_e4m3(W[r:r + 2048])[2] for r in range(0, len(W), 2048)])
+            if self._fmt == "fp8":
+                self._q[k] = np.concatenate([O.quantize_rows_e4m3(W[r:r + 2048])[2] for r in range(0, len(W), 2048)])
+            else:
+                self._q[k] = O.quantize_nvfp4(W)[3]
         return self._q[k]
 
     def __iter__(self):
@@ -51,19 +56,21 @@ class Fp8OracleWeights(Mapping):
         return len(self._s)
 
 
-def run_round(w, seqs=None, absorbed=False, with_logits=True, stored=None, d2t_override="default", fp8=False):
+def run_round(w, seqs=None, absorbed=False, with_logits=True, stored=None, d2t_override="default", fp8=False,
+              nvfp4=False):
     """GPU round (extend + gamma-1 decode steps + accept) and the oracle's forced-continuation round.
 
     ``seqs``: sequences the oracle checks (all by default); the GPU always runs the whole batch.
-    ``fp8``: the head stores its projection matrices as FP8 E4M3 with row scales (quantized on the GPU by
-    eagle3_quantize_e4m3); the oracle runs on its own quantization of the same weights.
+    ``fp8`` / ``nvfp4``: the head stores its projection matrices as FP8 E4M3 with row scales (NVFP4 with
+    block and matrix scales), quantized on the GPU by eagle3_quantize_e4m3 (eagle3_quantize_nvfp4); the
+    oracle runs on its own quantization of the same weights.
     """
     stored = WL.make_weights(w) if stored is None else stored
     lengths = WL.context_lengths(w)
     paged = WL.make_cache(w, lengths)
     ex = WL.make_extend(w, lengths)
     d2t = WL.make_d2t(w) if d2t_override == "default" else d2t_override
-    head = HN.DeviceHead(w, stored, fp8=fp8)
+    head = HN.DeviceHead(w, stored, fp8=fp8, nvfp4=nvfp4)
     try:
         dc = head.cache(paged)
         din = head.extend_inputs(ex)
@@ -91,7 +98,7 @@ def run_round(w, seqs=None, absorbed=False, with_logits=True, stored=None, d2t_o
         head.close()
 
     seqs = list(range(w.batch)) if seqs is None else list(seqs)
-    W = Fp8OracleWeights(stored) if fp8 else WL.F64Cache(stored)
+    W = QuantOracleWeights(stored, "fp8" if fp8 else "nvfp4") if (fp8 or nvfp4) else WL.F64Cache(stored)
     caches = [O.SeqCache(WL.as_f32(WL.cache_rows(w, b, int(lengths[b]))), w.max_ctx) for b in seqs]
     exs = WL.make_extend(w, lengths, seqs=seqs)
     aux = [WL.as_f32(a) for a in exs.aux]

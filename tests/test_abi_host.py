@@ -92,8 +92,10 @@ def test_accept_relaxed_rejects_bad_arguments(lib):
 def test_fp8_weight_format_checks_without_a_gpu(lib):
     # the format must be known, FP8 needs bf16 storage, and extends above the GEMV rows reserve the
     # bf16 expansion of the largest FP8 matrix pair (gate | up: 2 x 18432 x 7168 elements)
-    for kw in [dict(weight_format=2), dict(weight_format=E.WEIGHTS_FP8, dtype=E.F32),
-               dict(weight_format=E.WEIGHTS_FP8, hidden=7160)]:          # FP8 rows: K a multiple of 16
+    for kw in [dict(weight_format=3), dict(weight_format=E.WEIGHTS_FP8, dtype=E.F32),
+               dict(weight_format=E.WEIGHTS_FP8, hidden=7160),           # FP8 rows: K a multiple of 16
+               dict(weight_format=E.WEIGHTS_NVFP4, intermediate=18448),  # NVFP4 rows: K a multiple of 32
+               dict(weight_format=E.WEIGHTS_NVFP4, dtype=E.F32)]:
         with pytest.raises(E.Eagle3Error) as ei:
             E.eagle3_draft_workspace_bytes(_dsv3_config(**kw))
         assert ei.value.status in (E.ERR_INVALID_ARG, E.ERR_UNSUPPORTED), kw
@@ -115,6 +117,20 @@ def test_fp8_weight_format_checks_without_a_gpu(lib):
     assert lib.eagle3_quantize_e4m3(None, E.BF16, 4, 8, None, None, None) == E.ERR_INVALID_ARG
     assert lib.eagle3_quantize_e4m3(256, E.BF16, 0, 8, 256, 256, None) == E.ERR_INVALID_ARG
     assert lib.eagle3_quantize_e4m3(256, 7, 4, 8, 256, 256, None) == E.ERR_UNSUPPORTED
+    # NVFP4: valid for the DeepseekV3 head's sizes; the quantizer wants K a multiple of 32
+    assert E.eagle3_draft_workspace_bytes(_dsv3_config(weight_format=E.WEIGHTS_NVFP4, intermediate=18432)) > 0
+    assert E.eagle3_draft_workspace_bytes(_dsv3_config(weight_format=E.WEIGHTS_FP8, intermediate=18448)) > 0
+    assert lib.eagle3_quantize_nvfp4(None, E.BF16, 4, 32, None, None, None, None) == E.ERR_INVALID_ARG
+    assert lib.eagle3_quantize_nvfp4(256, E.BF16, 4, 48, 256, 256, 256, None) == E.ERR_UNSUPPORTED
+    assert lib.eagle3_quantize_nvfp4(256, 7, 4, 64, 256, 256, 256, None) == E.ERR_UNSUPPORTED
+    # an NVFP4 head needs its matrix scales as well as the block scales
+    cfg = _dsv3_config(weight_format=E.WEIGHTS_NVFP4)
+    w = E.eagle3_weights_t()
+    for n in E.WEIGHT_NAMES:
+        setattr(w, n, 256)
+    for n in E.FP8_WEIGHT_NAMES:
+        setattr(w, n + "_scale", 256)
+    assert lib.eagle3_draft_create(C.byref(cfg), C.byref(w), C.byref(h)) == E.ERR_INVALID_ARG
 
 
 def _mha_config(**kw):

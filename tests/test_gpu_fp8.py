@@ -84,3 +84,66 @@ def test_fp8_dsv3_b1_full_size_round():
     w = WL.workload("dsv3_b1")
     gpu, orc, seqs, paged = run_round(w, fp8=True)
     print(check_round(w, gpu, orc, seqs, paged, TOL_BF16))
+
+
+# ---------------------------------------------------------------- NVFP4
+def _quantize_nvfp4_on_gpu(W, dtype):
+    from eagle_speculative_decoding_eagle3_gb300 import eagle3 as E
+    from eagle_speculative_decoding_eagle3_gb300 import harness as HN
+    t = HN.to_device(WL.f32_to_bf16_bits(W) if dtype == "bf16" else W.astype(np.float32))
+    N, K = W.shape
+    codes = torch.full((N, K // 2), 0xAB, dtype=torch.uint8, device="cuda")
+    block = torch.full((N, K // 16), 0xCD, dtype=torch.uint8, device="cuda")
+    g = torch.full((1,), -1.0, dtype=torch.float32, device="cuda")
+    E.eagle3_quantize_nvfp4(t, E.BF16 if dtype == "bf16" else E.F32, N, K, codes, block, g)
+    torch.cuda.synchronize()
+    c = codes.cpu().numpy()
+    unpacked = np.empty((N, K), dtype=np.uint8)
+    unpacked[:, 0::2] = c & 0xF                      # the even element in the low nibble
+    unpacked[:, 1::2] = c >> 4
+    return unpacked, block.cpu().numpy(), g.cpu().numpy()
+
+
+@pytest.mark.parametrize("N,K,dtype", [(5, 64, "f32"), (37, 7168, "bf16"), (300, 2048, "bf16"), (64, 18432, "bf16")])
+def test_quantize_nvfp4_bit_exact(N, K, dtype):
+    W = WL.normal((N, K), 0.02, 12, f"fp4.q.{N}.{K}").astype(np.float32)
+    if dtype == "bf16":
+        W = WL.bf16_to_f32(WL.f32_to_bf16_bits(W))
+    W[min(2, N - 1), 16:32] = 0.0                              # an all-zero block
+    W[0, :16] = np.float32(2.0 ** -40)                         # a block whose E4M3 scale underflows to 0
+    if N >= 5:
+        # matrix maximum 2688 makes g = 1; a block with maximum 6 then has scale code E4M3(1) and e_b = 1,
+        # so its values are the exact E2M1 midpoints 0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5 (both signs),
+        # which must round to the even code
+        W[3, 0] = np.float32(2688.0)
+        W[4, 32:48] = np.array([6, 0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5, -0.25, -0.75, -1.25, -1.75, -2.5, -3.5, -5, 0],
+                               dtype=np.float32)
+    codes, block, g = _quantize_nvfp4_on_gpu(W, dtype)
+    ref_codes, ref_block, ref_g, _ = O.quantize_nvfp4(W)
+    assert np.float32(g[0]).view(np.uint32) == np.float32(ref_g).view(np.uint32)
+    np.testing.assert_array_equal(block, ref_block)
+    np.testing.assert_array_equal(codes, ref_codes)
+
+
+def test_nvfp4_round_gemv_and_tensor_core_extend():
+    w = _narrow(batch=3, ctx=(100, 700), t_new=3, gamma=4, accept_p=(0.7,) * 4, seed=86)
+    gpu, orc, seqs, paged = run_round(w, nvfp4=True)
+    print(check_round(w, gpu, orc, seqs, paged, TOL_BF16))
+
+
+def test_nvfp4_round_all_gemv():
+    w = _narrow(batch=2, ctx=(40, 300), t_new=3, gamma=3, accept_p=(0.7,) * 3, seed=87)
+    gpu, orc, seqs, paged = run_round(w, nvfp4=True)
+    print(check_round(w, gpu, orc, seqs, paged, TOL_BF16))
+
+
+def test_nvfp4_round_tensor_core_decode():
+    w = _narrow(batch=24, ctx=(30, 700), t_new=2, gamma=3, accept_p=(0.7,) * 3, seed=88)
+    gpu, orc, seqs, paged = run_round(w, seqs=[0, 11, 23], nvfp4=True)
+    print(check_round(w, gpu, orc, seqs, paged, TOL_BF16))
+
+
+def test_nvfp4_dsv3_b1_full_size_round():
+    w = WL.workload("dsv3_b1")
+    gpu, orc, seqs, paged = run_round(w, nvfp4=True)
+    print(check_round(w, gpu, orc, seqs, paged, TOL_BF16))
