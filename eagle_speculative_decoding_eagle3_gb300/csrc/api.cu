@@ -736,12 +736,14 @@ cudaError_t run_attention_mla(eagle3_draft& d, eagle3_kv_t* kv, int M, cudaStrea
 }
 
 // Split plan of the MHA attention: 128-slot chunks (one 32-slot tile per warp), doubled while the
-// (row, key/value head, split) CTAs exceed about 8 per SM or the rows' splits exceed the partials.
+// (row, key/value head, split) CTAs exceed about 8 per SM, the rows' splits exceed the partials, or a
+// row has more splits than the merge stages (1024).
 void mha_plan(const eagle3_draft& d, int M, int* splits, int* chunk) {
     const int ctx = d.cfg.max_ctx;
     auto ns = [&](int ch) { return (ctx + ch - 1) / ch; };
     int ch = 128;
-    while (ns(ch) > 1 && ((long)M * d.cfg.n_kv_heads * ns(ch) > 8L * d.num_sms || (size_t)M * ns(ch) > d.part_rows))
+    while (ns(ch) > 1 && ((long)M * d.cfg.n_kv_heads * ns(ch) > 8L * d.num_sms || (size_t)M * ns(ch) > d.part_rows ||
+                          ns(ch) > 1024))
         ch *= 2;
     *chunk = ch;
     *splits = ns(ch);

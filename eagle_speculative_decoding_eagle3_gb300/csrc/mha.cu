@@ -21,39 +21,48 @@ namespace e3 {
 
 constexpr int kMhaThreads = 128;          // 4 warps; each takes 32-slot tiles of the chunk in turn
 constexpr int kMhaWarps = kMhaThreads / 32;
+constexpr int kMhaAppendThreads = 256;
+constexpr int kMhaMaxSplits = 1024;       // split statistics a merge CTA stages in shared memory
 
+// Grid (rows, chunks of 256 work items): item i < (n_h + n_kv) d/2 rotates one (i, i + d/2) pair of q (in
+// place) or of k (into the cache); item i < n_kv d also copies one v element.  One item per thread, so no
+// thread waits on a chain of loads.
 template <typename T>
-__global__ void __launch_bounds__(256) mha_rope_append_kernel(const MhaArgs a) {
+__global__ void __launch_bounds__(kMhaAppendThreads) mha_rope_append_kernel(const MhaArgs a) {
     pdl_trigger();
     pdl_wait();
     const int r = blockIdx.x;
     const int nh = a.nh, nkv = a.nkv, d = a.d, half = d / 2;
+    const int i = blockIdx.y * kMhaAppendThreads + threadIdx.x;
     const int b = a.row_seq[r], pos = a.row_pos[r];
     const float* cs = a.rope_cos + (long)pos * half;
     const float* sn = a.rope_sin + (long)pos * half;
-    float* q = a.q + (long)r * nh * d;
-    for (int i = threadIdx.x; i < nh * half; i += blockDim.x) {
+    if (i < nh * half) {
+        float* q = a.q + (long)r * nh * d;
         const int h = i / half, j = i % half;
         const float x0 = q[h * d + j], x1 = q[h * d + j + half];
         q[h * d + j] = x0 * cs[j] - x1 * sn[j];
         q[h * d + j + half] = x0 * sn[j] + x1 * cs[j];
     }
+    const bool krot = i >= nh * half && i < (nh + nkv) * half;
+    const bool vcopy = i < nkv * d;
+    if (!krot && !vcopy) return;
     const int pi = pos / a.page_size;
     int page = -1;
     if (pi < a.max_pages) page = a.block_table[(long)b * a.max_pages + pi];
     if (page < 0 || page >= a.num_pages) {
-        if (threadIdx.x == 0) set_err(a.err, EAGLE3_DEVERR_PAGE);
+        if (threadIdx.x == 0 && blockIdx.y == 0) set_err(a.err, EAGLE3_DEVERR_PAGE);
         return;
     }
     const float* kv = a.kv + (long)r * 2 * nkv * d;
     T* dst = static_cast<T*>(a.cache) + ((long)page * a.page_size + pos % a.page_size) * (2L * nkv * d);
-    for (int i = threadIdx.x; i < nkv * half; i += blockDim.x) {
-        const int h = i / half, j = i % half;
+    if (krot) {
+        const int ik = i - nh * half, h = ik / half, j = ik % half;
         const float x0 = kv[h * d + j], x1 = kv[h * d + j + half];
         dst[h * d + j] = from_f<T>(x0 * cs[j] - x1 * sn[j]);
         dst[h * d + j + half] = from_f<T>(x0 * sn[j] + x1 * cs[j]);
     }
-    for (int i = threadIdx.x; i < nkv * d; i += blockDim.x) dst[nkv * d + i] = from_f<T>(kv[nkv * d + i]);
+    if (vcopy) dst[nkv * d + i] = from_f<T>(kv[nkv * d + i]);
 }
 
 // One CTA: row r, key/value head g, slots [s chunk, min((s + 1) chunk, pos + 1)).  Scores: each lane
@@ -200,21 +209,32 @@ __global__ void __launch_bounds__(kMhaThreads) mha_attention_kernel(const MhaArg
 }
 
 // One CTA per (row, head), one thread per output dimension: o = sum_s e^(m_s - M) o_s / sum_s e^(m_s - M) l_s
-// over the splits that hold any of the row's slots.
+// over the splits that hold any of the row's slots.  The splits' (m, l) are staged in shared memory first,
+// so the loop over o_s issues independent loads.
 __global__ void __launch_bounds__(256) mha_merge_kernel(const MhaArgs a) {
+    __shared__ float sm[kMhaMaxSplits], sl[kMhaMaxSplits];
+    __shared__ float red[8];
     pdl_trigger();
     pdl_wait();
     const int r = blockIdx.x, h = blockIdx.y, e = threadIdx.x;
     const int pos = a.row_pos[r];
-    const int nvalid = min(a.splits, (pos + a.chunk) / a.chunk);
+    const int nvalid = min(min(a.splits, kMhaMaxSplits), (pos + a.chunk) / a.chunk);
     const long pr0 = (long)r * a.splits;
-    float M = -INFINITY;
-    for (int s = 0; s < nvalid; ++s) M = fmaxf(M, a.part_ml[((pr0 + s) * a.nh + h) * 2]);
+    float mx = -INFINITY;
+    for (int s = e; s < nvalid; s += blockDim.x) {
+        sm[s] = a.part_ml[((pr0 + s) * a.nh + h) * 2];
+        sl[s] = a.part_ml[((pr0 + s) * a.nh + h) * 2 + 1];
+        mx = fmaxf(mx, sm[s]);
+    }
+    mx = warp_max(mx);
+    if ((e & 31) == 0) red[e >> 5] = mx;
+    __syncthreads();
+    float M = red[0];
+    for (int w = 1; w < (int)(blockDim.x + 31) / 32; ++w) M = fmaxf(M, red[w]);
     float L = 0.f, acc = 0.f;
     for (int s = 0; s < nvalid; ++s) {
-        const float ms = a.part_ml[((pr0 + s) * a.nh + h) * 2];
-        const float f = ms == -INFINITY ? 0.f : __expf(ms - M);
-        L += f * a.part_ml[((pr0 + s) * a.nh + h) * 2 + 1];
+        const float f = sm[s] == -INFINITY ? 0.f : __expf(sm[s] - M);
+        L += f * sl[s];
         if (e < a.d) acc += f * a.part_o[((pr0 + s) * a.nh + h) * a.d + e];
     }
     if (e < a.d) {
@@ -232,8 +252,10 @@ bool mha_supported(int nh, int nkv, int d) {
 }
 
 cudaError_t launch_mha_rope_append(const MhaArgs& a, cudaStream_t st) {
-    if (a.dt == BF16) return launch_pdl(mha_rope_append_kernel<bf16>, dim3(a.M), dim3(256), 0, st, a);
-    return launch_pdl(mha_rope_append_kernel<float>, dim3(a.M), dim3(256), 0, st, a);
+    const int items = (a.nh + a.nkv) * (a.d / 2) > a.nkv * a.d ? (a.nh + a.nkv) * (a.d / 2) : a.nkv * a.d;
+    const dim3 grid(a.M, (items + kMhaAppendThreads - 1) / kMhaAppendThreads);
+    if (a.dt == BF16) return launch_pdl(mha_rope_append_kernel<bf16>, grid, dim3(kMhaAppendThreads), 0, st, a);
+    return launch_pdl(mha_rope_append_kernel<float>, grid, dim3(kMhaAppendThreads), 0, st, a);
 }
 
 template <typename T, int D>
@@ -265,6 +287,7 @@ cudaError_t launch_mha_attention(const MhaArgs& a, cudaStream_t st) {
 }
 
 cudaError_t launch_mha_merge(const MhaArgs& a, cudaStream_t st) {
+    if (a.splits > kMhaMaxSplits) return cudaErrorInvalidValue;
     const int threads = (a.d + 31) / 32 * 32;
     return launch_pdl(mha_merge_kernel, dim3(a.M, a.nh), dim3(threads), 0, st, a);
 }
