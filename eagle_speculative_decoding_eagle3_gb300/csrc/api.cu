@@ -272,7 +272,7 @@ enum QMat { QM_FC = 0, QM_QA, QM_KVA, QM_QB, QM_O, QM_GATE, QM_UP, QM_DOWN, QM_L
 
 // Elements of the largest quantized matrix pair one tensor-core GEMM reads (q_a | kv_a and gate | up are
 // expanded together).
-size_t fp8_max_matrix(const eagle3_config_t& c) {
+size_t quant_max_matrix(const eagle3_config_t& c) {
     const size_t H = c.hidden, nh = c.n_heads, D = c.kv_lora_rank + c.qk_rope_dim;
     const size_t m[] = {H * 3 * H, (c.q_lora_rank + D) * 2 * H, nh * (c.qk_nope_dim + c.qk_rope_dim) * c.q_lora_rank,
                         H * nh * c.v_head_dim, 2 * (size_t)c.intermediate * H, H * c.intermediate,
@@ -397,7 +397,7 @@ Offsets plan(const eagle3_config_t& c, int num_sms) {
     o.xpe = L.take(slots * c.qk_rope_dim * b2);
     o.kvx = L.take(slots * nh * (c.qk_nope_dim + c.v_head_dim) * b2);
     o.tiles = L.take((size_t)o.tiles_cap * sizeof(int4));
-    o.wdq = L.take(tc && quant_head(c) && M > kGemvMaxRows ? fp8_max_matrix(c) * b2 : 0);
+    o.wdq = L.take(tc && quant_head(c) && M > kGemvMaxRows ? quant_max_matrix(c) * b2 : 0);
     o.total = L.off;
     return o;
 }
@@ -539,7 +539,7 @@ cudaError_t run_linear(eagle3_draft& d, const Lin& L, int kind, cudaStream_t st)
     if (L.wq != EAGLE3_WEIGHTS_DTYPE) {
         // quantized weights: expand the codes to bf16 (decoded value times its scales, rounded) in the
         // workspace; the GEMM then runs as for a bf16 head
-        if (!d.wdq || (size_t)(r0 + (L.w1 ? r1 : 0)) * L.K > fp8_max_matrix(d.cfg) || (L.w1 && !L.s1))
+        if (!d.wdq || (size_t)(r0 + (L.w1 ? r1 : 0)) * L.K > quant_max_matrix(d.cfg) || (L.w1 && !L.s1))
             return cudaErrorInvalidValue;
         auto expand = [&](const void* codes, const void* sc, const float* gs, long rows, bf16_t* out) {
             return traced(d, K_DEQUANT, st, [&] {
