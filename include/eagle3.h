@@ -55,7 +55,7 @@ extern "C" {
 typedef enum {
     EAGLE3_OK = 0,
     EAGLE3_ERR_INVALID_ARG = 1,   /* null pointer, size out of the configured bounds, misalignment */
-    EAGLE3_ERR_UNSUPPORTED = 2,   /* a shape or dtype this build does not implement */
+    EAGLE3_ERR_UNSUPPORTED = 2,   /* a shape or dtype the library does not implement */
     EAGLE3_ERR_STATE = 3,         /* decode before any extend, or batch mismatch */
     EAGLE3_ERR_OOM = 4,           /* workspace allocation failed at create */
     EAGLE3_ERR_CUDA = 5,          /* a CUDA runtime call failed (see eagle3_last_cuda_error) */
