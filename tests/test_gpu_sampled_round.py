@@ -101,3 +101,9 @@ def test_mla_shaped_bf16_sampled_round():
     w = WL.workload("dsv3_b1", hidden=1024, n_heads=8, q_lora_rank=256, intermediate=2048, target_vocab=8192,
                     draft_vocab=4096, batch=3, ctx=(100, 700), t_new=2, gamma=4, accept_p=(0.7,) * 4, seed=83)
     _sampled_round(w, 0.7, 20, 0.8, 33, TOL_BF16)
+
+
+def test_mha_tiny_f32_sampled_round():
+    # the MHA head through the same sampled decode and residual acceptance
+    w = WL.workload("mha_tiny_f32", gamma=4, accept_p=(0.7,) * 4)
+    _sampled_round(w, 0.8, 50, 0.9, 34, TOL_F32)
