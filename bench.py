@@ -633,7 +633,8 @@ def oracle_sample(w, stored, lengths, seconds_budget=30.0, decode_only=False, se
         rng = np.random.default_rng(seq)
         h = rng.standard_normal((1, w.hidden))
         O.draft_decode_step(hy, W, h, np.array([7]), cache, absorbed=True)
-        return 1, time.perf_counter() - t0, f"one fp64 decode step of sequence {seq} (absorbed attention form)"
+        form = "grouped-query attention" if w.attention == "mha" else "absorbed attention form"
+        return 1, time.perf_counter() - t0, f"one fp64 decode step of sequence {seq} ({form})"
     toks = 0
     aux = [WL.as_f32(a) for a in ex.aux]
     out = O.draft_extend(hy, W, aux, ex.tokens, ex.positions, ex.row_offsets, cache, absorbed=True)
