@@ -16,10 +16,13 @@
 //    for them).
 // Two kernels share this layout: gemv_kernel gives each warp whole rows; gemv_ks_kernel splits every row
 // across the warps of a row group, for layers whose rows are long and few per warp.
-// Weights are fp32, bf16 or FP8 E4M3 codes with one fp32 scale per output row (the draft head's FP8
-// post-training quantization, "EAGLE head deep dive", deployment): the FP8 kernels widen the codes
-// exactly to fp32, accumulate code * activation and multiply each output column's sum by its row scale.
-// The templates live in this header; gemv.cu instantiates the fp32 / bf16 weights, gemv_fp8.cu the FP8.
+// Weights are fp32, bf16, FP8 E4M3 codes with one fp32 scale per output row, or NVFP4 (E2M1 codes, an
+// E4M3 scale per 16 weights, an fp32 scale per matrix): the drafter's FP8 / NVFP4 post-training
+// quantization, "EAGLE head deep dive", deployment.  The FP8 kernels widen the codes exactly to fp32,
+// accumulate code * activation and multiply each output column's sum by its row scale; the NVFP4 path
+// (whole-row kernel only) sums each block of 16 products, multiplies it by the block's scale, and the
+// output by the matrix scale.  The templates live in this header; gemv.cu instantiates the fp32 / bf16
+// weights, gemv_fp8.cu the FP8 and gemv_fp4.cu the NVFP4 ones.
 #pragma once
 #include <float.h>
 #include <limits.h>
