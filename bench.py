@@ -715,6 +715,9 @@ def main(argv=None):
     line, w, stored, lengths, paged, d2t = run_ours(args, ws, rank, local)
     if rank == 0 and not args.no_cpu_baseline:
         toks, secs, desc = oracle_sample(w, stored, lengths)
+        if args.weights != "bf16":
+            # the quantized formats change the weight values the oracle multiplies, not its arithmetic
+            desc += f", on the unquantized weights (the {args.weights} head's oracle costs the same)"
         line["cpu_baseline"] = {"value": round(toks / secs, 4), "unit": UNIT, "cores": host_cores(),
                                 "kind": "oracle", "sample": desc}
     if rank == 0:
