@@ -345,6 +345,8 @@ accept_kernel(const int* draft, const int* target, int batch, int gamma, int* ac
 // relaxed_delta; §8: the per-row in_thinking_phase flag).  Position i of a thinking row accepts a draft
 // token listed among the target's k candidates with log-probability >= the best candidate's - delta;
 // other rows accept only the best candidate (the first listed among equal best).  One thread per row.
+// The threshold is formed in fp64 from the single-precision inputs, so the comparison is the exact
+// real-number one and not subject to a single-precision rounding of best - delta.
 __global__ void __launch_bounds__(kRowThreads)
 accept_relaxed_kernel(const int* draft, const int* ids, const float* lp, const unsigned char* think, int batch,
                       int gamma, int k, float delta, int* acc, int* hist) {
@@ -369,8 +371,9 @@ accept_relaxed_kernel(const int* draft, const int* ids, const float* lp, const u
             if (!relaxed) {
                 ok = tok == ci[first];
             } else {
+                const double thr = (double)best - (double)delta;
                 ok = false;
-                for (int j = 0; j < k; ++j) ok = ok || (ci[j] == tok && cl[j] >= best - delta);
+                for (int j = 0; j < k; ++j) ok = ok || (ci[j] == tok && (double)cl[j] >= thr);
             }
             if (!ok) break;
         }

@@ -5,11 +5,13 @@
 // that feeds the sampler.  Here the uniform random numbers are inputs, so a caller (or a test) draws
 // them once and every consumer uses the same ones.
 //
-// sample_kernel: one CTA of kThreads per row.  x = logits * (1 / temperature) in fp32; top_k keeps the
-// top_k largest x (lower indices first among equal values) found by a radix select on the order-
-// preserving integer image of x; the kept tokens are sorted (x descending, index ascending) by a bitonic
-// sort in shared memory; top_p keeps the shortest prefix whose softmax mass reaches top_p of the kept
-// mass; the kept weights are renormalised and u picks the token by inverse CDF in ascending index order.
+// sample_kernel: one CTA of kThreads per row.  x = logits / temperature; since the temperature is
+// positive, x is ordered exactly as the logits are, so top_k keeps the top_k largest logits (lower
+// indices first among equal values), found by a radix select on the order-preserving integer image of
+// the logits; the kept tokens are sorted (logit descending, index ascending) by a bitonic sort in shared
+// memory; their softmax weights are exp((l - l_max) / temperature) in fp32; top_p keeps the shortest
+// prefix whose mass reaches top_p of the kept mass; the kept weights are renormalised and u picks the
+// token by inverse CDF in ascending index order.
 // temperature 0 is the greedy argmax.  Without top_k the whole vocabulary is kept (top_p must be 1) and
 // the inverse CDF runs over it with a block-wide scan.
 //
@@ -114,7 +116,7 @@ __global__ void __launch_bounds__(smp::kThreads) sample_kernel(SampleArgs s) {
     __shared__ int itot[32];
     __shared__ int sh_int[4];
     __shared__ float sh_f[2];
-    extern __shared__ uint32_t keycache[];             // [V] keys of x = logits * (1 / T) when V fits
+    extern __shared__ uint32_t keycache[];             // [V] keys of the logits when V fits
     const int r = blockIdx.x, t = threadIdx.x, V = s.V;
     const float* l = s.logits + (long)r * s.ldl;
     float* probs = s.probs ? s.probs + (long)r * s.ldp : nullptr;
@@ -149,10 +151,10 @@ __global__ void __launch_bounds__(smp::kThreads) sample_kernel(SampleArgs s) {
             for (int i = t; i < s.probs_len; i += kThreads) probs[i] = i == o ? 1.f : 0.f;
         }
     } else if (s.top_k <= 0) {
-        // whole vocabulary: softmax and inverse CDF in index order
-        const float T = 1.f / s.temperature;   // x = logits * (1 / temperature), both rounded to fp32
+        // whole vocabulary: softmax of x = l / T and inverse CDF in index order
+        const float T = s.temperature;
         float m = -INFINITY;
-        for (int i = t; i < V; i += kThreads) m = fmaxf(m, l[i] * T);
+        for (int i = t; i < V; i += kThreads) m = fmaxf(m, l[i]);
         m = warp_max(m);
         if ((t & 31) == 0) wv[t >> 5] = m;
         __syncthreads();
@@ -166,7 +168,7 @@ __global__ void __launch_bounds__(smp::kThreads) sample_kernel(SampleArgs s) {
         // contiguous segment per thread, so the block scan follows the index order
         const int seg = (V + kThreads - 1) / kThreads, i0 = t * seg, i1 = min(V, i0 + seg);
         float part = 0.f;
-        for (int i = i0; i < i1; ++i) part += __expf(l[i] * T - m);
+        for (int i = i0; i < i1; ++i) part += __expf((l[i] - m) / T);
         const float incl = block_inclusive_scan(part, ftot);
         const float total = ftot[kThreads / 32 - 1];
         const float target = u * total;
@@ -174,7 +176,7 @@ __global__ void __launch_bounds__(smp::kThreads) sample_kernel(SampleArgs s) {
         int found = -1;
         if (cum <= target && target < incl) {
             for (int i = i0; i < i1; ++i) {
-                cum += __expf(l[i] * T - m);
+                cum += __expf((l[i] - m) / T);
                 if (target < cum) { found = i; break; }
             }
             if (found < 0) found = i1 - 1;
@@ -184,7 +186,7 @@ __global__ void __launch_bounds__(smp::kThreads) sample_kernel(SampleArgs s) {
         if (found >= 0) sh_int[0] = found;
         __syncthreads();
         token = sh_int[0];
-        qtok = __expf(l[token] * T - m) / total;
+        qtok = __expf((l[token] - m) / T) / total;
         if (probs) {
             if (s.probs_target && s.d2t) {
                 for (int i = t; i < s.probs_len; i += kThreads) probs[i] = 0.f;
@@ -192,18 +194,18 @@ __global__ void __launch_bounds__(smp::kThreads) sample_kernel(SampleArgs s) {
             }
             for (int i = t; i < V; i += kThreads) {
                 const int o = s.probs_target && s.d2t ? i + s.d2t[i] : i;
-                if (o >= 0 && o < s.probs_len) probs[o] = __expf(l[i] * T - m) / total;
+                if (o >= 0 && o < s.probs_len) probs[o] = __expf((l[i] - m) / T) / total;
             }
         }
     } else {
-        const float T = 1.f / s.temperature;   // x = logits * (1 / temperature), both rounded to fp32
+        const float T = s.temperature;
         const int K = min(s.top_k, min(kMaxTopK, V));
         const bool cached = V <= kKeyCache;
         if (cached) {
-            for (int i = t; i < V; i += kThreads) keycache[i] = fkey(l[i] * T);
+            for (int i = t; i < V; i += kThreads) keycache[i] = fkey(l[i]);
             __syncthreads();
         }
-        auto key_of = [&](int i) { return cached ? keycache[i] : fkey(l[i] * T); };
+        auto key_of = [&](int i) { return cached ? keycache[i] : fkey(l[i]); };
         // radix select of the K-th largest key, 8 bits at a time from the top
         uint32_t prefix = 0, pmask = 0;
         int need = K;
@@ -300,14 +302,14 @@ __global__ void __launch_bounds__(smp::kThreads) sample_kernel(SampleArgs s) {
             __syncthreads();
         }
         const int n = K;
-        // (x descending, index ascending) == (~key ascending, index ascending)
+        // (logit descending, index ascending) == (~key ascending, index ascending)
         int np2 = 2;
         while (np2 < n) np2 <<= 1;
         bitonic_sort(sorted, np2);
         const bool live = t < n;
         const int idx = live ? (int)(sorted[t] & 0xffffffffu) : 0;
-        const float x0 = l[(int)(sorted[0] & 0xffffffffu)] * T;
-        const float w = live ? __expf(l[idx] * T - x0) : 0.f;
+        const float l0 = l[(int)(sorted[0] & 0xffffffffu)];
+        const float w = live ? __expf((l[idx] - l0) / T) : 0.f;
         const float cum = block_inclusive_scan(w, ftot);
         const float total = ftot[kThreads / 32 - 1];
         // top-p: the shortest prefix whose mass reaches top_p of the total

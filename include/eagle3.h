@@ -281,7 +281,7 @@ EAGLE3_API eagle3_status_t eagle3_accept(const int32_t *draft, const int32_t *ta
  * in_thinking_phase flag).  For each position i of sequence b the target supplies its k candidate
  * tokens and their log-probabilities.  A row whose in_thinking flag is set accepts the drafted token when
  * it is one of the candidates with log-probability >= the best candidate's log-probability - delta
- * (formed in fp32); every other row accepts only the best candidate (the first listed among equal best).
+ * (the threshold formed in fp64 from the single-precision inputs: the exact comparison); every other row accepts only the best candidate (the first listed among equal best).
  * accepted_len[b] = number of leading accepted positions (0..gamma).
  *   draft           [batch, gamma] int32
  *   topk_ids        [batch, gamma, k] int32
@@ -306,10 +306,11 @@ typedef struct {
                             reaches top_p of their total */
 } eagle3_sampling_t;
 
-/* Draw one token per row from filtered logits: x = logits * (1 / temperature) (fp32); keep the top_k largest x
- * (lower indices first among equal values), then the top_p prefix in the order (x descending, index
- * ascending); renormalise the kept softmax weights and pick by inverse CDF over the kept tokens in
- * ascending index order with uniforms[r].
+/* Draw one token per row from filtered logits: x = logits / temperature; keep the top_k largest x (lower
+ * indices first among equal values; x is ordered as the logits are, so this set is exact), then the top_p
+ * prefix in the order (x descending, index ascending) by the softmax mass of x (fp32 weights
+ * exp((l - l_max) / temperature)); renormalise the kept weights and pick by inverse CDF over the kept
+ * tokens in ascending index order with uniforms[r].
  *   logits       [rows, ld] fp32, the first V entries of each row are the draft-vocabulary logits
  *   uniforms     [rows] fp32
  *   d2t          [V] int32 additive draft-to-target map or NULL (tokens are then draft ids)

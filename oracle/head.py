@@ -447,12 +447,13 @@ def accept_relaxed(draft, topk_ids, topk_logprobs, in_thinking, delta):
     outside it accepts only the target's best candidate (the greedy rule; among equal best
     log-probabilities the first listed wins).  The accepted length counts leading accepted positions.
     draft [B, G]; topk_ids, topk_logprobs [B, G, k]; in_thinking [B] (bool).  Returns (acc, hist) like
-    ``accept``.  The log-probabilities arrive in fp32 and the threshold best - delta decides an integer,
-    so it is formed and compared in fp32, as the GPU does."""
+    ``accept``.  The comparison lp >= best - delta is the plain real-number one on the given values:
+    the log-probabilities and delta are single-precision inputs, widened exactly to fp64, where the
+    threshold is formed."""
     draft = np.asarray(draft)
     ids = np.asarray(topk_ids)
-    lp = np.asarray(topk_logprobs, dtype=np.float32)
-    delta = np.float32(delta)
+    lp = np.asarray(topk_logprobs, dtype=np.float32).astype(np.float64)
+    delta = float(np.float32(delta))
     think = np.asarray(in_thinking, dtype=bool)
     B, G = draft.shape
     K = ids.shape[2]
@@ -481,11 +482,9 @@ def sample_filtered(logits, temperature, top_k, top_p, u):
     counter feeds the sampler).  The uniform u in [0, 1) is an input, so both sides draw the same number.
 
     Reading of the pages, which name the parameters but not their composition: temperature 0 is the
-    greedy argmax (lowest index among equal maxima).  Otherwise x = logits * (1 / temperature), the
-    reciprocal and the product rounded to fp32 as the GPU forms them (x decides which tokens are kept, so
-    both sides use the same fp32 values); top_k > 0 keeps the top_k largest x, lower indices first among
-    equal values; top_p < 1
-    then keeps the shortest prefix of those, in the order (x descending, index ascending), whose softmax
+    greedy argmax (lowest index among equal maxima).  Otherwise x = logits / temperature (in fp64 from
+    the given logits); top_k > 0 keeps the top_k largest x, lower indices first among equal values;
+    top_p < 1 then keeps the shortest prefix of those, in the order (x descending, index ascending), whose softmax
     mass reaches top_p of the kept mass.  The kept tokens' softmax weights are renormalised and u picks
     the token by inverse CDF over the kept tokens in ascending index order.
     Returns (token, probs) with probs [V] the final distribution (zero outside the kept set)."""
@@ -496,7 +495,7 @@ def sample_filtered(logits, temperature, top_k, top_p, u):
         t = int(np.flatnonzero(l == l.max())[0])
         probs[t] = 1.0
         return t, probs
-    x = (l * (np.float32(1.0) / np.float32(temperature))).astype(np.float32)
+    x = l.astype(np.float64) / float(temperature)
     order = sorted(range(V), key=lambda i: (-float(x[i]), i))
     kept = order[:top_k] if top_k > 0 else order
     m = float(x[kept[0]])

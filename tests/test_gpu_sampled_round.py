@@ -77,7 +77,7 @@ def _sampled_round(w, T, k, p, seed, tol):
             t_o, pr_o = O.sample_filtered(g_lg[s, b], T, k, p, float(u[s, b]))
             want = int(t_o + d2t_np[t_o])
             if int(g_tok[b, s]) != want:
-                near = {int(a + d2t_np[a]) for du in (-EPS, EPS) for dp in ((-EPS, 0.0, EPS) if p < 1 else (0.0,))
+                near = {int(a + d2t_np[a]) for du in (-EPS, 0.0, EPS) for dp in ((-EPS, 0.0, EPS) if p < 1 else (0.0,))
                         for a in [O.sample_filtered(g_lg[s, b], T, k, min(1.0, p + dp),
                                                     min(max(float(u[s, b]) + du, 0.0), 1 - 1e-9))[0]]}
                 assert int(g_tok[b, s]) in near, (s, b, int(g_tok[b, s]), want)

@@ -340,7 +340,7 @@ def test_sample_filtered_frequencies_match_softmax():
     # inverse-CDF sampling over a fine grid of u reproduces the renormalised softmax of the kept set
     l = np.array([1.0, 0.2, -0.5, 1.5, 0.0, 0.7], dtype=np.float32)
     T = 0.8
-    x = (l * (np.float32(1.0) / np.float32(T))).astype(np.float64)
+    x = l.astype(np.float64) / T
     for top_k, top_p, keep in [(0, 1.0, [0, 1, 2, 3, 4, 5]), (3, 1.0, [3, 0, 5]), (6, 0.5, [3, 0])]:
         w = np.zeros(6)
         w[keep] = np.exp(x[keep] - x[keep].max())
