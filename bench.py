@@ -29,8 +29,7 @@ sys.path.insert(0, ROOT)
 METRIC = "draft tokens/s on 1 GB300 (DSV3-shaped EAGLE3 head); % of HBM / tensor roofline"
 UNIT = "draft tokens/s"
 FALLBACK_HBM_GBS = 6800.0
-FALLBACK_BF16_TFLOPS = 1700.0   # sustained bf16 dense, one earlier GB300 measurement
-FALLBACK_BF16_TFLOPS = 1900.0
+FALLBACK_BF16_TFLOPS_SUSTAINED = 1700.0   # sustained bf16 dense, one earlier GB300 measurement
 
 
 # --------------------------------------------------------------------------------------------- setup
@@ -99,7 +98,7 @@ def peak_tensor(peaks):
     for k in ("bf16_tflops_sustained", "bf16_tflops"):
         if k in peaks:
             return float(peaks[k]), k
-    return FALLBACK_BF16_TFLOPS, "fallback"
+    return FALLBACK_BF16_TFLOPS_SUSTAINED, "fallback"
 
 
 def peak_hbm(peaks):
@@ -322,6 +321,39 @@ def decode_step_entry(decode_ms, steps, ws, B, G, model, hbm):
                     "first token's remap launch"}
 
 
+def workload_config(w, lengths, n_replicas, weights="bf16", sampling=None):
+    """The `config` object of the JSON line: the workload and what one step runs.  Both arms print the
+    same object for the same command line."""
+    fp8, nvfp4 = weights == "fp8", weights == "nvfp4"
+    B, G = w.batch, w.gamma
+    round_bytes = sum(b * n for b, n in algorithmic_bytes(w, lengths, fp8=fp8, nvfp4=nvfp4).values())
+    return {"workload": f"{w.name}: "
+                        + (f"Llama-style MHA EAGLE-3 head ({w.n_heads} heads, {w.n_kv_heads} key/value heads, "
+                           f"head_dim {w.head_dim}, {w.fc_inputs}-way fc) on a DSV3 target"
+                           if w.attention == "mha" else "DSV3-shaped EAGLE-3 head")
+                        + f", batch {B}, context {w.ctx[0]}-{w.ctx[1]}, "
+                        f"T_new {w.t_new}, gamma {G}, draft vocab {w.draft_vocab}"
+                        + (" with d2t" if w.d2t else ""),
+            "batch": B, "gamma": G, "ctx": list(w.ctx), "draft_vocab": w.draft_vocab,
+            "weights": ("FP8 E4M3 projection matrices with per-row fp32 scales (quantized on the GPU "
+                        "from the bf16 weights); kv_b, embedding and norms bf16") if fp8 else
+                       ("NVFP4 projection matrices: E2M1 codes, E4M3 scales per 16 weights, an fp32 scale "
+                        "per matrix (quantized on the GPU from the bf16 weights); kv_b, embedding and norms "
+                        "bf16") if nvfp4 else w.dtype,
+            "step": "extend + (gamma-1) decode steps + acceptance" if sampling is None else
+                    f"extend + (gamma-1) sampled decode steps (T {sampling[0]}, top_k {sampling[1]}, "
+                    f"top_p {sampling[2]}) + residual acceptance",
+            "l2": f"inputs larger than L2: {round_bytes / 1e9:.2f} GB of weights+KV streamed per step",
+            "parallelism": f"replicas x{n_replicas} (sequence-sharded, no collective)"}
+
+
+def parse_sampling(args):
+    if not args.sampling:
+        return None
+    T_s, k_s, p_s = args.sampling.split(",")
+    return float(T_s), int(k_s), float(p_s)
+
+
 # --------------------------------------------------------------------------------------------- our arm
 def run_ours(args, ws, rank, local):
     import numpy as np
@@ -360,10 +392,8 @@ def run_ours(args, ws, rank, local):
     tgt = torch.from_numpy(WL.synthetic_targets(w, toks.cpu().numpy())).cuda()
     assert head.error_word() == 0
 
-    sampling = None
-    if args.sampling:
-        T_s, k_s, p_s = args.sampling.split(",")
-        sampling = (float(T_s), int(k_s), float(p_s))
+    sampling = parse_sampling(args)
+    if sampling is not None:
         Vt = w.target_vocab if d2t is not None else w.draft_vocab
         gen = torch.Generator(device="cuda").manual_seed(1234)
         lg0 = torch.empty((B, w.draft_vocab), dtype=torch.float32, device="cuda")
@@ -444,6 +474,9 @@ def run_ours(args, ws, rank, local):
     launches += args.steps  # one acceptance launch per round
     assert head.error_word() == 0
     del graph
+    # every round drafts the same tokens against the same targets, so the last round's acceptance is
+    # every round's
+    acc_hist = [int(v) for v in hist.cpu().tolist()]
 
     # ---------------------------------------------------------------- decode steps alone
     # The same head after one extend, replaying decode(gamma) calls (gamma - 1 decode steps each, plus
@@ -566,30 +599,13 @@ def run_ours(args, ws, rank, local):
         "scaling": "weak", "vs_baseline": None,
         "dtype": (f"{'fp8_e4m3' if fp8 else 'nvfp4'} weights, bf16 activations and cache, fp32 accumulate"
                   if fp8 or nvfp4 else w.dtype), "data": "synthetic (seeded; random-init weights)",
-        "config": {"workload": f"{w.name}: "
-                               + (f"Llama-style MHA EAGLE-3 head ({w.n_heads} heads, {w.n_kv_heads} key/value heads, "
-                                  f"head_dim {w.head_dim}, {w.fc_inputs}-way fc) on a DSV3 target"
-                                  if w.attention == "mha" else "DSV3-shaped EAGLE-3 head")
-                               + f", batch {B}, context {w.ctx[0]}-{w.ctx[1]}, "
-                               f"T_new {w.t_new}, gamma {G}, draft vocab {w.draft_vocab}"
-                               + (" with d2t" if w.d2t else ""),
-                   "batch": B, "gamma": G, "ctx": list(w.ctx), "draft_vocab": w.draft_vocab,
-                   "weights": ("FP8 E4M3 projection matrices with per-row fp32 scales (quantized on the GPU "
-                               "from the bf16 weights); kv_b, embedding and norms bf16") if fp8 else
-                              ("NVFP4 projection matrices: E2M1 codes, E4M3 scales per 16 weights, an fp32 scale "
-                               "per matrix (quantized on the GPU from the bf16 weights); kv_b, embedding and norms "
-                               "bf16") if nvfp4 else w.dtype,
-                   "step": "extend + (gamma-1) decode steps + acceptance" if sampling is None else
-                           f"extend + (gamma-1) sampled decode steps (T {sampling[0]}, top_k {sampling[1]}, "
-                           f"top_p {sampling[2]}) + residual acceptance",
-                   "l2": f"inputs larger than L2: {round_bytes / 1e9:.2f} GB of weights+KV streamed per step",
-                   "parallelism": f"replicas x{ws} (sequence-sharded, no collective)"},
+        "config": workload_config(w, lengths, ws, args.weights, sampling),
         "roofline": ({"bound": "tensor", "kernel": dom, "achieved": round(achieved_tf, 1), "peak": tpeak,
                       "unit": "TFLOP/s", "frac": round(achieved_tf / tpeak, 4),
                       "traffic": measured_traffic(dom, traffic_key), "avg_us": round(dom_avg_s * 1e6, 2),
                       "algo_flops_per_launch": int(dom_flops), "algo_bytes_per_launch": int(dom_bytes),
                       "hbm_frac": round(achieved / hbm, 4),
-                      "peak_source": f"{src} ({tkey if src == 'measured' else 'fallback 1.7 PFLOP/s sustained'})"}
+                      "peak_source": f"{src} ({tkey if src == 'measured' else 'fallback 1.7 PFLOP/s sustained bf16'})"}
                      if tensor_bound else
                      {"bound": "hbm", "kernel": dom, "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
                       "frac": round(achieved / hbm, 4), "traffic": measured_traffic(dom, traffic_key),
@@ -598,6 +614,12 @@ def run_ours(args, ws, rank, local):
                       "tensor_frac": round(achieved_tf / tpeak, 4),
                       "peak_source": f"{src} ({'MEASURED_PEAKS.json hbm_gbs' if src == 'measured' else 'fallback 6.8 TB/s'})"}),
         "decode_step": decode_step_entry(decode_ms, args.steps, ws, B, G, model, hbm),
+        "acceptance": {"rule": "greedy" if sampling is None else "residual",
+                       "accepted_len_hist": acc_hist,
+                       "mean_accepted_len": round(sum(k * c for k, c in enumerate(acc_hist)) / max(1, sum(acc_hist)), 4),
+                       "note": "hist[k] = sequences of one round (rank 0) whose first k drafts were accepted; "
+                               "the synthetic targets agree with the drafts with the workload's per-position "
+                               "probabilities"},
         "step_roofline": {"algo_bytes": int(round_bytes), "achieved_gbs": round(round_bytes / step_s / 1e9, 1),
                           "frac": round(round_bytes / step_s / 1e9 / hbm, 4),
                           "algo_flops": int(round_flops),
@@ -658,27 +680,30 @@ def host_cores():
 
 
 def run_reference(args, rank):
-    """The oracle as it stands, timed on the host cores; each step is one fp64 decode step of one sequence."""
+    """The oracle as it stands, timed on the host cores.  Each step is the GPU arm's step, the drafting
+    round (extend + gamma - 1 decode steps), on one sequence of the batch (sequences are independent),
+    so the value is the same metric in the same unit on the same workload."""
     import workloads as WL
     w = WL.workload(args.workload)
     stored = WL.make_weights(w)
     lengths = WL.context_lengths(w)
-    for _ in range(args.warmup):
-        oracle_sample(w, stored, lengths, decode_only=True)
+    for i in range(args.warmup):
+        oracle_sample(w, stored, lengths, seconds_budget=float("inf"), seq=i % w.batch)
     tot_t, tot_k = 0.0, 0
     for i in range(args.steps):
-        k, t, desc = oracle_sample(w, stored, lengths, decode_only=True, seq=i % w.batch)
+        k, t, desc = oracle_sample(w, stored, lengths, seconds_budget=float("inf"), seq=i % w.batch)
         tot_t += t
         tot_k += k
     value = tot_k / tot_t
+    sample = (f"each step: one drafting round (extend with T_new {w.t_new} + {w.gamma - 1} decode steps, "
+              f"{w.gamma} draft tokens) of one of the {w.batch} sequences, in the fp64 oracle")
     return {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": UNIT, "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(tot_t / args.steps * 1e3, 2),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic (seeded; random-init weights)",
-            "config": {"workload": f"{w.name}", "batch": w.batch, "gamma": w.gamma,
-                       "sample": "each step: one decode step (1 draft token) of one sequence"},
+            "config": workload_config(w, lengths, args.gpus, args.weights, parse_sampling(args)),
             "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": host_cores(), "kind": "oracle",
-                             "sample": desc},
+                             "sample": sample},
             "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 

@@ -617,14 +617,10 @@ cudaError_t launch_absorb(const AttnArgs& a, cudaStream_t st) {
     dim3 grid(a.nh, a.dc / cols, (a.M + kAbsRows - 1) / kAbsRows);
     const int RG = 256 / (cols / 8);
     const size_t sm = ((size_t)kAbsRows * a.dn + (size_t)RG * kAbsRows * cols) * sizeof(float);
-    static bool attr[2] = {false, false};
-    const int ti = a.dt == BF16 ? 1 : 0;
-    if (!attr[ti]) {
-        cudaError_t e = a.dt == BF16
-            ? cudaFuncSetAttribute(absorb_kernel<bf16>, cudaFuncAttributeMaxDynamicSharedMemorySize, 96 * 1024)
-            : cudaFuncSetAttribute(absorb_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize, 96 * 1024);
+    {
+        cudaError_t e = a.dt == BF16 ? smem_optin((const void*)absorb_kernel<bf16>, 96 * 1024)
+                                     : smem_optin((const void*)absorb_kernel<float>, 96 * 1024);
         if (e != cudaSuccess) return e;
-        attr[ti] = true;
     }
     if (sm > 96 * 1024) return cudaErrorInvalidValue;
     if (a.dt == BF16) launch_pdl(absorb_kernel<bf16>, dim3(grid), dim3(256), sm, st, a);
@@ -637,12 +633,9 @@ static cudaError_t attn_launch(const AttnArgs& a, cudaStream_t st) {
     constexpr int D = DC + DR;
     constexpr int WORDS = D / (4 / sizeof(T));
     const size_t sm = (size_t)kHeadsPerCta * D * sizeof(float) + (size_t)kTile * (WORDS | 1) * sizeof(uint32_t);
-    static bool attr_set = false;
-    if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(attention_kernel<T, DC, DR>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
+    {
+        cudaError_t e = smem_optin((const void*)attention_kernel<T, DC, DR>, (int)sm);
         if (e != cudaSuccess) return e;
-        attr_set = true;
     }
     dim3 grid(a.splits, (a.nh + kHeadsPerCta - 1) / kHeadsPerCta, a.M);
     launch_pdl(attention_kernel<T, DC, DR>, dim3(grid), dim3(kAttnWarps * 32), sm, st, a);
@@ -652,12 +645,9 @@ static cudaError_t attn_launch(const AttnArgs& a, cudaStream_t st) {
 cudaError_t launch_attention(const AttnArgs& a, cudaStream_t st) {
     if (a.dc == 512 && a.dr == 64) {
         if (a.dt == BF16) {
-            static bool attr_set = false;
-            if (!attr_set) {
-                cudaError_t e = cudaFuncSetAttribute(attention_mma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                     (int)mla_mma::SMEM);
+            {
+                cudaError_t e = smem_optin((const void*)attention_mma_kernel, (int)mla_mma::SMEM);
                 if (e != cudaSuccess) return e;
-                attr_set = true;
             }
             if (!a.qa_bf) return cudaErrorInvalidValue;
             dim3 grid(a.splits, (a.nh + mla_mma::HEADS - 1) / mla_mma::HEADS, a.M);

@@ -11,6 +11,10 @@ namespace e3 {
 // FP8: E4M3 codes with per-row fp32 scales; FP4: NVFP4 (E2M1 codes, E4M3 scales per 16, fp32 per matrix)
 enum DType { F32 = 0, BF16 = 1, FP8 = 2, FP4 = 3 };
 
+// Opts `kernel` in to `bytes` of dynamic shared memory on the current device.  The opt-in is a property
+// of the device's context, so it is made once per (kernel, device) and remembered under a lock.
+cudaError_t smem_optin(const void* kernel, int bytes);
+
 // ---------------------------------------------------------------- weight-streaming GEMM
 // y[m, n] = sum_k A[m, k] * W[n, k] for m < M, n < N, with
 //   A given as up to 3 consecutive K-segments (a[s], row stride lda[s], width ka[s]),

@@ -59,11 +59,13 @@ cudaError_t device_slot(DeviceSlot* out) {
     return cudaSuccess;
 }
 
-// Split count: enough (N-tile, M-tile, split) CTAs for two per SM, at least four K-blocks per split, and
-// no more splits than the scratch holds (two always fit under the M * N limit).
+// Split count: one when the (N-tile, M-tile) CTAs already cover every SM (the GEMM then writes y itself
+// and the scratch is not touched); else enough split CTAs for two per SM, at least four K-blocks per
+// split, and no more splits than the scratch holds (two always fit under the M * N limit).
 int noalloc_splits(int num_sms, int M, int N, int K, int bn) {
     const long tiles = (long)((N + 127) / 128) * ((M + bn - 1) / bn);
-    long s = tiles >= num_sms ? 2 : (2L * num_sms + tiles - 1) / tiles;
+    if (tiles >= num_sms) return 1;
+    long s = (2L * num_sms + tiles - 1) / tiles;
     const long kmax = K / 64 / 4;
     if (s > kmax) s = kmax;
     while (s > 2 && s * (long)M * N * (long)sizeof(float) > (long)kNoallocPartBytes) --s;

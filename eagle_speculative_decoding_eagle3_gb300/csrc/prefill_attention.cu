@@ -289,12 +289,9 @@ cudaError_t launch_rope_q_rows(const PrefillArgs& a, cudaStream_t st) {
 }
 
 cudaError_t launch_prefill_attention(const PrefillArgs& a, cudaStream_t st) {
-    static bool attr_set = false;
-    if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(prefill_attention_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)pf::SMEM);
+    {
+        cudaError_t e = smem_optin((const void*)prefill_attention_kernel, (int)pf::SMEM);
         if (e != cudaSuccess) return e;
-        attr_set = true;
     }
     return launch_pdl(prefill_attention_kernel, dim3(a.ntiles_cap, a.nh), dim3(pf::THREADS), pf::SMEM, st, a);
 }

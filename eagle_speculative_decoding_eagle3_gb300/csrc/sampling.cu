@@ -448,12 +448,9 @@ cudaError_t launch_sample(const SampleArgs& s, cudaStream_t st) {
     if (s.V < 1 || s.V > 32 * smp::kMaxChunks || s.rows < 1 || (s.top_k > smp::kMaxTopK) ||
         (s.temperature > 0.f && s.top_k <= 0 && s.top_p < 1.f))
         return cudaErrorInvalidValue;
-    static bool attr_set = false;
-    if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(sample_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)(smp::kKeyCache * sizeof(uint32_t)));
+    {
+        cudaError_t e = smem_optin((const void*)sample_kernel, (int)(smp::kKeyCache * sizeof(uint32_t)));
         if (e != cudaSuccess) return e;
-        attr_set = true;
     }
     const bool cached = s.temperature > 0.f && s.top_k > 0 && s.V <= smp::kKeyCache;
     const size_t smem = cached ? (size_t)s.V * sizeof(uint32_t) : 0;

@@ -416,12 +416,9 @@ bool make_tma_2d(CUtensorMap* map, const void* ptr, long rows, long cols, long l
 template <int BN, int MODE>
 static cudaError_t tc_launch_bn(const TcParams& p, dim3 grid, cudaStream_t st) {
     using C = tc::Cfg<BN, MODE>;
-    static bool attr = false;
-    if (!attr) {
-        cudaError_t e = cudaFuncSetAttribute(tc::tc_gemm_kernel<BN, MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             C::SMEM);
+    {
+        cudaError_t e = smem_optin((const void*)tc::tc_gemm_kernel<BN, MODE>, (int)C::SMEM);
         if (e != cudaSuccess) return e;
-        attr = true;
     }
     cudaError_t le = launch_pdl(tc::tc_gemm_kernel<BN, MODE>, grid, dim3(tc::kThreads), (size_t)C::SMEM, st, p);
     if (le != cudaSuccess) return le;

@@ -57,19 +57,25 @@ class QuantOracleWeights(Mapping):
 
 
 def run_round(w, seqs=None, absorbed=False, with_logits=True, stored=None, d2t_override="default", fp8=False,
-              nvfp4=False):
+              nvfp4=False, gpu_inputs=None, oracle_inputs=None):
     """GPU round (extend + gamma-1 decode steps + accept) and the oracle's forced-continuation round.
 
     ``seqs``: sequences the oracle checks (all by default); the GPU always runs the whole batch.
     ``fp8`` / ``nvfp4``: the head stores its projection matrices as FP8 E4M3 with row scales (NVFP4 with
     block and matrix scales), quantized on the GPU by eagle3_quantize_e4m3 (eagle3_quantize_nvfp4); the
     oracle runs on its own quantization of the same weights.
+    ``gpu_inputs(ex, paged, d2t) -> d2t`` may edit the GPU's extend inputs and cache in place (and return
+    the GPU's vocab map); ``oracle_inputs(exs, d2t) -> d2t`` does the same for the oracle's (rows of the
+    checked sequences only).  Both default to the seeded inputs unchanged.
     """
     stored = WL.make_weights(w) if stored is None else stored
     lengths = WL.context_lengths(w)
     paged = WL.make_cache(w, lengths)
     ex = WL.make_extend(w, lengths)
     d2t = WL.make_d2t(w) if d2t_override == "default" else d2t_override
+    d2t_orc = d2t
+    if gpu_inputs is not None:
+        d2t = gpu_inputs(ex, paged, d2t)
     head = HN.DeviceHead(w, stored, fp8=fp8, nvfp4=nvfp4)
     try:
         dc = head.cache(paged)
@@ -101,18 +107,22 @@ def run_round(w, seqs=None, absorbed=False, with_logits=True, stored=None, d2t_o
     W = QuantOracleWeights(stored, "fp8" if fp8 else "nvfp4") if (fp8 or nvfp4) else WL.F64Cache(stored)
     caches = [O.SeqCache(WL.as_f32(WL.cache_rows(w, b, int(lengths[b]))), w.max_ctx) for b in seqs]
     exs = WL.make_extend(w, lengths, seqs=seqs)
+    if oracle_inputs is not None:
+        d2t_orc = oracle_inputs(exs, d2t_orc)
     aux = [WL.as_f32(a) for a in exs.aux]
-    orc = O.draft_round(w.hyper(), W, d2t, w.gamma, aux, exs.tokens, exs.positions, exs.row_offsets, caches,
+    orc = O.draft_round(w.hyper(), W, d2t_orc, w.gamma, aux, exs.tokens, exs.positions, exs.row_offsets, caches,
                         absorbed=absorbed, forced=gpu["tokens"][seqs])
     orc["caches"] = caches
     orc["lengths"] = lengths
+    orc["d2t"] = d2t_orc
     return gpu, orc, seqs, paged
 
 
-def check_round(w, gpu, orc, seqs, paged, tol):
-    """Assert every parity rule; returns a dict of the measured errors."""
+def check_round(w, gpu, orc, seqs, paged, tol, err=0):
+    """Assert every parity rule; returns a dict of the measured errors.  ``err``: the device error word
+    the round must leave (0 for valid inputs)."""
     G = w.gamma
-    assert gpu["err"] == 0, f"device error word {gpu['err']}"
+    assert gpu["err"] == err, f"device error word {gpu['err']}, expected {err}"
     rep = {}
     # hidden states of every step
     rep["hidden"] = row_rel_err(gpu["hidden"][:, seqs], orc["hidden"])
@@ -122,7 +132,7 @@ def check_round(w, gpu, orc, seqs, paged, tol):
         rep["logits"] = row_rel_err(gpu["logits"][:, seqs], orc["logits"])
         assert rep["logits"] <= tol, rep
     ties = 0
-    d2t = WL.make_d2t(w)
+    d2t = orc["d2t"]        # the vocab map the oracle's round used
     for s in range(G):
         for i, b in enumerate(seqs):
             lg = orc["logits"][s, i]

@@ -22,7 +22,13 @@ def test_reference_arm_prints_one_json_line_with_the_contract_keys(workload):
               "vs_baseline", "dtype", "data", "config"):
         assert k in d, k
     assert d["impl"] == "reference" and d["n_gpus"] == 1 and d["steps"] == 2 and d["higher_is_better"] is True
-    assert d["value"] > 0 and d["config"]["workload"] == workload
+    assert d["value"] > 0 and d["config"]["workload"].startswith(workload + ":")
+    # the same config object the GPU arm prints for this command line, so the two lines compare
+    sys.path.insert(0, ROOT)
+    import bench
+    import workloads as WL
+    w = WL.workload(workload)
+    assert d["config"] == bench.workload_config(w, WL.context_lengths(w), 1)
     cb = d["cpu_baseline"]
     assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["value"] == d["value"] and cb["sample"]
     assert d["e2e"] == {"value": d["value"], "unit": d["unit"], "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}

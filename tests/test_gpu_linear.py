@@ -6,6 +6,7 @@ import torch
 
 import oracle as O
 import workloads as WL
+from parity import row_rel_err
 
 pytestmark = pytest.mark.gpu
 
@@ -35,8 +36,7 @@ def test_linear_matches_oracle(head, M, N, K):
     torch.cuda.synchronize()
     assert head.error_word() == 0
     ref = O.linear(WL.bf16_to_f32(x), WL.bf16_to_f32(w))
-    got = y.cpu().numpy().astype(np.float64)
-    err = np.abs(got - ref).max() / np.abs(ref).max()
+    err = row_rel_err(y.cpu().numpy(), ref)      # per row: ||g - o||_inf / ||o||_inf
     assert err < 1e-5, err
 
 
@@ -54,6 +54,5 @@ def test_linear_pair_tiles_match_oracle(head, M):
     torch.cuda.synchronize()
     assert head.error_word() == 0
     ref = O.linear(WL.bf16_to_f32(x), WL.bf16_to_f32(w))
-    got = y.cpu().numpy().astype(np.float64)
-    err = np.abs(got - ref).max() / np.abs(ref).max()
+    err = row_rel_err(y.cpu().numpy(), ref)      # per row: ||g - o||_inf / ||o||_inf
     assert err < 1e-5, err
