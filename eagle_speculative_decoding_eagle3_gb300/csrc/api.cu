@@ -189,6 +189,35 @@ void attn_plan(const eagle3_draft& d, int M, int* splits, int* chunk) {
     *chunk = s > 1 ? (int)ch : 0;
 }
 
+// The tcgen05 latent attention serves the DeepseekV3 geometry in bf16 (128 heads, latent 512, rope 64)
+// with cache pages of a multiple of 64 slots.
+bool attention_tc_ok(const eagle3_draft& d) {
+    const eagle3_config_t& c = d.cfg;
+    return c.dtype == EAGLE3_BF16 && c.attention != EAGLE3_ATTN_MHA && c.n_heads == 128 && c.kv_lora_rank == 512 &&
+           c.qk_rope_dim == 64 && c.page_size % 64 == 0;
+}
+
+// Split plan of the tcgen05 attention: fixed chunks of whole 64-slot tiles (splits past a row's context
+// exit at once and the merge skips them), sized so the CTA pairs of the longest possible contexts fill
+// about one wave (few rows) or four waves (more rows), with at most splits_cap splits and the partials
+// within the workspace.
+void attn_plan_tc(const eagle3_draft& d, int M, int* splits, int* chunk) {
+    const long pairs = d.num_sms / 2 > 0 ? d.num_sms / 2 : 1, ctx = d.cfg.max_ctx;
+    const long waves = M < kAttnChunkRows ? 1 : 4;
+    long ch = (ctx * M + waves * pairs - 1) / (waves * pairs);
+    const long ch_min = (ctx + d.splits_cap - 1) / d.splits_cap;
+    if (ch < ch_min) ch = ch_min;
+    if (ch < 128) ch = 128;
+    ch = (ch + 63) / 64 * 64;
+    long s = (ctx + ch - 1) / ch;
+    while (s > 1 && (s > d.splits_cap || (size_t)M * s > d.part_rows)) {
+        ch *= 2;
+        s = (ctx + ch - 1) / ch;
+    }
+    *splits = (int)s;
+    *chunk = (int)((s > 1 ? ch : (ctx + 63) / 64 * 64));
+}
+
 bool mha_head(const eagle3_config_t& c) { return c.attention == EAGLE3_ATTN_MHA; }
 int fc_inputs(const eagle3_config_t& c) { return c.fc_inputs == 0 ? 3 : c.fc_inputs; }
 // width rotated by RoPE: d_r (MLA) or the whole head_dim (MHA)
@@ -718,7 +747,9 @@ cudaError_t run_attention_mla(eagle3_draft& d, eagle3_kv_t* kv, int M, cudaStrea
         aa.M = M; aa.nh = nh; aa.dn = dn; aa.dr = dr; aa.dc = dc; aa.dv = dv;
         aa.sigma = attention_scale(c);
         aa.page_size = c.page_size; aa.max_pages = c.max_pages_per_seq; aa.num_pages = kv->num_pages; aa.err = d.err;
-        attn_plan(d, M, &aa.splits, &aa.chunk);
+        const bool tc_attn = attention_tc_ok(d);
+        if (tc_attn) attn_plan_tc(d, M, &aa.splits, &aa.chunk);
+        else attn_plan(d, M, &aa.splits, &aa.chunk);
         aa.dt = ra.dt;
         aa.row_seq = d.row_seq; aa.row_pos = d.row_pos; aa.block_table = kv->block_table;
         aa.cache = kv->data; aa.kv_b = w.kv_b; aa.q = d.q; aa.rope_cos = d.rope_cos; aa.rope_sin = d.rope_sin;
@@ -736,7 +767,7 @@ cudaError_t run_attention_mla(eagle3_draft& d, eagle3_kv_t* kv, int M, cudaStrea
         // o_lat: written by the attention kernel itself for a single split, else by the split merge; then
         // o_h = W_UV,h o_lat,h over the value rows of kv_b
         if (tc) aa.olat_bf = d.olat_bf; else aa.olat = d.olat;
-        E3_TRY(traced(d, K_ATTN, st, [&] { return launch_attention(aa, st); }));
+        E3_TRY(traced(d, K_ATTN, st, [&] { return tc_attn ? launch_attention_tc(aa, st) : launch_attention(aa, st); }));
         if (aa.splits > 1) E3_TRY(traced(d, K_COMBINE, st, [&] { return launch_merge(aa, st); }));
         if (tc) {
             E3_TRY(run_batched(d, K_UNABSORB, M, d.olat_bf, (long)nh * dc, dc, w.kv_b, (long)nh * (dn + dv), dn, dn + dv,

@@ -225,6 +225,10 @@ cudaError_t launch_transpose_wuk(const void* kv_b, int nh, int dn, int dv, int d
                                  cudaStream_t st);
 bool attention_supported(int dc, int dr, int dn, int dv);
 int attention_heads_per_cta(int dt, int dc, int dr);
+// tcgen05 latent attention (bf16 cache, 128 heads, latent 512 + rope 64, fixed-chunk splits of 64k
+// slots, pages of 64k slots): one CTA pair per (split, row); same partial / o_lat outputs as above
+bool attention_tc_supported(const AttnArgs& a);
+cudaError_t launch_attention_tc(const AttnArgs& a, cudaStream_t st);
 
 // ---------------------------------------------------------------- tcgen05 GEMM (bf16, many rows)
 // out[m, n] = sum_k W[n, k] X[m, k]; W from mw[0] (rows < np0) and mw[1] (rows >= np0, or the up

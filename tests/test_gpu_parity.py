@@ -53,6 +53,27 @@ def test_mla_shaped_bf16_round():
     print(check_round(w, gpu, orc, seqs, paged, TOL_BF16))
 
 
+# 128 heads with the DeepseekV3 latent geometry: the tcgen05 latent attention (a CTA pair per row and
+# split, scores split over K across the pair) on a narrow hidden size
+MLA128 = dict(hidden=1024, n_heads=128, q_lora_rank=256, intermediate=2048, target_vocab=8192, draft_vocab=4096)
+
+
+@pytest.mark.parametrize("over", [
+    # GEMV decode (3 rows), tensor-core extend (9 rows); ragged contexts over several splits and pages
+    dict(batch=3, ctx=(100, 700), t_new=3, gamma=4, accept_p=(0.7,) * 4, seed=85),
+    # every call on the tensor-core path (24 and 48 rows)
+    dict(batch=24, ctx=(30, 700), t_new=2, gamma=3, accept_p=(0.7,) * 3, seed=86),
+    # contexts short enough for a single split (o_lat written by the attention kernel itself)
+    dict(batch=3, ctx=(3, 20), t_new=5, gamma=3, accept_p=(0.7,) * 3, seed=87),
+    # extend on an empty cache: causal attention among the new rows only
+    dict(batch=2, ctx=(0, 0), t_new=9, gamma=3, accept_p=(0.7,) * 3, seed=88),
+])
+def test_mla_128_heads_tensor_core_attention(over):
+    w = WL.workload("dsv3_b1", **MLA128, **over)
+    gpu, orc, seqs, paged = run_round(w, absorbed=True)
+    print(check_round(w, gpu, orc, seqs, paged, TOL_BF16))
+
+
 def test_dsv3_b1_full_size_round():
     # the batch-1 DeepseekV3-shaped workload at full size (4096-token cache, 32000-entry draft vocab
     # with d2t), as the benchmark runs it; the oracle follows the unabsorbed definition
