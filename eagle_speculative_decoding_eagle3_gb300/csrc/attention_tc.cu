@@ -32,7 +32,8 @@
 // The running maximum is updated lazily (only when a tile's maximum exceeds it by more than 2^8), so
 // O is rescaled in TMEM only on those rare tiles.
 //
-// Warps: 0 TMA producer (the cache tiles through the block table, a 3-deep ring);
+// Warps: 0 TMA producer (the cache tiles through the block table, one 3D box of five 64-column chunks
+// per tile, a 3-deep ring);
 // 1 TMEM owner and MMA issuer; 2-5 query loaders, then score readers (TMEM lanes = heads; a warp either
 // sends its heads' partial scores to the peer or owns their softmax); 6-9 rescale O rows when asked,
 // zero the cache rows past the context in the last tile (their P is 0, but 0 x NaN would poison O), and
@@ -95,7 +96,7 @@ static_assert(SMEM <= 227 * 1024, "shared memory");
 
 struct Params {
     AttnArgs a;
-    CUtensorMap mkv;   // cache viewed as [num_pages * page_size, 576], box 64 x 64
+    CUtensorMap mkv;   // cache rows as 64-column chunks [chunk][row][64], box 5 chunks x 64 rows
 };
 
 }  // namespace mla_tc
@@ -184,9 +185,7 @@ __global__ void __launch_bounds__(mla_tc::THREADS, 1) attention_tc_kernel(const 
                     if (page >= 0 && page < a.num_pages) {
                         mbar_expect_tx(bar(B_KV_FULL + st), KV_STAGE);
                         const int row = page * a.page_size + tt % a.page_size;
-                        for (int lc = 0; lc < NCH; ++lc)
-                            tma_load_2d(su32(stage + lc * KV_CHUNK), &p.mkv, bar(B_KV_FULL + st), (lc + 4 * (int)c) * 64,
-                                        row);
+                        tma_load_3d(su32(stage), &p.mkv, bar(B_KV_FULL + st), 0, row, 4 * (int)c);   // 5 chunks
                         ++issued;
                     } else {   // a page outside the cache reads as zeros and is flagged
                         for (int q = 0; q < KV_STAGE / 16; ++q)
@@ -204,38 +203,52 @@ __global__ void __launch_bounds__(mla_tc::THREADS, 1) attention_tc_kernel(const 
                 constexpr uint32_t idesc_pv = instr_desc_mn(128, 256, true);
                 bool ok = mbar_wait(bar(B_Q_FULL), 0, WAIT);
                 tc_fence_after();
-                auto issue_scores = [&](int i) -> bool {
-                    const int st = i % STAGES, sb = i % NS;
-                    if (!mbar_wait(bar(B_KV_FULL + st), (i / STAGES) & 1, WAIT)) return false;
-                    if (!mbar_wait(bar(B_S_EMPTY + sb), ((i / NS) & 1) ^ 1, WAIT)) return false;
-                    tc_fence_after();
-                    const uint32_t stage = su32(kvs + st * KV_STAGE);
-                    const uint32_t d = tmem + TM_S + T * sb;
-                    // K step ks covers cache columns KSPLIT c + 16 ks: local chunk (col / 64 - 4c), step
-                    // (col % 64) / 16 of its 128-byte rows; its query part is TMEM columns 8 ks ..
+                // Event loop: the scores of tile j go out as soon as their cache tile has landed and the
+                // score buffer has been read, and P V of tile i as soon as its P rows are in place, so
+                // neither waits behind the other (the tensor core runs them in issue order).
+                int js = 0, ipv = 0;
+                uint32_t idle = 0;
+                while (ok && ipv < ntiles) {
+                    bool progressed = false;
+                    if (js < ntiles) {
+                        const int st = js % STAGES, sb = js % NS;
+                        if (mbar_try(bar(B_KV_FULL + st), (js / STAGES) & 1) &&
+                            mbar_try(bar(B_S_EMPTY + sb), ((js / NS) & 1) ^ 1)) {
+                            tc_fence_after();
+                            const uint32_t stage = su32(kvs + st * KV_STAGE);
+                            const uint32_t d = tmem + TM_S + T * sb;
+                            // K step ks covers cache columns KSPLIT c + 16 ks: local chunk (col / 64 - 4c), step
+                            // (col % 64) / 16 of its 128-byte rows; its query part is TMEM columns 8 ks ..
 #pragma unroll
-                    for (int ks = 0; ks < KSTEPS; ++ks) {
-                        const int col = KSPLIT * (int)c + 16 * ks;
-                        const int lc = col / 64 - 4 * (int)c, kk = (col % 64) / 16;
-                        mma_bf16_ta(d, tmem + TM_Q + 8 * ks, smem_desc(stage + lc * KV_CHUNK) + 2 * kk, idesc_s,
-                                    ks > 0 ? 1u : 0u);
+                            for (int ks = 0; ks < KSTEPS; ++ks) {
+                                const int col = KSPLIT * (int)c + 16 * ks;
+                                const int lc = col / 64 - 4 * (int)c, kk = (col % 64) / 16;
+                                mma_bf16_ta(d, tmem + TM_Q + 8 * ks, smem_desc(stage + lc * KV_CHUNK) + 2 * kk, idesc_s,
+                                            ks > 0 ? 1u : 0u);
+                            }
+                            mma_commit(bar(B_S_FULL + sb));
+                            ++js;
+                            progressed = true;
+                        }
                     }
-                    mma_commit(bar(B_S_FULL + sb));
-                    return true;
-                };
-                if (ok) ok = issue_scores(0);
-                for (int i = 0; ok && i < ntiles; ++i) {
-                    if (i + 1 < ntiles && !issue_scores(i + 1)) { ok = false; break; }
-                    const int pb = i % NB, st = i % STAGES;
-                    if (!mbar_wait(bar(B_R_DONE + pb), (i / NB) & 1, WAIT)) { ok = false; break; }
-                    tc_fence_after();
-                    const uint32_t stage = su32(kvs + st * KV_STAGE);
+                    if (ipv < js) {
+                        const int pb = ipv % NB, st = ipv % STAGES;
+                        if (mbar_try(bar(B_R_DONE + pb), (ipv / NB) & 1)) {
+                            tc_fence_after();
+                            const uint32_t stage = su32(kvs + st * KV_STAGE);
 #pragma unroll
-                    for (int kk = 0; kk < T / 16; ++kk)
-                        mma_bf16(tmem + TM_O, smem_desc(su32(ps + pb * P_BYTES)) + 2 * kk,
-                                 smem_desc_mn(stage + kk * 16 * 128, KV_CHUNK), idesc_pv, (i > 0 || kk > 0) ? 1u : 0u);
-                    mma_commit(bar(B_KV_EMPTY + st));
-                    mma_commit_multicast(bar(B_P_FREE + pb), 0x3);
+                            for (int kk = 0; kk < T / 16; ++kk)
+                                mma_bf16(tmem + TM_O, smem_desc(su32(ps + pb * P_BYTES)) + 2 * kk,
+                                         smem_desc_mn(stage + kk * 16 * 128, KV_CHUNK), idesc_pv,
+                                         (ipv > 0 || kk > 0) ? 1u : 0u);
+                            mma_commit(bar(B_KV_EMPTY + st));
+                            mma_commit_multicast(bar(B_P_FREE + pb), 0x3);
+                            ++ipv;
+                            progressed = true;
+                        }
+                    }
+                    if (progressed) idle = 0;
+                    else if (++idle > WAIT || *abort_flag) ok = false;
                 }
                 if (!ok) *abort_flag = 1;
                 else mma_commit(bar(B_O_READY));
@@ -309,16 +322,25 @@ __global__ void __launch_bounds__(mla_tc::THREADS, 1) attention_tc_kernel(const 
                 if (!ok) break;
                 const float4* xr = reinterpret_cast<const float4*>(xs + xb * (X_BYTES / 4) + (h - 64 * (int)c) * XROW);
                 const int cnt = min(T, t1 - (t0 + i * T));
-                float mt = -INFINITY;
 #pragma unroll
                 for (int j = 0; j < T / 4; ++j) {
                     const float4 v = xr[j];
-                    sv[4 * j] = 4 * j < cnt ? (sv[4 * j] + v.x) * scale2 : -INFINITY;
-                    sv[4 * j + 1] = 4 * j + 1 < cnt ? (sv[4 * j + 1] + v.y) * scale2 : -INFINITY;
-                    sv[4 * j + 2] = 4 * j + 2 < cnt ? (sv[4 * j + 2] + v.z) * scale2 : -INFINITY;
-                    sv[4 * j + 3] = 4 * j + 3 < cnt ? (sv[4 * j + 3] + v.w) * scale2 : -INFINITY;
-                    mt = fmaxf(fmaxf(mt, fmaxf(sv[4 * j], sv[4 * j + 1])), fmaxf(sv[4 * j + 2], sv[4 * j + 3]));
+                    sv[4 * j] = (sv[4 * j] + v.x) * scale2;
+                    sv[4 * j + 1] = (sv[4 * j + 1] + v.y) * scale2;
+                    sv[4 * j + 2] = (sv[4 * j + 2] + v.z) * scale2;
+                    sv[4 * j + 3] = (sv[4 * j + 3] + v.w) * scale2;
                 }
+                if (cnt < T) {
+#pragma unroll
+                    for (int j = 0; j < T; ++j)
+                        if (j >= cnt) sv[j] = -INFINITY;
+                }
+                float mx[8];
+#pragma unroll
+                for (int k = 0; k < 8; ++k) mx[k] = sv[k];
+#pragma unroll
+                for (int j = 8; j < T; ++j) mx[j & 7] = fmaxf(mx[j & 7], sv[j]);
+                const float mt = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])), fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
                 float alpha = 1.f;
                 if (m_ref == -INFINITY) {
                     m_ref = mt;
@@ -327,13 +349,13 @@ __global__ void __launch_bounds__(mla_tc::THREADS, 1) attention_tc_kernel(const 
                     l *= alpha;
                     m_ref = mt;
                 }
-                float ls = 0.f;
+                float ps8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
                 for (int j = 0; j < T; ++j) {
                     sv[j] = ex2_approx(sv[j] - m_ref);   // P is rounded to bf16; exp2 to ~2 ulp is plenty
-                    ls += sv[j];
+                    ps8[j & 7] += sv[j];
                 }
-                l += ls;
+                l += ((ps8[0] + ps8[1]) + (ps8[2] + ps8[3])) + ((ps8[4] + ps8[5]) + (ps8[6] + ps8[7]));
                 // the previous use of this P buffer (tile i - NB) must be consumed in both CTAs
                 ok = __all_sync(0xffffffffu, i < NB || mbar_wait_cluster(bar(B_P_FREE + pb), ((i / NB) & 1) ^ 1, WAIT));
                 if (!ok) break;
@@ -496,7 +518,7 @@ cudaError_t launch_attention_tc(const AttnArgs& a, cudaStream_t st) {
     Params p;
     memset(&p, 0, sizeof(p));
     p.a = a;
-    if (!make_tma_2d(&p.mkv, a.cache, (long)a.num_pages * a.page_size, D, D, T)) return cudaErrorInvalidValue;
+    if (!make_tma_chunks(&p.mkv, a.cache, (long)a.num_pages * a.page_size, D, T, NCH)) return cudaErrorInvalidValue;
     cudaError_t e = smem_optin((const void*)attention_tc_kernel, SMEM);
     if (e != cudaSuccess) return e;
     cudaLaunchAttribute attr[2];

@@ -255,6 +255,7 @@ struct TcParams {
     int* err;
 };
 bool make_tma_2d(CUtensorMap* map, const void* ptr, long rows, long cols, long ld, int box_rows);
+bool make_tma_chunks(CUtensorMap* map, const void* ptr, long rows, long cols, int box_rows, int box_chunks);
 int tc_pick_bn(int M);
 cudaError_t launch_tc_gemm(TcParams& p, int bn, int splits, cudaStream_t st);
 

@@ -337,6 +337,21 @@ bool make_tma_2d(CUtensorMap* map, const void* ptr, long rows, long cols, long l
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// A row-major bf16 matrix [rows, cols] viewed as 64-column chunks: dimension 0 the 64 columns of a chunk,
+// dimension 1 the rows, dimension 2 the chunk index (stride 128 B), so one box of box_rows rows and
+// box_chunks chunks lands in shared memory chunk-major: [chunk][row][64 columns], 128-byte swizzled.
+bool make_tma_chunks(CUtensorMap* map, const void* ptr, long rows, long cols, int box_rows, int box_chunks) {
+    auto enc = tma_encoder();
+    if (!enc || !ptr || ((uintptr_t)ptr & 15) || cols % 64) return false;
+    cuuint64_t dims[3] = {64, (cuuint64_t)rows, (cuuint64_t)(cols / 64)};
+    cuuint64_t strides[2] = {(cuuint64_t)cols * 2, 128};
+    cuuint32_t box[3] = {64, (cuuint32_t)box_rows, (cuuint32_t)box_chunks};
+    cuuint32_t estr[3] = {1, 1, 1};
+    return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 template <int BN, int MODE>
 static cudaError_t tc_launch_bn(const TcParams& p, dim3 grid, cudaStream_t st) {
     using C = tc::Cfg<BN, MODE>;
