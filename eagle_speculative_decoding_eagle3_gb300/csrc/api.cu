@@ -190,11 +190,12 @@ void attn_plan(const eagle3_draft& d, int M, int* splits, int* chunk) {
 }
 
 // The tcgen05 latent attention serves the DeepseekV3 geometry in bf16 (128 heads, latent 512, rope 64)
-// with cache pages of a multiple of 64 slots.
-bool attention_tc_ok(const eagle3_draft& d) {
+// with cache pages of a multiple of 64 slots, from kAttnChunkRows rows per call.  Below that (batch-1
+// decode) the mma.sync kernel's lighter launch (no cluster, no TMEM) is the faster one.
+bool attention_tc_ok(const eagle3_draft& d, int M) {
     const eagle3_config_t& c = d.cfg;
-    return c.dtype == EAGLE3_BF16 && c.attention != EAGLE3_ATTN_MHA && c.n_heads == 128 && c.kv_lora_rank == 512 &&
-           c.qk_rope_dim == 64 && c.page_size % 64 == 0;
+    return M >= kAttnChunkRows && c.dtype == EAGLE3_BF16 && c.attention != EAGLE3_ATTN_MHA && c.n_heads == 128 &&
+           c.kv_lora_rank == 512 && c.qk_rope_dim == 64 && c.page_size % 64 == 0;
 }
 
 // Split plan of the tcgen05 attention: fixed chunks of whole 64-slot tiles (splits past a row's context
@@ -747,7 +748,7 @@ cudaError_t run_attention_mla(eagle3_draft& d, eagle3_kv_t* kv, int M, cudaStrea
         aa.M = M; aa.nh = nh; aa.dn = dn; aa.dr = dr; aa.dc = dc; aa.dv = dv;
         aa.sigma = attention_scale(c);
         aa.page_size = c.page_size; aa.max_pages = c.max_pages_per_seq; aa.num_pages = kv->num_pages; aa.err = d.err;
-        const bool tc_attn = attention_tc_ok(d);
+        const bool tc_attn = attention_tc_ok(d, M);
         if (tc_attn) attn_plan_tc(d, M, &aa.splits, &aa.chunk);
         else attn_plan(d, M, &aa.splits, &aa.chunk);
         aa.dt = ra.dt;

@@ -38,6 +38,11 @@ fusion or reordering).  Pins (``tests/test_oracle_*.py``):
                     saturation at 6; the NVFP4 rule restated element by element; the block error bound
   accept_relaxed    rows outside thinking == greedy accept; k = 1 or delta below every gap ==
                     greedy; hand example with the default delta 0.6; monotone in delta
+  accept_typical    one-hot targets reduce it to greedy acceptance; uniform targets give the closed
+                    form 1/V > min(eps, delta / V); the entropy against scipy.stats.entropy and the
+                    identity exp(-H) = prod p^p on a hand distribution; monotone in eps and delta
+  philox4x64_10 /   bit-exact against numpy.random.Philox (an independent implementation of the same
+  philox_uniforms   published generator); uniforms exact in fp32, in [0, 1), mean and variance
   draft_extend /    composition invariants: one T-row extend == T one-row extends
   draft_decode_step (same cache rows and hidden); batch and page-placement independence;
                     residual pass-through with zeroed projections; fc only on 3H input
@@ -50,5 +55,5 @@ from .head import (  # noqa: F401
     softmax_scale, split_kv_b, mla_attention, mha_attention, decoder_rows, final_logits, argmax_lowest,
     top2_gap, d2t_remap, SeqCache, draft_extend, draft_decode_step, draft_round, accept, accept_relaxed,
     sample_filtered, accept_residual, e4m3_decode, e4m3_encode, e4m3_encode_array, quantize_rows_e4m3,
-    e2m1_decode, e2m1_encode_array, quantize_nvfp4,
+    e2m1_decode, e2m1_encode_array, quantize_nvfp4, accept_typical, philox4x64_10, philox_uniforms,
 )

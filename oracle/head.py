@@ -689,3 +689,76 @@ def quantize_nvfp4(W):
     vals = np.where(codes & 8, -1.0, 1.0) * _E2M1_POS[codes & 7]
     deq = vals.reshape(N, K // 16, 16) * _E4M3_ALL[sb][:, :, None] * np.float64(g)
     return codes, sb, g, deq.reshape(N, K)
+
+
+def accept_typical(draft, target_probs, epsilon, delta):
+    """Typical acceptance ([MAX-walkthrough] §10 names "typical-acceptance" among the values of
+    --rejection-sampling-strategy without stating the rule).
+
+    Reading: the published typical-acceptance rule of Medusa (Cai et al. 2024): the drafted token x at
+    position i is accepted when the target's probability of it exceeds min(epsilon, delta exp(-H(p_i))),
+    with H(p_i) = -sum_v p_i(v) ln p_i(v) the entropy (nats) of the target's distribution there.  The
+    accepted length counts leading accepted positions; a token outside the vocabulary is never
+    accepted.  draft [B, G] ids; target_probs [B, G, V].  Returns (acc [B], hist [G + 1])."""
+    draft = np.asarray(draft)
+    p = np.asarray(target_probs, dtype=np.float64)
+    B, G = draft.shape
+    V = p.shape[2]
+    eps, dlt = float(epsilon), float(delta)
+
+    def entropy(q):
+        h = 0.0
+        for v in np.flatnonzero(q > 0):
+            h -= q[v] * math.log(q[v])
+        return h
+
+    acc = np.zeros(B, dtype=np.int32)
+    for b in range(B):
+        k = 0
+        while k < G:
+            x = int(draft[b, k])
+            if not 0 <= x < V:
+                break
+            thr = min(eps, dlt * math.exp(-entropy(p[b, k])))
+            if not p[b, k, x] > thr:
+                break
+            k += 1
+        acc[b] = k
+    hist = np.zeros(G + 1, dtype=np.int32)
+    for k in acc:
+        hist[k] += 1
+    return acc, hist
+
+
+# Philox4x64-10 (Salmon, Moraes, Dror, Shaw: "Parallel random numbers: as easy as 1, 2, 3", SC 2011):
+# ten rounds of two 64 x 64 -> 128-bit multiplications on a 4-word counter, with a 2-word key bumped by
+# the Weyl constants after each round.
+_PHILOX_M = (0xD2E7470EE14C6C93, 0xCA5A826395121157)
+_PHILOX_W = (0x9E3779B97F4A7C15, 0xBB67AE8584CAA73B)
+_U64 = (1 << 64) - 1
+
+
+def philox4x64_10(counter, key):
+    """One Philox4x64-10 block: four 64-bit words from a 4-word counter and a 2-word key."""
+    x = [int(w) & _U64 for w in counter]
+    k0, k1 = int(key[0]) & _U64, int(key[1]) & _U64
+    for _ in range(10):
+        p0 = _PHILOX_M[0] * x[0]
+        p1 = _PHILOX_M[1] * x[2]
+        x = [((p1 >> 64) ^ x[1] ^ k0) & _U64, p1 & _U64, ((p0 >> 64) ^ x[3] ^ k1) & _U64, p0 & _U64]
+        k0 = (k0 + _PHILOX_W[0]) & _U64
+        k1 = (k1 + _PHILOX_W[1]) & _U64
+    return x
+
+
+def philox_uniforms(seed, offset, n):
+    """The stream of uniforms in [0, 1) of the device generator (eagle3_philox_uniforms): element i is
+    word i mod 4 of the Philox4x64-10 block whose counter is the 256-bit integer offset + floor(i / 4)
+    (little-endian words) under key (seed, 0), its top 24 bits scaled by 2^-24 (exact in fp32).
+    Returns float64 values (all exactly representable in float32)."""
+    out = np.zeros(int(n), dtype=np.float64)
+    for i in range(int(n)):
+        c = int(offset) + i // 4
+        words = philox4x64_10([(c >> (64 * j)) & _U64 for j in range(4)], (int(seed), 0))
+        out[i] = (words[i % 4] >> 40) * 2.0 ** -24
+    return out

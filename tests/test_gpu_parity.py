@@ -59,13 +59,14 @@ MLA128 = dict(hidden=1024, n_heads=128, q_lora_rank=256, intermediate=2048, targ
 
 
 @pytest.mark.parametrize("over", [
-    # GEMV decode (3 rows), tensor-core extend (9 rows); ragged contexts over several splits and pages
-    dict(batch=3, ctx=(100, 700), t_new=3, gamma=4, accept_p=(0.7,) * 4, seed=85),
+    # GEMV decode (3 rows, mma.sync attention), tensor-core extend (18 rows, tcgen05 attention); ragged
+    # contexts over several splits and pages
+    dict(batch=3, ctx=(100, 700), t_new=6, gamma=4, accept_p=(0.7,) * 4, seed=85),
     # every call on the tensor-core path (24 and 48 rows)
     dict(batch=24, ctx=(30, 700), t_new=2, gamma=3, accept_p=(0.7,) * 3, seed=86),
-    # contexts short enough for a single split (o_lat written by the attention kernel itself)
-    dict(batch=3, ctx=(3, 20), t_new=5, gamma=3, accept_p=(0.7,) * 3, seed=87),
-    # extend on an empty cache: causal attention among the new rows only
+    # contexts short enough for a single split (o_lat written by the attention kernel itself), 20 rows
+    dict(batch=4, ctx=(3, 20), t_new=5, gamma=3, accept_p=(0.7,) * 3, seed=87),
+    # extend on an empty cache: causal attention among the new rows only (18 rows)
     dict(batch=2, ctx=(0, 0), t_new=9, gamma=3, accept_p=(0.7,) * 3, seed=88),
 ])
 def test_mla_128_heads_tensor_core_attention(over):

@@ -565,3 +565,102 @@ def test_quantize_nvfp4_rule_and_error_bound():
                 continue
             err = np.abs(deq[n, 16 * b:16 * b + 16] - blk)
             assert np.all(err <= np.maximum(np.abs(blk) * 0.25, 0.25 * eff) * (1 + 1e-6) + 1e-12)
+
+
+# ---- typical acceptance (Medusa's rule, a reading of the strategy named in the MAX walkthrough §10)
+def test_accept_typical_one_hot_targets_reduce_to_greedy():
+    # a one-hot target distribution has zero entropy: the threshold is min(eps, delta) < 1, so a drafted
+    # token is accepted exactly when it is the target's argmax
+    rng = np.random.default_rng(31)
+    B, G, V = 30, 5, 17
+    tgt = rng.integers(0, V, size=(B, G))
+    p = np.zeros((B, G, V))
+    p[np.arange(B)[:, None], np.arange(G)[None, :], tgt] = 1.0
+    draft = np.where(rng.random((B, G)) < 0.75, tgt, (tgt + 1 + rng.integers(0, V - 1, size=(B, G))) % V)
+    for eps, dlt in ((0.09, 0.3), (0.5, 0.9), (0.99, 0.01)):
+        acc, hist = O.accept_typical(draft, p, eps, dlt)
+        g_acc, g_hist = O.accept(draft, tgt)
+        np.testing.assert_array_equal(acc, g_acc)
+        np.testing.assert_array_equal(hist, g_hist)
+
+
+def test_accept_typical_uniform_target_closed_form():
+    # uniform over V: H = ln V, so the threshold is min(eps, delta / V) and p(x) = 1 / V; acceptance
+    # happens exactly when delta < 1 or eps < 1 / V
+    V = 10
+    p = np.full((1, 1, V), 1.0 / V)
+    for eps, dlt, want in ((0.09, 0.3, 1), (0.5, 1.5, 0), (0.05, 1.5, 1), (0.5, 0.99, 1), (0.2, 2.0, 0)):
+        acc, _ = O.accept_typical([[3]], p, eps, dlt)
+        assert acc[0] == want, (eps, dlt)
+
+
+def test_accept_typical_entropy_against_library_and_product_identity():
+    import scipy.stats
+    # two-point distribution (0.9, 0.1): exp(-H) = 0.9^0.9 * 0.1^0.1 = 0.72247... (product identity)
+    q = np.array([0.9, 0.1, 0.0])
+    e_minus_h = 0.9 ** 0.9 * 0.1 ** 0.1
+    assert abs(math.exp(-scipy.stats.entropy(q)) - e_minus_h) < 1e-15
+    p = q[None, None, :]
+    # delta exp(-H) just above / below p(x) = 0.1 decides the minority token
+    dlt_hi = 0.1 / e_minus_h * (1 + 1e-9)
+    dlt_lo = 0.1 / e_minus_h * (1 - 1e-9)
+    assert O.accept_typical([[1]], p, 1.0, dlt_hi)[0][0] == 0
+    assert O.accept_typical([[1]], p, 1.0, dlt_lo)[0][0] == 1
+    # random distributions: the rule evaluated with scipy's entropy gives the same lengths
+    rng = np.random.default_rng(32)
+    B, G, V = 25, 4, 40
+    p = rng.dirichlet(np.ones(V) * 0.2, size=(B, G))
+    draft = np.argsort(-p, axis=2)[:, :, 0]
+    draft = np.where(rng.random((B, G)) < 0.5, draft, rng.integers(0, V, size=(B, G)))
+    eps, dlt = 0.09, 0.3
+    want = np.zeros(B, dtype=np.int32)
+    for b in range(B):
+        k = 0
+        while k < G and p[b, k, draft[b, k]] > min(eps, dlt * math.exp(-scipy.stats.entropy(p[b, k]))):
+            k += 1
+        want[b] = k
+    np.testing.assert_array_equal(O.accept_typical(draft, p, eps, dlt)[0], want)
+
+
+def test_accept_typical_monotone_in_thresholds():
+    rng = np.random.default_rng(33)
+    B, G, V = 40, 6, 30
+    p = rng.dirichlet(np.ones(V) * 0.5, size=(B, G))
+    draft = rng.integers(0, V, size=(B, G))
+    prev = None
+    for eps in (0.5, 0.2, 0.09, 0.03, 0.0):
+        acc, hist = O.accept_typical(draft, p, eps, 0.3)
+        assert hist.sum() == B
+        if prev is not None:
+            assert np.all(acc >= prev)
+        prev = acc
+    # a token outside the vocabulary is never accepted
+    assert O.accept_typical([[V + 2]], p[:1, :1], 0.0, 0.0)[0][0] == 0
+
+
+# ---- Philox4x64-10 (the device generator of the sampled rounds' uniforms)
+def test_philox_matches_numpy_philox():
+    # numpy.random.Philox is an independent implementation of the same generator; it increments its
+    # counter before producing each block
+    U64 = (1 << 64) - 1
+    for key in ([0, 0], [123, 456], [U64, 7], [0xdeadbeefcafebabe, 0x0123456789abcdef]):
+        for ctr in ([0, 0, 0, 0], [5, 0, 0, 0], [U64 - 2, 0, 0, 0], [U64, U64, 3, 9]):
+            g = np.random.Philox(counter=np.array(ctr, dtype=np.uint64), key=np.array(key, dtype=np.uint64))
+            raw = [int(x) for x in g.random_raw(8)]
+            c = ctr[0] + (ctr[1] << 64) + (ctr[2] << 128) + (ctr[3] << 192)
+            blocks = []
+            for j in (1, 2):
+                cj = (c + j) & ((1 << 256) - 1)
+                blocks += O.philox4x64_10([(cj >> (64 * w)) & U64 for w in range(4)], key)
+            assert blocks == raw, (key, ctr)
+
+
+def test_philox_uniform_stream_properties():
+    u = O.philox_uniforms(2024, 0, 4000)
+    assert np.all(u >= 0.0) and np.all(u < 1.0)
+    np.testing.assert_array_equal(u.astype(np.float32).astype(np.float64), u)      # exact in fp32
+    assert abs(u.mean() - 0.5) < 0.02 and abs(u.var() - 1.0 / 12) < 0.01
+    # element i of (seed, offset) is element i + 4 * offset of (seed, 0)
+    np.testing.assert_array_equal(O.philox_uniforms(2024, 3, 20), u[12:32])
+    # a different seed gives a different stream
+    assert not np.array_equal(O.philox_uniforms(2025, 0, 64), u[:64])
