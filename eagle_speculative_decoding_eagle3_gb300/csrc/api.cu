@@ -1182,6 +1182,23 @@ eagle3_status_t eagle3_sample(const float* logits, int32_t rows, int32_t V, int6
     return EAGLE3_OK;
 }
 
+eagle3_status_t eagle3_accept_typical(const int32_t* draft, const float* target_probs, int32_t batch, int32_t gamma,
+                                      int32_t V, float epsilon, float delta, int32_t* accepted_len, int32_t* hist,
+                                      void* stream) {
+    if (!draft || !target_probs || !accepted_len) return EAGLE3_ERR_INVALID_ARG;
+    if (batch < 1 || gamma < 1 || gamma > 4096 || V < 1 || !(epsilon >= 0.f) || !(delta >= 0.f))
+        return EAGLE3_ERR_INVALID_ARG;
+    E3_CUDA(launch_accept_typical(draft, target_probs, batch, gamma, V, epsilon, delta, accepted_len, hist,
+                                  (cudaStream_t)stream));
+    return EAGLE3_OK;
+}
+
+eagle3_status_t eagle3_philox_uniforms(uint64_t seed, uint64_t offset, int64_t n, float* out, void* stream) {
+    if (n < 0 || (n > 0 && !out)) return EAGLE3_ERR_INVALID_ARG;
+    E3_CUDA(launch_philox_uniforms(seed, offset, (long)n, out, (cudaStream_t)stream));
+    return EAGLE3_OK;
+}
+
 eagle3_status_t eagle3_accept_residual(const int32_t* draft, const float* draft_probs, const float* target_probs,
                                        const float* u_accept, const float* u_resample, int32_t batch, int32_t gamma,
                                        int32_t V, int32_t* accepted_len, int32_t* next_token, int32_t* hist,

@@ -135,6 +135,11 @@ struct ResidualArgs {
 };
 cudaError_t launch_sample(const SampleArgs& s, cudaStream_t st);
 cudaError_t launch_accept_residual(const ResidualArgs& a, cudaStream_t st);
+// typical acceptance: accept x while p(x) > min(epsilon, delta exp(-H(p))); target_probs [B, gamma, V]
+cudaError_t launch_accept_typical(const int* draft, const float* target_probs, int batch, int gamma, int V,
+                                  float epsilon, float delta, int* accepted_len, int* hist, cudaStream_t st);
+// out[i] = uniform i of the Philox4x64-10 stream (seed, offset), i < n
+cudaError_t launch_philox_uniforms(uint64_t seed, uint64_t offset, long n, float* out, cudaStream_t st);
 
 // ---------------------------------------------------------------- causal attention of a long extend
 // (unabsorbed; DeepseekV3 geometry d_n 128, d_r 64, d_v 128)

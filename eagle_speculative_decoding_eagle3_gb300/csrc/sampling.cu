@@ -433,6 +433,78 @@ __global__ void __launch_bounds__(smp::kThreads) accept_residual_kernel(Residual
     }
 }
 
+// Typical acceptance: the published rule of Medusa (Cai et al. 2024), read for the "typical-acceptance"
+// strategy that "Eagle3 DeepseekV3 in MAX" §10 names: position i accepts its drafted token x while
+// p_i(x) > min(epsilon, delta exp(-H(p_i))), H the entropy (nats) of the target's distribution there.
+// One CTA per sequence; the entropy of each position is a block reduction (fp32, log of each positive
+// probability), and the walk stops at the first rejection.
+__global__ void __launch_bounds__(smp::kThreads)
+accept_typical_kernel(const int* draft, const float* target_probs, int gamma, int V, float epsilon, float delta,
+                      int* accepted_len) {
+    pdl_trigger();
+    pdl_wait();
+    __shared__ float red[32];
+    __shared__ int decision;
+    const int b = blockIdx.x, t = threadIdx.x;
+    int k = 0;
+    for (; k < gamma; ++k) {
+        const long pos = (long)b * gamma + k;
+        const int x = draft[pos];
+        if (x < 0 || x >= V) break;          // an id outside the vocabulary is never accepted
+        const float* p = target_probs + pos * V;
+        float h = 0.f;
+        for (int v = t; v < V; v += blockDim.x) {
+            const float q = p[v];
+            if (q > 0.f) h -= q * logf(q);
+        }
+        h = block_sum(h, red);
+        if (t == 0) decision = p[x] > fminf(epsilon, delta * expf(-h)) ? 1 : 0;
+        __syncthreads();
+        const int ok = decision;
+        __syncthreads();
+        if (!ok) break;
+    }
+    if (t == 0) accepted_len[b] = k;
+}
+
+// Philox4x64-10 (Salmon, Moraes, Dror, Shaw, "Parallel random numbers: as easy as 1, 2, 3", SC 2011): ten
+// rounds of two 64 x 64 -> 128-bit products over a 4-word counter; the 2-word key is bumped by the Weyl
+// constants after each round.
+__device__ __forceinline__ void philox4x64_10(uint64_t* c, uint64_t k0, uint64_t k1) {
+    constexpr uint64_t M0 = 0xD2E7470EE14C6C93ull, M1 = 0xCA5A826395121157ull;
+    constexpr uint64_t W0 = 0x9E3779B97F4A7C15ull, W1 = 0xBB67AE8584CAA73Bull;
+#pragma unroll
+    for (int round = 0; round < 10; ++round) {
+        const uint64_t hi0 = __umul64hi(M0, c[0]), lo0 = M0 * c[0];
+        const uint64_t hi1 = __umul64hi(M1, c[2]), lo1 = M1 * c[2];
+        const uint64_t x0 = hi1 ^ c[1] ^ k0, x2 = hi0 ^ c[3] ^ k1;
+        c[0] = x0; c[1] = lo1; c[2] = x2; c[3] = lo0;
+        k0 += W0;
+        k1 += W1;
+    }
+}
+
+// out[i] = word i % 4 of the block whose counter is the 256-bit integer offset + i / 4, key (seed, 0): its
+// top 24 bits times 2^-24, a uniform in [0, 1) that fp32 holds exactly.  One block per thread.
+__global__ void philox_uniforms_kernel(uint64_t seed, uint64_t offset, long n, float* out) {
+    pdl_trigger();
+    pdl_wait();
+    const long nb = (n + 3) / 4;
+    for (long j = (long)blockIdx.x * blockDim.x + threadIdx.x; j < nb; j += (long)gridDim.x * blockDim.x) {
+        uint64_t c[4];
+        c[0] = offset + (uint64_t)j;
+        c[1] = c[0] < offset ? 1ull : 0ull;   // carry into the next counter word
+        c[2] = 0;
+        c[3] = 0;
+        philox4x64_10(c, seed, 0);
+#pragma unroll
+        for (int w = 0; w < 4; ++w) {
+            const long i = 4 * j + w;
+            if (i < n) out[i] = (float)(uint32_t)(c[w] >> 40) * 0x1p-24f;
+        }
+    }
+}
+
 __global__ void acceptance_hist_kernel(const int* acc, int batch, int gamma, int* hist) {
     pdl_trigger();
     pdl_wait();
@@ -455,6 +527,25 @@ cudaError_t launch_sample(const SampleArgs& s, cudaStream_t st) {
     const bool cached = s.temperature > 0.f && s.top_k > 0 && s.V <= smp::kKeyCache;
     const size_t smem = cached ? (size_t)s.V * sizeof(uint32_t) : 0;
     return launch_pdl(sample_kernel, dim3(s.rows), dim3(smp::kThreads), smem, st, s);
+}
+
+cudaError_t launch_accept_typical(const int* draft, const float* target_probs, int batch, int gamma, int V,
+                                  float epsilon, float delta, int* accepted_len, int* hist, cudaStream_t st) {
+    if (batch < 1 || gamma < 1 || V < 1) return cudaErrorInvalidValue;
+    cudaError_t e = launch_pdl(accept_typical_kernel, dim3(batch), dim3(smp::kThreads), 0, st, draft, target_probs, gamma, V,
+                               epsilon, delta, accepted_len);
+    if (e != cudaSuccess || !hist) return e;
+    return launch_pdl(acceptance_hist_kernel, dim3(1), dim3(256), (gamma + 1) * sizeof(int), st, (const int*)accepted_len,
+                      batch, gamma, hist);
+}
+
+cudaError_t launch_philox_uniforms(uint64_t seed, uint64_t offset, long n, float* out, cudaStream_t st) {
+    if (n < 0) return cudaErrorInvalidValue;
+    if (n == 0) return cudaSuccess;
+    const long nb = (n + 3) / 4;
+    const long blocks = (nb + 255) / 256;
+    return launch_pdl(philox_uniforms_kernel, dim3((unsigned)(blocks < 1184 ? blocks : 1184)), dim3(256), 0, st, seed,
+                      offset, n, out);
 }
 
 cudaError_t launch_accept_residual(const ResidualArgs& a, cudaStream_t st) {

@@ -87,6 +87,8 @@ def _lib():
         lib.eagle3_sample.argtypes = [P, C.c_int32, C.c_int32, C.c_int64, C.POINTER(eagle3_sampling_t), P, P,
                                       C.c_int32, P, P, P, C.c_int32, C.c_int32, P]
         lib.eagle3_accept_residual.argtypes = [P, P, P, P, P, C.c_int32, C.c_int32, C.c_int32, P, P, P, P]
+        lib.eagle3_accept_typical.argtypes = [P, P, C.c_int32, C.c_int32, C.c_int32, C.c_float, C.c_float, P, P, P]
+        lib.eagle3_philox_uniforms.argtypes = [C.c_uint64, C.c_uint64, C.c_int64, P, P]
         lib.eagle3_draft_decode_sampled.argtypes = [P, C.c_int32, P, C.POINTER(eagle3_kv_t),
                                                     C.POINTER(eagle3_sampling_t), P, P, P, P, C.c_int32, C.c_int32,
                                                     P, P, P]
@@ -103,7 +105,7 @@ def _lib():
         lib.eagle3_draft_profile_reset.argtypes = [P]
         for f in ("eagle3_draft_profile_enable", "eagle3_draft_profile_read", "eagle3_draft_profile_reset",
                   "eagle3_draft_create", "eagle3_draft_workspace_bytes", "eagle3_draft_extend", "eagle3_draft_decode",
-                  "eagle3_accept", "eagle3_accept_relaxed", "eagle3_sample", "eagle3_accept_residual", "eagle3_draft_decode_sampled", "eagle3_linear", "eagle3_linear_noalloc", "eagle3_draft_get_error", "eagle3_draft_clear_error", "eagle3_draft_destroy"):
+                  "eagle3_accept", "eagle3_accept_relaxed", "eagle3_sample", "eagle3_accept_residual", "eagle3_accept_typical", "eagle3_philox_uniforms", "eagle3_draft_decode_sampled", "eagle3_linear", "eagle3_linear_noalloc", "eagle3_draft_get_error", "eagle3_draft_clear_error", "eagle3_draft_destroy"):
             getattr(lib, f).restype = C.c_int
         _L = lib
     return _L
@@ -252,6 +254,17 @@ def eagle3_accept_residual(draft, draft_probs, target_probs, u_accept, u_resampl
     _check("eagle3_accept_residual", _lib().eagle3_accept_residual(
         _ptr(draft), _ptr(draft_probs), _ptr(target_probs), _ptr(u_accept), _ptr(u_resample), int(batch),
         int(gamma), int(V), _ptr(accepted_len), _ptr(next_token), _ptr(hist), _stream(stream)))
+
+
+def eagle3_accept_typical(draft, target_probs, batch, gamma, V, epsilon, delta, accepted_len, hist=None, stream=None):
+    _check("eagle3_accept_typical", _lib().eagle3_accept_typical(
+        _ptr(draft), _ptr(target_probs), int(batch), int(gamma), int(V), float(epsilon), float(delta),
+        _ptr(accepted_len), _ptr(hist), _stream(stream)))
+
+
+def eagle3_philox_uniforms(seed, offset, n, out, stream=None):
+    _check("eagle3_philox_uniforms", _lib().eagle3_philox_uniforms(
+        int(seed), int(offset), int(n), _ptr(out), _stream(stream)))
 
 
 def eagle3_draft_get_error(handle) -> int:

@@ -361,6 +361,33 @@ EAGLE3_API eagle3_status_t eagle3_accept_residual(const int32_t *draft, const fl
                                                   int32_t *accepted_len, int32_t *next_token, int32_t *hist,
                                                   void *stream);
 
+/* Typical acceptance ("Eagle3 DeepseekV3 in MAX" §10 names the typical-acceptance strategy of
+ * --rejection-sampling-strategy without stating it; the rule here is the published one of Medusa, Cai
+ * et al. 2024): position i of sequence b accepts its drafted token x while
+ *   p_i(x) > min(epsilon, delta * exp(-H(p_i))),   H(p_i) = -sum_v p_i(v) ln p_i(v)  (nats),
+ * p_i the target's distribution at that position; accepted_len[b] = number of leading accepted positions
+ * (0..gamma); an id outside [0, V) is never accepted.  No bonus token is drawn: the caller takes the
+ * target's own next token, as for greedy acceptance.  Medusa's defaults are epsilon 0.09, delta 0.3.
+ *   draft         [batch, gamma] int32 target-vocabulary ids
+ *   target_probs  [batch, gamma, V] fp32
+ *   accepted_len  [batch] int32 out; hist [gamma + 1] int32 out or NULL, as in eagle3_accept
+ * One CTA per sequence; the entropy is summed in fp32.  Returns EAGLE3_ERR_INVALID_ARG for null required
+ * pointers, batch, gamma or V < 1, gamma > 4096, or a negative (or NaN) epsilon or delta. */
+EAGLE3_API eagle3_status_t eagle3_accept_typical(const int32_t *draft, const float *target_probs, int32_t batch,
+                                                 int32_t gamma, int32_t V, float epsilon, float delta,
+                                                 int32_t *accepted_len, int32_t *hist, void *stream);
+
+/* Device uniforms from a seed and a counter ("Eagle3 DeepseekV3 in MAX" §8: a seed counter feeds the
+ * sampler), so a sampled round draws its random numbers without a host copy.  The generator is
+ * Philox4x64-10 (Salmon, Moraes, Dror, Shaw, "Parallel random numbers: as easy as 1, 2, 3", SC 2011):
+ * out[i] is word i mod 4 of the block whose 256-bit counter is offset + floor(i / 4) (little-endian
+ * 64-bit words) under the key (seed, 0), its top 24 bits times 2^-24 (a value in [0, 1) exact in fp32).
+ * Successive calls take fresh numbers by advancing offset by ceil(n / 4).
+ *   out  [n] fp32 out (device memory)
+ * Returns EAGLE3_ERR_INVALID_ARG for n < 0 or a null out with n > 0; n == 0 launches nothing. */
+EAGLE3_API eagle3_status_t eagle3_philox_uniforms(uint64_t seed, uint64_t offset, int64_t n, float *out,
+                                                  void *stream);
+
 /* Per-row FP8 E4M3 quantization of one weight matrix (the drafter's post-training FP8 quantization,
  * "EAGLE head deep dive", deployment; the form EAGLE3_WEIGHTS_FP8 reads).  For every row n of w:
  *   scale[n] = max_k |w[n, k]| / 448 in fp32 (1 for an all-zero row),

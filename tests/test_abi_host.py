@@ -89,6 +89,24 @@ def test_accept_relaxed_rejects_bad_arguments(lib):
         assert ei.value.status == E.ERR_INVALID_ARG, kw
 
 
+def test_typical_acceptance_and_uniforms_reject_bad_arguments(lib):
+    for kw in [dict(draft=None), dict(probs=None), dict(batch=0), dict(gamma=0), dict(V=0), dict(eps=-0.1),
+               dict(dlt=float("nan")), dict(acc=None)]:
+        args = dict(draft=16, probs=16, batch=2, gamma=3, V=10, eps=0.09, dlt=0.3, acc=16)
+        args.update(kw)
+        with pytest.raises(E.Eagle3Error) as ei:
+            E.eagle3_accept_typical(args["draft"], args["probs"], args["batch"], args["gamma"], args["V"], args["eps"],
+                                    args["dlt"], args["acc"])
+        assert ei.value.status == E.ERR_INVALID_ARG, kw
+    with pytest.raises(E.Eagle3Error) as ei:
+        E.eagle3_philox_uniforms(1, 0, -1, 16)
+    assert ei.value.status == E.ERR_INVALID_ARG
+    with pytest.raises(E.Eagle3Error) as ei:
+        E.eagle3_philox_uniforms(1, 0, 8, None)
+    assert ei.value.status == E.ERR_INVALID_ARG
+    E.eagle3_philox_uniforms(1, 0, 0, None)   # nothing to draw: no launch, no GPU needed
+
+
 def test_fp8_weight_format_checks_without_a_gpu(lib):
     # the format must be known, FP8 needs bf16 storage, and extends above the GEMV rows reserve the
     # bf16 expansion of the largest FP8 matrix pair (gate | up: 2 x 18432 x 7168 elements)

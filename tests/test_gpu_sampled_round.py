@@ -17,7 +17,7 @@ pytestmark = pytest.mark.gpu
 EPS = 1e-4
 
 
-def _sampled_round(w, T, k, p, seed, tol):
+def _sampled_round(w, T, k, p, seed, tol, philox_seed=None):
     from eagle_speculative_decoding_eagle3_gb300 import build
     from eagle_speculative_decoding_eagle3_gb300 import eagle3 as E
     from eagle_speculative_decoding_eagle3_gb300 import harness as HN
@@ -31,6 +31,16 @@ def _sampled_round(w, T, k, p, seed, tol):
     B, G, H, Vd, Vt = w.batch, w.gamma, w.hidden, w.draft_vocab, w.target_vocab
     rng = np.random.default_rng(seed)
     u = rng.random((G, B)).astype(np.float32)
+    u_dev = torch.from_numpy(u).cuda()
+    if philox_seed is not None:
+        # the draws come from the device generator (no host copy); the oracle takes the same stream from
+        # its own statement of the generator
+        u_dev = torch.empty(G * B, dtype=torch.float32, device="cuda")
+        E.eagle3_philox_uniforms(philox_seed, 0, G * B, u_dev)
+        u = O.philox_uniforms(philox_seed, 0, G * B).astype(np.float32).reshape(G, B)
+        torch.cuda.synchronize()
+        np.testing.assert_array_equal(u_dev.cpu().numpy().reshape(G, B), u)
+        u_dev = u_dev.view(G, B)
     head = HN.DeviceHead(w, stored)
     try:
         dc = head.cache(paged)
@@ -41,7 +51,7 @@ def _sampled_round(w, T, k, p, seed, tol):
         probs = torch.zeros((B, G, Vt), dtype=torch.float32, device="cuda")
         d2t_dev = HN.to_device(d2t) if d2t is not None else None
         head.extend(din, dc, hidden_out=hid[0], logits_out=lg[0])
-        head.decode_sampled(G, d2t_dev, dc, T, k, p, lg[0], torch.from_numpy(u).cuda(), toks, probs, Vt, True,
+        head.decode_sampled(G, d2t_dev, dc, T, k, p, lg[0], u_dev, toks, probs, Vt, True,
                             hidden_out=hid[1:] if G > 1 else None, logits_out=lg[1:] if G > 1 else None)
         torch.cuda.synchronize()
         assert head.error_word() == 0
@@ -53,6 +63,10 @@ def _sampled_round(w, T, k, p, seed, tol):
             tp[b, 0] = q[b, 0]
         ua = rng.random((B, G)).astype(np.float32)
         ur = rng.random((B, G)).astype(np.float32)
+        if philox_seed is not None:
+            off = (G * B + 3) // 4
+            ua = O.philox_uniforms(philox_seed, off, B * G).astype(np.float32).reshape(B, G)
+            ur = O.philox_uniforms(philox_seed, off + (B * G + 3) // 4, B * G).astype(np.float32).reshape(B, G)
         acc = torch.zeros(B, dtype=torch.int32, device="cuda")
         nxt = torch.zeros(B, dtype=torch.int32, device="cuda")
         hist = torch.zeros(G + 1, dtype=torch.int32, device="cuda")
@@ -101,6 +115,12 @@ def test_mla_shaped_bf16_sampled_round():
     w = WL.workload("dsv3_b1", hidden=1024, n_heads=8, q_lora_rank=256, intermediate=2048, target_vocab=8192,
                     draft_vocab=4096, batch=3, ctx=(100, 700), t_new=2, gamma=4, accept_p=(0.7,) * 4, seed=83)
     _sampled_round(w, 0.7, 20, 0.8, 33, TOL_BF16)
+
+
+def test_tiny_f32_sampled_round_device_uniforms():
+    # every uniform of the round from the device Philox stream (seed counter): no host draw
+    w = WL.workload("tiny_f32", gamma=4, accept_p=(0.7,) * 4, seed=1002)
+    _sampled_round(w, 0.9, 40, 0.95, 35, TOL_F32, philox_seed=0x5EED)
 
 
 def test_mha_tiny_f32_sampled_round():

@@ -136,3 +136,52 @@ def test_sample_top_k_boundary_on_ties(k):
         np.testing.assert_array_equal(probs[r] > 0, pr_o > 0)      # the same kept set, ties included
         if tok[r] != t_o:
             assert tok[r] in _allowed(l[r], 1.0, k, 1.0, float(u[r])), (r, tok[r], t_o)
+
+
+@pytest.mark.parametrize("seed,offset,n", [(0, 0, 1), (7, 0, 10001), (0xDEADBEEFCAFEBABE, 12345, 4099),
+                                           (3, (1 << 64) - 3, 33)])
+def test_philox_uniforms_match_oracle(seed, offset, n):
+    # bit-exact against the oracle's statement of the stream; the last case carries into counter word 1
+    from eagle_speculative_decoding_eagle3_gb300 import build
+    from eagle_speculative_decoding_eagle3_gb300 import eagle3 as E
+    build.build()
+    out = torch.full((n + 5,), -1.0, dtype=torch.float32, device="cuda")
+    E.eagle3_philox_uniforms(seed, offset, n, out)
+    torch.cuda.synchronize()
+    got = out.cpu().numpy()
+    np.testing.assert_array_equal(got[:n].astype(np.float64), O.philox_uniforms(seed, offset, n))
+    assert np.all(got[n:] == -1.0)                     # nothing past n is written
+
+
+def _typical_case(seed, B, G, V, conc):
+    rng = np.random.default_rng(seed)
+    p = rng.dirichlet(np.ones(V) * conc, size=(B, G)).astype(np.float32)
+    best = np.argmax(p, axis=2)
+    draft = np.where(rng.random((B, G)) < 0.7, best, rng.integers(0, V, size=(B, G)))
+    draft[0, :] = best[0, :]                          # a row that accepts through its whole length
+    draft[1, 0] = V + 5                               # an id outside the vocabulary
+    return draft.astype(np.int32), p
+
+
+@pytest.mark.parametrize("B,G,V,conc,eps,dlt", [(37, 5, 777, 0.3, 0.09, 0.3), (9, 7, 32000, 0.05, 0.09, 0.3),
+                                                (64, 3, 129, 2.0, 0.3, 0.9), (5, 2, 1000, 0.01, 0.0, 0.0)])
+def test_accept_typical_matches_oracle(B, G, V, conc, eps, dlt):
+    # the entropy is an fp32 sum on the GPU and an fp64 one in the oracle: where a probability sits within
+    # 1e-4 (relative) of its threshold either decision is accepted, i.e. the GPU length lies between the
+    # oracle's lengths with both thresholds scaled by 1 + 1e-4 and by 1 - 1e-4
+    from eagle_speculative_decoding_eagle3_gb300 import build
+    from eagle_speculative_decoding_eagle3_gb300 import eagle3 as E
+    build.build()
+    draft, p = _typical_case(B * 7 + V, B, G, V, conc)
+    acc = torch.full((B,), -1, dtype=torch.int32, device="cuda")
+    hist = torch.full((G + 1,), -1, dtype=torch.int32, device="cuda")
+    E.eagle3_accept_typical(torch.from_numpy(draft).cuda(), torch.from_numpy(p).cuda(), B, G, V, eps, dlt, acc, hist)
+    torch.cuda.synchronize()
+    acc, hist = acc.cpu().numpy(), hist.cpu().numpy()
+    want, _ = O.accept_typical(draft, p, np.float32(eps), np.float32(dlt))
+    lo, _ = O.accept_typical(draft, p, np.float32(eps) * (1 + 1e-4), np.float32(dlt) * (1 + 1e-4))
+    hi, _ = O.accept_typical(draft, p, np.float32(eps) * (1 - 1e-4), np.float32(dlt) * (1 - 1e-4))
+    assert np.all((acc >= lo) & (acc <= hi)), (acc, want)
+    assert np.mean(acc == want) >= 0.9
+    np.testing.assert_array_equal(hist, np.bincount(acc, minlength=G + 1))
+    assert acc[0] == want[0] and acc[1] == 0
