@@ -397,12 +397,13 @@ def run_ours(args, ws, rank, local):
         Vt = w.target_vocab if d2t is not None else w.draft_vocab
         gen = torch.Generator(device="cuda").manual_seed(1234)
         lg0 = torch.empty((B, w.draft_vocab), dtype=torch.float32, device="cuda")
-        u_draw = torch.rand((G, B), generator=gen, device="cuda")
+        # every uniform of a round comes from the device Philox stream (the sampler's seed counter)
+        u_draw = torch.empty((G, B), dtype=torch.float32, device="cuda")
+        u_acc = torch.empty((B, G), dtype=torch.float32, device="cuda")
+        u_res = torch.empty((B, G), dtype=torch.float32, device="cuda")
         q_probs = torch.empty((B, G, Vt), dtype=torch.float32, device="cuda")
         tprobs = torch.rand((B, G + 1, Vt), generator=gen, device="cuda") ** 4
         tprobs /= tprobs.sum(dim=2, keepdim=True)
-        u_acc = torch.rand((B, G), generator=gen, device="cuda")
-        u_res = torch.rand((B, G), generator=gen, device="cuda")
         nxt = torch.zeros(B, dtype=torch.int32, device="cuda")
 
     def run_round(st, dev_in):
@@ -412,6 +413,10 @@ def run_ours(args, ws, rank, local):
             head.decode(G, d2t_dev, cache, toks, stream=st)
             E.eagle3_accept(toks, tgt, B, G, acc, hist, stream=st)
             return
+        n = G * B
+        E.eagle3_philox_uniforms(1234, 0, n, u_draw, stream=st)
+        E.eagle3_philox_uniforms(1234, (n + 3) // 4, n, u_acc, stream=st)
+        E.eagle3_philox_uniforms(1234, 2 * ((n + 3) // 4), n, u_res, stream=st)
         head.extend(dev_in, cache, logits_out=lg0, stream=st)
         head.decode_sampled(G, d2t_dev, cache, sampling[0], sampling[1], sampling[2], lg0, u_draw, toks, q_probs,
                             q_probs.shape[2], d2t is not None, stream=st)
@@ -471,7 +476,9 @@ def run_ours(args, ws, rank, local):
     ms = ev0.elapsed_time(ev1)
     ms_max = reduce_max(ms, ws)
     prof_dom, launches = read_profile()
-    launches += args.steps  # one acceptance launch per round
+    # launches outside the handle per round: greedy acceptance (one kernel); sampled rounds also draw
+    # three uniform arrays and run residual acceptance with its histogram
+    launches += args.steps * (1 if sampling is None else 5)
     assert head.error_word() == 0
     del graph
     # every round drafts the same tokens against the same targets, so the last round's acceptance is
@@ -526,8 +533,9 @@ def run_ours(args, ws, rank, local):
     o_acc = torch.empty(B, dtype=torch.int32).pin_memory()
     o_hist = torch.empty(G + 1, dtype=torch.int32).pin_memory()
     d_in = {k: (v if k != "aux" else list(v)) for k, v in din.items()}
-    # sampled rounds also bring the uniforms and the target distributions from the host
-    h_samp = [] if sampling is None else [(t, pin(t)) for t in (u_draw, tprobs, u_acc, u_res)]
+    # sampled rounds also bring the target distributions from the host (their uniforms are drawn on the
+    # device)
+    h_samp = [] if sampling is None else [(tprobs, pin(tprobs))]
     h2d = sum(a.numel() * a.element_size() for a in h_aux) + sum(
         t.numel() * t.element_size() for t in (h_tok, h_pos, h_ro, h_tgt)) + sum(
         h.numel() * h.element_size() for _, h in h_samp)

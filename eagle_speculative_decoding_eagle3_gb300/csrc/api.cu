@@ -769,6 +769,12 @@ cudaError_t run_attention_mla(eagle3_draft& d, eagle3_kv_t* kv, int M, cudaStrea
         // o_h = W_UV,h o_lat,h over the value rows of kv_b
         if (tc) aa.olat_bf = d.olat_bf; else aa.olat = d.olat;
         E3_TRY(traced(d, K_ATTN, st, [&] { return tc_attn ? launch_attention_tc(aa, st) : launch_attention(aa, st); }));
+        // few rows with split partials: the merge and the value up-projection in one kernel
+        const bool fused = !tc && aa.splits > 1 && merge_unabsorb_supported(aa);
+        if (fused) {
+            E3_TRY(traced(d, K_UNABSORB, st, [&] { return launch_merge_unabsorb(aa, st); }));
+            return cudaSuccess;
+        }
         if (aa.splits > 1) E3_TRY(traced(d, K_COMBINE, st, [&] { return launch_merge(aa, st); }));
         if (tc) {
             E3_TRY(run_batched(d, K_UNABSORB, M, d.olat_bf, (long)nh * dc, dc, w.kv_b, (long)nh * (dn + dv), dn, dn + dv,

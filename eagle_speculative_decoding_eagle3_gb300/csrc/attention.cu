@@ -20,6 +20,7 @@
 #include "common.cuh"
 #include "kernels.h"
 #include "mma_sync.cuh"
+#include "../../include/eagle3.h"
 
 namespace e3 {
 
@@ -528,6 +529,125 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const AttnArgs a) 
         u.y = pack2_bf16(v.z, v.w);
         *reinterpret_cast<uint2*>(a.olat_bf + off) = u;
     }
+}
+
+// Split merge fused with the value up-projection, for few rows (the weight-streaming path): CTA h
+// stages W_UV,h (the d_v value rows of kv_b for head h, d_v x d_c bf16, contiguous) into shared memory
+// with one bulk copy issued before the wait on the attention kernel, merges the head's split partials
+// of every row into o_lat (shared memory), then forms o[r, h] = W_UV,h o_lat[r, h] (warp w: rows
+// v = 16w .. 16w + 15, lanes over d_c, a warp reduction per output).  d_c 512, d_v 128, M <= 8 rows.
+namespace mu {
+constexpr int DC = 512, DV = 128, THREADS = 256, MAXR = 8;
+constexpr int W_BYTES = DV * DC * 2;
+constexpr size_t SMEM = (size_t)W_BYTES + (size_t)MAXR * DC * 4 + 64;
+}  // namespace mu
+
+__global__ void __launch_bounds__(mu::THREADS, 1) merge_unabsorb_kernel(const AttnArgs a) {
+    using namespace mu;
+    pdl_trigger();
+    extern __shared__ __align__(128) unsigned char msm[];
+    bf16* w = reinterpret_cast<bf16*>(msm);                              // [DV][DC]
+    float* ol = reinterpret_cast<float*>(msm + W_BYTES);                 // [M][DC]
+    uint64_t* bar = reinterpret_cast<uint64_t*>(msm + W_BYTES + MAXR * DC * 4);
+    __shared__ float wsp[64];
+    const int h = blockIdx.x, t = threadIdx.x, lane = t & 31, warp = t >> 5;
+    const uint32_t sbar = smem_u32(bar);
+    if (t == 0) {
+        asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(sbar));
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(sbar), "r"(W_BYTES) : "memory");
+        const bf16* src = reinterpret_cast<const bf16*>(a.kv_b) + ((long)h * (a.dn + a.dv) + a.dn) * DC;
+        asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+                     ::"r"(smem_u32(w)), "l"(src), "r"(W_BYTES), "r"(sbar) : "memory");
+    }
+    pdl_wait();
+    const int S = a.splits;
+    for (int r = 0; r < a.M; ++r) {
+        const long base = ((long)r * a.nh + h) * S;
+        const int Sv = a.chunk > 0 ? min(S, (a.row_pos[r] + a.chunk) / a.chunk) : S;
+        __syncthreads();   // wsp of the previous row is consumed
+        if (t < 32) {
+            float m0 = -FLT_MAX, m1 = -FLT_MAX, l0 = 0.f, l1 = 0.f;
+            if (t < Sv) { m0 = a.part_ml[(base + t) * 2]; l0 = a.part_ml[(base + t) * 2 + 1]; }
+            if (t + 32 < Sv) { m1 = a.part_ml[(base + t + 32) * 2]; l1 = a.part_ml[(base + t + 32) * 2 + 1]; }
+            const float mx = warp_max(fmaxf(m0, m1));
+            const float e0 = l0 > 0.f ? __expf(m0 - mx) : 0.f;
+            const float e1 = l1 > 0.f ? __expf(m1 - mx) : 0.f;
+            const float den = warp_sum(e0 * l0 + e1 * l1);
+            const float inv = den > 0.f ? 1.f / den : 0.f;
+            wsp[t] = e0 * inv;
+            wsp[t + 32] = e1 * inv;
+        }
+        __syncthreads();
+        // thread t: columns 4 (t % 128) .. + 3 of the splits sp = t / 128, + 2, ...: 16-byte loads, eight in
+        // flight per thread; the two halves meet in shared memory
+        const int cq = t & 127, g = t >> 7;
+        float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int sp0 = g; sp0 < Sv; sp0 += 16) {
+            float4 pv[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const int sp = sp0 + 2 * j;
+                pv[j] = sp < Sv ? *reinterpret_cast<const float4*>(a.part_o + (base + sp) * DC + 4 * cq)
+                                : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const int sp = sp0 + 2 * j;
+                const float ws = sp < Sv ? wsp[sp] : 0.f;
+                v.x = fmaf(ws, pv[j].x, v.x); v.y = fmaf(ws, pv[j].y, v.y);
+                v.z = fmaf(ws, pv[j].z, v.z); v.w = fmaf(ws, pv[j].w, v.w);
+            }
+        }
+        float4* row = reinterpret_cast<float4*>(ol + r * DC);
+        if (g == 1) row[cq] = v;
+        __syncthreads();
+        if (g == 0) {
+            const float4 u = row[cq];
+            row[cq] = make_float4(v.x + u.x, v.y + u.y, v.z + u.z, v.w + u.w);
+        }
+    }
+    // the staged weights (bounded wait; a wait that runs out flags the call and leaves the outputs alone)
+    bool ok = false;
+    for (uint32_t i = 0; i < (1u << 22) && !ok; ++i) {
+        uint32_t done;
+        asm volatile("{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], 0;\n selp.u32 %0, 1, 0, p;\n}\n"
+                     : "=r"(done) : "r"(sbar) : "memory");
+        ok = done != 0;
+    }
+    __syncthreads();
+    if (!ok) {
+        if (t == 0) set_err(a.err, EAGLE3_DEVERR_TIMEOUT);
+        return;
+    }
+    for (int r = 0; r < a.M; ++r) {
+        float x[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j) x[j] = ol[r * DC + lane * 16 + j];
+        for (int v = warp * 16; v < warp * 16 + 16; ++v) {
+            const uint4* wr = reinterpret_cast<const uint4*>(w + (long)v * DC + lane * 16);
+            float f[16];
+            unpack_bf16x8(wr[0], f);
+            unpack_bf16x8(wr[1], f + 8);
+            float acc = 0.f;
+#pragma unroll
+            for (int j = 0; j < 16; ++j) acc = fmaf(f[j], x[j], acc);
+            acc = warp_sum(acc);
+            if (lane == 0) a.o[((long)r * a.nh + h) * DV + v] = acc;
+        }
+    }
+}
+
+bool merge_unabsorb_supported(const AttnArgs& a) {
+    return a.dt == BF16 && a.dc == mu::DC && a.dv == mu::DV && a.M <= mu::MAXR && a.splits >= 1 && a.splits <= 64 &&
+           a.o != nullptr && ((uintptr_t)a.kv_b & 15u) == 0;
+}
+
+cudaError_t launch_merge_unabsorb(const AttnArgs& a, cudaStream_t st) {
+    if (!merge_unabsorb_supported(a)) return cudaErrorInvalidValue;
+    cudaError_t e = smem_optin((const void*)merge_unabsorb_kernel, (int)mu::SMEM);
+    if (e != cudaSuccess) return e;
+    return launch_pdl(merge_unabsorb_kernel, dim3(a.nh), dim3(mu::THREADS), mu::SMEM, st, a);
 }
 
 cudaError_t launch_merge(const AttnArgs& a, cudaStream_t st) {

@@ -223,6 +223,10 @@ cudaError_t launch_absorb(const AttnArgs& a, cudaStream_t st);
 cudaError_t launch_attention(const AttnArgs& a, cudaStream_t st);
 // split-K merge into o_lat (olat and/or olat_bf); the value up-projection then runs as a GEMM
 cudaError_t launch_merge(const AttnArgs& a, cudaStream_t st);
+// split merge fused with o = W_UV o_lat into a.o (fp32), for at most 8 rows of a bf16 head with d_c 512,
+// d_v 128 and more than one split
+bool merge_unabsorb_supported(const AttnArgs& a);
+cudaError_t launch_merge_unabsorb(const AttnArgs& a, cudaStream_t st);
 // rotated rope query into qa / qa_bf[:, :, dc:] (the tensor-core path forms q_lat separately)
 cudaError_t launch_rope_q(const AttnArgs& a, cudaStream_t st);
 // W_UK,h^T for every head: out[h, c, i] = kv_b[h*(dn+dv) + i, c]  (bf16)
