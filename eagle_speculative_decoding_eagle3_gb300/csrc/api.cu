@@ -440,7 +440,7 @@ Offsets plan(const eagle3_config_t& c, int num_sms) {
     // unabsorbed extend attention: gathered latent rows, expanded keys/values, query tile map
     const bool pre = prefill_allowed(c);
     const size_t slots = pre ? (size_t)B * c.max_ctx : 0;
-    o.tiles_cap = pre ? prefill_tiles_cap((int)M, (int)B) : 0;
+    o.tiles_cap = pre ? prefill_tiles_cap((int)M, (int)B, 64) : 0;   // the finer of the two tile heights
     o.xc = L.take(slots * c.kv_lora_rank * b2);
     o.xpe = L.take(slots * c.qk_rope_dim * b2);
     o.kvx = L.take(slots * nh * (c.qk_nope_dim + c.v_head_dim) * b2);
@@ -691,12 +691,16 @@ cudaError_t run_prefill_attention(eagle3_draft& d, eagle3_kv_t* kv, int M, int b
     memset(&pa, 0, sizeof(pa));
     pa.M = M; pa.B = batch; pa.nh = nh; pa.max_ctx = c.max_ctx;
     pa.page_size = c.page_size; pa.max_pages = c.max_pages_per_seq; pa.num_pages = kv->num_pages;
-    pa.ntiles_cap = prefill_tiles_cap(M, batch);
     pa.sigma = attention_scale(c);
     pa.row_offsets = row_offsets; pa.row_pos = d.row_pos; pa.block_table = kv->block_table; pa.cache = kv->data;
     pa.xc = d.xc; pa.xpe = d.xpe; pa.kv = d.kvx; pa.q = d.q_bf; pa.qf = nullptr;
     pa.rope_cos = d.rope_cos; pa.rope_sin = d.rope_sin;
     pa.tiles = d.tiles; pa.o_bf = d.o_bf; pa.err = d.err;
+    // 128-row query tiles on tcgen05; the mma.sync kernel (64-row tiles) where TMA cannot address the rows
+    pa.bq = 128;
+    const bool tc_pf = prefill_tc_supported(pa);
+    if (!tc_pf) pa.bq = 64;
+    pa.ntiles_cap = prefill_tiles_cap(M, batch, pa.bq);
     if (pa.ntiles_cap > d.tiles_cap) return cudaErrorInvalidValue;
     E3_TRY(traced(d, K_ROPE_Q, st, [&] { return launch_rope_q_rows(pa, st); }));
     E3_TRY(traced(d, K_KV_GATHER, st, [&] { return launch_kv_gather(pa, st); }));
@@ -706,7 +710,7 @@ cudaError_t run_prefill_attention(eagle3_draft& d, eagle3_kv_t* kv, int M, int b
         E3_TRY(run_linear(d, L, K_KV_EXPAND, st));
     }
     E3_TRY(traced(d, K_PREFILL_TILES, st, [&] { return launch_prefill_tiles(pa, st); }));
-    return traced(d, K_ATTN, st, [&] { return launch_prefill_attention(pa, st); });
+    return traced(d, K_ATTN, st, [&] { return tc_pf ? launch_prefill_tc(pa, st) : launch_prefill_attention(pa, st); });
 }
 
 // The MLA attention block of a layer: q_a | kv_a, latent norms and cache append, q_b, then absorbed

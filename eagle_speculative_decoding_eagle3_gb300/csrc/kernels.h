@@ -146,6 +146,7 @@ cudaError_t launch_philox_uniforms(uint64_t seed, uint64_t offset, long n, float
 struct PrefillArgs {
     int M, B, nh, max_ctx, page_size, max_pages, num_pages;
     int ntiles_cap;                    // entries of `tiles` (prefill_tiles_cap)
+    int bq;                            // query rows per tile: 64 (mma.sync kernel) or 128 (tcgen05 kernel)
     float sigma;
     const int* row_offsets;            // [B + 1] rows of each sequence in this extend
     const int* row_pos;                // [M] positions
@@ -164,11 +165,14 @@ struct PrefillArgs {
     int* err;
 };
 bool prefill_supported(int dt, int dn, int dr, int dv);
-int prefill_tiles_cap(int M, int B);
+int prefill_tiles_cap(int M, int B, int bq);
 cudaError_t launch_kv_gather(const PrefillArgs& a, cudaStream_t st);
 cudaError_t launch_prefill_tiles(const PrefillArgs& a, cudaStream_t st);
 cudaError_t launch_rope_q_rows(const PrefillArgs& a, cudaStream_t st);
 cudaError_t launch_prefill_attention(const PrefillArgs& a, cudaStream_t st);
+// tcgen05 flash attention of the same extend (bq 128): the same o_bf output
+bool prefill_tc_supported(const PrefillArgs& a);
+cudaError_t launch_prefill_tc(const PrefillArgs& a, cudaStream_t st);
 
 // ---------------------------------------------------------------- MHA attention (Llama-style head)
 struct MhaArgs {

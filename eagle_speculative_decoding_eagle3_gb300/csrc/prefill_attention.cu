@@ -74,7 +74,7 @@ __global__ void __launch_bounds__(256) kv_gather_kernel(const PrefillArgs a) {
     }
 }
 
-// Tile map: for each sequence its ceil(T_b / 64) query tiles, last (heaviest) first; unused entries
+// Tile map: for each sequence its ceil(T_b / bq) query tiles, last (heaviest) first; unused entries
 // get sequence -1.  One CTA; thread 0 scans the tile counts.
 __global__ void __launch_bounds__(256) prefill_tiles_kernel(const PrefillArgs a) {
     pdl_trigger();
@@ -85,19 +85,19 @@ __global__ void __launch_bounds__(256) prefill_tiles_kernel(const PrefillArgs a)
         for (int b = 0; b < a.B; ++b) {
             start[b] = acc;
             const int r0 = max(0, min(a.M, a.row_offsets[b])), r1 = max(r0, min(a.M, a.row_offsets[b + 1]));
-            acc += (r1 - r0 + pf::BQ - 1) / pf::BQ;
+            acc += (r1 - r0 + a.bq - 1) / a.bq;
         }
         start[a.B] = min(acc, a.ntiles_cap);
     }
     __syncthreads();
     for (int b = threadIdx.x; b < a.B; b += blockDim.x) {
         const int r0 = max(0, min(a.M, a.row_offsets[b])), r1 = max(r0, min(a.M, a.row_offsets[b + 1]));
-        const int nt = (r1 - r0 + pf::BQ - 1) / pf::BQ;
+        const int nt = (r1 - r0 + a.bq - 1) / a.bq;
         for (int i = 0; i < nt; ++i) {
             const int idx = start[b] + (nt - 1 - i);
             if (idx >= a.ntiles_cap) continue;
-            const int row = r0 + i * pf::BQ;
-            a.tiles[idx] = make_int4(b, row, min(pf::BQ, r1 - row), 0);
+            const int row = r0 + i * a.bq;
+            a.tiles[idx] = make_int4(b, row, min(a.bq, r1 - row), 0);
         }
     }
     for (int i = start[a.B] + threadIdx.x; i < a.ntiles_cap; i += blockDim.x) a.tiles[i] = make_int4(-1, 0, 0, 0);
@@ -289,6 +289,7 @@ cudaError_t launch_rope_q_rows(const PrefillArgs& a, cudaStream_t st) {
 }
 
 cudaError_t launch_prefill_attention(const PrefillArgs& a, cudaStream_t st) {
+    if (a.bq != pf::BQ) return cudaErrorInvalidValue;
     {
         cudaError_t e = smem_optin((const void*)prefill_attention_kernel, (int)pf::SMEM);
         if (e != cudaSuccess) return e;
@@ -296,6 +297,6 @@ cudaError_t launch_prefill_attention(const PrefillArgs& a, cudaStream_t st) {
     return launch_pdl(prefill_attention_kernel, dim3(a.ntiles_cap, a.nh), dim3(pf::THREADS), pf::SMEM, st, a);
 }
 
-int prefill_tiles_cap(int M, int B) { return (M + pf::BQ - 1) / pf::BQ + B; }
+int prefill_tiles_cap(int M, int B, int bq) { return (M + bq - 1) / bq + B; }
 
 }  // namespace e3
