@@ -2,18 +2,26 @@
 //
 // "Eagle3 DeepseekV3 in MAX" §3.1 and §10 name the sampling parameters of the drafts (temperature,
 // top-k, top-p) and the rejection-sampling strategies (greedy, residual, ...), and §8 a seed counter
-// that feeds the sampler.  Here the uniform random numbers are inputs, so a caller (or a test) draws
-// them once and every consumer uses the same ones.
+// that feeds the sampler.  The uniform random numbers are inputs (drawn by the caller, or on the device by
+// philox_uniforms_kernel below), so every consumer of a draw sees the same number.
 //
-// sample_kernel: one CTA of kThreads per row.  x = logits / temperature; since the temperature is
-// positive, x is ordered exactly as the logits are, so top_k keeps the top_k largest logits (lower
-// indices first among equal values), found by a radix select on the order-preserving integer image of
-// the logits; the kept tokens are sorted (logit descending, index ascending) by a bitonic sort in shared
-// memory; their softmax weights are exp((l - l_max) / temperature) in fp32; top_p keeps the shortest
-// prefix whose mass reaches top_p of the kept mass; the kept weights are renormalised and u picks the
-// token by inverse CDF in ascending index order.
-// temperature 0 is the greedy argmax.  Without top_k the whole vocabulary is kept (top_p must be 1) and
-// the inverse CDF runs over it with a block-wide scan.
+// sample_kernel: one thread-block cluster of kCluster CTAs per row; CTA g owns the logits of slice g of
+// the row and keeps their order-preserving integer keys in shared memory.  x = logits / temperature; since
+// the temperature is positive, x is ordered exactly as the logits are, so
+//  * top_k keeps the top_k largest logits, lower indices first among equal values.  Each CTA finds the
+//    top_k of its slice by a radix select on the 64-bit value (key, ~index), which is distinct for every
+//    token and orders the tokens exactly as the rule does; CTA 0 gathers the cluster's candidates through
+//    distributed shared memory and selects the top_k among them the same way.  The kept tokens are sorted
+//    (logit descending, index ascending) by a bitonic sort; their softmax weights are
+//    exp((l - l_max) / temperature) in fp32; top_p keeps the shortest prefix whose mass reaches top_p of
+//    the kept mass; the kept weights are renormalised and u picks the token by inverse CDF in ascending
+//    index order.
+//  * without top_k the whole vocabulary is kept (top_p must be 1): each CTA sums exp((l - m_g) / T) over
+//    its slice, the cluster combines the slice masses in units of the row maximum, and the CTA whose
+//    slice holds the draw u * total finds the token by a block scan of its slice in index order.
+//  * temperature 0 is the greedy argmax (largest (key, ~index)).
+// A probability row that maps through d2t is zeroed by all CTAs of the cluster before the cluster barrier
+// that precedes the writes of the kept probabilities.
 //
 // accept_residual_kernel: one CTA per sequence; the speculative-sampling rule (accept x with
 // probability min(1, p(x) / q(x)); at the first rejection draw from max(0, p - q) renormalised; after
@@ -23,14 +31,18 @@
 
 #include "common.cuh"
 #include "kernels.h"
+#include "tcgen05.cuh"
 
 namespace e3 {
 
 namespace smp {
 constexpr int kThreads = 1024;
+constexpr int kWarps = kThreads / 32;
+constexpr int kCluster = 8;                       // CTAs per row
 constexpr int kMaxTopK = 1024;
-constexpr int kKeyCache = 40960;   // rows up to this many logits keep their sort keys in shared memory
-constexpr int kMaxChunks = 4096;   // rows of at most 131072 logits
+constexpr int kMaxV = 131072;                     // logits per row
+constexpr int kMaxSlice = kMaxV / kCluster;       // keys per CTA
+constexpr int kSmemMax = kMaxSlice * 4 + kCluster * kMaxTopK * 8;
 }  // namespace smp
 
 // order-preserving image of a float: larger floats give larger unsigned keys
@@ -38,6 +50,15 @@ __device__ __forceinline__ uint32_t fkey(float x) {
     const uint32_t b = __float_as_uint(x);
     return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
 }
+// the float of a key (exact inverse of fkey)
+__device__ __forceinline__ float unkey(uint32_t k) {
+    return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
+}
+// The selection value of token i with key k: larger logits first, lower indices first among equal ones.
+__device__ __forceinline__ unsigned long long cval(uint32_t k, int i) {
+    return ((unsigned long long)k << 32) | (uint32_t)~(uint32_t)i;
+}
+__device__ __forceinline__ int cidx(unsigned long long c) { return (int)~(uint32_t)c; }
 
 // inclusive block scan of one float per thread (kThreads threads); returns the thread's inclusive sum
 __device__ float block_inclusive_scan(float v, float* warp_tot) {
@@ -63,29 +84,6 @@ __device__ float block_inclusive_scan(float v, float* warp_tot) {
     return v + (warp > 0 ? warp_tot[warp - 1] : 0.f);
 }
 
-__device__ int block_inclusive_scan_int(int v, int* warp_tot) {
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        const int n = __shfl_up_sync(0xffffffffu, v, o);
-        if (lane >= o) v += n;
-    }
-    __syncthreads();
-    if (lane == 31) warp_tot[warp] = v;
-    __syncthreads();
-    if (warp == 0) {
-        int t = lane < (int)(blockDim.x >> 5) ? warp_tot[lane] : 0;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const int n = __shfl_up_sync(0xffffffffu, t, o);
-            if (lane >= o) t += n;
-        }
-        warp_tot[lane] = t;
-    }
-    __syncthreads();
-    return v + (warp > 0 ? warp_tot[warp - 1] : 0);
-}
-
 // bitonic sort of the first n (a power of two <= kThreads) packed (key, index) pairs in shared memory,
 // ascending
 __device__ void bitonic_sort(unsigned long long* a, int n) {
@@ -103,221 +101,245 @@ __device__ void bitonic_sort(unsigned long long* a, int n) {
     }
 }
 
-__global__ void __launch_bounds__(smp::kThreads) sample_kernel(SampleArgs s) {
+struct SelectShared {
+    int whist[smp::kWarps][256];   // per-warp radix histograms (keeps the atomics of different warps apart)
+    int hist[256];
+    int sh[4];
+};
+
+// The K largest of n distinct 64-bit values get(0..n-1), 1 <= K <= n: on return exactly the values with
+// (v & mask) >= prefix are the K largest.  Radix select from the top byte; the search ends early once every
+// value left in the chosen bin is kept.
+template <typename Get>
+__device__ void select_largest(int n, int K, Get get, SelectShared& S, unsigned long long& prefix_out,
+                               unsigned long long& mask_out) {
+    const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
+    unsigned long long prefix = 0, mask = 0;
+    int need = K;
+    for (int shift = 56; shift >= 0; shift -= 8) {
+        for (int i = t; i < smp::kWarps * 256; i += blockDim.x) (&S.whist[0][0])[i] = 0;
+        __syncthreads();
+        for (int i0 = 0; i0 < n; i0 += blockDim.x) {
+            const int i = i0 + t;
+            int bin = 256;
+            if (i < n) {
+                const unsigned long long v = get(i);
+                if ((v & mask) == prefix) bin = (int)((v >> shift) & 255u);
+            }
+            // lanes sharing lane 0's bin add once through lane 0; the others add one by one
+            const int b0 = __shfl_sync(0xffffffffu, bin, 0);
+            const unsigned same = __ballot_sync(0xffffffffu, bin == b0);
+            if (bin < 256) {
+                if (bin != b0) atomicAdd(&S.whist[warp][bin], 1);
+                else if (lane == 0) atomicAdd(&S.whist[warp][b0], __popc(same));
+            }
+        }
+        __syncthreads();
+        for (int b = t; b < 256; b += blockDim.x) {
+            int c = 0;
+#pragma unroll 8
+            for (int w = 0; w < smp::kWarps; ++w) c += S.whist[w][b];
+            S.hist[b] = c;
+        }
+        __syncthreads();
+        if (warp == 0) {
+            // lane L holds bins 255 - 8L down to 248 - 8L; the bin where the count from the top reaches
+            // `need` is found by a warp scan, then inside the lane's eight bins
+            int c8 = 0;
+#pragma unroll
+            for (int q = 0; q < 8; ++q) c8 += S.hist[255 - 8 * lane - q];
+            int incl = c8;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int x = __shfl_up_sync(0xffffffffu, incl, o);
+                if (lane >= o) incl += x;
+            }
+            const unsigned hit = __ballot_sync(0xffffffffu, incl >= need);
+            if (lane == __ffs(hit) - 1) {
+                int acc = incl - c8, d = 255 - 8 * lane;
+                for (int q = 0; q < 7; ++q, --d) {
+                    if (acc + S.hist[d] >= need) break;
+                    acc += S.hist[d];
+                }
+                S.sh[0] = d;
+                S.sh[1] = acc;
+                S.sh[2] = S.hist[d];
+            }
+        }
+        __syncthreads();
+        const int d = S.sh[0], above = S.sh[1], inbin = S.sh[2];
+        prefix |= (unsigned long long)d << shift;
+        mask |= 255ull << shift;
+        need -= above;
+        if (inbin == need) break;   // block-uniform: the whole bin is kept
+    }
+    prefix_out = prefix;
+    mask_out = mask;
+}
+
+// Largest 64-bit value over the block (every thread gets it).
+__device__ unsigned long long block_max_u64(unsigned long long v, unsigned long long* scratch) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = max(v, __shfl_xor_sync(0xffffffffu, v, o));
+    __syncthreads();
+    if (lane == 0) scratch[warp] = v;
+    __syncthreads();
+    v = lane < (int)(blockDim.x >> 5) ? scratch[lane] : 0ull;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = max(v, __shfl_xor_sync(0xffffffffu, v, o));
+    return v;
+}
+
+__device__ float block_max_f32(float v, float* scratch) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    v = warp_max(v);
+    __syncthreads();
+    if (lane == 0) scratch[warp] = v;
+    __syncthreads();
+    v = lane < (int)(blockDim.x >> 5) ? scratch[lane] : -INFINITY;
+    return warp_max(v);
+}
+
+__global__ void __launch_bounds__(smp::kThreads, 1) sample_kernel(SampleArgs s) {
     using namespace smp;
+    using namespace tc;
     pdl_trigger();
     pdl_wait();
-    __shared__ unsigned long long sorted[kThreads];   // (key, index) packed; reused
-    __shared__ float wv[kThreads];
-    __shared__ int hist[256];
-    __shared__ int whist[kThreads / 32][256];         // per-warp radix histograms
-    __shared__ int ccount[kMaxChunks];                // equal-key counts, then prefixes, per 32 indices
-    __shared__ float ftot[32];
-    __shared__ int itot[32];
+    __shared__ SelectShared S;
+    __shared__ unsigned long long sorted[kThreads];   // (~key, index) packed
+    __shared__ unsigned long long red64[kWarps];
+    __shared__ float ftot[kWarps];
     __shared__ int sh_int[4];
     __shared__ float sh_f[2];
-    extern __shared__ uint32_t keycache[];             // [V] keys of the logits when V fits
-    const int r = blockIdx.x, t = threadIdx.x, V = s.V;
+    __shared__ unsigned long long xchg;                // read by the peers: greedy best / candidate count
+    __shared__ float xm, xs;                           // read by the peers: slice maximum and mass
+    __shared__ int cnts[kCluster];
+    __shared__ float pm[kCluster], psum[kCluster];
+    extern __shared__ __align__(16) unsigned char dyn[];
+    const int r = blockIdx.y, t = threadIdx.x, V = s.V;
+    const int g = (int)cluster_rank();
+    const int SL = (V + kCluster - 1) / kCluster;
+    const int base = min(V, g * SL), n = min(V, base + SL) - base;   // this CTA's slice [base, base + n)
+    uint32_t* keys = reinterpret_cast<uint32_t*>(dyn);
+    unsigned long long* cand = reinterpret_cast<unsigned long long*>(dyn + (((size_t)SL * 4 + 15) & ~(size_t)15));
     const float* l = s.logits + (long)r * s.ldl;
     float* probs = s.probs ? s.probs + (long)r * s.ldp : nullptr;
+    const bool mapped = s.probs_target && s.d2t;
+    const bool greedy = s.temperature <= 0.f, full = !greedy && s.top_k <= 0;
+    const float T = s.temperature;
     const float u = s.uniforms[r];
-    int token = 0;
-    float qtok = 1.f;
 
-    if (s.temperature <= 0.f) {
-        // greedy: max with the lowest index
-        float bv = -INFINITY;
-        int bi = INT_MAX;
-        for (int i = t; i < V; i += kThreads)
-            if (l[i] > bv) { bv = l[i]; bi = i; }
-        for (int o = 16; o > 0; o >>= 1) {
-            const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-            const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-            if (ov > bv || (ov == bv && oi < bi)) { bv = ov; bi = oi; }
+    // the slice's keys: eight loads in flight per thread
+    for (int i0 = 0; i0 < n; i0 += 8 * kThreads) {
+        float v[8];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+            const int i = i0 + q * kThreads + t;
+            v[q] = i < n ? __ldg(l + base + i) : 0.f;
         }
-        if ((t & 31) == 0) { wv[t >> 5] = bv; sorted[t >> 5] = (unsigned long long)bi; }
-        __syncthreads();
-        if (t == 0) {
-            float b = wv[0];
-            int bidx = (int)sorted[0];
-            for (int w = 1; w < kThreads / 32; ++w)
-                if (wv[w] > b || (wv[w] == b && (int)sorted[w] < bidx)) { b = wv[w]; bidx = (int)sorted[w]; }
-            sh_int[0] = bidx;
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+            const int i = i0 + q * kThreads + t;
+            if (i < n) keys[i] = fkey(v[q]);
         }
-        __syncthreads();
-        token = sh_int[0];
-        if (probs) {
-            const int o = s.probs_target && s.d2t ? token + s.d2t[token] : token;
-            for (int i = t; i < s.probs_len; i += kThreads) probs[i] = i == o ? 1.f : 0.f;
+    }
+    // zero the probability row where only some entries get written, a share per CTA
+    if (probs && (!full || mapped)) {
+        const int PL = s.probs_len, ch = (PL + kCluster - 1) / kCluster;
+        const int z0 = min(PL, g * ch), z1 = min(PL, z0 + ch);
+        for (int i = z0 + t; i < z1; i += kThreads) probs[i] = 0.f;
+    }
+    __syncthreads();
+
+    int token = -1;       // >= 0 in the CTA that writes the row's outputs
+    float qtok = 1.f;
+    if (greedy) {
+        unsigned long long best = 0;
+        for (int i = t; i < n; i += kThreads) best = max(best, cval(keys[i], base + i));
+        best = block_max_u64(best, red64);
+        if (t == 0) xchg = best;
+        cluster_sync();
+        if (g == 0 && t < 32) {
+            unsigned long long b = 0;
+            if (t < kCluster && t * SL < V) b = ld_cluster_u64(mapa(su32(&xchg), t));
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) b = max(b, __shfl_xor_sync(0xffffffffu, b, o));
+            if (t == 0) sh_int[0] = cidx(b);
         }
-    } else if (s.top_k <= 0) {
-        // whole vocabulary: softmax of x = l / T and inverse CDF in index order
-        const float T = s.temperature;
-        float m = -INFINITY;
-        for (int i = t; i < V; i += kThreads) m = fmaxf(m, l[i]);
-        m = warp_max(m);
-        if ((t & 31) == 0) wv[t >> 5] = m;
-        __syncthreads();
-        if (t < 32) {
-            float mm = wv[t];
-            mm = warp_max(mm);
-            if (t == 0) sh_f[0] = mm;
-        }
-        __syncthreads();
-        m = sh_f[0];
-        // contiguous segment per thread, so the block scan follows the index order
-        const int seg = (V + kThreads - 1) / kThreads, i0 = t * seg, i1 = min(V, i0 + seg);
-        float part = 0.f;
-        for (int i = i0; i < i1; ++i) part += __expf((l[i] - m) / T);
-        const float incl = block_inclusive_scan(part, ftot);
-        const float total = ftot[kThreads / 32 - 1];
-        const float target = u * total;
-        float cum = incl - part;
-        int found = -1;
-        if (cum <= target && target < incl) {
-            for (int i = i0; i < i1; ++i) {
-                cum += __expf((l[i] - m) / T);
-                if (target < cum) { found = i; break; }
-            }
-            if (found < 0) found = i1 - 1;
-        }
-        if (t == 0) sh_int[0] = V - 1;   // u rounding past the total: the last token
-        __syncthreads();
-        if (found >= 0) sh_int[0] = found;
+        cluster_sync();   // the peers' words have been read
+        if (g != 0) return;
         __syncthreads();
         token = sh_int[0];
-        qtok = __expf((l[token] - m) / T) / total;
-        if (probs) {
-            if (s.probs_target && s.d2t) {
-                for (int i = t; i < s.probs_len; i += kThreads) probs[i] = 0.f;
-                __syncthreads();
-            }
-            for (int i = t; i < V; i += kThreads) {
-                const int o = s.probs_target && s.d2t ? i + s.d2t[i] : i;
-                if (o >= 0 && o < s.probs_len) probs[o] = __expf((l[i] - m) / T) / total;
-            }
+        if (probs && t == 0) {
+            const int o = mapped ? token + s.d2t[token] : token;
+            if (o >= 0 && o < s.probs_len) probs[o] = 1.f;
         }
-    } else {
-        const float T = s.temperature;
-        const int K = min(s.top_k, min(kMaxTopK, V));
-        const bool cached = V <= kKeyCache;
-        if (cached) {
-            for (int i = t; i < V; i += kThreads) keycache[i] = fkey(l[i]);
+    } else if (!full) {
+        const int K = min(s.top_k, V);
+        // this slice's top K (all of it when it holds no more than K tokens)
+        if (n <= K) {
+            for (int i = t; i < n; i += kThreads) cand[i] = cval(keys[i], base + i);
+            if (t == 0) xchg = (unsigned long long)n;
+        } else {
+            unsigned long long pre, msk;
+            select_largest(n, K, [&](int i) { return cval(keys[i], base + i); }, S, pre, msk);
+            if (t == 0) sh_int[2] = 0;
             __syncthreads();
+            for (int i = t; i < n; i += kThreads) {
+                const unsigned long long c = cval(keys[i], base + i);
+                if ((c & msk) >= pre) cand[atomicAdd(&sh_int[2], 1)] = c;
+            }
+            if (t == 0) xchg = (unsigned long long)K;
         }
-        auto key_of = [&](int i) { return cached ? keycache[i] : fkey(l[i]); };
-        // radix select of the K-th largest key, 8 bits at a time from the top
-        uint32_t prefix = 0, pmask = 0;
-        int need = K;
-        const int warp = t >> 5;
-        for (int shift = 24; shift >= 0; shift -= 8) {
-            for (int i = t; i < (kThreads / 32) * 256; i += kThreads) (&whist[0][0])[i] = 0;
+        cluster_sync();   // every CTA's candidates and count are visible to CTA 0
+        if (g == 0) {
+            if (t < kCluster) cnts[t] = t * SL < V ? (int)ld_cluster_u64(mapa(su32(&xchg), t)) : 0;
             __syncthreads();
-            // logits cluster in a few exponents, so most keys share a bin: every warp counts into its own
-            // histogram, which keeps the atomics of different warps apart
-            for (int i0 = 0; i0 < V; i0 += kThreads) {
-                const int i = i0 + t;
-                int bin = 256;
-                if (i < V) {
-                    const uint32_t k = key_of(i);
-                    if ((k & pmask) == prefix) bin = (int)((k >> shift) & 255u);
-                }
-                // lanes sharing lane 0's bin add once through lane 0; the others add one by one
-                const int b0 = __shfl_sync(0xffffffffu, bin, 0);
-                const unsigned same = __ballot_sync(0xffffffffu, bin == b0);
-                if (bin < 256) {
-                    if (bin != b0) atomicAdd(&whist[warp][bin], 1);
-                    else if ((t & 31) == 0) atomicAdd(&whist[warp][b0], __popc(same));
-                }
+            // the peers' candidates after this CTA's own (at most K <= kThreads per CTA: one per thread)
+            unsigned long long v[kCluster];
+            int off = cnts[0];
+#pragma unroll
+            for (int h = 1; h < kCluster; ++h)
+                v[h] = t < cnts[h] ? ld_cluster_u64(mapa(su32(cand + t), h)) : 0ull;
+#pragma unroll
+            for (int h = 1; h < kCluster; ++h) {
+                if (t < cnts[h]) cand[off + t] = v[h];
+                off += cnts[h];
             }
-            __syncthreads();
-            for (int b = t; b < 256; b += kThreads) {
-                int c = 0;
-                for (int w = 0; w < kThreads / 32; ++w) c += whist[w][b];
-                hist[b] = c;
-            }
-            __syncthreads();
-            if (t == 0) {
-                int acc = 0, d = 255;
-                for (; d > 0; --d) {
-                    if (acc + hist[d] >= need) break;
-                    acc += hist[d];
-                }
-                sh_int[0] = d;
-                sh_int[1] = acc;
-                sh_int[3] = hist[d];   // after the last pass: the number of keys equal to the threshold
-            }
-            __syncthreads();
-            prefix |= (uint32_t)sh_int[0] << shift;
-            pmask |= 255u << shift;
-            need -= sh_int[1];
-            __syncthreads();
+            if (t == 0) sh_int[3] = off;
         }
-        const uint32_t kth = prefix;   // keys > kth are all kept; `need` of the keys == kth, lowest index first
-        // gather: keys above the threshold, then the first `need` equal keys in index order
+        cluster_sync();   // CTA 0 holds every candidate; the peers are done
+        if (g != 0) return;
+        const int total = sh_int[3];
+        unsigned long long pre = 0, msk = 0;   // keeps every candidate when there are no more than K
+        if (total > K) select_largest(total, K, [&](int i) { return cand[i]; }, S, pre, msk);
         if (t == 0) sh_int[2] = 0;
         sorted[t] = ~0ull;
         __syncthreads();
-        // when every key equal to the threshold is kept (the usual case) one pass gathers them all
-        const bool all_eq = sh_int[3] == need;
-        for (int i = t; i < V; i += kThreads) {
-            const uint32_t k = key_of(i);
-            if (k > kth || (all_eq && k == kth)) {
-                const int slot = atomicAdd(&sh_int[2], 1);
-                sorted[slot] = ((unsigned long long)(~k) << 32) | (uint32_t)i;
-            }
+        for (int i = t; i < total; i += kThreads) {
+            const unsigned long long c = cand[i];
+            if ((c & msk) >= pre) sorted[atomicAdd(&sh_int[2], 1)] = ~c;   // (~key, index)
         }
         __syncthreads();
-        if (!all_eq)
-        {
-            // equal keys in index order: per 32-index chunk counts by ballot, one scan over the chunk counts,
-            // then ranks inside the chunks that hold any of the `need` first equal keys
-            const int base = sh_int[2];
-            const int nchunk = (V + 31) / 32;
-            for (int c = warp; c < nchunk; c += kThreads / 32) {
-                const int i = c * 32 + (t & 31);
-                const unsigned bal = __ballot_sync(0xffffffffu, i < V && key_of(i) == kth);
-                if ((t & 31) == 0) ccount[c] = __popc(bal);
-            }
-            __syncthreads();
-            const int per = (nchunk + kThreads - 1) / kThreads, c0 = t * per, c1 = min(nchunk, c0 + per);
-            int mine = 0;
-            for (int c = c0; c < c1; ++c) mine += ccount[c];
-            int run = block_inclusive_scan_int(mine, itot) - mine;
-            for (int c = c0; c < c1; ++c) {
-                const int cn = ccount[c];
-                ccount[c] = run;
-                run += cn;
-            }
-            __syncthreads();
-            for (int c = warp; c < nchunk; c += kThreads / 32) {
-                const int start = ccount[c];
-                if (start >= need) continue;   // warp-uniform
-                const int i = c * 32 + (t & 31);
-                const bool eq = i < V && key_of(i) == kth;
-                const unsigned bal = __ballot_sync(0xffffffffu, eq);
-                const int rank = start + __popc(bal & ((1u << (t & 31)) - 1u));
-                if (eq && rank < need) sorted[base + rank] = ((unsigned long long)(~kth) << 32) | (uint32_t)i;
-            }
-            __syncthreads();
-        }
-        const int n = K;
+        const int nk = min(K, total);
         // (logit descending, index ascending) == (~key ascending, index ascending)
         int np2 = 2;
-        while (np2 < n) np2 <<= 1;
+        while (np2 < nk) np2 <<= 1;
         bitonic_sort(sorted, np2);
-        const bool live = t < n;
+        const bool live = t < nk;
         const int idx = live ? (int)(sorted[t] & 0xffffffffu) : 0;
-        const float l0 = l[(int)(sorted[0] & 0xffffffffu)];
-        const float w = live ? __expf((l[idx] - l0) / T) : 0.f;
+        const float lt = live ? unkey(~(uint32_t)(sorted[t] >> 32)) : 0.f;
+        const float l0 = unkey(~(uint32_t)(sorted[0] >> 32));
+        const float w = live ? __expf((lt - l0) / T) : 0.f;
         const float cum = block_inclusive_scan(w, ftot);
-        const float total = ftot[kThreads / 32 - 1];
+        const float totw = ftot[kWarps - 1];
         // top-p: the shortest prefix whose mass reaches top_p of the total
-        int keep = n;
+        int keep = nk;
         if (s.top_p < 1.f) {
-            if (t == 0) sh_int[3] = n;
+            if (t == 0) sh_int[3] = nk;
             __syncthreads();
-            const float lim = s.top_p * total;
+            const float lim = s.top_p * totw;
             const float prev = cum - w;
             if (live && cum >= lim && prev < lim) sh_int[3] = t + 1;
             __syncthreads();
@@ -333,7 +355,7 @@ __global__ void __launch_bounds__(smp::kThreads) sample_kernel(SampleArgs s) {
         const float w2 = k2 ? __uint_as_float((uint32_t)(sorted[t] & 0xffffffffu)) : 0.f;
         const int i2 = k2 ? (int)(sorted[t] >> 32) : 0;
         const float c2 = block_inclusive_scan(w2, ftot);
-        const float kept_total = ftot[kThreads / 32 - 1];
+        const float kept_total = ftot[kWarps - 1];
         const float target = u * kept_total;
         if (t == 0) {   // u rounding past the kept total: the last kept token
             sh_int[0] = (int)(sorted[keep - 1] >> 32);
@@ -344,16 +366,71 @@ __global__ void __launch_bounds__(smp::kThreads) sample_kernel(SampleArgs s) {
         __syncthreads();
         token = sh_int[0];
         qtok = sh_f[1] / kept_total;
-        if (probs) {
-            for (int i = t; i < s.probs_len; i += kThreads) probs[i] = 0.f;
+        if (probs && k2) {
+            const int o = mapped ? i2 + s.d2t[i2] : i2;
+            if (o >= 0 && o < s.probs_len) probs[o] = w2 / kept_total;
+        }
+    } else {
+        // whole vocabulary: this slice's maximum and mass, in index order (a contiguous run per thread)
+        float mloc = -INFINITY;
+        for (int i = t; i < n; i += kThreads) mloc = fmaxf(mloc, unkey(keys[i]));
+        mloc = block_max_f32(mloc, ftot);
+        const int seg = (n + kThreads - 1) / kThreads, i0 = min(n, t * seg), i1 = min(n, i0 + seg);
+        float part = 0.f;
+        for (int i = i0; i < i1; ++i) part += __expf((unkey(keys[i]) - mloc) / T);
+        const float incl = block_inclusive_scan(part, ftot);
+        if (t == 0) { xm = mloc; xs = ftot[kWarps - 1]; }
+        cluster_sync();
+        if (t < kCluster) {
+            const bool any = t * SL < V;
+            pm[t] = any ? ld_cluster_f32(mapa(su32(&xm), t)) : -INFINITY;
+            psum[t] = any ? ld_cluster_f32(mapa(su32(&xs), t)) : 0.f;
+        }
+        cluster_sync();   // the peers' words have been read
+        // the row maximum, every slice's mass in its units and this slice's offset (the same arithmetic in
+        // every CTA, so the slices' ranges tile [0, total))
+        float m = -INFINITY;
+#pragma unroll
+        for (int h = 0; h < kCluster; ++h) m = fmaxf(m, pm[h]);
+        float total = 0.f, cg = 0.f, wg = 0.f, sg = 1.f;
+#pragma unroll
+        for (int h = 0; h < kCluster; ++h) {
+            const float sc = psum[h] > 0.f ? __expf((pm[h] - m) / T) : 0.f;
+            const float wh = psum[h] * sc;
+            if (h == g) { cg = total; wg = wh; sg = sc; }
+            total += wh;
+        }
+        const float target = u * total;
+        const int last = (V - 1) / SL;   // the last CTA with tokens takes a draw that rounds past the total
+        const bool mine = n > 0 && target >= cg && (target < cg + wg || g == last);
+        if (mine) {
+            const float tl = (target - cg) / sg;   // the draw in this slice's units
+            if (t == 0) sh_int[0] = base + n - 1;
             __syncthreads();
-            if (k2) {
-                const int o = s.probs_target && s.d2t ? i2 + s.d2t[i2] : i2;
-                if (o >= 0 && o < s.probs_len) probs[o] = w2 / kept_total;
+            int found = -1;
+            if (incl - part <= tl && tl < incl) {
+                float c = incl - part;
+                for (int i = i0; i < i1; ++i) {
+                    c += __expf((unkey(keys[i]) - mloc) / T);
+                    if (tl < c) { found = i; break; }
+                }
+                if (found < 0) found = i1 - 1;
+            }
+            __syncthreads();
+            if (found >= 0) sh_int[0] = base + found;
+            __syncthreads();
+            token = sh_int[0];
+            qtok = __expf((unkey(keys[token - base]) - m) / T) / total;
+        }
+        if (probs) {
+            for (int i = t; i < n; i += kThreads) {
+                const int v = base + i;
+                const int o = mapped ? v + s.d2t[v] : v;
+                if (o >= 0 && o < s.probs_len) probs[o] = __expf((unkey(keys[i]) - m) / T) / total;
             }
         }
     }
-    if (t == 0) {
+    if (token >= 0 && t == 0) {
         int out = token;
         if (s.d2t) {
             out = token + s.d2t[token];
@@ -517,16 +594,31 @@ __global__ void acceptance_hist_kernel(const int* acc, int batch, int gamma, int
 }
 
 cudaError_t launch_sample(const SampleArgs& s, cudaStream_t st) {
-    if (s.V < 1 || s.V > 32 * smp::kMaxChunks || s.rows < 1 || (s.top_k > smp::kMaxTopK) ||
+    using namespace smp;
+    if (s.V < 1 || s.V > kMaxV || s.rows < 1 || s.rows > 65535 || s.top_k > kMaxTopK ||
         (s.temperature > 0.f && s.top_k <= 0 && s.top_p < 1.f))
         return cudaErrorInvalidValue;
-    {
-        cudaError_t e = smem_optin((const void*)sample_kernel, (int)(smp::kKeyCache * sizeof(uint32_t)));
-        if (e != cudaSuccess) return e;
-    }
-    const bool cached = s.temperature > 0.f && s.top_k > 0 && s.V <= smp::kKeyCache;
-    const size_t smem = cached ? (size_t)s.V * sizeof(uint32_t) : 0;
-    return launch_pdl(sample_kernel, dim3(s.rows), dim3(smp::kThreads), smem, st, s);
+    cudaError_t e = smem_optin((const void*)sample_kernel, kSmemMax + 16);
+    if (e != cudaSuccess) return e;
+    const int SL = (s.V + kCluster - 1) / kCluster;
+    const bool topk = s.temperature > 0.f && s.top_k > 0;
+    const size_t smem = (((size_t)SL * 4 + 15) & ~(size_t)15) +
+                        (topk ? (size_t)kCluster * (s.top_k < s.V ? s.top_k : s.V) * 8 : 0);
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = kCluster;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(kCluster, s.rows);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
+    return cudaLaunchKernelEx(&cfg, sample_kernel, s);
 }
 
 cudaError_t launch_accept_typical(const int* draft, const float* target_probs, int batch, int gamma, int V,

@@ -185,3 +185,34 @@ def test_accept_typical_matches_oracle(B, G, V, conc, eps, dlt):
     assert np.mean(acc == want) >= 0.9
     np.testing.assert_array_equal(hist, np.bincount(acc, minlength=G + 1))
     assert acc[0] == want[0] and acc[1] == 0
+
+
+@pytest.mark.parametrize("V", [5, 100, 8191, 129280])
+@pytest.mark.parametrize("T,k,p", [(0.0, 0, 1.0), (0.9, 0, 1.0), (1.0, 50, 0.9), (0.6, 1024, 1.0)])
+def test_sample_slices_without_d2t(V, T, k, p):
+    # the row is split over the CTAs of a cluster: fewer tokens than CTAs (5), slices of 13 (100), a
+    # ragged last slice (8191) and the full target vocabulary (129280); probabilities in draft ids
+    from eagle_speculative_decoding_eagle3_gb300 import build
+    from eagle_speculative_decoding_eagle3_gb300 import eagle3 as E
+    build.build()
+    rows = 3
+    l = _logits(V * 7 + k, rows, max(V, 32))[:, :V].copy()
+    u = np.random.default_rng(V + 11).random(rows).astype(np.float32)
+    u[0] = 0.0                                          # the first kept token
+    tok = torch.zeros(rows, dtype=torch.int32, device="cuda")
+    tp = torch.zeros(rows, dtype=torch.float32, device="cuda")
+    probs = torch.full((rows, V), -1.0, dtype=torch.float32, device="cuda")
+    E.eagle3_sample(torch.from_numpy(l).cuda(), rows, V, V, T, k, p, torch.from_numpy(u).cuda(), None, 0, tok,
+                    tp, probs, V, False)
+    torch.cuda.synchronize()
+    tok, tp, probs = tok.cpu().numpy(), tp.cpu().numpy(), probs.cpu().numpy()
+    for r in range(rows):
+        t_o, pr_o = O.sample_filtered(l[r], T, k, p, float(u[r]))
+        if tok[r] != t_o:
+            assert tok[r] in _allowed(l[r], T, k, p, float(u[r])), (r, tok[r], t_o)
+            continue
+        assert abs(tp[r] - pr_o[t_o]) <= 1e-4 * max(pr_o[t_o], 1e-3), (r, tp[r], pr_o[t_o])
+        keep_same = p >= 1.0 or len({tuple(np.flatnonzero(O.sample_filtered(l[r], T, k, q, 0.5)[1]))
+                                     for q in (p - EPS, p, min(1.0, p + EPS))}) == 1
+        if keep_same:
+            np.testing.assert_allclose(probs[r], pr_o, atol=2e-6, rtol=1e-4)

@@ -186,6 +186,11 @@ WORKLOADS: dict[str, Workload] = {
     "dsv3_b256": Workload(
         name="dsv3_b256", draft_vocab=32000, batch=256, ctx=(4096, 16384), t_new=1, gamma=7, d2t="sorted",
         accept_p=tuple(0.9 * (0.5 / 0.9) ** (i / 6) for i in range(7)), seed=1004, **_DSV3),
+    # the batch-256 attention shape (contexts U[4096, 16384]) on 32 sequences with a small vocabulary: a
+    # profiler capture of the latent attention holds about 2 GB on the device
+    "dsv3_b256_small": Workload(
+        name="dsv3_b256_small", draft_vocab=4096, batch=32, ctx=(4096, 16384), t_new=1, gamma=3, d2t="sorted",
+        accept_p=(0.9, 0.8, 0.7), seed=1007, **dict(_DSV3, target_vocab=8192)),
     # the Llama-style MHA head on the same target: tiny fp32 head (2-way fc, 4 query heads per key/value
     # head) and a DeepseekV3-width head (hidden 7168 = 56 heads x 128, 8 key/value heads, 3-way fc) at
     # batch 1; no MHA head configuration is printed on the pages, these sizes are a reading
