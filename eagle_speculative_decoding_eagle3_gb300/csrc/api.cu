@@ -535,16 +535,38 @@ struct Lin {
 
 bool use_tc(const eagle3_draft& d, int M) { return d.tc_ok && M > kGemvMaxRows; }
 
-// split-K count for a tensor-core GEMM: enough CTAs to stream the weights with every SM
+// Split-K count for a tensor-core GEMM: the count that minimises a wave model of the launch.  One CTA
+// per SM at a time; a CTA streams its share of the weight tile at the SM's share of the HBM bandwidth (or
+// runs its MMAs, when they take longer), plus a fixed start and drain cost; CTAs run in waves of num_sms,
+// so a grid just past a multiple of the SM count pays a whole extra wave.  Every split adds a write and a
+// read of the fp32 partial planes, and the reduction kernel's launch.  Fewer splits win ties.
 int tc_splits(const eagle3_draft& d, int M, int N, int K, int bn, bool glu) {
     const long tiles = (long)((N + 127) / 128) * ((M + bn - 1) / bn);
-    if (tiles >= d.num_sms) return 1;
-    long s = (2L * d.num_sms + tiles - 1) / tiles;
-    const long kmax = K / 64 / 4;                // at least 4 K-blocks per split
-    if (s > kmax) s = kmax;
-    const long per = (long)(glu ? 2 : 1) * M * N * 4;
-    while (s > 1 && s * per > (long)kSplitKBytes) --s;
-    return s < 1 ? 1 : (int)s;
+    const int nkb = K / 64;
+    const int smax = nkb / 4 < 64 ? nkb / 4 : 64;   // at least 4 K-blocks per split
+    if (smax < 2) return 1;
+    const double hbm = 6.0e12, sm_bw = hbm / d.num_sms;   // achievable bytes/s, whole GPU and per SM
+    const double mac_rate = 7.0e12;                       // dense bf16 MACs/s of one SM's tensor core
+    const double c0 = 2.0e-6, c_sum = 4.0e-6;             // per-CTA start/drain; the reduction launch
+    const double np = glu ? 2.0 : 1.0;
+    const double plane = np * M * N * 4.0;
+    int best = 1;
+    double t_best = 1e30;
+    for (int s = 1; s <= smax; ++s) {
+        const int per = (nkb + s - 1) / s, eff = (nkb + per - 1) / per;   // the launcher's split count
+        if (eff != s) continue;
+        if (s > 1 && s * plane > (double)kSplitKBytes) break;
+        const long waves = (tiles * s + d.num_sms - 1) / d.num_sms;
+        const double t_mem = np * 128.0 * per * 64 * 2 / sm_bw;
+        const double t_mma = np * 128.0 * bn * per * 64 / mac_rate;
+        double t = waves * ((t_mem > t_mma ? t_mem : t_mma) + c0);
+        if (s > 1) t += 2.0 * s * plane / hbm + c_sum;
+        if (t < 0.97 * t_best) {
+            t_best = t;
+            best = s;
+        }
+    }
+    return best;
 }
 
 cudaError_t run_linear(eagle3_draft& d, const Lin& L, int kind, cudaStream_t st) {

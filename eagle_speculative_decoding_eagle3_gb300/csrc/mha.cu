@@ -15,6 +15,7 @@
 
 #include "common.cuh"
 #include "kernels.h"
+#include "mma_sync.cuh"
 #include "../../include/eagle3.h"
 
 namespace e3 {
@@ -65,13 +66,20 @@ __global__ void __launch_bounds__(kMhaAppendThreads) mha_rope_append_kernel(cons
     if (vcopy) dst[nkv * d + i] = from_f<T>(kv[nkv * d + i]);
 }
 
-// One CTA: row r, key/value head g, slots [s chunk, min((s + 1) chunk, pos + 1)).  Scores: each lane
-// takes one slot of a 32-slot tile and forms the G dot products over the whole key row (the G query
-// rows sit in shared memory and are read as broadcasts).  Values: each lane owns d/32 output dimensions
-// of every head and walks the tile's slots, with each slot's probabilities shuffled from its lane.
+// One CTA: row r, key/value head g, slots [s chunk, min((s + 1) chunk, pos + 1)).  Each warp takes
+// 32-slot tiles in turn.  The tile's value rows go to the warp's shared-memory buffer by cp.async first;
+// meanwhile each lane loads its slot's whole key row (every load of the row in flight at once) and forms
+// the G dot products (the G query rows sit in shared memory and are read as broadcasts).  Values: each
+// lane owns d/32 output dimensions of every head and walks the staged rows, with each slot's
+// probabilities shuffled from its lane.
+template <typename T, int D>
+constexpr int mha_vstage_bytes() { return kMhaWarps * 32 * D * (int)sizeof(T); }
+
 template <typename T, int D, int G>
 __global__ void __launch_bounds__(kMhaThreads) mha_attention_kernel(const MhaArgs a) {
     constexpr int DL = D / 32;                       // output dimensions per lane
+    constexpr int CPR = D * (int)sizeof(T) / 16;     // 16-byte chunks of a value row
+    extern __shared__ __align__(16) unsigned char mha_dyn[];
     __shared__ float qs[G][D];
     __shared__ float wm[kMhaWarps][G], wl[kMhaWarps][G];
     __shared__ float so[G][D];
@@ -99,6 +107,7 @@ __global__ void __launch_bounds__(kMhaThreads) mha_attention_kernel(const MhaArg
 #pragma unroll
         for (int e = 0; e < DL; ++e) o[h][e] = 0.f;
     }
+    T* vs = reinterpret_cast<T*>(mha_dyn) + (long)warp * 32 * D;   // this warp's staged value rows
     for (int tb = start + 32 * warp; tb < end; tb += 32 * kMhaWarps) {
         const int j = tb + lane;
         bool valid = j < end;
@@ -113,15 +122,30 @@ __global__ void __launch_bounds__(kMhaThreads) mha_attention_kernel(const MhaArg
                 off = ((long)page * a.page_size + j % a.page_size) * rowlen;
             }
         }
+        // the tile's value rows into shared memory (chunk c: row c / CPR, 16 bytes c % CPR)
+        __syncwarp();                                // the previous tile's rows have been read
+#pragma unroll 4
+        for (int c = lane; c < 32 * CPR; c += 32) {
+            const int row = c / CPR, q = c % CPR;
+            const long ro = __shfl_sync(0xffffffffu, off, row);
+            const bool rv = __shfl_sync(0xffffffffu, valid ? 1 : 0, row) != 0;
+            if (rv)
+                cp_async16(smem_u32(vs + (long)row * D) + 16 * q,
+                           reinterpret_cast<const unsigned char*>(cache + ro + (long)a.nkv * D + (long)g * D) + 16 * q);
+        }
+        cp_async_commit();
         float sc[G];
 #pragma unroll
         for (int h = 0; h < G; ++h) sc[h] = 0.f;
         if (valid) {
             const T* kr = cache + off + (long)g * D;
-#pragma unroll 4
+            Raw8<T> kraw[D / 8];
+#pragma unroll
+            for (int c = 0; c < D / 8; ++c) kraw[c] = ld8<false>(kr + 8 * c);
+#pragma unroll
             for (int c = 0; c < D / 8; ++c) {
                 float kv8[8];
-                widen(ld8<false>(kr + 8 * c), kv8);
+                widen(kraw[c], kv8);
 #pragma unroll
                 for (int h = 0; h < G; ++h)
 #pragma unroll
@@ -143,11 +167,13 @@ __global__ void __launch_bounds__(kMhaThreads) mha_attention_kernel(const MhaArg
             m[h] = mn;
         }
         const int nt = min(32, end - tb);
+        const unsigned vmask = __ballot_sync(0xffffffffu, valid);
+        cp_async_wait<0>();
+        __syncwarp();
+#pragma unroll 4
         for (int jj = 0; jj < nt; ++jj) {
-            const long voff = __shfl_sync(0xffffffffu, off, jj);
-            const bool vval = __shfl_sync(0xffffffffu, valid ? 1 : 0, jj) != 0;
-            if (!vval) continue;
-            const T* vr = cache + voff + (long)a.nkv * D + (long)g * D + lane * DL;
+            if (!((vmask >> jj) & 1u)) continue;     // a slot without a row (flagged) adds nothing
+            const T* vr = vs + (long)jj * D + lane * DL;
             float v[DL];
 #pragma unroll
             for (int e = 0; e < DL; ++e) v[e] = to_f(vr[e]);
@@ -258,14 +284,22 @@ cudaError_t launch_mha_rope_append(const MhaArgs& a, cudaStream_t st) {
     return launch_pdl(mha_rope_append_kernel<float>, grid, dim3(kMhaAppendThreads), 0, st, a);
 }
 
+template <typename T, int D, int G>
+static cudaError_t launch_attn_dg(const MhaArgs& a, dim3 grid, cudaStream_t st) {
+    constexpr int smem = mha_vstage_bytes<T, D>();
+    cudaError_t e = smem_optin((const void*)mha_attention_kernel<T, D, G>, smem);
+    if (e != cudaSuccess) return e;
+    return launch_pdl(mha_attention_kernel<T, D, G>, grid, dim3(kMhaThreads), (size_t)smem, st, a);
+}
+
 template <typename T, int D>
 static cudaError_t launch_attn_g(const MhaArgs& a, dim3 grid, cudaStream_t st) {
     switch (a.nh / a.nkv) {
-        case 1: return launch_pdl(mha_attention_kernel<T, D, 1>, grid, dim3(kMhaThreads), 0, st, a);
-        case 2: return launch_pdl(mha_attention_kernel<T, D, 2>, grid, dim3(kMhaThreads), 0, st, a);
-        case 4: return launch_pdl(mha_attention_kernel<T, D, 4>, grid, dim3(kMhaThreads), 0, st, a);
-        case 7: return launch_pdl(mha_attention_kernel<T, D, 7>, grid, dim3(kMhaThreads), 0, st, a);
-        case 8: return launch_pdl(mha_attention_kernel<T, D, 8>, grid, dim3(kMhaThreads), 0, st, a);
+        case 1: return launch_attn_dg<T, D, 1>(a, grid, st);
+        case 2: return launch_attn_dg<T, D, 2>(a, grid, st);
+        case 4: return launch_attn_dg<T, D, 4>(a, grid, st);
+        case 7: return launch_attn_dg<T, D, 7>(a, grid, st);
+        case 8: return launch_attn_dg<T, D, 8>(a, grid, st);
         default: return cudaErrorInvalidValue;
     }
 }

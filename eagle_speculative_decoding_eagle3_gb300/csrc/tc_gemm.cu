@@ -286,13 +286,55 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
     }
 }
 
-// Split-K reduction: out = epi(sum_z part[z]) for STORE / RESID / GLU.
+// Split-K reduction: out = epi(sum_z part[z]) for STORE / RESID / GLU, the planes summed in split order.
+// With N a multiple of 4 a thread takes four consecutive outputs and keeps four planes' loads in flight.
 __global__ void tc_splitk_reduce(const TcParams p, int splits, int glu) {
     pdl_trigger();
     pdl_wait();
     const long total = (long)p.M * p.N;
     const long plane = total;
     const int np = glu ? 2 : 1;
+    if ((p.N & 3) == 0) {
+        for (long i4 = blockIdx.x * (long)blockDim.x + threadIdx.x; i4 < total / 4; i4 += (long)gridDim.x * blockDim.x) {
+            const long i = 4 * i4;
+            float v[4] = {0.f, 0.f, 0.f, 0.f}, u[4] = {0.f, 0.f, 0.f, 0.f};
+            int z = 0;
+            for (; z + 4 <= splits; z += 4) {
+                float4 a[4], b[4];
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    a[q] = __ldcg(reinterpret_cast<const float4*>(p.part + (long)(z + q) * np * plane + i));
+                    if (glu) b[q] = __ldcg(reinterpret_cast<const float4*>(p.part + (long)(z + q) * np * plane + plane + i));
+                }
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    v[0] += a[q].x; v[1] += a[q].y; v[2] += a[q].z; v[3] += a[q].w;
+                    if (glu) { u[0] += b[q].x; u[1] += b[q].y; u[2] += b[q].z; u[3] += b[q].w; }
+                }
+            }
+            for (; z < splits; ++z) {
+                const float4 a = __ldcg(reinterpret_cast<const float4*>(p.part + (long)z * np * plane + i));
+                v[0] += a.x; v[1] += a.y; v[2] += a.z; v[3] += a.w;
+                if (glu) {
+                    const float4 b = __ldcg(reinterpret_cast<const float4*>(p.part + (long)z * np * plane + plane + i));
+                    u[0] += b.x; u[1] += b.y; u[2] += b.z; u[3] += b.w;
+                }
+            }
+            const long m = i / p.N, n = i % p.N;
+            float r[4] = {0.f, 0.f, 0.f, 0.f};
+            if (!glu && p.epi == EPI_RESID) {
+#pragma unroll
+                for (int e = 0; e < 4; ++e) r[e] = p.resid[m * p.ldr + n + e];
+            }
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const float out = glu ? silu(v[e]) * u[e] : v[e] + r[e];
+                if (p.y) p.y[m * p.ldy + n + e] = out;
+                if (p.ybf) p.ybf[m * p.ldybf + n + e] = __float2bfloat16_rn(out);
+            }
+        }
+        return;
+    }
     for (long i = blockIdx.x * (long)blockDim.x + threadIdx.x; i < total; i += (long)gridDim.x * blockDim.x) {
         float v = 0.f, u = 0.f;
         for (int z = 0; z < splits; ++z) {
@@ -402,7 +444,8 @@ cudaError_t launch_tc_gemm(TcParams& p, int bn, int splits, cudaStream_t st) {
 #undef TC_CASE
     if (e != cudaSuccess || splits == 1) return e;
     const long total = (long)p.M * p.N;
-    int blocks = (int)((total + 255) / 256);
+    const long items = (p.N & 3) == 0 ? total / 4 : total;
+    int blocks = (int)((items + 255) / 256);
     if (blocks > 4096) blocks = 4096;
     return launch_pdl(tc::tc_splitk_reduce, dim3(blocks), dim3(256), 0, st, p, splits, glu ? 1 : 0);
     return cudaGetLastError();
