@@ -645,8 +645,15 @@ cudaError_t run_linear(eagle3_draft& d, const Lin& L, int kind, cudaStream_t st)
     int splits = L.epi == EPI_ARGMAX ? 1 : tc_splits(d, L.M, L.N, L.K, bn, glu);
     // Large problems take 256 weight rows per CTA: the staged activation tile then feeds two MMAs,
     // halving the shared-memory traffic per FLOP, which bounds 128-row tiles on long-K layers.
+    // Persistent CTAs (one per SM, the next tile's loads and MMAs overlapping this tile's epilogue) for
+    // unsplit one-matrix GEMMs with more tiles than SMs whose epilogue is a large share of a tile: the
+    // lm_head's argmax, short K, or a single token tile (decode batches).
+    const long tiles = (long)((L.N + 127) / 128) * ((L.M + bn - 1) / bn);
+    const bool persist = !glu && splits == 1 && tiles > d.num_sms && (L.epi == EPI_ARGMAX || L.K <= 1024 || L.M <= bn);
     const long pair_tiles = (long)((L.N + 255) / 256) * ((L.M + bn - 1) / bn);
-    if (!glu && L.epi != EPI_ARGMAX && bn == 256 && pair_tiles >= 2L * d.num_sms) {
+    if (persist) {
+        p.persist = d.num_sms;
+    } else if (!glu && L.epi != EPI_ARGMAX && bn == 256 && pair_tiles >= 2L * d.num_sms) {
         p.pair = 1;
         splits = 1;
     }

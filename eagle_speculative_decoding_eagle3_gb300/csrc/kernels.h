@@ -259,6 +259,8 @@ struct TcParams {
     int epi;                      // EPI_STORE / EPI_RESID / EPI_GLU / EPI_ARGMAX
     int pair;                     // STORE / RESID at 256 tokens per tile: each CTA takes two 128-row
                                   // weight tiles that share the activation tile (0 = one tile)
+    int persist;                  // > 0: one-matrix, unsplit GEMMs with more tiles than this run on this
+                                  // many persistent CTAs (double-buffered TMEM accumulators); 0 = a CTA per tile
     float* y; long ldy;           // fp32 output (optional)
     __nv_bfloat16* ybf; long ldybf;  // bf16 output (optional)
     const float* resid; long ldr;

@@ -85,20 +85,31 @@ __device__ float block_inclusive_scan(float v, float* warp_tot) {
 }
 
 // bitonic sort of the first n (a power of two <= kThreads) packed (key, index) pairs in shared memory,
-// ascending
+// ascending.  Thread t holds element t in a register; a compare-exchange with a partner in the same warp
+// (distance j < 32) goes through a shuffle, only the longer distances through shared memory and barriers.
 __device__ void bitonic_sort(unsigned long long* a, int n) {
     const int t = threadIdx.x;
+    unsigned long long v = t < n ? a[t] : ~0ull;
     for (int k = 2; k <= n; k <<= 1) {
         for (int j = k >> 1; j > 0; j >>= 1) {
-            const int p = t ^ j;
-            if (t < n && p > t) {
-                const bool up = (t & k) == 0;
-                const unsigned long long x = a[t], y = a[p];
-                if ((x > y) == up) { a[t] = y; a[p] = x; }
+            unsigned long long w;
+            if (j >= 32) {
+                __syncthreads();   // the previous exchange's reads are done
+                if (t < n) a[t] = v;
+                __syncthreads();
+                w = t < n ? a[t ^ j] : v;
+            } else {
+                w = __shfl_xor_sync(0xffffffffu, v, j);
             }
-            __syncthreads();
+            // of the pair (t, t ^ j) the lower index keeps the minimum in an ascending block (t & k) == 0
+            const bool up = (t & k) == 0, lower = (t & j) == 0;
+            const unsigned long long lo = v < w ? v : w, hi = v < w ? w : v;
+            v = up == lower ? lo : hi;
         }
     }
+    __syncthreads();
+    if (t < n) a[t] = v;
+    __syncthreads();
 }
 
 struct SelectShared {

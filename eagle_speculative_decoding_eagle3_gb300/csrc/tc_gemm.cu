@@ -286,6 +286,255 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
     }
 }
 
+// Persistent variant for one-matrix GEMMs with more output tiles than SMs and no split (the lm_head with its
+// argmax, q_b, and short-K GEMMs of an extend).  One CTA per SM walks the tiles lin = blockIdx.x,
+// + gridDim.x, ... in the grouped order above.  The TMA ring runs across tile boundaries and two TMEM
+// accumulators alternate (MMA into one while the epilogue warps drain the other), so a tile's epilogue
+// and the next tile's pipeline fill overlap its neighbours' loads and MMAs.  The epilogue scratch (the
+// argmax partials of the four warps, or the staged bf16 output tile) has its own shared memory, since
+// the ring keeps streaming.
+template <int BN> struct PCfg {
+    static constexpr int P_BYTES = BM * BK * 2;
+    static constexpr int Q_BYTES = BN * BK * 2;
+    static constexpr int STAGE = P_BYTES + Q_BYTES;
+    static constexpr int OPITCH = BM + 8;                  // staged row pitch (bf16), 16-byte multiple
+    static constexpr int OBUF = BN * OPITCH * 2;
+    static constexpr int ABUF = 4 * BN * 8;
+    static constexpr int SCRATCH = ((OBUF > ABUF ? OBUF : ABUF) + 1023) / 1024 * 1024;
+    static constexpr int STAGES0 = (222 * 1024 - SCRATCH - 2048) / STAGE;
+    static constexpr int STAGES = STAGES0 > 6 ? 6 : STAGES0;
+    static constexpr int TMEM_COLS = 2 * BN <= 32 ? 32 : 2 * BN <= 64 ? 64 : 2 * BN <= 128 ? 128 : 2 * BN <= 256 ? 256 : 512;
+    static constexpr int SMEM = STAGES * STAGE + SCRATCH + 1024 + 256;
+    static_assert(STAGES >= 2, "at least a double-buffered ring");
+    static_assert(SMEM <= 227 * 1024, "shared memory");
+};
+
+template <int BN>
+__global__ void __launch_bounds__(kThreads, 1) tc_gemm_persist_kernel(const __grid_constant__ TcParams p) {
+    pdl_trigger();
+    using C = PCfg<BN>;
+    constexpr int S = C::STAGES;
+    extern __shared__ unsigned char smem_raw[];
+    unsigned char* base = reinterpret_cast<unsigned char*>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+    unsigned char* scratch = base + S * C::STAGE;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(scratch + C::SCRATCH);
+    // bars[0..S) full, bars[S..2S) empty, bars[2S + b] accumulator b ready, bars[2S + 2 + b] accumulator b free
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * S + 4);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+    auto bar = [&](int i) { return su32(&bars[i]); };
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int nx = (p.N + BM - 1) / BM, ny = (p.M + BN - 1) / BN, ntiles = nx * ny;
+    const int my_tiles = blockIdx.x < ntiles ? (ntiles - 1 - blockIdx.x) / gridDim.x + 1 : 0;
+    auto tile_of = [&](int lin, int& ntile, int& mtile) {
+        if (ny > 1) {
+            constexpr int G = 8;
+            const int g = lin / (G * nx), in = lin % (G * nx);
+            const int gsize = min(G, ny - g * G);
+            mtile = g * G + in % gsize;
+            ntile = in / gsize;
+        } else {
+            ntile = lin;
+            mtile = 0;
+        }
+    };
+    const int nkb = p.nkb;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < S; ++s) {
+            mbar_init(bar(s), 1);
+            mbar_init(bar(S + s), 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(bar(2 * S + b), 1);
+            mbar_init(bar(2 * S + 2 + b), 4);   // one arrival per epilogue warp
+        }
+        *abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(su32(tmem_slot)),
+                     "r"(C::TMEM_COLS));
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    int issued = 0;
+    pdl_wait();
+
+    if (warp == 0 && lane == 0 && nkb > 0) {
+        // ---------------- TMA producer: every k-block of every tile of this CTA, one ring
+        int i = 0;
+        for (int t = 0; t < my_tiles; ++t) {
+            int ntile, mtile;
+            tile_of(blockIdx.x + t * gridDim.x, ntile, mtile);
+            const int n0 = ntile * BM, m0 = mtile * BN;
+            const bool second = n0 >= p.np0;
+            const CUtensorMap* mw = second ? &p.mw[1] : &p.mw[0];
+            const int wrow = second ? n0 - p.np0 : n0;
+            for (int kb = 0; kb < nkb; ++kb, ++i) {
+                const int s = i % S;
+                if (!mbar_wait(bar(S + s), ((uint32_t)(i / S) & 1u) ^ 1u)) { *abort_flag = 1; break; }
+                if (*abort_flag) break;
+                unsigned char* st = base + s * C::STAGE;
+                const uint32_t full = bar(s);
+                mbar_expect_tx(full, C::STAGE);
+                tma_load_2d(su32(st), mw, full, kb * BK, wrow);
+                const int qs = kb >= p.kseg[1] ? 2 : (kb >= p.kseg[0] ? 1 : 0);
+                const int kl = kb - (qs == 0 ? 0 : p.kseg[qs - 1]);
+                tma_load_2d(su32(st + C::P_BYTES), &p.mx[qs], full, kl * BK, m0);
+                ++issued;
+            }
+            if (*abort_flag) break;
+        }
+    } else if (warp == 1 && lane == 0 && nkb > 0) {
+        // ---------------- MMA issuer: tile t accumulates into TMEM columns [BN (t & 1), + BN)
+        constexpr uint32_t idesc = instr_desc(BN);
+        int i = 0;
+        bool ok = true;
+        for (int t = 0; t < my_tiles && ok; ++t) {
+            const int b = t & 1;
+            ok = mbar_wait(bar(2 * S + 2 + b), ((uint32_t)(t >> 1) & 1u) ^ 1u) && !*abort_flag;
+            if (!ok) break;
+            tc_fence_after();
+            for (int kb = 0; kb < nkb; ++kb, ++i) {
+                const int s = i % S;
+                if (!mbar_wait(bar(s), (uint32_t)(i / S) & 1u)) { ok = false; break; }
+                tc_fence_after();
+                const uint32_t st = su32(base + s * C::STAGE);
+                const uint64_t da = smem_desc(st), db = smem_desc(st + C::P_BYTES);
+#pragma unroll
+                for (int kk = 0; kk < BK / 16; ++kk)
+                    mma_bf16(tmem + BN * b, da + 2 * kk, db + 2 * kk, idesc, (kb > 0 || kk > 0) ? 1u : 0u);
+                mma_commit(bar(S + s));
+            }
+            if (ok) mma_commit(bar(2 * S + b));
+        }
+        if (!ok) *abort_flag = 1;
+    } else if (warp >= 2) {
+        // ---------------- epilogue: TMEM lanes [32q, 32q + 32) are readable by warp q = warp % 4
+        const int q = warp & 3;
+        const int et = threadIdx.x - 64;   // 0..127 over the four epilogue warps
+        const bool staged = p.epi != EPI_ARGMAX && p.epi != EPI_RESID && p.y == nullptr && p.ybf != nullptr;
+        __nv_bfloat16* obuf = reinterpret_cast<__nv_bfloat16*>(scratch);
+        float* rv = reinterpret_cast<float*>(scratch);
+        int* ri = reinterpret_cast<int*>(scratch + 4 * BN * sizeof(float));
+        constexpr int CW = BN >= 32 ? 32 : 16;
+        for (int t = 0; t < my_tiles; ++t) {
+            const int b = t & 1;
+            int ntile, mtile;
+            tile_of(blockIdx.x + t * gridDim.x, ntile, mtile);
+            const int n0 = ntile * BM, m0 = mtile * BN;
+            const int n = n0 + 32 * q + lane;
+            const bool nvalid = n < p.N;
+            // every epilogue warp runs every tile (the named barriers below count on it); after a wait ran
+            // out the tiles are written as zeros
+            bool ok = nkb > 0 && !*abort_flag && mbar_wait(bar(2 * S + b), (uint32_t)(t >> 1) & 1u);
+            ok = __all_sync(0xffffffffu, ok);   // tcgen05.ld is warp-collective
+            if (!ok && nkb > 0) *abort_flag = 1;
+            tc_fence_after();
+            const uint32_t trow = tmem + BN * b + ((uint32_t)(32 * q) << 16);
+            for (int c = 0; c < BN; c += CW) {
+                float v[CW];
+                if (ok) {
+                    if (CW == 32) tmem_ld32(trow + c, v);
+                    else tmem_ld16(trow + c, v);
+                } else {
+#pragma unroll
+                    for (int j = 0; j < CW; ++j) v[j] = 0.f;
+                }
+                if (p.epi == EPI_ARGMAX) {
+                    // per token: (max, argmax) over this warp's 32 features, lowest index on ties
+#pragma unroll
+                    for (int j = 0; j < CW; ++j) {
+                        float bvv = nvalid ? v[j] : -FLT_MAX;
+                        int bi = nvalid ? n : INT_MAX;
+                        const int m = m0 + c + j;
+                        if (p.logits && nvalid && m < p.M) p.logits[(long)m * p.ldl + n] = v[j];
+#pragma unroll
+                        for (int o = 16; o > 0; o >>= 1) {
+                            const float ov = __shfl_xor_sync(0xffffffffu, bvv, o);
+                            const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+                            if (better(ov, oi, bvv, bi)) { bvv = ov; bi = oi; }
+                        }
+                        if (lane == 0) {
+                            rv[q * BN + c + j] = bvv;
+                            ri[q * BN + c + j] = bi;
+                        }
+                    }
+                    continue;
+                }
+                float rr[CW];
+                if (p.epi == EPI_RESID) {
+#pragma unroll
+                    for (int j = 0; j < CW; ++j) {
+                        const int m = m0 + c + j;
+                        rr[j] = (nvalid && m < p.M) ? p.resid[(long)m * p.ldr + n] : 0.f;
+                    }
+                }
+#pragma unroll
+                for (int j = 0; j < CW; ++j) {
+                    const int m = m0 + c + j;
+                    if (!nvalid || m >= p.M) continue;
+                    const float out = p.epi == EPI_RESID ? v[j] + rr[j] : v[j];
+                    if (staged) {
+                        obuf[(c + j) * C::OPITCH + (n - n0)] = __float2bfloat16_rn(out);
+                        continue;
+                    }
+                    if (p.y) p.y[(long)m * p.ldy + n] = out;
+                    if (p.ybf) p.ybf[(long)m * p.ldybf + n] = __float2bfloat16_rn(out);
+                }
+            }
+            // the accumulator is read out: the MMA warp may start the tile after next in it
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(2 * S + 2 + b));
+            if (staged || p.epi == EPI_ARGMAX) {
+                asm volatile("bar.sync 1, 128;" ::: "memory");   // the four epilogue warps
+                if (staged) {
+                    constexpr int CPR = BM / 8;                   // 16-byte chunks per staged row
+                    for (int i = et; i < BN * CPR; i += 128) {
+                        const int row = i / CPR, ch = i % CPR;
+                        const int m = m0 + row, nf = n0 + ch * 8;
+                        if (m >= p.M || nf >= p.N) continue;
+                        *reinterpret_cast<uint4*>(p.ybf + (long)m * p.ldybf + nf) =
+                            *reinterpret_cast<const uint4*>(obuf + row * C::OPITCH + ch * 8);
+                    }
+                } else {
+                    for (int j = et; j < BN; j += 128) {
+                        const int m = m0 + j;
+                        if (m >= p.M) continue;
+                        float bb = rv[j];
+                        int bi = ri[j];
+                        for (int w = 1; w < 4; ++w)
+                            if (better(rv[w * BN + j], ri[w * BN + j], bb, bi)) { bb = rv[w * BN + j]; bi = ri[w * BN + j]; }
+                        p.pval[(long)m * p.npart + ntile] = bb;
+                        p.pidx[(long)m * p.npart + ntile] = bi;
+                    }
+                }
+                asm volatile("bar.sync 1, 128;" ::: "memory");   // scratch is free for the next tile
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (*abort_flag) {
+        if (threadIdx.x == 0) atomicOr(p.err, EAGLE3_DEVERR_TIMEOUT);
+        // drain this CTA's own copies still in flight (bounded) before its shared memory goes away
+        if (warp == 0 && lane == 0) {
+            for (int i = max(0, issued - S); i < issued; ++i)
+                mbar_wait(bar(i % S), (uint32_t)(i / S) & 1u);
+        }
+        __syncthreads();
+    }
+    if (warp == 1) {
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(C::TMEM_COLS));
+    }
+}
+
 // Split-K reduction: out = epi(sum_z part[z]) for STORE / RESID / GLU, the planes summed in split order.
 // With N a multiple of 4 a thread takes four consecutive outputs and keeps four planes' loads in flight.
 __global__ void tc_splitk_reduce(const TcParams p, int splits, int glu) {
@@ -394,6 +643,14 @@ bool make_tma_chunks(CUtensorMap* map, const void* ptr, long rows, long cols, in
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+template <int BN>
+static cudaError_t tc_launch_persist(const TcParams& p, int ctas, cudaStream_t st) {
+    using C = tc::PCfg<BN>;
+    cudaError_t e = smem_optin((const void*)tc::tc_gemm_persist_kernel<BN>, (int)C::SMEM);
+    if (e != cudaSuccess) return e;
+    return launch_pdl(tc::tc_gemm_persist_kernel<BN>, dim3(ctas), dim3(tc::kThreads), (size_t)C::SMEM, st, p);
+}
+
 template <int BN, int MODE>
 static cudaError_t tc_launch_bn(const TcParams& p, dim3 grid, cudaStream_t st) {
     using C = tc::Cfg<BN, MODE>;
@@ -427,6 +684,18 @@ cudaError_t launch_tc_gemm(TcParams& p, int bn, int splits, cudaStream_t st) {
     dim3 grid((p.N + rows_per_cta - 1) / rows_per_cta, (p.M + bn - 1) / bn, splits * p.nbatch);
     if (p.epi == EPI_ARGMAX) p.npart = grid.x;
     cudaError_t e;
+    const long tiles = (long)grid.x * grid.y;
+    if (p.persist > 0 && !pair && !glu && splits == 1 && p.nbatch == 1 && tiles > p.persist) {
+        const int ctas = p.persist;
+        switch (bn) {
+            case 16: return tc_launch_persist<16>(p, ctas, st);
+            case 32: return tc_launch_persist<32>(p, ctas, st);
+            case 64: return tc_launch_persist<64>(p, ctas, st);
+            case 128: return tc_launch_persist<128>(p, ctas, st);
+            case 256: return tc_launch_persist<256>(p, ctas, st);
+            default: return cudaErrorInvalidValue;
+        }
+    }
 #define TC_CASE(B)                                                                                       \
     case B:                                                                                              \
         e = glu ? tc_launch_bn<B, tc::kGlu>(p, grid, st) : tc_launch_bn<B, tc::kSingle>(p, grid, st);   \
