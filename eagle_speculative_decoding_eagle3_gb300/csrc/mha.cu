@@ -257,11 +257,21 @@ __global__ void __launch_bounds__(256) mha_merge_kernel(const MhaArgs a) {
     __syncthreads();
     float M = red[0];
     for (int w = 1; w < (int)(blockDim.x + 31) / 32; ++w) M = fmaxf(M, red[w]);
+    // eight splits' partial outputs in flight at a time (independent loads, then the weighted sum in
+    // split order)
     float L = 0.f, acc = 0.f;
-    for (int s = 0; s < nvalid; ++s) {
-        const float f = sm[s] == -INFINITY ? 0.f : __expf(sm[s] - M);
-        L += f * sl[s];
-        if (e < a.d) acc += f * a.part_o[((pr0 + s) * a.nh + h) * a.d + e];
+    for (int s0 = 0; s0 < nvalid; s0 += 8) {
+        float po[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u)
+            po[u] = (s0 + u < nvalid && e < a.d) ? a.part_o[((pr0 + s0 + u) * a.nh + h) * a.d + e] : 0.f;
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            if (s0 + u >= nvalid) break;
+            const float f = sm[s0 + u] == -INFINITY ? 0.f : __expf(sm[s0 + u] - M);
+            L += f * sl[s0 + u];
+            acc += f * po[u];
+        }
     }
     if (e < a.d) {
         const float v = acc / L;

@@ -191,6 +191,11 @@ WORKLOADS: dict[str, Workload] = {
     "dsv3_b256_small": Workload(
         name="dsv3_b256_small", draft_vocab=4096, batch=32, ctx=(4096, 16384), t_new=1, gamma=3, d2t="sorted",
         accept_p=(0.9, 0.8, 0.7), seed=1007, **dict(_DSV3, target_vocab=8192)),
+    # the batch-64 decode shape with a 32000-entry vocabulary (no d2t): its lm_head still has more output
+    # tiles than SMs (the persistent GEMM), while a profiler capture holds about 3 GB on the device
+    "dsv3_b64_small": Workload(
+        name="dsv3_b64_small", draft_vocab=32000, batch=64, ctx=(1024, 8192), t_new=1, gamma=3, d2t=None,
+        accept_p=(0.7, 0.7, 0.7), seed=1008, **dict(_DSV3, target_vocab=32000)),
     # the Llama-style MHA head on the same target: tiny fp32 head (2-way fc, 4 query heads per key/value
     # head) and a DeepseekV3-width head (hidden 7168 = 56 heads x 128, 8 key/value heads, 3-way fc) at
     # batch 1; no MHA head configuration is printed on the pages, these sizes are a reading
