@@ -649,7 +649,7 @@ cudaError_t run_linear(eagle3_draft& d, const Lin& L, int kind, cudaStream_t st)
     // unsplit one-matrix GEMMs with more tiles than SMs whose epilogue is a large share of a tile: the
     // lm_head's argmax, short K, or a single token tile (decode batches).
     const long tiles = (long)((L.N + 127) / 128) * ((L.M + bn - 1) / bn);
-    const bool persist = !glu && splits == 1 && tiles > d.num_sms && (L.epi == EPI_ARGMAX || L.K <= 1024 || L.M <= bn);
+    const bool persist = !glu && splits == 1 && tiles > d.num_sms && (L.epi == EPI_ARGMAX || L.K <= 2048 || L.M <= bn);
     const long pair_tiles = (long)((L.N + 255) / 256) * ((L.M + bn - 1) / bn);
     if (persist) {
         p.persist = d.num_sms;
@@ -1205,7 +1205,8 @@ eagle3_status_t eagle3_sample(const float* logits, int32_t rows, int32_t V, int6
                               const eagle3_sampling_t* params, const float* uniforms, const int32_t* d2t,
                               int32_t target_vocab, int32_t* tokens, float* token_prob, float* probs,
                               int32_t probs_len, int32_t probs_in_target, void* stream) {
-    if (!logits || !uniforms || !tokens || rows < 1 || V < 1 || V > 131072 || ld < V || !sampling_ok(params))
+    if (!logits || !uniforms || !tokens || rows < 1 || rows > 65535 || V < 1 || V > 131072 || ld < V ||
+        !sampling_ok(params))
         return EAGLE3_ERR_INVALID_ARG;
     if (d2t && target_vocab < 1) return EAGLE3_ERR_INVALID_ARG;
     if (probs && probs_len < (probs_in_target && d2t ? target_vocab : V)) return EAGLE3_ERR_INVALID_ARG;

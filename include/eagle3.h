@@ -318,8 +318,9 @@ typedef struct {
  *   token_prob   [rows] fp32 out or NULL: the drawn token's final probability
  *   probs        [rows, probs_len] fp32 out or NULL: the final distribution, indexed by target ids when
  *                probs_in_target is non-zero (zeros elsewhere), else by draft ids
- * One CTA per row.  Returns EAGLE3_ERR_INVALID_ARG for null required pointers, rows or V < 1, V > 131072, ld < V,
- * top_k outside 0..1024, top_p outside (0, 1], top_p < 1 without top_k, or a negative temperature. */
+ * One thread-block cluster of 8 CTAs per row, each CTA owning an eighth of the row's logits.  Returns
+ * EAGLE3_ERR_INVALID_ARG for null required pointers, rows outside 1..65535, V < 1, V > 131072, ld < V, top_k
+ * outside 0..1024, top_p outside (0, 1], top_p < 1 without top_k, or a negative temperature. */
 EAGLE3_API eagle3_status_t eagle3_sample(const float *logits, int32_t rows, int32_t V, int64_t ld,
                                          const eagle3_sampling_t *params, const float *uniforms, const int32_t *d2t,
                                          int32_t target_vocab, int32_t *tokens, float *token_prob, float *probs,

@@ -183,3 +183,18 @@ def test_mha_config_checks_without_a_gpu(lib):
         setattr(w, nm, 256)
     assert lib.eagle3_draft_create(C.byref(cfg), C.byref(w), C.byref(h)) == E.ERR_INVALID_ARG
     assert h.value is None
+
+
+def test_sample_rejects_bad_arguments(lib):
+    # one cluster of 8 CTAs per row along the grid's y dimension: rows past 65535 are refused on the host,
+    # as are rows or vocabularies outside range and inconsistent filters (no launch, no GPU needed)
+    base = dict(logits=16, rows=2, V=100, ld=100, T=0.8, k=50, p=0.9, u=16, tokens=16)
+    for kw in [dict(logits=None), dict(u=None), dict(tokens=None), dict(rows=0), dict(rows=65536), dict(V=0),
+               dict(V=131073, ld=131073), dict(ld=99), dict(k=1025), dict(k=-1), dict(p=0.0), dict(p=1.5),
+               dict(k=0, p=0.5), dict(T=-1.0)]:
+        args = dict(base)
+        args.update(kw)
+        with pytest.raises(E.Eagle3Error) as ei:
+            E.eagle3_sample(args["logits"], args["rows"], args["V"], args["ld"], args["T"], args["k"], args["p"],
+                            args["u"], None, 0, args["tokens"])
+        assert ei.value.status == E.ERR_INVALID_ARG, kw
