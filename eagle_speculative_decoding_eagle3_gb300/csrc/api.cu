@@ -530,10 +530,18 @@ struct Lin {
     float* logits = nullptr; long ldl = 0;     // ARGMAX debug output
     // grouped rows (GEMV path only): see GemvArgs
     int w_grp = 0; long w_grp_stride = 0; int w_row0 = 0;
+    bool force_tc = false;   // run on the tensor-core GEMM whatever the row count
     int a_grp = 0; long a_grp_stride = 0;
 };
 
 bool use_tc(const eagle3_draft& d, int M) { return d.tc_ok && M > kGemvMaxRows; }
+
+// The lm_head scores 5 to 8 rows on the tensor cores too: the GEMV would multiply every weight by each
+// row's activations from L1, and at that many rows the L1 reads, not HBM, set its pace.  (Quantized heads
+// keep the GEMV: their expansion buffer exists only for heads that take more than 8 rows.)
+bool head_tc(const eagle3_draft& d, int rows) {
+    return use_tc(d, rows) || (d.tc_ok && rows >= 5 && !quant_head(d.cfg) && d.z_bf != nullptr);
+}
 
 // Split-K count for a tensor-core GEMM: the count that minimises a wave model of the launch.  One CTA
 // per SM at a time; a CTA streams its share of the weight tile at the SM's share of the HBM bandwidth (or
@@ -570,7 +578,7 @@ int tc_splits(const eagle3_draft& d, int M, int N, int K, int bn, bool glu) {
 }
 
 cudaError_t run_linear(eagle3_draft& d, const Lin& L, int kind, cudaStream_t st) {
-    if (!use_tc(d, L.M)) {
+    if (!L.force_tc && !use_tc(d, L.M)) {
         GemvArgs g;
         memset(&g, 0, sizeof(g));
         for (int i = 0; i < L.na; ++i) { g.a[i] = L.a32[i]; g.lda[i] = L.lda[i]; g.ka[i] = L.ka[i]; }
@@ -920,6 +928,7 @@ cudaError_t run_head(eagle3_draft& d, int batch, float* logits_out, cudaStream_t
     Lin L = lin1(d, batch, d.z, d.z_bf, d.cfg.hidden, d.w.lm_head, d.cfg.draft_vocab);
     quant(d, L, QM_LM, d.w.lm_head_scale);
     L.epi = EPI_ARGMAX; L.logits = logits_out; L.ldl = d.cfg.draft_vocab;
+    L.force_tc = head_tc(d, batch);
     return run_linear(d, L, K_LM_HEAD, st);
 }
 
@@ -1056,7 +1065,7 @@ eagle3_status_t eagle3_draft_extend(eagle3_draft_t* d, const void* const aux_hid
                                   d->row_seq, d->row_pos, st);
     }));
     E3_CUDA(run_layer(*d, cache, M, d->f, st, batch, row_offsets));
-    const bool tch = use_tc(*d, batch);
+    const bool tch = head_tc(*d, batch);
     E3_CUDA(traced(*d, K_FINAL, st, [&] {
         return launch_final(ra, true, batch, M, row_offsets, d->h2, d->w.final_norm, d->row_pos, d->carry, d->z,
                             tch ? d->z_bf : nullptr, hidden_out, cache->lengths, st);
@@ -1095,7 +1104,7 @@ eagle3_status_t eagle3_draft_decode(eagle3_draft_t* d, int32_t gamma, const int3
         float* lo = logits_out ? logits_out + (size_t)(s - 1) * B * c.draft_vocab : nullptr;
         E3_CUDA(traced(*d, K_FINAL, st, [&] {
             return launch_final(ra, false, B, B, nullptr, d->h2, d->w.final_norm, d->row_pos, d->carry, d->z,
-                                tc ? d->z_bf : nullptr, ho, cache->lengths, st);
+                                head_tc(*d, B) ? d->z_bf : nullptr, ho, cache->lengths, st);
         }));
         E3_CUDA(run_head(*d, B, lo, st));
         E3_CUDA(traced(*d, K_ARGMAX, st, [&] {
@@ -1154,7 +1163,7 @@ eagle3_status_t eagle3_draft_decode_sampled(eagle3_draft_t* d, int32_t gamma, co
         float* lo = logits_out ? logits_out + (size_t)(s - 1) * B * Vd : d->logits;
         E3_CUDA(traced(*d, K_FINAL, st, [&] {
             return launch_final(ra, false, B, B, nullptr, d->h2, d->w.final_norm, d->row_pos, d->carry, d->z,
-                                tc ? d->z_bf : nullptr, ho, cache->lengths, st);
+                                head_tc(*d, B) ? d->z_bf : nullptr, ho, cache->lengths, st);
         }));
         {
             Lin L = lin1(*d, B, d->z, d->z_bf, H, d->w.lm_head, Vd);
