@@ -33,7 +33,8 @@
 // O is rescaled in TMEM only on those rare tiles.
 //
 // Warps: 0 TMA producer (the cache tiles through the block table, one 3D box of five 64-column chunks
-// per tile, a 3-deep ring);
+// per tile, a 4-deep ring; the shared memory goes to cache stages rather than to second P and exchange
+// buffers, since a stage stays occupied until its tile's P V completes);
 // 1 TMEM owner and MMA issuer; 2-5 query loaders, then score readers (TMEM lanes = heads; a warp either
 // sends its heads' partial scores to the peer or owns their softmax); 6-9 rescale O rows when asked,
 // zero the cache rows past the context in the last tile (their P is 0, but 0 x NaN would poison O), and
@@ -57,8 +58,8 @@ constexpr int T = 64;                  // slots per tile
 constexpr int NCH = 5;                 // 64-column chunks staged per CTA
 constexpr int KSPLIT = 288;            // score columns of CTA 0 (CTA 1 takes the rest)
 constexpr int KSTEPS = KSPLIT / 16;
-constexpr int STAGES = 3;
-constexpr int NS = 1, NB = 2, NX = 2;  // score buffers (TMEM), P / alpha buffers, exchange buffers
+constexpr int STAGES = 4;
+constexpr int NS = 1, NB = 1, NX = 1;  // score buffers (TMEM), P / alpha buffers, exchange buffers
 constexpr float TAU = 8.f;             // lazy rescale threshold, in base-2 exponent units
 constexpr int KV_CHUNK = T * 128;      // 8 KB: 64 rows x 64 bf16
 constexpr int KV_STAGE = NCH * KV_CHUNK;
