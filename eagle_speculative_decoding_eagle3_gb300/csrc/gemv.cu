@@ -5,9 +5,9 @@
 namespace e3 {
 
 // Upper bound of the ARGMAX partials per row (one per CTA): both kernels run one wave of at most
-// kGemvCtasPerSm CTAs per SM.  The launch reports the count it used in GemvArgs::npart.
+// kGemvMaxCtasPerSm CTAs per SM.  The launch reports the count it used in GemvArgs::npart.
 int gemv_argmax_parts(int N, int num_sms) {
-    const long slots = (long)num_sms * kGemvCtasPerSm;
+    const long slots = (long)num_sms * kGemvMaxCtasPerSm;
     return (int)(N < slots ? N : slots);
 }
 

@@ -4,11 +4,13 @@
 // q_b, o_proj, gate | up, down, lm_head, the per-head value up-projection; "Eagle3 DeepseekV3 in MAX"
 // §4).  At a handful of rows a layer is bound by streaming W from HBM once, so the kernel is laid out
 // for HBM:
-//  * one balanced wave: the grid holds kGemvCtasPerSm CTAs per SM and every warp owns an equal range of
-//    weight rows (rows_per_warp), so no SM idles in a half-empty last wave;
+//  * one balanced wave: the grid holds gemv_cps CTAs per SM (two; three for FP8 weights outside the GLU,
+//    where the arithmetic per byte leaves a warp computing for longer between its load batches and a
+//    third CTA with half the loads per batch keeps more of them in flight) and every warp owns an equal
+//    range of weight rows (rows_per_warp), so no SM idles in a half-empty last wave;
 //  * a warp streams R of its rows at once (R = 1 or 4), each with U 16-byte non-allocating loads per
-//    lane (lane l reads elements [8l + 256c, +8) of a row; FP8: [16l + 512c, +16)), so about 16 loads of
-//    16 B are in flight per lane and ~128 KB per SM whatever the row length;
+//    lane (lane l reads elements [8l + 256c, +8) of a row; FP8: [16l + 512c, +16)), so gemv_loads (16 at
+//    two CTAs per SM, 8 at three) loads of 16 B are in flight per lane whatever the row length;
 //  * the activation rows (up to MR) stay L1/L2 resident and are loaded once per chunk for all R rows;
 //  * at the end of each pass the warp reduces its partial dot products and applies the fused epilogue:
 //    store, residual add, SiLU(gate) * up (two weight rows per output), or a running row argmax with
@@ -33,11 +35,13 @@
 namespace e3 {
 
 constexpr int kGemvWarps = 8;
-constexpr int kGemvCtasPerSm = 2;
-constexpr int kLoadsInFlight = 16;     // 16-byte weight loads per lane per iteration (32 of 8 B for FP8)
+constexpr int kGemvMaxCtasPerSm = 3;   // the largest gemv_cps: sizes the argmax partials
 
 template <typename T> constexpr bool kIsFp8 = false;
 template <> constexpr bool kIsFp8<fp8e4> = true;
+// CTAs per SM of a GEMV launch and the 16-byte weight loads per lane and iteration that fit its registers
+template <typename TW, int EPI> constexpr int gemv_cps() { return kIsFp8<TW> && EPI != EPI_GLU ? 3 : 2; }
+template <typename TW, int EPI> constexpr int gemv_loads() { return gemv_cps<TW, EPI>() >= 3 ? 8 : 16; }
 template <typename T> constexpr bool kIsFp4 = false;
 template <> constexpr bool kIsFp4<fp4x2> = true;
 
@@ -82,11 +86,11 @@ __device__ __forceinline__ float matrix_scale(const GemvArgs& g, bool glu, int n
 }
 
 template <typename TA, typename TW, int MR, int EPI, int R>
-__global__ void __launch_bounds__(kGemvWarps * 32, kGemvCtasPerSm) gemv_kernel(const GemvArgs g, int rows_per_warp) {
+__global__ void __launch_bounds__(kGemvWarps * 32, gemv_cps<TW, EPI>()) gemv_kernel(const GemvArgs g, int rows_per_warp) {
     constexpr int NW = (EPI == EPI_GLU) ? 2 : 1;   // weight rows read per output column
     constexpr int EL = WUnit<TW>::EL, CW = kChunk<TW>, PK = WUnit<TW>::PK;
     constexpr bool F4 = kIsFp4<TW>;
-    constexpr int U0 = kLoadsInFlight / (R * NW) * 16 / WUnit<TW>::BYTES;
+    constexpr int U0 = gemv_loads<TW, EPI>() / (R * NW) * 16 / WUnit<TW>::BYTES;
     constexpr int U = U0 < 1 ? 1 : U0;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int m0 = blockIdx.x * MR;
@@ -261,16 +265,16 @@ __global__ void __launch_bounds__(kGemvWarps * 32, kGemvCtasPerSm) gemv_kernel(c
 // K-split variant for long rows (bf16 or FP8 weights, no row grouping).  A CTA owns `rpc` consecutive output
 // columns; its 8 warps form RG = 8 / KS row groups of KS warps, and the KS warps of a group split K
 // (warp k of a group reads the warp chunks [k nch / KS, (k + 1) nch / KS) of every row).  A group
-// streams R rows at once (U chunks each, 16 loads of 16 B in flight per lane), so one activation load
+// streams R rows at once (U chunks each, gemv_loads loads of 16 B in flight per lane), so one activation load
 // feeds R rows instead of the whole-row kernel's few, and a layer with few rows per warp (q_a | kv_a:
 // 2112 rows for 2432 warps) still keeps every warp busy.  Each round the RG groups take one pass of R
 // rows each; the KS partial sums of every output meet in shared memory, where the epilogue is applied.
 template <typename TA, typename TW, int MR, int EPI, int R>
-__global__ void __launch_bounds__(kGemvWarps * 32, kGemvCtasPerSm) gemv_ks_kernel(const GemvArgs g, int rpc, int KS) {
+__global__ void __launch_bounds__(kGemvWarps * 32, gemv_cps<TW, EPI>()) gemv_ks_kernel(const GemvArgs g, int rpc, int KS) {
     constexpr int NW = (EPI == EPI_GLU) ? 2 : 1;
     constexpr int EL = WUnit<TW>::EL, CW = kChunk<TW>;
     static_assert(!kIsFp4<TW>, "NVFP4 weights stream through the whole-row kernel");
-    constexpr int U0 = kLoadsInFlight / (R * NW) * 16 / WUnit<TW>::BYTES;
+    constexpr int U0 = gemv_loads<TW, EPI>() / (R * NW) * 16 / WUnit<TW>::BYTES;
     static_assert(R * MR <= 32, "one epilogue thread per (row group, row, activation row)");
     constexpr int U = U0 < 1 ? 1 : U0;
     constexpr int OUT = MR * R * NW;                 // partial sums per warp and pass
@@ -432,29 +436,29 @@ static int gemv_ks_slices(int nch) {
     return 1;
 }
 
-// Rows per pass of the K-split kernel: 16 loads of 16 B in flight per lane and the accumulators within
-// the register budget of two CTAs per SM.
+// Rows per pass of the K-split kernel: the accumulators within the register budget of two CTAs per SM
+// (the FP8 kernels at three CTAs per SM take the same rows with half the loads per pass).
 template <int MR, int EPI>
 constexpr int gemv_ks_rows() {
     return (EPI == EPI_GLU ? 4 : 8) / (MR >= 8 ? 4 : (MR >= 4 ? 2 : 1));
 }
 
-// Columns per CTA of the K-split kernel: one balanced wave of kGemvCtasPerSm CTAs per SM, whole passes.
-static void gemv_ks_split(int N, int num_sms, int R, int* rpc, int* ctas) {
-    const long slots = (long)num_sms * kGemvCtasPerSm;
+// Columns per CTA of the K-split kernel: one balanced wave of cps CTAs per SM, whole passes.
+static void gemv_ks_split(int N, int num_sms, int cps, int R, int* rpc, int* ctas) {
+    const long slots = (long)num_sms * cps;
     int r = (int)((N + slots - 1) / slots);
     r = (r + R - 1) / R * R;
     *rpc = r;
     *ctas = (N + r - 1) / r;
 }
 
-// Rows per warp and CTAs along N for one balanced wave of kGemvCtasPerSm CTAs per SM.  A grouped GEMV
-// keeps every pass of R rows inside one activation group.
-static void gemv_split(int N, int num_sms, int group, int* rows_per_warp, int* ctas, int* R) {
-    const long warps = (long)num_sms * kGemvCtasPerSm * kGemvWarps;
+// Rows per warp and CTAs along N for one balanced wave of cps CTAs per SM.  A grouped GEMV keeps every pass
+// of R rows inside one activation group.
+static void gemv_split(int N, int num_sms, int cps, int group, int* rows_per_warp, int* ctas, int* R) {
+    const long warps = (long)num_sms * cps * kGemvWarps;
     int rpw = (int)((N + warps - 1) / warps);
     if (rpw < 1) rpw = 1;
-    *R = rpw < 4 ? rpw : 4;                              // 16 / R loads per row keep 16 in flight
+    *R = rpw < 4 ? rpw : 4;                              // the loads of a batch spread over R rows
     if (group && *R > 1) {                               // passes must not straddle a group
         *R = 4;
         int r = (rpw + 3) / 4 * 4;
@@ -482,7 +486,7 @@ template <typename TA, typename TW, int MR, int EPI>
 static cudaError_t launch_ks(GemvArgs& g, int KS, int num_sms, cudaStream_t st) {
     constexpr int R = gemv_ks_rows<MR, EPI>();
     int rpc, ctas;
-    gemv_ks_split(g.N, num_sms, R, &rpc, &ctas);
+    gemv_ks_split(g.N, num_sms, gemv_cps<TW, EPI>(), R, &rpc, &ctas);
     if (EPI == EPI_ARGMAX) g.npart = ctas;
     dim3 grid((g.M + MR - 1) / MR, ctas);
     return launch_pdl(gemv_ks_kernel<TA, TW, MR, EPI, R>, grid, dim3(kGemvWarps * 32), 0, st, g, rpc, KS);
@@ -496,7 +500,7 @@ static cudaError_t launch_mr(GemvArgs& g, int num_sms, cudaStream_t st) {
     // load and streams slightly faster (gate | up, lm_head, q_b on a GB300).
     const int KS = gemv_ks_slices((g.K + kChunk<TW> - 1) / kChunk<TW>);
     int rpw, ctas, R;
-    gemv_split(g.N, num_sms, g.a_grp, &rpw, &ctas, &R);
+    gemv_split(g.N, num_sms, gemv_cps<TW, EPI>(), g.a_grp, &rpw, &ctas, &R);
     if constexpr (!kIsFp4<TW>) {
         if (sizeof(TW) <= 2 && KS > 1 && rpw <= 4 && !g.w_grp && !g.a_grp) {
             switch (MR) {
