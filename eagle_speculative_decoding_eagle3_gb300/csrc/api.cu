@@ -906,7 +906,9 @@ cudaError_t run_layer(eagle3_draft& d, eagle3_kv_t* kv, int M, const float* fuse
         E3_TRY(run_linear(d, L, K_O_PROJ, st));
     }
     E3_TRY(traced(d, K_POST_NORM, st, [&] {
-        return launch_rmsnorm(M, H, c.rms_eps, ra.dt, d.h1, w.post_attn_norm, d.y, tc ? d.y_bf : nullptr, st);
+        // the tensor-core GEMM reads only the bf16 copy
+        return launch_rmsnorm(M, H, c.rms_eps, ra.dt, d.h1, w.post_attn_norm, tc ? nullptr : d.y, tc ? d.y_bf : nullptr,
+                              st);
     }));
     {
         Lin L = lin1(d, M, d.y, d.y_bf, H, w.gate, I);
@@ -1062,7 +1064,7 @@ eagle3_status_t eagle3_draft_extend(eagle3_draft_t* d, const void* const aux_hid
     }
     E3_CUDA(traced(*d, K_EMBED, st, [&] {
         return launch_embed_norms(ra, false, M, tokens, positions, row_offsets, batch, nullptr, nullptr, d->f,
-                                  d->w.embed, d->w.input_norm, d->w.hidden_norm, d->x, tc ? d->x_bf : nullptr,
+                                  d->w.embed, d->w.input_norm, d->w.hidden_norm, tc ? nullptr : d->x, tc ? d->x_bf : nullptr,
                                   d->row_seq, d->row_pos, st);
     }));
     E3_CUDA(run_layer(*d, cache, M, d->f, st, batch, row_offsets));
@@ -1097,7 +1099,7 @@ eagle3_status_t eagle3_draft_decode(eagle3_draft_t* d, int32_t gamma, const int3
     for (int s = 1; s < gamma; ++s) {
         E3_CUDA(traced(*d, K_EMBED, st, [&] {
             return launch_embed_norms(ra, true, B, nullptr, nullptr, nullptr, B, d->tok_in, cache->lengths, d->carry,
-                                      d->w.embed, d->w.input_norm, d->w.hidden_norm, d->x, tc ? d->x_bf : nullptr,
+                                      d->w.embed, d->w.input_norm, d->w.hidden_norm, tc ? nullptr : d->x, tc ? d->x_bf : nullptr,
                                       d->row_seq, d->row_pos, st);
         }));
         E3_CUDA(run_layer(*d, cache, B, d->carry, st));
@@ -1156,7 +1158,7 @@ eagle3_status_t eagle3_draft_decode_sampled(eagle3_draft_t* d, int32_t gamma, co
     for (int s = 1; s < gamma; ++s) {
         E3_CUDA(traced(*d, K_EMBED, st, [&] {
             return launch_embed_norms(ra, true, B, nullptr, nullptr, nullptr, B, d->tok_in, cache->lengths, d->carry,
-                                      d->w.embed, d->w.input_norm, d->w.hidden_norm, d->x, tc ? d->x_bf : nullptr,
+                                      d->w.embed, d->w.input_norm, d->w.hidden_norm, tc ? nullptr : d->x, tc ? d->x_bf : nullptr,
                                       d->row_seq, d->row_pos, st);
         }));
         E3_CUDA(run_layer(*d, cache, B, d->carry, st));

@@ -38,7 +38,8 @@ __device__ __forceinline__ void store_row8(float* p, const float* v) {
     reinterpret_cast<float4*>(p)[1] = make_float4(v[4], v[5], v[6], v[7]);
 }
 
-// x[r] = [ RMS(E[token]) * w_in | RMS(fused[r]) * w_hid ]  (2H wide).
+// x[r] = [ RMS(E[token]) * w_in | RMS(fused[r]) * w_hid ]  (2H wide), in fp32 (x, for the GEMV) and/or bf16
+// (x_bf, for the tensor-core GEMM); either may be null.
 // The token embedding is the target's table ("Eagle3 DeepseekV3 in MAX" §5); the two streams are
 // normalised separately and concatenated ("EAGLE head deep dive" part 3; MAX §4).
 template <typename T>
@@ -109,8 +110,10 @@ embed_norms_kernel(RowArgs a, int decode, const int* tokens, const int* position
             load_row8(w_hid + 8 * c, wh);
 #pragma unroll
             for (int k = 0; k < 8; ++k) { o1[k] = ev[i][k] * ie * wi[k]; o2[k] = fv[i][k] * iff * wh[k]; }
-            store_row8(xr + 8 * c, o1);
-            store_row8(xr + H + 8 * c, o2);
+            if (x) {
+                store_row8(xr + 8 * c, o1);
+                store_row8(xr + H + 8 * c, o2);
+            }
             if (x_bf) {
                 store_bf8(x_bf + (long)r * 2 * H + 8 * c, o1);
                 store_bf8(x_bf + (long)r * 2 * H + H + 8 * c, o2);
@@ -210,7 +213,7 @@ rmsnorm_kernel(int H, float eps, const float* x, const T* w, float* y, bf16* y_b
             load_row8(w + 8 * c, wv);
 #pragma unroll
             for (int k = 0; k < 8; ++k) v[i][k] *= inv * wv[k];
-            store_row8(y + r * H + 8 * c, v[i]);
+            if (y) store_row8(y + r * H + 8 * c, v[i]);
             if (y_bf) store_bf8(y_bf + r * H + 8 * c, v[i]);
         }
     }
