@@ -610,7 +610,7 @@ cudaError_t run_linear(eagle3_draft& d, const Lin& L, int kind, cudaStream_t st)
     }
     TcParams p;
     memset(&p, 0, sizeof(p));
-    const int bn = tc_pick_bn(L.M);
+    int bn = tc_pick_bn(L.M);
     const bool glu = L.epi == EPI_GLU;
     const void* w0 = L.w0;
     const void* w1 = L.w1;
@@ -638,8 +638,6 @@ cudaError_t run_linear(eagle3_draft& d, const Lin& L, int kind, cudaStream_t st)
     }
     if (!make_tma_2d(&p.mw[0], w0, r0, L.K, L.K, 128)) return cudaErrorInvalidValue;
     if (w1 && !make_tma_2d(&p.mw[1], w1, r1, L.K, L.K, 128)) return cudaErrorInvalidValue;
-    for (int i = 0; i < L.na; ++i)
-        if (!make_tma_2d(&p.mx[i], L.a16[i], L.M, L.ka[i], L.lda[i], bn)) return cudaErrorInvalidValue;
     p.np0 = L.w1 && !glu ? L.n0rows : 1 << 30;
     p.N = L.N; p.M = L.M; p.K = L.K;
     p.kseg[0] = L.na > 1 ? L.ka[0] / 64 : 1 << 30;
@@ -657,15 +655,25 @@ cudaError_t run_linear(eagle3_draft& d, const Lin& L, int kind, cudaStream_t st)
     // Persistent CTAs (one per SM, the next tile's loads and MMAs overlapping this tile's epilogue) for
     // unsplit one-matrix GEMMs with more tiles than SMs whose epilogue is a large share of a tile: the
     // lm_head's argmax, short K, or a single token tile (decode batches).
-    const long tiles = (long)((L.N + 127) / 128) * ((L.M + bn - 1) / bn);
+    long tiles = (long)((L.N + 127) / 128) * ((L.M + bn - 1) / bn);
     const bool persist = !glu && splits == 1 && tiles > d.num_sms && (L.epi == EPI_ARGMAX || L.K <= 2048 || L.M <= bn);
     const long pair_tiles = (long)((L.N + 255) / 256) * ((L.M + bn - 1) / bn);
     if (persist) {
+        // one token tile of up to 256 rows leaves each CTA one or two weight tiles, so half of them idle
+        // through the last; narrower token tiles (down to 64 rows) give every CTA four or more (batch 256:
+        // q_b 44 -> 38 us).  Not for the argmax epilogue, whose per-tile reduction then runs four times
+        // over (batch-256 lm_head 168 -> 181 us).
+        while (L.epi != EPI_ARGMAX && bn > 64 && L.M <= bn && tiles < 4L * d.num_sms) {
+            bn /= 2;
+            tiles = (long)((L.N + 127) / 128) * ((L.M + bn - 1) / bn);
+        }
         p.persist = d.num_sms;
     } else if (!glu && L.epi != EPI_ARGMAX && bn == 256 && pair_tiles >= 2L * d.num_sms) {
         p.pair = 1;
         splits = 1;
     }
+    for (int i = 0; i < L.na; ++i)
+        if (!make_tma_2d(&p.mx[i], L.a16[i], L.M, L.ka[i], L.lda[i], bn)) return cudaErrorInvalidValue;
     cudaError_t e = traced(d, kind, st, [&] { return launch_tc_gemm(p, bn, splits, st); });
     if (L.epi == EPI_ARGMAX) d.npart = p.npart;
     return e;
