@@ -92,6 +92,17 @@ def test_mla_shaped_bf16_tensor_core_rounds():
     print(check_round(w, gpu, orc, seqs, paged, TOL_BF16))
 
 
+@pytest.mark.parametrize("batch", [6, 24])
+def test_persistent_lm_head_ragged_vocabulary(batch):
+    # a 20,100-entry draft vocabulary: 157 full 128-row weight tiles and a ragged one, more tiles than SMs,
+    # so the lm_head's argmax runs on the persistent tcgen05 GEMM (at 6 rows per decode step too)
+    w = WL.workload("dsv3_b1", hidden=1024, n_heads=8, q_lora_rank=256, intermediate=2048,
+                    target_vocab=40000, draft_vocab=20100, batch=batch, ctx=(30, 300), t_new=2, gamma=3,
+                    accept_p=(0.7,) * 3, seed=90 + batch)
+    gpu, orc, seqs, paged = run_round(w)
+    print(check_round(w, gpu, orc, seqs, paged, TOL_BF16))
+
+
 def test_dsv3_extend_rows_tensor_core():
     # full DeepseekV3 head dimensions, 2 sequences x 256 new rows on an empty cache (causal extend)
     w = WL.workload("dsv3_extend", batch=2, t_new=256, gamma=2, accept_p=(0.7, 0.7))
