@@ -170,9 +170,22 @@ void attn_plan(const eagle3_draft& d, int M, int* splits, int* chunk) {
     const long rows = (long)M * hg, ctx = d.cfg.max_ctx;
     *chunk = 0;
     if (M < kAttnChunkRows) {
-        long s = (2L * d.num_sms + rows - 1) / rows;
+        // Each row's context is divided evenly over the splits.  The 64-head mma.sync kernel holds one
+        // CTA per SM: its (split, head block, row) CTAs fill one wave, so the longest context takes the
+        // fewest 32-slot tiles per CTA (4097 slots: 2 tiles over 76 splits instead of 3 over 64 in a
+        // second wave's worth of CTAs); the merge fused with the value projection takes up to 128 splits
+        // (at most 8 rows), the plain merge 64.  Other kernels plan two CTAs per SM.
+        const bool dt_bf = d.cfg.dtype == EAGLE3_BF16;
+        const bool one = attention_one_cta_per_sm(dt_bf ? BF16 : F32, d.cfg.kv_lora_rank, d.cfg.qk_rope_dim);
+        long s = one ? d.num_sms / rows : (2L * d.num_sms + rows - 1) / rows;
+        long cap = d.splits_cap;
+        if (one && dt_bf && M <= 8 && d.cfg.kv_lora_rank == 512 && d.cfg.v_head_dim == 128) {
+            cap = (d.cfg.max_ctx + 31) / 32;
+            if (cap > kMergeUnabsorbMaxSplits) cap = kMergeUnabsorbMaxSplits;
+        }
+        if (s > cap) s = cap;
         if (s < 1) s = 1;
-        if (s > d.splits_cap) s = d.splits_cap;
+        while (s > 1 && (size_t)M * s > d.part_rows) --s;
         *splits = (int)s;
         return;
     }
@@ -818,9 +831,14 @@ cudaError_t run_attention_mla(eagle3_draft& d, eagle3_kv_t* kv, int M, cudaStrea
         // o_lat: written by the attention kernel itself for a single split, else by the split merge; then
         // o_h = W_UV,h o_lat,h over the value rows of kv_b
         if (tc) aa.olat_bf = d.olat_bf; else aa.olat = d.olat;
+        // few rows with split partials: the merge and the value up-projection in one kernel (more than 64
+        // splits only there)
+        bool fused = !tc && aa.splits > 1 && merge_unabsorb_supported(aa);
+        if (!fused && aa.splits > 64) {
+            aa.splits = 64;
+            fused = !tc && merge_unabsorb_supported(aa);
+        }
         E3_TRY(traced(d, K_ATTN, st, [&] { return tc_attn ? launch_attention_tc(aa, st) : launch_attention(aa, st); }));
-        // few rows with split partials: the merge and the value up-projection in one kernel
-        const bool fused = !tc && aa.splits > 1 && merge_unabsorb_supported(aa);
         if (fused) {
             E3_TRY(traced(d, K_UNABSORB, st, [&] { return launch_merge_unabsorb(aa, st); }));
             return cudaSuccess;

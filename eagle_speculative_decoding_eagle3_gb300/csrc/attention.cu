@@ -30,6 +30,19 @@ constexpr int kAttnWarps = 8;
 constexpr int kHeadsPerWarp = 2;
 constexpr int kHeadsPerCta = kAttnWarps * kHeadsPerWarp;
 
+// Slots of row r (context n = pos + 1) per split: the fixed chunk, else ceil(n / splits); either way
+// rounded up to whole 32-slot tiles, so the leading splits cover the context and the rest are empty.
+__device__ __forceinline__ int split_chunk(const AttnArgs& a, int n) {
+    const int chunk = a.chunk > 0 ? a.chunk : (n + a.splits - 1) / a.splits;
+    return (chunk + kTile - 1) / kTile * kTile;
+}
+// Splits of row r that hold partials (an empty split writes none and the merges read none)
+__device__ __forceinline__ int live_splits(const AttnArgs& a, int r) {
+    const int n = a.row_pos[r] + 1;
+    const int chunk = split_chunk(a, n);
+    return min(a.splits, (n + chunk - 1) / chunk);
+}
+
 // qa[r, h] = [ W_UK,h^T q_nope[r, h] | RoPE(q_pe[r, h], pos_r) ]  (fp32, plus a bf16 copy when asked)
 // Grid (head, column block of kAbsCols latent columns, row block).  Thread (cc, rg) owns 8 columns and
 // the W_UK rows rg, rg + RG, ...: all of its (dn / RG) 16-byte weight loads are issued together, then
@@ -147,13 +160,10 @@ __global__ void __launch_bounds__(kAttnWarps * 32) attention_kernel(const AttnAr
     const int s = blockIdx.x, hg = blockIdx.y, r = blockIdx.z;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int b = a.row_seq[r], pos = a.row_pos[r], n = pos + 1;
-    int chunk = a.chunk > 0 ? a.chunk : (n + a.splits - 1) / a.splits;
-    chunk = (chunk + kTile - 1) / kTile * kTile;
+    const int chunk = split_chunk(a, n);
     const int t0 = s * chunk, t1 = min(n, t0 + chunk);
     const int h0 = hg * kHeadsPerCta;
-    if (a.chunk > 0 && t0 >= t1) {   // past this row's context: an empty split that the merge skips
-        return;
-    }
+    if (t0 >= t1) return;   // past this row's context: an empty split that the merge skips
 
     for (int t = threadIdx.x; t < kHeadsPerCta * D; t += blockDim.x) {
         const int hh = t / D, d = t % D, h = h0 + hh;
@@ -290,11 +300,11 @@ __global__ void __launch_bounds__(mla_mma::WARPS * 32, 1) attention_mma_kernel(c
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, gq = lane >> 2, tig = lane & 3;
     const int hgrp = warp & 3, half = warp >> 2;
     const int b = a.row_seq[r], pos = a.row_pos[r], n = pos + 1;
-    int chunk = a.chunk > 0 ? a.chunk : (n + a.splits - 1) / a.splits;
-    chunk = (chunk + T - 1) / T * T;
+    static_assert(T == kTile, "split chunks are whole 32-slot tiles");
+    const int chunk = split_chunk(a, n);
     const int t0 = s * chunk, t1 = min(n, t0 + chunk);
     const int h0 = hb * HEADS;
-    if (a.chunk > 0 && t0 >= t1) return;   // past this row's context: an empty split that the merge skips
+    if (t0 >= t1) return;   // past this row's context: an empty split that the merge skips
 
     // Q: heads h0 .. h0 + 63 of row r (zero rows past n_heads)
     for (int c = tid; c < HEADS * (D / 8); c += WARPS * 32) {
@@ -449,7 +459,7 @@ __global__ void __launch_bounds__(mla_mma::WARPS * 32, 1) attention_mma_kernel(c
         }
         const long base = ((long)r * a.nh + h) * a.splits + s;
         if (half == 0 && tig == 0) {
-            a.part_ml[base * 2] = (t0 < t1) ? m_r[rr] : -FLT_MAX;
+            a.part_ml[base * 2] = m_r[rr];
             a.part_ml[base * 2 + 1] = l_r[rr];
         }
 #pragma unroll
@@ -478,8 +488,8 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const AttnArgs a) 
     const int S = a.splits;
     const long base = ((long)r * a.nh + h) * S;
     const int C4 = a.dc / 4, G = MULTI ? blockDim.x / C4 : 1;
-    // fixed chunks: only the splits that cover part of this row's context hold partials
-    const int Sv = a.chunk > 0 ? min(S, (a.row_pos[r] + a.chunk) / a.chunk) : S;
+    // only the splits that cover part of this row's context hold partials
+    const int Sv = live_splits(a, r);
     const int t = threadIdx.x, col4 = t % C4, grp = t / C4;
     const bool active = grp < G;
     float4 o[J];
@@ -549,7 +559,7 @@ __global__ void __launch_bounds__(mu::THREADS, 1) merge_unabsorb_kernel(const At
     bf16* w = reinterpret_cast<bf16*>(msm);                              // [DV][DC]
     float* ol = reinterpret_cast<float*>(msm + W_BYTES);                 // [M][DC]
     uint64_t* bar = reinterpret_cast<uint64_t*>(msm + W_BYTES + MAXR * DC * 4);
-    __shared__ float wsp[64];
+    __shared__ float wsp[kMergeUnabsorbMaxSplits];
     const int h = blockIdx.x, t = threadIdx.x, lane = t & 31, warp = t >> 5;
     const uint32_t sbar = smem_u32(bar);
     if (t == 0) {
@@ -564,19 +574,30 @@ __global__ void __launch_bounds__(mu::THREADS, 1) merge_unabsorb_kernel(const At
     const int S = a.splits;
     for (int r = 0; r < a.M; ++r) {
         const long base = ((long)r * a.nh + h) * S;
-        const int Sv = a.chunk > 0 ? min(S, (a.row_pos[r] + a.chunk) / a.chunk) : S;
+        const int Sv = live_splits(a, r);
         __syncthreads();   // wsp of the previous row is consumed
-        if (t < 32) {
-            float m0 = -FLT_MAX, m1 = -FLT_MAX, l0 = 0.f, l1 = 0.f;
-            if (t < Sv) { m0 = a.part_ml[(base + t) * 2]; l0 = a.part_ml[(base + t) * 2 + 1]; }
-            if (t + 32 < Sv) { m1 = a.part_ml[(base + t + 32) * 2]; l1 = a.part_ml[(base + t + 32) * 2 + 1]; }
-            const float mx = warp_max(fmaxf(m0, m1));
-            const float e0 = l0 > 0.f ? __expf(m0 - mx) : 0.f;
-            const float e1 = l1 > 0.f ? __expf(m1 - mx) : 0.f;
-            const float den = warp_sum(e0 * l0 + e1 * l1);
+        if (t < 32) {      // lane t weighs splits t, t + 32, t + 64, t + 96
+            constexpr int J = kMergeUnabsorbMaxSplits / 32;
+            float m[J], l[J];
+            float mx = -FLT_MAX;
+#pragma unroll
+            for (int j = 0; j < J; ++j) {
+                const int sp = t + 32 * j;
+                m[j] = sp < Sv ? a.part_ml[(base + sp) * 2] : -FLT_MAX;
+                l[j] = sp < Sv ? a.part_ml[(base + sp) * 2 + 1] : 0.f;
+                mx = fmaxf(mx, m[j]);
+            }
+            mx = warp_max(mx);
+            float den = 0.f;
+#pragma unroll
+            for (int j = 0; j < J; ++j) {
+                m[j] = l[j] > 0.f ? __expf(m[j] - mx) : 0.f;
+                den = fmaf(m[j], l[j], den);
+            }
+            den = warp_sum(den);
             const float inv = den > 0.f ? 1.f / den : 0.f;
-            wsp[t] = e0 * inv;
-            wsp[t + 32] = e1 * inv;
+#pragma unroll
+            for (int j = 0; j < J; ++j) wsp[t + 32 * j] = m[j] * inv;
         }
         __syncthreads();
         // thread t: columns 4 (t % 128) .. + 3 of the splits sp = t / 128, + 2, ...: 16-byte loads, eight in
@@ -639,7 +660,7 @@ __global__ void __launch_bounds__(mu::THREADS, 1) merge_unabsorb_kernel(const At
 }
 
 bool merge_unabsorb_supported(const AttnArgs& a) {
-    return a.dt == BF16 && a.dc == mu::DC && a.dv == mu::DV && a.M <= mu::MAXR && a.splits >= 1 && a.splits <= 64 &&
+    return a.dt == BF16 && a.dc == mu::DC && a.dv == mu::DV && a.M <= mu::MAXR && a.splits >= 1 && a.splits <= kMergeUnabsorbMaxSplits &&
            a.o != nullptr && ((uintptr_t)a.kv_b & 15u) == 0;
 }
 
@@ -729,6 +750,10 @@ bool attention_supported(int dc, int dr, int dn, int dv) {
 
 int attention_heads_per_cta(int dt, int dc, int dr) {
     return (dt == BF16 && dc == 512 && dr == 64) ? mla_mma::HEADS : kHeadsPerCta;
+}
+
+bool attention_one_cta_per_sm(int dt, int dc, int dr) {
+    return dt == BF16 && dc == 512 && dr == 64;   // mla_mma::SMEM (158 KB) leaves room for one CTA
 }
 
 cudaError_t launch_absorb(const AttnArgs& a, cudaStream_t st) {

@@ -228,7 +228,8 @@ cudaError_t launch_attention(const AttnArgs& a, cudaStream_t st);
 // split-K merge into o_lat (olat and/or olat_bf); the value up-projection then runs as a GEMM
 cudaError_t launch_merge(const AttnArgs& a, cudaStream_t st);
 // split merge fused with o = W_UV o_lat into a.o (fp32), for at most 8 rows of a bf16 head with d_c 512,
-// d_v 128 and more than one split
+// d_v 128 and 2 .. kMergeUnabsorbMaxSplits splits (the plain merge takes at most 64)
+constexpr int kMergeUnabsorbMaxSplits = 128;
 bool merge_unabsorb_supported(const AttnArgs& a);
 cudaError_t launch_merge_unabsorb(const AttnArgs& a, cudaStream_t st);
 // rotated rope query into qa / qa_bf[:, :, dc:] (the tensor-core path forms q_lat separately)
@@ -238,6 +239,8 @@ cudaError_t launch_transpose_wuk(const void* kv_b, int nh, int dn, int dv, int d
                                  cudaStream_t st);
 bool attention_supported(int dc, int dr, int dn, int dv);
 int attention_heads_per_cta(int dt, int dc, int dr);
+// true where the latent attention kernel holds one CTA per SM (the 64-head mma.sync kernel)
+bool attention_one_cta_per_sm(int dt, int dc, int dr);
 // tcgen05 latent attention (bf16 cache, 128 heads, latent 512 + rope 64, fixed-chunk splits of 64k
 // slots, pages of 64k slots): one CTA pair per (split, row); same partial / o_lat outputs as above
 bool attention_tc_supported(const AttnArgs& a);

@@ -68,6 +68,9 @@ MLA128 = dict(hidden=1024, n_heads=128, q_lora_rank=256, intermediate=2048, targ
     dict(batch=4, ctx=(3, 20), t_new=5, gamma=3, accept_p=(0.7,) * 3, seed=87),
     # extend on an empty cache: causal attention among the new rows only (18 rows)
     dict(batch=2, ctx=(0, 0), t_new=9, gamma=3, accept_p=(0.7,) * 3, seed=88),
+    # one sequence: the decode steps divide 2300+ slots over 76 splits of one 32-slot tile (72 of them
+    # live), merged with the value projection past the plain merge's 64 splits
+    dict(batch=1, ctx=(2300, 2300), t_new=3, gamma=3, accept_p=(0.7,) * 3, seed=89),
 ])
 def test_mla_128_heads_tensor_core_attention(over):
     w = WL.workload("dsv3_b1", **MLA128, **over)
