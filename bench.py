@@ -355,6 +355,12 @@ def parse_sampling(args):
 
 
 # --------------------------------------------------------------------------------------------- our arm
+def slice_as(buf, off, like):
+    """A view with `like`'s dtype and shape over the bytes buf[off:] of a uint8 buffer."""
+    n = like.numel() * like.element_size()
+    return buf[off:off + n].view(like.dtype).view(like.shape)
+
+
 def run_ours(args, ws, rank, local):
     import numpy as np
     import torch
@@ -380,9 +386,14 @@ def run_ours(args, ws, rank, local):
     len0 = cache.lengths.clone()
     din = head.extend_inputs(ex)
     d2t_dev = HN.to_device(d2t) if d2t is not None else None
-    toks = torch.zeros((B, G), dtype=torch.int32, device="cuda")
-    acc = torch.zeros(B, dtype=torch.int32, device="cuda")
-    hist = torch.zeros(G + 1, dtype=torch.int32, device="cuda")
+    # the round's results (drafts, accepted lengths, histogram) share one int32 buffer in 16-byte aligned
+    # parts, so the end-to-end step reads them back in one device-to-host copy
+    o_acc = -(-B * G // 4) * 4
+    o_hist = o_acc + -(-B // 4) * 4
+    res = torch.zeros(o_hist + G + 1, dtype=torch.int32, device="cuda")
+    toks = res[:B * G].view(B, G)
+    acc = res[o_acc:o_acc + B]
+    hist = res[o_hist:o_hist + G + 1]
     stream = torch.cuda.current_stream()
 
     # one round to fix the drafts, then synthetic targets from them (the drafts are deterministic)
@@ -405,6 +416,27 @@ def run_ours(args, ws, rank, local):
         tprobs = torch.rand((B, G + 1, Vt), generator=gen, device="cuda") ** 4
         tprobs /= tprobs.sum(dim=2, keepdim=True)
         nxt = torch.zeros(B, dtype=torch.int32, device="cuda")
+
+    # every input a round reads from the host (auxiliary hidden states, tokens, positions, row offsets,
+    # the targets' tokens or distributions) lives in one device buffer of 256-byte aligned slices, so the
+    # end-to-end step sends them in one host-to-device copy
+    ins = list(din["aux"]) + [din["tokens"], din["positions"], din["row_offsets"], tgt]
+    if sampling is not None:
+        ins.append(tprobs)
+    offs, in_bytes = [], 0
+    for t in ins:
+        offs.append(in_bytes)
+        in_bytes += -(-t.numel() * t.element_size() // 256) * 256
+    d_pack = torch.empty(in_bytes, dtype=torch.uint8, device="cuda")
+    packed = [slice_as(d_pack, o, t) for o, t in zip(offs, ins)]
+    for dst, src in zip(packed, ins):
+        dst.copy_(src)
+    na = len(din["aux"])
+    din = dict(din, aux=packed[:na], tokens=packed[na], positions=packed[na + 1], row_offsets=packed[na + 2])
+    tgt = packed[na + 3]
+    if sampling is not None:
+        tprobs = packed[na + 4]
+    del ins
 
     def run_round(st, dev_in):
         cache.lengths.copy_(len0)
@@ -525,35 +557,17 @@ def run_ours(args, ws, rank, local):
 
     # ---------------------------------------------------------------- end to end, host buffers
     e2e_steps = args.e2e_steps or max(3, args.steps)
-    pin = lambda t: t.cpu().pin_memory()  # noqa: E731
-    h_aux = [pin(a) for a in din["aux"]]
-    h_tok, h_pos, h_ro = pin(din["tokens"]), pin(din["positions"]), pin(din["row_offsets"])
-    h_tgt = pin(tgt)
-    o_toks = torch.empty((B, G), dtype=torch.int32).pin_memory()
-    o_acc = torch.empty(B, dtype=torch.int32).pin_memory()
-    o_hist = torch.empty(G + 1, dtype=torch.int32).pin_memory()
-    d_in = {k: (v if k != "aux" else list(v)) for k, v in din.items()}
-    # sampled rounds also bring the target distributions from the host (their uniforms are drawn on the
-    # device)
-    h_samp = [] if sampling is None else [(tprobs, pin(tprobs))]
-    h2d = sum(a.numel() * a.element_size() for a in h_aux) + sum(
-        t.numel() * t.element_size() for t in (h_tok, h_pos, h_ro, h_tgt)) + sum(
-        h.numel() * h.element_size() for _, h in h_samp)
-    d2h = sum(t.numel() * t.element_size() for t in (o_toks, o_acc, o_hist))
+    # the packed inputs as the host holds them (pinned); sampled rounds bring the target distributions
+    # too (their uniforms are drawn on the device)
+    h_pack = d_pack.cpu().pin_memory()
+    h_res = torch.empty(res.shape, dtype=res.dtype).pin_memory()
+    h2d = h_pack.numel() * h_pack.element_size()
+    d2h = h_res.numel() * h_res.element_size()
 
     def e2e_step():
-        for a, h in zip(d_in["aux"], h_aux):
-            a.copy_(h, non_blocking=True)
-        d_in["tokens"].copy_(h_tok, non_blocking=True)
-        d_in["positions"].copy_(h_pos, non_blocking=True)
-        d_in["row_offsets"].copy_(h_ro, non_blocking=True)
-        tgt.copy_(h_tgt, non_blocking=True)
-        for dv, hv in h_samp:
-            dv.copy_(hv, non_blocking=True)
-        run_round(stream, d_in)
-        o_toks.copy_(toks, non_blocking=True)
-        o_acc.copy_(acc, non_blocking=True)
-        o_hist.copy_(hist, non_blocking=True)
+        d_pack.copy_(h_pack, non_blocking=True)
+        run_round(stream, din)
+        h_res.copy_(res, non_blocking=True)
         stream.synchronize()
 
     for _ in range(3):
