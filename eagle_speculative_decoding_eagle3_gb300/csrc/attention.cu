@@ -44,16 +44,18 @@ __device__ __forceinline__ int live_splits(const AttnArgs& a, int r) {
 }
 
 // qa[r, h] = [ W_UK,h^T q_nope[r, h] | RoPE(q_pe[r, h], pos_r) ]  (fp32, plus a bf16 copy when asked)
-// Grid (head, column block of kAbsCols latent columns, row block).  Thread (cc, rg) owns 8 columns and
-// the W_UK rows rg, rg + RG, ...: all of its (dn / RG) 16-byte weight loads are issued together, then
-// the RG row groups are reduced through shared memory.  The rope part is written by column block 0.
+// Grid (head, column block of kAbsCols latent columns, block of ROWS rows).  Thread (cc, rg) owns 8
+// columns and the W_UK rows rg, rg + RG, ...: all of its (dn / RG) 16-byte weight loads are issued
+// together, then the RG row groups are reduced through shared memory.  The rope part is written by
+// column block 0.  A single bf16 row (batch-1 decode) takes ROWS = 1: its accumulators fit four CTAs per
+// SM, so the 128 heads x 4 column blocks run as one wave instead of two.
 constexpr int kAbsCols = 128;
-template <typename T>
-__global__ void __launch_bounds__(256) absorb_kernel(const AttnArgs a) {
-    extern __shared__ float sm[];           // [kAbsRows][dn] q_nope, then [RG][kAbsRows][cols] partials
+template <typename T, int ROWS>
+__global__ void __launch_bounds__(256, ROWS == 1 ? 4 : 0) absorb_kernel(const AttnArgs a) {
+    extern __shared__ float sm[];           // [ROWS][dn] q_nope, then [RG][ROWS][cols] partials
     constexpr int kMaxLoads = 8;
-    const int h = blockIdx.x, cb = blockIdx.y, r0 = blockIdx.z * kAbsRows;
-    const int nr = min(kAbsRows, a.M - r0);
+    const int h = blockIdx.x, cb = blockIdx.y, r0 = blockIdx.z * ROWS;
+    const int nr = min(ROWS, a.M - r0);
     const int dqk = a.dn + a.dr, D = a.dc + a.dr;
     const int cols = min(kAbsCols, a.dc), c0 = cb * cols;
     const int nchunk = cols / 8;
@@ -71,8 +73,8 @@ __global__ void __launch_bounds__(256) absorb_kernel(const AttnArgs a) {
     }
     pdl_wait();
     float* qn = sm;
-    float* part = sm + kAbsRows * a.dn;
-    for (int t = threadIdx.x; t < kAbsRows * a.dn; t += blockDim.x) {
+    float* part = sm + ROWS * a.dn;
+    for (int t = threadIdx.x; t < ROWS * a.dn; t += blockDim.x) {
         const int i = t / a.dn, k = t % a.dn;
         qn[t] = (i < nr) ? a.q[((long)(r0 + i) * a.nh + h) * dqk + k] : 0.f;
     }
@@ -92,9 +94,9 @@ __global__ void __launch_bounds__(256) absorb_kernel(const AttnArgs a) {
         }
     }
     __syncthreads();
-    float acc[kAbsRows][8];
+    float acc[ROWS][8];
 #pragma unroll
-    for (int i = 0; i < kAbsRows; ++i)
+    for (int i = 0; i < ROWS; ++i)
 #pragma unroll
         for (int e = 0; e < 8; ++e) acc[i][e] = 0.f;
     for (int k0 = rg; rg < RG && k0 < a.dn; k0 += RG * kMaxLoads) {
@@ -112,7 +114,7 @@ __global__ void __launch_bounds__(256) absorb_kernel(const AttnArgs a) {
                 float w[8];
                 widen(wr[j], w);
 #pragma unroll
-                for (int i = 0; i < kAbsRows; ++i) {
+                for (int i = 0; i < ROWS; ++i) {
                     const float q = qn[i * a.dn + k];
 #pragma unroll
                     for (int e = 0; e < 8; ++e) acc[i][e] = fmaf(q, w[e], acc[i][e]);
@@ -122,8 +124,8 @@ __global__ void __launch_bounds__(256) absorb_kernel(const AttnArgs a) {
     }
     if (rg < RG) {
 #pragma unroll
-        for (int i = 0; i < kAbsRows; ++i) {
-            float4* dst = reinterpret_cast<float4*>(part + ((long)rg * kAbsRows + i) * cols + 8 * cc);
+        for (int i = 0; i < ROWS; ++i) {
+            float4* dst = reinterpret_cast<float4*>(part + ((long)rg * ROWS + i) * cols + 8 * cc);
             dst[0] = make_float4(acc[i][0], acc[i][1], acc[i][2], acc[i][3]);
             dst[1] = make_float4(acc[i][4], acc[i][5], acc[i][6], acc[i][7]);
         }
@@ -132,7 +134,7 @@ __global__ void __launch_bounds__(256) absorb_kernel(const AttnArgs a) {
     for (int t = threadIdx.x; t < nr * cols; t += blockDim.x) {
         const int i = t / cols, c = t % cols;
         float v = 0.f;
-        for (int g = 0; g < RG; ++g) v += part[((long)g * kAbsRows + i) * cols + c];
+        for (int g = 0; g < RG; ++g) v += part[((long)g * ROWS + i) * cols + c];
         const long o = ((long)(r0 + i) * a.nh + h) * D + c0 + c;
         a.qa[o] = v;
         if (a.qa_bf) a.qa_bf[o] = __float2bfloat16_rn(v);
@@ -759,17 +761,21 @@ bool attention_one_cta_per_sm(int dt, int dc, int dr) {
 cudaError_t launch_absorb(const AttnArgs& a, cudaStream_t st) {
     const int cols = a.dc < kAbsCols ? a.dc : kAbsCols;
     if (a.dc % cols) return cudaErrorInvalidValue;
-    dim3 grid(a.nh, a.dc / cols, (a.M + kAbsRows - 1) / kAbsRows);
+    const bool one = a.dt == BF16 && a.M == 1;
+    const int rows = one ? 1 : kAbsRows;
+    dim3 grid(a.nh, a.dc / cols, (a.M + rows - 1) / rows);
     const int RG = 256 / (cols / 8);
-    const size_t sm = ((size_t)kAbsRows * a.dn + (size_t)RG * kAbsRows * cols) * sizeof(float);
+    const size_t sm = ((size_t)rows * a.dn + (size_t)RG * rows * cols) * sizeof(float);
+    const void* k = one ? (const void*)absorb_kernel<bf16, 1>
+                        : a.dt == BF16 ? (const void*)absorb_kernel<bf16, kAbsRows> : (const void*)absorb_kernel<float, kAbsRows>;
     {
-        cudaError_t e = a.dt == BF16 ? smem_optin((const void*)absorb_kernel<bf16>, 96 * 1024)
-                                     : smem_optin((const void*)absorb_kernel<float>, 96 * 1024);
+        cudaError_t e = smem_optin(k, 96 * 1024);
         if (e != cudaSuccess) return e;
     }
     if (sm > 96 * 1024) return cudaErrorInvalidValue;
-    if (a.dt == BF16) launch_pdl(absorb_kernel<bf16>, dim3(grid), dim3(256), sm, st, a);
-    else launch_pdl(absorb_kernel<float>, dim3(grid), dim3(256), sm, st, a);
+    if (one) launch_pdl(absorb_kernel<bf16, 1>, dim3(grid), dim3(256), sm, st, a);
+    else if (a.dt == BF16) launch_pdl(absorb_kernel<bf16, kAbsRows>, dim3(grid), dim3(256), sm, st, a);
+    else launch_pdl(absorb_kernel<float, kAbsRows>, dim3(grid), dim3(256), sm, st, a);
     return cudaGetLastError();
 }
 
