@@ -46,3 +46,22 @@ def test_mha_model_counts_its_own_projections_and_cache_rows():
     ext = 2.0 * nh * 2 * d * visible
     dec = [2.0 * nh * 2 * d * sum(int(l) + w.t_new + s for l in L) for s in range(1, w.gamma)]
     assert abs(f["attention"][0] * f["attention"][1] - (ext + sum(dec))) < 1e-6 * (ext + sum(dec))
+
+
+def test_packed_views_keep_dtype_shape_and_bytes():
+    # the end-to-end step's packed input buffer: typed views at 256-byte aligned offsets of one byte buffer
+    import torch
+    parts = [torch.arange(12, dtype=torch.bfloat16).view(3, 4), torch.arange(5, dtype=torch.int32),
+             torch.rand(2, 3, 7, dtype=torch.float32)]
+    offs, n = [], 0
+    for t in parts:
+        offs.append(n)
+        n += -(-t.numel() * t.element_size() // 256) * 256
+    buf = torch.zeros(n, dtype=torch.uint8)
+    views = [bench.slice_as(buf, o, t) for o, t in zip(offs, parts)]
+    for v, t in zip(views, parts):
+        v.copy_(t)
+    for o, v, t in zip(offs, views, parts):
+        assert o % 256 == 0 and v.dtype == t.dtype and v.shape == t.shape
+        assert torch.equal(v, t)
+        assert v.data_ptr() == buf.data_ptr() + o
