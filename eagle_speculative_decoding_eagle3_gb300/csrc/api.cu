@@ -409,7 +409,8 @@ Offsets plan(const eagle3_config_t& c, int num_sms) {
     // argmax partials per scored row: the GEMV writes one per CTA, the tensor-core GEMM one per 128 rows
     o.npart = gemv_argmax_parts(c.draft_vocab, num_sms);
     if (tc && (c.draft_vocab + 127) / 128 > o.npart) o.npart = (c.draft_vocab + 127) / 128;
-    // (row, split) partials: few rows use at most M + 2 * num_sms pairs (splits = ceil(2 SMs / (M groups)));
+    // (row, split) partials: few rows use at most M + 2 * num_sms pairs (splits = ceil(2 SMs / row groups),
+    // or SMs / row groups for the one-CTA-per-SM kernel);
     // fixed chunks are planned for about kAttnWaves * num_sms pairs and shrunk to fit this capacity
     o.part_rows = (size_t)M + (size_t)kAttnWaves * num_sms + 1;
     Layout L;
